@@ -1,0 +1,279 @@
+"""Pins of the oracle to things other than itself.
+
+Each ``pin_*`` function takes an :class:`oracle.Oracle` and raises
+``AssertionError`` when the oracle disagrees with what the pages, the
+mathematics or an independent routine fix.  ``tests/test_oracle.py`` runs them
+on the real oracle; ``tests/test_oracle_mutations.py`` runs them on copies of
+the oracle with a planted mistake and checks that some pin fails.
+"""
+
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+import inputs
+from oracle import brute
+
+
+def _bits(a):
+    return np.ascontiguousarray(a, dtype=np.float16).view(np.uint16)
+
+
+def _rows(a):
+    return _bits(a).tolist()
+
+
+# ---------------------------------------------------------------------------
+# fp16 conversions against numpy's independent implementation
+# ---------------------------------------------------------------------------
+
+def pin_half_roundtrip(orc):
+    """fp16 -> double decodes every finite bit pattern like numpy does, and
+    double -> fp16 rounds like numpy (nearest even, direct from double)."""
+    allbits = np.arange(65536, dtype=np.uint16)
+    vals = allbits.view(np.float16).astype(np.float64)
+    finite = np.isfinite(vals)
+    for b in allbits[finite][::7]:
+        assert orc.half_to_double(int(b)) == float(allbits[b:b + 1].view(np.float16)[0])
+    rng = np.random.default_rng(1)
+    cands = np.concatenate([
+        rng.standard_normal(2000) * 10.0 ** rng.integers(-9, 5, 2000),
+        # exact midpoints between neighbouring fp16 values: ties
+        (vals[finite][1:400:3] + np.nextafter(vals[finite][1:400:3].astype(np.float16),
+                                              np.float16(np.inf)).astype(np.float64)) / 2,
+        np.array([65504.0, 65519.99, 65520.0, 2.0 ** -24, 2.0 ** -25, 3 * 2.0 ** -26,
+                  0.0, -0.0, 1.0 + 2.0 ** -11, 1.0 + 3 * 2.0 ** -11]),
+    ])
+    for v in cands:
+        with np.errstate(over="ignore"):
+            want = int(np.array([v], np.float64).astype(np.float16).view(np.uint16)[0])
+        got = orc.double_to_half(float(v))
+        assert got == want, (v, hex(got), hex(want))
+
+
+# ---------------------------------------------------------------------------
+# the fp32 code rule against exact rational rounding, exhaustively per scale
+# ---------------------------------------------------------------------------
+
+def _exact_codes(x16: np.ndarray, a16: np.ndarray) -> np.ndarray:
+    """round_half_even(127*x/a) in exact integer arithmetic (vectorised).
+
+    x = mx * 2^ex and a = ma * 2^ea with integer significands, so
+    127*x/a = 127*mx*2^(ex-ea) / ma; scale both to integers and round."""
+    def split(v):
+        m, e = np.frexp(v.astype(np.float64))       # v = m * 2^e, m in [0.5,1)
+        mi = np.rint(m * 2048).astype(np.int64)      # 11-bit significand
+        return mi, e.astype(np.int64) - 11
+    mx, ex = split(x16)
+    ma, ea = split(a16)
+    sh = ex - ea
+    num = 127 * mx
+    den = ma.copy()
+    pos = sh >= 0
+    num = np.where(pos, num << np.where(pos, sh, 0), num)
+    den = np.where(~pos, den << np.where(~pos, -sh, 0), den)
+    sign = np.sign(num)
+    num = np.abs(num)
+    q, r = np.divmod(num, den)
+    twice = 2 * r
+    up = (twice > den) | ((twice == den) & (q % 2 == 1))
+    return (sign * (q + up)).astype(np.int64)
+
+
+def pin_code_rule_exhaustive(orc, n_scales: int = 48):
+    """For a spread of absmax values a (including the ones that produce exact
+    ties, a = 127 * 2^s), every fp16 x with |x| <= a is coded like the exactly
+    rounded rational round_half_even(127 x / a)."""
+    allv = np.arange(0, 0x7C00, dtype=np.uint16).view(np.float16)  # all finite >= 0
+    rng = np.random.default_rng(2)
+    scales = list(np.float16(127) * np.float16(2.0) ** np.arange(-8, 8, 2).astype(np.float16))
+    scales += list(allv[rng.integers(1, len(allv), n_scales)])
+    scales += [np.float16(1.0), np.float16(6.0), np.float16(65504.0), allv[1], allv[1023]]
+    for a in scales:
+        a = np.float16(a)
+        if not a > 0:
+            continue
+        xs = allv[allv <= a]
+        xs = np.concatenate([xs, -xs[1:]])
+        # rows of the weight: each row holds a first, so its absmax is a
+        step = 4095
+        for s in range(0, len(xs), step):
+            chunk = xs[s:s + step]
+            W = np.empty((1, len(chunk) + 1), np.float16)
+            W[0, 0] = a
+            W[0, 1:] = chunk
+            Wq, sw = orc.quantize_weight(W)
+            assert sw[0] == np.float32(a)
+            want = _exact_codes(chunk, np.full(len(chunk), a))
+            got = Wq[0, 1:].astype(np.int64)
+            bad = np.flatnonzero(got != want)
+            assert len(bad) == 0, (float(a), chunk[bad[:3]], got[bad[:3]], want[bad[:3]])
+
+
+# ---------------------------------------------------------------------------
+# whole layer against the exact brute force
+# ---------------------------------------------------------------------------
+
+def _compare_with_brute(orc, X, W, tau):
+    Wq, sw = orc.quantize_weight(W)
+    r = orc.linear(X, Wq, sw, W, tau)
+    b = brute.linear(_rows(X), _rows(W), tau)
+    assert r["O"].tolist() == b["O"], (r["O"], b["O"])
+    assert np.array_equal(Wq, np.array(b["Wq"], np.int8).reshape(Wq.shape))
+    assert np.array_equal(sw.astype(np.float64), np.array([float(v) for v in b["sw"]]))
+    assert np.array_equal(r["sx"].astype(np.float64), np.array([float(v) for v in b["sx"]]))
+    assert np.array_equal(r["Xq"], np.array(b["Xq"], np.int8).reshape(r["Xq"].shape))
+    assert np.array_equal(r["acc"].astype(np.int64), np.array(b["acc"], np.int64).reshape(r["acc"].shape))
+    yb = np.array(b["Y"], np.uint16).reshape(r["Y"].shape)
+    yo = r["Y"].view(np.uint16)
+    bad = np.argwhere(yb != yo)
+    assert len(bad) == 0, (bad[:3], yo[tuple(bad[0])], yb[tuple(bad[0])])
+
+
+def pin_brute_tiny_config(orc):
+    """The tiny workload (T16 K256 N256, columns 7 and 133 x20, tau 6)."""
+    w = inputs.tiny()
+    _compare_with_brute(orc, w.X, w.W, w.tau)
+
+
+def pin_brute_random_small(orc):
+    """Random tiny shapes and thresholds, with edge rows: an all-zero row, a
+    row of only outliers, columns exactly at tau, |O| = 0 and |O| = K."""
+    rng = np.random.default_rng(3)
+    for i, (T, K, N) in enumerate([(1, 1, 1), (3, 5, 2), (7, 16, 9), (16, 32, 8),
+                                   (5, 24, 17), (2, 48, 3), (32, 8, 32)]):
+        X = (rng.standard_normal((T, K)) * 3).astype(np.float16)
+        W = (rng.standard_normal((N, K)) * 0.05).astype(np.float16)
+        if T > 2:
+            X[1] = 0                    # an all-zero row
+            X[2] = 7.5                  # a row whose every column is an outlier
+        if K > 3:
+            X[0, 3] = -6.0              # exactly at the threshold: an outlier (>=)
+        for tau in (6.0, 1.5, 0.0, math.inf, 2.0 ** 0.5):
+            _compare_with_brute(orc, X, W, tau)
+
+
+# ---------------------------------------------------------------------------
+# invariants of the method
+# ---------------------------------------------------------------------------
+
+def pin_tau_inf_integer_inputs(orc):
+    """tau = inf, integer-valued inputs with +-127 in every row: scales are 127,
+    codes equal the inputs, acc is the exact integer product, and
+    Y = fp16(X W^T) exactly (127/127 = 1; at K = 4 every |acc| <= 4*127^2
+    stays inside fp16's range, at K = 256 large values overflow to inf on
+    both sides)."""
+    for adv, K in ((False, 256), (True, 256), (False, 4), (True, 4)):
+        X, W = inputs.int_valued(8, K, 24, seed=4, adversarial=adv)
+        Wq, sw = orc.quantize_weight(W)
+        r = orc.linear(X, Wq, sw, W, math.inf)
+        assert len(r["O"]) == 0
+        assert np.all(sw == 127) and np.all(r["sx"] == 127)
+        assert np.array_equal(Wq, W.astype(np.int8)) and np.array_equal(r["Xq"], X.astype(np.int8))
+        exact = X.astype(np.int64) @ W.astype(np.int64).T       # library integer matmul
+        assert np.array_equal(r["acc"].astype(np.int64), exact)
+        with np.errstate(over="ignore"):
+            ref = exact.astype(np.float64).astype(np.float16)
+        assert np.array_equal(r["Y"].view(np.uint16), ref.view(np.uint16))
+
+
+def pin_tau_zero_is_fp16_matmul(orc):
+    """tau = 0: every column (zero columns included) is an outlier, so the int8
+    part vanishes and Y is the fp16 matmul X W^T rounded once."""
+    rng = np.random.default_rng(5)
+    X = rng.standard_normal((6, 40)).astype(np.float16)
+    X[:, 11] = 0  # a zero column still counts: |0| >= 0
+    W = (rng.standard_normal((10, 40)) * 0.1).astype(np.float16)
+    Wq, sw = orc.quantize_weight(W)
+    r = orc.linear(X, Wq, sw, W, 0.0)
+    assert r["O"].tolist() == list(range(40))
+    assert np.all(r["sx"] == 0) and not r["Xq"].any() and not r["acc"].any()
+    ref = (X.astype(np.float64) @ W.astype(np.float64).T).astype(np.float16)
+    assert np.array_equal(r["Y"].view(np.uint16), ref.view(np.uint16))
+
+
+def pin_outliers_are_column_scan(orc):
+    """The outlier set equals a direct numpy column scan of |X| >= tau."""
+    w = inputs.random_small(12, 300, 4, n_cols=5, seed=6)
+    for tau in (6.0, 3.0, 20.0, 0.0):
+        want = np.flatnonzero((np.abs(w.X.astype(np.float32)) >= np.float32(tau)).any(axis=0))
+        assert orc.outlier_columns(w.X, tau).tolist() == want.tolist()
+    tiny = inputs.tiny()
+    O = orc.outlier_columns(tiny.X, tiny.tau).tolist()
+    assert 7 in O and 133 in O
+
+
+def pin_permutation_invariance(orc):
+    """Permuting the K columns of X and W jointly permutes O and leaves acc
+    and Y bit-identical."""
+    w = inputs.random_small(9, 64, 12, n_cols=3, seed=7)
+    Wq, sw = orc.quantize_weight(w.W)
+    r = orc.linear(w.X, Wq, sw, w.W, w.tau)
+    perm = np.random.default_rng(8).permutation(64)
+    Xp, Wp = w.X[:, perm], w.W[:, perm]
+    Wqp, swp = orc.quantize_weight(Wp)
+    rp = orc.linear(Xp, Wqp, swp, Wp, w.tau)
+    assert sorted(perm[rp["O"]].tolist()) == r["O"].tolist()
+    assert np.array_equal(r["acc"], rp["acc"])
+    assert np.array_equal(r["Y"].view(np.uint16), rp["Y"].view(np.uint16))
+
+
+def pin_code_extremes(orc):
+    """Every row's codes reach +-127 unless its scale is zero; none is -128."""
+    w = inputs.random_small(10, 128, 20, n_cols=2, seed=9)
+    Wq, sw = orc.quantize_weight(w.W)
+    r = orc.linear(w.X, Wq, sw, w.W, w.tau)
+    for q, s in list(zip(r["Xq"], r["sx"])) + list(zip(Wq, sw)):
+        if s == 0:
+            assert not q.any()
+        else:
+            assert np.abs(q.astype(np.int32)).max() == 127
+        assert q.min() >= -127
+
+
+def pin_hand_example(orc):
+    """A worked example, derived by hand from the definitions.
+
+    X = [[1, -2, 8, 0.5], [3, 1, -1, 2]], W = [[0.5, 1, -1, 2], [-4, 2, 1, 0.25]],
+    tau = 6.  Column 2 holds 8 >= 6: O = [2].
+    sx = [max(1,2,0.5), max(3,1,2)] = [2, 3]; sw = [2, 4].
+    Xq row 0: 127/2 = 63.5 -> 64 (tie, even), -127, 0 (outlier), 31.75 -> 32.
+    Xq row 1: 127, 42.33 -> 42, 0, 84.67 -> 85.
+    Wq row 0: 31.75 -> 32, 63.5 -> 64, -63.5 -> -64, 127.
+    Wq row 1: -127, 63.5 -> 64, 31.75 -> 32, 7.9375 -> 8.
+    acc = [[2048-8128+4064, -8128-8128+256], [4064+2688+10795, -16129+2688+680]]
+        = [[-2016, -16000], [17547, -12761]].
+    out = X[:,2] W[:,2]^T = [[-8, 8], [1, -1]].
+    Y[0,0] = -2016*2*2/16129 - 8 = -8.49997 -> -8.5 (fp16 step 2^-7 there).
+    Y[0,1] = 8 - 128000/16129 = 1032/16129 = 0.063984 -> 1048 * 2^-14.
+    Y[1,0] = 105282/16129 + 1 = 7.527497 -> 1927 * 2^-8.
+    Y[1,1] = -153132/16129 - 1 = -10.494203 -> -1343 * 2^-7.
+    """
+    X = np.array([[1, -2, 8, 0.5], [3, 1, -1, 2]], np.float16)
+    W = np.array([[0.5, 1, -1, 2], [-4, 2, 1, 0.25]], np.float16)
+    Wq, sw = orc.quantize_weight(W)
+    r = orc.linear(X, Wq, sw, W, 6.0)
+    assert r["O"].tolist() == [2]
+    assert r["sx"].tolist() == [2.0, 3.0] and sw.tolist() == [2.0, 4.0]
+    assert r["Xq"].tolist() == [[64, -127, 0, 32], [127, 42, 0, 85]]
+    assert Wq.tolist() == [[32, 64, -64, 127], [-127, 64, 32, 8]]
+    assert r["acc"].tolist() == [[-2016, -16000], [17547, -12761]]
+    assert r["out"].tolist() == [[-8.0, 8.0], [1.0, -1.0]]
+    want = [[-8.5, 1048 * 2.0 ** -14], [1927 * 2.0 ** -8, -1343 * 2.0 ** -7]]
+    assert r["Y"].astype(np.float64).tolist() == want
+
+
+ALL_PINS = [
+    pin_half_roundtrip,
+    pin_code_rule_exhaustive,
+    pin_hand_example,
+    pin_brute_tiny_config,
+    pin_brute_random_small,
+    pin_tau_inf_integer_inputs,
+    pin_tau_zero_is_fp16_matmul,
+    pin_outliers_are_column_scan,
+    pin_permutation_invariance,
+    pin_code_extremes,
+]

@@ -1,0 +1,55 @@
+"""Planted mistakes in the oracle are caught by its pins (CPU only).
+
+Each case copies ``oracle/oracle.c`` to a temporary directory, changes one
+expression into a plausible mistake (a wrong comparison, a dropped term, a
+wrong sign or index, a transposed operand, a different rounding), compiles
+the copy and runs the pins on it: at least one pin must fail.  The real
+oracle is never modified.
+"""
+
+import os
+import shutil
+
+import pytest
+
+import oracle
+import oracle_pins
+from oracle import build_oracle
+
+MUTATIONS = {
+    "threshold_gt": ("if (x >= tau) hit = 1;", "if (x > tau) hit = 1;"),
+    "absmax_includes_outliers": ("if (flag_buf[k]) continue;", "(void)0;"),
+    "code_by_reciprocal": ("float q = rintf(num / a);", "float q = rintf(num * (1.0f / a));"),
+    "code_truncates": ("float q = rintf(num / a);", "float q = truncf(num / a);"),
+    "code_scale_128": ("float num = 127.0f * x;", "float num = 128.0f * x;"),
+    "drop_outlier_term": ("double v = p / 16129.0 + out[r * N + n];", "double v = p / 16129.0;"),
+    "outlier_term_sign": ("double v = p / 16129.0 + out[r * N + n];",
+                          "double v = p / 16129.0 - out[r * N + n];"),
+    "dequant_127": ("double v = p / 16129.0", "double v = p / 16384.0"),
+    "weight_index_reversed": ("s += (int64_t)x[k] * (int64_t)w[k];",
+                              "s += (int64_t)x[k] * (int64_t)w[K - 1 - k];"),
+    "transposed_weight": ("const int8_t *w = Wq + n * K;", "const int8_t *w = Wq + n;"),
+    "outlier_weight_from_row": ("orc_half_to_double(W16[n * K + O[j]]);",
+                                "orc_half_to_double(W16[O[j] * K + n % K]);"),
+    "half_round_floor": ("double n = rint(ldexp(a, 10 - E));", "double n = floor(ldexp(a, 10 - E));"),
+    "weight_scale_first_col": ("if (x > a) a = x;\n    }\n    sw[n] = a;",
+                               "if (k == 0) a = x;\n    }\n    sw[n] = a;"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_planted_mistake_is_caught(tmp_path, name):
+    old, new = MUTATIONS[name]
+    src = open(build_oracle.SRC).read()
+    assert src.count(old) == 1, f"mutation anchor not unique/present: {old!r}"
+    mut = tmp_path / "oracle_mut.c"
+    mut.write_text(src.replace(old, new))
+    lib = build_oracle.build(str(mut), str(tmp_path / "liboracle_mut.so"), extra=("-w",))
+    orc = oracle.Oracle(lib)
+    failed = []
+    for pin in oracle_pins.ALL_PINS:
+        try:
+            pin(orc)
+        except (AssertionError, IndexError, ValueError):
+            failed.append(pin.__name__)
+    assert failed, f"mutation {name} survived every pin"
