@@ -1,0 +1,492 @@
+#!/usr/bin/env python3
+"""Benchmark of the LLM.int8() decomposition linear on B300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload decode|prefill|large|sweep|tiny]
+
+Prints ONE JSON line (rank 0).  Metric: effective TOPS = 2*T*N*K / time of
+the int8 decomposition linear, whole job.
+
+Default workload: the decode GEMV configuration (X fp16 [16, 4096] with 4
+seeded outlier columns x U(8,60), W fp16 [4096, 4096] ~ N(0, 0.02), tau 6).
+A step is one token batch through a stack of 16 such layers, each with its
+own weight, so that the 16 x 16.8 MB of int8 weights (268 MB) exceed the
+126 MB L2 and every call streams its weight from HBM.  The timed region
+replays CUDA graphs of captured library calls; inputs are resident in HBM.
+
+`e2e` is the same metric through the public API with host buffers: per call
+a pinned host->device copy of X, the library call, and a device->host copy of
+Y, all inside the timed region.
+
+`roofline` is for the dominant kernel: its algorithmic bytes (or flops) per
+launch over its average duration, measured with CUDA events around each
+launch (library profiling mode) over an eager pass of the same steps.
+
+`--impl reference` times the CPU oracle (the reference arm of this build):
+each step is a bounded sample of the same workload (all rows of X, a
+rotating slice of output channels), so that the whole run ends in minutes.
+
+Multi-GPU (torchrun): replicas.  Each rank runs the same workload on its own
+batch with no collective on the data path (weak scaling); the time is the
+maximum over ranks between barriers.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import inputs  # noqa: E402
+
+METRIC = "int8-decomposed linear effective TOPS (2*T*N*K/s)"
+L2_BYTES = 126 * 1024 * 1024
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# workloads
+# ---------------------------------------------------------------------------
+
+def make_workload(name: str, T: int):
+    if name == "decode":
+        return inputs.decode(T=T)
+    if name == "prefill":
+        return inputs.prefill()
+    if name == "large":
+        return inputs.large()
+    if name == "sweep":
+        return inputs.sweep(0.001, 6.0)
+    if name == "tiny":
+        return inputs.tiny()
+    raise ValueError(name)
+
+
+def algorithmic_bytes(T, N, K, nO):
+    """Bytes the method must move for one call: X read once, Wq + scales read
+    once, the outlier columns of W16, Y written once."""
+    return 2 * T * K + N * K + 4 * N + 2 * N * nO + 2 * T * N
+
+
+def kernel_algorithmic(kernel, T, N, K, nO):
+    """(bytes, flops) per launch of one kernel, for the roofline."""
+    if kernel in ("gemv_decode", "decode_fused"):
+        # weight codes + scales + outlier weight columns + codes of X + Y
+        b = N * K + 4 * N + 2 * N * nO + T * K + 2 * T * N
+        if kernel == "decode_fused":
+            b += 2 * T * K - T * K  # reads fp16 X instead of int8 codes
+        return b, 2 * T * N * K
+    if kernel in ("gemm_mma", "gemm_tc"):
+        return N * K + 2 * T * K + 2 * T * N + 2 * N * nO, 2 * T * N * K + 2 * T * N * nO
+    if kernel == "outlier_scan":
+        return 2 * T * K, 0
+    if kernel == "quantize_rows":
+        return 2 * T * K + T * K + 2 * T * nO, 0
+    return 0, 0
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region (NVML reads only; nothing is set)
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    REASONS = {
+        "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20, "hw_thermal_slowdown": 0x40,
+        "hw_power_brake_slowdown": 0x80, "sw_power_cap": 0x4, "gpu_idle": 0x1,
+    }
+
+    def __init__(self, index: int, period: float = 0.02):
+        self.samples, self.reasons = [], set()
+        self.max_mhz = None
+        self._stop = threading.Event()
+        self.ok = False
+        try:
+            import pynvml
+            pynvml.nvmlInit()
+            self.nv = pynvml
+            self.h = pynvml.nvmlDeviceGetHandleByIndex(index)
+            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
+            self.ok = True
+        except Exception as e:  # no NVML: report it, do not guess
+            self.err = repr(e)
+        self.period = period
+
+    def _run(self):
+        while not self._stop.is_set():
+            try:
+                self.samples.append(self.nv.nvmlDeviceGetClockInfo(self.h, self.nv.NVML_CLOCK_SM))
+                r = self.nv.nvmlDeviceGetCurrentClocksEventReasons(self.h)
+                for k, bit in self.REASONS.items():
+                    if r & bit:
+                        self.reasons.add(k)
+            except Exception:
+                pass
+            time.sleep(self.period)
+
+    def __enter__(self):
+        if self.ok:
+            self.t = threading.Thread(target=self._run, daemon=True)
+            self.t.start()
+        return self
+
+    def __exit__(self, *a):
+        if self.ok:
+            self._stop.set()
+            self.t.join()
+
+    def summary(self):
+        if not self.ok:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvml_unavailable"]}
+        med = statistics.median(self.samples) if self.samples else None
+        return {"sm_mhz": med, "sm_max_mhz": self.max_mhz, "samples": len(self.samples),
+                "reasons": sorted(self.reasons - {"gpu_idle"})}
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (replicas)
+# ---------------------------------------------------------------------------
+
+def dist_setup(gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if os.environ.get("BENCH_BACKEND", "nccl") == "nccl" else "gloo"
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+def run_ours(args, world, rank, local):
+    import torch
+
+    from int8_mixed_precision_04_b300 import binding, build
+    build.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    lib = binding.load()
+
+    w = make_workload(args.workload, args.T)
+    T, K, N, tau = w.T, w.K, w.N, w.tau
+    wq_bytes = N * K
+    # enough distinct weights that one step's weight traffic exceeds 2x L2
+    layers = max(1, math.ceil(2 * L2_BYTES / (wq_bytes + 2 * N * K)))
+    if args.workload == "decode":
+        layers = max(layers, 16)
+    layers = min(layers, args.max_layers)
+
+    Xh = torch.from_numpy(w.X)
+    W16_0 = torch.from_numpy(w.W).to(dev)
+    W16s, Wqs, sws = [], [], []
+    for i in range(layers):
+        # distinct copies of the same weight (same numbers, distinct memory)
+        Wc = W16_0.clone() if i else W16_0
+        Wq, sw = binding.quantize_weight(Wc)
+        W16s.append(Wc)
+        Wqs.append(Wq)
+        sws.append(sw)
+    Xs = [Xh.to(dev) for _ in range(layers)]
+    Ys = [torch.empty((T, N), dtype=torch.float16, device=dev) for _ in range(layers)]
+    ws = torch.empty(binding.workspace_bytes(T, N, K), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def step(s):
+        for i in range(layers):
+            binding.linear(Xs[i], Wqs[i], sws[i], W16s[i], tau, Y=Ys[i], workspace=ws, stream=s)
+
+    # outlier count of this workload (for byte accounting)
+    dbg = binding.linear_debug(Xs[0], Wqs[0], sws[0], W16s[0], tau)
+    nO = int(dbg["nO"].item())
+    del dbg
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(args.warmup, 3)):
+            step(stream)
+    stream.synchronize()
+
+    # graphs: one graph per step-chunk of G steps
+    G = max(1, min(args.steps, 8 if layers >= 16 else 32))
+    before = lib.bnb_launch_count()
+    g_main = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_main, stream=stream):
+        for _ in range(G):
+            step(stream)
+    launches_per_step = (lib.bnb_launch_count() - before) / G
+    rem = args.steps % G
+    g_rem = None
+    if rem:
+        g_rem = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_rem, stream=stream):
+            for _ in range(rem):
+                step(stream)
+    for _ in range(2):
+        g_main.replay()
+    torch.cuda.synchronize()
+
+    start = torch.cuda.Event(enable_timing=True)
+    stop = torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local)
+    barrier(world)
+    torch.cuda.synchronize()
+    with sampler:
+        start.record(stream)
+        for _ in range(args.steps // G):
+            g_main.replay()
+        if g_rem is not None:
+            g_rem.replay()
+        stop.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    ms = start.elapsed_time(stop)
+    ms = max_over_ranks(ms, world, dev)
+    calls = args.steps * layers
+    ops = 2 * T * N * K
+    value = world * calls * ops / (ms * 1e-3) / 1e12
+    alg_bytes = algorithmic_bytes(T, N, K, nO)
+    gbs = world * calls * alg_bytes / (ms * 1e-3) / 1e9
+
+    # per-kernel durations: eager pass of the same steps with event timing
+    prof_steps = min(args.steps, max(1, 4000 // layers))
+    binding.profile_enable(True)
+    with torch.cuda.stream(stream):
+        for _ in range(prof_steps):
+            step(stream)
+    stream.synchronize()
+    binding.profile_enable(False)
+    prof = binding.profile_collect()
+    dominant = max(prof.items(), key=lambda kv: kv[1][0])
+    kname, (kms, kn) = dominant
+    kavg_s = kms / kn * 1e-3
+    kb, kf = kernel_algorithmic(kname, T, N, K, nO)
+    peaks, peak_src = load_peaks()
+    if kname in ("gemv_decode", "decode_fused", "outlier_scan", "quantize_rows") or T <= 16:
+        roof = {"bound": "hbm", "achieved": kb / kavg_s / 1e9, "peak": peaks["hbm_gbs"],
+                "unit": "GB/s"}
+    else:
+        roof = {"bound": "tensor", "achieved": kf / kavg_s / 1e12,
+                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = args.traffic
+    roof["kernel"] = kname
+    roof["peak_source"] = f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured" else peak_src
+    roof["kernel_avg_us"] = kavg_s * 1e6
+    roof["alg_bytes_per_launch"] = kb
+
+    # e2e through the public API with host buffers
+    Xpin = Xh.pin_memory()
+    Ypin = torch.empty((T, N), dtype=torch.float16).pin_memory()
+    e2e_calls = min(calls, args.e2e_calls)
+    with torch.cuda.stream(stream):
+        for i in range(min(10, e2e_calls)):
+            Xs[0].copy_(Xpin, non_blocking=True)
+            binding.linear(Xs[0], Wqs[i % layers], sws[i % layers], W16s[i % layers], tau,
+                           Y=Ys[0], workspace=ws, stream=stream)
+            Ypin.copy_(Ys[0], non_blocking=True)
+        stream.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        e0.record(stream)
+        for i in range(e2e_calls):
+            Xs[0].copy_(Xpin, non_blocking=True)
+            binding.linear(Xs[0], Wqs[i % layers], sws[i % layers], W16s[i % layers], tau,
+                           Y=Ys[0], workspace=ws, stream=stream)
+            Ypin.copy_(Ys[0], non_blocking=True)
+        e1.record(stream)
+        stream.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    e2e_val = world * e2e_calls * ops / (e2e_ms * 1e-3) / 1e12
+
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "TOPS",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms / args.steps,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "int8xint8->int32 + fp16 outliers, fp16 out",
+        "data": "synthetic (seeded, inputs module)",
+        "config": {
+            "workload": f"{args.workload}: X fp16 [{T},{K}], W fp16 [{N},{K}], tau {tau}",
+            "T": T, "K": K, "N": N, "tau": tau, "n_outliers": nO,
+            "layers_per_step": layers,
+            "l2": f"{layers} distinct weights per step ({layers * (wq_bytes) / 1e6:.0f} MB int8) "
+                  f"vs 126 MB L2",
+            "timing": "CUDA graph replay of captured library calls, CUDA events",
+            "parallelism": f"replicas x{world}",
+            "path": lib.bnb_int8_linear_path(T, N, K),
+        },
+        "gb_per_s": gbs,
+        "alg_bytes_per_call": alg_bytes,
+        "e2e": {"value": e2e_val, "unit": "TOPS", "h2d_bytes_per_step": 2 * T * K,
+                "d2h_bytes_per_step": 2 * T * N, "calls": e2e_calls,
+                "note": "per call: pinned H2D of X, bnb_int8_linear, D2H of Y (eager)"},
+        "gpu_launches": int(round(launches_per_step * args.steps)),
+        "launches_per_step": launches_per_step,
+        "roofline": roof,
+        "kernels": {k: {"avg_us": v[0] / v[1] * 1e3, "launches": v[1]} for k, v in prof.items()},
+        "clocks": sampler.summary(),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_budget)
+    return line
+
+
+# ---------------------------------------------------------------------------
+# the oracle on the host cores: cpu_baseline and --impl reference
+# ---------------------------------------------------------------------------
+
+class OracleArm:
+    """One bounded sample of the workload per step: activation pass over all
+    T rows, then S4..S6 for all T rows against a rotating slice of `n_slice`
+    output channels."""
+
+    def __init__(self, w, n_slice: int):
+        import oracle
+        self.orc = oracle.get()
+        self.w = w
+        self.Wq, self.sw = self.orc.quantize_weight(w.W)
+        self.n_slice = max(1, min(n_slice, w.N))
+        self.pos = 0
+
+    def step(self):
+        n0 = self.pos
+        n1 = min(self.w.N, n0 + self.n_slice)
+        self.pos = 0 if n1 >= self.w.N else n1
+        self.orc.linear(self.w.X, self.Wq[n0:n1], self.sw[n0:n1], self.w.W[n0:n1], self.w.tau)
+        return 2 * self.w.T * (n1 - n0) * self.w.K
+
+
+def _calibrate(w, target_s):
+    arm = OracleArm(w, 64)
+    t0 = time.perf_counter()
+    arm.step()
+    dt = time.perf_counter() - t0
+    per_chan = dt / 64
+    return max(1, int(target_s / max(per_chan, 1e-9)))
+
+
+def cpu_baseline(w, budget_s: float = 15.0):
+    import oracle
+    n_slice = _calibrate(w, budget_s / 4)
+    arm = OracleArm(w, n_slice)
+    ops = 0
+    t0 = time.perf_counter()
+    while time.perf_counter() - t0 < budget_s:
+        ops += arm.step()
+    dt = time.perf_counter() - t0
+    return {"value": ops / dt / 1e12, "unit": "TOPS", "cores": oracle.get().num_threads(),
+            "kind": "oracle",
+            "sample": f"{w.name}: all {w.T} rows x {ops // (2 * w.T * w.K)} output channels "
+                      f"({dt:.1f} s, slices of {n_slice} channels)"}
+
+
+def run_reference(args, world, rank, local):
+    if rank != 0:
+        return None
+    import oracle
+    w = make_workload(args.workload, args.T)
+    total_steps = args.steps + args.warmup
+    per_step = min(2.0, args.ref_budget / max(total_steps, 1))
+    n_slice = _calibrate(w, per_step)
+    arm = OracleArm(w, n_slice)
+    for _ in range(args.warmup):
+        arm.step()
+    ops = 0
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        ops += arm.step()
+    dt = time.perf_counter() - t0
+    val = ops / dt / 1e12
+    cores = oracle.get().num_threads()
+    sample = (f"{w.name}: per step all {w.T} rows x {n_slice} output channels "
+              f"(of {w.N}), K={w.K}")
+    return {
+        "impl": "reference",
+        "metric": METRIC, "value": val, "unit": "TOPS", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "int8xint8->int32 + fp16 outliers (CPU oracle, fp64 epilogue)",
+        "data": "synthetic (seeded, inputs module)",
+        "config": {"workload": f"{args.workload}: X fp16 [{w.T},{w.K}], W fp16 [{w.N},{w.K}], "
+                               f"tau {w.tau}", "T": w.T, "K": w.K, "N": w.N, "tau": w.tau},
+        "cpu_baseline": {"value": val, "unit": "TOPS", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": val, "unit": "TOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="decode",
+                    choices=["decode", "prefill", "large", "sweep", "tiny"])
+    ap.add_argument("--T", type=int, default=16, help="tokens of the decode workload")
+    ap.add_argument("--max-layers", type=int, default=64)
+    ap.add_argument("--e2e-calls", type=int, default=2000)
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--ref-budget", type=float, default=120.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="dram bytes per launch of the dominant kernel from an ncu capture")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    world, rank, local = dist_setup(args.gpus)
+    if args.impl == "reference":
+        line = run_reference(args, world, rank, local)
+    else:
+        line = run_ours(args, world, rank, local)
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

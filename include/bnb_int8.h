@@ -1,0 +1,174 @@
+/*
+ * bnb_int8.h -- C ABI of the LLM.int8() mixed-precision decomposition linear
+ * for NVIDIA B300 (sm_103a).
+ *
+ * The operation (Y = X W^T with outlier decomposition) is the one the pages
+ * describe as LLM.int8(): feature dimensions of the activations whose values
+ * are large ("outliers") are multiplied in 16-bit, every other value is
+ * quantized vector-wise to int8, multiplied in int8 and converted back to
+ * 16-bit at the end ("Hugging Face Quantization with bitsandbytes: 4-bit &
+ * 8-bit Models Explained", section 2 "LLM.int8(): Quantizing Without
+ * Degrading Large Models"; "bitsandbytes: GPU-Accelerated Inference and
+ * Training at Lower Bit Depths", section "How LLM.int8() quantizes weights
+ * and activations").  The outlier cut-off is llm_int8_threshold, default 6.0
+ * (same Hugging Face page, section 3).  Weights are quantized once, when the
+ * model is loaded ("bitsandbytes" glossary page, introduction).
+ *
+ * Definitions used by every call (T tokens, K features, N output channels):
+ *   O       = { k : |X[t,k]| >= tau for some t }, ascending       (outliers)
+ *   sx[t]   = max over k not in O of |X[t,k]|                     (row scale)
+ *   sw[n]   = max over all k of |W[n,k]|                          (channel scale)
+ *   Xq[t,k] = 0 for k in O, else rint(fl32(127 X[t,k]) / sx[t])    (ties to even;
+ *             0 when sx[t] = 0); Wq likewise with sw[n]
+ *   acc     = Xq Wq^T, exact int32
+ *   Y[t,n]  = fp16( acc[t,n] * (sx[t]/127) * (sw[n]/127)
+ *                   + sum_{k in O} X[t,k] * W16[n,k] )
+ *
+ * Conventions shared by all entry points:
+ *   - Every data pointer is a DEVICE pointer to a dense row-major array; the
+ *     caller allocates and owns all of them.  The library never allocates,
+ *     frees or synchronises (except bnb_last_device_status, which syncs the
+ *     given stream).
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Work is enqueued asynchronously on it.
+ *   - fp16 data is IEEE binary16, passed as void*.
+ *   - Argument errors are detected on the host before anything is enqueued;
+ *     in that case nothing is written.
+ *   - Alignment: every pointer 16-byte aligned, K a multiple of 16.
+ *   - Y must not alias X, W16, Wq or the workspace.
+ *   - X must be finite.  tau may be +INFINITY (no outliers); tau NaN or
+ *     negative is an argument error.
+ *   - Calls on different streams with different workspaces may run
+ *     concurrently; two calls that share a workspace must be ordered.
+ */
+#ifndef BNB_INT8_H
+#define BNB_INT8_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  BNB_OK = 0,
+  BNB_ERR_INVALID_ARG = 1, /* NULL pointer, T/N/K <= 0, tau NaN or < 0,
+                              workspace too small, aliasing output */
+  BNB_ERR_UNSUPPORTED = 2, /* K % 16 != 0, pointer not 16-byte aligned,
+                              size beyond the limits below, device is not
+                              compute capability 10.3 */
+  BNB_ERR_CUDA = 3,        /* a CUDA call or kernel launch failed */
+  BNB_ERR_TIMEOUT = 4      /* a bounded device-side wait gave up; reported
+                              through bnb_last_device_status */
+} bnb_status_t;
+
+/* Size limits of one call. */
+#define BNB_MAX_K (1 << 20)
+#define BNB_MAX_T (1 << 22)
+#define BNB_MAX_N (1 << 22)
+
+/*
+ * Bytes of device workspace that bnb_int8_linear / bnb_int8_linear_debug
+ * need for a call of this shape (0 for a non-positive dimension).  The
+ * workspace holds the outlier column mask and index list, the row scales,
+ * the activation codes and the compacted fp16 outlier block; it needs no
+ * initialisation and its contents after a call are unspecified except the
+ * device status word read by bnb_last_device_status.
+ */
+size_t bnb_int8_linear_workspace_bytes(int64_t T, int64_t N, int64_t K);
+
+/*
+ * Weight quantization, run once per weight (at load time).
+ *   W16    [N x K] fp16, input.
+ *   Wq     [N x K] int8, output: Wq[n,k] = rint(fl32(127 W16[n,k]) / sw[n]).
+ *   Wscale [N] fp32, output: sw[n] = max_k |W16[n,k]| (absmax, not absmax/127).
+ * Errors: BNB_ERR_INVALID_ARG (NULL, N<=0, K<=0), BNB_ERR_UNSUPPORTED
+ * (alignment, K % 16, limits, device), BNB_ERR_CUDA (launch).
+ */
+bnb_status_t bnb_int8_quantize_weight(const void *W16, int64_t N, int64_t K,
+                                      int8_t *Wq, float *Wscale, void *stream);
+
+/*
+ * The decomposition linear Y = X W^T (definitions above).
+ *   X      [T x K] fp16 activations.
+ *   Wq     [N x K] int8 and Wscale [N] fp32 from bnb_int8_quantize_weight.
+ *   W16    [N x K] fp16 weight, source of the outlier columns.
+ *   tau    outlier threshold (>= 0, may be +INFINITY).
+ *   Y      [T x N] fp16 output, written once.
+ *   workspace/workspace_bytes: at least bnb_int8_linear_workspace_bytes(T,N,K).
+ * The outlier set is computed per call from all T rows and stays on the
+ * device.  Errors as for bnb_int8_quantize_weight, plus BNB_ERR_INVALID_ARG
+ * for a small workspace.  A device-side wait that gives up writes
+ * BNB_ERR_TIMEOUT into the workspace status word.
+ */
+bnb_status_t bnb_int8_linear(const void *X, int64_t T, int64_t K, const int8_t *Wq,
+                             const float *Wscale, const void *W16, int64_t N,
+                             float tau, void *Y, void *workspace,
+                             size_t workspace_bytes, void *stream);
+
+/*
+ * bnb_int8_linear that also exports its intermediates (for parity tests).
+ * Same arguments as bnb_int8_linear, then (each may be NULL to skip):
+ *   Xq          [T x K] int8 activation codes (0 in outlier columns)
+ *   Xscale      [T] fp32 row scales sx
+ *   outlier_idx [K] int32, entries [0, n_outliers) hold O ascending
+ *   n_outliers  [1] int32, |O|
+ *   acc         [T x N] int32 exact accumulators Xq Wq^T
+ * Y is computed by the same kernels as bnb_int8_linear.
+ */
+bnb_status_t bnb_int8_linear_debug(const void *X, int64_t T, int64_t K,
+                                   const int8_t *Wq, const float *Wscale,
+                                   const void *W16, int64_t N, float tau, void *Y,
+                                   void *workspace, size_t workspace_bytes,
+                                   void *stream, int8_t *Xq, float *Xscale,
+                                   int32_t *outlier_idx, int32_t *n_outliers,
+                                   int32_t *acc);
+
+/*
+ * Synchronises `stream`, then reads the device status word of `workspace`
+ * into *out (BNB_OK, or BNB_ERR_TIMEOUT after a bounded wait gave up) and
+ * clears it.  Returns BNB_ERR_CUDA if the synchronisation or copy failed.
+ */
+bnb_status_t bnb_last_device_status(const void *workspace, void *stream, int32_t *out);
+
+/* Static, human-readable name of a status code. */
+const char *bnb_status_string(bnb_status_t s);
+
+/*
+ * Number of kernel launches this library has enqueued in this process
+ * (memsets included), for accounting in benchmarks.
+ */
+uint64_t bnb_launch_count(void);
+
+/*
+ * Which kernel path bnb_int8_linear takes for a shape: 1 = fused decode
+ * GEMV (small T), 2 = tensor-core GEMM (tcgen05), 3 = warp-level mma GEMM.
+ */
+int bnb_int8_linear_path(int64_t T, int64_t N, int64_t K);
+
+/*
+ * Per-kernel timing with CUDA events (off by default).  While enabled, every
+ * launch the library enqueues is bracketed by two events recorded on the
+ * launch's stream (events are created on demand and reused; no device memory
+ * is allocated).  Do not enable it while a stream is being captured into a
+ * CUDA graph.
+ *   bnb_profile_enable(1/0)     start / stop recording.
+ *   bnb_profile_collect(ms, n)  waits for the recorded events, adds each
+ *                               kernel's summed duration (ms) and launch count
+ *                               into ms[id] and n[id] for id in
+ *                               [0, bnb_profile_kernel_count()), then forgets
+ *                               the records.  Returns BNB_ERR_CUDA if an event
+ *                               query failed.
+ *   bnb_profile_kernel_name(id) static name of kernel id (NULL if out of range).
+ */
+void bnb_profile_enable(int on);
+bnb_status_t bnb_profile_collect(double *ms, uint64_t *n);
+int bnb_profile_kernel_count(void);
+const char *bnb_profile_kernel_name(int id);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BNB_INT8_H */

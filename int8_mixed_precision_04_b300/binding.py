@@ -1,0 +1,193 @@
+"""Thin ctypes binding of ``libbnbint8.so`` (argument marshalling only).
+
+Every function here has the name and arguments of a C entry point in
+``include/bnb_int8.h``; tensors are passed as device pointers, the stream as
+torch's current stream handle.  All arithmetic happens in the CUDA library.
+The library must have been built (``build.py`` / ``__graft_entry__.build``):
+there is no fallback, a missing library raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import enum
+import os
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libbnbint8.so")
+
+_P = ctypes.c_void_p
+_I64 = ctypes.c_int64
+
+
+class Status(enum.IntEnum):
+    OK = 0
+    INVALID_ARG = 1
+    UNSUPPORTED = 2
+    CUDA = 3
+    TIMEOUT = 4
+
+
+class BnbError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = Status(status) if status in Status._value2member_map_ else status
+        super().__init__(f"{where}: {self.status!r}")
+
+
+class Lib:
+    """The loaded C library with typed entry points."""
+
+    SYMBOLS = ("bnb_int8_linear_workspace_bytes", "bnb_int8_quantize_weight",
+               "bnb_int8_linear", "bnb_int8_linear_debug", "bnb_last_device_status",
+               "bnb_status_string", "bnb_launch_count", "bnb_int8_linear_path",
+               "bnb_profile_enable", "bnb_profile_collect", "bnb_profile_kernel_count",
+               "bnb_profile_kernel_name")
+
+    def __init__(self, path: str = LIB_PATH):
+        if not os.path.exists(path):
+            raise FileNotFoundError(
+                f"{path} is not built; run `python -m int8_mixed_precision_04_b300.build`")
+        self.path = path
+        L = ctypes.CDLL(path)
+        L.bnb_int8_linear_workspace_bytes.restype = ctypes.c_size_t
+        L.bnb_int8_linear_workspace_bytes.argtypes = [_I64, _I64, _I64]
+        L.bnb_int8_quantize_weight.restype = ctypes.c_int
+        L.bnb_int8_quantize_weight.argtypes = [_P, _I64, _I64, _P, _P, _P]
+        L.bnb_int8_linear.restype = ctypes.c_int
+        L.bnb_int8_linear.argtypes = [_P, _I64, _I64, _P, _P, _P, _I64, ctypes.c_float, _P, _P,
+                                      ctypes.c_size_t, _P]
+        L.bnb_int8_linear_debug.restype = ctypes.c_int
+        L.bnb_int8_linear_debug.argtypes = L.bnb_int8_linear.argtypes + [_P, _P, _P, _P, _P]
+        L.bnb_last_device_status.restype = ctypes.c_int
+        L.bnb_last_device_status.argtypes = [_P, _P, ctypes.POINTER(ctypes.c_int32)]
+        L.bnb_status_string.restype = ctypes.c_char_p
+        L.bnb_status_string.argtypes = [ctypes.c_int]
+        L.bnb_launch_count.restype = ctypes.c_uint64
+        L.bnb_launch_count.argtypes = []
+        L.bnb_int8_linear_path.restype = ctypes.c_int
+        L.bnb_int8_linear_path.argtypes = [_I64, _I64, _I64]
+        L.bnb_profile_enable.restype = None
+        L.bnb_profile_enable.argtypes = [ctypes.c_int]
+        L.bnb_profile_collect.restype = ctypes.c_int
+        L.bnb_profile_collect.argtypes = [ctypes.POINTER(ctypes.c_double),
+                                          ctypes.POINTER(ctypes.c_uint64)]
+        L.bnb_profile_kernel_count.restype = ctypes.c_int
+        L.bnb_profile_kernel_count.argtypes = []
+        L.bnb_profile_kernel_name.restype = ctypes.c_char_p
+        L.bnb_profile_kernel_name.argtypes = [ctypes.c_int]
+        self.c = L
+
+    def __getattr__(self, name):
+        return getattr(self.c, name)
+
+
+_lib = None
+
+
+def load() -> Lib:
+    global _lib
+    if _lib is None:
+        _lib = Lib()
+    return _lib
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(rc, where):
+    if rc != 0:
+        raise BnbError(rc, where)
+
+
+def workspace_bytes(T: int, N: int, K: int) -> int:
+    return load().bnb_int8_linear_workspace_bytes(T, N, K)
+
+
+def quantize_weight(W16, Wq=None, Wscale=None, stream=None):
+    """bnb_int8_quantize_weight: W16 [N,K] fp16 (cuda) -> (Wq int8 [N,K], sw fp32 [N])."""
+    import torch
+    N, K = W16.shape
+    if Wq is None:
+        Wq = torch.empty((N, K), dtype=torch.int8, device=W16.device)
+    if Wscale is None:
+        Wscale = torch.empty((N,), dtype=torch.float32, device=W16.device)
+    rc = load().bnb_int8_quantize_weight(_ptr(W16), N, K, _ptr(Wq), _ptr(Wscale), _stream(stream))
+    _check(rc, "bnb_int8_quantize_weight")
+    return Wq, Wscale
+
+
+def _alloc_ws(T, N, K, device):
+    import torch
+    return torch.empty((workspace_bytes(T, N, K),), dtype=torch.uint8, device=device)
+
+
+def linear(X, Wq, Wscale, W16, tau: float, Y=None, workspace=None, stream=None):
+    """bnb_int8_linear: X [T,K] fp16 -> Y [T,N] fp16 (all cuda tensors)."""
+    import torch
+    T, K = X.shape
+    N = Wq.shape[0]
+    if Y is None:
+        Y = torch.empty((T, N), dtype=torch.float16, device=X.device)
+    if workspace is None:
+        workspace = _alloc_ws(T, N, K, X.device)
+    rc = load().bnb_int8_linear(_ptr(X), T, K, _ptr(Wq), _ptr(Wscale), _ptr(W16), N,
+                                float(tau), _ptr(Y), _ptr(workspace), workspace.numel(),
+                                _stream(stream))
+    _check(rc, "bnb_int8_linear")
+    return Y
+
+
+def linear_debug(X, Wq, Wscale, W16, tau: float, stream=None, want_acc: bool = True):
+    """bnb_int8_linear_debug; returns dict(Y, Xq, sx, O, acc) as cuda tensors."""
+    import torch
+    T, K = X.shape
+    N = Wq.shape[0]
+    dev = X.device
+    Y = torch.empty((T, N), dtype=torch.float16, device=dev)
+    Xq = torch.empty((T, K), dtype=torch.int8, device=dev)
+    sx = torch.empty((T,), dtype=torch.float32, device=dev)
+    O = torch.empty((K,), dtype=torch.int32, device=dev)
+    nO = torch.empty((1,), dtype=torch.int32, device=dev)
+    acc = torch.empty((T, N), dtype=torch.int32, device=dev) if want_acc else None
+    ws = _alloc_ws(T, N, K, dev)
+    rc = load().bnb_int8_linear_debug(_ptr(X), T, K, _ptr(Wq), _ptr(Wscale), _ptr(W16), N,
+                                      float(tau), _ptr(Y), _ptr(ws), ws.numel(), _stream(stream),
+                                      _ptr(Xq), _ptr(sx), _ptr(O), _ptr(nO), _ptr(acc))
+    _check(rc, "bnb_int8_linear_debug")
+    return {"Y": Y, "Xq": Xq, "sx": sx, "O": O, "nO": nO, "acc": acc, "workspace": ws}
+
+
+def last_device_status(workspace, stream=None) -> int:
+    out = ctypes.c_int32(0)
+    rc = load().bnb_last_device_status(_ptr(workspace), _stream(stream), ctypes.byref(out))
+    _check(rc, "bnb_last_device_status")
+    return out.value
+
+
+def launch_count() -> int:
+    return load().bnb_launch_count()
+
+
+def linear_path(T: int, N: int, K: int) -> int:
+    return load().bnb_int8_linear_path(T, N, K)
+
+
+def profile_enable(on: bool) -> None:
+    load().bnb_profile_enable(1 if on else 0)
+
+
+def profile_collect() -> dict:
+    """{kernel name: (total ms, launches)} recorded since the last collect."""
+    L = load()
+    n = L.bnb_profile_kernel_count()
+    ms = (ctypes.c_double * n)()
+    cnt = (ctypes.c_uint64 * n)()
+    _check(L.bnb_profile_collect(ms, cnt), "bnb_profile_collect")
+    return {L.bnb_profile_kernel_name(i).decode(): (ms[i], cnt[i]) for i in range(n) if cnt[i]}

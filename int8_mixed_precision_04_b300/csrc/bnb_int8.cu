@@ -1,0 +1,253 @@
+// C-ABI host layer: argument validation, workspace carving, kernel dispatch.
+// Declarations and the contract of every entry point are in include/bnb_int8.h.
+#include <atomic>
+#include <cmath>
+#include <cstring>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace bnb {
+
+static std::atomic<uint64_t> g_launches{0};
+void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+static inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+static inline bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+struct Layout {
+  size_t status, counters, colmask, O, sx, xcodes, xo, total;
+  int64_t kpad;
+};
+
+static Layout layout_of(int64_t T, int64_t K) {
+  Layout L;
+  L.kpad = (K + 63) / 64 * 64;
+  size_t off = 0;
+  L.status = off;
+  off += 256;
+  L.counters = off;
+  off += 256;
+  L.colmask = off;
+  off += align_up((size_t)((K + 31) / 32) * 4, 256);
+  L.O = off;
+  off += align_up((size_t)(K + 64) * 4, 256);
+  L.sx = off;
+  off += align_up((size_t)T * 4, 256);
+  L.xcodes = off;
+  off += align_up((size_t)T * (size_t)K * 2, 256);
+  L.xo = off;
+  off += align_up((size_t)T * (size_t)L.kpad * 2, 256);
+  L.total = off;
+  return L;
+}
+
+static constexpr size_t kWsSlack = 256;  // the carved layout starts at the next 256-byte boundary
+
+static Workspace carve(void *ws, int64_t T, int64_t K) {
+  const Layout L = layout_of(T, K);
+  char *base = reinterpret_cast<char *>(align_up((uintptr_t)ws, 256));
+  Workspace w;
+  w.status = reinterpret_cast<int32_t *>(base + L.status);
+  w.counters = reinterpret_cast<uint32_t *>(base + L.counters);
+  w.colmask = reinterpret_cast<uint32_t *>(base + L.colmask);
+  w.O = reinterpret_cast<int32_t *>(base + L.O);
+  w.sx = reinterpret_cast<float *>(base + L.sx);
+  w.xcodes = base + L.xcodes;
+  w.xo = reinterpret_cast<__half *>(base + L.xo);
+  w.kpad = L.kpad;
+  return w;
+}
+
+// Exact fp16 value of a bit pattern (host side).
+static double half_bits_value(uint32_t h) {
+  const int e = (h >> 10) & 0x1f, m = h & 0x3ff;
+  if (e == 0) return std::ldexp((double)m, -24);
+  if (e == 31) return INFINITY;
+  return std::ldexp((double)(1024 + m), e - 25);
+}
+
+// Smallest non-negative fp16 bit pattern whose value is >= tau (0x7c00, the
+// infinity pattern, when no finite fp16 value reaches tau).  For finite fp16
+// x:  |x| >= tau  <=>  (bits(x) & 0x7fff) >= threshold_bits(tau).
+static uint32_t threshold_bits(float tau) {
+  uint32_t lo = 0, hi = 0x7c00;  // answer in [lo, hi]
+  while (lo < hi) {
+    const uint32_t mid = (lo + hi) / 2;
+    if (half_bits_value(mid) >= (double)tau)
+      hi = mid;
+    else
+      lo = mid + 1;
+  }
+  return lo;
+}
+
+static int device_sms(int dev) {
+  static std::atomic<int> cache[64];
+  if (dev < 0 || dev >= 64) return kB300Sms;
+  int v = cache[dev].load(std::memory_order_relaxed);
+  if (v > 0) return v;
+  if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
+    v = kB300Sms;
+  cache[dev].store(v, std::memory_order_relaxed);
+  return v;
+}
+
+// BNB_OK if the current device is compute capability 10.3.
+static bnb_status_t check_device(int *dev_out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return BNB_ERR_CUDA;
+  static std::atomic<int> ok_cache[64];
+  if (dev >= 0 && dev < 64 && ok_cache[dev].load(std::memory_order_relaxed) == 1) {
+    *dev_out = dev;
+    return BNB_OK;
+  }
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+    return BNB_ERR_CUDA;
+  if (major != 10 || minor != 3) return BNB_ERR_UNSUPPORTED;
+  if (dev >= 0 && dev < 64) ok_cache[dev].store(1, std::memory_order_relaxed);
+  *dev_out = dev;
+  return BNB_OK;
+}
+
+static bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
+  const uintptr_t x = (uintptr_t)a, y = (uintptr_t)b;
+  return x < y + nb && y < x + na;
+}
+
+// T <= 16 and the codes fit the GEMV's shared-memory block.
+static int choose_path(int64_t T, int64_t N, int64_t K) {
+  (void)N;
+  const int64_t pitch = (K + 127) / 128 * 128 + 64;
+  if (T <= 16 && 16 * pitch <= 200 * 1024) return 1;
+  return 3;
+}
+
+static bnb_status_t linear_impl(const void *X, int64_t T, int64_t K, const int8_t *Wq,
+                                const float *Wscale, const void *W16, int64_t N, float tau,
+                                void *Y, void *workspace, size_t workspace_bytes,
+                                void *stream_v, int8_t *dbg_xq, float *dbg_sx,
+                                int32_t *dbg_O, int32_t *dbg_nO, int32_t *dbg_acc) {
+  if (!X || !Wq || !Wscale || !W16 || !Y || !workspace) return BNB_ERR_INVALID_ARG;
+  if (T <= 0 || N <= 0 || K <= 0) return BNB_ERR_INVALID_ARG;
+  if (std::isnan(tau) || tau < 0.0f) return BNB_ERR_INVALID_ARG;
+  if (T > BNB_MAX_T || N > BNB_MAX_N || K > BNB_MAX_K) return BNB_ERR_UNSUPPORTED;
+  if (workspace_bytes < bnb_int8_linear_workspace_bytes(T, N, K)) return BNB_ERR_INVALID_ARG;
+  if (K % 16 != 0) return BNB_ERR_UNSUPPORTED;
+  if (!aligned16(X) || !aligned16(Wq) || !aligned16(Wscale) || !aligned16(W16) ||
+      !aligned16(Y) || !aligned16(workspace))
+    return BNB_ERR_UNSUPPORTED;
+  if ((dbg_xq && !aligned16(dbg_xq)) || (dbg_acc && !aligned16(dbg_acc)))
+    return BNB_ERR_UNSUPPORTED;
+  const size_t ybytes = (size_t)T * (size_t)N * 2;
+  if (overlaps(Y, ybytes, X, (size_t)T * K * 2) || overlaps(Y, ybytes, W16, (size_t)N * K * 2) ||
+      overlaps(Y, ybytes, Wq, (size_t)N * K) || overlaps(Y, ybytes, workspace, workspace_bytes))
+    return BNB_ERR_INVALID_ARG;
+  int dev = 0;
+  bnb_status_t st = check_device(&dev);
+  if (st != BNB_OK) return st;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_v);
+  const Workspace ws = carve(workspace, T, K);
+  const int path = choose_path(T, N, K);
+  const uint32_t thr = threshold_bits(tau);
+  // status word, counters and the outlier column mask are contiguous and
+  // zeroed by every call with one memset
+  const size_t zero_bytes = 512 + (size_t)((K + 31) / 32) * 4;
+  {
+    ProfScope ps(kKidMemset, stream);
+    if (cudaMemsetAsync(ws.status, 0, zero_bytes, stream) != cudaSuccess) return BNB_ERR_CUDA;
+  }
+  note_launch();
+  cudaError_t e = launch_act_pass(X, T, K, thr, ws, /*code_mode=*/0, /*with_xo=*/true, dbg_xq,
+                                  device_sms(dev), stream);
+  if (e != cudaSuccess) return BNB_ERR_CUDA;
+  if (path == 1)
+    e = launch_gemv_decode(T, K, Wq, Wscale, W16, N, Y, ws, dbg_acc, stream);
+  else
+    e = launch_gemm_mma(T, K, Wq, Wscale, W16, N, Y, ws, dbg_acc, stream);
+  if (e != cudaSuccess) return BNB_ERR_CUDA;
+  if (dbg_sx && cudaMemcpyAsync(dbg_sx, ws.sx, (size_t)T * 4, cudaMemcpyDeviceToDevice, stream) != cudaSuccess)
+    return BNB_ERR_CUDA;
+  if (dbg_O && cudaMemcpyAsync(dbg_O, ws.O, (size_t)K * 4, cudaMemcpyDeviceToDevice, stream) != cudaSuccess)
+    return BNB_ERR_CUDA;
+  if (dbg_nO && cudaMemcpyAsync(dbg_nO, ws.counters + 1, 4, cudaMemcpyDeviceToDevice, stream) != cudaSuccess)
+    return BNB_ERR_CUDA;
+  return BNB_OK;
+}
+
+}  // namespace bnb
+
+using namespace bnb;
+
+extern "C" {
+
+size_t bnb_int8_linear_workspace_bytes(int64_t T, int64_t N, int64_t K) {
+  (void)N;
+  if (T <= 0 || N <= 0 || K <= 0 || T > BNB_MAX_T || N > BNB_MAX_N || K > BNB_MAX_K) return 0;
+  return layout_of(T, K).total + kWsSlack;
+}
+
+bnb_status_t bnb_int8_quantize_weight(const void *W16, int64_t N, int64_t K, int8_t *Wq,
+                                      float *Wscale, void *stream) {
+  if (!W16 || !Wq || !Wscale) return BNB_ERR_INVALID_ARG;
+  if (N <= 0 || K <= 0) return BNB_ERR_INVALID_ARG;
+  if (N > BNB_MAX_N || K > BNB_MAX_K) return BNB_ERR_UNSUPPORTED;
+  if (K % 16 != 0 || !aligned16(W16) || !aligned16(Wq) || !aligned16(Wscale))
+    return BNB_ERR_UNSUPPORTED;
+  if (overlaps(Wq, (size_t)N * K, W16, (size_t)N * K * 2)) return BNB_ERR_INVALID_ARG;
+  int dev = 0;
+  bnb_status_t st = check_device(&dev);
+  if (st != BNB_OK) return st;
+  cudaError_t e = launch_quantize_weight(W16, N, K, Wq, Wscale, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? BNB_OK : BNB_ERR_CUDA;
+}
+
+bnb_status_t bnb_int8_linear(const void *X, int64_t T, int64_t K, const int8_t *Wq,
+                             const float *Wscale, const void *W16, int64_t N, float tau,
+                             void *Y, void *workspace, size_t workspace_bytes, void *stream) {
+  return linear_impl(X, T, K, Wq, Wscale, W16, N, tau, Y, workspace, workspace_bytes, stream,
+                     nullptr, nullptr, nullptr, nullptr, nullptr);
+}
+
+bnb_status_t bnb_int8_linear_debug(const void *X, int64_t T, int64_t K, const int8_t *Wq,
+                                   const float *Wscale, const void *W16, int64_t N, float tau,
+                                   void *Y, void *workspace, size_t workspace_bytes,
+                                   void *stream, int8_t *Xq, float *Xscale,
+                                   int32_t *outlier_idx, int32_t *n_outliers, int32_t *acc) {
+  return linear_impl(X, T, K, Wq, Wscale, W16, N, tau, Y, workspace, workspace_bytes, stream,
+                     Xq, Xscale, outlier_idx, n_outliers, acc);
+}
+
+bnb_status_t bnb_last_device_status(const void *workspace, void *stream, int32_t *out) {
+  if (!workspace || !out) return BNB_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return BNB_ERR_CUDA;
+  int32_t *status = reinterpret_cast<int32_t *>(align_up((uintptr_t)workspace, 256));
+  int32_t v = 0;
+  if (cudaMemcpy(&v, status, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return BNB_ERR_CUDA;
+  if (cudaMemset(status, 0, 4) != cudaSuccess) return BNB_ERR_CUDA;
+  *out = v;
+  return BNB_OK;
+}
+
+const char *bnb_status_string(bnb_status_t s) {
+  switch (s) {
+    case BNB_OK: return "BNB_OK";
+    case BNB_ERR_INVALID_ARG: return "BNB_ERR_INVALID_ARG";
+    case BNB_ERR_UNSUPPORTED: return "BNB_ERR_UNSUPPORTED";
+    case BNB_ERR_CUDA: return "BNB_ERR_CUDA";
+    case BNB_ERR_TIMEOUT: return "BNB_ERR_TIMEOUT";
+  }
+  return "BNB_ERR_UNKNOWN";
+}
+
+uint64_t bnb_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int bnb_int8_linear_path(int64_t T, int64_t N, int64_t K) {
+  if (T <= 0 || N <= 0 || K <= 0) return 0;
+  return choose_path(T, N, K);
+}
+
+}  // extern "C"

@@ -1,0 +1,61 @@
+// Internal launch interface between the C-ABI host layer and the kernels.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+
+namespace bnb {
+
+// Process-wide count of kernel launches issued by this library.
+void note_launch();
+
+// Kernel ids of the per-kernel event timing (names in profile.cu).
+enum KernelId {
+  kKidMemset = 0,
+  kKidOutlierScan,
+  kKidQuantRows,
+  kKidGemv,
+  kKidGemmMma,
+  kKidGemmTc,
+  kKidQuantWeight,
+  kKidDecodeFused,
+  kKernelCount
+};
+
+// Brackets one launch with two events when profiling is enabled (no-op
+// otherwise).
+class ProfScope {
+ public:
+  ProfScope(int kid, cudaStream_t s);
+  ~ProfScope();
+  ProfScope(const ProfScope &) = delete;
+  ProfScope &operator=(const ProfScope &) = delete;
+
+ private:
+  int kid_;
+  cudaStream_t s_;
+  cudaEvent_t a_;
+};
+
+cudaError_t launch_quantize_weight(const void *W16, int64_t N, int64_t K, int8_t *Wq,
+                                   float *sw, cudaStream_t stream);
+
+// S2 + S3.  code_mode 0: int8 codes, 1: fp16 integer codes.  with_xo: write
+// the padded fp16 outlier block.
+cudaError_t launch_act_pass(const void *X, int64_t T, int64_t K, uint32_t thr_bits,
+                            const Workspace &ws, int code_mode, bool with_xo,
+                            int8_t *dbg_xq, int num_sms, cudaStream_t stream);
+
+// S4..S6 for small T (T <= 16): int8 codes from the workspace.
+cudaError_t launch_gemv_decode(int64_t T, int64_t K, const int8_t *Wq, const float *sw,
+                               const void *W16, int64_t N, void *Y, const Workspace &ws,
+                               int32_t *dbg_acc, cudaStream_t stream);
+
+// S4..S6 with warp-level mma.sync (legacy tensor path), int8 codes.
+cudaError_t launch_gemm_mma(int64_t T, int64_t K, const int8_t *Wq, const float *sw,
+                            const void *W16, int64_t N, void *Y, const Workspace &ws,
+                            int32_t *dbg_acc, cudaStream_t stream);
+
+}  // namespace bnb

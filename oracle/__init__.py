@@ -56,6 +56,9 @@ class Oracle:
             getattr(lib, name).restype = ctypes.c_int
         self.lib = lib
 
+    def num_threads(self) -> int:
+        return int(self.lib.orc_num_threads())
+
     # ---- elementwise helpers -------------------------------------------------
     def half_to_double(self, bits: int) -> float:
         return self.lib.orc_half_to_double(bits)

@@ -36,6 +36,7 @@
  * (oracle/build_oracle.py).
  */
 #include <math.h>
+#include <omp.h>
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
@@ -43,6 +44,9 @@
 #define ORC_OK 0
 #define ORC_ERR_RANGE 1 /* an int32 accumulator would overflow */
 #define ORC_ERR_ARG 2
+
+/* Threads the OpenMP loops below use (for reporting a CPU baseline). */
+int orc_num_threads(void) { return omp_get_max_threads(); }
 
 /* ---- fp16 <-> double, written from the IEEE 754 binary16 definition ---- */
 

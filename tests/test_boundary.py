@@ -1,0 +1,125 @@
+"""The C-ABI library: it loads, exports every declared symbol, and rejects bad
+arguments on the host before touching a device (CPU only)."""
+
+import ctypes
+import math
+import os
+import re
+
+import pytest
+
+from int8_mixed_precision_04_b300 import binding, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADERS = [os.path.join(ROOT, "include", f) for f in os.listdir(os.path.join(ROOT, "include"))
+           if f.endswith(".h")]
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return binding.Lib()
+
+
+def declared_functions():
+    names = set()
+    for h in HEADERS:
+        text = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        for m in re.finditer(r"^\s*[A-Za-z_][\w\s\*]*?\b(bnb_\w+)\s*\(", text, flags=re.M):
+            names.add(m.group(1))
+    return sorted(names)
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for want in ("bnb_int8_quantize_weight", "bnb_int8_linear", "bnb_int8_linear_debug",
+                 "bnb_int8_linear_workspace_bytes", "bnb_last_device_status", "bnb_status_string"):
+        assert want in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib.c, name), name
+    for name in binding.Lib.SYMBOLS:
+        assert name in declared_functions(), name
+
+
+def test_status_strings(lib):
+    for s in binding.Status:
+        assert lib.bnb_status_string(int(s)).decode() == "BNB_ERR_" + s.name if s else True
+    assert lib.bnb_status_string(0) == b"BNB_OK"
+    assert lib.bnb_status_string(99) == b"BNB_ERR_UNKNOWN"
+
+
+def test_workspace_bytes(lib):
+    assert lib.bnb_int8_linear_workspace_bytes(0, 1, 16) == 0
+    assert lib.bnb_int8_linear_workspace_bytes(1, 0, 16) == 0
+    assert lib.bnb_int8_linear_workspace_bytes(-1, 1, 16) == 0
+    small = lib.bnb_int8_linear_workspace_bytes(16, 256, 256)
+    big = lib.bnb_int8_linear_workspace_bytes(4096, 28672, 8192)
+    # at least the codes (2 B/elem worst case) and the padded outlier block
+    assert big >= 4096 * 8192 * 4
+    assert small < big
+    assert lib.bnb_int8_linear_workspace_bytes(1 << 23, 16, 16) == 0  # beyond BNB_MAX_T
+
+
+FAKE = 0x10000  # 16-byte aligned, never dereferenced: every case fails on the host
+
+
+def _linear(lib, X=FAKE, T=16, K=256, Wq=FAKE, sw=FAKE, W16=FAKE, N=256, tau=6.0, Y=FAKE * 64,
+            ws=FAKE * 256, ws_bytes=None):
+    if ws_bytes is None:
+        ws_bytes = lib.bnb_int8_linear_workspace_bytes(T, N, K) if T > 0 and N > 0 and K > 0 else 0
+    return lib.bnb_int8_linear(X, T, K, Wq, sw, W16, N, ctypes.c_float(tau), Y, ws, ws_bytes, None)
+
+
+@pytest.mark.parametrize("case,want", [
+    (dict(X=None), binding.Status.INVALID_ARG),
+    (dict(Wq=None), binding.Status.INVALID_ARG),
+    (dict(sw=None), binding.Status.INVALID_ARG),
+    (dict(W16=None), binding.Status.INVALID_ARG),
+    (dict(Y=None), binding.Status.INVALID_ARG),
+    (dict(ws=None), binding.Status.INVALID_ARG),
+    (dict(T=0), binding.Status.INVALID_ARG),
+    (dict(N=-3), binding.Status.INVALID_ARG),
+    (dict(K=0), binding.Status.INVALID_ARG),
+    (dict(tau=math.nan), binding.Status.INVALID_ARG),
+    (dict(tau=-1.0), binding.Status.INVALID_ARG),
+    (dict(ws_bytes=100), binding.Status.INVALID_ARG),
+    (dict(K=24, ws_bytes=1 << 30), binding.Status.UNSUPPORTED),
+    (dict(X=FAKE + 8), binding.Status.UNSUPPORTED),
+    (dict(Y=FAKE * 64 + 4), binding.Status.UNSUPPORTED),
+    (dict(T=1 << 23, ws_bytes=1 << 40), binding.Status.UNSUPPORTED),
+    (dict(Y=FAKE), binding.Status.INVALID_ARG),  # Y aliases X
+])
+def test_linear_rejects_on_host(lib, case, want):
+    assert _linear(lib, **case) == want
+
+
+@pytest.mark.parametrize("args,want", [
+    ((None, 4, 16, FAKE, FAKE), binding.Status.INVALID_ARG),
+    ((FAKE, 0, 16, FAKE, FAKE), binding.Status.INVALID_ARG),
+    ((FAKE, 4, 20, FAKE, FAKE), binding.Status.UNSUPPORTED),
+    ((FAKE, 4, 16, FAKE + 1, FAKE), binding.Status.UNSUPPORTED),
+    ((FAKE, 4, 16, FAKE, None), binding.Status.INVALID_ARG),
+])
+def test_quantize_weight_rejects_on_host(lib, args, want):
+    assert lib.bnb_int8_quantize_weight(*args, None) == want
+
+
+def test_last_device_status_rejects_null(lib):
+    out = ctypes.c_int32(0)
+    assert lib.bnb_last_device_status(None, None, ctypes.byref(out)) == binding.Status.INVALID_ARG
+
+
+def test_paths(lib):
+    assert lib.bnb_int8_linear_path(16, 4096, 4096) == 1
+    assert lib.bnb_int8_linear_path(1, 4096, 4096) == 1
+    assert lib.bnb_int8_linear_path(17, 4096, 4096) in (2, 3)
+    assert lib.bnb_int8_linear_path(2048, 11008, 4096) in (2, 3)
+    assert lib.bnb_int8_linear_path(0, 1, 16) == 0
+
+
+def test_missing_library_raises(tmp_path):
+    with pytest.raises(FileNotFoundError):
+        binding.Lib(str(tmp_path / "nope.so"))

@@ -1,0 +1,111 @@
+"""CUDA path vs the oracle, element by element, through the C ABI (GPU)."""
+
+import math
+
+import numpy as np
+import pytest
+
+import inputs
+from parity import run_and_compare, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    import torch
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    from int8_mixed_precision_04_b300 import binding, build
+    build.build()
+    binding.load()
+
+
+def test_tiny(orc):
+    w = inputs.tiny()
+    r, ref = run_and_compare(orc, w.X, w.W, w.tau, what="tiny")
+    assert 7 in ref["O"] and 133 in ref["O"]
+
+
+@pytest.mark.parametrize("T", inputs.DECODE_TS)
+def test_decode(orc, T):
+    w = inputs.decode(T=T)
+    run_and_compare(orc, w.X, w.W, w.tau, what=f"decode T={T}")
+
+
+@pytest.mark.parametrize("T,K,N,ncols", [
+    (1, 16, 1, 0), (3, 48, 7, 1), (16, 272, 129, 2), (17, 64, 300, 3), (33, 1040, 65, 4),
+    (130, 512, 257, 5), (200, 2064, 131, 7), (257, 128, 1000, 2), (64, 4096, 64, 9),
+])
+@pytest.mark.parametrize("tau", [6.0, 3.0, 0.0, math.inf])
+def test_ragged_shapes(orc, T, K, N, ncols, tau):
+    w = inputs.random_small(T, K, N, ncols, seed=T * 7 + K + N, tau=tau)
+    run_and_compare(orc, w.X, w.W, tau, what=f"T{T} K{K} N{N} tau{tau}")
+
+
+@pytest.mark.parametrize("T", [5, 40])
+def test_edge_rows(orc, T):
+    """An all-zero row, a row whose every column is an outlier, a value exactly
+    at the threshold, and zero weight rows."""
+    w = inputs.random_small(T, 320, 96, 3, seed=99)
+    X, W = w.X.copy(), w.W.copy()
+    X[1] = 0
+    X[2] = 9.0
+    X[3, 10] = -6.0
+    W[5] = 0
+    run_and_compare(orc, X, W, 6.0, what="edge rows")
+
+
+@pytest.mark.parametrize("T,K", [(16, 8192), (256, 8192), (48, 1024)])
+@pytest.mark.parametrize("adversarial", [False, True])
+def test_integer_inputs_exact(orc, T, K, adversarial):
+    """tau = inf on integer inputs: codes equal the inputs and acc is the exact
+    integer product, up to 127^2 * K in magnitude (1.3e8 at K = 8192)."""
+    X, W = inputs.int_valued(T, K, 72, seed=5, adversarial=adversarial)
+    r, ref = run_and_compare(orc, X, W, math.inf, what="integer inputs")
+    if adversarial:
+        assert np.abs(ref["acc"]).max() == 127 * 127 * K
+
+
+def test_workspace_reuse(orc):
+    """Consecutive calls on one workspace with different thresholds."""
+    import torch
+
+    from int8_mixed_precision_04_b300 import binding
+    w = inputs.random_small(24, 256, 40, 4, seed=3)
+    X = torch.from_numpy(w.X).cuda()
+    W = torch.from_numpy(w.W).cuda()
+    Wq, sw = binding.quantize_weight(W)
+    ws = torch.empty(binding.workspace_bytes(24, 40, 256), dtype=torch.uint8, device="cuda")
+    Wq_o, sw_o = orc.quantize_weight(w.W)
+    for tau in (6.0, 0.0, math.inf, 3.0, 6.0):
+        Y = binding.linear(X, Wq, sw, W, tau, workspace=ws)
+        ref = orc.linear(w.X, Wq_o, sw_o, w.W, tau)
+        from parity import check_y
+        check_y(Y.cpu().numpy(), ref["Y"], f"reuse tau={tau}")
+
+
+@pytest.mark.parametrize("frac", inputs.SWEEP_FRACTIONS)
+@pytest.mark.parametrize("tau", inputs.SWEEP_TAUS)
+def test_sweep_reduced(orc, frac, tau):
+    """The decomposition sweep's 16 points at a reduced size (K = N = 1024)."""
+    w = inputs.sweep(frac, tau, T=512, K=1024, N=1024)
+    run_and_compare(orc, w.X, w.W, tau, what=f"sweep-reduced f{frac} tau{tau}")
+
+
+# ---- full sizes of the named workloads, on sampled rows --------------------
+
+def test_prefill_full(orc):
+    w = inputs.prefill()
+    run_and_compare(orc, w.X, w.W, w.tau, rows=sample_rows(w.T), what="prefill")
+
+
+def test_large_full(orc):
+    w = inputs.large()
+    run_and_compare(orc, w.X, w.W, w.tau, rows=sample_rows(w.T), what="large")
+
+
+@pytest.mark.parametrize("frac", inputs.SWEEP_FRACTIONS)
+@pytest.mark.parametrize("tau", inputs.SWEEP_TAUS)
+def test_sweep_full(orc, frac, tau):
+    w = inputs.sweep(frac, tau)
+    run_and_compare(orc, w.X, w.W, tau, rows=sample_rows(w.T, 32), what=f"sweep f{frac} tau{tau}")
