@@ -19,8 +19,9 @@ a pinned host->device copy of X, the library call, and a device->host copy of
 Y, all inside the timed region.
 
 `roofline` is for the dominant kernel: its algorithmic bytes (or flops) per
-launch over its average duration, measured with CUDA events around each
-launch (library profiling mode) over an eager pass of the same steps.
+launch over its average duration, measured with CUDA events around a CUDA
+graph of that kernel alone (library profiling mode 2, which re-launches only
+the main kernel on the act-pass results the timed calls left behind).
 
 `--impl reference` times the CPU oracle (the reference arm of this build):
 each step is a bounded sample of the same workload (all rows of X, a
@@ -87,12 +88,9 @@ def algorithmic_bytes(T, N, K, nO):
 
 def kernel_algorithmic(kernel, T, N, K, nO):
     """(bytes, flops) per launch of one kernel, for the roofline."""
-    if kernel in ("gemv_decode", "decode_fused"):
-        # weight codes + scales + outlier weight columns + codes of X + Y
-        b = N * K + 4 * N + 2 * N * nO + T * K + 2 * T * N
-        if kernel == "decode_fused":
-            b += 2 * T * K - T * K  # reads fp16 X instead of int8 codes
-        return b, 2 * T * N * K
+    if kernel == "dec_gemv":
+        # weight codes + scales + outlier weight columns + int8 codes of X + Y
+        return N * K + 4 * N + 2 * N * nO + T * K + 2 * T * N, 2 * T * N * K
     if kernel in ("gemm_mma", "gemm_tc"):
         return N * K + 2 * T * K + 2 * T * N + 2 * N * nO, 2 * T * N * K + 2 * T * N * nO
     if kernel == "outlier_scan":
@@ -107,56 +105,81 @@ def kernel_algorithmic(kernel, T, N, K, nO):
 # ---------------------------------------------------------------------------
 
 class ClockSampler:
-    REASONS = {
-        "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20, "hw_thermal_slowdown": 0x40,
-        "hw_power_brake_slowdown": 0x80, "sw_power_cap": 0x4, "gpu_idle": 0x1,
-    }
+    """Samples SM clock and clock-event reasons with an nvidia-smi subprocess
+    (read-only queries) while the timed region runs."""
 
-    def __init__(self, index: int, period: float = 0.02):
-        self.samples, self.reasons = [], set()
-        self.max_mhz = None
-        self._stop = threading.Event()
-        self.ok = False
-        try:
-            import pynvml
-            pynvml.nvmlInit()
-            self.nv = pynvml
-            self.h = pynvml.nvmlDeviceGetHandleByIndex(index)
-            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
-            self.ok = True
-        except Exception as e:  # no NVML: report it, do not guess
-            self.err = repr(e)
-        self.period = period
+    FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
 
-    def _run(self):
-        while not self._stop.is_set():
-            try:
-                self.samples.append(self.nv.nvmlDeviceGetClockInfo(self.h, self.nv.NVML_CLOCK_SM))
-                r = self.nv.nvmlDeviceGetCurrentClocksEventReasons(self.h)
-                for k, bit in self.REASONS.items():
-                    if r & bit:
-                        self.reasons.add(k)
-            except Exception:
-                pass
-            time.sleep(self.period)
+    def __init__(self, index: int, period_ms: int = 50):
+        self.cmd = ["nvidia-smi", "-i", str(index), "--query-gpu=" + ",".join(self.FIELDS),
+                    "--format=csv,noheader,nounits", "-lms", str(period_ms)]
+        self.lines = []  # (arrival time, fields)
+        self.t0 = self.t1 = None
+        self.p = None
+
+    def _reader(self):
+        for line in self.p.stdout:
+            self.lines.append((time.perf_counter(), [f.strip() for f in line.split(",")]))
 
     def __enter__(self):
-        if self.ok:
-            self.t = threading.Thread(target=self._run, daemon=True)
-            self.t.start()
+        import subprocess
+        try:
+            self.p = subprocess.Popen(self.cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                      text=True)
+        except OSError:
+            self.p = None
+            return self
+        self.th = threading.Thread(target=self._reader, daemon=True)
+        self.th.start()
+        deadline = time.perf_counter() + 5.0
+        while not self.lines and time.perf_counter() < deadline:  # first sample in
+            time.sleep(0.01)
         return self
 
+    def mark_start(self):
+        self.t0 = time.perf_counter()
+
+    def mark_stop(self):
+        self.t1 = time.perf_counter()
+
     def __exit__(self, *a):
-        if self.ok:
-            self._stop.set()
-            self.t.join()
+        if self.p is not None:
+            time.sleep(0.06)
+            self.p.terminate()
+            try:
+                self.p.wait(timeout=5)
+            except Exception:
+                self.p.kill()
+            self.th.join(timeout=5)
 
     def summary(self):
-        if not self.ok:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvml_unavailable"]}
-        med = statistics.median(self.samples) if self.samples else None
-        return {"sm_mhz": med, "sm_max_mhz": self.max_mhz, "samples": len(self.samples),
-                "reasons": sorted(self.reasons - {"gpu_idle"})}
+        if self.p is None or not self.lines:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        inside = [f for (t, f) in self.lines
+                  if self.t0 is not None and self.t0 <= t <= self.t1 + 0.06]
+        window = "timed region"
+        if not inside:  # region shorter than the sampling period: nearest samples
+            inside = [f for (t, f) in self.lines][-3:]
+            window = "samples adjacent to a timed region shorter than the sampling period"
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(f[0]) for f in inside if num(f[0]) is not None]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for f in inside:
+            for name, val in zip(names, f[4:8]):
+                if val.strip().lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": num(inside[0][1]), "samples": len(inside), "window": window,
+                "power_w_max": max((num(f[2]) or 0) for f in inside),
+                "reasons": sorted(reasons)}
 
 
 # ---------------------------------------------------------------------------
@@ -263,9 +286,10 @@ def run_ours(args, world, rank, local):
     start = torch.cuda.Event(enable_timing=True)
     stop = torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(local)
-    barrier(world)
-    torch.cuda.synchronize()
     with sampler:
+        barrier(world)
+        torch.cuda.synchronize()
+        sampler.mark_start()
         start.record(stream)
         for _ in range(args.steps // G):
             g_main.replay()
@@ -273,6 +297,7 @@ def run_ours(args, world, rank, local):
             g_rem.replay()
         stop.record(stream)
         torch.cuda.synchronize()
+        sampler.mark_stop()
     barrier(world)
     ms = start.elapsed_time(stop)
     ms = max_over_ranks(ms, world, dev)
@@ -282,21 +307,35 @@ def run_ours(args, world, rank, local):
     alg_bytes = algorithmic_bytes(T, N, K, nO)
     gbs = world * calls * alg_bytes / (ms * 1e-3) / 1e9
 
-    # per-kernel durations: eager pass of the same steps with event timing
-    prof_steps = min(args.steps, max(1, 4000 // layers))
-    binding.profile_enable(True)
-    with torch.cuda.stream(stream):
-        for _ in range(prof_steps):
-            step(stream)
-    stream.synchronize()
-    binding.profile_enable(False)
-    prof = binding.profile_collect()
-    dominant = max(prof.items(), key=lambda kv: kv[1][0])
-    kname, (kms, kn) = dominant
-    kavg_s = kms / kn * 1e-3
+    # the dominant kernel alone: a graph of main-kernel-only launches (library
+    # profiling mode 2 reuses the act-pass results left in the workspace by the
+    # calls above, same X and tau), timed with CUDA events on its stream
+    path = lib.bnb_int8_linear_path(T, N, K)
+    kname = {1: "dec_gemv", 2: "gemm_tc", 3: "gemm_mma"}[path]
+    Gk = max(1, min(G, 8))
+    binding.profile_enable(2)
+    try:
+        g_k = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_k, stream=stream):
+            for _ in range(Gk):
+                step(stream)
+    finally:
+        binding.profile_enable(0)
+    g_k.replay()
+    torch.cuda.synchronize()
+    reps = max(1, min(args.steps // Gk, 2000))
+    k0 = torch.cuda.Event(enable_timing=True)
+    k1 = torch.cuda.Event(enable_timing=True)
+    k0.record(stream)
+    for _ in range(reps):
+        g_k.replay()
+    k1.record(stream)
+    torch.cuda.synchronize()
+    kms = k0.elapsed_time(k1)
+    kavg_s = kms * 1e-3 / (reps * Gk * layers)
     kb, kf = kernel_algorithmic(kname, T, N, K, nO)
     peaks, peak_src = load_peaks()
-    if kname in ("gemv_decode", "decode_fused", "outlier_scan", "quantize_rows") or T <= 16:
+    if path == 1:
         roof = {"bound": "hbm", "achieved": kb / kavg_s / 1e9, "peak": peaks["hbm_gbs"],
                 "unit": "GB/s"}
     else:
@@ -305,9 +344,21 @@ def run_ours(args, world, rank, local):
     roof["frac"] = roof["achieved"] / roof["peak"]
     roof["traffic"] = args.traffic
     roof["kernel"] = kname
-    roof["peak_source"] = f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured" else peak_src
+    roof["peak_source"] = ("measured (MEASURED_PEAKS.json)" if peak_src == "measured"
+                           else "fallback")
     roof["kernel_avg_us"] = kavg_s * 1e6
     roof["alg_bytes_per_launch"] = kb
+    roof["timing"] = f"graph of {Gk * layers} {kname} launches x {reps} replays, CUDA events"
+
+    # per-kernel breakdown of whole calls: eager, event-bracketed (includes
+    # launch gaps and loses the programmatic-launch overlap; shares only)
+    binding.profile_enable(1)
+    with torch.cuda.stream(stream):
+        for _ in range(max(1, min(args.steps, 2000 // layers))):
+            step(stream)
+    stream.synchronize()
+    binding.profile_enable(0)
+    prof = binding.profile_collect()
 
     # e2e through the public API with host buffers
     Xpin = Xh.pin_memory()
@@ -365,7 +416,8 @@ def run_ours(args, world, rank, local):
         "gpu_launches": int(round(launches_per_step * args.steps)),
         "launches_per_step": launches_per_step,
         "roofline": roof,
-        "kernels": {k: {"avg_us": v[0] / v[1] * 1e3, "launches": v[1]} for k, v in prof.items()},
+        "kernels_eager_events": {k: {"avg_us": v[0] / v[1] * 1e3, "launches": v[1]}
+                                 for k, v in prof.items()},
         "clocks": sampler.summary(),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -460,7 +512,7 @@ def run_reference(args, world, rank, local):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--steps", type=int, default=10000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="decode",

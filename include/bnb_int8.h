@@ -142,18 +142,27 @@ const char *bnb_status_string(bnb_status_t s);
 uint64_t bnb_launch_count(void);
 
 /*
- * Which kernel path bnb_int8_linear takes for a shape: 1 = fused decode
- * GEMV (small T), 2 = tensor-core GEMM (tcgen05), 3 = warp-level mma GEMM.
+ * Which kernel path bnb_int8_linear takes for a shape on the current device:
+ * 1 = decode (T <= 16, K <= 4608, N <= 32 x SMs), 2 = tensor-core GEMM
+ * (tcgen05), 3 = warp-level mma GEMM.
  */
 int bnb_int8_linear_path(int64_t T, int64_t N, int64_t K);
 
 /*
- * Per-kernel timing with CUDA events (off by default).  While enabled, every
- * launch the library enqueues is bracketed by two events recorded on the
- * launch's stream (events are created on demand and reused; no device memory
- * is allocated).  Do not enable it while a stream is being captured into a
- * CUDA graph.
- *   bnb_profile_enable(1/0)     start / stop recording.
+ * Profiling aids (off by default; for benchmarks, not for production calls).
+ *   bnb_profile_enable(1)  per-kernel timing: every launch the library
+ *                          enqueues is bracketed by two CUDA events recorded
+ *                          on the launch's stream (events are created on
+ *                          demand and reused; no device memory is allocated).
+ *                          Do not use while a stream is being captured.
+ *   bnb_profile_enable(2)  main-kernel-only mode: bnb_int8_linear enqueues
+ *                          only the main kernel of its path (the decode GEMV
+ *                          or the GEMM), reusing the activation-pass results
+ *                          that the previous full call on the same workspace
+ *                          left there.  Its result is correct only if that
+ *                          call had the same X and tau.  Used to time the
+ *                          dominant kernel alone.
+ *   bnb_profile_enable(0)  back to normal operation.
  *   bnb_profile_collect(ms, n)  waits for the recorded events, adds each
  *                               kernel's summed duration (ms) and launch count
  *                               into ms[id] and n[id] for id in
@@ -162,7 +171,7 @@ int bnb_int8_linear_path(int64_t T, int64_t N, int64_t K);
  *                               query failed.
  *   bnb_profile_kernel_name(id) static name of kernel id (NULL if out of range).
  */
-void bnb_profile_enable(int on);
+void bnb_profile_enable(int mode);
 bnb_status_t bnb_profile_collect(double *ms, uint64_t *n);
 int bnb_profile_kernel_count(void);
 const char *bnb_profile_kernel_name(int id);

@@ -179,8 +179,9 @@ def linear_path(T: int, N: int, K: int) -> int:
     return load().bnb_int8_linear_path(T, N, K)
 
 
-def profile_enable(on: bool) -> None:
-    load().bnb_profile_enable(1 if on else 0)
+def profile_enable(mode) -> None:
+    """0 off, 1 per-kernel event timing, 2 main-kernel-only launches."""
+    load().bnb_profile_enable(int(mode))
 
 
 def profile_collect() -> dict:

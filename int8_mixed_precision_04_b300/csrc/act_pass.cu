@@ -130,6 +130,7 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_rows_kernel(
     for (int w = 0; w < kQuantThreads / 32; w++) m = max(m, red[w]);
     __syncthreads();
     const float a = h2f_bits(m);
+    const float r = code_recip(a);
     if (threadIdx.x == 0) sx[t] = a;
     for (int64_t v = threadIdx.x; v < vecs; v += kQuantThreads) {
       const uint32_t fl = (__ldg(colmask + (v >> 2)) >> (8 * (v & 3))) & 0xffu;
@@ -138,8 +139,8 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_rows_kernel(
       int c[8];
 #pragma unroll
       for (int i = 0; i < 4; i++) {
-        c[2 * i] = ((fl >> (2 * i)) & 1) ? 0 : code_of(h2f_bits(w[i] & 0xffffu), a);
-        c[2 * i + 1] = ((fl >> (2 * i + 1)) & 1) ? 0 : code_of(h2f_bits(w[i] >> 16), a);
+        c[2 * i] = ((fl >> (2 * i)) & 1) ? 0 : code_of(h2f_bits(w[i] & 0xffffu), a, r);
+        c[2 * i + 1] = ((fl >> (2 * i + 1)) & 1) ? 0 : code_of(h2f_bits(w[i] >> 16), a, r);
       }
       uint32_t p0 = 0, p1 = 0;
 #pragma unroll

@@ -29,7 +29,7 @@ static Layout layout_of(int64_t T, int64_t K) {
   L.counters = off;
   off += 256;
   L.colmask = off;
-  off += align_up((size_t)((K + 31) / 32) * 4, 256);
+  off += align_up((size_t)((K + 255) / 256) * 8 * 4, 256);
   L.O = off;
   off += align_up((size_t)(K + 64) * 4, 256);
   L.sx = off;
@@ -117,11 +117,10 @@ static bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
   return x < y + nb && y < x + na;
 }
 
-// T <= 16 and the codes fit the GEMV's shared-memory block.
-static int choose_path(int64_t T, int64_t N, int64_t K) {
-  (void)N;
-  const int64_t pitch = (K + 127) / 128 * 128 + 64;
-  if (T <= 16 && 16 * pitch <= 200 * 1024) return 1;
+// 1: decode (T <= 16, the codes and a 32-row weight slice fit shared memory,
+// at most 32 output channels per SM), else a GEMM.
+static int choose_path(int64_t T, int64_t N, int64_t K, int sms = kB300Sms) {
+  if (T <= 16 && K <= kDecodeMaxK && N <= 32LL * sms) return 1;
   return 3;
 }
 
@@ -150,24 +149,32 @@ static bnb_status_t linear_impl(const void *X, int64_t T, int64_t K, const int8_
   if (st != BNB_OK) return st;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_v);
   const Workspace ws = carve(workspace, T, K);
-  const int path = choose_path(T, N, K);
+  const int path = choose_path(T, N, K, device_sms(dev));
   const uint32_t thr = threshold_bits(tau);
-  // status word, counters and the outlier column mask are contiguous and
-  // zeroed by every call with one memset
-  const size_t zero_bytes = 512 + (size_t)((K + 31) / 32) * 4;
-  {
-    ProfScope ps(kKidMemset, stream);
-    if (cudaMemsetAsync(ws.status, 0, zero_bytes, stream) != cudaSuccess) return BNB_ERR_CUDA;
-  }
-  note_launch();
-  cudaError_t e = launch_act_pass(X, T, K, thr, ws, /*code_mode=*/0, /*with_xo=*/true, dbg_xq,
-                                  device_sms(dev), stream);
-  if (e != cudaSuccess) return BNB_ERR_CUDA;
-  if (path == 1)
-    e = launch_gemv_decode(T, K, Wq, Wscale, W16, N, Y, ws, dbg_acc, stream);
-  else
+  cudaError_t e;
+  if (path == 1) {
+    // decode: no memset, the act-pass kernel clears the status word
+    e = launch_decode(X, T, K, thr, Wq, Wscale, W16, N, Y, ws, dbg_xq, dbg_acc,
+                      device_sms(dev), stream);
+    if (e != cudaSuccess) return BNB_ERR_CUDA;
+  } else {
+    if (!profile_only_main()) {
+      // status word, counters and the outlier column mask are contiguous and
+      // zeroed by every call with one memset
+      const size_t zero_bytes = 512 + (size_t)((K + 255) / 256) * 8 * 4;
+      {
+        ProfScope ps(kKidMemset, stream);
+        if (cudaMemsetAsync(ws.status, 0, zero_bytes, stream) != cudaSuccess)
+          return BNB_ERR_CUDA;
+      }
+      note_launch();
+      e = launch_act_pass(X, T, K, thr, ws, /*code_mode=*/0, /*with_xo=*/true, dbg_xq,
+                          device_sms(dev), stream);
+      if (e != cudaSuccess) return BNB_ERR_CUDA;
+    }
     e = launch_gemm_mma(T, K, Wq, Wscale, W16, N, Y, ws, dbg_acc, stream);
-  if (e != cudaSuccess) return BNB_ERR_CUDA;
+    if (e != cudaSuccess) return BNB_ERR_CUDA;
+  }
   if (dbg_sx && cudaMemcpyAsync(dbg_sx, ws.sx, (size_t)T * 4, cudaMemcpyDeviceToDevice, stream) != cudaSuccess)
     return BNB_ERR_CUDA;
   if (dbg_O && cudaMemcpyAsync(dbg_O, ws.O, (size_t)K * 4, cudaMemcpyDeviceToDevice, stream) != cudaSuccess)
@@ -247,7 +254,9 @@ uint64_t bnb_launch_count(void) { return g_launches.load(std::memory_order_relax
 
 int bnb_int8_linear_path(int64_t T, int64_t N, int64_t K) {
   if (T <= 0 || N <= 0 || K <= 0) return 0;
-  return choose_path(T, N, K);
+  int dev = 0, sms = kB300Sms;
+  if (cudaGetDevice(&dev) == cudaSuccess) sms = device_sms(dev);
+  return choose_path(T, N, K, sms);
 }
 
 }  // extern "C"

@@ -17,11 +17,15 @@ constexpr int32_t kDevTimeout = BNB_ERR_TIMEOUT;
 // device attribute, this is only a default for host-side heuristics.
 constexpr int kB300Sms = 148;
 
+// Largest K the decode path holds in shared memory: 32 weight rows and 16
+// code rows of K + 64 bytes, plus small buffers, within 227 KB.
+constexpr int64_t kDecodeMaxK = 4608;
+
 // Workspace layout, carved identically by the host for every call.
 struct Workspace {
   int32_t *status;     // [4]  device status word + spare
   uint32_t *counters;  // [4]  block-completion counter, |O| (counters[1])
-  uint32_t *colmask;   // [ceil(K/32)] outlier column bitmask
+  uint32_t *colmask;   // [8 * ceil(K/256)] outlier column bitmask
   int32_t *O;          // [K + 64] outlier column list, ascending
   float *sx;           // [T] row scales
   void *xcodes;        // [T x K] codes: int8 (decode) or fp16 integers (GEMM)
@@ -45,12 +49,52 @@ __device__ __forceinline__ float h2f_bits(uint32_t h) {
   return __half2float(__ushort_as_half((unsigned short)h));
 }
 
-// Vector-wise int8 code of x against absmax a: rint(fl32(127 x) / a), ties to
-// even; 0 when a == 0.  127*x is exact for fp16 x; the division is the IEEE
-// round-to-nearest fp32 division.
-__device__ __forceinline__ int code_of(float x, float a) {
-  if (a == 0.0f) return 0;
-  return __float2int_rn(__fdiv_rn(127.0f * x, a));
+// Vector-wise int8 code of x against absmax a > 0: the integer nearest to
+// v = 127 x / a, ties to even (which is what rint(fl32(127 x) / a) gives,
+// since a single fp32 rounding of that quotient never crosses or creates a
+// half-integer).  Division-free and exact:
+//   p = x * r with r ~ 127/a is within 127 * 2^-23 of v, so f = floor(p) and
+//   the half-integer c = f + 0.5 bracket v's rounding decision;
+//   fma(c, a, -127 x) rounds c*a - 127x once, so its SIGN is exact and equals
+//   sign(c - v): negative -> round up, positive -> down, zero -> tie -> even.
+// 127 x is exact in fp32 for fp16 x.  Requires |x| <= a, a > 0 finite.
+__device__ __forceinline__ int code_exact(float x, float a, float r) {
+  const float p = x * r;
+  const float f = floorf(p);
+  const float s = fmaf(f + 0.5f, a, -127.0f * x);
+  int q = (int)f;
+  if (s < 0.0f)
+    q += 1;
+  else if (s == 0.0f)
+    q += q & 1;
+  return q;
+}
+
+// 127 / a for the code rule above (0 when a == 0, in which case every code
+// is 0 and code_exact is not used).
+__device__ __forceinline__ float code_recip(float a) { return a > 0.0f ? 127.0f / a : 0.0f; }
+
+__device__ __forceinline__ int code_of(float x, float a, float r) {
+  return a > 0.0f ? code_exact(x, a, r) : 0;
+}
+
+// Four signed int8 codes (one 32-bit word) -> four fp16 integers (two half2
+// words).  fp16 with exponent field 25 has unit spacing on [1024, 2048), so
+// the bit pattern 0x6400 | u is exactly 1024 + u for a byte u; with
+// u = code + 128 the value minus 1152 is the code, exactly.
+__device__ __forceinline__ void s8x4_to_f16x4(uint32_t w, uint32_t &lo, uint32_t &hi) {
+  const uint32_t u = w ^ 0x80808080u;
+  asm("prmt.b32 %0, %1, %2, 0x4140;" : "=r"(lo) : "r"(u), "r"(0x64646464u));
+  asm("prmt.b32 %0, %1, %2, 0x4342;" : "=r"(hi) : "r"(u), "r"(0x64646464u));
+  const uint32_t bias = 0x64806480u;  // (1152, 1152)
+  asm("sub.rn.f16x2 %0, %0, %1;" : "+r"(lo) : "r"(bias));
+  asm("sub.rn.f16x2 %0, %0, %1;" : "+r"(hi) : "r"(bias));
+}
+
+// Programmatic dependent launch controls.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 __device__ __forceinline__ uint64_t global_timer_ns() {

@@ -20,12 +20,16 @@ enum KernelId {
   kKidGemmMma,
   kKidGemmTc,
   kKidQuantWeight,
-  kKidDecodeFused,
+  kKidDecAct,
   kKernelCount
 };
 
-// Brackets one launch with two events when profiling is enabled (no-op
-// otherwise).
+// Profiling mode 2: launch only the main (dominant) kernel of a path,
+// reusing the activation-pass results already in the workspace.
+bool profile_only_main();
+
+// Brackets one launch with two events when profiling mode 1 is enabled
+// (no-op otherwise).
 class ProfScope {
  public:
   ProfScope(int kid, cudaStream_t s);
@@ -48,10 +52,12 @@ cudaError_t launch_act_pass(const void *X, int64_t T, int64_t K, uint32_t thr_bi
                             const Workspace &ws, int code_mode, bool with_xo,
                             int8_t *dbg_xq, int num_sms, cudaStream_t stream);
 
-// S4..S6 for small T (T <= 16): int8 codes from the workspace.
-cudaError_t launch_gemv_decode(int64_t T, int64_t K, const int8_t *Wq, const float *sw,
-                               const void *W16, int64_t N, void *Y, const Workspace &ws,
-                               int32_t *dbg_acc, cudaStream_t stream);
+// The whole layer for T <= 16, K <= kDecodeMaxK, N <= 32 x SMs: two
+// PDL-chained kernels (act pass in one cluster, then the GEMV).
+cudaError_t launch_decode(const void *X, int64_t T, int64_t K, uint32_t thr, const int8_t *Wq,
+                          const float *sw, const void *W16, int64_t N, void *Y,
+                          const Workspace &ws, int8_t *dbg_xq, int32_t *dbg_acc, int num_sms,
+                          cudaStream_t stream);
 
 // S4..S6 with warp-level mma.sync (legacy tensor path), int8 codes.
 cudaError_t launch_gemm_mma(int64_t T, int64_t K, const int8_t *Wq, const float *sw,

@@ -1,4 +1,5 @@
 // Per-kernel CUDA-event timing (see bnb_profile_* in include/bnb_int8.h).
+#include <atomic>
 #include <mutex>
 #include <vector>
 
@@ -7,8 +8,8 @@
 namespace bnb {
 
 static const char *const kKernelNames[kKernelCount] = {
-    "memset_status_mask", "outlier_scan", "quantize_rows", "gemv_decode",
-    "gemm_mma",           "gemm_tc",      "quantize_weight", "decode_fused"};
+    "memset_status_mask", "outlier_scan", "quantize_rows", "dec_gemv",
+    "gemm_mma",           "gemm_tc",      "quantize_weight", "dec_act"};
 
 namespace {
 struct Rec {
@@ -17,6 +18,7 @@ struct Rec {
 };
 std::mutex g_mu;
 bool g_on = false;
+std::atomic<int> g_mode{0};
 std::vector<Rec> g_recs;
 std::vector<cudaEvent_t> g_pool;
 
@@ -31,6 +33,8 @@ cudaEvent_t take_event() {
   return e;
 }
 }  // namespace
+
+bool profile_only_main() { return g_mode.load(std::memory_order_relaxed) == 2; }
 
 ProfScope::ProfScope(int kid, cudaStream_t s) : kid_(kid), s_(s), a_(nullptr) {
   std::lock_guard<std::mutex> lk(g_mu);
@@ -60,9 +64,10 @@ using namespace bnb;
 
 extern "C" {
 
-void bnb_profile_enable(int on) {
+void bnb_profile_enable(int mode) {
   std::lock_guard<std::mutex> lk(g_mu);
-  g_on = on != 0;
+  g_on = mode == 1;
+  g_mode.store(mode == 1 || mode == 2 ? mode : 0, std::memory_order_relaxed);
 }
 
 bnb_status_t bnb_profile_collect(double *ms, uint64_t *n) {

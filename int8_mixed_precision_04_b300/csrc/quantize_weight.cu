@@ -32,6 +32,7 @@ __global__ void __launch_bounds__(256) quantize_weight_kernel(
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
     const float a = h2f_bits(m);
+    const float r = code_recip(a);
     if (lane == 0) sw[n] = a;
     uint2 *out = reinterpret_cast<uint2 *>(Wq + n * K);
     for (int64_t v = lane; v < vecs; v += 32) {
@@ -40,8 +41,8 @@ __global__ void __launch_bounds__(256) quantize_weight_kernel(
       uint32_t packed[2] = {0, 0};
 #pragma unroll
       for (int i = 0; i < 4; i++) {
-        int c0 = code_of(h2f_bits(w[i] & 0xffffu), a);
-        int c1 = code_of(h2f_bits(w[i] >> 16), a);
+        int c0 = code_of(h2f_bits(w[i] & 0xffffu), a, r);
+        int c1 = code_of(h2f_bits(w[i] >> 16), a, r);
         uint32_t two = ((uint32_t)(c0 & 0xff)) | ((uint32_t)(c1 & 0xff) << 8);
         packed[i / 2] |= two << (16 * (i % 2));
       }
