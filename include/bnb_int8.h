@@ -132,6 +132,38 @@ bnb_status_t bnb_int8_linear_debug(const void *X, int64_t T, int64_t K,
  */
 bnb_status_t bnb_last_device_status(const void *workspace, void *stream, int32_t *out);
 
+/*
+ * bnb_int8_linear without a caller-supplied workspace, for callers that
+ * cannot allocate device memory: a runtime that plans all device memory
+ * ahead of time and forbids allocation once it is serving, a
+ * latency-critical loop in which cudaMalloc (which may synchronise the
+ * device) is not allowed, or a host framework that owns the device memory
+ * and hands out none.  The pages have no counterpart to this entry point; it
+ * computes exactly what bnb_int8_linear computes, with the same kernels.
+ *
+ * The workspace is one static device array of BNB_NOALLOC_SCRATCH_BYTES
+ * inside this library, held on every GPU that loads the library until the
+ * process exits.  The call allocates nothing (no cudaMalloc, cudaFree or
+ * allocating library routine).
+ *   Arguments as for bnb_int8_linear, without workspace/workspace_bytes.
+ *   Calls whose bnb_int8_linear_workspace_bytes(T, N, K) exceeds
+ *   BNB_NOALLOC_SCRATCH_BYTES are rejected with BNB_ERR_UNSUPPORTED before
+ *   anything is enqueued (at K = 4096 that admits T up to about 500).
+ *   The first call on a device looks up the array's device address with
+ *   that device current (cudaGetSymbolAddress) and caches it; make that first
+ *   call before any stream capture.  BNB_ERR_CUDA if the lookup fails.
+ *   Every call, on every stream, shares the one array and leaves its contents
+ *   behind; each call clears on the device what must start at zero.  Calls
+ *   that may overlap on the GPU (different streams, or concurrent host
+ *   threads without ordering) race on the array and give undefined results:
+ *   order them on one stream.  The device status word of these calls is not
+ *   readable through bnb_last_device_status.
+ */
+#define BNB_NOALLOC_SCRATCH_BYTES (8u << 20)
+bnb_status_t bnb_int8_linear_noalloc(const void *X, int64_t T, int64_t K, const int8_t *Wq,
+                                     const float *Wscale, const void *W16, int64_t N,
+                                     float tau, void *Y, void *stream);
+
 /* Static, human-readable name of a status code. */
 const char *bnb_status_string(bnb_status_t s);
 

@@ -41,7 +41,7 @@ class Lib:
                "bnb_int8_linear", "bnb_int8_linear_debug", "bnb_last_device_status",
                "bnb_status_string", "bnb_launch_count", "bnb_int8_linear_path",
                "bnb_profile_enable", "bnb_profile_collect", "bnb_profile_kernel_count",
-               "bnb_profile_kernel_name")
+               "bnb_profile_kernel_name", "bnb_int8_linear_noalloc")
 
     def __init__(self, path: str = LIB_PATH):
         if not os.path.exists(path):
@@ -58,6 +58,9 @@ class Lib:
                                       ctypes.c_size_t, _P]
         L.bnb_int8_linear_debug.restype = ctypes.c_int
         L.bnb_int8_linear_debug.argtypes = L.bnb_int8_linear.argtypes + [_P, _P, _P, _P, _P]
+        L.bnb_int8_linear_noalloc.restype = ctypes.c_int
+        L.bnb_int8_linear_noalloc.argtypes = [_P, _I64, _I64, _P, _P, _P, _I64, ctypes.c_float,
+                                              _P, _P]
         L.bnb_last_device_status.restype = ctypes.c_int
         L.bnb_last_device_status.argtypes = [_P, _P, ctypes.POINTER(ctypes.c_int32)]
         L.bnb_status_string.restype = ctypes.c_char_p
@@ -141,6 +144,20 @@ def linear(X, Wq, Wscale, W16, tau: float, Y=None, workspace=None, stream=None):
                                 float(tau), _ptr(Y), _ptr(workspace), workspace.numel(),
                                 _stream(stream))
     _check(rc, "bnb_int8_linear")
+    return Y
+
+
+def linear_noalloc(X, Wq, Wscale, W16, tau: float, Y=None, stream=None):
+    """bnb_int8_linear_noalloc: as :func:`linear`, with the library's static
+    scratch array instead of a workspace (for callers that cannot allocate)."""
+    import torch
+    T, K = X.shape
+    N = Wq.shape[0]
+    if Y is None:
+        Y = torch.empty((T, N), dtype=torch.float16, device=X.device)
+    rc = load().bnb_int8_linear_noalloc(_ptr(X), T, K, _ptr(Wq), _ptr(Wscale), _ptr(W16), N,
+                                        float(tau), _ptr(Y), _stream(stream))
+    _check(rc, "bnb_int8_linear_noalloc")
     return Y
 
 
