@@ -229,8 +229,10 @@ def run_ours(args, world, rank, local):
     w = make_workload(args.workload, args.T)
     T, K, N, tau = w.T, w.K, w.N, w.tau
     wq_bytes = N * K
-    # enough distinct weights that one step's weight traffic exceeds 2x L2
-    layers = max(1, math.ceil(2 * L2_BYTES / (wq_bytes + 2 * N * K)))
+    # enough distinct layers (own weight, input and output each) that the
+    # bytes one step streams (int8 weight + fp16 activations) exceed 2x L2,
+    # so no call finds its operands in L2 from the previous step
+    layers = max(1, math.ceil(2 * L2_BYTES / (wq_bytes + 2 * T * K)))
     if args.workload == "decode":
         layers = max(layers, 16)
     layers = min(layers, args.max_layers)
@@ -279,14 +281,17 @@ def run_ours(args, world, rank, local):
         with torch.cuda.graph(g_rem, stream=stream):
             for _ in range(rem):
                 step(stream)
-    for _ in range(2):
-        g_main.replay()
+    # CUDAGraph.replay() launches on torch's current stream: every replay and
+    # every event below runs with `stream` current, so the events time it
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            g_main.replay()
     torch.cuda.synchronize()
 
     start = torch.cuda.Event(enable_timing=True)
     stop = torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(local)
-    with sampler:
+    with sampler, torch.cuda.stream(stream):
         barrier(world)
         torch.cuda.synchronize()
         sampler.mark_start()
@@ -321,15 +326,16 @@ def run_ours(args, world, rank, local):
                 step(stream)
     finally:
         binding.profile_enable(0)
-    g_k.replay()
-    torch.cuda.synchronize()
-    reps = max(1, min(args.steps // Gk, 2000))
+    reps = max(3, min(args.steps // Gk, 2000))
     k0 = torch.cuda.Event(enable_timing=True)
     k1 = torch.cuda.Event(enable_timing=True)
-    k0.record(stream)
-    for _ in range(reps):
+    with torch.cuda.stream(stream):
         g_k.replay()
-    k1.record(stream)
+        torch.cuda.synchronize()
+        k0.record(stream)
+        for _ in range(reps):
+            g_k.replay()
+        k1.record(stream)
     torch.cuda.synchronize()
     kms = k0.elapsed_time(k1)
     kavg_s = kms * 1e-3 / (reps * Gk * layers)
@@ -402,8 +408,9 @@ def run_ours(args, world, rank, local):
             "workload": f"{args.workload}: X fp16 [{T},{K}], W fp16 [{N},{K}], tau {tau}",
             "T": T, "K": K, "N": N, "tau": tau, "n_outliers": nO,
             "layers_per_step": layers,
-            "l2": f"{layers} distinct weights per step ({layers * (wq_bytes) / 1e6:.0f} MB int8) "
-                  f"vs 126 MB L2",
+            "l2": f"inputs larger than L2: {layers} distinct layers per step "
+                  f"({layers * (wq_bytes + 2 * T * K) / 1e6:.0f} MB of int8 weights and fp16 "
+                  f"activations) vs 126 MB L2",
             "timing": "CUDA graph replay of captured library calls, CUDA events",
             "parallelism": f"replicas x{world}",
             "path": lib.bnb_int8_linear_path(T, N, K),

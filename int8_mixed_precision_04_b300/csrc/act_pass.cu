@@ -102,8 +102,8 @@ template <int kMode>
 __global__ void __launch_bounds__(kQuantThreads) quantize_rows_kernel(
     const uint4 *__restrict__ X, int64_t T, int64_t K, const uint32_t *__restrict__ colmask,
     const uint32_t *__restrict__ counters, const int32_t *__restrict__ O,
-    float *__restrict__ sx, void *__restrict__ codes, __half *__restrict__ xo, int64_t kpad,
-    int8_t *__restrict__ dbg_xq) {
+    float *__restrict__ sx, float *__restrict__ sxd, void *__restrict__ codes,
+    __half *__restrict__ xo, int64_t kpad, int8_t *__restrict__ dbg_xq) {
   __shared__ uint32_t red[kQuantThreads / 32];
   const int64_t vecs = K / 8;
   const uint32_t lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -131,7 +131,10 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_rows_kernel(
     __syncthreads();
     const float a = h2f_bits(m);
     const float r = code_recip(a);
-    if (threadIdx.x == 0) sx[t] = a;
+    if (threadIdx.x == 0) {
+      sx[t] = a;
+      sxd[t] = __fdiv_rn(a, 127.0f);
+    }
     for (int64_t v = threadIdx.x; v < vecs; v += kQuantThreads) {
       const uint32_t fl = (__ldg(colmask + (v >> 2)) >> (8 * (v & 3))) & 0xffu;
       uint4 q = __ldg(row + v);
@@ -200,11 +203,11 @@ cudaError_t launch_act_pass(const void *X, int64_t T, int64_t K, uint32_t thr_bi
   if (code_mode == 0)
     quantize_rows_kernel<0><<<(unsigned)qblocks, kQuantThreads, 0, stream>>>(
         reinterpret_cast<const uint4 *>(X), T, K, ws.colmask, ws.counters, ws.O, ws.sx,
-        ws.xcodes, with_xo ? ws.xo : nullptr, ws.kpad, dbg_xq);
+        ws.sxd, ws.xcodes, with_xo ? ws.xo : nullptr, ws.kpad, dbg_xq);
   else
     quantize_rows_kernel<1><<<(unsigned)qblocks, kQuantThreads, 0, stream>>>(
         reinterpret_cast<const uint4 *>(X), T, K, ws.colmask, ws.counters, ws.O, ws.sx,
-        ws.xcodes, with_xo ? ws.xo : nullptr, ws.kpad, dbg_xq);
+        ws.sxd, ws.xcodes, with_xo ? ws.xo : nullptr, ws.kpad, dbg_xq);
   note_launch();
   return cudaGetLastError();
 }

@@ -2,6 +2,7 @@
 // Declarations and the contract of every entry point are in include/bnb_int8.h.
 #include <atomic>
 #include <cmath>
+#include <cstdlib>
 #include <cstring>
 
 #include "common.cuh"
@@ -16,7 +17,7 @@ static inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; 
 static inline bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 
 struct Layout {
-  size_t status, counters, colmask, O, sx, xcodes, xo, total;
+  size_t status, counters, colmask, O, sx, sxd, xcodes, xo, total;
   int64_t kpad;
 };
 
@@ -33,6 +34,8 @@ static Layout layout_of(int64_t T, int64_t K) {
   L.O = off;
   off += align_up((size_t)(K + 64) * 4, 256);
   L.sx = off;
+  off += align_up((size_t)T * 4, 256);
+  L.sxd = off;
   off += align_up((size_t)T * 4, 256);
   L.xcodes = off;
   off += align_up((size_t)T * (size_t)K * 2, 256);
@@ -53,6 +56,7 @@ static Workspace carve(void *ws, int64_t T, int64_t K) {
   w.colmask = reinterpret_cast<uint32_t *>(base + L.colmask);
   w.O = reinterpret_cast<int32_t *>(base + L.O);
   w.sx = reinterpret_cast<float *>(base + L.sx);
+  w.sxd = reinterpret_cast<float *>(base + L.sxd);
   w.xcodes = base + L.xcodes;
   w.xo = reinterpret_cast<__half *>(base + L.xo);
   w.kpad = L.kpad;
@@ -117,11 +121,21 @@ static bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
   return x < y + nb && y < x + na;
 }
 
+// Environment override BNB_GEMM=mma selects the legacy warp-level GEMM for
+// shapes that would take the tcgen05 GEMM (for side-by-side measurement).
+static bool force_mma() {
+  static const bool v = [] {
+    const char *e = std::getenv("BNB_GEMM");
+    return e != nullptr && std::strcmp(e, "mma") == 0;
+  }();
+  return v;
+}
+
 // 1: decode (T <= 16, the codes and a 32-row weight slice fit shared memory,
-// at most 32 output channels per SM), else a GEMM.
+// at most 32 output channels per SM); 2: tcgen05 GEMM; 3: legacy mma GEMM.
 static int choose_path(int64_t T, int64_t N, int64_t K, int sms = kB300Sms) {
   if (T <= 16 && K <= kDecodeMaxK && N <= 32LL * sms) return 1;
-  return 3;
+  return force_mma() ? 3 : 2;
 }
 
 static bnb_status_t linear_impl(const void *X, int64_t T, int64_t K, const int8_t *Wq,
@@ -168,11 +182,15 @@ static bnb_status_t linear_impl(const void *X, int64_t T, int64_t K, const int8_
           return BNB_ERR_CUDA;
       }
       note_launch();
-      e = launch_act_pass(X, T, K, thr, ws, /*code_mode=*/0, /*with_xo=*/true, dbg_xq,
-                          device_sms(dev), stream);
+      // the tcgen05 GEMM reads fp16 integer codes, the mma GEMM int8 codes
+      e = launch_act_pass(X, T, K, thr, ws, /*code_mode=*/path == 2 ? 1 : 0, /*with_xo=*/true,
+                          dbg_xq, device_sms(dev), stream);
       if (e != cudaSuccess) return BNB_ERR_CUDA;
     }
-    e = launch_gemm_mma(T, K, Wq, Wscale, W16, N, Y, ws, dbg_acc, stream);
+    if (path == 2)
+      e = launch_gemm_tc(T, K, Wq, Wscale, W16, N, Y, ws, dbg_acc, device_sms(dev), stream);
+    else
+      e = launch_gemm_mma(T, K, Wq, Wscale, W16, N, Y, ws, dbg_acc, stream);
     if (e != cudaSuccess) return BNB_ERR_CUDA;
   }
   if (dbg_sx && cudaMemcpyAsync(dbg_sx, ws.sx, (size_t)T * 4, cudaMemcpyDeviceToDevice, stream) != cudaSuccess)

@@ -28,6 +28,7 @@ struct Workspace {
   uint32_t *colmask;   // [8 * ceil(K/256)] outlier column bitmask
   int32_t *O;          // [K + 64] outlier column list, ascending
   float *sx;           // [T] row scales
+  float *sxd;          // [T] row scales / 127 (GEMM epilogue)
   void *xcodes;        // [T x K] codes: int8 (decode) or fp16 integers (GEMM)
   __half *xo;          // [T x kpad] compacted fp16 outlier block
   int64_t kpad;        // pitch of xo in elements (K rounded up to 64)

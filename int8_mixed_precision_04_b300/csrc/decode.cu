@@ -31,6 +31,7 @@
 #include "common.cuh"
 #include "kernels.h"
 #include "mma_frag.cuh"
+#include "sm100_ptx.cuh"
 
 namespace bnb {
 
@@ -55,56 +56,6 @@ __host__ __device__ constexpr int64_t dec_wregion(int64_t K) {
 
 size_t decode_smem_bytes(int64_t K) {
   return (size_t)(dec_wregion(K) + 16 * dec_pitch(K)) + (16 * 32 + 16) * sizeof(float) + 256;
-}
-
-// ---------------------------------------------------------------------------
-// mbarrier / bulk-copy helpers (bounded waits)
-// ---------------------------------------------------------------------------
-
-__device__ __forceinline__ uint32_t smem_addr(const void *p) {
-  return (uint32_t)__cvta_generic_to_shared(p);
-}
-__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count));
-}
-__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
-               "r"(bytes)
-               : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-      " selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(smem_addr(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-// Wait with a time limit (about 2 s); on expiry record a timeout in the
-// workspace status word and return false.
-__device__ __noinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, int32_t *status) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_timer_ns();
-  for (uint32_t it = 1;; it++) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 255u) == 0 && global_timer_ns() - t0 > 2000000000ull) {
-      atomicExch(status, kDevTimeout);
-      return false;
-    }
-  }
-}
-__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes,
-                                         uint64_t *bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
-          "r"(smem_addr(dst)),
-      "l"(src), "r"(bytes), "r"(smem_addr(bar))
-      : "memory");
 }
 
 // ---------------------------------------------------------------------------

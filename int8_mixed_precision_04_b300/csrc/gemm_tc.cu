@@ -1,0 +1,531 @@
+// S4..S6 on the fifth-generation tensor core (tcgen05), for T > 16.
+//
+// What is computed (per output element, t a token, n an output channel):
+//   acc[t,n] = sum_k Xq[t,k] Wq[n,k]                 exact int32
+//   Y[t,n]   = fp16( acc (sx[t]/127)(sw[n]/127) + sum_{k in O} X[t,k] W16[n,k] )
+// i.e. the bulk multiplied in int8 and the outlier feature dimensions in
+// 16-bit, converted back to 16-bit once at the end ("Hugging Face
+// Quantization with bitsandbytes: 4-bit & 8-bit Models Explained", section 2;
+// "bitsandbytes: GPU-Accelerated Inference and Training at Lower Bit
+// Depths", section "How LLM.int8() quantizes weights and activations").
+//
+// Exact int8 products on fp16 tensor cores.  The int8 MMA kind is not
+// available for sm_103a, so the codes (integers in [-127, 127], exact in
+// fp16) go through kind::f16 MMAs with fp32 accumulation.  Every product is
+// an exact integer below 2^14 and every partial sum of at most 1024 columns
+// is below 127^2 * 1024 < 2^24, so the fp32 accumulator holds it exactly.
+// The accumulator is therefore restarted every 1024 columns ("chunk") and
+// drained into an int32 running sum by the epilogue warps: two tensor-memory
+// buffers alternate between chunks, so the drain of one overlaps the MMAs of
+// the next.
+//
+// Tile: 128 output channels (MMA M, tensor-memory lanes) x 256 tokens (MMA N,
+// tensor-memory columns); k advances 64 columns per pipeline stage.
+//   A operand  W codes widened to fp16 integers by four converter warps from
+//              an int8 tile (TMA, 64-byte swizzle) into the 128-byte-swizzled
+//              K-major layout the MMA reads.
+//   B operand  activation codes, already fp16 integers in HBM (written by the
+//              activation pass), loaded by TMA with the 128-byte swizzle.
+// After the int8 chunks, the outlier product runs as one more fp32 chunk:
+// A = W16 columns O gathered by the converter warps, B = the compacted fp16
+// outlier block XO (TMA).  The epilogue combines both and writes Y once.
+//
+// Warp roles (20 warps): 0 TMA producer, 1 MMA issuer and tensor-memory
+// owner, 2-3 converters (two weight rows per thread), 4-19 epilogue (four
+// warps per 32-lane quadrant of tensor memory, one per 64-column quarter, so
+// that each thread holds 64 int32 running sums in registers).  Persistent CTAs, one
+// per SM, walk the tiles with the token tile fastest so that concurrently
+// running CTAs share weight tiles in L2.  Every wait is bounded; a timeout
+// raises a CTA-wide abort flag, records BNB_ERR_TIMEOUT and lets all roles
+// leave, after which in-flight copies and MMAs are waited for and tensor
+// memory is freed.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "sm100_ptx.cuh"
+
+namespace bnb {
+
+namespace {
+
+constexpr int kBM = 128;       // output channels per tile
+constexpr int kBN = 256;       // tokens per tile
+constexpr int kBK = 64;        // k columns per stage (128 bytes of fp16)
+constexpr int kStages = 4;
+constexpr int kChunkStages = 16;  // 16 x 64 = 1024 columns per exact fp32 chunk
+constexpr int kThreads = 640;
+constexpr int kConvWarp0 = 2, kConvWarps = 2;
+constexpr int kEpiWarp0 = 4, kEpiWarps = 16;
+constexpr int kEpiCols = kBN / 4;  // columns per epilogue thread
+constexpr uint32_t kTmemCols = 512;  // two fp32 buffers of kBN columns
+
+constexpr int kXBytes = kBN * kBK * 2;   // B operand tile (fp16)
+constexpr int kWhBytes = kBM * kBK * 2;  // A operand tile (fp16)
+constexpr int kWqBytes = kBM * kBK;      // int8 weight tile
+constexpr int kStageBytes = kXBytes + kWhBytes + kWqBytes;
+static_assert(kStageBytes % 1024 == 0, "stages must keep 1024-byte swizzle alignment");
+constexpr size_t kSmemBytes = (size_t)kStages * kStageBytes + 1024;
+
+// Instruction descriptor of kind::f16: D fp32, A and B fp16, both K-major,
+// N = kBN, M = kBM.
+constexpr uint32_t kIdesc = (1u << 4) | ((uint32_t)(kBN >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
+
+// Shared-memory matrix descriptor of a K-major tile with the 128-byte
+// swizzle: rows of 128 bytes, 8-row groups 1024 bytes apart.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  uint64_t d = (uint64_t)((saddr >> 4) & 0x3FFFu);  // start address
+  d |= (uint64_t)1 << 16;                            // leading offset (unused with this swizzle)
+  d |= (uint64_t)(1024 >> 4) << 32;                  // stride offset: next 8-row group
+  d |= (uint64_t)1 << 46;                            // descriptor version of tcgen05
+  d |= (uint64_t)2 << 61;                            // 128-byte swizzle
+  return d;
+}
+
+struct TcArgs {
+  int64_t T, K, N;
+  int t_tiles, n_tiles;
+  int s_int;  // k stages of the int8 part, ceil(K / 64)
+  const float *sw;
+  const unsigned short *W16;
+  __half *Y;
+  const float *sxd;  // [T] sx / 127
+  const int32_t *O;
+  const uint32_t *nO;
+  int32_t *dbg_acc;
+  int32_t *status;
+};
+
+struct TcSmem {
+  uint64_t full[kStages];   // TMA bytes landed
+  uint64_t conv[kStages];   // widened / gathered A operand written
+  uint64_t empty[kStages];  // MMAs reading the stage done
+  uint64_t accf[2];         // chunk complete in tensor-memory buffer b
+  uint64_t acce[2];         // epilogue finished reading buffer b
+  uint64_t fin;             // MMA warp's own completion fence at exit
+  uint64_t done;            // every epilogue warp has finished with tensor memory
+  uint32_t tmem_base;
+  int abort;
+};
+
+__device__ __forceinline__ uint8_t *stage_x(uint8_t *s, int st) { return s + st * kStageBytes; }
+__device__ __forceinline__ uint8_t *stage_wh(uint8_t *s, int st) {
+  return s + st * kStageBytes + kXBytes;
+}
+__device__ __forceinline__ uint8_t *stage_wq(uint8_t *s, int st) {
+  return s + st * kStageBytes + kXBytes + kWhBytes;
+}
+
+// All lanes wait (each acquires the barrier's phase); the outcome is made
+// warp-uniform.
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, TcSmem &sm,
+                                          int32_t *status) {
+  const bool ok = mbar_wait_abortable(bar, parity, &sm.abort, status);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// Row scales sx/127 of tokens t .. t+7 (0 past T), loaded in program order
+// (volatile) so that the compiler does not hoist them all at once.
+__device__ __forceinline__ void ld_scales8(const float *sxd, int64_t t, int64_t T, float (&s)[8]) {
+  if (t + 8 <= T) {
+    const float *q = sxd + t;  // 32-byte aligned: t is a multiple of 8
+    asm volatile("ld.global.nc.v4.f32 {%0,%1,%2,%3}, [%4];"
+                 : "=f"(s[0]), "=f"(s[1]), "=f"(s[2]), "=f"(s[3])
+                 : "l"(q));
+    asm volatile("ld.global.nc.v4.f32 {%0,%1,%2,%3}, [%4];"
+                 : "=f"(s[4]), "=f"(s[5]), "=f"(s[6]), "=f"(s[7])
+                 : "l"(q + 4));
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) s[i] = t + i < T ? __ldg(sxd + t + i) : 0.0f;
+  }
+}
+
+// 16 int8 codes -> 16 fp16 integers (two 16-byte granules).
+__device__ __forceinline__ void widen16(const uint4 &v, uint4 &g0, uint4 &g1) {
+  s8x4_to_f16x4(v.x, g0.x, g0.y);
+  s8x4_to_f16x4(v.y, g0.z, g0.w);
+  s8x4_to_f16x4(v.z, g1.x, g1.y);
+  s8x4_to_f16x4(v.w, g1.z, g1.w);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
+                   const __grid_constant__ CUtensorMap tm_xo, const TcArgs p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  __shared__ TcSmem sm;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kStages; i++) {
+      mbar_init(&sm.full[i], 1);
+      mbar_init(&sm.conv[i], kConvWarps);
+      mbar_init(&sm.empty[i], 1);
+    }
+    for (int b = 0; b < 2; b++) {
+      mbar_init(&sm.accf[b], 1);
+      mbar_init(&sm.acce[b], kEpiWarps);
+    }
+    mbar_init(&sm.fin, 1);
+    mbar_init(&sm.done, kEpiWarps);
+    sm.abort = 0;
+    mbar_init_fence();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tm_x);
+    tma_prefetch_desc(&tm_w);
+    tma_prefetch_desc(&tm_xo);
+  }
+  if (warp == 1) {
+    tmem_alloc(&sm.tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
+
+  // everything below reads what the activation pass wrote
+  pdl_wait();
+  const int nO = (int)__ldcg(p.nO);
+  const int s_int = p.s_int;
+  const int s_out = (nO + kBK - 1) / kBK;
+  const int nst = s_int + s_out;
+  const int ntiles = p.t_tiles * p.n_tiles;
+
+  // Register split (launch: 640 x 96 = 61440): warpgroup 0 drops to 64, the
+  // four epilogue warpgroups rise to 104 (128 x 64 + 512 x 104 = 61440).
+  // Each warpgroup's branch starts with its own setmaxnreg and never rejoins
+  // the others.
+  if (warp < kEpiWarp0) {
+    regs_dec<64>();
+    // ---------------- TMA producer ----------------
+    if (warp == 0 && lane == 0) {
+      uint32_t it = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+        const int t0 = (tile % p.t_tiles) * kBN, n0 = (tile / p.t_tiles) * kBM;
+        for (int s = 0; s < nst; ++s, ++it) {
+          const int st = it % kStages;
+          const uint32_t ph = (it / kStages) & 1u;
+          if (!mbar_wait_abortable(&sm.empty[st], ph ^ 1u, &sm.abort, p.status)) {
+            ok = false;
+            break;
+          }
+          if (s < s_int) {
+            mbar_expect_tx(&sm.full[st], kXBytes + kWqBytes);
+            tma_load_2d(stage_x(smem, st), &tm_x, s * kBK, t0, &sm.full[st]);
+            tma_load_2d(stage_wq(smem, st), &tm_w, s * kBK, n0, &sm.full[st]);
+          } else {
+            mbar_expect_tx(&sm.full[st], kXBytes);
+            tma_load_2d(stage_x(smem, st), &tm_xo, (s - s_int) * kBK, t0, &sm.full[st]);
+          }
+        }
+      }
+      // copies still in flight land before the CTA may exit
+      for (uint32_t j = it > (uint32_t)kStages ? it - kStages : 0; j < it; ++j)
+        mbar_wait_bounded(&sm.full[j % kStages], (j / kStages) & 1u, p.status);
+    }
+    // ---------------- MMA issuer ----------------
+    if (warp == 1 && lane == 0) {
+      uint32_t it = 0, g = 0;
+      bool ok = true;
+      const int nci = (s_int + kChunkStages - 1) / kChunkStages;
+      const int nchunks = nci + (s_out > 0 ? 1 : 0);
+      for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+        int s = 0;
+        for (int c = 0; c < nchunks && ok; ++c, ++g) {
+          const int s_end = c < nci ? min(s_int, (c + 1) * kChunkStages) : nst;
+          const uint32_t buf = g & 1u;
+          if (!mbar_wait_abortable(&sm.acce[buf], ((g >> 1) & 1u) ^ 1u, &sm.abort, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t d = tmem + buf * kBN;
+          const int s0 = s;
+          for (; s < s_end; ++s, ++it) {
+            const int st = it % kStages;
+            if (!mbar_wait_abortable(&sm.conv[st], (it / kStages) & 1u, &sm.abort, p.status)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint64_t ad = sw128_desc(smem_addr(stage_wh(smem, st)));
+            const uint64_t bd = sw128_desc(smem_addr(stage_x(smem, st)));
+#pragma unroll
+            for (int k = 0; k < kBK / 16; ++k)  // 16 fp16 = 32 bytes per MMA
+              umma_f16(d, ad + 2 * k, bd + 2 * k, kIdesc, (s > s0 || k > 0) ? 1u : 0u);
+            umma_commit(&sm.empty[st]);
+          }
+          if (ok) umma_commit(&sm.accf[buf]);
+        }
+      }
+      // every MMA issued above has completed before tensor memory is freed
+      umma_commit(&sm.fin);
+      mbar_wait_bounded(&sm.fin, 0, p.status);
+    }
+    if (warp == 1) {
+      // free tensor memory once every epilogue warp is done reading it
+      __syncwarp();
+      mbar_wait_bounded(&sm.done, 0, p.status);
+      tc_fence_after();
+      tmem_dealloc(tmem, kTmemCols);
+    }
+    // ---------------- converters: weight rows r0 and r0 + 64 ----------------
+    if (warp >= kConvWarp0) {
+      const int r0 = threadIdx.x - kConvWarp0 * 32;  // 0..63
+      const int64_t K = p.K, N = p.N;
+      uint32_t it = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+        const int64_t nb = (int64_t)(tile / p.t_tiles) * kBM;
+        for (int s = 0; s < nst; ++s, ++it) {
+          const int st = it % kStages;
+          if (!warp_wait(&sm.full[st], (it / kStages) & 1u, sm, p.status)) {
+            ok = false;
+            break;
+          }
+          if (s < s_int) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int r = r0 + 64 * h;
+              // int8 row r: 64 bytes, 16-byte chunk q stored at q ^ ((r >> 1) & 3)
+              const uint8_t *wq = stage_wq(smem, st) + r * 64;
+              uint8_t *wh = stage_wh(smem, st) + r * 128;
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                const uint4 v = *reinterpret_cast<const uint4 *>(wq + 16 * (q ^ ((r >> 1) & 3)));
+                uint4 g0, g1;
+                widen16(v, g0, g1);
+                *reinterpret_cast<uint4 *>(wh + 16 * ((2 * q) ^ (r & 7))) = g0;
+                *reinterpret_cast<uint4 *>(wh + 16 * ((2 * q + 1) ^ (r & 7))) = g1;
+              }
+            }
+          } else {
+            // outlier columns O[jb .. jb+63] of W16 rows (zero past |O| or N)
+            const int jb = (s - s_int) * kBK;
+            for (int h = 0; h < 2; ++h) {
+              const int r = r0 + 64 * h;
+              const int64_t n = nb + r;
+              const unsigned short *wrow = p.W16 + n * K;
+              uint8_t *wh = stage_wh(smem, st) + r * 128;
+              for (int gi = 0; gi < 8; ++gi) {
+                const int j0 = jb + 8 * gi;
+                uint4 v = make_uint4(0, 0, 0, 0);
+                if (n < N && j0 < nO) {
+                  const int32_t k0 = __ldcg(p.O + j0);
+                  const bool full8 = j0 + 7 < nO;
+                  const int32_t k7 = full8 ? __ldcg(p.O + j0 + 7) : -1;
+                  if (full8 && k7 - k0 == 7 && (k0 & 7) == 0) {
+                    v = __ldg(reinterpret_cast<const uint4 *>(wrow + k0));  // 8 adjacent columns
+                  } else {
+                    uint32_t hv[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                      hv[e] = (j0 + e < nO) ? (uint32_t)__ldg(wrow + __ldcg(p.O + j0 + e)) : 0u;
+                    v = make_uint4(hv[0] | (hv[1] << 16), hv[2] | (hv[3] << 16),
+                                   hv[4] | (hv[5] << 16), hv[6] | (hv[7] << 16));
+                  }
+                }
+                *reinterpret_cast<uint4 *>(wh + 16 * (gi ^ (r & 7))) = v;
+              }
+            }
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sm.conv[st]);
+        }
+      }
+    }
+  } else {
+    regs_inc<104>();
+    // ---------------- epilogue ----------------
+    const int e = warp - kEpiWarp0;
+    const int quad = warp & 3, part = e >> 2;
+    const uint32_t lane_field = (uint32_t)(32 * quad) << 16;
+    const int64_t T = p.T, N = p.N;
+    const int nci = (s_int + kChunkStages - 1) / kChunkStages;
+    uint32_t g = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+      const int64_t t0 = (int64_t)(tile % p.t_tiles) * kBN + part * kEpiCols;
+      const int64_t n = (int64_t)(tile / p.t_tiles) * kBM + 32 * quad + lane;
+      int acc[kEpiCols];
+      for (int c = 0; c < nci; ++c, ++g) {
+        const uint32_t buf = g & 1u;
+        if (!warp_wait(&sm.accf[buf], (g >> 1) & 1u, sm, p.status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t base = tmem + lane_field + buf * kBN + part * kEpiCols;
+#pragma unroll
+        for (int j = 0; j < kEpiCols / 8; ++j) {
+          uint32_t v[8];
+          tmem_ld8(base + 8 * j, v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int q = __float2int_rn(__uint_as_float(v[i]));
+            acc[8 * j + i] = c == 0 ? q : acc[8 * j + i] + q;
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.acce[buf]);
+      }
+      if (!ok) break;
+      if (p.dbg_acc && n < N) {
+#pragma unroll
+        for (int i = 0; i < kEpiCols; ++i)
+          if (t0 + i < T) p.dbg_acc[(t0 + i) * N + n] = acc[i];
+      }
+      const bool has_out = s_out > 0;
+      const uint32_t obuf = g & 1u;
+      if (has_out) {
+        if (!warp_wait(&sm.accf[obuf], (g >> 1) & 1u, sm, p.status)) break;
+        tc_fence_after();
+      }
+      const float swn = n < N ? __fdiv_rn(__ldg(p.sw + n), 127.0f) : 0.0f;
+      const uint32_t obase = tmem + lane_field + obuf * kBN + part * kEpiCols;
+#pragma unroll
+      for (int j = 0; j < kEpiCols / 8; ++j) {
+        const int64_t tj = t0 + 8 * j;
+        uint32_t o[8];
+        if (has_out) {
+          tmem_ld8(obase + 8 * j, o);
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) o[i] = 0u;
+        }
+        float sx[8];
+        ld_scales8(p.sxd, tj, T, sx);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          o[i] = __float_as_uint(fmaf((float)acc[8 * j + i] * sx[i], swn, __uint_as_float(o[i])));
+        // lanes pair up so that each store writes two adjacent channels
+#pragma unroll
+        for (int i = 0; i < 8; i += 2) {
+          const int64_t ta = tj + i;
+          const float ya = __uint_as_float(o[i]), yb = __uint_as_float(o[i + 1]);
+          const float recv = __shfl_xor_sync(0xffffffffu, (lane & 1) ? ya : yb, 1);
+          if ((N & 1) == 0) {
+            if (lane & 1) {
+              if (ta + 1 < T && n < N)
+                *reinterpret_cast<__half2 *>(p.Y + (ta + 1) * N + n - 1) = __floats2half2_rn(recv, yb);
+            } else {
+              if (ta < T && n < N)
+                *reinterpret_cast<__half2 *>(p.Y + ta * N + n) = __floats2half2_rn(ya, recv);
+            }
+          } else if (n < N) {
+            if (ta < T) p.Y[ta * N + n] = __float2half_rn(ya);
+            if (ta + 1 < T) p.Y[(ta + 1) * N + n] = __float2half_rn(yb);
+          }
+        }
+      }
+      if (has_out) {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.acce[obuf]);
+        ++g;
+      }
+    }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.done);
+  }
+  // No block-wide barrier follows: the warpgroups run under different
+  // register budgets and leave independently.
+}
+
+// ---- host side ----------------------------------------------------------------
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// 2-D row-major tensor [outer x inner] with `row_bytes` between rows.
+bool encode_2d(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint64_t inner,
+               uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
+               CUtensorMapSwizzle swz) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, dt, 2, const_cast<void *>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_tc(int64_t T, int64_t K, const int8_t *Wq, const float *sw,
+                           const void *W16, int64_t N, void *Y, const Workspace &ws,
+                           int32_t *dbg_acc, int num_sms, cudaStream_t stream) {
+  static bool attr_set = false;  // benign race: every writer sets the same value
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  CUtensorMap tm_x, tm_w, tm_xo;
+  if (!encode_2d(&tm_x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, ws.xcodes, (uint64_t)K, (uint64_t)T,
+                 (uint64_t)K * 2, kBK, kBN, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_2d(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, Wq, (uint64_t)K, (uint64_t)N, (uint64_t)K,
+                 kBK, kBM, CU_TENSOR_MAP_SWIZZLE_64B) ||
+      !encode_2d(&tm_xo, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, ws.xo, (uint64_t)ws.kpad, (uint64_t)T,
+                 (uint64_t)ws.kpad * 2, kBK, kBN, CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  TcArgs a;
+  a.T = T;
+  a.K = K;
+  a.N = N;
+  a.t_tiles = (int)((T + kBN - 1) / kBN);
+  a.n_tiles = (int)((N + kBM - 1) / kBM);
+  a.s_int = (int)((K + kBK - 1) / kBK);
+  a.sw = sw;
+  a.W16 = reinterpret_cast<const unsigned short *>(W16);
+  a.Y = reinterpret_cast<__half *>(Y);
+  a.sxd = ws.sxd;
+  a.O = ws.O;
+  a.nO = ws.counters + 1;
+  a.dbg_acc = dbg_acc;
+  a.status = ws.status;
+  const int64_t tiles = (int64_t)a.t_tiles * a.n_tiles;
+  const unsigned grid = (unsigned)(tiles < num_sms ? tiles : num_sms);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  ProfScope ps(kKidGemmTc, stream);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_tc_kernel, tm_x, tm_w, tm_xo, a);
+  note_launch();
+  return e;
+}
+
+}  // namespace bnb
