@@ -10,9 +10,11 @@ the int8 decomposition linear, whole job.
 Default workload: the decode GEMV configuration (X fp16 [16, 4096] with 4
 seeded outlier columns x U(8,60), W fp16 [4096, 4096] ~ N(0, 0.02), tau 6).
 A step is one token batch through a stack of 16 such layers, each with its
-own weight, so that the 16 x 16.8 MB of int8 weights (268 MB) exceed the
-126 MB L2 and every call streams its weight from HBM.  The timed region
-replays CUDA graphs of captured library calls; inputs are resident in HBM.
+own weight, input and output, so that the 16 x 16.8 MB of int8 weights
+(268 MB) exceed the 126 MB L2 and every call streams its weight from HBM.
+The timed region replays CUDA graphs of captured library calls; inputs are
+resident in HBM.  `--workload prefill|large|sweep|tiny` runs the other named
+shapes the same way (with as many layers as it takes to exceed 2x L2).
 
 `e2e` is the same metric through the public API with host buffers: per call
 a pinned host->device copy of X, the library call, and a device->host copy of
@@ -20,8 +22,9 @@ Y, all inside the timed region.
 
 `roofline` is for the dominant kernel: its algorithmic bytes (or flops) per
 launch over its average duration, measured with CUDA events around a CUDA
-graph of that kernel alone (library profiling mode 2, which re-launches only
-the main kernel on the act-pass results the timed calls left behind).
+graph of that kernel alone (library profiling mode 2, which launches only the
+main kernel of the path: the fused decode kernel, or the GEMM on the
+activation-pass results the timed calls left behind).
 
 `--impl reference` times the CPU oracle (the reference arm of this build):
 each step is a bounded sample of the same workload (all rows of X, a
@@ -88,9 +91,10 @@ def algorithmic_bytes(T, N, K, nO):
 
 def kernel_algorithmic(kernel, T, N, K, nO):
     """(bytes, flops) per launch of one kernel, for the roofline."""
-    if kernel == "dec_gemv":
-        # weight codes + scales + outlier weight columns + int8 codes of X + Y
-        return N * K + 4 * N + 2 * N * nO + T * K + 2 * T * N, 2 * T * N * K
+    if kernel == "dec_fused":
+        # the whole decode call: X read once, weight codes + scales + outlier
+        # weight columns, Y written once
+        return 2 * T * K + N * K + 4 * N + 2 * N * nO + 2 * T * N, 2 * T * N * K
     if kernel in ("gemm_mma", "gemm_tc"):
         return N * K + 2 * T * K + 2 * T * N + 2 * N * nO, 2 * T * N * K + 2 * T * N * nO
     if kernel == "outlier_scan":
@@ -316,7 +320,7 @@ def run_ours(args, world, rank, local):
     # profiling mode 2 reuses the act-pass results left in the workspace by the
     # calls above, same X and tau), timed with CUDA events on its stream
     path = lib.bnb_int8_linear_path(T, N, K)
-    kname = {1: "dec_gemv", 2: "gemm_tc", 3: "gemm_mma"}[path]
+    kname = {1: "dec_fused", 2: "gemm_tc", 3: "gemm_mma"}[path]
     Gk = max(1, min(G, 8))
     binding.profile_enable(2)
     try:

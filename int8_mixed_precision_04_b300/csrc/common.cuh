@@ -5,7 +5,7 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
-#include "../../include/bnb_int8.h"
+#include "bnb_int8.h"
 
 namespace bnb {
 
@@ -17,9 +17,10 @@ constexpr int32_t kDevTimeout = BNB_ERR_TIMEOUT;
 // device attribute, this is only a default for host-side heuristics.
 constexpr int kB300Sms = 148;
 
-// Largest K the decode path holds in shared memory: 32 weight rows and 16
-// code rows of K + 64 bytes, plus small buffers, within 227 KB.
-constexpr int64_t kDecodeMaxK = 4608;
+// Largest K of the decode path: 32 weight rows and 16 code rows of K + 64
+// bytes plus the outlier list fit in 227 KB, and the activation pass gives
+// each of 16 warps x 32 lanes one 8-column vector.
+constexpr int64_t kDecodeMaxK = 4096;
 
 // Workspace layout, carved identically by the host for every call.
 struct Workspace {

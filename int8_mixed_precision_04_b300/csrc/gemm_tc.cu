@@ -57,9 +57,26 @@ constexpr int kBN = 256;       // tokens per tile
 constexpr int kBK = 64;        // k columns per stage (128 bytes of fp16)
 constexpr int kStages = 4;
 constexpr int kChunkStages = 16;  // 16 x 64 = 1024 columns per exact fp32 chunk
-constexpr int kThreads = 640;
-constexpr int kConvWarp0 = 2, kConvWarps = 2;
-constexpr int kEpiWarp0 = 4, kEpiWarps = 16;
+// Converter warps: 4 (warpgroup 1 of their own; measured 1.36x faster than 2,
+// because widening the weight tile bounds the MMA rate) or 2 (warps 2-3 of
+// warpgroup 0).
+#ifndef BNB_TC_CONV_WARPS
+#define BNB_TC_CONV_WARPS 4
+#endif
+constexpr int kConvWarps = BNB_TC_CONV_WARPS;
+static_assert(kConvWarps == 2 || kConvWarps == 4, "2 or 4 converter warps");
+constexpr int kConvWarp0 = kConvWarps == 2 ? 2 : 4;
+constexpr int kConvRows = kBM / (kConvWarps * 32);  // weight rows per converter thread
+constexpr int kEpiWarp0 = kConvWarps == 2 ? 4 : 8, kEpiWarps = 16;
+constexpr int kThreads = (kEpiWarp0 + kEpiWarps) * 32;
+// Register split; the sum never exceeds the launch's threads x registers
+// (640 x 96 or 768 x 80, what ptxas grants under __launch_bounds__(kThreads, 1)).
+constexpr int kRegsWG0 = kConvWarps == 2 ? 64 : 32;
+constexpr int kRegsConv = 64;  // warpgroup 1 when it holds the converters
+constexpr int kRegsEpi = kConvWarps == 2 ? 104 : 96;
+static_assert(kConvWarps == 2 ? 128 * kRegsWG0 + 512 * kRegsEpi <= 640 * 96
+                              : 128 * kRegsWG0 + 128 * kRegsConv + 512 * kRegsEpi <= 768 * 80,
+              "register split exceeds the launch budget");
 constexpr int kEpiCols = kBN / 4;  // columns per epilogue thread
 constexpr uint32_t kTmemCols = 512;  // two fp32 buffers of kBN columns
 
@@ -152,6 +169,77 @@ __device__ __forceinline__ void widen16(const uint4 &v, uint4 &g0, uint4 &g1) {
   s8x4_to_f16x4(v.w, g1.z, g1.w);
 }
 
+// Converter warps: widen the int8 weight tile of each stage into the fp16
+// A operand (or, in the outlier stages, gather the W16 outlier columns).
+// Thread ct owns weight rows ct, ct + 32 * kConvWarps, ...
+__device__ __forceinline__ void converter_role(uint8_t *smem, TcSmem &sm, const TcArgs &p,
+                                               int nO, int s_int, int nst, int ntiles) {
+  const int ct = threadIdx.x - kConvWarp0 * 32;  // 0 .. 32 * kConvWarps - 1
+  const int lane = threadIdx.x & 31;
+  const int64_t K = p.K, N = p.N;
+  uint32_t it = 0;
+  bool ok = true;
+  for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+    const int64_t nb = (int64_t)(tile / p.t_tiles) * kBM;
+    for (int s = 0; s < nst; ++s, ++it) {
+      const int st = it % kStages;
+      if (!warp_wait(&sm.full[st], (it / kStages) & 1u, sm, p.status)) {
+        ok = false;
+        break;
+      }
+      if (s < s_int) {
+#pragma unroll
+        for (int h = 0; h < kConvRows; ++h) {
+          const int r = ct + kConvWarps * 32 * h;
+          // int8 row r: 64 bytes, 16-byte chunk q stored at q ^ ((r >> 1) & 3)
+          const uint8_t *wq = stage_wq(smem, st) + r * 64;
+          uint8_t *wh = stage_wh(smem, st) + r * 128;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const uint4 v = *reinterpret_cast<const uint4 *>(wq + 16 * (q ^ ((r >> 1) & 3)));
+            uint4 g0, g1;
+            widen16(v, g0, g1);
+            *reinterpret_cast<uint4 *>(wh + 16 * ((2 * q) ^ (r & 7))) = g0;
+            *reinterpret_cast<uint4 *>(wh + 16 * ((2 * q + 1) ^ (r & 7))) = g1;
+          }
+        }
+      } else {
+        // outlier columns O[jb .. jb+63] of W16 rows (zero past |O| or N)
+        const int jb = (s - s_int) * kBK;
+        for (int h = 0; h < kConvRows; ++h) {
+          const int r = ct + kConvWarps * 32 * h;
+          const int64_t n = nb + r;
+          const unsigned short *wrow = p.W16 + n * K;
+          uint8_t *wh = stage_wh(smem, st) + r * 128;
+          for (int gi = 0; gi < 8; ++gi) {
+            const int j0 = jb + 8 * gi;
+            uint4 v = make_uint4(0, 0, 0, 0);
+            if (n < N && j0 < nO) {
+              const int32_t k0 = __ldcg(p.O + j0);
+              const bool full8 = j0 + 7 < nO;
+              const int32_t k7 = full8 ? __ldcg(p.O + j0 + 7) : -1;
+              if (full8 && k7 - k0 == 7 && (k0 & 7) == 0) {
+                v = __ldg(reinterpret_cast<const uint4 *>(wrow + k0));  // 8 adjacent columns
+              } else {
+                uint32_t hv[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                  hv[e] = (j0 + e < nO) ? (uint32_t)__ldg(wrow + __ldcg(p.O + j0 + e)) : 0u;
+                v = make_uint4(hv[0] | (hv[1] << 16), hv[2] | (hv[3] << 16),
+                               hv[4] | (hv[5] << 16), hv[6] | (hv[7] << 16));
+              }
+            }
+            *reinterpret_cast<uint4 *>(wh + 16 * (gi ^ (r & 7))) = v;
+          }
+        }
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.conv[st]);
+    }
+  }
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
                    const __grid_constant__ CUtensorMap tm_xo, const TcArgs p) {
@@ -197,12 +285,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int nst = s_int + s_out;
   const int ntiles = p.t_tiles * p.n_tiles;
 
-  // Register split (launch: 640 x 96 = 61440): warpgroup 0 drops to 64, the
-  // four epilogue warpgroups rise to 104 (128 x 64 + 512 x 104 = 61440).
-  // Each warpgroup's branch starts with its own setmaxnreg and never rejoins
-  // the others.
-  if (warp < kEpiWarp0) {
-    regs_dec<64>();
+  // Register split (see kRegs*): each warpgroup's branch starts with its own
+  // setmaxnreg and never rejoins the others.
+  if (warp < 4) {
+    regs_dec<kRegsWG0>();
     // ---------------- TMA producer ----------------
     if (warp == 0 && lane == 0) {
       uint32_t it = 0;
@@ -276,74 +362,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       tmem_dealloc(tmem, kTmemCols);
     }
-    // ---------------- converters: weight rows r0 and r0 + 64 ----------------
-    if (warp >= kConvWarp0) {
-      const int r0 = threadIdx.x - kConvWarp0 * 32;  // 0..63
-      const int64_t K = p.K, N = p.N;
-      uint32_t it = 0;
-      bool ok = true;
-      for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
-        const int64_t nb = (int64_t)(tile / p.t_tiles) * kBM;
-        for (int s = 0; s < nst; ++s, ++it) {
-          const int st = it % kStages;
-          if (!warp_wait(&sm.full[st], (it / kStages) & 1u, sm, p.status)) {
-            ok = false;
-            break;
-          }
-          if (s < s_int) {
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              const int r = r0 + 64 * h;
-              // int8 row r: 64 bytes, 16-byte chunk q stored at q ^ ((r >> 1) & 3)
-              const uint8_t *wq = stage_wq(smem, st) + r * 64;
-              uint8_t *wh = stage_wh(smem, st) + r * 128;
-#pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                const uint4 v = *reinterpret_cast<const uint4 *>(wq + 16 * (q ^ ((r >> 1) & 3)));
-                uint4 g0, g1;
-                widen16(v, g0, g1);
-                *reinterpret_cast<uint4 *>(wh + 16 * ((2 * q) ^ (r & 7))) = g0;
-                *reinterpret_cast<uint4 *>(wh + 16 * ((2 * q + 1) ^ (r & 7))) = g1;
-              }
-            }
-          } else {
-            // outlier columns O[jb .. jb+63] of W16 rows (zero past |O| or N)
-            const int jb = (s - s_int) * kBK;
-            for (int h = 0; h < 2; ++h) {
-              const int r = r0 + 64 * h;
-              const int64_t n = nb + r;
-              const unsigned short *wrow = p.W16 + n * K;
-              uint8_t *wh = stage_wh(smem, st) + r * 128;
-              for (int gi = 0; gi < 8; ++gi) {
-                const int j0 = jb + 8 * gi;
-                uint4 v = make_uint4(0, 0, 0, 0);
-                if (n < N && j0 < nO) {
-                  const int32_t k0 = __ldcg(p.O + j0);
-                  const bool full8 = j0 + 7 < nO;
-                  const int32_t k7 = full8 ? __ldcg(p.O + j0 + 7) : -1;
-                  if (full8 && k7 - k0 == 7 && (k0 & 7) == 0) {
-                    v = __ldg(reinterpret_cast<const uint4 *>(wrow + k0));  // 8 adjacent columns
-                  } else {
-                    uint32_t hv[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                      hv[e] = (j0 + e < nO) ? (uint32_t)__ldg(wrow + __ldcg(p.O + j0 + e)) : 0u;
-                    v = make_uint4(hv[0] | (hv[1] << 16), hv[2] | (hv[3] << 16),
-                                   hv[4] | (hv[5] << 16), hv[6] | (hv[7] << 16));
-                  }
-                }
-                *reinterpret_cast<uint4 *>(wh + 16 * (gi ^ (r & 7))) = v;
-              }
-            }
-          }
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&sm.conv[st]);
-        }
-      }
-    }
+    if (kConvWarps == 2 && warp >= kConvWarp0) converter_role(smem, sm, p, nO, s_int, nst, ntiles);
+  } else if (kConvWarps == 4 && warp < kEpiWarp0) {
+    regs_dec<kRegsConv>();
+    converter_role(smem, sm, p, nO, s_int, nst, ntiles);
   } else {
-    regs_inc<104>();
+    regs_inc<kRegsEpi>();
     // ---------------- epilogue ----------------
     const int e = warp - kEpiWarp0;
     const int quad = warp & 3, part = e >> 2;

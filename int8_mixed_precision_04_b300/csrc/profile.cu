@@ -8,8 +8,8 @@
 namespace bnb {
 
 static const char *const kKernelNames[kKernelCount] = {
-    "memset_status_mask", "outlier_scan", "quantize_rows", "dec_gemv",
-    "gemm_mma",           "gemm_tc",      "quantize_weight", "dec_act"};
+    "memset_status_mask", "outlier_scan", "quantize_rows", "dec_fused",
+    "gemm_mma",           "gemm_tc",      "quantize_weight"};
 
 namespace {
 struct Rec {
