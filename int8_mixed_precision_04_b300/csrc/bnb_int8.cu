@@ -132,9 +132,10 @@ static bool force_mma() {
 }
 
 // 1: decode (T <= 16, the codes and a 32-row weight slice fit shared memory,
-// at most 32 output channels per SM); 2: tcgen05 GEMM; 3: legacy mma GEMM.
-static int choose_path(int64_t T, int64_t N, int64_t K, int sms = kB300Sms) {
-  if (T <= 16 && K <= kDecodeMaxK && N <= 32LL * sms) return 1;
+// at most 32 output channels per resident CTA); 2: tcgen05 GEMM; 3: legacy
+// mma GEMM.
+static int choose_path(int64_t T, int64_t N, int64_t K, int dev) {
+  if (T <= 16 && K <= kDecodeMaxK && N <= 32LL * decode_max_ctas(dev)) return 1;
   return force_mma() ? 3 : 2;
 }
 
@@ -163,13 +164,13 @@ static bnb_status_t linear_impl(const void *X, int64_t T, int64_t K, const int8_
   if (st != BNB_OK) return st;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_v);
   const Workspace ws = carve(workspace, T, K);
-  const int path = choose_path(T, N, K, device_sms(dev));
+  const int path = choose_path(T, N, K, dev);
   const uint32_t thr = threshold_bits(tau);
   cudaError_t e;
   if (path == 1) {
     // decode: no memset, the act-pass kernel clears the status word
     e = launch_decode(X, T, K, thr, Wq, Wscale, W16, N, Y, ws, dbg_xq, dbg_acc,
-                      device_sms(dev), stream);
+                      decode_max_ctas(dev), stream);
     if (e != cudaSuccess) return BNB_ERR_CUDA;
   } else {
     if (!profile_only_main()) {
@@ -272,9 +273,9 @@ uint64_t bnb_launch_count(void) { return g_launches.load(std::memory_order_relax
 
 int bnb_int8_linear_path(int64_t T, int64_t N, int64_t K) {
   if (T <= 0 || N <= 0 || K <= 0) return 0;
-  int dev = 0, sms = kB300Sms;
-  if (cudaGetDevice(&dev) == cudaSuccess) sms = device_sms(dev);
-  return choose_path(T, N, K, sms);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) dev = -1;
+  return choose_path(T, N, K, dev);
 }
 
 }  // extern "C"

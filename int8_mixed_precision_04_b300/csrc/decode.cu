@@ -1,21 +1,25 @@
 // The whole layer for decode-sized T (T <= 16) in one kernel per call.
 //
 // dec_fused: one CTA per slice of at most 32 output channels (one CTA per
-// SM).  At launch all its threads put the CTA's whole int8 weight slice in
-// flight with 16-byte async copies, before waiting on the previous kernel of
-// the stream (the weight does not depend on X).  While the
-// weight streams in, the 16 consumer warps run the activation pass over all
-// of X themselves, so that no second kernel and no inter-kernel dependency
-// sits on the path:
-//   - warp w owns a slab of 256 columns; every lane one 8-column vector of
-//     all T rows.  A column is an outlier feature dimension when |x| >= tau
-//     in some row ("Hugging Face Quantization with bitsandbytes: 4-bit &
-//     8-bit Models Explained", sections 2 and 3); the test needs only that
-//     column, so it is lane-local.  The row maxima over non-outlier columns
-//     are reduced per warp, then across warps through shared memory;
-//   - vector-wise int8 codes rint(fl32(127 x) / sx) of the non-outlier
-//     columns go to shared memory, and the ascending outlier column list is
-//     compacted from per-warp counts.
+// SM), in thread-block clusters of kDecCluster CTAs.  At launch the producer
+// warp puts the CTA's whole int8 weight slice in flight on the copy engine
+// (one bulk copy per row), before waiting on the previous kernel of the
+// stream (the weight does not depend on X).  While the weight streams in,
+// the cluster runs the
+// activation pass cooperatively, so that no second kernel and no
+// inter-kernel dependency sits on the path, and no CTA repeats the others'
+// work:
+//   - CTA rank c owns a quarter of the columns; each consumer lane one
+//     8-column vector of four rows.  A column is an outlier feature dimension
+//     when |x| >= tau in some row ("Hugging Face Quantization with
+//     bitsandbytes: 4-bit & 8-bit Models Explained", sections 2 and 3): the
+//     four row-quads' flags are OR-ed through shared memory.  Row maxima over
+//     non-outlier columns are reduced per warp, per CTA, and across the
+//     cluster through distributed shared memory, as are the outlier counts;
+//   - each CTA then writes the vector-wise int8 codes rint(fl32(127 x) / sx)
+//     of its columns, its part of the ascending outlier list and the X values
+//     of the first outlier columns, into the shared memory of every CTA of
+//     the cluster.
 // CTA 0 also writes sx, O and |O| to the workspace (and the codes when
 // asked), for the debug entry point.
 // Then each consumer warp owns one K-range for all four 8-row groups: it
@@ -27,6 +31,10 @@
 // ones.  Epilogue: the int32 partials are summed, scaled by (sx/127)(sw/127),
 // the 16-bit outlier product is added ("converted back to 16-bit at the end",
 // same page, section 2) and Y is written once.
+#include <cooperative_groups.h>
+
+#include <atomic>
+
 #include "common.cuh"
 #include "kernels.h"
 #include "mma_frag.cuh"
@@ -39,7 +47,11 @@ constexpr int kDecThreads = (kDecWarps + 1) * 32;  // + one producer warp
 constexpr int kDecMaxRows = 32;                    // output channels per CTA (4 groups of 8)
 constexpr int kDecChunkK = 1024;                   // fp32 accumulation is drained this often
 constexpr int kDecOutSmall = 64;                   // outlier columns the producer warp sums
-static_assert(kDecodeMaxK <= kDecWarps * 256, "one 8-column vector per act-pass lane");
+constexpr int kDecCluster = 4;                     // CTAs sharing one activation pass
+// act pass: consumer lane L handles vector (L & 127) of its CTA's columns and
+// rows 4 * (L >> 7) .. +3, so a CTA covers at most 128 vectors
+static_assert(kDecodeMaxK <= kDecCluster * 128 * 8, "act-pass lanes cover every column");
+static_assert(kDecWarps == 16, "four row-quads of four warps");
 
 __host__ __device__ constexpr int64_t dec_pitch(int64_t K) { return K + 64; }  // bytes per row
 // K columns of MMA warp w: [w * range, min(K, (w + 1) * range)), range a multiple of 64
@@ -53,12 +65,23 @@ __host__ __device__ constexpr int64_t dec_wregion(int64_t K) {
 }
 __host__ __device__ constexpr int64_t dec_ocap(int64_t K) { return (K + 7) / 8 * 8; }
 
-// weight rows, code rows, outlier list (uint16), osm [16][32], sxs [16],
-// part [16 warps][16 rows], cnt [16 warps], one mbarrier
+// dynamic: weight rows, code rows, outlier list (uint16)
 size_t decode_smem_bytes(int64_t K) {
-  return (size_t)(dec_wregion(K) + 16 * dec_pitch(K) + 2 * dec_ocap(K)) +
-         (16 * 32 + 16 + kDecWarps * 16 + kDecWarps) * 4 + 8;
+  return (size_t)(dec_wregion(K) + 16 * dec_pitch(K) + 2 * dec_ocap(K));
 }
+
+// small static buffers of one CTA (partly read by the other CTAs of its cluster)
+struct DecSmall {
+  uint64_t wbar;            // the CTA's weight slice has landed
+  uint64_t obar;            // producer warp's outlier sums are in osm
+  float osm[16 * 32];       // [t][row] outlier sums of the first kDecOutSmall columns
+  float sxs[16];            // row scales sx
+  uint32_t part[kDecWarps * 4];  // [warp][row of its quad] partial row maxima (fp16 bits)
+  uint32_t pub[20];         // published to the cluster: [t] CTA row maxima, [16] outlier count
+  uint32_t wcnt[4];         // outlier count of each quad-0 warp
+  uint8_t fpart[4 * 128];   // [quad][vector] outlier flags of four rows
+  unsigned short xo[16 * kDecOutSmall];  // [t][j] X at the first outlier columns (fp16)
+};
 
 struct DecArgs {
   const uint4 *X;              // [T x K] fp16 as 16-byte vectors
@@ -96,34 +119,31 @@ __global__ void __launch_bounds__(kDecThreads, 1) dec_fused_kernel(const DecArgs
   uint8_t *ws = smem;                                          // [32][pitch] weight codes
   uint8_t *xs = smem + dec_wregion(K);                         // [16][pitch] activation codes
   uint16_t *ocols = reinterpret_cast<uint16_t *>(xs + 16 * pitch);  // outlier columns
-  float *osm = reinterpret_cast<float *>(ocols + dec_ocap(K));  // [16 t][32 rows]
-  float *sxs = osm + 16 * 32;                                   // [16] row scales
-  uint32_t *part = reinterpret_cast<uint32_t *>(sxs + 16);      // [16 warps][16 rows]
-  uint32_t *cnt = part + kDecWarps * 16;                        // [16 warps]
-  uint64_t *obar = reinterpret_cast<uint64_t *>(cnt + kDecWarps);
+  __shared__ DecSmall sm;
+  float *osm = sm.osm, *sxs = sm.sxs;
+  uint64_t *obar = &sm.obar;
   uint32_t *red = reinterpret_cast<uint32_t *>(smem);  // [16 warps][32][16], after the main loop
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int T = p.T;
   const int64_t n0 = (int64_t)blockIdx.x * p.rows_per_cta;
-  const int64_t rows = min(p.N, n0 + p.rows_per_cta) - n0;  // 1..32
+  const int64_t rows = min(p.N, n0 + p.rows_per_cta) - n0;  // <= 32; <= 0 for trailing CTAs
 
-  if (threadIdx.x == 0) {
-    mbar_init(obar, 32);
-    mbar_init_fence();
-  }
-  // The whole weight slice in flight at once: every thread issues 16-byte
-  // async copies of its share (consecutive threads, consecutive chunks of a
-  // row).  Weight rows past `rows`, code rows past T and the pads past K are
-  // never written: the MMAs mask columns past K, and accumulator rows >= T or
-  // columns >= rows are never stored.
-  {
-    const int64_t cpr = K / 16;  // 16-byte chunks per row
-    for (int64_t i = threadIdx.x; i < rows * cpr; i += kDecThreads) {
-      const int64_t r = i / cpr, c = (i - r * cpr) * 16;
-      cp_async16(ws + r * pitch + c, p.Wq + (n0 + r) * K + c, true);
+  if (warp == kDecWarps) {
+    // The whole weight slice in flight at once, on the copy engine: one bulk
+    // copy per weight row, so that every warp is free for the activation
+    // pass while the slice streams in.  Weight rows past `rows`, code rows
+    // past T and the pads past K are never written: the MMAs mask columns
+    // past K, and accumulator rows >= T or columns >= rows are never stored.
+    if (lane == 0) {
+      mbar_init(&sm.wbar, 1);
+      mbar_init(obar, 32);
+      mbar_init_fence();
+      mbar_expect_tx(&sm.wbar, (uint32_t)(rows > 0 ? rows * K : 0));
     }
-    cp_async_commit();
+    __syncwarp();
+    for (int64_t r = lane; r < rows; r += 32)
+      bulk_g2s(ws + r * pitch, p.Wq + (n0 + r) * K, (uint32_t)K, &sm.wbar);
   }
   __syncthreads();
   // the next kernel on the stream may launch now; it waits for our completion
@@ -131,20 +151,29 @@ __global__ void __launch_bounds__(kDecThreads, 1) dec_fused_kernel(const DecArgs
   // X may be the output of the previous kernel on the stream
   pdl_wait();
 
-  // ---- activation pass, phase 1: outlier columns and partial row maxima ----
+  namespace cg = cooperative_groups;
+  cg::cluster_group cluster = cg::this_cluster();
+  const int crank = (int)cluster.block_rank();
+
+  // ---- activation pass 1: outlier columns and partial row maxima ----
   const int64_t vecs = K / 8;
-  const int64_t v = (int64_t)warp * 32 + lane;  // this lane's 8-column vector
-  const bool live = warp < kDecWarps && v < vecs;
-  uint4 x[16];
+  const int64_t vpc = (vecs + kDecCluster - 1) / kDecCluster;  // vectors per CTA (<= 128)
+  const int quad = (threadIdx.x >> 7) & 3;                      // rows 4 quad .. 4 quad + 3
+  const int64_t vl = threadIdx.x & 127;
+  const int64_t v = crank * vpc + vl;                           // this lane's 8-column vector
+  const bool live = warp < kDecWarps && vl < vpc && v < vecs;
+  uint4 x[4];
   uint32_t flags = 0;
   if (warp < kDecWarps) {
 #pragma unroll
-    for (int t = 0; t < 16; t++)  // all loads in flight before any is used
-      x[t] = (t < T && live) ? __ldg(p.X + t * vecs + v) : make_uint4(0, 0, 0, 0);
+    for (int r = 0; r < 4; r++) {  // all loads in flight before any is used
+      const int t = 4 * quad + r;
+      x[r] = (t < T && live) ? __ldg(p.X + t * vecs + v) : make_uint4(0, 0, 0, 0);
+    }
 #pragma unroll
-    for (int t = 0; t < 16; t++) {
-      if (t < T) {  // padding rows must not flag columns (tau = 0 flags a zero)
-        const uint32_t w[4] = {x[t].x, x[t].y, x[t].z, x[t].w};
+    for (int r = 0; r < 4; r++) {
+      if (4 * quad + r < T) {  // padding rows must not flag columns (tau = 0 flags a zero)
+        const uint32_t w[4] = {x[r].x, x[r].y, x[r].z, x[r].w};
 #pragma unroll
         for (int i = 0; i < 4; i++) {
           flags |= (uint32_t)(abs_bits_lo(w[i]) >= p.thr) << (2 * i);
@@ -153,9 +182,17 @@ __global__ void __launch_bounds__(kDecThreads, 1) dec_fused_kernel(const DecArgs
       }
     }
     if (!live) flags = 0;
+    sm.fpart[quad * 128 + vl] = (uint8_t)flags;
+  }
+  __syncthreads();
+  if (warp < kDecWarps) {
+    // a column is an outlier if any of the call's rows flags it
+    flags = live ? (uint32_t)(sm.fpart[vl] | sm.fpart[128 + vl] | sm.fpart[256 + vl] |
+                              sm.fpart[384 + vl])
+                 : 0u;
 #pragma unroll
-    for (int t = 0; t < 16; t++) {
-      const uint32_t w[4] = {x[t].x, x[t].y, x[t].z, x[t].w};
+    for (int r = 0; r < 4; r++) {
+      const uint32_t w[4] = {x[r].x, x[r].y, x[r].z, x[r].w};
       uint32_t m = 0;
 #pragma unroll
       for (int i = 0; i < 4; i++) {
@@ -164,38 +201,52 @@ __global__ void __launch_bounds__(kDecThreads, 1) dec_fused_kernel(const DecArgs
       }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
-      if (lane == 0) part[warp * 16 + t] = m;
+      if (lane == 0) sm.part[warp * 4 + r] = m;
     }
-    uint32_t c = __popc(flags);
+    if (quad == 0) {  // warps 0..3 hold each column of this CTA once
+      uint32_t c = __popc(flags);
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
-    if (lane == 0) cnt[warp] = c;
+      for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+      if (lane == 0) sm.wcnt[warp] = c;
+    }
   }
   __syncthreads();
+  if (threadIdx.x < 16) {  // this CTA's maximum of row t over its non-outlier columns
+    const int t = threadIdx.x, q = t >> 2, r = t & 3;
+    uint32_t m = 0;
+    for (int w = 4 * q; w < 4 * q + 4; w++) m = max(m, sm.part[w * 4 + r]);
+    sm.pub[t] = m;
+  } else if (threadIdx.x == 16) {
+    sm.pub[16] = sm.wcnt[0] + sm.wcnt[1] + sm.wcnt[2] + sm.wcnt[3];
+  }
+  cluster.sync();  // every CTA's row maxima and outlier count are published
 
-  // |O| and this warp's offset in the ascending outlier list
-  uint32_t nO_u = 0, base = 0;
-  for (int w = 0; w < kDecWarps; w++) {
-    const uint32_t cc = cnt[w];
+  // ---- activation pass 2: row scales, outlier list, int8 codes (cluster-wide) ----
+  uint32_t nO_u = 0, base = 0;  // |O| and this CTA's offset in the ascending outlier list
+  for (int c = 0; c < kDecCluster; c++) {
+    const uint32_t cc = cluster.map_shared_rank(sm.pub, c)[16];
     nO_u += cc;
-    if (w < warp) base += cc;
+    if (c < crank) base += cc;
   }
   const int32_t nO = (int32_t)nO_u;
-
-  // ---- activation pass, phase 2: row scales, outlier list, int8 codes ----
   if (warp < kDecWarps) {
     uint32_t m = 0;
     if (lane < 16)
-      for (int w = 0; w < kDecWarps; w++) m = max(m, part[w * 16 + lane]);
-    const float a_lane = h2f_bits(m);  // sx of row `lane` (0 for rows >= T)
+      for (int c = 0; c < kDecCluster; c++) m = max(m, cluster.map_shared_rank(sm.pub, c)[lane]);
+    const float a_lane = h2f_bits(m);      // sx of row `lane` (0 for rows >= T)
+    const float rc_lane = code_recip(a_lane);  // 127 / sx, one division per row
     if (warp == 0 && lane < 16) sxs[lane] = a_lane;
-    if (blockIdx.x == 0 && warp == 0) {
-      if (lane < T) p.sx_out[lane] = a_lane;
-      if (lane == 0) {
-        *p.nO_out = nO_u;
-        *p.status = kDevOk;
-      }
+    uint8_t *xs_c[kDecCluster];
+    uint16_t *oc_c[kDecCluster];
+    unsigned short *xo_c[kDecCluster];
+#pragma unroll
+    for (int c = 0; c < kDecCluster; c++) {
+      xs_c[c] = cluster.map_shared_rank(xs, c);
+      oc_c[c] = cluster.map_shared_rank(ocols, c);
+      xo_c[c] = cluster.map_shared_rank(sm.xo, c);
     }
+    // this CTA's outliers in the ascending list: warps (of each row-quad) by
+    // column, lanes by column, bits.  Every row-quad holds the same columns.
     const uint32_t pc = __popc(flags);
     uint32_t incl = pc;
 #pragma unroll
@@ -205,25 +256,35 @@ __global__ void __launch_bounds__(kDecThreads, 1) dec_fused_kernel(const DecArgs
     }
     if (live && flags) {
       uint32_t j = base + incl - pc;
+      for (int w = 0; w < (warp & 3); w++) j += sm.wcnt[w];
 #pragma unroll
       for (int b = 0; b < 8; b++)
         if ((flags >> b) & 1) {
-          ocols[j] = (uint16_t)(8 * v + b);
-          if (blockIdx.x == 0) p.O_out[j] = (int32_t)(8 * v + b);
+          if (quad == 0)
+            for (int c = 0; c < kDecCluster; c++) oc_c[c][j] = (uint16_t)(8 * v + b);
+          if (j < (uint32_t)kDecOutSmall) {  // X at this outlier column, rows of this quad
+#pragma unroll
+            for (int r = 0; r < 4; r++) {
+              const int t = 4 * quad + r;
+              const unsigned short hb = (unsigned short)(((&x[r].x)[b >> 1] >> (16 * (b & 1))) & 0xffffu);
+              if (t < T)
+                for (int c = 0; c < kDecCluster; c++) xo_c[c][t * kDecOutSmall + j] = hb;
+            }
+          }
           ++j;
         }
     }
 #pragma unroll
-    for (int t = 0; t < 16; t++) {
+    for (int r = 0; r < 4; r++) {
+      const int t = 4 * quad + r;
       const float a = __shfl_sync(0xffffffffu, a_lane, t);
-      if (t >= T || !live) continue;
-      const float r = code_recip(a);
-      const uint32_t w[4] = {x[t].x, x[t].y, x[t].z, x[t].w};
+      const float rc = __shfl_sync(0xffffffffu, rc_lane, t);
+      const uint32_t w[4] = {x[r].x, x[r].y, x[r].z, x[r].w};
       int cd[8];
 #pragma unroll
       for (int i = 0; i < 4; i++) {
-        cd[2 * i] = ((flags >> (2 * i)) & 1) ? 0 : code_of(h2f_bits(w[i] & 0xffffu), a, r);
-        cd[2 * i + 1] = ((flags >> (2 * i + 1)) & 1) ? 0 : code_of(h2f_bits(w[i] >> 16), a, r);
+        cd[2 * i] = ((flags >> (2 * i)) & 1) ? 0 : code_of(h2f_bits(w[i] & 0xffffu), a, rc);
+        cd[2 * i + 1] = ((flags >> (2 * i + 1)) & 1) ? 0 : code_of(h2f_bits(w[i] >> 16), a, rc);
       }
       uint32_t p0 = 0, p1 = 0;
 #pragma unroll
@@ -231,13 +292,38 @@ __global__ void __launch_bounds__(kDecThreads, 1) dec_fused_kernel(const DecArgs
         p0 |= (uint32_t)(cd[i] & 0xff) << (8 * i);
         p1 |= (uint32_t)(cd[4 + i] & 0xff) << (8 * i);
       }
-      *reinterpret_cast<uint2 *>(xs + t * pitch + 8 * v) = make_uint2(p0, p1);
-      if (blockIdx.x == 0 && p.dbg_xq)
-        reinterpret_cast<uint2 *>(p.dbg_xq)[t * vecs + v] = make_uint2(p0, p1);
+      // even lanes store 16 codes (their vector and the next lane's) at once
+      const uint32_t q0 = __shfl_down_sync(0xffffffffu, p0, 1);
+      const uint32_t q1 = __shfl_down_sync(0xffffffffu, p1, 1);
+      if (t >= T || !live) continue;
+      if ((vpc & 1) == 0) {
+        // vpc even: an even lane holds an even vector (16-byte aligned codes)
+        // and its odd neighbour is live, so it writes both
+        if ((lane & 1) == 0)
+          for (int c = 0; c < kDecCluster; c++)
+            *reinterpret_cast<uint4 *>(xs_c[c] + t * pitch + 8 * v) = make_uint4(p0, p1, q0, q1);
+      } else {
+        for (int c = 0; c < kDecCluster; c++)
+          *reinterpret_cast<uint2 *>(xs_c[c] + t * pitch + 8 * v) = make_uint2(p0, p1);
+      }
     }
   }
-  cp_async_wait_all();  // this thread's weight copies have landed
-  __syncthreads();      // all weight rows, codes, outlier list and row scales are in shared memory
+  cluster.sync();  // every CTA holds all codes, the outlier list and its X values
+
+  if (blockIdx.x == 0) {  // the activation pass's results, for the debug entry point
+    if (threadIdx.x < T) p.sx_out[threadIdx.x] = sxs[threadIdx.x];
+    if (threadIdx.x == 0) {
+      *p.nO_out = nO_u;
+      *p.status = kDevOk;
+    }
+    for (int32_t j = threadIdx.x; j < nO; j += kDecThreads) p.O_out[j] = ocols[j];
+    if (p.dbg_xq)
+      for (int64_t i = threadIdx.x; i < (int64_t)T * vecs; i += kDecThreads) {
+        const int64_t t = i / vecs, vv = i - t * vecs;
+        reinterpret_cast<uint2 *>(p.dbg_xq)[i] = *reinterpret_cast<const uint2 *>(xs + t * pitch + 8 * vv);
+      }
+  }
+  if (rows <= 0) return;  // a cluster's last CTAs may have no output channels
 
   if (warp == kDecWarps) {
     // ---- producer warp: the first outlier columns for this slice, lane = row ----
@@ -246,12 +332,16 @@ __global__ void __launch_bounds__(kDecThreads, 1) dec_fused_kernel(const DecArgs
 #pragma unroll
     for (int t = 0; t < 16; t++) o[t] = 0.f;
     const int64_t n = n0 + min((int64_t)lane, rows - 1);
-    for (int32_t j = 0; j < nsmall; j++) {
-      const int64_t k = ocols[j];
-      const float wv = h2f_bits(__ldg(p.W16 + n * K + k));
+    for (int32_t jb = 0; jb < nsmall; jb += 8) {
+      float wv[8];
 #pragma unroll
-      for (int t = 0; t < 16; t++)
-        if (t < T) o[t] = fmaf(h2f_bits(__ldg(p.X16 + t * K + k)), wv, o[t]);
+      for (int e = 0; e < 8; e++)  // eight independent loads in flight
+        wv[e] = jb + e < nsmall ? h2f_bits(__ldg(p.W16 + n * K + ocols[jb + e])) : 0.f;
+#pragma unroll
+      for (int e = 0; e < 8; e++)
+#pragma unroll
+        for (int t = 0; t < 16; t++)
+          if (t < T && jb + e < nsmall) o[t] = fmaf(h2f_bits(sm.xo[t * kDecOutSmall + jb + e]), wv[e], o[t]);
     }
 #pragma unroll
     for (int t = 0; t < 16; t++) osm[t * 32 + lane] = o[t];
@@ -263,7 +353,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) dec_fused_kernel(const DecArgs
   const int g = lane >> 2, q = lane & 3;
   const int64_t k0 = warp * range, k1 = min(K, k0 + range);
   int acc[4][4] = {};
-  if (k1 > k0) {
+  if (k1 > k0 && mbar_wait_bounded(&sm.wbar, 0, p.status)) {
     float f[4][4] = {};
     int nb = 0;
     for (int64_t kb = k0; kb < k1; kb += 64) {
@@ -368,18 +458,40 @@ __global__ void __launch_bounds__(kDecThreads, 1) dec_fused_kernel(const DecArgs
 // host side
 // ---------------------------------------------------------------------------
 
+// CTAs of dec_fused that can be resident at once, in whole clusters (queried
+// once per device; the nominal B300 count when no device answers).
+int decode_max_ctas(int dev) {
+  static std::atomic<int> cache[64];
+  if (dev >= 0 && dev < 64) {
+    const int v = cache[dev].load(std::memory_order_relaxed);
+    if (v > 0) return v;
+  }
+  int n = 0;
+  if (cudaFuncSetAttribute(dec_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)decode_smem_bytes(kDecodeMaxK)) == cudaSuccess) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(kDecCluster * 64);
+    cfg.blockDim = dim3(kDecThreads);
+    cfg.dynamicSmemBytes = decode_smem_bytes(kDecodeMaxK);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kDecCluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, dec_fused_kernel, &cfg) != cudaSuccess) n = 0;
+  }
+  (void)cudaGetLastError();  // a failed query is not a launch error
+  const int v = n > 0 ? n * kDecCluster : kB300Sms / kDecCluster * kDecCluster;
+  if (n > 0 && dev >= 0 && dev < 64) cache[dev].store(v, std::memory_order_relaxed);
+  return v;
+}
+
 cudaError_t launch_decode(const void *X, int64_t T, int64_t K, uint32_t thr, const int8_t *Wq,
                           const float *sw, const void *W16, int64_t N, void *Y,
-                          const Workspace &ws, int8_t *dbg_xq, int32_t *dbg_acc, int num_sms,
+                          const Workspace &ws, int8_t *dbg_xq, int32_t *dbg_acc, int max_ctas,
                           cudaStream_t stream) {
-  static bool attr_set = false;  // benign race: every writer sets the same value
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(dec_fused_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)decode_smem_bytes(kDecodeMaxK));
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
   DecArgs a;
   a.X = reinterpret_cast<const uint4 *>(X);
   a.X16 = reinterpret_cast<const unsigned short *>(X);
@@ -387,9 +499,12 @@ cudaError_t launch_decode(const void *X, int64_t T, int64_t K, uint32_t thr, con
   a.K = K;
   a.N = N;
   a.thr = thr;
-  int64_t ctas = min((int64_t)num_sms, (N + 7) / 8);
-  a.rows_per_cta = (N + ctas - 1) / ctas;  // <= 32: the host only routes N <= 32 * SMs here
-  ctas = (N + a.rows_per_cta - 1) / a.rows_per_cta;
+  // enough whole clusters for at most 32 output channels per CTA (the host
+  // only routes N <= 32 * max_ctas here), all of them resident at once
+  const int64_t want = min((int64_t)max_ctas, ((N + 7) / 8 + kDecCluster - 1) / kDecCluster * kDecCluster);
+  a.rows_per_cta = (N + want - 1) / want;
+  const int64_t used = (N + a.rows_per_cta - 1) / a.rows_per_cta;
+  const int64_t ctas = (used + kDecCluster - 1) / kDecCluster * kDecCluster;
   a.Wq = Wq;
   a.sw = sw;
   a.W16 = reinterpret_cast<const unsigned short *>(W16);
@@ -405,11 +520,15 @@ cudaError_t launch_decode(const void *X, int64_t T, int64_t K, uint32_t thr, con
   cfg.blockDim = dim3(kDecThreads);
   cfg.dynamicSmemBytes = decode_smem_bytes(K);
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kDecCluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = profile_only_main() ? 0 : 1;  // profiling mode 2: no overlap with the previous call
+  cfg.numAttrs = profile_only_main() ? 1 : 2;  // profiling mode 2: no overlap with the previous call
   ProfScope ps(kKidDecFused, stream);
   const cudaError_t e = cudaLaunchKernelEx(&cfg, dec_fused_kernel, a);
   note_launch();
