@@ -131,11 +131,10 @@ static bool force_mma() {
   return v;
 }
 
-// 1: decode (T <= 16, the codes and a 32-row weight slice fit shared memory,
-// at most 32 output channels per resident CTA); 2: tcgen05 GEMM; 3: legacy
-// mma GEMM.
+// 1: decode (T <= 16, K <= kDecodeMaxK, at most 128 output channels per
+// resident cluster); 2: tcgen05 GEMM; 3: legacy mma GEMM.
 static int choose_path(int64_t T, int64_t N, int64_t K, int dev) {
-  if (T <= 16 && K <= kDecodeMaxK && N <= 32LL * decode_max_ctas(dev)) return 1;
+  if (T <= 16 && K <= kDecodeMaxK && N <= decode_max_n(dev)) return 1;
   return force_mma() ? 3 : 2;
 }
 
@@ -169,8 +168,7 @@ static bnb_status_t linear_impl(const void *X, int64_t T, int64_t K, const int8_
   cudaError_t e;
   if (path == 1) {
     // decode: no memset, the act-pass kernel clears the status word
-    e = launch_decode(X, T, K, thr, Wq, Wscale, W16, N, Y, ws, dbg_xq, dbg_acc,
-                      decode_max_ctas(dev), stream);
+    e = launch_decode(X, T, K, thr, Wq, Wscale, W16, N, Y, ws, dbg_xq, dbg_acc, stream);
     if (e != cudaSuccess) return BNB_ERR_CUDA;
   } else {
     if (!profile_only_main()) {

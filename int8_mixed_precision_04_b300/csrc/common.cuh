@@ -76,6 +76,25 @@ __device__ __forceinline__ int code_exact(float x, float a, float r) {
 // is 0 and code_exact is not used).
 __device__ __forceinline__ float code_recip(float a) { return a > 0.0f ? 127.0f / a : 0.0f; }
 
+// The same code as code_exact, from ALU operations only (no rounding or
+// float-to-integer conversion instructions), returned as q mod 256 (the
+// int8 code's byte):
+//   M = 1.5 * 2^23 has unit spacing, so (p + M) - M is p rounded to an
+//   integer and one comparison turns it into f = floor(p) (any f within a
+//   few ulp of v's floor serves, since the fma below decides exactly);
+//   f + M is exact for |f| < 2^22 with bit pattern bits(M) + f, whose low
+//   byte is f mod 256 (bits(M) ends in a zero byte).
+// Requires |x| <= a, a > 0 finite, or x = a = 0 (which gives 0).
+__device__ __forceinline__ uint32_t code_byte(float x, float a, float r) {
+  constexpr float kM = 12582912.0f;
+  const float p = x * r;
+  const float rn = (p + kM) - kM;
+  const float f = rn > p ? rn - 1.0f : rn;
+  const float s = fmaf(f + 0.5f, a, -127.0f * x);
+  const uint32_t fb = __float_as_uint(f + kM);
+  return fb + (s < 0.0f ? 1u : (s == 0.0f ? (fb & 1u) : 0u));
+}
+
 __device__ __forceinline__ int code_of(float x, float a, float r) {
   return a > 0.0f ? code_exact(x, a, r) : 0;
 }

@@ -129,21 +129,10 @@ __global__ void __launch_bounds__(kDecThreads, 1) dec_fused_kernel(const DecArgs
   const int64_t n0 = (int64_t)blockIdx.x * p.rows_per_cta;
   const int64_t rows = min(p.N, n0 + p.rows_per_cta) - n0;  // <= 32; <= 0 for trailing CTAs
 
-  if (warp == kDecWarps) {
-    // The whole weight slice in flight at once, on the copy engine: one bulk
-    // copy per weight row, so that every warp is free for the activation
-    // pass while the slice streams in.  Weight rows past `rows`, code rows
-    // past T and the pads past K are never written: the MMAs mask columns
-    // past K, and accumulator rows >= T or columns >= rows are never stored.
-    if (lane == 0) {
-      mbar_init(&sm.wbar, 1);
-      mbar_init(obar, 32);
-      mbar_init_fence();
-      mbar_expect_tx(&sm.wbar, (uint32_t)(rows > 0 ? rows * K : 0));
-    }
-    __syncwarp();
-    for (int64_t r = lane; r < rows; r += 32)
-      bulk_g2s(ws + r * pitch, p.Wq + (n0 + r) * K, (uint32_t)K, &sm.wbar);
+  if (warp == kDecWarps && lane == 0) {
+    mbar_init(&sm.wbar, 1);
+    mbar_init(obar, 32);
+    mbar_init_fence();
   }
   __syncthreads();
   // the next kernel on the stream may launch now; it waits for our completion
@@ -164,12 +153,26 @@ __global__ void __launch_bounds__(kDecThreads, 1) dec_fused_kernel(const DecArgs
   const bool live = warp < kDecWarps && vl < vpc && v < vecs;
   uint4 x[4];
   uint32_t flags = 0;
-  if (warp < kDecWarps) {
+  if (warp == kDecWarps) {
+    // The whole weight slice in flight at once, on the copy engine: one bulk
+    // copy per weight row, so that every warp is free for the activation
+    // pass while the slice streams in.  It goes out right behind the X loads,
+    // so that the few X bytes on the critical path do not queue behind the
+    // weights.  Weight rows past `rows`, code rows past T and the pads past K
+    // are never written: the MMAs mask columns past K, and accumulator rows
+    // >= T or columns >= rows are never stored.
+    asm volatile("bar.sync 2, %0;" ::"r"(kDecThreads) : "memory");  // X loads issued
+    if (lane == 0) mbar_expect_tx(&sm.wbar, (uint32_t)(rows > 0 ? rows * K : 0));
+    __syncwarp();
+    for (int64_t r = lane; r < rows; r += 32)
+      bulk_g2s(ws + r * pitch, p.Wq + (n0 + r) * K, (uint32_t)K, &sm.wbar);
+  } else {
 #pragma unroll
     for (int r = 0; r < 4; r++) {  // all loads in flight before any is used
       const int t = 4 * quad + r;
       x[r] = (t < T && live) ? __ldg(p.X + t * vecs + v) : make_uint4(0, 0, 0, 0);
     }
+    asm volatile("bar.arrive 2, %0;" ::"r"(kDecThreads) : "memory");
 #pragma unroll
     for (int r = 0; r < 4; r++) {
       if (4 * quad + r < T) {  // padding rows must not flag columns (tau = 0 flags a zero)
@@ -222,17 +225,26 @@ __global__ void __launch_bounds__(kDecThreads, 1) dec_fused_kernel(const DecArgs
   cluster.sync();  // every CTA's row maxima and outlier count are published
 
   // ---- activation pass 2: row scales, outlier list, int8 codes (cluster-wide) ----
-  uint32_t nO_u = 0, base = 0;  // |O| and this CTA's offset in the ascending outlier list
+  // all remote reads in flight at once: row maxima (lane & 15) and counts
+  uint32_t rmax[kDecCluster], rcnt[kDecCluster];
+#pragma unroll
   for (int c = 0; c < kDecCluster; c++) {
-    const uint32_t cc = cluster.map_shared_rank(sm.pub, c)[16];
-    nO_u += cc;
-    if (c < crank) base += cc;
+    const uint32_t *pub = cluster.map_shared_rank(sm.pub, c);
+    rmax[c] = pub[lane & 15];
+    rcnt[c] = pub[16];
+  }
+  uint32_t nO_u = 0, base = 0;  // |O| and this CTA's offset in the ascending outlier list
+#pragma unroll
+  for (int c = 0; c < kDecCluster; c++) {
+    nO_u += rcnt[c];
+    if (c < crank) base += rcnt[c];
   }
   const int32_t nO = (int32_t)nO_u;
   if (warp < kDecWarps) {
     uint32_t m = 0;
-    if (lane < 16)
-      for (int c = 0; c < kDecCluster; c++) m = max(m, cluster.map_shared_rank(sm.pub, c)[lane]);
+#pragma unroll
+    for (int c = 0; c < kDecCluster; c++) m = max(m, rmax[c]);
+    if (lane >= 16) m = 0;
     const float a_lane = h2f_bits(m);      // sx of row `lane` (0 for rows >= T)
     const float rc_lane = code_recip(a_lane);  // 127 / sx, one division per row
     if (warp == 0 && lane < 16) sxs[lane] = a_lane;
@@ -280,17 +292,18 @@ __global__ void __launch_bounds__(kDecThreads, 1) dec_fused_kernel(const DecArgs
       const float a = __shfl_sync(0xffffffffu, a_lane, t);
       const float rc = __shfl_sync(0xffffffffu, rc_lane, t);
       const uint32_t w[4] = {x[r].x, x[r].y, x[r].z, x[r].w};
-      int cd[8];
-#pragma unroll
-      for (int i = 0; i < 4; i++) {
-        cd[2 * i] = ((flags >> (2 * i)) & 1) ? 0 : code_of(h2f_bits(w[i] & 0xffffu), a, rc);
-        cd[2 * i + 1] = ((flags >> (2 * i + 1)) & 1) ? 0 : code_of(h2f_bits(w[i] >> 16), a, rc);
-      }
       uint32_t p0 = 0, p1 = 0;
 #pragma unroll
       for (int i = 0; i < 4; i++) {
-        p0 |= (uint32_t)(cd[i] & 0xff) << (8 * i);
-        p1 |= (uint32_t)(cd[4 + i] & 0xff) << (8 * i);
+        const uint32_t c0 =
+            ((flags >> (2 * i)) & 1) ? 0u : code_byte(h2f_bits(w[i] & 0xffffu), a, rc);
+        const uint32_t c1 =
+            ((flags >> (2 * i + 1)) & 1) ? 0u : code_byte(h2f_bits(w[i] >> 16), a, rc);
+        const uint32_t two = (c0 & 0xffu) | ((c1 & 0xffu) << 8);
+        if (i < 2)
+          p0 |= two << (16 * i);
+        else
+          p1 |= two << (16 * (i - 2));
       }
       // even lanes store 16 codes (their vector and the next lane's) at once
       const uint32_t q0 = __shfl_down_sync(0xffffffffu, p0, 1);
@@ -488,10 +501,16 @@ int decode_max_ctas(int dev) {
   return v;
 }
 
+// Output channels the decode path can take: at most 32 per resident CTA.
+int64_t decode_max_n(int dev) { return 32LL * decode_max_ctas(dev); }
+
 cudaError_t launch_decode(const void *X, int64_t T, int64_t K, uint32_t thr, const int8_t *Wq,
                           const float *sw, const void *W16, int64_t N, void *Y,
-                          const Workspace &ws, int8_t *dbg_xq, int32_t *dbg_acc, int max_ctas,
+                          const Workspace &ws, int8_t *dbg_xq, int32_t *dbg_acc,
                           cudaStream_t stream) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) dev = -1;
+  const int max_ctas = decode_max_ctas(dev);
   DecArgs a;
   a.X = reinterpret_cast<const uint4 *>(X);
   a.X16 = reinterpret_cast<const unsigned short *>(X);

@@ -51,13 +51,14 @@ cudaError_t launch_act_pass(const void *X, int64_t T, int64_t K, uint32_t thr_bi
                             const Workspace &ws, int code_mode, bool with_xo,
                             int8_t *dbg_xq, int num_sms, cudaStream_t stream);
 
-// The whole layer for T <= 16, K <= kDecodeMaxK, N <= 32 x decode_max_ctas
-// in one kernel (activation pass fused into the GEMV, shared by clusters of
+// The whole layer for T <= 16, K <= kDecodeMaxK, N <= decode_max_n(dev) in
+// one kernel (activation pass fused into the GEMV and shared by clusters of
 // CTAs), launched with programmatic dependent launch.
 int decode_max_ctas(int dev);
+int64_t decode_max_n(int dev);
 cudaError_t launch_decode(const void *X, int64_t T, int64_t K, uint32_t thr, const int8_t *Wq,
                           const float *sw, const void *W16, int64_t N, void *Y,
-                          const Workspace &ws, int8_t *dbg_xq, int32_t *dbg_acc, int max_ctas,
+                          const Workspace &ws, int8_t *dbg_xq, int32_t *dbg_acc,
                           cudaStream_t stream);
 
 // S4..S6 on tcgen05 tensor cores (fp16 integer codes from the activation

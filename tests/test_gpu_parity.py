@@ -66,6 +66,27 @@ def test_integer_inputs_exact(orc, T, K, adversarial):
         assert np.abs(ref["acc"]).max() == 127 * 127 * K
 
 
+@pytest.mark.parametrize("T", [16, 40])
+def test_code_rounding_ties(orc, T):
+    """Every code is an exact half-integer quotient: row absmax 127 * 2^e and
+    values (k + 1/2) * 2^e, so 127 x / sx = k + 1/2 and the code must round to
+    the even neighbour (the decode path at T = 16, the GEMM path at T = 40)."""
+    rng = np.random.default_rng(17)
+    K = 512
+    X = np.empty((T, K), dtype=np.float64)
+    for t in range(T):
+        e = int(rng.integers(-9, 6))
+        vals = (rng.integers(-127, 127, size=K) + 0.5) * 2.0 ** e
+        vals[rng.integers(0, K)] = 127.0 * 2.0 ** e * (1 if t % 2 else -1)
+        X[t] = vals
+    X16 = X.astype(np.float16)
+    assert np.array_equal(X16.astype(np.float64), X)  # every value exact in fp16
+    W = (rng.standard_normal((96, K)) * 0.02).astype(np.float16)
+    r, ref = run_and_compare(orc, X16, W, math.inf, what=f"ties T{T}")
+    q = ref["Xq"].astype(np.int64)
+    assert np.all(q % 2 == 0) or np.any(np.abs(q) == 127)  # ties went to even codes
+
+
 def test_workspace_reuse(orc):
     """Consecutive calls on one workspace with different thresholds."""
     import torch
