@@ -72,9 +72,10 @@ typedef enum {
  * Bytes of device workspace that bnb_int8_linear / bnb_int8_linear_debug
  * need for a call of this shape (0 for a non-positive dimension).  The
  * workspace holds the outlier column mask and index list, the row scales,
- * the activation codes and the compacted fp16 outlier block; it needs no
- * initialisation and its contents after a call are unspecified except the
- * device status word read by bnb_last_device_status.
+ * the activation codes, the fp16 outlier block of X and W16's outlier
+ * columns for the GEMM path; it needs no initialisation and its contents
+ * after a call are unspecified except the device status word read by
+ * bnb_last_device_status.
  */
 size_t bnb_int8_linear_workspace_bytes(int64_t T, int64_t N, int64_t K);
 
@@ -148,7 +149,7 @@ bnb_status_t bnb_last_device_status(const void *workspace, void *stream, int32_t
  *   Arguments as for bnb_int8_linear, without workspace/workspace_bytes.
  *   Calls whose bnb_int8_linear_workspace_bytes(T, N, K) exceeds
  *   BNB_NOALLOC_SCRATCH_BYTES are rejected with BNB_ERR_UNSUPPORTED before
- *   anything is enqueued (at K = 4096 that admits T up to about 500).
+ *   anything is enqueued (at K = N = 4096 that admits T up to 382).
  *   The first call on a device looks up the array's device address with
  *   that device current (cudaGetSymbolAddress) and caches it; make that first
  *   call before any stream capture.  BNB_ERR_CUDA if the lookup fails.

@@ -10,7 +10,9 @@
 //   the ascending index list O and |O| (no grid-wide wait is needed).
 // S3 (quantize_rows_kernel): per row, sx[t] = max |X[t,k]| over non-outlier
 //   k; codes rint(fl32(127 x)/sx) for non-outlier k, 0 for outliers; and the
-//   fp16 outlier block XO[t,j] = X[t,O[j]], zero-padded to a multiple of 64.
+//   fp16 outlier block: compacted, XO[t,j] = X[t,O[j]] zero-padded to a
+//   multiple of 64, or, when outliers are dense (outlier_block_dense), X
+//   masked to the outlier columns (zero elsewhere) over all K columns.
 //
 // Both kernels are HBM-bound: 16-byte coalesced loads, warp-shuffle and
 // shared-memory reductions.
@@ -108,6 +110,7 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_rows_kernel(
   const int64_t vecs = K / 8;
   const uint32_t lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int32_t nO = (int32_t)__ldcg(counters + 1);
+  const bool dense = kMode == 1 && outlier_block_dense(nO, K);  // the tcgen05 GEMM's form
   for (int64_t t = blockIdx.x; t < T; t += gridDim.x) {
     const uint4 *row = X + t * vecs;
     uint32_t m = 0;
@@ -163,8 +166,16 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_rows_kernel(
         reinterpret_cast<uint4 *>(codes)[t * vecs + v] = make_uint4(h[0], h[1], h[2], h[3]);
       }
       if (dbg_xq) reinterpret_cast<uint2 *>(dbg_xq)[t * vecs + v] = make_uint2(p0, p1);
+      if (xo && dense) {  // X masked to the outlier columns, zero elsewhere
+        uint32_t m[4];
+#pragma unroll
+        for (int i = 0; i < 4; i++)
+          m[i] = (((fl >> (2 * i)) & 1) ? (w[i] & 0xffffu) : 0u) |
+                 (((fl >> (2 * i + 1)) & 1) ? (w[i] & 0xffff0000u) : 0u);
+        *reinterpret_cast<uint4 *>(xo + t * kpad + 8 * v) = make_uint4(m[0], m[1], m[2], m[3]);
+      }
     }
-    if (xo) {
+    if (xo && !dense) {  // compacted outlier block XO[t, j] = X[t, O[j]], zero to a multiple of 64
       const unsigned short *xr = reinterpret_cast<const unsigned short *>(row);
       const int32_t jend = (nO + 63) & ~63;
       for (int32_t j = threadIdx.x; j < jend; j += kQuantThreads) {
@@ -208,6 +219,34 @@ cudaError_t launch_act_pass(const void *X, int64_t T, int64_t K, uint32_t thr_bi
     quantize_rows_kernel<1><<<(unsigned)qblocks, kQuantThreads, 0, stream>>>(
         reinterpret_cast<const uint4 *>(X), T, K, ws.colmask, ws.counters, ws.O, ws.sx,
         ws.sxd, ws.xcodes, with_xo ? ws.xo : nullptr, ws.kpad, dbg_xq);
+  note_launch();
+  return cudaGetLastError();
+}
+
+// One warp per weight row: w16o[n, j] = W16[n, O[j]] for j < |O|, zero up to
+// the next multiple of 64.  Each element is one scattered sector of W16; the
+// copy is made once per call, so the GEMM's token tiles read it by TMA.
+__global__ void __launch_bounds__(256) gather_outlier_weights_kernel(
+    const unsigned short *__restrict__ W16, int64_t N, int64_t K, const int32_t *__restrict__ O,
+    const uint32_t *__restrict__ counters, unsigned short *__restrict__ w16o, int64_t opad) {
+  const int32_t nO = (int32_t)__ldcg(counters + 1);
+  if (outlier_block_dense(nO, K)) return;  // the GEMM reads W16 itself
+  const int32_t jend = (nO + 63) & ~63;
+  const int64_t warps = (int64_t)gridDim.x * (blockDim.x / 32);
+  const int lane = threadIdx.x & 31;
+  for (int64_t n = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32; n < N; n += warps)
+    for (int32_t j = lane; j < jend; j += 32)
+      w16o[n * opad + j] = j < nO ? __ldg(W16 + n * K + __ldcg(O + j)) : (unsigned short)0;
+}
+
+cudaError_t launch_gather_outlier_weights(const void *W16, int64_t N, int64_t K,
+                                          const Workspace &ws, int num_sms, cudaStream_t stream) {
+  int64_t blocks = (N + 7) / 8;
+  if (blocks > 8LL * num_sms) blocks = 8LL * num_sms;
+  ProfScope ps(kKidGatherW16, stream);
+  gather_outlier_weights_kernel<<<(unsigned)blocks, 256, 0, stream>>>(
+      reinterpret_cast<const unsigned short *>(W16), N, K, ws.O, ws.counters,
+      reinterpret_cast<unsigned short *>(ws.w16o), ws.opad);
   note_launch();
   return cudaGetLastError();
 }

@@ -17,11 +17,11 @@ static inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; 
 static inline bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 
 struct Layout {
-  size_t status, counters, colmask, O, sx, sxd, xcodes, xo, total;
-  int64_t kpad;
+  size_t status, counters, colmask, O, sx, sxd, xcodes, xo, w16o, total;
+  int64_t kpad, opad;
 };
 
-static Layout layout_of(int64_t T, int64_t K) {
+static Layout layout_of(int64_t T, int64_t N, int64_t K) {
   Layout L;
   L.kpad = (K + 63) / 64 * 64;
   size_t off = 0;
@@ -41,14 +41,17 @@ static Layout layout_of(int64_t T, int64_t K) {
   off += align_up((size_t)T * (size_t)K * 2, 256);
   L.xo = off;
   off += align_up((size_t)T * (size_t)L.kpad * 2, 256);
+  L.opad = ((K / 16 > 0 ? K / 16 : 1) + 63) / 64 * 64;  // holds any sparse outlier set
+  L.w16o = off;
+  off += align_up((size_t)N * (size_t)L.opad * 2, 256);
   L.total = off;
   return L;
 }
 
 static constexpr size_t kWsSlack = 256;  // the carved layout starts at the next 256-byte boundary
 
-static Workspace carve(void *ws, int64_t T, int64_t K) {
-  const Layout L = layout_of(T, K);
+static Workspace carve(void *ws, int64_t T, int64_t N, int64_t K) {
+  const Layout L = layout_of(T, N, K);
   char *base = reinterpret_cast<char *>(align_up((uintptr_t)ws, 256));
   Workspace w;
   w.status = reinterpret_cast<int32_t *>(base + L.status);
@@ -60,6 +63,8 @@ static Workspace carve(void *ws, int64_t T, int64_t K) {
   w.xcodes = base + L.xcodes;
   w.xo = reinterpret_cast<__half *>(base + L.xo);
   w.kpad = L.kpad;
+  w.w16o = reinterpret_cast<__half *>(base + L.w16o);
+  w.opad = L.opad;
   return w;
 }
 
@@ -162,7 +167,7 @@ static bnb_status_t linear_impl(const void *X, int64_t T, int64_t K, const int8_
   bnb_status_t st = check_device(&dev);
   if (st != BNB_OK) return st;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_v);
-  const Workspace ws = carve(workspace, T, K);
+  const Workspace ws = carve(workspace, T, N, K);
   const int path = choose_path(T, N, K, dev);
   const uint32_t thr = threshold_bits(tau);
   cudaError_t e;
@@ -185,6 +190,10 @@ static bnb_status_t linear_impl(const void *X, int64_t T, int64_t K, const int8_
       e = launch_act_pass(X, T, K, thr, ws, /*code_mode=*/path == 2 ? 1 : 0, /*with_xo=*/true,
                           dbg_xq, device_sms(dev), stream);
       if (e != cudaSuccess) return BNB_ERR_CUDA;
+      if (path == 2) {  // W16 at a sparse outlier set, compacted once per call
+        e = launch_gather_outlier_weights(W16, N, K, ws, device_sms(dev), stream);
+        if (e != cudaSuccess) return BNB_ERR_CUDA;
+      }
     }
     if (path == 2)
       e = launch_gemm_tc(T, K, Wq, Wscale, W16, N, Y, ws, dbg_acc, device_sms(dev), stream);
@@ -208,9 +217,8 @@ using namespace bnb;
 extern "C" {
 
 size_t bnb_int8_linear_workspace_bytes(int64_t T, int64_t N, int64_t K) {
-  (void)N;
   if (T <= 0 || N <= 0 || K <= 0 || T > BNB_MAX_T || N > BNB_MAX_N || K > BNB_MAX_K) return 0;
-  return layout_of(T, K).total + kWsSlack;
+  return layout_of(T, N, K).total + kWsSlack;
 }
 
 bnb_status_t bnb_int8_quantize_weight(const void *W16, int64_t N, int64_t K, int8_t *Wq,

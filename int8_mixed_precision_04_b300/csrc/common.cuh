@@ -22,6 +22,16 @@ constexpr int kB300Sms = 148;
 // each of 16 warps x 32 lanes one 8-column vector.
 constexpr int64_t kDecodeMaxK = 4096;
 
+// The fp16 outlier block of the GEMM path is dense (X masked to the outlier
+// columns over all K, multiplied as one dense fp16 GEMM against W16 tiles)
+// when more than 1/16 of the columns are outliers; otherwise it is
+// compacted, against W16's outlier columns compacted once per call.  A
+// compacted column costs one scattered W16 sector per output channel, a
+// dense one a fraction of a tensor-core stage: they break even near K/8.
+__host__ __device__ __forceinline__ bool outlier_block_dense(int64_t nO, int64_t K) {
+  return nO * 16 > K;
+}
+
 // Workspace layout, carved identically by the host for every call.
 struct Workspace {
   int32_t *status;     // [4]  device status word + spare
@@ -31,8 +41,10 @@ struct Workspace {
   float *sx;           // [T] row scales
   float *sxd;          // [T] row scales / 127 (GEMM epilogue)
   void *xcodes;        // [T x K] codes: int8 (decode) or fp16 integers (GEMM)
-  __half *xo;          // [T x kpad] compacted fp16 outlier block
+  __half *xo;          // [T x kpad] fp16 outlier block (compacted, or masked X when dense)
   int64_t kpad;        // pitch of xo in elements (K rounded up to 64)
+  __half *w16o;        // [N x opad] W16 at the outlier columns (compacted; GEMM path, sparse)
+  int64_t opad;        // pitch of w16o in elements: floor(K / 16) rounded up to 64
 };
 
 __device__ __forceinline__ uint32_t lane_id() {

@@ -26,9 +26,12 @@
 //              K-major layout the MMA reads.
 //   B operand  activation codes, already fp16 integers in HBM (written by the
 //              activation pass), loaded by TMA with the 128-byte swizzle.
-// After the int8 chunks, the outlier product runs as one more fp32 chunk:
-// A = W16 columns O gathered by the converter warps, B = the compacted fp16
-// outlier block XO (TMA).  The epilogue combines both and writes Y once.
+// After the int8 chunks, the outlier product runs as one more fp32 chunk,
+// both operands by TMA: A = W16 at the outlier columns (compacted once per
+// call by a small gather kernel) and B = the compacted fp16 outlier block
+// XO; or, when outliers are dense (more than K/16), a dense fp16 product over
+// all K columns with A = W16 tiles and B = X masked to the outlier columns.
+// The epilogue combines both and writes Y once.
 //
 // Warp roles (20 warps): 0 TMA producer, 1 MMA issuer and tensor-memory
 // owner, 2-3 converters (two weight rows per thread), 4-19 epilogue (four
@@ -169,18 +172,18 @@ __device__ __forceinline__ void widen16(const uint4 &v, uint4 &g0, uint4 &g1) {
   s8x4_to_f16x4(v.w, g1.z, g1.w);
 }
 
-// Converter warps: widen the int8 weight tile of each stage into the fp16
-// A operand (or, in the outlier stages, gather the W16 outlier columns).
+// Converter warps: widen the int8 weight tile of each int8 stage into the
+// fp16 A operand.  In the outlier stages TMA has put the fp16 A tile there
+// already (W16, or its compacted outlier columns); the converters only pass
+// the stage on to the MMA.
 // Thread ct owns weight rows ct, ct + 32 * kConvWarps, ...
 __device__ __forceinline__ void converter_role(uint8_t *smem, TcSmem &sm, const TcArgs &p,
-                                               int nO, int s_int, int nst, int ntiles) {
+                                               int s_int, int nst, int ntiles) {
   const int ct = threadIdx.x - kConvWarp0 * 32;  // 0 .. 32 * kConvWarps - 1
   const int lane = threadIdx.x & 31;
-  const int64_t K = p.K, N = p.N;
   uint32_t it = 0;
   bool ok = true;
   for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
-    const int64_t nb = (int64_t)(tile / p.t_tiles) * kBM;
     for (int s = 0; s < nst; ++s, ++it) {
       const int st = it % kStages;
       if (!warp_wait(&sm.full[st], (it / kStages) & 1u, sm, p.status)) {
@@ -203,35 +206,6 @@ __device__ __forceinline__ void converter_role(uint8_t *smem, TcSmem &sm, const 
             *reinterpret_cast<uint4 *>(wh + 16 * ((2 * q + 1) ^ (r & 7))) = g1;
           }
         }
-      } else {
-        // outlier columns O[jb .. jb+63] of W16 rows (zero past |O| or N)
-        const int jb = (s - s_int) * kBK;
-        for (int h = 0; h < kConvRows; ++h) {
-          const int r = ct + kConvWarps * 32 * h;
-          const int64_t n = nb + r;
-          const unsigned short *wrow = p.W16 + n * K;
-          uint8_t *wh = stage_wh(smem, st) + r * 128;
-          for (int gi = 0; gi < 8; ++gi) {
-            const int j0 = jb + 8 * gi;
-            uint4 v = make_uint4(0, 0, 0, 0);
-            if (n < N && j0 < nO) {
-              const int32_t k0 = __ldcg(p.O + j0);
-              const bool full8 = j0 + 7 < nO;
-              const int32_t k7 = full8 ? __ldcg(p.O + j0 + 7) : -1;
-              if (full8 && k7 - k0 == 7 && (k0 & 7) == 0) {
-                v = __ldg(reinterpret_cast<const uint4 *>(wrow + k0));  // 8 adjacent columns
-              } else {
-                uint32_t hv[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e)
-                  hv[e] = (j0 + e < nO) ? (uint32_t)__ldg(wrow + __ldcg(p.O + j0 + e)) : 0u;
-                v = make_uint4(hv[0] | (hv[1] << 16), hv[2] | (hv[3] << 16),
-                               hv[4] | (hv[5] << 16), hv[6] | (hv[7] << 16));
-              }
-            }
-            *reinterpret_cast<uint4 *>(wh + 16 * (gi ^ (r & 7))) = v;
-          }
-        }
       }
       fence_proxy_async_smem();
       __syncwarp();
@@ -242,7 +216,8 @@ __device__ __forceinline__ void converter_role(uint8_t *smem, TcSmem &sm, const 
 
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
-                   const __grid_constant__ CUtensorMap tm_xo, const TcArgs p) {
+                   const __grid_constant__ CUtensorMap tm_xo, const __grid_constant__ CUtensorMap tm_w16,
+                   const __grid_constant__ CUtensorMap tm_w16o, const TcArgs p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   __shared__ TcSmem sm;
@@ -267,6 +242,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tm_x);
     tma_prefetch_desc(&tm_w);
     tma_prefetch_desc(&tm_xo);
+    tma_prefetch_desc(&tm_w16);
+    tma_prefetch_desc(&tm_w16o);
   }
   if (warp == 1) {
     tmem_alloc(&sm.tmem_base, kTmemCols);
@@ -281,7 +258,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   pdl_wait();
   const int nO = (int)__ldcg(p.nO);
   const int s_int = p.s_int;
-  const int s_out = (nO + kBK - 1) / kBK;
+  // outlier stages: the compacted block against gathered W16 columns, or,
+  // with dense outliers, X masked to them against every W16 column
+  const bool dense = outlier_block_dense(nO, p.K);
+  const int s_out = dense ? s_int : (nO + kBK - 1) / kBK;
   const int nst = s_int + s_out;
   const int ntiles = p.t_tiles * p.n_tiles;
 
@@ -306,9 +286,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_expect_tx(&sm.full[st], kXBytes + kWqBytes);
             tma_load_2d(stage_x(smem, st), &tm_x, s * kBK, t0, &sm.full[st]);
             tma_load_2d(stage_wq(smem, st), &tm_w, s * kBK, n0, &sm.full[st]);
-          } else {
-            mbar_expect_tx(&sm.full[st], kXBytes);
+          } else {  // outlier stage: fp16 A tile straight into the A operand slot
+            mbar_expect_tx(&sm.full[st], kXBytes + kWhBytes);
             tma_load_2d(stage_x(smem, st), &tm_xo, (s - s_int) * kBK, t0, &sm.full[st]);
+            tma_load_2d(stage_wh(smem, st), dense ? &tm_w16 : &tm_w16o, (s - s_int) * kBK, n0,
+                        &sm.full[st]);
           }
         }
       }
@@ -362,10 +344,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       tmem_dealloc(tmem, kTmemCols);
     }
-    if (kConvWarps == 2 && warp >= kConvWarp0) converter_role(smem, sm, p, nO, s_int, nst, ntiles);
+    if (kConvWarps == 2 && warp >= kConvWarp0) converter_role(smem, sm, p, s_int, nst, ntiles);
   } else if (kConvWarps == 4 && warp < kEpiWarp0) {
     regs_dec<kRegsConv>();
-    converter_role(smem, sm, p, nO, s_int, nst, ntiles);
+    converter_role(smem, sm, p, s_int, nst, ntiles);
   } else {
     regs_inc<kRegsEpi>();
     // ---------------- epilogue ----------------
@@ -511,13 +493,18 @@ cudaError_t launch_gemm_tc(int64_t T, int64_t K, const int8_t *Wq, const float *
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  CUtensorMap tm_x, tm_w, tm_xo;
+  CUtensorMap tm_x, tm_w, tm_xo, tm_w16, tm_w16o;
   if (!encode_2d(&tm_x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, ws.xcodes, (uint64_t)K, (uint64_t)T,
                  (uint64_t)K * 2, kBK, kBN, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !encode_2d(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, Wq, (uint64_t)K, (uint64_t)N, (uint64_t)K,
                  kBK, kBM, CU_TENSOR_MAP_SWIZZLE_64B) ||
-      !encode_2d(&tm_xo, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, ws.xo, (uint64_t)ws.kpad, (uint64_t)T,
-                 (uint64_t)ws.kpad * 2, kBK, kBN, CU_TENSOR_MAP_SWIZZLE_128B))
+      // the outlier block's inner extent is K (columns past K read as zeros)
+      !encode_2d(&tm_xo, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, ws.xo, (uint64_t)K, (uint64_t)T,
+                 (uint64_t)ws.kpad * 2, kBK, kBN, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_2d(&tm_w16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, W16, (uint64_t)K, (uint64_t)N,
+                 (uint64_t)K * 2, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_2d(&tm_w16o, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, ws.w16o, (uint64_t)ws.opad,
+                 (uint64_t)N, (uint64_t)ws.opad * 2, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   TcArgs a;
   a.T = T;
@@ -547,7 +534,7 @@ cudaError_t launch_gemm_tc(int64_t T, int64_t K, const int8_t *Wq, const float *
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   ProfScope ps(kKidGemmTc, stream);
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_tc_kernel, tm_x, tm_w, tm_xo, a);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_tc_kernel, tm_x, tm_w, tm_xo, tm_w16, tm_w16o, a);
   note_launch();
   return e;
 }

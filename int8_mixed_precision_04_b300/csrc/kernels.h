@@ -20,6 +20,7 @@ enum KernelId {
   kKidGemmMma,
   kKidGemmTc,
   kKidQuantWeight,
+  kKidGatherW16,
   kKernelCount
 };
 
@@ -50,6 +51,12 @@ cudaError_t launch_quantize_weight(const void *W16, int64_t N, int64_t K, int8_t
 cudaError_t launch_act_pass(const void *X, int64_t T, int64_t K, uint32_t thr_bits,
                             const Workspace &ws, int code_mode, bool with_xo,
                             int8_t *dbg_xq, int num_sms, cudaStream_t stream);
+
+// W16[n, O[j]] for a sparse outlier set (outlier_block_dense false) into the
+// workspace's compacted block w16o [N x opad], zero past |O|; nothing when
+// the outlier set is dense.
+cudaError_t launch_gather_outlier_weights(const void *W16, int64_t N, int64_t K,
+                                          const Workspace &ws, int num_sms, cudaStream_t stream);
 
 // The whole layer for T <= 16, K <= kDecodeMaxK, N <= decode_max_n(dev) in
 // one kernel (activation pass fused into the GEMV and shared by clusters of
