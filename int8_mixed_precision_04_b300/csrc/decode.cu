@@ -369,7 +369,6 @@ __global__ void __launch_bounds__(kDecThreads, 1) dec_fused_kernel(const DecArgs
   if (k1 > k0 && mbar_wait_bounded(&sm.wbar, 0, p.status)) {
     float f[4][4] = {};
     int nb = 0;
-#pragma unroll 4
     for (int64_t kb = k0; kb < k1; kb += 64) {
       const uint32_t lv = (kb + 16 * q < k1) ? 0xffffffffu : 0u;  // columns past K feed zeros
       uint32_t xa[8], xb[8];
