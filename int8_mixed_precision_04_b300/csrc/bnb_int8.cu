@@ -136,10 +136,10 @@ static bool force_mma() {
   return v;
 }
 
-// 1: decode (T <= 16, K <= kDecodeMaxK, at most 128 output channels per
-// resident cluster); 2: tcgen05 GEMM; 3: legacy mma GEMM.
+// 1: decode (T <= 16, K <= kDecodeMaxK, N within what the resident decode
+// CTAs hold in one wave); 2: tcgen05 GEMM; 3: legacy mma GEMM.
 static int choose_path(int64_t T, int64_t N, int64_t K, int dev) {
-  if (T <= 16 && K <= kDecodeMaxK && N <= decode_max_n(dev)) return 1;
+  if (T <= 16 && K <= kDecodeMaxK && N <= decode_max_n(dev, K)) return 1;
   return force_mma() ? 3 : 2;
 }
 

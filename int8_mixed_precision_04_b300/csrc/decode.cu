@@ -1,39 +1,39 @@
 // The whole layer for decode-sized T (T <= 16) in one kernel per call.
 //
-// dec_fused: one CTA per slice of at most 32 output channels (one CTA per
-// SM), in thread-block clusters of kDecCluster CTAs.  At launch the producer
-// warp puts the CTA's whole int8 weight slice in flight on the copy engine
-// (one bulk copy per row), before waiting on the previous kernel of the
-// stream (the weight does not depend on X).  While the weight streams in,
-// the cluster runs the
-// activation pass cooperatively, so that no second kernel and no
+// dec_fused: one CTA per slice of at most 40 output channels (one CTA per
+// SM), in thread-block clusters of kC CTAs (8, 16 or 4: the first whose
+// resident clusters hold every slice at once).  Right behind its X loads the
+// producer warp puts the CTA's whole int8 weight slice in flight on the copy
+// engine (one bulk copy per row).  While the weight streams in, the cluster
+// runs the activation pass cooperatively, so that no second kernel and no
 // inter-kernel dependency sits on the path, and no CTA repeats the others'
 // work:
-//   - CTA rank c owns a quarter of the columns; each consumer lane one
-//     8-column vector of four rows.  A column is an outlier feature dimension
-//     when |x| >= tau in some row ("Hugging Face Quantization with
-//     bitsandbytes: 4-bit & 8-bit Models Explained", sections 2 and 3): the
-//     four row-quads' flags are OR-ed through shared memory.  Row maxima over
-//     non-outlier columns are reduced per warp, per CTA, and across the
-//     cluster through distributed shared memory, as are the outlier counts;
-//   - each CTA then writes the vector-wise int8 codes rint(fl32(127 x) / sx)
-//     of its columns, its part of the ascending outlier list and the X values
-//     of the first outlier columns, into the shared memory of every CTA of
-//     the cluster.
-// CTA 0 also writes sx, O and |O| to the workspace (and the codes when
-// asked), for the debug entry point.
-// Then each consumer warp owns one K-range for all four 8-row groups: it
-// widens the int8 codes of X and W to fp16 integers in registers and runs
-// 16x8x16 fp16 MMAs with fp32 accumulation, converted to int32 at least
-// every 1024 columns (127^2 * 1024 < 2^24, so every fp32 partial sum is an
-// exact integer).  The producer warp adds up the first outlier columns of W16
-// times X for the slice while the MMAs run; the consumers split any further
-// ones.  Epilogue: the int32 partials are summed, scaled by (sx/127)(sw/127),
-// the 16-bit outlier product is added ("converted back to 16-bit at the end",
+//   - CTA rank c owns 1/kC of the columns; each consumer thread one 8-column
+//     vector of 16/kC rows.  A column is an outlier feature dimension when
+//     |x| >= tau in some row ("Hugging Face Quantization with bitsandbytes:
+//     4-bit & 8-bit Models Explained", sections 2 and 3): the row groups'
+//     flags are OR-ed through shared memory.  Each CTA's row maxima over its
+//     non-outlier columns and its outlier count go to every CTA of the
+//     cluster;
+//   - each CTA then sends its columns' vector-wise int8 codes
+//     rint(fl32(127 x) / sx), its part of the outlier column mask and the X
+//     values of the first outlier columns to every CTA of the cluster.
+// Every exchange is a remote store into the receiving CTA's shared memory
+// counted on an mbarrier there (no cluster-wide barrier: its release would
+// wait for the weight copies in flight).  CTA 0 also writes sx, O and |O| to
+// the workspace (and the codes when asked), for the debug entry point.
+// Then each consumer warp owns one K-range for all of the slice's 8-channel
+// groups: it widens the int8 codes of X and W to fp16 integers in registers
+// and runs 16x8x16 fp16 MMAs with fp32 accumulation, converted to int32 at
+// least every 1024 columns (127^2 * 1024 < 2^24, so every fp32 partial sum is
+// an exact integer).  The producer warp lists the outlier columns and adds up
+// the first ones of W16 times X for the slice while the MMAs run; the
+// consumers split any further ones.  Epilogue (one output per consumer
+// thread): the int32 partials are summed, scaled by (sx/127)(sw/127), the
+// 16-bit outlier product is added ("converted back to 16-bit at the end",
 // same page, section 2) and Y is written once.
-#include <cooperative_groups.h>
-
 #include <atomic>
+#include <cstdlib>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -43,15 +43,27 @@
 namespace bnb {
 
 constexpr int kDecWarps = 16;                      // consumer warps (one K-range each)
-constexpr int kDecThreads = (kDecWarps + 1) * 32;  // + one producer warp
-constexpr int kDecMaxRows = 32;                    // output channels per CTA (4 groups of 8)
+constexpr int kDecConsumers = kDecWarps * 32;      // consumer threads
+constexpr int kDecThreads = kDecConsumers + 32;    // + one producer warp
+constexpr int kDecGroups = 5;                      // 8-channel MMA groups of a slice, at most
+constexpr int kDecMaxRows = kDecGroups * 8;        // output channels per CTA, at most
 constexpr int kDecChunkK = 1024;                   // fp32 accumulation is drained this often
 constexpr int kDecOutSmall = 64;                   // outlier columns the producer warp sums
-constexpr int kDecCluster = 4;                     // CTAs sharing one activation pass
-// act pass: consumer lane L handles vector (L & 127) of its CTA's columns and
-// rows 4 * (L >> 7) .. +3, so a CTA covers at most 128 vectors
-static_assert(kDecodeMaxK <= kDecCluster * 128 * 8, "act-pass lanes cover every column");
-static_assert(kDecWarps == 16, "four row-quads of four warps");
+constexpr int kDecRedStride = kDecGroups * 4 + 1;  // words per lane in the reduction (odd)
+constexpr int kDecMaskWords = (int)(kDecodeMaxK / 32);
+
+// Activation-pass geometry of a cluster of kC CTAs: a CTA covers at most
+// kVpc 8-column vectors; consumer thread i takes vector i % kVpc of rows
+// i / kVpc + kC * j (j < kRpt), so warp w holds vector block w % kWpg of row
+// group w / kWpg.
+template <int kC>
+struct DecAct {
+  static constexpr int kVpc = kDecConsumers / kC;  // 32, 64, 128 for kC 16, 8, 4
+  static constexpr int kRpt = 16 / kC;             // rows per thread
+  static constexpr int kWpg = kVpc / 32;           // warps per row group
+  static_assert(kVpc % 32 == 0 && kRpt >= 1 && kRpt <= 4 && kWpg <= 4, "act-pass geometry");
+  static_assert(kDecodeMaxK <= kC * kVpc * 8, "act-pass threads cover every column");
+};
 
 __host__ __device__ constexpr int64_t dec_pitch(int64_t K) { return K + 64; }  // bytes per row
 // K columns of MMA warp w: [w * range, min(K, (w + 1) * range)), range a multiple of 64
@@ -59,28 +71,33 @@ __host__ __device__ constexpr int64_t dec_range(int64_t K) {
   return ((K + kDecWarps - 1) / kDecWarps + 63) / 64 * 64;
 }
 // The weight region is reused for the cross-warp reduction after the main loop.
-constexpr int64_t kDecRedBytes = (int64_t)kDecWarps * 32 * 16 * 4;
-__host__ __device__ constexpr int64_t dec_wregion(int64_t K) {
-  return kDecMaxRows * dec_pitch(K) > kDecRedBytes ? kDecMaxRows * dec_pitch(K) : kDecRedBytes;
+constexpr int64_t kDecRedBytes = (int64_t)kDecWarps * 32 * kDecRedStride * 4;
+__host__ __device__ constexpr int64_t dec_wregion(int64_t K, int64_t rows) {
+  return rows * dec_pitch(K) > kDecRedBytes ? rows * dec_pitch(K) : kDecRedBytes;
 }
 __host__ __device__ constexpr int64_t dec_ocap(int64_t K) { return (K + 7) / 8 * 8; }
 
-// dynamic: weight rows, code rows, outlier list (uint16)
-size_t decode_smem_bytes(int64_t K) {
-  return (size_t)(dec_wregion(K) + 16 * dec_pitch(K) + 2 * dec_ocap(K));
+// dynamic: weight rows, code rows, outlier column list (uint16).  The MMAs
+// also read the (unused) rows past `rows` of a partial 8-channel group: at
+// most 7 rows, which land in the code rows.
+size_t decode_smem_bytes(int64_t K, int64_t rows) {
+  return (size_t)(dec_wregion(K, rows) + 16 * dec_pitch(K) + 2 * dec_ocap(K));
 }
 
-// small static buffers of one CTA (partly read by the other CTAs of its cluster)
+// small static buffers of one CTA (partly written by the other CTAs of its cluster)
 struct DecSmall {
   uint64_t wbar;            // the CTA's weight slice has landed
   uint64_t obar;            // producer warp's outlier sums are in osm
-  float osm[16 * 32];       // [t][row] outlier sums of the first kDecOutSmall columns
+  uint64_t pbar;            // every CTA's row maxima and outlier count are in pubs
+  uint64_t cbar;            // every CTA's codes, mask words and outlier X values are here
+  float osm[16 * kDecMaxRows];  // [t][row] outlier sums of the first kDecOutSmall columns
   float sxs[16];            // row scales sx
-  uint32_t part[kDecWarps * 4];  // [warp][row of its quad] partial row maxima (fp16 bits)
-  uint32_t pub[20];         // published to the cluster: [t] CTA row maxima, [16] outlier count
-  uint32_t wcnt[4];         // outlier count of each quad-0 warp
-  uint8_t fpart[4 * 128];   // [quad][vector] outlier flags of four rows
-  unsigned short xo[16 * kDecOutSmall];  // [t][j] X at the first outlier columns (fp16)
+  uint32_t part[kDecWarps * 4];  // [warp][j] partial row maxima (fp16 bits)
+  uint32_t pubs[16][17];    // [CTA][t] its row maxima (fp16 bits), [CTA][16] its outlier count
+  uint32_t wcnt[4];         // outlier count of each vector block (row group 0's warps)
+  uint32_t mask[kDecMaskWords];  // outlier columns, bit b of word w = column 32 w + b
+  uint8_t fpart[kDecConsumers];  // [row group][vector] outlier flags
+  uint32_t xo[16 * kDecOutSmall];  // [t][j] X at the first outlier columns (fp16 bits)
 };
 
 struct DecArgs {
@@ -89,7 +106,8 @@ struct DecArgs {
   int T;
   int64_t K, N;
   uint32_t thr;                // smallest fp16 magnitude bits >= tau
-  int64_t rows_per_cta;
+  int64_t rows_per_cta;        // <= kDecMaxRows
+  int64_t wregion;             // bytes of the weight region, dec_wregion(K, rows_per_cta)
   const int8_t *Wq;
   const float *sw;
   const unsigned short *W16;
@@ -110,49 +128,99 @@ __device__ __forceinline__ void widen16(const uint4 &v, uint32_t (&h)[8]) {
   s8x4_to_f16x4(v.w, h[6], h[7]);
 }
 
-// Fragment convention (see mma_frag.cuh): lane (g = lane/4, q = lane%4) holds
-// columns [kb + 16q, kb + 16q + 16) of X rows g and g+8 and of weight row g
-// of a group; word pair (2mm, 2mm+1) of each widened vector feeds MMA mm.
+// One consumer warp's K-range [k0, k1) for the slice's first `ng` 8-channel
+// groups, into exact int32 accumulators.  Fragment convention (see
+// mma_frag.cuh): lane (g = lane/4, q = lane%4) holds columns
+// [kb + 16q, kb + 16q + 16) of X rows g and g+8 and of weight row g of a
+// group; word pair (2mm, 2mm+1) of each widened vector feeds MMA mm.
+// kRagged: the range ends inside a 64-column block, whose columns past k1
+// (never written in shared memory) are fed as zeros; otherwise no lane needs
+// a mask.
+template <bool kRagged>
+__device__ __forceinline__ void dec_mma_range(const uint8_t *xs, const uint8_t *ws,
+                                              int64_t pitch, int g, int q, int64_t k0,
+                                              int64_t k1, int ng,
+                                              int (&acc)[kDecGroups][4]) {
+  float f[kDecGroups][4] = {};
+  int nb = 0;
+  for (int64_t kb = k0; kb < k1; kb += 64) {
+    const uint32_t lv = (!kRagged || kb + 16 * q < k1) ? 0xffffffffu : 0u;
+    uint32_t xa[8], xb[8];
+    widen16(*reinterpret_cast<const uint4 *>(xs + g * pitch + kb + 16 * q), xa);
+    widen16(*reinterpret_cast<const uint4 *>(xs + (g + 8) * pitch + kb + 16 * q), xb);
+#pragma unroll
+    for (int gi = 0; gi < kDecGroups; gi++) {
+      if (gi < ng) {
+        uint32_t h[8];
+        widen16(*reinterpret_cast<const uint4 *>(ws + (gi * 8 + g) * pitch + kb + 16 * q), h);
+#pragma unroll
+        for (int mm = 0; mm < 4; mm++)
+          mma_f16_16x8x16(f[gi], xa[2 * mm] & lv, xb[2 * mm] & lv, xa[2 * mm + 1] & lv,
+                          xb[2 * mm + 1] & lv, h[2 * mm] & lv, h[2 * mm + 1] & lv);
+      }
+    }
+    if (++nb == kDecChunkK / 64 || kb + 64 >= k1) {  // exact drain into int32
+      nb = 0;
+#pragma unroll
+      for (int gi = 0; gi < kDecGroups; gi++)
+#pragma unroll
+        for (int j = 0; j < 4; j++) {
+          acc[gi][j] += __float2int_rn(f[gi][j]);
+          f[gi][j] = 0.f;
+        }
+    }
+  }
+}
+
+template <int kC>
 __global__ void __launch_bounds__(kDecThreads, 1) dec_fused_kernel(const DecArgs p) {
+  using G = DecAct<kC>;
   extern __shared__ __align__(128) uint8_t smem[];
   const int64_t K = p.K, pitch = dec_pitch(K), range = dec_range(K);
-  uint8_t *ws = smem;                                          // [32][pitch] weight codes
-  uint8_t *xs = smem + dec_wregion(K);                         // [16][pitch] activation codes
+  uint8_t *ws = smem;                                          // [rows][pitch] weight codes
+  uint8_t *xs = smem + p.wregion;                              // [16][pitch] activation codes
   uint16_t *ocols = reinterpret_cast<uint16_t *>(xs + 16 * pitch);  // outlier columns
   __shared__ DecSmall sm;
   float *osm = sm.osm, *sxs = sm.sxs;
   uint64_t *obar = &sm.obar;
-  uint32_t *red = reinterpret_cast<uint32_t *>(smem);  // [16 warps][32][16], after the main loop
+  uint32_t *red = reinterpret_cast<uint32_t *>(smem);  // [16 warps][32][21], after the main loop
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int T = p.T;
   const int64_t n0 = (int64_t)blockIdx.x * p.rows_per_cta;
-  const int64_t rows = min(p.N, n0 + p.rows_per_cta) - n0;  // <= 32; <= 0 for trailing CTAs
+  const int64_t rows = min(p.N, n0 + p.rows_per_cta) - n0;  // <= 40; <= 0 for trailing CTAs
 
   if (warp == kDecWarps && lane == 0) {
     mbar_init(&sm.wbar, 1);
     mbar_init(obar, 32);
+    mbar_init(&sm.pbar, 1);
+    mbar_init(&sm.cbar, 1);
     mbar_init_fence();
   }
   __syncthreads();
+  // The cluster's mbarriers are initialised once every CTA has arrived here;
+  // each thread waits for that just before its first remote store.  No
+  // thread publishes anything through this phase, so the arrival is relaxed
+  // (a release arrival would also wait for the CTA's copies in flight).
+  cluster_arrive_relaxed();
   // the next kernel on the stream may launch now; it waits for our completion
   pdl_trigger();
   // X may be the output of the previous kernel on the stream
   pdl_wait();
+  if (blockIdx.x == 0 && threadIdx.x == 0) *p.status = kDevOk;  // a wait that gives up overwrites it
 
-  namespace cg = cooperative_groups;
-  cg::cluster_group cluster = cg::this_cluster();
-  const int crank = (int)cluster.block_rank();
+  uint32_t crank;
+  asm("mov.u32 %0, %%cluster_ctarank;" : "=r"(crank));
 
-  // ---- activation pass 1: outlier columns and partial row maxima ----
   const int64_t vecs = K / 8;
-  const int64_t vpc = (vecs + kDecCluster - 1) / kDecCluster;  // vectors per CTA (<= 128)
-  const int quad = (threadIdx.x >> 7) & 3;                      // rows 4 quad .. 4 quad + 3
-  const int64_t vl = threadIdx.x & 127;
-  const int64_t v = crank * vpc + vl;                           // this lane's 8-column vector
+  // vectors per CTA (<= kVpc), a multiple of 4 so that each outlier-mask word
+  // (four vectors) belongs to one CTA
+  const int64_t vpc = ((vecs + kC - 1) / kC + 3) / 4 * 4;
+  const int64_t words = (vecs + 3) / 4;  // outlier-mask words
+  const int grp = (threadIdx.x & (kDecConsumers - 1)) / G::kVpc;  // row group (consumers)
+  const int64_t vl = threadIdx.x % G::kVpc;
+  const int64_t v = crank * vpc + vl;          // this thread's 8-column vector
   const bool live = warp < kDecWarps && vl < vpc && v < vecs;
-  uint4 x[4];
-  uint32_t flags = 0;
   if (warp == kDecWarps) {
     // The whole weight slice in flight at once, on the copy engine: one bulk
     // copy per weight row, so that every warp is free for the activation
@@ -161,22 +229,26 @@ __global__ void __launch_bounds__(kDecThreads, 1) dec_fused_kernel(const DecArgs
     // weights.  Weight rows past `rows`, code rows past T and the pads past K
     // are never written: the MMAs mask columns past K, and accumulator rows
     // >= T or columns >= rows are never stored.
-    asm volatile("bar.sync 2, %0;" ::"r"(kDecThreads) : "memory");  // X loads issued
+    named_bar_sync(2, kDecThreads);  // X loads issued
     if (lane == 0) mbar_expect_tx(&sm.wbar, (uint32_t)(rows > 0 ? rows * K : 0));
     __syncwarp();
     for (int64_t r = lane; r < rows; r += 32)
       bulk_g2s(ws + r * pitch, p.Wq + (n0 + r) * K, (uint32_t)K, &sm.wbar);
+    cluster_wait();
   } else {
+    // ---- activation pass 1: outlier columns and partial row maxima ----
+    uint4 x[G::kRpt];
+    uint32_t flags = 0;
 #pragma unroll
-    for (int r = 0; r < 4; r++) {  // all loads in flight before any is used
-      const int t = 4 * quad + r;
-      x[r] = (t < T && live) ? __ldg(p.X + t * vecs + v) : make_uint4(0, 0, 0, 0);
+    for (int j = 0; j < G::kRpt; j++) {  // all loads in flight before any is used
+      const int t = grp + kC * j;
+      x[j] = (t < T && live) ? __ldg(p.X + t * vecs + v) : make_uint4(0, 0, 0, 0);
     }
-    asm volatile("bar.arrive 2, %0;" ::"r"(kDecThreads) : "memory");
+    named_bar_arrive(2, kDecThreads);
 #pragma unroll
-    for (int r = 0; r < 4; r++) {
-      if (4 * quad + r < T) {  // padding rows must not flag columns (tau = 0 flags a zero)
-        const uint32_t w[4] = {x[r].x, x[r].y, x[r].z, x[r].w};
+    for (int j = 0; j < G::kRpt; j++) {
+      if (grp + kC * j < T) {  // padding rows must not flag columns (tau = 0 flags a zero)
+        const uint32_t w[4] = {x[j].x, x[j].y, x[j].z, x[j].w};
 #pragma unroll
         for (int i = 0; i < 4; i++) {
           flags |= (uint32_t)(abs_bits_lo(w[i]) >= p.thr) << (2 * i);
@@ -185,17 +257,16 @@ __global__ void __launch_bounds__(kDecThreads, 1) dec_fused_kernel(const DecArgs
       }
     }
     if (!live) flags = 0;
-    sm.fpart[quad * 128 + vl] = (uint8_t)flags;
-  }
-  __syncthreads();
-  if (warp < kDecWarps) {
+    sm.fpart[grp * G::kVpc + vl] = (uint8_t)flags;
+    named_bar_sync(1, kDecConsumers);
     // a column is an outlier if any of the call's rows flags it
-    flags = live ? (uint32_t)(sm.fpart[vl] | sm.fpart[128 + vl] | sm.fpart[256 + vl] |
-                              sm.fpart[384 + vl])
-                 : 0u;
+    flags = 0;
+    if (live)
 #pragma unroll
-    for (int r = 0; r < 4; r++) {
-      const uint32_t w[4] = {x[r].x, x[r].y, x[r].z, x[r].w};
+      for (int r = 0; r < kC; r++) flags |= sm.fpart[r * G::kVpc + vl];
+#pragma unroll
+    for (int j = 0; j < G::kRpt; j++) {
+      const uint32_t w[4] = {x[j].x, x[j].y, x[j].z, x[j].w};
       uint32_t m = 0;
 #pragma unroll
       for (int i = 0; i < 4; i++) {
@@ -204,265 +275,297 @@ __global__ void __launch_bounds__(kDecThreads, 1) dec_fused_kernel(const DecArgs
       }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
-      if (lane == 0) sm.part[warp * 4 + r] = m;
+      if (lane == 0) sm.part[warp * 4 + j] = m;
     }
-    if (quad == 0) {  // warps 0..3 hold each column of this CTA once
+    if (grp == 0) {  // row group 0 holds each column of this CTA once
       uint32_t c = __popc(flags);
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
       if (lane == 0) sm.wcnt[warp] = c;
     }
-  }
-  __syncthreads();
-  if (threadIdx.x < 16) {  // this CTA's maximum of row t over its non-outlier columns
-    const int t = threadIdx.x, q = t >> 2, r = t & 3;
-    uint32_t m = 0;
-    for (int w = 4 * q; w < 4 * q + 4; w++) m = max(m, sm.part[w * 4 + r]);
-    sm.pub[t] = m;
-  } else if (threadIdx.x == 16) {
-    sm.pub[16] = sm.wcnt[0] + sm.wcnt[1] + sm.wcnt[2] + sm.wcnt[3];
-  }
-  cluster.sync();  // every CTA's row maxima and outlier count are published
-
-  // ---- activation pass 2: row scales, outlier list, int8 codes (cluster-wide) ----
-  // all remote reads in flight at once: row maxima (lane & 15) and counts
-  uint32_t rmax[kDecCluster], rcnt[kDecCluster];
+    named_bar_sync(1, kDecConsumers);
+    cluster_wait();  // every CTA's mbarriers are initialised
+    if (threadIdx.x < 17) {
+      // this CTA's maximum of row t over its non-outlier columns (t < 16) or
+      // its outlier count (16), stored into every CTA of the cluster
+      uint32_t val = 0;
+      if (threadIdx.x < 16) {
+        const int t = threadIdx.x, rg = t % kC, j = t / kC;
 #pragma unroll
-  for (int c = 0; c < kDecCluster; c++) {
-    const uint32_t *pub = cluster.map_shared_rank(sm.pub, c);
-    rmax[c] = pub[lane & 15];
-    rcnt[c] = pub[16];
-  }
-  uint32_t nO_u = 0, base = 0;  // |O| and this CTA's offset in the ascending outlier list
-#pragma unroll
-  for (int c = 0; c < kDecCluster; c++) {
-    nO_u += rcnt[c];
-    if (c < crank) base += rcnt[c];
-  }
-  const int32_t nO = (int32_t)nO_u;
-  if (warp < kDecWarps) {
-    uint32_t m = 0;
-#pragma unroll
-    for (int c = 0; c < kDecCluster; c++) m = max(m, rmax[c]);
-    if (lane >= 16) m = 0;
-    const float a_lane = h2f_bits(m);      // sx of row `lane` (0 for rows >= T)
-    const float rc_lane = code_recip(a_lane);  // 127 / sx, one division per row
-    if (warp == 0 && lane < 16) sxs[lane] = a_lane;
-    uint8_t *xs_c[kDecCluster];
-    uint16_t *oc_c[kDecCluster];
-    unsigned short *xo_c[kDecCluster];
-#pragma unroll
-    for (int c = 0; c < kDecCluster; c++) {
-      xs_c[c] = cluster.map_shared_rank(xs, c);
-      oc_c[c] = cluster.map_shared_rank(ocols, c);
-      xo_c[c] = cluster.map_shared_rank(sm.xo, c);
-    }
-    // this CTA's outliers in the ascending list: warps (of each row-quad) by
-    // column, lanes by column, bits.  Every row-quad holds the same columns.
-    const uint32_t pc = __popc(flags);
-    uint32_t incl = pc;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += y;
-    }
-    if (live && flags) {
-      uint32_t j = base + incl - pc;
-      for (int w = 0; w < (warp & 3); w++) j += sm.wcnt[w];
-#pragma unroll
-      for (int b = 0; b < 8; b++)
-        if ((flags >> b) & 1) {
-          if (quad == 0)
-            for (int c = 0; c < kDecCluster; c++) oc_c[c][j] = (uint16_t)(8 * v + b);
-          if (j < (uint32_t)kDecOutSmall) {  // X at this outlier column, rows of this quad
-#pragma unroll
-            for (int r = 0; r < 4; r++) {
-              const int t = 4 * quad + r;
-              const unsigned short hb = (unsigned short)(((&x[r].x)[b >> 1] >> (16 * (b & 1))) & 0xffffu);
-              if (t < T)
-                for (int c = 0; c < kDecCluster; c++) xo_c[c][t * kDecOutSmall + j] = hb;
-            }
-          }
-          ++j;
-        }
-    }
-#pragma unroll
-    for (int r = 0; r < 4; r++) {
-      const int t = 4 * quad + r;
-      const float a = __shfl_sync(0xffffffffu, a_lane, t);
-      const float rc = __shfl_sync(0xffffffffu, rc_lane, t);
-      const uint32_t w[4] = {x[r].x, x[r].y, x[r].z, x[r].w};
-      uint32_t p0 = 0, p1 = 0;
-#pragma unroll
-      for (int i = 0; i < 4; i++) {
-        const uint32_t c0 =
-            ((flags >> (2 * i)) & 1) ? 0u : code_byte(h2f_bits(w[i] & 0xffffu), a, rc);
-        const uint32_t c1 =
-            ((flags >> (2 * i + 1)) & 1) ? 0u : code_byte(h2f_bits(w[i] >> 16), a, rc);
-        const uint32_t two = (c0 & 0xffu) | ((c1 & 0xffu) << 8);
-        if (i < 2)
-          p0 |= two << (16 * i);
-        else
-          p1 |= two << (16 * (i - 2));
-      }
-      // even lanes store 16 codes (their vector and the next lane's) at once
-      const uint32_t q0 = __shfl_down_sync(0xffffffffu, p0, 1);
-      const uint32_t q1 = __shfl_down_sync(0xffffffffu, p1, 1);
-      if (t >= T || !live) continue;
-      if ((vpc & 1) == 0) {
-        // vpc even: an even lane holds an even vector (16-byte aligned codes)
-        // and its odd neighbour is live, so it writes both
-        if ((lane & 1) == 0)
-          for (int c = 0; c < kDecCluster; c++)
-            *reinterpret_cast<uint4 *>(xs_c[c] + t * pitch + 8 * v) = make_uint4(p0, p1, q0, q1);
+        for (int w = 0; w < G::kWpg; w++) val = max(val, sm.part[(rg * G::kWpg + w) * 4 + j]);
       } else {
-        for (int c = 0; c < kDecCluster; c++)
-          *reinterpret_cast<uint2 *>(xs_c[c] + t * pitch + 8 * v) = make_uint2(p0, p1);
+#pragma unroll
+        for (int w = 0; w < G::kWpg; w++) val += sm.wcnt[w];
+      }
+      const uint32_t dst = smem_addr(&sm.pubs[crank][threadIdx.x]), bar = smem_addr(&sm.pbar);
+#pragma unroll
+      for (int c = 0; c < kC; c++) st_async_b32(mapa(dst, c), val, mapa(bar, c));
+      if (threadIdx.x == 0) mbar_expect_tx(&sm.pbar, kC * 17 * 4);
+    }
+    if (mbar_wait_cluster_bounded(&sm.pbar, 0, p.status)) {
+      // ---- activation pass 2: row scales, int8 codes, outlier mask (cluster-wide) ----
+      uint32_t nO = 0, base = 0;
+#pragma unroll
+      for (int c = 0; c < kC; c++) {
+        const uint32_t n = sm.pubs[c][16];
+        nO += n;
+        if (c < (int)crank) base += n;
+      }
+      float a_r[G::kRpt], rc_r[G::kRpt];
+#pragma unroll
+      for (int j = 0; j < G::kRpt; j++) {
+        const int t = grp + kC * j;
+        uint32_t m = 0;
+#pragma unroll
+        for (int c = 0; c < kC; c++) m = max(m, sm.pubs[c][t]);
+        a_r[j] = h2f_bits(t < T ? m : 0u);  // sx; 0 for rows >= T
+        rc_r[j] = code_recip(a_r[j]);       // one division per row
+      }
+      if (threadIdx.x < 16) {
+        uint32_t m = 0;
+#pragma unroll
+        for (int c = 0; c < kC; c++) m = max(m, sm.pubs[c][threadIdx.x]);
+        sxs[threadIdx.x] = h2f_bits((int)threadIdx.x < T ? m : 0u);
+      }
+      // bytes every CTA receives: the codes of all T rows, every mask word and
+      // the X values of the first outlier columns
+      const uint32_t incoming = (uint32_t)T * (uint32_t)K + 4u * (uint32_t)words +
+                                4u * (uint32_t)T * min(nO, (uint32_t)kDecOutSmall);
+      if (threadIdx.x == 0) mbar_expect_tx(&sm.cbar, incoming);
+      const uint32_t cbar = smem_addr(&sm.cbar);
+      if (grp == 0) {  // mask word v/4 from the flags of vectors v .. v+3 (one CTA's)
+        const uint32_t f1 = __shfl_down_sync(0xffffffffu, flags, 1);
+        const uint32_t f2 = __shfl_down_sync(0xffffffffu, flags, 2);
+        const uint32_t f3 = __shfl_down_sync(0xffffffffu, flags, 3);
+        if ((vl & 3) == 0 && vl < vpc && v < vecs) {  // each word exactly once
+          const uint32_t word = flags | (f1 << 8) | (f2 << 16) | (f3 << 24);
+          const uint32_t dst = smem_addr(&sm.mask[v / 4]);
+#pragma unroll
+          for (int c = 0; c < kC; c++) st_async_b32(mapa(dst, c), word, mapa(cbar, c));
+        }
+      }
+      // X at the first outlier columns: this CTA's outliers sit at positions
+      // base.. of the ascending list, ordered by vector block, lane and bit.
+      // Every row group holds the same columns.
+      if (__any_sync(0xffffffffu, flags != 0)) {
+        const uint32_t pc = __popc(flags);
+        uint32_t incl = pc;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        if (live && flags) {
+          uint32_t j = base + incl - pc;
+          for (int w = 0; w < warp % G::kWpg; w++) j += sm.wcnt[w];
+          for (int b = 0; b < 8 && j < (uint32_t)kDecOutSmall; b++)
+            if ((flags >> b) & 1) {
+#pragma unroll
+              for (int r = 0; r < G::kRpt; r++) {
+                const int t = grp + kC * r;
+                const uint32_t hb = ((&x[r].x)[b >> 1] >> (16 * (b & 1))) & 0xffffu;
+                if (t < T) {
+                  const uint32_t dst = smem_addr(&sm.xo[t * kDecOutSmall + j]);
+                  for (int c = 0; c < kC; c++) st_async_b32(mapa(dst, c), hb, mapa(cbar, c));
+                }
+              }
+              ++j;
+            }
+        }
+      }
+#pragma unroll
+      for (int r = 0; r < G::kRpt; r++) {
+        const int t = grp + kC * r;
+        const float a = a_r[r], rc = rc_r[r];
+        const uint32_t w[4] = {x[r].x, x[r].y, x[r].z, x[r].w};
+        uint32_t p0 = 0, p1 = 0;
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+          const uint32_t c0 =
+              ((flags >> (2 * i)) & 1) ? 0u : code_byte(h2f_bits(w[i] & 0xffffu), a, rc);
+          const uint32_t c1 =
+              ((flags >> (2 * i + 1)) & 1) ? 0u : code_byte(h2f_bits(w[i] >> 16), a, rc);
+          const uint32_t two = (c0 & 0xffu) | ((c1 & 0xffu) << 8);
+          if (i < 2)
+            p0 |= two << (16 * i);
+          else
+            p1 |= two << (16 * (i - 2));
+        }
+        // even lanes store 16 codes (their vector and the next lane's) at once:
+        // vpc is even, so an even thread's vector is even (16-byte aligned codes)
+        // and its odd neighbour is live with it
+        const uint32_t q0 = __shfl_down_sync(0xffffffffu, p0, 1);
+        const uint32_t q1 = __shfl_down_sync(0xffffffffu, p1, 1);
+        if (t >= T || !live || (lane & 1)) continue;
+        const uint32_t dst = smem_addr(xs + t * pitch + 8 * v);
+#pragma unroll
+        for (int c = 0; c < kC; c++) st_async_v4(mapa(dst, c), p0, p1, q0, q1, mapa(cbar, c));
       }
     }
   }
-  cluster.sync();  // every CTA holds all codes, the outlier list and its X values
+  // every CTA's codes, mask words and outlier X values are here (this also
+  // keeps the CTA alive until the last remote store into it has landed)
+  const bool have = mbar_wait_cluster_bounded(&sm.pbar, 0, p.status) &&
+                    mbar_wait_cluster_bounded(&sm.cbar, 0, p.status);
+  int32_t nO = 0;
+  if (have)
+#pragma unroll
+    for (int c = 0; c < kC; c++) nO += (int32_t)sm.pubs[c][16];
 
   if (blockIdx.x == 0) {  // the activation pass's results, for the debug entry point
     if (threadIdx.x < T) p.sx_out[threadIdx.x] = sxs[threadIdx.x];
-    if (threadIdx.x == 0) {
-      *p.nO_out = nO_u;
-      *p.status = kDevOk;
-    }
-    for (int32_t j = threadIdx.x; j < nO; j += kDecThreads) p.O_out[j] = ocols[j];
     if (p.dbg_xq)
       for (int64_t i = threadIdx.x; i < (int64_t)T * vecs; i += kDecThreads) {
         const int64_t t = i / vecs, vv = i - t * vecs;
         reinterpret_cast<uint2 *>(p.dbg_xq)[i] = *reinterpret_cast<const uint2 *>(xs + t * pitch + 8 * vv);
       }
   }
+  if (!have) {  // a bounded wait gave up (recorded in the status word)
+    if (warp == kDecWarps && rows > 0) (void)mbar_wait_bounded(&sm.wbar, 0, p.status);  // copies in flight
+    return;
+  }
   if (rows <= 0) return;  // a cluster's last CTAs may have no output channels
 
   if (warp == kDecWarps) {
-    // ---- producer warp: the first outlier columns for this slice, lane = row ----
-    const int32_t nsmall = min(nO, kDecOutSmall);
-    float o[16];
+    // ---- producer warp: the ascending outlier list from the mask, then the
+    // first outlier columns for this slice, lane = channel ----
+    {
+      const int64_t wpl = (words + 31) / 32;
+      const int64_t w0 = min(words, lane * wpl), w1 = min(words, w0 + wpl);
+      uint32_t cnt = 0;
+      for (int64_t w = w0; w < w1; w++) cnt += __popc(sm.mask[w]);
+      uint32_t incl = cnt;
 #pragma unroll
-    for (int t = 0; t < 16; t++) o[t] = 0.f;
-    const int64_t n = n0 + min((int64_t)lane, rows - 1);
-    for (int32_t jb = 0; jb < nsmall; jb += 8) {
-      float wv[8];
-#pragma unroll
-      for (int e = 0; e < 8; e++)  // eight independent loads in flight
-        wv[e] = jb + e < nsmall ? h2f_bits(__ldg(p.W16 + n * K + ocols[jb + e])) : 0.f;
-#pragma unroll
-      for (int e = 0; e < 8; e++)
-#pragma unroll
-        for (int t = 0; t < 16; t++)
-          if (t < T && jb + e < nsmall) o[t] = fmaf(h2f_bits(sm.xo[t * kDecOutSmall + jb + e]), wv[e], o[t]);
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      uint32_t j = incl - cnt;
+      for (int64_t w = w0; w < w1; w++)
+        for (uint32_t m = sm.mask[w]; m; m &= m - 1) ocols[j++] = (uint16_t)(32 * w + __ffs(m) - 1);
+      __syncwarp();
+      named_bar_arrive(3, kDecThreads);  // the list is complete for the consumers
+      if (blockIdx.x == 0) {
+        for (int32_t i = lane; i < nO; i += 32) p.O_out[i] = ocols[i];
+        if (lane == 0) *p.nO_out = (uint32_t)nO;
+      }
     }
+    const int32_t nsmall = min(nO, kDecOutSmall);
+    for (int64_t rr = lane; rr < rows; rr += 32) {
+      float o[16];
 #pragma unroll
-    for (int t = 0; t < 16; t++) osm[t * 32 + lane] = o[t];
+      for (int t = 0; t < 16; t++) o[t] = 0.f;
+      const int64_t n = n0 + min(rr, rows - 1);
+      for (int32_t jb = 0; jb < nsmall; jb += 8) {
+        float wv[8];
+#pragma unroll
+        for (int e = 0; e < 8; e++)  // eight independent loads in flight
+          wv[e] = jb + e < nsmall ? h2f_bits(__ldg(p.W16 + n * K + ocols[jb + e])) : 0.f;
+#pragma unroll
+        for (int e = 0; e < 8; e++)
+#pragma unroll
+          for (int t = 0; t < 16; t++)
+            if (t < T && jb + e < nsmall) o[t] = fmaf(h2f_bits(sm.xo[t * kDecOutSmall + jb + e]), wv[e], o[t]);
+      }
+#pragma unroll
+      for (int t = 0; t < 16; t++) osm[t * kDecMaxRows + rr] = o[t];
+    }
     mbar_arrive(obar);  // 32 arrivals: osm is written
     return;
   }
 
-  // ---- consumer warps: K-range [k0, k1) for all four row groups ----
+  // ---- consumer warps: K-range [k0, k1) for every 8-channel group ----
   const int g = lane >> 2, q = lane & 3;
+  const int ng = (int)((rows + 7) / 8);
+  // Epilogue items: thread i takes accumulator word idx = i / 32 (and, for
+  // i < 128, idx + 16: the fifth group) of lane i % 32 of every warp; the
+  // channel scales are loaded while the MMAs run.
+  const int el = threadIdx.x & 31, eg = el >> 2, eq = el & 3;
+  const int nitems = threadIdx.x < 128 ? 2 : 1;
+  int e_t[2], e_n[2];
+  float e_sw[2];
+#pragma unroll
+  for (int it = 0; it < 2; it++) {
+    const int idx = threadIdx.x / 32 + 16 * it, gi = idx >> 2, j = idx & 3;
+    e_t[it] = eg + 8 * (j >> 1);
+    e_n[it] = gi * 8 + 2 * eq + (j & 1);
+    e_sw[it] = (it < nitems && e_n[it] < rows) ? __ldg(p.sw + n0 + e_n[it]) : 0.f;
+  }
   const int64_t k0 = warp * range, k1 = min(K, k0 + range);
-  int acc[4][4] = {};
+  int acc[kDecGroups][4] = {};
   if (k1 > k0 && mbar_wait_bounded(&sm.wbar, 0, p.status)) {
-    float f[4][4] = {};
-    int nb = 0;
-    for (int64_t kb = k0; kb < k1; kb += 64) {
-      const uint32_t lv = (kb + 16 * q < k1) ? 0xffffffffu : 0u;  // columns past K feed zeros
-      uint32_t xa[8], xb[8];
-      widen16(*reinterpret_cast<const uint4 *>(xs + g * pitch + kb + 16 * q), xa);
-      widen16(*reinterpret_cast<const uint4 *>(xs + (g + 8) * pitch + kb + 16 * q), xb);
-#pragma unroll
-      for (int gi = 0; gi < 4; gi++) {
-        uint32_t h[8];
-        widen16(*reinterpret_cast<const uint4 *>(ws + (gi * 8 + g) * pitch + kb + 16 * q), h);
-#pragma unroll
-        for (int mm = 0; mm < 4; mm++)
-          mma_f16_16x8x16(f[gi], xa[2 * mm] & lv, xb[2 * mm] & lv, xa[2 * mm + 1] & lv,
-                          xb[2 * mm + 1] & lv, h[2 * mm] & lv, h[2 * mm + 1] & lv);
-      }
-      if (++nb == kDecChunkK / 64 || kb + 64 >= k1) {  // exact drain into int32
-        nb = 0;
-#pragma unroll
-        for (int gi = 0; gi < 4; gi++)
-#pragma unroll
-          for (int j = 0; j < 4; j++) {
-            acc[gi][j] += __float2int_rn(f[gi][j]);
-            f[gi][j] = 0.f;
-          }
-      }
-    }
+    if (((k1 - k0) & 63) == 0)
+      dec_mma_range<false>(xs, ws, pitch, g, q, k0, k1, ng, acc);
+    else
+      dec_mma_range<true>(xs, ws, pitch, g, q, k0, k1, ng, acc);
   }
   // outlier columns beyond the first kDecOutSmall: split over the consumer warps
-  float o[4][4] = {};
+  named_bar_sync(3, kDecThreads);  // the producer has listed them
+  const bool big = nO > kDecOutSmall;  // the same in every warp
+  float o[kDecGroups][4] = {};
   for (int32_t j = kDecOutSmall + warp; j < nO; j += kDecWarps) {
     const int64_t k = ocols[j];
     const float x0 = g < T ? h2f_bits(__ldg(p.X16 + (int64_t)g * K + k)) : 0.f;
     const float x1 = g + 8 < T ? h2f_bits(__ldg(p.X16 + (int64_t)(g + 8) * K + k)) : 0.f;
 #pragma unroll
-    for (int gi = 0; gi < 4; gi++) {
-      const int64_t na = n0 + min((int64_t)gi * 8 + 2 * q, rows - 1);
-      const int64_t nb = n0 + min((int64_t)gi * 8 + 2 * q + 1, rows - 1);
-      const float wa = h2f_bits(__ldg(p.W16 + na * K + k));
-      const float wb = h2f_bits(__ldg(p.W16 + nb * K + k));
-      o[gi][0] = fmaf(x0, wa, o[gi][0]);
-      o[gi][1] = fmaf(x0, wb, o[gi][1]);
-      o[gi][2] = fmaf(x1, wa, o[gi][2]);
-      o[gi][3] = fmaf(x1, wb, o[gi][3]);
+    for (int gi = 0; gi < kDecGroups; gi++) {
+      if (gi < ng) {
+        const int64_t na = n0 + min((int64_t)gi * 8 + 2 * q, rows - 1);
+        const int64_t nb = n0 + min((int64_t)gi * 8 + 2 * q + 1, rows - 1);
+        const float wa = h2f_bits(__ldg(p.W16 + na * K + k));
+        const float wb = h2f_bits(__ldg(p.W16 + nb * K + k));
+        o[gi][0] = fmaf(x0, wa, o[gi][0]);
+        o[gi][1] = fmaf(x0, wb, o[gi][1]);
+        o[gi][2] = fmaf(x1, wa, o[gi][2]);
+        o[gi][3] = fmaf(x1, wb, o[gi][3]);
+      }
     }
   }
-  // cross-warp reduction: red[warp][lane][gi*4 + j], in the weight region once
-  // every consumer warp is past its main loop
-  asm volatile("bar.sync 1, %0;" ::"r"(kDecWarps * 32));
-  uint32_t *mine = red + (warp * 32 + lane) * 16;
+  // cross-warp reduction: red[warp][lane][gi*4 + j] (stride 21 words, so that
+  // the epilogue's column reads are free of bank conflicts), in the weight
+  // region once every consumer warp is past its main loop
+  named_bar_sync(1, kDecConsumers);
+  uint32_t *mine = red + (warp * 32 + lane) * kDecRedStride;
 #pragma unroll
-  for (int gi = 0; gi < 4; gi++)
+  for (int gi = 0; gi < kDecGroups; gi++)
 #pragma unroll
     for (int j = 0; j < 4; j++) mine[gi * 4 + j] = (uint32_t)acc[gi][j];
-  asm volatile("bar.sync 1, %0;" ::"r"(kDecWarps * 32));
-  if (warp < 4) {
-    const int gi = warp;
-    int a[4] = {0, 0, 0, 0};
-    for (int w = 0; w < kDecWarps; w++) {
-      const uint32_t *src = red + (w * 32 + lane) * 16 + gi * 4;
+  named_bar_sync(1, kDecConsumers);
+  int e_acc[2] = {0, 0};
 #pragma unroll
-      for (int j = 0; j < 4; j++) a[j] += (int)src[j];
+  for (int it = 0; it < 2; it++)
+    if (it < nitems) {
+      const int idx = threadIdx.x / 32 + 16 * it;
+#pragma unroll
+      for (int w = 0; w < kDecWarps; w++) e_acc[it] += (int)red[(w * 32 + el) * kDecRedStride + idx];
     }
-#pragma unroll
-    for (int j = 0; j < 4; j++) acc[0][j] = a[j];
-  }
-  const bool big = nO > kDecOutSmall;  // the same in every warp
+  float e_out[2] = {0.f, 0.f};
   if (big) {
-    asm volatile("bar.sync 1, %0;" ::"r"(kDecWarps * 32));
+    named_bar_sync(1, kDecConsumers);
 #pragma unroll
-    for (int gi = 0; gi < 4; gi++)
+    for (int gi = 0; gi < kDecGroups; gi++)
 #pragma unroll
       for (int j = 0; j < 4; j++) mine[gi * 4 + j] = __float_as_uint(o[gi][j]);
-    asm volatile("bar.sync 1, %0;" ::"r"(kDecWarps * 32));
+    named_bar_sync(1, kDecConsumers);
+#pragma unroll
+    for (int it = 0; it < 2; it++)
+      if (it < nitems) {
+        const int idx = threadIdx.x / 32 + 16 * it;
+#pragma unroll
+        for (int w = 0; w < kDecWarps; w++)
+          e_out[it] += __uint_as_float(red[(w * 32 + el) * kDecRedStride + idx]);
+      }
   }
-  if (warp < 4) {
-    const int gi = warp;
-    float ov[4] = {0.f, 0.f, 0.f, 0.f};
-    if (big)
-      for (int w = 0; w < kDecWarps; w++) {
-        const uint32_t *src = red + (w * 32 + lane) * 16 + gi * 4;
+  const bool ok_o = mbar_wait_bounded(obar, 0, p.status);
 #pragma unroll
-        for (int j = 0; j < 4; j++) ov[j] += __uint_as_float(src[j]);
-      }
-    const bool ok_o = mbar_wait_bounded(obar, 0, p.status);
-#pragma unroll
-    for (int j = 0; j < 4; j++) {
-      const int64_t t = g + 8 * (j / 2);
-      const int64_t nl = (int64_t)gi * 8 + 2 * q + (j % 2);
-      if (t < T && nl < rows && ok_o) {
-        const int64_t n = n0 + nl;
-        const float st = sxs[t] / 127.0f, sn = __ldg(p.sw + n) / 127.0f;
-        const float y = fmaf((float)acc[0][j] * st, sn, ov[j] + osm[t * 32 + nl]);
-        p.Y[t * p.N + n] = __float2half_rn(y);
-        if (p.dbg_acc) p.dbg_acc[t * p.N + n] = acc[0][j];
-      }
+  for (int it = 0; it < 2; it++) {
+    const int t = e_t[it], nl = e_n[it];
+    if (it < nitems && t < T && nl < rows && ok_o) {
+      const int64_t n = n0 + nl;
+      const float st = sxs[t] / 127.0f, sn = e_sw[it] / 127.0f;
+      const float y = fmaf((float)e_acc[it] * st, sn, e_out[it] + osm[t * kDecMaxRows + nl]);
+      p.Y[t * p.N + n] = __float2half_rn(y);
+      if (p.dbg_acc) p.dbg_acc[t * p.N + n] = e_acc[it];
     }
   }
 }
@@ -471,38 +574,107 @@ __global__ void __launch_bounds__(kDecThreads, 1) dec_fused_kernel(const DecArgs
 // host side
 // ---------------------------------------------------------------------------
 
-// CTAs of dec_fused that can be resident at once, in whole clusters (queried
-// once per device; the nominal B300 count when no device answers).
-int decode_max_ctas(int dev) {
-  static std::atomic<int> cache[64];
-  if (dev >= 0 && dev < 64) {
-    const int v = cache[dev].load(std::memory_order_relaxed);
-    if (v > 0) return v;
-  }
+namespace {
+
+constexpr int kDecClusterSizes[3] = {8, 16, 4};  // order of preference (measured)
+
+// CTAs of dec_fused<kC> resident at once, in whole clusters (0 if the query
+// fails); also opens the kernel's shared-memory limit to `dyn_max`.
+template <int kC>
+int dec_resident_ctas(int dyn_max) {
+  if (cudaFuncSetAttribute(dec_fused_kernel<kC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           dyn_max) != cudaSuccess)
+    return 0;
+  if (kC > 8 && cudaFuncSetAttribute(dec_fused_kernel<kC>,
+                                     cudaFuncAttributeNonPortableClusterSizeAllowed,
+                                     1) != cudaSuccess)
+    return 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(kC * 16);
+  cfg.blockDim = dim3(kDecThreads);
+  cfg.dynamicSmemBytes = decode_smem_bytes(kDecodeMaxK, 32);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kC;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   int n = 0;
-  if (cudaFuncSetAttribute(dec_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)decode_smem_bytes(kDecodeMaxK)) == cudaSuccess) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(kDecCluster * 64);
-    cfg.blockDim = dim3(kDecThreads);
-    cfg.dynamicSmemBytes = decode_smem_bytes(kDecodeMaxK);
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = kDecCluster;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    if (cudaOccupancyMaxActiveClusters(&n, dec_fused_kernel, &cfg) != cudaSuccess) n = 0;
-  }
-  (void)cudaGetLastError();  // a failed query is not a launch error
-  const int v = n > 0 ? n * kDecCluster : kB300Sms / kDecCluster * kDecCluster;
-  if (n > 0 && dev >= 0 && dev < 64) cache[dev].store(v, std::memory_order_relaxed);
-  return v;
+  if (cudaOccupancyMaxActiveClusters(&n, dec_fused_kernel<kC>, &cfg) != cudaSuccess) n = 0;
+  return n * kC;
 }
 
-// Output channels the decode path can take: at most 32 per resident CTA.
-int64_t decode_max_n(int dev) { return 32LL * decode_max_ctas(dev); }
+struct DecCfg {
+  int ctas[3];  // resident CTAs for each entry of kDecClusterSizes (0: not available)
+  int dyn_max;  // dynamic shared memory a CTA may use
+};
+
+// Queried once per device; the nominal B300 figures when no device answers.
+DecCfg decode_cfg(int dev) {
+  static std::atomic<int64_t> cache[64][2];
+  if (dev >= 0 && dev < 64) {
+    const int64_t v = cache[dev][0].load(std::memory_order_relaxed);
+    if (v > 0)
+      return DecCfg{{(int)(v & 0xffff), (int)((v >> 16) & 0xffff), (int)(v >> 32)},
+                    (int)cache[dev][1].load(std::memory_order_relaxed)};
+  }
+  int optin = 0;
+  cudaFuncAttributes fa = {};
+  DecCfg r{{0, 0, 0}, 0};
+  if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev < 0 ? 0 : dev) ==
+          cudaSuccess &&
+      cudaFuncGetAttributes(&fa, dec_fused_kernel<8>) == cudaSuccess) {
+    r.dyn_max = optin - (int)fa.sharedSizeBytes;
+    r.ctas[0] = dec_resident_ctas<8>(r.dyn_max);
+    r.ctas[1] = dec_resident_ctas<16>(r.dyn_max);
+    r.ctas[2] = dec_resident_ctas<4>(r.dyn_max);
+  }
+  (void)cudaGetLastError();  // a failed query is not a launch error
+  if (r.ctas[0] + r.ctas[1] + r.ctas[2] == 0)
+    return DecCfg{{0, 0, kB300Sms / 4 * 4}, (int)decode_smem_bytes(kDecodeMaxK, 32)};
+  if (dev >= 0 && dev < 64) {
+    cache[dev][1].store(r.dyn_max, std::memory_order_relaxed);
+    cache[dev][0].store((int64_t)r.ctas[0] | ((int64_t)r.ctas[1] << 16) | ((int64_t)r.ctas[2] << 32),
+                        std::memory_order_relaxed);
+  }
+  return r;
+}
+
+// Output channels a CTA can hold at this K (at most kDecMaxRows).
+int64_t dec_rows_cap(const DecCfg &c, int64_t K) {
+  int64_t rows = kDecMaxRows;
+  while (rows > 8 && decode_smem_bytes(K, rows) > (size_t)c.dyn_max) rows--;
+  return rows;
+}
+
+// The first cluster size, in kDecClusterSizes' order, whose resident CTAs
+// hold N output channels in one wave; -1 if none does.  The environment
+// override BNB_DECODE_CLUSTER=8|16|4 takes that size instead whenever it
+// holds the call (for tests and side-by-side measurement).
+int decode_pick(const DecCfg &c, int64_t N, int64_t K) {
+  const int64_t cap = dec_rows_cap(c, K);
+  const int64_t need = (N + cap - 1) / cap;
+  if (const char *e = std::getenv("BNB_DECODE_CLUSTER")) {
+    const int f = std::atoi(e);
+    for (int i = 0; i < 3; i++)
+      if (kDecClusterSizes[i] == f && c.ctas[i] >= need) return i;
+  }
+  for (int i = 0; i < 3; i++)
+    if (c.ctas[i] >= need) return i;
+  return -1;
+}
+
+}  // namespace
+
+// Output channels the decode path takes at this K: what the resident CTAs of
+// the best-covered cluster size hold.
+int64_t decode_max_n(int dev, int64_t K) {
+  const DecCfg c = decode_cfg(dev);
+  const int most = c.ctas[0] > c.ctas[1] ? (c.ctas[0] > c.ctas[2] ? c.ctas[0] : c.ctas[2])
+                                         : (c.ctas[1] > c.ctas[2] ? c.ctas[1] : c.ctas[2]);
+  return (int64_t)most * dec_rows_cap(c, K);
+}
 
 cudaError_t launch_decode(const void *X, int64_t T, int64_t K, uint32_t thr, const int8_t *Wq,
                           const float *sw, const void *W16, int64_t N, void *Y,
@@ -510,7 +682,10 @@ cudaError_t launch_decode(const void *X, int64_t T, int64_t K, uint32_t thr, con
                           cudaStream_t stream) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) dev = -1;
-  const int max_ctas = decode_max_ctas(dev);
+  const DecCfg dc = decode_cfg(dev);
+  const int pick = decode_pick(dc, N, K);
+  if (pick < 0) return cudaErrorInvalidValue;  // the host routes only shapes that fit here
+  const int kc = kDecClusterSizes[pick];
   DecArgs a;
   a.X = reinterpret_cast<const uint4 *>(X);
   a.X16 = reinterpret_cast<const unsigned short *>(X);
@@ -518,12 +693,13 @@ cudaError_t launch_decode(const void *X, int64_t T, int64_t K, uint32_t thr, con
   a.K = K;
   a.N = N;
   a.thr = thr;
-  // enough whole clusters for at most 32 output channels per CTA (the host
-  // only routes N <= 32 * max_ctas here), all of them resident at once
-  const int64_t want = min((int64_t)max_ctas, ((N + 7) / 8 + kDecCluster - 1) / kDecCluster * kDecCluster);
+  // the resident CTAs (whole clusters) share the channels evenly, at least 8
+  // per CTA
+  const int64_t want = min((int64_t)dc.ctas[pick], ((N + 7) / 8 + kc - 1) / kc * kc);
   a.rows_per_cta = (N + want - 1) / want;
   const int64_t used = (N + a.rows_per_cta - 1) / a.rows_per_cta;
-  const int64_t ctas = (used + kDecCluster - 1) / kDecCluster * kDecCluster;
+  const int64_t ctas = (used + kc - 1) / kc * kc;
+  a.wregion = dec_wregion(K, a.rows_per_cta);
   a.Wq = Wq;
   a.sw = sw;
   a.W16 = reinterpret_cast<const unsigned short *>(W16);
@@ -537,11 +713,11 @@ cudaError_t launch_decode(const void *X, int64_t T, int64_t K, uint32_t thr, con
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)ctas);
   cfg.blockDim = dim3(kDecThreads);
-  cfg.dynamicSmemBytes = decode_smem_bytes(K);
+  cfg.dynamicSmemBytes = decode_smem_bytes(K, a.rows_per_cta);
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = kDecCluster;
+  attr[0].val.clusterDim.x = (unsigned)kc;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -549,7 +725,9 @@ cudaError_t launch_decode(const void *X, int64_t T, int64_t K, uint32_t thr, con
   cfg.attrs = attr;
   cfg.numAttrs = profile_only_main() ? 1 : 2;  // profiling mode 2: no overlap with the previous call
   ProfScope ps(kKidDecFused, stream);
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, dec_fused_kernel, a);
+  const cudaError_t e = kc == 8    ? cudaLaunchKernelEx(&cfg, dec_fused_kernel<8>, a)
+                        : kc == 16 ? cudaLaunchKernelEx(&cfg, dec_fused_kernel<16>, a)
+                                   : cudaLaunchKernelEx(&cfg, dec_fused_kernel<4>, a);
   note_launch();
   return e;
 }

@@ -58,11 +58,10 @@ cudaError_t launch_act_pass(const void *X, int64_t T, int64_t K, uint32_t thr_bi
 cudaError_t launch_gather_outlier_weights(const void *W16, int64_t N, int64_t K,
                                           const Workspace &ws, int num_sms, cudaStream_t stream);
 
-// The whole layer for T <= 16, K <= kDecodeMaxK, N <= decode_max_n(dev) in
-// one kernel (activation pass fused into the GEMV and shared by clusters of
-// CTAs), launched with programmatic dependent launch.
-int decode_max_ctas(int dev);
-int64_t decode_max_n(int dev);
+// The whole layer for T <= 16, K <= kDecodeMaxK, N <= decode_max_n(dev, K)
+// in one kernel (activation pass fused into the GEMV and shared by clusters
+// of CTAs), launched with programmatic dependent launch.
+int64_t decode_max_n(int dev, int64_t K);
 cudaError_t launch_decode(const void *X, int64_t T, int64_t K, uint32_t thr, const int8_t *Wq,
                           const float *sw, const void *W16, int64_t N, void *Y,
                           const Workspace &ws, int8_t *dbg_xq, int32_t *dbg_acc,

@@ -32,6 +32,24 @@ def test_decode(orc, T):
     run_and_compare(orc, w.X, w.W, w.tau, what=f"decode T={T}")
 
 
+@pytest.mark.parametrize("cluster", [16, 8, 4])
+@pytest.mark.parametrize("T,K,N,ncols", [
+    (16, 4096, 1024, 4), (5, 272, 200, 2), (16, 1040, 96, 70), (11, 2048, 520, 9),
+    (16, 4096, 3900, 70),
+])
+def test_decode_cluster_sizes(orc, monkeypatch, cluster, T, K, N, ncols):
+    """The decode kernel with each cluster size it can run (16, 8 or 4 CTAs
+    sharing one activation pass): CTAs with few or no columns, slices of up
+    to 35 channels (a partial fifth 8-channel group), and more outlier columns
+    than the producer warp sums alone.  A size whose resident CTAs cannot
+    hold the call falls back to one that can."""
+    from int8_mixed_precision_04_b300 import binding
+    monkeypatch.setenv("BNB_DECODE_CLUSTER", str(cluster))
+    assert binding.load().bnb_int8_linear_path(T, N, K) == 1
+    w = inputs.random_small(T, K, N, ncols, seed=K + N + cluster, tau=6.0)
+    run_and_compare(orc, w.X, w.W, 6.0, what=f"decode cluster {cluster} T{T} K{K} N{N}")
+
+
 @pytest.mark.parametrize("T,K,N,ncols", [
     (1, 16, 1, 0), (3, 48, 7, 1), (16, 272, 129, 2), (17, 64, 300, 3), (33, 1040, 65, 4),
     (130, 512, 257, 5), (200, 2064, 131, 7), (257, 128, 1000, 2), (64, 4096, 64, 9),
