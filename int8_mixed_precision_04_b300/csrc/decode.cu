@@ -48,7 +48,7 @@ constexpr int kDecThreads = kDecConsumers + 32;    // + one producer warp
 constexpr int kDecGroups = 5;                      // 8-channel MMA groups of a slice, at most
 constexpr int kDecMaxRows = kDecGroups * 8;        // output channels per CTA, at most
 constexpr int kDecChunkK = 1024;                   // fp32 accumulation is drained this often
-constexpr int kDecOutSmall = 64;                   // outlier columns the producer warp sums
+constexpr int kDecOutSmall = 8;                    // outlier columns of W16 fetched by TMA
 constexpr int kDecRedStride = kDecGroups * 4 + 1;  // words per lane in the reduction (odd)
 constexpr int kDecMaskWords = (int)(kDecodeMaxK / 32);
 
@@ -87,10 +87,13 @@ size_t decode_smem_bytes(int64_t K, int64_t rows) {
 // small static buffers of one CTA (partly written by the other CTAs of its cluster)
 struct DecSmall {
   uint64_t wbar;            // the CTA's weight slice has landed
-  uint64_t obar;            // producer warp's outlier sums are in osm
+  uint64_t wobar;           // W16 at the first outlier columns is in wos
   uint64_t pbar;            // every CTA's row maxima and outlier count are in pubs
-  uint64_t cbar;            // every CTA's codes, mask words and outlier X values are here
-  float osm[16 * kDecMaxRows];  // [t][row] outlier sums of the first kDecOutSmall columns
+  uint64_t cbar;            // every CTA's codes and outlier-mask words are here
+  uint64_t xbar;            // the first outlier columns and their X values are here
+  uint64_t lbar;            // the producer warp has listed every outlier column
+  // [j][row][8]: W16[n0 + row, 8 (O[j] / 8) .. + 8), one TMA box per outlier column j
+  alignas(128) uint16_t wos[kDecOutSmall][kDecMaxRows][8];
   float sxs[16];            // row scales sx
   uint32_t part[kDecWarps * 4];  // [warp][j] partial row maxima (fp16 bits)
   uint32_t pubs[16][17];    // [CTA][t] its row maxima (fp16 bits), [CTA][16] its outlier count
@@ -98,6 +101,7 @@ struct DecSmall {
   uint32_t mask[kDecMaskWords];  // outlier columns, bit b of word w = column 32 w + b
   uint8_t fpart[kDecConsumers];  // [row group][vector] outlier flags
   uint32_t xo[16 * kDecOutSmall];  // [t][j] X at the first outlier columns (fp16 bits)
+  uint32_t oc[kDecOutSmall];       // the first outlier columns
 };
 
 struct DecArgs {
@@ -173,7 +177,8 @@ __device__ __forceinline__ void dec_mma_range(const uint8_t *xs, const uint8_t *
 }
 
 template <int kC>
-__global__ void __launch_bounds__(kDecThreads, 1) dec_fused_kernel(const DecArgs p) {
+__global__ void __launch_bounds__(kDecThreads, 1)
+    dec_fused_kernel(const __grid_constant__ CUtensorMap tm_w16, const DecArgs p) {
   using G = DecAct<kC>;
   extern __shared__ __align__(128) uint8_t smem[];
   const int64_t K = p.K, pitch = dec_pitch(K), range = dec_range(K);
@@ -181,8 +186,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) dec_fused_kernel(const DecArgs
   uint8_t *xs = smem + p.wregion;                              // [16][pitch] activation codes
   uint16_t *ocols = reinterpret_cast<uint16_t *>(xs + 16 * pitch);  // outlier columns
   __shared__ DecSmall sm;
-  float *osm = sm.osm, *sxs = sm.sxs;
-  uint64_t *obar = &sm.obar;
+  float *sxs = sm.sxs;
   uint32_t *red = reinterpret_cast<uint32_t *>(smem);  // [16 warps][32][21], after the main loop
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -192,9 +196,11 @@ __global__ void __launch_bounds__(kDecThreads, 1) dec_fused_kernel(const DecArgs
 
   if (warp == kDecWarps && lane == 0) {
     mbar_init(&sm.wbar, 1);
-    mbar_init(obar, 32);
+    mbar_init(&sm.wobar, 1);
     mbar_init(&sm.pbar, 1);
     mbar_init(&sm.cbar, 1);
+    mbar_init(&sm.xbar, 1);
+    mbar_init(&sm.lbar, 32);
     mbar_init_fence();
   }
   __syncthreads();
@@ -235,7 +241,57 @@ __global__ void __launch_bounds__(kDecThreads, 1) dec_fused_kernel(const DecArgs
     for (int64_t r = lane; r < rows; r += 32)
       bulk_g2s(ws + r * pitch, p.Wq + (n0 + r) * K, (uint32_t)K, &sm.wbar);
     cluster_wait();
-  } else {
+    // W16 at the first outlier columns for this slice, as soon as the columns
+    // are known: one TMA box (8 columns x the slice's channels) per column.
+    // The copy engine serves these right behind the weight slice; plain loads
+    // issued now would wait behind the weight stream and the exchange traffic
+    // for several microseconds.  Then the whole ascending outlier list from
+    // the mask.  The consumers' waits are bounded, so wobar and lbar are
+    // signalled even after a wait gave up.
+    bool ok = mbar_wait_cluster_bounded(&sm.pbar, 0, p.status);
+    int32_t nO = 0;
+    if (ok)
+#pragma unroll
+      for (int c = 0; c < kC; c++) nO += (int32_t)sm.pubs[c][16];
+    const int32_t nsmall = min(nO, kDecOutSmall);
+    if (rows > 0) {
+      const bool fetch = ok && nsmall > 0 && mbar_wait_cluster_bounded(&sm.xbar, 0, p.status);
+      if (lane == 0)
+        mbar_expect_tx(&sm.wobar, fetch ? (uint32_t)(nsmall * 16 * p.rows_per_cta) : 0u);
+      __syncwarp();
+      if (fetch && lane < nsmall)
+        tma_load_2d(&sm.wos[lane][0][0], &tm_w16, (int32_t)(sm.oc[lane] & ~7u), (int32_t)n0,
+                    &sm.wobar);
+    }
+    ok = ok && mbar_wait_cluster_bounded(&sm.cbar, 0, p.status);
+    if (ok) {
+      const int64_t wpl = (words + 31) / 32;
+      const int64_t w0 = min(words, lane * wpl), w1 = min(words, w0 + wpl);
+      uint32_t cnt = 0;
+      for (int64_t w = w0; w < w1; w++) cnt += __popc(sm.mask[w]);
+      uint32_t incl = cnt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      uint32_t j = incl - cnt;
+      for (int64_t w = w0; w < w1; w++)
+        for (uint32_t m = sm.mask[w]; m; m &= m - 1) ocols[j++] = (uint16_t)(32 * w + __ffs(m) - 1);
+      __syncwarp();
+      if (blockIdx.x == 0) {
+        for (int32_t i = lane; i < nO; i += 32) p.O_out[i] = ocols[i];
+        if (lane == 0) *p.nO_out = (uint32_t)nO;
+      }
+    }
+    mbar_arrive(&sm.lbar);  // 32 arrivals: the list is complete (or a wait gave up)
+    if (rows > 0) {  // no copy outlives the CTA
+      (void)mbar_wait_bounded(&sm.wbar, 0, p.status);
+      (void)mbar_wait_bounded(&sm.wobar, 0, p.status);
+    }
+    return;
+  }
+  {
     // ---- activation pass 1: outlier columns and partial row maxima ----
     uint4 x[G::kRpt];
     uint32_t flags = 0;
@@ -327,12 +383,13 @@ __global__ void __launch_bounds__(kDecThreads, 1) dec_fused_kernel(const DecArgs
         for (int c = 0; c < kC; c++) m = max(m, sm.pubs[c][threadIdx.x]);
         sxs[threadIdx.x] = h2f_bits((int)threadIdx.x < T ? m : 0u);
       }
-      // bytes every CTA receives: the codes of all T rows, every mask word and
-      // the X values of the first outlier columns
-      const uint32_t incoming = (uint32_t)T * (uint32_t)K + 4u * (uint32_t)words +
-                                4u * (uint32_t)T * min(nO, (uint32_t)kDecOutSmall);
-      if (threadIdx.x == 0) mbar_expect_tx(&sm.cbar, incoming);
-      const uint32_t cbar = smem_addr(&sm.cbar);
+      // bytes every CTA receives: the codes of all T rows and every mask word
+      // (cbar); the first outlier columns and their X values (xbar)
+      if (threadIdx.x == 0) {
+        mbar_expect_tx(&sm.cbar, (uint32_t)T * (uint32_t)K + 4u * (uint32_t)words);
+        mbar_expect_tx(&sm.xbar, 4u * (1u + (uint32_t)T) * min(nO, (uint32_t)kDecOutSmall));
+      }
+      const uint32_t cbar = smem_addr(&sm.cbar), xbar = smem_addr(&sm.xbar);
       if (grp == 0) {  // mask word v/4 from the flags of vectors v .. v+3 (one CTA's)
         const uint32_t f1 = __shfl_down_sync(0xffffffffu, flags, 1);
         const uint32_t f2 = __shfl_down_sync(0xffffffffu, flags, 2);
@@ -344,9 +401,9 @@ __global__ void __launch_bounds__(kDecThreads, 1) dec_fused_kernel(const DecArgs
           for (int c = 0; c < kC; c++) st_async_b32(mapa(dst, c), word, mapa(cbar, c));
         }
       }
-      // X at the first outlier columns: this CTA's outliers sit at positions
-      // base.. of the ascending list, ordered by vector block, lane and bit.
-      // Every row group holds the same columns.
+      // The first outlier columns and their X values: this CTA's outliers sit
+      // at positions base.. of the ascending list, ordered by vector block,
+      // lane and bit.  Every row group holds the same columns.
       if (__any_sync(0xffffffffu, flags != 0)) {
         const uint32_t pc = __popc(flags);
         uint32_t incl = pc;
@@ -360,13 +417,18 @@ __global__ void __launch_bounds__(kDecThreads, 1) dec_fused_kernel(const DecArgs
           for (int w = 0; w < warp % G::kWpg; w++) j += sm.wcnt[w];
           for (int b = 0; b < 8 && j < (uint32_t)kDecOutSmall; b++)
             if ((flags >> b) & 1) {
+              if (grp == 0) {
+                const uint32_t dst = smem_addr(&sm.oc[j]);
+                for (int c = 0; c < kC; c++)
+                  st_async_b32(mapa(dst, c), (uint32_t)(8 * v + b), mapa(xbar, c));
+              }
 #pragma unroll
               for (int r = 0; r < G::kRpt; r++) {
                 const int t = grp + kC * r;
                 const uint32_t hb = ((&x[r].x)[b >> 1] >> (16 * (b & 1))) & 0xffffu;
                 if (t < T) {
                   const uint32_t dst = smem_addr(&sm.xo[t * kDecOutSmall + j]);
-                  for (int c = 0; c < kC; c++) st_async_b32(mapa(dst, c), hb, mapa(cbar, c));
+                  for (int c = 0; c < kC; c++) st_async_b32(mapa(dst, c), hb, mapa(xbar, c));
                 }
               }
               ++j;
@@ -403,76 +465,26 @@ __global__ void __launch_bounds__(kDecThreads, 1) dec_fused_kernel(const DecArgs
       }
     }
   }
-  // every CTA's codes, mask words and outlier X values are here (this also
-  // keeps the CTA alive until the last remote store into it has landed)
-  const bool have = mbar_wait_cluster_bounded(&sm.pbar, 0, p.status) &&
-                    mbar_wait_cluster_bounded(&sm.cbar, 0, p.status);
+  // every CTA's codes, mask words, first outlier columns and their X values
+  // are here (this also keeps the CTA alive until the last remote store into
+  // it has landed)
+  bool have = mbar_wait_cluster_bounded(&sm.pbar, 0, p.status);
   int32_t nO = 0;
   if (have)
 #pragma unroll
     for (int c = 0; c < kC; c++) nO += (int32_t)sm.pubs[c][16];
+  have = have && mbar_wait_cluster_bounded(&sm.cbar, 0, p.status) &&
+         mbar_wait_cluster_bounded(&sm.xbar, 0, p.status);
 
   if (blockIdx.x == 0) {  // the activation pass's results, for the debug entry point
     if (threadIdx.x < T) p.sx_out[threadIdx.x] = sxs[threadIdx.x];
     if (p.dbg_xq)
-      for (int64_t i = threadIdx.x; i < (int64_t)T * vecs; i += kDecThreads) {
+      for (int64_t i = threadIdx.x; i < (int64_t)T * vecs; i += kDecConsumers) {
         const int64_t t = i / vecs, vv = i - t * vecs;
         reinterpret_cast<uint2 *>(p.dbg_xq)[i] = *reinterpret_cast<const uint2 *>(xs + t * pitch + 8 * vv);
       }
   }
-  if (!have) {  // a bounded wait gave up (recorded in the status word)
-    if (warp == kDecWarps && rows > 0) (void)mbar_wait_bounded(&sm.wbar, 0, p.status);  // copies in flight
-    return;
-  }
-  if (rows <= 0) return;  // a cluster's last CTAs may have no output channels
-
-  if (warp == kDecWarps) {
-    // ---- producer warp: the ascending outlier list from the mask, then the
-    // first outlier columns for this slice, lane = channel ----
-    {
-      const int64_t wpl = (words + 31) / 32;
-      const int64_t w0 = min(words, lane * wpl), w1 = min(words, w0 + wpl);
-      uint32_t cnt = 0;
-      for (int64_t w = w0; w < w1; w++) cnt += __popc(sm.mask[w]);
-      uint32_t incl = cnt;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-      }
-      uint32_t j = incl - cnt;
-      for (int64_t w = w0; w < w1; w++)
-        for (uint32_t m = sm.mask[w]; m; m &= m - 1) ocols[j++] = (uint16_t)(32 * w + __ffs(m) - 1);
-      __syncwarp();
-      named_bar_arrive(3, kDecThreads);  // the list is complete for the consumers
-      if (blockIdx.x == 0) {
-        for (int32_t i = lane; i < nO; i += 32) p.O_out[i] = ocols[i];
-        if (lane == 0) *p.nO_out = (uint32_t)nO;
-      }
-    }
-    const int32_t nsmall = min(nO, kDecOutSmall);
-    for (int64_t rr = lane; rr < rows; rr += 32) {
-      float o[16];
-#pragma unroll
-      for (int t = 0; t < 16; t++) o[t] = 0.f;
-      const int64_t n = n0 + min(rr, rows - 1);
-      for (int32_t jb = 0; jb < nsmall; jb += 8) {
-        float wv[8];
-#pragma unroll
-        for (int e = 0; e < 8; e++)  // eight independent loads in flight
-          wv[e] = jb + e < nsmall ? h2f_bits(__ldg(p.W16 + n * K + ocols[jb + e])) : 0.f;
-#pragma unroll
-        for (int e = 0; e < 8; e++)
-#pragma unroll
-          for (int t = 0; t < 16; t++)
-            if (t < T && jb + e < nsmall) o[t] = fmaf(h2f_bits(sm.xo[t * kDecOutSmall + jb + e]), wv[e], o[t]);
-      }
-#pragma unroll
-      for (int t = 0; t < 16; t++) osm[t * kDecMaxRows + rr] = o[t];
-    }
-    mbar_arrive(obar);  // 32 arrivals: osm is written
-    return;
-  }
+  if (!have || rows <= 0) return;  // a wait gave up (status word), or no channels here
 
   // ---- consumer warps: K-range [k0, k1) for every 8-channel group ----
   const int g = lane >> 2, q = lane & 3;
@@ -499,11 +511,12 @@ __global__ void __launch_bounds__(kDecThreads, 1) dec_fused_kernel(const DecArgs
     else
       dec_mma_range<true>(xs, ws, pitch, g, q, k0, k1, ng, acc);
   }
-  // outlier columns beyond the first kDecOutSmall: split over the consumer warps
-  named_bar_sync(3, kDecThreads);  // the producer has listed them
-  const bool big = nO > kDecOutSmall;  // the same in every warp
+  // outlier columns beyond the first kDecOutSmall: split over the consumer
+  // warps, from the producer warp's list
+  const bool big = nO > kDecOutSmall &&  // the same in every warp
+                   mbar_wait_bounded(&sm.lbar, 0, p.status);
   float o[kDecGroups][4] = {};
-  for (int32_t j = kDecOutSmall + warp; j < nO; j += kDecWarps) {
+  for (int32_t j = kDecOutSmall + warp; big && j < nO; j += kDecWarps) {
     const int64_t k = ocols[j];
     const float x0 = g < T ? h2f_bits(__ldg(p.X16 + (int64_t)g * K + k)) : 0.f;
     const float x1 = g + 8 < T ? h2f_bits(__ldg(p.X16 + (int64_t)(g + 8) * K + k)) : 0.f;
@@ -556,14 +569,22 @@ __global__ void __launch_bounds__(kDecThreads, 1) dec_fused_kernel(const DecArgs
           e_out[it] += __uint_as_float(red[(w * 32 + el) * kDecRedStride + idx]);
       }
   }
-  const bool ok_o = mbar_wait_bounded(obar, 0, p.status);
+  // the first outlier columns: X from the exchange, W16 from the TMA boxes
+  const int nsmall = nO < kDecOutSmall ? nO : kDecOutSmall;
+  const bool ok_o = mbar_wait_bounded(&sm.wobar, 0, p.status);
+#pragma unroll
+  for (int it = 0; it < 2; it++)
+    if (it < nitems && e_n[it] < rows)
+      for (int j = 0; j < nsmall; j++)
+        e_out[it] = fmaf(h2f_bits(sm.xo[e_t[it] * kDecOutSmall + j]),
+                         h2f_bits(sm.wos[j][e_n[it]][sm.oc[j] & 7u]), e_out[it]);
 #pragma unroll
   for (int it = 0; it < 2; it++) {
     const int t = e_t[it], nl = e_n[it];
     if (it < nitems && t < T && nl < rows && ok_o) {
       const int64_t n = n0 + nl;
       const float st = sxs[t] / 127.0f, sn = e_sw[it] / 127.0f;
-      const float y = fmaf((float)e_acc[it] * st, sn, e_out[it] + osm[t * kDecMaxRows + nl]);
+      const float y = fmaf((float)e_acc[it] * st, sn, e_out[it]);
       p.Y[t * p.N + n] = __float2half_rn(y);
       if (p.dbg_acc) p.dbg_acc[t * p.N + n] = e_acc[it];
     }
@@ -700,6 +721,13 @@ cudaError_t launch_decode(const void *X, int64_t T, int64_t K, uint32_t thr, con
   const int64_t used = (N + a.rows_per_cta - 1) / a.rows_per_cta;
   const int64_t ctas = (used + kc - 1) / kc * kc;
   a.wregion = dec_wregion(K, a.rows_per_cta);
+  // W16 in boxes of 8 columns x one slice's channels (outlier columns only,
+  // so no L2 promotion beyond the sector)
+  CUtensorMap tm;
+  if (!encode_2d(&tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, W16, (uint64_t)K, (uint64_t)N,
+                 (uint64_t)K * 2, 8, (uint32_t)a.rows_per_cta, CU_TENSOR_MAP_SWIZZLE_NONE,
+                 CU_TENSOR_MAP_L2_PROMOTION_NONE))
+    return cudaErrorInvalidValue;
   a.Wq = Wq;
   a.sw = sw;
   a.W16 = reinterpret_cast<const unsigned short *>(W16);
@@ -725,9 +753,9 @@ cudaError_t launch_decode(const void *X, int64_t T, int64_t K, uint32_t thr, con
   cfg.attrs = attr;
   cfg.numAttrs = profile_only_main() ? 1 : 2;  // profiling mode 2: no overlap with the previous call
   ProfScope ps(kKidDecFused, stream);
-  const cudaError_t e = kc == 8    ? cudaLaunchKernelEx(&cfg, dec_fused_kernel<8>, a)
-                        : kc == 16 ? cudaLaunchKernelEx(&cfg, dec_fused_kernel<16>, a)
-                                   : cudaLaunchKernelEx(&cfg, dec_fused_kernel<4>, a);
+  const cudaError_t e = kc == 8    ? cudaLaunchKernelEx(&cfg, dec_fused_kernel<8>, tm, a)
+                        : kc == 16 ? cudaLaunchKernelEx(&cfg, dec_fused_kernel<16>, tm, a)
+                                   : cudaLaunchKernelEx(&cfg, dec_fused_kernel<4>, tm, a);
   note_launch();
   return e;
 }

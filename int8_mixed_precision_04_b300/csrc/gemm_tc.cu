@@ -43,9 +43,6 @@
 // leave, after which in-flight copies and MMAs are waited for and tensor
 // memory is freed.
 #include <cuda.h>
-#include <cudaTypedefs.h>
-
-#include <mutex>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -452,35 +449,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ---- host side ----------------------------------------------------------------
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void *ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-  });
-  return fn;
-}
-
-// 2-D row-major tensor [outer x inner] with `row_bytes` between rows.
-bool encode_2d(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint64_t inner,
-               uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
-               CUtensorMapSwizzle swz) {
-  auto fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[2] = {inner, outer};
-  cuuint64_t strides[1] = {row_bytes};
-  cuuint32_t box[2] = {box_inner, box_outer};
-  cuuint32_t estr[2] = {1, 1};
-  return fn(m, dt, 2, const_cast<void *>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 }  // namespace
 
 cudaError_t launch_gemm_tc(int64_t T, int64_t K, const int8_t *Wq, const float *sw,
@@ -495,16 +463,16 @@ cudaError_t launch_gemm_tc(int64_t T, int64_t K, const int8_t *Wq, const float *
   }
   CUtensorMap tm_x, tm_w, tm_xo, tm_w16, tm_w16o;
   if (!encode_2d(&tm_x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, ws.xcodes, (uint64_t)K, (uint64_t)T,
-                 (uint64_t)K * 2, kBK, kBN, CU_TENSOR_MAP_SWIZZLE_128B) ||
+                 (uint64_t)K * 2, kBK, kBN, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B) ||
       !encode_2d(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, Wq, (uint64_t)K, (uint64_t)N, (uint64_t)K,
-                 kBK, kBM, CU_TENSOR_MAP_SWIZZLE_64B) ||
+                 kBK, kBM, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B) ||
       // the outlier block's inner extent is K (columns past K read as zeros)
       !encode_2d(&tm_xo, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, ws.xo, (uint64_t)K, (uint64_t)T,
-                 (uint64_t)ws.kpad * 2, kBK, kBN, CU_TENSOR_MAP_SWIZZLE_128B) ||
+                 (uint64_t)ws.kpad * 2, kBK, kBN, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B) ||
       !encode_2d(&tm_w16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, W16, (uint64_t)K, (uint64_t)N,
-                 (uint64_t)K * 2, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B) ||
+                 (uint64_t)K * 2, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B) ||
       !encode_2d(&tm_w16o, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, ws.w16o, (uint64_t)ws.opad,
-                 (uint64_t)N, (uint64_t)ws.opad * 2, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B))
+                 (uint64_t)N, (uint64_t)ws.opad * 2, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B))
     return cudaErrorInvalidValue;
   TcArgs a;
   a.T = T;

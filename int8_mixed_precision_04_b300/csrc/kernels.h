@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -10,6 +11,13 @@ namespace bnb {
 
 // Process-wide count of kernel launches issued by this library.
 void note_launch();
+
+// Tensor map of a 2-D row-major tensor [outer x inner] with `row_bytes`
+// between rows, loaded in boxes of box_outer x box_inner elements (false if
+// the driver entry point is missing or rejects the layout).
+bool encode_2d(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint64_t inner,
+               uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
+               CUtensorMapSwizzle swz, CUtensorMapL2promotion l2);
 
 // Kernel ids of the per-kernel event timing (names in profile.cu).
 enum KernelId {
