@@ -475,6 +475,8 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     for (int c = 0; c < kC; c++) nO += (int32_t)sm.pubs[c][16];
   have = have && mbar_wait_cluster_bounded(&sm.cbar, 0, p.status) &&
          mbar_wait_cluster_bounded(&sm.xbar, 0, p.status);
+  // the same outcome for every consumer thread: named barriers follow
+  have = named_bar_and(1, kDecConsumers, have);
 
   if (blockIdx.x == 0) {  // the activation pass's results, for the debug entry point
     if (threadIdx.x < T) p.sx_out[threadIdx.x] = sxs[threadIdx.x];
