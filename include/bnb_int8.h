@@ -176,8 +176,9 @@ uint64_t bnb_launch_count(void);
 
 /*
  * Which kernel path bnb_int8_linear takes for a shape on the current device:
- * 1 = decode (T <= 16, K <= 4608, N <= 32 x SMs), 2 = tensor-core GEMM
- * (tcgen05), 3 = warp-level mma GEMM.
+ * 1 = decode (T <= 16, K <= 4096 and N within what the decode kernel's
+ * resident CTAs hold at up to 40 output channels each: 4620 at K = 4096 on
+ * B300), 2 = tensor-core GEMM (tcgen05), 3 = warp-level mma GEMM.
  */
 int bnb_int8_linear_path(int64_t T, int64_t N, int64_t K);
 
