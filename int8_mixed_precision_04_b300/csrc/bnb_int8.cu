@@ -187,13 +187,10 @@ static bnb_status_t linear_impl(const void *X, int64_t T, int64_t K, const int8_
       }
       note_launch();
       // the tcgen05 GEMM reads fp16 integer codes, the mma GEMM int8 codes
+      // (for the tcgen05 GEMM the same launch compacts W16 at a sparse outlier set)
       e = launch_act_pass(X, T, K, thr, ws, /*code_mode=*/path == 2 ? 1 : 0, /*with_xo=*/true,
-                          dbg_xq, device_sms(dev), stream);
+                          W16, N, dbg_xq, device_sms(dev), stream);
       if (e != cudaSuccess) return BNB_ERR_CUDA;
-      if (path == 2) {  // W16 at a sparse outlier set, compacted once per call
-        e = launch_gather_outlier_weights(W16, N, K, ws, device_sms(dev), stream);
-        if (e != cudaSuccess) return BNB_ERR_CUDA;
-      }
     }
     if (path == 2)
       e = launch_gemm_tc(T, K, Wq, Wscale, W16, N, Y, ws, dbg_acc, device_sms(dev), stream);

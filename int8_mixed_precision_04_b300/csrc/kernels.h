@@ -28,7 +28,6 @@ enum KernelId {
   kKidGemmMma,
   kKidGemmTc,
   kKidQuantWeight,
-  kKidGatherW16,
   kKernelCount
 };
 
@@ -57,14 +56,8 @@ cudaError_t launch_quantize_weight(const void *W16, int64_t N, int64_t K, int8_t
 // S2 + S3.  code_mode 0: int8 codes, 1: fp16 integer codes.  with_xo: write
 // the padded fp16 outlier block.
 cudaError_t launch_act_pass(const void *X, int64_t T, int64_t K, uint32_t thr_bits,
-                            const Workspace &ws, int code_mode, bool with_xo,
-                            int8_t *dbg_xq, int num_sms, cudaStream_t stream);
-
-// W16[n, O[j]] for a sparse outlier set (outlier_block_dense false) into the
-// workspace's compacted block w16o [N x opad], zero past |O|; nothing when
-// the outlier set is dense.
-cudaError_t launch_gather_outlier_weights(const void *W16, int64_t N, int64_t K,
-                                          const Workspace &ws, int num_sms, cudaStream_t stream);
+                            const Workspace &ws, int code_mode, bool with_xo, const void *W16,
+                            int64_t N, int8_t *dbg_xq, int num_sms, cudaStream_t stream);
 
 // The whole layer for T <= 16, K <= kDecodeMaxK, N <= decode_max_n(dev, K)
 // in one kernel (activation pass fused into the GEMV and shared by clusters

@@ -9,7 +9,7 @@ namespace bnb {
 
 static const char *const kKernelNames[kKernelCount] = {
     "memset_status_mask", "outlier_scan", "quantize_rows", "dec_fused",
-    "gemm_mma",           "gemm_tc",      "quantize_weight", "gather_outlier_weights"};
+    "gemm_mma",           "gemm_tc",      "quantize_weight"};
 
 namespace {
 struct Rec {

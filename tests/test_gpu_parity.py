@@ -60,6 +60,18 @@ def test_ragged_shapes(orc, T, K, N, ncols, tau):
     run_and_compare(orc, w.X, w.W, tau, what=f"T{T} K{K} N{N} tau{tau}")
 
 
+@pytest.mark.parametrize("T,K,N,ncols,tau", [
+    (300, 1024, 200, 5, 6.0), (149, 4096, 96, 70, 6.0), (40, 2048, 64, 3, 0.0),
+    (700, 512, 130, 40, 3.0), (17, 256, 300, 1, 6.0), (33, 16384, 64, 9, 6.0),
+])
+def test_act_pass_forms(orc, T, K, N, ncols, tau):
+    """The GEMM path's activation pass: rows held in registers (K <= 8192) and
+    read twice (K = 16384), sparse outlier blocks with the W16 gather, dense
+    outlier blocks, and as many W16 rows as tokens or many more."""
+    w = inputs.random_small(T, K, N, ncols, seed=T + K + ncols, tau=tau)
+    run_and_compare(orc, w.X, w.W, tau, what=f"act pass T{T} K{K} tau{tau}")
+
+
 @pytest.mark.parametrize("T", [5, 40])
 def test_edge_rows(orc, T):
     """An all-zero row, a row whose every column is an outlier, a value exactly
