@@ -127,6 +127,29 @@ bnb_status_t bnb_int8_linear_debug(const void *X, int64_t T, int64_t K,
                                    int32_t *acc);
 
 /*
+ * bnb_int8_linear with the activations and the result in host memory: on
+ * `stream`, copies X from X_host into X_dev, runs bnb_int8_linear(X_dev ->
+ * Y_dev) and copies Y_dev back into Y_host, so that one call moves a step's
+ * input in and its result out.  The pages have no counterpart to this entry
+ * point; the layer itself is bnb_int8_linear, unchanged.
+ *   X_host [T x K] fp16 and Y_host [T x N] fp16: host memory.  Page-locked
+ *          (pinned) memory makes both copies asynchronous; with pageable
+ *          memory the CUDA runtime stages them and the call may block.  The
+ *          caller keeps X_host unchanged and Y_host unread until the stream
+ *          has passed this call.
+ *   X_dev [T x K] and Y_dev [T x N]: device buffers the caller owns (the
+ *          same rules as X and Y of bnb_int8_linear; they must not overlap).
+ *   Other arguments and errors as for bnb_int8_linear, plus
+ *   BNB_ERR_INVALID_ARG for a NULL host or device buffer.  Argument errors
+ *   are detected before anything is enqueued.
+ */
+bnb_status_t bnb_int8_linear_from_host(const void *X_host, int64_t T, int64_t K,
+                                       const int8_t *Wq, const float *Wscale, const void *W16,
+                                       int64_t N, float tau, void *Y_host, void *X_dev,
+                                       void *Y_dev, void *workspace, size_t workspace_bytes,
+                                       void *stream);
+
+/*
  * Synchronises `stream`, then reads the device status word of `workspace`
  * into *out (BNB_OK, or BNB_ERR_TIMEOUT after a bounded wait gave up) and
  * clears it.  Returns BNB_ERR_CUDA if the synchronisation or copy failed.

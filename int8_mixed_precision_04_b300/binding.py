@@ -41,7 +41,8 @@ class Lib:
                "bnb_int8_linear", "bnb_int8_linear_debug", "bnb_last_device_status",
                "bnb_status_string", "bnb_launch_count", "bnb_int8_linear_path",
                "bnb_profile_enable", "bnb_profile_collect", "bnb_profile_kernel_count",
-               "bnb_profile_kernel_name", "bnb_int8_linear_noalloc")
+               "bnb_profile_kernel_name", "bnb_int8_linear_noalloc",
+               "bnb_int8_linear_from_host")
 
     def __init__(self, path: str = LIB_PATH):
         if not os.path.exists(path):
@@ -61,6 +62,9 @@ class Lib:
         L.bnb_int8_linear_noalloc.restype = ctypes.c_int
         L.bnb_int8_linear_noalloc.argtypes = [_P, _I64, _I64, _P, _P, _P, _I64, ctypes.c_float,
                                               _P, _P]
+        L.bnb_int8_linear_from_host.restype = ctypes.c_int
+        L.bnb_int8_linear_from_host.argtypes = [_P, _I64, _I64, _P, _P, _P, _I64, ctypes.c_float,
+                                                _P, _P, _P, _P, ctypes.c_size_t, _P]
         L.bnb_last_device_status.restype = ctypes.c_int
         L.bnb_last_device_status.argtypes = [_P, _P, ctypes.POINTER(ctypes.c_int32)]
         L.bnb_status_string.restype = ctypes.c_char_p
@@ -145,6 +149,20 @@ def linear(X, Wq, Wscale, W16, tau: float, Y=None, workspace=None, stream=None):
                                 _stream(stream))
     _check(rc, "bnb_int8_linear")
     return Y
+
+
+def linear_from_host(X_host, Wq, Wscale, W16, tau: float, Y_host, X_dev, Y_dev, workspace,
+                     stream=None):
+    """bnb_int8_linear_from_host: X_host [T,K] fp16 (pinned cpu tensor) -> Y_host
+    [T,N] fp16 (pinned cpu tensor), through the caller's device buffers X_dev,
+    Y_dev and workspace, all enqueued on `stream`."""
+    T, K = X_host.shape
+    N = Wq.shape[0]
+    rc = load().bnb_int8_linear_from_host(_ptr(X_host), T, K, _ptr(Wq), _ptr(Wscale), _ptr(W16),
+                                          N, float(tau), _ptr(Y_host), _ptr(X_dev), _ptr(Y_dev),
+                                          _ptr(workspace), workspace.numel(), _stream(stream))
+    _check(rc, "bnb_int8_linear_from_host")
+    return Y_host
 
 
 def linear_noalloc(X, Wq, Wscale, W16, tau: float, Y=None, stream=None):

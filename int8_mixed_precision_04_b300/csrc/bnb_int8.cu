@@ -143,11 +143,10 @@ static int choose_path(int64_t T, int64_t N, int64_t K, int dev) {
   return force_mma() ? 3 : 2;
 }
 
-static bnb_status_t linear_impl(const void *X, int64_t T, int64_t K, const int8_t *Wq,
-                                const float *Wscale, const void *W16, int64_t N, float tau,
-                                void *Y, void *workspace, size_t workspace_bytes,
-                                void *stream_v, int8_t *dbg_xq, float *dbg_sx,
-                                int32_t *dbg_O, int32_t *dbg_nO, int32_t *dbg_acc) {
+// The argument checks of bnb_int8_linear (nothing is enqueued).
+static bnb_status_t linear_check(const void *X, int64_t T, int64_t K, const int8_t *Wq,
+                                 const float *Wscale, const void *W16, int64_t N, float tau,
+                                 const void *Y, const void *workspace, size_t workspace_bytes) {
   if (!X || !Wq || !Wscale || !W16 || !Y || !workspace) return BNB_ERR_INVALID_ARG;
   if (T <= 0 || N <= 0 || K <= 0) return BNB_ERR_INVALID_ARG;
   if (std::isnan(tau) || tau < 0.0f) return BNB_ERR_INVALID_ARG;
@@ -157,12 +156,22 @@ static bnb_status_t linear_impl(const void *X, int64_t T, int64_t K, const int8_
   if (!aligned16(X) || !aligned16(Wq) || !aligned16(Wscale) || !aligned16(W16) ||
       !aligned16(Y) || !aligned16(workspace))
     return BNB_ERR_UNSUPPORTED;
-  if ((dbg_xq && !aligned16(dbg_xq)) || (dbg_acc && !aligned16(dbg_acc)))
-    return BNB_ERR_UNSUPPORTED;
   const size_t ybytes = (size_t)T * (size_t)N * 2;
   if (overlaps(Y, ybytes, X, (size_t)T * K * 2) || overlaps(Y, ybytes, W16, (size_t)N * K * 2) ||
       overlaps(Y, ybytes, Wq, (size_t)N * K) || overlaps(Y, ybytes, workspace, workspace_bytes))
     return BNB_ERR_INVALID_ARG;
+  return BNB_OK;
+}
+
+static bnb_status_t linear_impl(const void *X, int64_t T, int64_t K, const int8_t *Wq,
+                                const float *Wscale, const void *W16, int64_t N, float tau,
+                                void *Y, void *workspace, size_t workspace_bytes,
+                                void *stream_v, int8_t *dbg_xq, float *dbg_sx,
+                                int32_t *dbg_O, int32_t *dbg_nO, int32_t *dbg_acc) {
+  bnb_status_t chk = linear_check(X, T, K, Wq, Wscale, W16, N, tau, Y, workspace, workspace_bytes);
+  if (chk != BNB_OK) return chk;
+  if ((dbg_xq && !aligned16(dbg_xq)) || (dbg_acc && !aligned16(dbg_acc)))
+    return BNB_ERR_UNSUPPORTED;
   int dev = 0;
   bnb_status_t st = check_device(&dev);
   if (st != BNB_OK) return st;
@@ -238,6 +247,30 @@ bnb_status_t bnb_int8_linear(const void *X, int64_t T, int64_t K, const int8_t *
                              void *Y, void *workspace, size_t workspace_bytes, void *stream) {
   return linear_impl(X, T, K, Wq, Wscale, W16, N, tau, Y, workspace, workspace_bytes, stream,
                      nullptr, nullptr, nullptr, nullptr, nullptr);
+}
+
+bnb_status_t bnb_int8_linear_from_host(const void *X_host, int64_t T, int64_t K,
+                                       const int8_t *Wq, const float *Wscale, const void *W16,
+                                       int64_t N, float tau, void *Y_host, void *X_dev,
+                                       void *Y_dev, void *workspace, size_t workspace_bytes,
+                                       void *stream) {
+  if (!X_host || !Y_host || !X_dev || !Y_dev) return BNB_ERR_INVALID_ARG;
+  if (T <= 0 || K <= 0 || N <= 0) return BNB_ERR_INVALID_ARG;
+  const size_t xbytes = (size_t)T * (size_t)K * 2, ybytes = (size_t)T * (size_t)N * 2;
+  if (overlaps(X_dev, xbytes, Y_dev, ybytes)) return BNB_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  // the layer's own argument checks run before anything is enqueued
+  bnb_status_t r = linear_check(X_dev, T, K, Wq, Wscale, W16, N, tau, Y_dev, workspace,
+                                workspace_bytes);
+  if (r != BNB_OK) return r;
+  if (cudaMemcpyAsync(X_dev, X_host, xbytes, cudaMemcpyHostToDevice, st) != cudaSuccess)
+    return BNB_ERR_CUDA;
+  r = linear_impl(X_dev, T, K, Wq, Wscale, W16, N, tau, Y_dev, workspace, workspace_bytes,
+                  stream, nullptr, nullptr, nullptr, nullptr, nullptr);
+  if (r != BNB_OK) return r;
+  if (cudaMemcpyAsync(Y_host, Y_dev, ybytes, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return BNB_ERR_CUDA;
+  return BNB_OK;
 }
 
 bnb_status_t bnb_int8_linear_debug(const void *X, int64_t T, int64_t K, const int8_t *Wq,

@@ -123,3 +123,27 @@ def test_paths(lib):
 def test_missing_library_raises(tmp_path):
     with pytest.raises(FileNotFoundError):
         binding.Lib(str(tmp_path / "nope.so"))
+
+
+@pytest.mark.parametrize("case,want", [
+    (dict(xh=None), binding.Status.INVALID_ARG),
+    (dict(yh=None), binding.Status.INVALID_ARG),
+    (dict(xd=None), binding.Status.INVALID_ARG),
+    (dict(yd=None), binding.Status.INVALID_ARG),
+    (dict(yd=FAKE * 64 + 16), binding.Status.INVALID_ARG),   # Y_dev overlaps X_dev
+    (dict(T=0), binding.Status.INVALID_ARG),
+    (dict(tau=-1.0), binding.Status.INVALID_ARG),
+    (dict(K=250), binding.Status.UNSUPPORTED),
+])
+def test_from_host_rejects_on_host(lib, case, want):
+    """bnb_int8_linear_from_host checks its buffers and the layer's arguments
+    before enqueuing a copy."""
+    a = dict(xh=FAKE, T=16, K=256, N=256, tau=6.0, yh=FAKE * 2, xd=FAKE * 64,
+             yd=FAKE * 96, ws=FAKE * 256)
+    a.update(case)
+    T, K, N = a["T"], a["K"], a["N"]
+    ws_bytes = lib.bnb_int8_linear_workspace_bytes(T, N, K) if min(T, K, N) > 0 else 0
+    rc = lib.bnb_int8_linear_from_host(a["xh"], T, K, FAKE, FAKE, FAKE, N,
+                                       ctypes.c_float(a["tau"]), a["yh"], a["xd"], a["yd"],
+                                       a["ws"], ws_bytes, None)
+    assert rc == want

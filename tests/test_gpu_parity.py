@@ -135,6 +135,36 @@ def test_workspace_reuse(orc):
         check_y(Y.cpu().numpy(), ref["Y"], f"reuse tau={tau}")
 
 
+@pytest.mark.parametrize("T,K,N", [(16, 4096, 4096), (300, 1024, 200)])
+def test_from_host(orc, T, K, N):
+    """bnb_int8_linear_from_host (pinned host X in, pinned host Y out, on two
+    streams in turn) gives the oracle's Y and exactly bnb_int8_linear's."""
+    import torch
+
+    from int8_mixed_precision_04_b300 import binding
+    from parity import check_y
+    w = inputs.random_small(T, K, N, 4, seed=T + N)
+    W = torch.from_numpy(w.W).cuda()
+    Wq, sw = binding.quantize_weight(W)
+    Y_ref = binding.linear(torch.from_numpy(w.X).cuda(), Wq, sw, W, 6.0).cpu()
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    outs = []
+    for i in range(4):
+        Xh = torch.from_numpy(w.X).pin_memory()
+        Yh = torch.empty((T, N), dtype=torch.float16).pin_memory()
+        Xd = torch.empty((T, K), dtype=torch.float16, device="cuda")
+        Yd = torch.empty((T, N), dtype=torch.float16, device="cuda")
+        ws = torch.empty(binding.workspace_bytes(T, N, K), dtype=torch.uint8, device="cuda")
+        binding.linear_from_host(Xh, Wq, sw, W, 6.0, Yh, Xd, Yd, ws, stream=streams[i % 2])
+        outs.append((Yh, Xd, Yd, ws))
+    torch.cuda.synchronize()
+    Wq_o, sw_o = orc.quantize_weight(w.W)
+    ref = orc.linear(w.X, Wq_o, sw_o, w.W, 6.0)
+    for Yh, *_ in outs:
+        assert torch.equal(Yh, Y_ref)
+        check_y(Yh.numpy(), ref["Y"], f"from host T{T}")
+
+
 @pytest.mark.parametrize("frac", inputs.SWEEP_FRACTIONS)
 @pytest.mark.parametrize("tau", inputs.SWEEP_TAUS)
 def test_sweep_reduced(orc, frac, tau):
