@@ -52,7 +52,7 @@ class Oracle:
         lib.orc_double_to_half.argtypes = [ctypes.c_double]
         for name in ("orc_quantize_weight", "orc_outlier_columns",
                      "orc_quantize_activations", "orc_int8_matmul_rows",
-                     "orc_linear_rows"):
+                     "orc_linear_rows", "orc_quantize_blockwise", "orc_dequantize_blockwise"):
             getattr(lib, name).restype = ctypes.c_int
         self.lib = lib
 
@@ -65,6 +65,27 @@ class Oracle:
 
     def double_to_half(self, v: float) -> int:
         return self.lib.orc_double_to_half(v)
+
+    # ---- the blockwise 8-bit codec of optimizer states ---------------------------
+    def quantize_blockwise(self, x: np.ndarray, block: int):
+        """fp32 values -> (int8 codes, fp32 absmax per block of ``block``)."""
+        x = np.ascontiguousarray(x, dtype=np.float32).ravel()
+        n = x.size
+        q = np.empty(n, np.int8)
+        absmax = np.empty((n + block - 1) // block, np.float32)
+        rc = self.lib.orc_quantize_blockwise(_ptr(x), _I64(n), _I64(block), _ptr(q),
+                                             _ptr(absmax))
+        assert rc == 0, rc
+        return q, absmax
+
+    def dequantize_blockwise(self, q: np.ndarray, absmax: np.ndarray, block: int):
+        q = np.ascontiguousarray(q, dtype=np.int8).ravel()
+        absmax = np.ascontiguousarray(absmax, dtype=np.float32)
+        y = np.empty(q.size, np.float32)
+        rc = self.lib.orc_dequantize_blockwise(_ptr(q), _ptr(absmax), _I64(q.size),
+                                               _I64(block), _ptr(y))
+        assert rc == 0, rc
+        return y
 
     # ---- S1 -------------------------------------------------------------------
     def quantize_weight(self, W16: np.ndarray):

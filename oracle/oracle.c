@@ -234,3 +234,48 @@ int orc_linear_rows(const uint16_t *X, int64_t T, int64_t K, const int8_t *Wq,
   orc_dequant_rows(acc, sx, sw, out, rows, nrows, N, Y);
   return rc;
 }
+
+/* ---- the blockwise 8-bit codec of optimizer states ----
+ * 8-bit optimizers keep their states quantized block-wise ("bitsandbytes:
+ * GPU-Accelerated Inference and Training at Lower Bit Depths", section
+ * "8-bit optimizers for full-model training"); each block carries its own
+ * scaling factor, which limits what one outlier does to its neighbours (page
+ * "bitsandbytes", section "What it provides").  Readings (the pages give no
+ * block size and no code map): fp32 values in blocks of B consecutive
+ * elements (the last block may be short), the block's scale is its absmax
+ * a, the code is q = rint(fl32(fl32(127 * x) / a)) in IEEE fp32, ties to
+ * even (0 when a = 0), and the decoded value is fl32(fl32(q * a) / 127). */
+int orc_quantize_blockwise(const float *x, int64_t n, int64_t B, int8_t *q, float *absmax) {
+  if (n < 0 || B <= 0) return ORC_ERR_ARG;
+  const int64_t nb = (n + B - 1) / B;
+#pragma omp parallel for schedule(static)
+  for (int64_t b = 0; b < nb; b++) {
+    const int64_t i0 = b * B, i1 = i0 + B < n ? i0 + B : n;
+    float a = 0.0f;
+    for (int64_t i = i0; i < i1; i++) {
+      const float v = fabsf(x[i]);
+      if (v > a) a = v;
+    }
+    absmax[b] = a;
+    for (int64_t i = i0; i < i1; i++) {
+      if (a == 0.0f) {
+        q[i] = 0;
+      } else {
+        const float num = 127.0f * x[i];
+        q[i] = (int8_t)rintf(num / a);
+      }
+    }
+  }
+  return ORC_OK;
+}
+
+int orc_dequantize_blockwise(const int8_t *q, const float *absmax, int64_t n, int64_t B,
+                             float *y) {
+  if (n < 0 || B <= 0) return ORC_ERR_ARG;
+#pragma omp parallel for schedule(static)
+  for (int64_t i = 0; i < n; i++) {
+    const float prod = (float)q[i] * absmax[i / B];
+    y[i] = prod / 127.0f;
+  }
+  return ORC_OK;
+}

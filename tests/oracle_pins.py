@@ -265,6 +265,106 @@ def pin_hand_example(orc):
     assert r["Y"].astype(np.float64).tolist() == want
 
 
+
+# ---------------------------------------------------------------------------
+# the blockwise 8-bit codec of optimizer states
+# ---------------------------------------------------------------------------
+
+def _bw_closed_form_blocks(rng, nblocks, B):
+    """Blocks whose absmax is +-127 * 2^e; every other value is k * 2^e (code
+    k, decodes to itself) or (k + 1/2) * 2^e (an exact tie: the even
+    neighbour).  Returns values, codes and decoded values fixed by that."""
+    xs, qs, ys = [], [], []
+    for _ in range(nblocks):
+        e = int(rng.integers(-30, 30))
+        s = 2.0 ** e
+        sign = 1 if rng.integers(0, 2) else -1
+        k = rng.integers(-126, 127, size=B - 1)
+        tie = rng.integers(0, 2, size=B - 1).astype(bool)
+        vals = np.where(tie, (k + 0.5) * s, k * s)
+        codes = np.where(tie, np.where(k % 2 == 0, k, k + 1), k)
+        pos = int(rng.integers(0, B))
+        xs.append(np.insert(vals, pos, sign * 127 * s))
+        qs.append(np.insert(codes, pos, sign * 127))
+        ys.append(np.insert(codes * s, pos, sign * 127 * s))
+    return (np.concatenate(xs).astype(np.float32), np.concatenate(qs).astype(np.int64),
+            np.concatenate(ys).astype(np.float32))
+
+
+def pin_blockwise_closed_forms(orc):
+    """Exact quotients give their integer code and decode to themselves;
+    exact ties round to the even neighbour; the absmax has code +-127."""
+    rng = np.random.default_rng(11)
+    for B in (64, 256):
+        x, q_want, y_want = _bw_closed_form_blocks(rng, 24, B)
+        q, a = orc.quantize_blockwise(x, B)
+        assert np.array_equal(q.astype(np.int64), q_want)
+        assert np.array_equal(a, np.abs(x).reshape(-1, B).max(axis=1))
+        y = orc.dequantize_blockwise(q, a, B)
+        assert np.array_equal(y, y_want)
+
+
+def pin_blockwise_error_bound(orc):
+    """Random states with a different magnitude per block and a short last
+    block: each block's scale is its absmax, codes stay within +-127 and reach
+    it in every nonzero block, and every decoded value is within half a code
+    step (a / 254) of the value, up to fp32 rounding."""
+    rng = np.random.default_rng(12)
+    B, n = 128, 128 * 37 + 45
+    mag = 10.0 ** rng.uniform(-8, 3, size=(n + B - 1) // B)
+    x = (rng.standard_normal(n) * np.repeat(mag, B)[:n]).astype(np.float32)
+    q, a = orc.quantize_blockwise(x, B)
+    y = orc.dequantize_blockwise(q, a, B)
+    for b in range(a.size):
+        xb = x[b * B:(b + 1) * B]
+        assert a[b] == np.abs(xb).max()
+        qb = q[b * B:(b + 1) * B].astype(np.int64)
+        assert np.abs(qb).max() == 127
+        err = np.abs(y[b * B:(b + 1) * B].astype(np.float64) - xb.astype(np.float64))
+        assert err.max() <= float(a[b]) * (1 / 254 + 1e-6)
+
+
+def pin_blockwise_locality(orc):
+    """Each block carries its own scale, which limits what one outlier does to
+    its neighbours (page "bitsandbytes", section "What it provides"): a value
+    made 1000 times larger changes its own block's scale and codes only."""
+    rng = np.random.default_rng(13)
+    B = 256
+    x = rng.standard_normal(B * 9).astype(np.float32)
+    q0, a0 = orc.quantize_blockwise(x, B)
+    x2 = x.copy()
+    x2[4 * B + 17] *= 1000
+    q1, a1 = orc.quantize_blockwise(x2, B)
+    changed = {i // B for i in np.nonzero(q0 != q1)[0]} | set(np.nonzero(a0 != a1)[0].tolist())
+    assert changed == {4}
+
+
+def pin_blockwise_zero_and_scaling(orc):
+    """An all-zero block has scale 0, codes 0 and decodes to 0; a block
+    multiplied by 2^k keeps its codes and has its scale multiplied by 2^k."""
+    rng = np.random.default_rng(14)
+    B = 64
+    x = rng.standard_normal(B * 6).astype(np.float32)
+    x[2 * B:3 * B] = 0
+    q, a = orc.quantize_blockwise(x, B)
+    assert a[2] == 0 and not q[2 * B:3 * B].any()
+    assert not orc.dequantize_blockwise(q, a, B)[2 * B:3 * B].any()
+    for k in (-40, -3, 5, 60):
+        q2, a2 = orc.quantize_blockwise(x * np.float32(2.0 ** k), B)
+        assert np.array_equal(q2, q)
+        assert np.array_equal(a2, a * np.float32(2.0 ** k))
+
+
+def pin_blockwise_memory(orc):
+    """8-bit codes take one quarter of the fp32 memory ("An 8-bit integer
+    requires one-quarter the memory of float32", bitsandbytes GPU page,
+    section "Quantization"), plus one fp32 scale per block."""
+    B, n = 256, 256 * 100 + 3
+    q, a = orc.quantize_blockwise(np.ones(n, np.float32), B)
+    assert q.nbytes == n and a.nbytes == 4 * ((n + B - 1) // B)
+    assert abs((q.nbytes + a.nbytes) / (4 * n) - (0.25 + 1 / B)) < 1e-3
+
+
 ALL_PINS = [
     pin_half_roundtrip,
     pin_code_rule_exhaustive,
@@ -276,4 +376,9 @@ ALL_PINS = [
     pin_outliers_are_column_scan,
     pin_permutation_invariance,
     pin_code_extremes,
+    pin_blockwise_closed_forms,
+    pin_blockwise_error_bound,
+    pin_blockwise_locality,
+    pin_blockwise_zero_and_scaling,
+    pin_blockwise_memory,
 ]

@@ -34,6 +34,12 @@ MUTATIONS = {
     "half_round_floor": ("double n = rint(ldexp(a, 10 - E));", "double n = floor(ldexp(a, 10 - E));"),
     "weight_scale_first_col": ("if (x > a) a = x;\n    }\n    sw[n] = a;",
                                "if (k == 0) a = x;\n    }\n    sw[n] = a;"),
+    "blockwise_truncates": ("q[i] = (int8_t)rintf(num / a);", "q[i] = (int8_t)truncf(num / a);"),
+    "blockwise_scale_of_whole_tensor": ("for (int64_t i = i0; i < i1; i++) {\n      const float v",
+                                        "for (int64_t i = 0; i < n; i++) {\n      const float v"),
+    "blockwise_block_shifted": ("const int64_t i0 = b * B, i1", "const int64_t i0 = b * B + 1, i1"),
+    "blockwise_decode_128": ("y[i] = prod / 127.0f;", "y[i] = prod / 128.0f;"),
+    "blockwise_scale_of_first": ("if (v > a) a = v;", "if (i == i0) a = v;"),
 }
 
 
