@@ -552,6 +552,136 @@ def run_reference(args, world, rank, local):
     }
 
 
+def run_blockwise(args, world, rank, local):
+    """The blockwise 8-bit codec of optimizer states: one step quantizes the
+    fp32 state of the large MLP weight (28672 x 8192 values, 940 MB) in blocks
+    of 256 and decodes it back.  Metric: algorithmic GB/s of the step
+    (quantize reads 4n and writes n + 4n/B; dequantize reads n + 4n/B and
+    writes 4n)."""
+    import torch
+
+    from int8_mixed_precision_04_b300 import binding, build
+    build.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    binding.load()
+    peaks, peak_src = load_peaks()
+    n, B = 28672 * 8192, 256
+    nb = (n + B - 1) // B
+    g = torch.Generator(device=dev)
+    g.manual_seed(1234 + rank)
+    x = torch.randn(n, generator=g, device=dev, dtype=torch.float32) * 1e-3
+    codes = torch.empty(n, dtype=torch.int8, device=dev)
+    absmax = torch.empty(nb, dtype=torch.float32, device=dev)
+    y = torch.empty(n, dtype=torch.float32, device=dev)
+    qbytes, dbytes = 4 * n + n + 4 * nb, n + 4 * nb + 4 * n
+    stream = torch.cuda.Stream(device=dev)
+
+    def graph_of(fn, reps):
+        with torch.cuda.stream(stream):
+            for _ in range(args.warmup):
+                fn()
+        torch.cuda.synchronize()
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=stream):
+            for _ in range(reps):
+                fn()
+        return gr
+
+    def timed(gr, reps, replays, sampler=None):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            gr.replay()
+            barrier(world)
+            torch.cuda.synchronize()
+            if sampler:
+                sampler.mark_start()
+            e0.record(stream)
+            for _ in range(replays):
+                gr.replay()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            if sampler:
+                sampler.mark_stop()
+        return max_over_ranks(e0.elapsed_time(e1), world, dev) / (reps * replays)
+
+    def quant():
+        binding.quantize_blockwise(x, B, codes=codes, absmax=absmax, stream=stream)
+
+    def dequant():
+        binding.dequantize_blockwise(codes, absmax, B, y=y, stream=stream)
+
+    def step():
+        quant()
+        dequant()
+
+    reps = 4
+    replays = max(1, args.steps // reps) if args.steps < 10000 else 10
+    gs = graph_of(step, reps)
+    sampler = ClockSampler(local)
+    with sampler:
+        step_ms = timed(gs, reps, replays, sampler)
+    q_ms = timed(graph_of(quant, reps), reps, replays)
+    d_ms = timed(graph_of(dequant, reps), reps, replays)
+    value = world * (qbytes + dbytes) / (step_ms * 1e-3) / 1e9
+    q_gbs = qbytes / (q_ms * 1e-3) / 1e9
+    # e2e: the fp32 state from pinned host memory, the codec, the decoded
+    # state back to pinned host memory
+    xh = x.cpu().pin_memory()
+    yh = torch.empty(n, dtype=torch.float32).pin_memory()
+    with torch.cuda.stream(stream):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(2):
+            x.copy_(xh, non_blocking=True)
+            step()
+            yh.copy_(y, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev) / 2
+    line = {
+        "metric": "blockwise int8 codec GB/s (algorithmic bytes of quantize + dequantize)",
+        "value": value, "unit": "GB/s", "n_gpus": world, "steps": reps * replays,
+        "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "fp32 -> int8 + fp32 absmax -> fp32",
+        "data": "synthetic (seeded torch normal x 1e-3)",
+        "config": {"workload": f"blockwise: fp32 state [{n}] (28672 x 8192), blocks of {B}",
+                   "n": n, "block": B,
+                   "l2": "inputs larger than L2: 940 MB state vs 126 MB L2",
+                   "timing": "CUDA graph replay, CUDA events", "parallelism": f"replicas x{world}"},
+        "e2e": {"value": (qbytes + dbytes) / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+                "h2d_bytes_per_step": 4 * n, "d2h_bytes_per_step": 4 * n, "calls": 2,
+                "note": "pinned H2D of the state, quantize + dequantize, D2H of the decoded state"},
+        "gpu_launches": 2 * reps * replays,
+        "roofline": {"bound": "hbm", "achieved": q_gbs, "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": q_gbs / peaks["hbm_gbs"], "traffic": None,
+                     "kernel": "quantize_blockwise", "peak_source": peak_src,
+                     "kernel_avg_us": q_ms * 1e3, "alg_bytes_per_launch": qbytes,
+                     "dequantize_avg_us": d_ms * 1e3,
+                     "dequantize_gbs": dbytes / (d_ms * 1e-3) / 1e9},
+        "clocks": sampler.summary(),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        import oracle
+        orc = oracle.get()
+        m = 1 << 24
+        xs = x[:m].cpu().numpy()
+        t0 = time.perf_counter()
+        reps_cpu = 0
+        while time.perf_counter() - t0 < args.cpu_budget:
+            q_o, a_o = orc.quantize_blockwise(xs, B)
+            orc.dequantize_blockwise(q_o, a_o, B)
+            reps_cpu += 1
+        dt = time.perf_counter() - t0
+        line["cpu_baseline"] = {"value": reps_cpu * (10 * m + 8 * (m // B)) / dt / 1e9,
+                                "unit": "GB/s", "cores": orc.num_threads(), "kind": "oracle",
+                                "sample": f"the first {m} values, {reps_cpu} passes in {dt:.1f} s"}
+    return line
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -559,7 +689,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="decode",
-                    choices=["decode", "prefill", "large", "sweep", "tiny"])
+                    choices=["decode", "prefill", "large", "sweep", "tiny", "blockwise"])
     ap.add_argument("--T", type=int, default=16, help="tokens of the decode workload")
     ap.add_argument("--max-layers", type=int, default=64)
     ap.add_argument("--e2e-calls", type=int, default=2000)
@@ -574,6 +704,8 @@ def main():
     world, rank, local = dist_setup(args.gpus)
     if args.impl == "reference":
         line = run_reference(args, world, rank, local)
+    elif args.workload == "blockwise":
+        line = run_blockwise(args, world, rank, local)
     else:
         line = run_ours(args, world, rank, local)
     if rank == 0 and line is not None:

@@ -150,6 +150,31 @@ bnb_status_t bnb_int8_linear_from_host(const void *X_host, int64_t T, int64_t K,
                                        void *stream);
 
 /*
+ * The blockwise 8-bit codec of optimizer states.  8-bit optimizers keep their
+ * states quantized block-wise, each block with its own scaling factor
+ * ("bitsandbytes: GPU-Accelerated Inference and Training at Lower Bit
+ * Depths", section "8-bit optimizers for full-model training"; page
+ * "bitsandbytes", section "What it provides").  Blocks are `block`
+ * consecutive values (a power of two from 64 to 2048; the last block may be
+ * short); a block's scale is its absmax a.
+ *   bnb_int8_quantize_blockwise: x [n] fp32 -> codes [n] int8,
+ *     codes[i] = rint(fl32(fl32(127 x[i]) / a)) (IEEE fp32, ties to even; 0
+ *     when a = 0), and absmax [ceil(n / block)] fp32.
+ *   bnb_int8_dequantize_blockwise: codes [n], absmax -> y [n] fp32,
+ *     y[i] = fl32(fl32(codes[i] * a) / 127).
+ * Device pointers, 16-byte aligned, caller-owned; outputs must not overlap
+ * inputs.  Errors: BNB_ERR_INVALID_ARG (NULL, n <= 0, overlap),
+ * BNB_ERR_UNSUPPORTED (block size, alignment, n > BNB_MAX_BLOCKWISE_N,
+ * device), BNB_ERR_CUDA (launch).  The pages give no block size: the
+ * Python binding defaults to 256.
+ */
+#define BNB_MAX_BLOCKWISE_N (1LL << 40)
+bnb_status_t bnb_int8_quantize_blockwise(const float *x, int64_t n, int64_t block, int8_t *codes,
+                                         float *absmax, void *stream);
+bnb_status_t bnb_int8_dequantize_blockwise(const int8_t *codes, const float *absmax, int64_t n,
+                                           int64_t block, float *y, void *stream);
+
+/*
  * Synchronises `stream`, then reads the device status word of `workspace`
  * into *out (BNB_OK, or BNB_ERR_TIMEOUT after a bounded wait gave up) and
  * clears it.  Returns BNB_ERR_CUDA if the synchronisation or copy failed.

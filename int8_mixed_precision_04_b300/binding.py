@@ -42,7 +42,8 @@ class Lib:
                "bnb_status_string", "bnb_launch_count", "bnb_int8_linear_path",
                "bnb_profile_enable", "bnb_profile_collect", "bnb_profile_kernel_count",
                "bnb_profile_kernel_name", "bnb_int8_linear_noalloc",
-               "bnb_int8_linear_from_host")
+               "bnb_int8_linear_from_host", "bnb_int8_quantize_blockwise",
+               "bnb_int8_dequantize_blockwise")
 
     def __init__(self, path: str = LIB_PATH):
         if not os.path.exists(path):
@@ -65,6 +66,10 @@ class Lib:
         L.bnb_int8_linear_from_host.restype = ctypes.c_int
         L.bnb_int8_linear_from_host.argtypes = [_P, _I64, _I64, _P, _P, _P, _I64, ctypes.c_float,
                                                 _P, _P, _P, _P, ctypes.c_size_t, _P]
+        L.bnb_int8_quantize_blockwise.restype = ctypes.c_int
+        L.bnb_int8_quantize_blockwise.argtypes = [_P, _I64, _I64, _P, _P, _P]
+        L.bnb_int8_dequantize_blockwise.restype = ctypes.c_int
+        L.bnb_int8_dequantize_blockwise.argtypes = [_P, _P, _I64, _I64, _P, _P]
         L.bnb_last_device_status.restype = ctypes.c_int
         L.bnb_last_device_status.argtypes = [_P, _P, ctypes.POINTER(ctypes.c_int32)]
         L.bnb_status_string.restype = ctypes.c_char_p
@@ -163,6 +168,36 @@ def linear_from_host(X_host, Wq, Wscale, W16, tau: float, Y_host, X_dev, Y_dev, 
                                           _ptr(workspace), workspace.numel(), _stream(stream))
     _check(rc, "bnb_int8_linear_from_host")
     return Y_host
+
+
+BLOCKWISE_DEFAULT = 256  # the pages give no block size
+
+
+def quantize_blockwise(x, block: int = BLOCKWISE_DEFAULT, codes=None, absmax=None, stream=None):
+    """bnb_int8_quantize_blockwise: fp32 cuda tensor -> (int8 codes, fp32
+    absmax per block of ``block`` values)."""
+    import torch
+    n = x.numel()
+    if codes is None:
+        codes = torch.empty(n, dtype=torch.int8, device=x.device)
+    if absmax is None:
+        absmax = torch.empty((n + block - 1) // block, dtype=torch.float32, device=x.device)
+    rc = load().bnb_int8_quantize_blockwise(_ptr(x), n, block, _ptr(codes), _ptr(absmax),
+                                            _stream(stream))
+    _check(rc, "bnb_int8_quantize_blockwise")
+    return codes, absmax
+
+
+def dequantize_blockwise(codes, absmax, block: int = BLOCKWISE_DEFAULT, y=None, stream=None):
+    """bnb_int8_dequantize_blockwise: (int8 codes, fp32 absmax) -> fp32."""
+    import torch
+    n = codes.numel()
+    if y is None:
+        y = torch.empty(n, dtype=torch.float32, device=codes.device)
+    rc = load().bnb_int8_dequantize_blockwise(_ptr(codes), _ptr(absmax), n, block, _ptr(y),
+                                              _stream(stream))
+    _check(rc, "bnb_int8_dequantize_blockwise")
+    return y
 
 
 def linear_noalloc(X, Wq, Wscale, W16, tau: float, Y=None, stream=None):

@@ -242,6 +242,44 @@ bnb_status_t bnb_int8_quantize_weight(const void *W16, int64_t N, int64_t K, int
   return e == cudaSuccess ? BNB_OK : BNB_ERR_CUDA;
 }
 
+static bool blockwise_size_ok(int64_t block) {
+  return block >= 64 && block <= 2048 && (block & (block - 1)) == 0;
+}
+
+bnb_status_t bnb_int8_quantize_blockwise(const float *x, int64_t n, int64_t block, int8_t *codes,
+                                         float *absmax, void *stream) {
+  if (!x || !codes || !absmax || n <= 0) return BNB_ERR_INVALID_ARG;
+  if (!blockwise_size_ok(block) || n > BNB_MAX_BLOCKWISE_N) return BNB_ERR_UNSUPPORTED;
+  if (!aligned16(x) || !aligned16(codes) || !aligned16(absmax)) return BNB_ERR_UNSUPPORTED;
+  const size_t nb = (size_t)((n + block - 1) / block);
+  if (overlaps(codes, (size_t)n, x, (size_t)n * 4) || overlaps(absmax, nb * 4, x, (size_t)n * 4) ||
+      overlaps(absmax, nb * 4, codes, (size_t)n))
+    return BNB_ERR_INVALID_ARG;
+  int dev = 0;
+  bnb_status_t st = check_device(&dev);
+  if (st != BNB_OK) return st;
+  const cudaError_t e = launch_quantize_blockwise(x, n, (int)block, codes, absmax, device_sms(dev),
+                                                  reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? BNB_OK : BNB_ERR_CUDA;
+}
+
+bnb_status_t bnb_int8_dequantize_blockwise(const int8_t *codes, const float *absmax, int64_t n,
+                                           int64_t block, float *y, void *stream) {
+  if (!codes || !absmax || !y || n <= 0) return BNB_ERR_INVALID_ARG;
+  if (!blockwise_size_ok(block) || n > BNB_MAX_BLOCKWISE_N) return BNB_ERR_UNSUPPORTED;
+  if (!aligned16(codes) || !aligned16(absmax) || !aligned16(y)) return BNB_ERR_UNSUPPORTED;
+  const size_t nb = (size_t)((n + block - 1) / block);
+  if (overlaps(y, (size_t)n * 4, codes, (size_t)n) || overlaps(y, (size_t)n * 4, absmax, nb * 4))
+    return BNB_ERR_INVALID_ARG;
+  int dev = 0;
+  bnb_status_t st = check_device(&dev);
+  if (st != BNB_OK) return st;
+  const cudaError_t e = launch_dequantize_blockwise(codes, absmax, n, (int)block, y,
+                                                    device_sms(dev),
+                                                    reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? BNB_OK : BNB_ERR_CUDA;
+}
+
 bnb_status_t bnb_int8_linear(const void *X, int64_t T, int64_t K, const int8_t *Wq,
                              const float *Wscale, const void *W16, int64_t N, float tau,
                              void *Y, void *workspace, size_t workspace_bytes, void *stream) {

@@ -28,6 +28,8 @@ enum KernelId {
   kKidGemmMma,
   kKidGemmTc,
   kKidQuantWeight,
+  kKidQuantBlockwise,
+  kKidDequantBlockwise,
   kKernelCount
 };
 
@@ -58,6 +60,13 @@ cudaError_t launch_quantize_weight(const void *W16, int64_t N, int64_t K, int8_t
 cudaError_t launch_act_pass(const void *X, int64_t T, int64_t K, uint32_t thr_bits,
                             const Workspace &ws, int code_mode, bool with_xo, const void *W16,
                             int64_t N, int8_t *dbg_xq, int num_sms, cudaStream_t stream);
+
+// The blockwise 8-bit codec (blocks of B values, B a power of two in
+// [64, 2048]): fp32 -> int8 codes + per-block absmax, and back.
+cudaError_t launch_quantize_blockwise(const float *x, int64_t n, int B, int8_t *codes,
+                                      float *absmax, int num_sms, cudaStream_t stream);
+cudaError_t launch_dequantize_blockwise(const int8_t *codes, const float *absmax, int64_t n,
+                                        int B, float *y, int num_sms, cudaStream_t stream);
 
 // The whole layer for T <= 16, K <= kDecodeMaxK, N <= decode_max_n(dev, K)
 // in one kernel (activation pass fused into the GEMV and shared by clusters

@@ -9,7 +9,8 @@ namespace bnb {
 
 static const char *const kKernelNames[kKernelCount] = {
     "memset_status_mask", "outlier_scan", "quantize_rows", "dec_fused",
-    "gemm_mma",           "gemm_tc",      "quantize_weight"};
+    "gemm_mma",           "gemm_tc",      "quantize_weight",
+    "quantize_blockwise", "dequantize_blockwise"};
 
 namespace {
 struct Rec {

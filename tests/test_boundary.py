@@ -147,3 +147,25 @@ def test_from_host_rejects_on_host(lib, case, want):
                                        ctypes.c_float(a["tau"]), a["yh"], a["xd"], a["yd"],
                                        a["ws"], ws_bytes, None)
     assert rc == want
+
+
+@pytest.mark.parametrize("case,want", [
+    (dict(x=None), binding.Status.INVALID_ARG),
+    (dict(q=None), binding.Status.INVALID_ARG),
+    (dict(a=None), binding.Status.INVALID_ARG),
+    (dict(n=0), binding.Status.INVALID_ARG),
+    (dict(block=100), binding.Status.UNSUPPORTED),
+    (dict(block=32), binding.Status.UNSUPPORTED),
+    (dict(block=4096), binding.Status.UNSUPPORTED),
+    (dict(x=FAKE + 4), binding.Status.UNSUPPORTED),
+    (dict(q=FAKE + 64), binding.Status.INVALID_ARG),  # codes inside x
+])
+def test_blockwise_rejects_on_host(lib, case, want):
+    """The blockwise codec checks its arguments before touching a device."""
+    a = dict(x=FAKE, n=1 << 16, block=256, q=FAKE * 64, a=FAKE * 128)
+    a.update(case)
+    assert lib.bnb_int8_quantize_blockwise(a["x"], a["n"], a["block"], a["q"], a["a"], None) == want
+    if "x" not in case:  # the decoder's own checks, same buffers reversed
+        rc = lib.bnb_int8_dequantize_blockwise(a["q"], a["a"], a["n"], a["block"], FAKE * 256, None)
+        if case.get("q", 1) is None or case.get("a", 1) is None or "n" in case or "block" in case:
+            assert rc == want
