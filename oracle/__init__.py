@@ -138,7 +138,7 @@ class Oracle:
 
     # ---- S2..S6 ---------------------------------------------------------------
     def linear(self, X16: np.ndarray, Wq: np.ndarray, sw: np.ndarray, W16: np.ndarray,
-               tau: float, rows=None):
+               tau: float, rows=None, bias=None):
         """Whole layer.  Returns a dict with O, Xq, sx (all rows) and, for
         ``rows`` (default: all), acc (int32), out (float64) and Y (float16)."""
         X16 = np.ascontiguousarray(X16, dtype=np.float16)
@@ -158,7 +158,9 @@ class Oracle:
         Y = np.empty((R, N), np.float16)
         rc = self.lib.orc_linear_rows(
             _ptr(X16.view(np.uint16)), _I64(T), _I64(K), _ptr(Wq), _ptr(sw),
-            _ptr(W16.view(np.uint16)), _I64(N), ctypes.c_float(tau), _ptr(rows), _I64(R),
+            _ptr(W16.view(np.uint16)), _I64(N), ctypes.c_float(tau),
+            None if bias is None else _ptr(np.ascontiguousarray(bias, dtype=np.float16).view(np.uint16)),
+            _ptr(rows), _I64(R),
             _ptr(Xq), _ptr(sx), _ptr(O), ctypes.byref(nO), _ptr(acc), _ptr(out),
             _ptr(Y.view(np.uint16)))
         assert rc == 0, "int32 accumulator overflow"

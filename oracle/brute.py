@@ -69,11 +69,12 @@ def code(x: Fraction, a: Fraction) -> int:
     return round_half_even(Fraction(127) * x / a)
 
 
-def linear(X_bits, W_bits, tau: float):
+def linear(X_bits, W_bits, tau: float, bias_bits=None):
     """The whole decomposition linear on tiny lists of fp16 bit patterns.
 
     X_bits: T lists of K ints, W_bits: N lists of K ints.  Returns a dict with
-    O, Xq, sx, Wq, sw, acc and Y (fp16 bit patterns), all exact.
+    O, Xq, sx, Wq, sw, acc and Y (fp16 bit patterns), all exact.  bias_bits:
+    N fp16 bit patterns added before the final rounding (or None).
     """
     T, K, N = len(X_bits), len(X_bits[0]) if X_bits else 0, len(W_bits)
     X = [[half_bits_to_fraction(b) for b in row] for row in X_bits]
@@ -97,6 +98,8 @@ def linear(X_bits, W_bits, tau: float):
         for n in range(N):
             v = Fraction(acc[t][n]) * sx[t] * sw[n] / 16129
             v += sum((X[t][k] * W[n][k] for k in O), Fraction(0))
+            if bias_bits is not None:
+                v += half_bits_to_fraction(bias_bits[n])
             row.append(fraction_to_half_bits(v))
         Y.append(row)
     return {"O": O, "Xq": Xq, "sx": sx, "Wq": Wq, "sw": sw, "acc": acc, "Y": Y}

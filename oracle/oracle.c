@@ -27,7 +27,11 @@
  *  - code q = rint(fl32(127*x) / a) in IEEE fp32, ties to even; a = 0 gives 0;
  *  - Y = fp16_rne(acc*sx*sw/127^2 + sum_j X[t,O_j]*W[n,O_j]), evaluated here
  *    in double, one final rounding to fp16;
- *  - the outlier weights are the fp16 weights W16, not dequantized codes.
+ *  - the outlier weights are the fp16 weights W16, not dequantized codes;
+ *  - an optional fp16 bias b[n] (the layer is a drop-in replacement for
+ *    PyTorch's Linear: bitsandbytes GPU page, section "How LLM.int8()
+ *    quantizes weights and activations") is added before the one rounding:
+ *    Y = fp16_rne(acc*sx*sw/127^2 + sum_j X[t,O_j]*W[n,O_j] + b[n]).
  *
  * Codes are decided in fp32 because the kernel decides them in fp32; the
  * tests pin this rule against exact rational rounding.
@@ -204,13 +208,14 @@ void orc_outlier_matmul_rows(const uint16_t *X, const uint16_t *W16, int64_t T,
  * (at most 31 + 11 + 11 significant bits); one division, one addition, one
  * final rounding to fp16. */
 void orc_dequant_rows(const int32_t *acc, const float *sx, const float *sw,
-                      const double *out, const int64_t *rows, int64_t nrows,
-                      int64_t N, uint16_t *Y) {
+                      const double *out, const uint16_t *bias, const int64_t *rows,
+                      int64_t nrows, int64_t N, uint16_t *Y) {
 #pragma omp parallel for collapse(2) schedule(static)
   for (int64_t r = 0; r < nrows; r++) {
     for (int64_t n = 0; n < N; n++) {
       double p = (double)acc[r * N + n] * (double)sx[rows[r]] * (double)sw[n];
       double v = p / 16129.0 + out[r * N + n];
+      if (bias) v += orc_half_to_double(bias[n]);  /* nn.Linear's bias, before the one rounding */
       Y[r * N + n] = orc_double_to_half(v);
     }
   }
@@ -222,8 +227,8 @@ void orc_dequant_rows(const int32_t *acc, const float *sx, const float *sw,
  * (NULL to skip) except acc and out, which the caller provides as scratch. */
 int orc_linear_rows(const uint16_t *X, int64_t T, int64_t K, const int8_t *Wq,
                     const float *sw, const uint16_t *W16, int64_t N, float tau,
-                    const int64_t *rows, int64_t nrows, int8_t *Xq, float *sx,
-                    int32_t *O, int32_t *nO, int32_t *acc, double *out,
+                    const uint16_t *bias, const int64_t *rows, int64_t nrows, int8_t *Xq,
+                    float *sx, int32_t *O, int32_t *nO, int32_t *acc, double *out,
                     uint16_t *Y) {
   int rc = orc_outlier_columns(X, T, K, tau, O, nO);
   if (rc) return rc;
@@ -231,7 +236,7 @@ int orc_linear_rows(const uint16_t *X, int64_t T, int64_t K, const int8_t *Wq,
   if (rc) return rc;
   rc = orc_int8_matmul_rows(Xq, Wq, T, N, K, rows, nrows, acc);
   orc_outlier_matmul_rows(X, W16, T, N, K, O, *nO, rows, nrows, out);
-  orc_dequant_rows(acc, sx, sw, out, rows, nrows, N, Y);
+  orc_dequant_rows(acc, sx, sw, out, bias, rows, nrows, N, Y);
   return rc;
 }
 

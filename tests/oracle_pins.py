@@ -116,10 +116,11 @@ def pin_code_rule_exhaustive(orc, n_scales: int = 48):
 # whole layer against the exact brute force
 # ---------------------------------------------------------------------------
 
-def _compare_with_brute(orc, X, W, tau):
+def _compare_with_brute(orc, X, W, tau, bias=None):
     Wq, sw = orc.quantize_weight(W)
-    r = orc.linear(X, Wq, sw, W, tau)
-    b = brute.linear(_rows(X), _rows(W), tau)
+    r = orc.linear(X, Wq, sw, W, tau, bias=bias)
+    b = brute.linear(_rows(X), _rows(W), tau,
+                     None if bias is None else _bits(np.asarray(bias, np.float16)).tolist())
     assert r["O"].tolist() == b["O"], (r["O"], b["O"])
     assert np.array_equal(Wq, np.array(b["Wq"], np.int8).reshape(Wq.shape))
     assert np.array_equal(sw.astype(np.float64), np.array([float(v) for v in b["sw"]]))
@@ -153,6 +154,35 @@ def pin_brute_random_small(orc):
             X[0, 3] = -6.0              # exactly at the threshold: an outlier (>=)
         for tau in (6.0, 1.5, 0.0, math.inf, 2.0 ** 0.5):
             _compare_with_brute(orc, X, W, tau)
+
+
+def pin_bias_brute(orc):
+    """An fp16 bias per output channel (the layer stands in for PyTorch's
+    Linear, whose bias is added to x W^T) is added before the one rounding to
+    fp16: against the exact brute force, with biases that dominate the sum,
+    cancel it and sit far below its last bit."""
+    rng = np.random.default_rng(11)
+    for T, K, N in ((1, 1, 1), (3, 5, 4), (7, 16, 9), (4, 40, 13)):
+        X = (rng.standard_normal((T, K)) * 3).astype(np.float16)
+        W = (rng.standard_normal((N, K)) * 0.05).astype(np.float16)
+        bias = (rng.standard_normal(N) * rng.choice([1e-4, 0.5, 300.0], N)).astype(np.float16)
+        for tau in (6.0, 1.5, math.inf):
+            _compare_with_brute(orc, X, W, tau, bias)
+
+
+def pin_bias_integer(orc):
+    """tau = inf, integer inputs with +-127 in every row and an integer bias:
+    Y = fp16(X W^T + b) exactly; a zero bias gives the unbiased layer's
+    values."""
+    X, W = inputs.int_valued(8, 4, 24, seed=12, adversarial=True)
+    bias = np.arange(-12, 12, dtype=np.float64) * 37
+    Wq, sw = orc.quantize_weight(W)
+    r = orc.linear(X, Wq, sw, W, math.inf, bias=bias.astype(np.float16))
+    exact = X.astype(np.int64) @ W.astype(np.int64).T + bias.astype(np.int64)[None, :]
+    assert np.array_equal(r["Y"].view(np.uint16), exact.astype(np.float64).astype(np.float16).view(np.uint16))
+    r0 = orc.linear(X, Wq, sw, W, math.inf, bias=np.zeros(24, np.float16))
+    r1 = orc.linear(X, Wq, sw, W, math.inf)
+    assert np.array_equal(r0["Y"].astype(np.float64), r1["Y"].astype(np.float64))
 
 
 # ---------------------------------------------------------------------------
@@ -371,6 +401,8 @@ ALL_PINS = [
     pin_hand_example,
     pin_brute_tiny_config,
     pin_brute_random_small,
+    pin_bias_brute,
+    pin_bias_integer,
     pin_tau_inf_integer_inputs,
     pin_tau_zero_is_fp16_matmul,
     pin_outliers_are_column_scan,

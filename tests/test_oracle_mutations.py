@@ -34,6 +34,11 @@ MUTATIONS = {
     "half_round_floor": ("double n = rint(ldexp(a, 10 - E));", "double n = floor(ldexp(a, 10 - E));"),
     "weight_scale_first_col": ("if (x > a) a = x;\n    }\n    sw[n] = a;",
                                "if (k == 0) a = x;\n    }\n    sw[n] = a;"),
+    "bias_dropped": ("if (bias) v += orc_half_to_double(bias[n]);", "(void)bias;"),
+    "bias_sign": ("if (bias) v += orc_half_to_double(bias[n]);",
+                  "if (bias) v -= orc_half_to_double(bias[n]);"),
+    "bias_of_next_channel": ("if (bias) v += orc_half_to_double(bias[n]);",
+                             "if (bias) v += orc_half_to_double(bias[(n + 1) % N]);"),
     "blockwise_truncates": ("q[i] = (int8_t)rintf(num / a);", "q[i] = (int8_t)truncf(num / a);"),
     "blockwise_scale_of_whole_tensor": ("for (int64_t i = i0; i < i1; i++) {\n      const float v",
                                         "for (int64_t i = 0; i < n; i++) {\n      const float v"),
