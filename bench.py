@@ -85,10 +85,10 @@ def make_workload(name: str, T: int):
     raise ValueError(name)
 
 
-def algorithmic_bytes(T, N, K, nO):
+def algorithmic_bytes(T, N, K, nO, bias=False):
     """Bytes the method must move for one call: X read once, Wq + scales read
-    once, the outlier columns of W16, Y written once."""
-    return 2 * T * K + N * K + 4 * N + 2 * N * nO + 2 * T * N
+    once, the outlier columns of W16, the fp16 bias if any, Y written once."""
+    return 2 * T * K + N * K + 4 * N + 2 * N * nO + 2 * T * N + (2 * N if bias else 0)
 
 
 # DRAM bytes per launch of a dominant kernel from an ncu capture of this
@@ -96,7 +96,7 @@ def algorithmic_bytes(T, N, K, nO):
 # is the one that was captured (first 16 hex digits of its SHA-256).
 MEASURED_TRAFFIC = {
     # kernel: (source file, source digest, (T, K, N), dram read + write bytes)
-    "dec_fused": ("decode.cu", "e3cc3b15fb8cc669", (16, 4096, 4096), 19113216 + 0),
+    "dec_fused": ("decode.cu", "a5cb3b195f803291", (16, 4096, 4096), 19114752 + 0),
 }
 
 
@@ -110,14 +110,16 @@ def measured_traffic(kernel, T, K, N):
     return rec[3] if digest == rec[1] else None
 
 
-def kernel_algorithmic(kernel, T, N, K, nO):
+def kernel_algorithmic(kernel, T, N, K, nO, bias=False):
     """(bytes, flops) per launch of one kernel, for the roofline."""
+    b = 2 * N if bias else 0
     if kernel == "dec_fused":
         # the whole decode call: X read once, weight codes + scales + outlier
-        # weight columns, Y written once
-        return 2 * T * K + N * K + 4 * N + 2 * N * nO + 2 * T * N, 2 * T * N * K
+        # weight columns (+ bias), Y written once
+        return 2 * T * K + N * K + 4 * N + 2 * N * nO + 2 * T * N + b, 2 * T * N * K
     if kernel in ("gemm_mma", "gemm_tc"):
-        return N * K + 2 * T * K + 2 * T * N + 2 * N * nO, 2 * T * N * K + 2 * T * N * nO
+        return (N * K + 2 * T * K + 2 * T * N + 2 * N * nO + b,
+                2 * T * N * K + 2 * T * N * nO)
     if kernel == "outlier_scan":
         return 2 * T * K, 0
     if kernel == "quantize_rows":
@@ -273,13 +275,21 @@ def run_ours(args, world, rank, local):
         Wqs.append(Wq)
         sws.append(sw)
     Xs = [Xh.to(dev) for _ in range(layers)]
+    # optional fp16 bias per layer (nn.Linear's), through bnb_int8_linear_bias
+    Bs = ([torch.from_numpy(inputs.bias(N, K, seed=i)).to(dev) for i in range(layers)]
+          if args.bias else [None] * layers)
     Ys = [torch.empty((T, N), dtype=torch.float16, device=dev) for _ in range(layers)]
     ws = torch.empty(binding.workspace_bytes(T, N, K), dtype=torch.uint8, device=dev)
     stream = torch.cuda.Stream(device=dev)
 
     def step(s):
         for i in range(layers):
-            binding.linear(Xs[i], Wqs[i], sws[i], W16s[i], tau, Y=Ys[i], workspace=ws, stream=s)
+            if args.bias:
+                binding.linear_bias(Xs[i], Wqs[i], sws[i], W16s[i], Bs[i], tau, Y=Ys[i],
+                                    workspace=ws, stream=s)
+            else:
+                binding.linear(Xs[i], Wqs[i], sws[i], W16s[i], tau, Y=Ys[i], workspace=ws,
+                               stream=s)
 
     # outlier count of this workload (for byte accounting)
     dbg = binding.linear_debug(Xs[0], Wqs[0], sws[0], W16s[0], tau)
@@ -334,7 +344,7 @@ def run_ours(args, world, rank, local):
     calls = args.steps * layers
     ops = 2 * T * N * K
     value = world * calls * ops / (ms * 1e-3) / 1e12
-    alg_bytes = algorithmic_bytes(T, N, K, nO)
+    alg_bytes = algorithmic_bytes(T, N, K, nO, args.bias)
     gbs = world * calls * alg_bytes / (ms * 1e-3) / 1e9
 
     # the dominant kernel alone: a graph of main-kernel-only launches (library
@@ -364,7 +374,7 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
     kms = k0.elapsed_time(k1)
     kavg_s = kms * 1e-3 / (reps * Gk * layers)
-    kb, kf = kernel_algorithmic(kname, T, N, K, nO)
+    kb, kf = kernel_algorithmic(kname, T, N, K, nO, args.bias)
     peaks, peak_src = load_peaks()
     if path == 1:
         roof = {"bound": "hbm", "achieved": kb / kavg_s / 1e9, "peak": peaks["hbm_gbs"],
@@ -373,7 +383,8 @@ def run_ours(args, world, rank, local):
         roof = {"bound": "tensor", "achieved": kf / kavg_s / 1e12,
                 "peak": peaks["bf16_tflops"], "unit": "TFLOP/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = args.traffic if args.traffic is not None else measured_traffic(kname, T, K, N)
+    roof["traffic"] = (args.traffic if args.traffic is not None
+                       else None if args.bias else measured_traffic(kname, T, K, N))
     roof["kernel"] = kname
     roof["peak_source"] = ("measured (MEASURED_PEAKS.json)" if peak_src == "measured"
                            else "fallback")
@@ -407,7 +418,8 @@ def run_ours(args, world, rank, local):
     def e2e_call(i):
         j = i % 2
         binding.linear_from_host(Xpin[j], Wqs[i % layers], sws[i % layers], W16s[i % layers], tau,
-                                 Ypin[j], Xdev[j], Ydev[j], wss[j], stream=streams2[j])
+                                 Ypin[j], Xdev[j], Ydev[j], wss[j], stream=streams2[j],
+                                 bias=Bs[i % layers])
 
     for i in range(min(10, e2e_calls)):
         e2e_call(i)
@@ -442,7 +454,7 @@ def run_ours(args, world, rank, local):
         "data": "synthetic (seeded, inputs module)",
         "config": {
             "workload": f"{args.workload}: X fp16 [{T},{K}], W fp16 [{N},{K}], tau {tau}",
-            "T": T, "K": K, "N": N, "tau": tau, "n_outliers": nO,
+            "T": T, "K": K, "N": N, "tau": tau, "n_outliers": nO, "bias": bool(args.bias),
             "layers_per_step": layers,
             "l2": f"inputs larger than L2: {layers} distinct layers per step "
                   f"({layers * (wq_bytes + 2 * T * K) / 1e6:.0f} MB of int8 weights and fp16 "
@@ -696,6 +708,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--ref-budget", type=float, default=120.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--bias", action="store_true",
+                    help="layers with an fp16 bias (bnb_int8_linear_bias)")
     ap.add_argument("--traffic", type=float, default=None,
                     help="dram bytes per launch of the dominant kernel from an ncu capture")
     args = ap.parse_args()

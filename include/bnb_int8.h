@@ -109,6 +109,21 @@ bnb_status_t bnb_int8_linear(const void *X, int64_t T, int64_t K, const int8_t *
                              size_t workspace_bytes, void *stream);
 
 /*
+ * bnb_int8_linear with a bias: the layer is a drop-in replacement for
+ * PyTorch's Linear (bitsandbytes GPU page, section "How LLM.int8() quantizes
+ * weights and activations"), whose bias b is added to x W^T.  b[n] is added
+ * in fp32 before the one rounding of Y to fp16:
+ *   Y[t,n] = fp16(acc[t,n] sx[t] sw[n] / 127^2 + sum_{j in O} X[t,j] W16[n,j] + b[n]).
+ *   bias   [N] fp16 on the device, 16-byte aligned, read only; NULL gives
+ *          bnb_int8_linear.  It must not overlap Y.
+ * Other arguments, errors and the device status word as for bnb_int8_linear.
+ */
+bnb_status_t bnb_int8_linear_bias(const void *X, int64_t T, int64_t K, const int8_t *Wq,
+                                  const float *Wscale, const void *W16, const void *bias,
+                                  int64_t N, float tau, void *Y, void *workspace,
+                                  size_t workspace_bytes, void *stream);
+
+/*
  * bnb_int8_linear that also exports its intermediates (for parity tests).
  * Same arguments as bnb_int8_linear, then (each may be NULL to skip):
  *   Xq          [T x K] int8 activation codes (0 in outlier columns)
@@ -128,10 +143,11 @@ bnb_status_t bnb_int8_linear_debug(const void *X, int64_t T, int64_t K,
 
 /*
  * bnb_int8_linear with the activations and the result in host memory: on
- * `stream`, copies X from X_host into X_dev, runs bnb_int8_linear(X_dev ->
- * Y_dev) and copies Y_dev back into Y_host, so that one call moves a step's
- * input in and its result out.  The pages have no counterpart to this entry
- * point; the layer itself is bnb_int8_linear, unchanged.
+ * `stream`, copies X from X_host into X_dev, runs bnb_int8_linear_bias(X_dev
+ * -> Y_dev) and copies Y_dev back into Y_host, so that one call moves a
+ * step's input in and its result out.  The pages have no counterpart to this
+ * entry point; the layer itself is bnb_int8_linear_bias, unchanged.
+ *   bias   [N] fp16 on the device or NULL, as for bnb_int8_linear_bias.
  *   X_host [T x K] fp16 and Y_host [T x N] fp16: host memory.  Page-locked
  *          (pinned) memory makes both copies asynchronous; with pageable
  *          memory the CUDA runtime stages them and the call may block.  The
@@ -145,7 +161,8 @@ bnb_status_t bnb_int8_linear_debug(const void *X, int64_t T, int64_t K,
  */
 bnb_status_t bnb_int8_linear_from_host(const void *X_host, int64_t T, int64_t K,
                                        const int8_t *Wq, const float *Wscale, const void *W16,
-                                       int64_t N, float tau, void *Y_host, void *X_dev,
+                                       const void *bias, int64_t N, float tau, void *Y_host,
+                                       void *X_dev,
                                        void *Y_dev, void *workspace, size_t workspace_bytes,
                                        void *stream);
 

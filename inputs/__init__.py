@@ -142,3 +142,11 @@ def int_valued(T: int, K: int, N: int, seed: int, adversarial: bool = False):
         X[np.arange(T), rng.integers(0, K, size=T)] = 127
         W[np.arange(N), rng.integers(0, K, size=N)] = -127
     return X.astype(np.float16), W.astype(np.float16)
+
+
+def bias(N: int, K: int, seed: int = 0) -> np.ndarray:
+    """fp16 bias [N] drawn like PyTorch Linear's default initialisation,
+    uniform on [-1/sqrt(K), 1/sqrt(K)]."""
+    rng = np.random.default_rng(seed + 7919)
+    bound = 1.0 / math.sqrt(K)
+    return rng.uniform(-bound, bound, size=N).astype(np.float16)

@@ -6,8 +6,9 @@ The compute lives in the CUDA library ``libbnbint8.so`` behind the C ABI of
 CPU fallback: without the built library every entry point raises.
 """
 
-from .binding import (BnbError, Lib, Status, linear, linear_debug, load, quantize_weight,
-                      workspace_bytes)
+from .binding import (BnbError, Lib, Status, linear, linear_bias, linear_debug, load,
+                      quantize_weight, workspace_bytes)
+from .linear8bit import Linear8bitLt
 
-__all__ = ["BnbError", "Lib", "Status", "linear", "linear_debug", "load", "quantize_weight",
-           "workspace_bytes"]
+__all__ = ["BnbError", "Lib", "Linear8bitLt", "Status", "linear", "linear_bias", "linear_debug",
+           "load", "quantize_weight", "workspace_bytes"]

@@ -43,7 +43,7 @@ class Lib:
                "bnb_profile_enable", "bnb_profile_collect", "bnb_profile_kernel_count",
                "bnb_profile_kernel_name", "bnb_int8_linear_noalloc",
                "bnb_int8_linear_from_host", "bnb_int8_quantize_blockwise",
-               "bnb_int8_dequantize_blockwise")
+               "bnb_int8_dequantize_blockwise", "bnb_int8_linear_bias")
 
     def __init__(self, path: str = LIB_PATH):
         if not os.path.exists(path):
@@ -58,13 +58,16 @@ class Lib:
         L.bnb_int8_linear.restype = ctypes.c_int
         L.bnb_int8_linear.argtypes = [_P, _I64, _I64, _P, _P, _P, _I64, ctypes.c_float, _P, _P,
                                       ctypes.c_size_t, _P]
+        L.bnb_int8_linear_bias.restype = ctypes.c_int
+        L.bnb_int8_linear_bias.argtypes = [_P, _I64, _I64, _P, _P, _P, _P, _I64, ctypes.c_float,
+                                           _P, _P, ctypes.c_size_t, _P]
         L.bnb_int8_linear_debug.restype = ctypes.c_int
         L.bnb_int8_linear_debug.argtypes = L.bnb_int8_linear.argtypes + [_P, _P, _P, _P, _P]
         L.bnb_int8_linear_noalloc.restype = ctypes.c_int
         L.bnb_int8_linear_noalloc.argtypes = [_P, _I64, _I64, _P, _P, _P, _I64, ctypes.c_float,
                                               _P, _P]
         L.bnb_int8_linear_from_host.restype = ctypes.c_int
-        L.bnb_int8_linear_from_host.argtypes = [_P, _I64, _I64, _P, _P, _P, _I64, ctypes.c_float,
+        L.bnb_int8_linear_from_host.argtypes = [_P, _I64, _I64, _P, _P, _P, _P, _I64, ctypes.c_float,
                                                 _P, _P, _P, _P, ctypes.c_size_t, _P]
         L.bnb_int8_quantize_blockwise.restype = ctypes.c_int
         L.bnb_int8_quantize_blockwise.argtypes = [_P, _I64, _I64, _P, _P, _P]
@@ -156,15 +159,33 @@ def linear(X, Wq, Wscale, W16, tau: float, Y=None, workspace=None, stream=None):
     return Y
 
 
+def linear_bias(X, Wq, Wscale, W16, bias, tau: float, Y=None, workspace=None, stream=None):
+    """bnb_int8_linear_bias: as :func:`linear`, plus an fp16 bias [N] (cuda)
+    added before the rounding of Y; ``bias=None`` passes NULL."""
+    import torch
+    T, K = X.shape
+    N = Wq.shape[0]
+    if Y is None:
+        Y = torch.empty((T, N), dtype=torch.float16, device=X.device)
+    if workspace is None:
+        workspace = _alloc_ws(T, N, K, X.device)
+    rc = load().bnb_int8_linear_bias(_ptr(X), T, K, _ptr(Wq), _ptr(Wscale), _ptr(W16),
+                                     _ptr(bias), N, float(tau), _ptr(Y), _ptr(workspace),
+                                     workspace.numel(), _stream(stream))
+    _check(rc, "bnb_int8_linear_bias")
+    return Y
+
+
 def linear_from_host(X_host, Wq, Wscale, W16, tau: float, Y_host, X_dev, Y_dev, workspace,
-                     stream=None):
+                     stream=None, bias=None):
     """bnb_int8_linear_from_host: X_host [T,K] fp16 (pinned cpu tensor) -> Y_host
     [T,N] fp16 (pinned cpu tensor), through the caller's device buffers X_dev,
-    Y_dev and workspace, all enqueued on `stream`."""
+    Y_dev and workspace, all enqueued on `stream`; ``bias`` an optional fp16
+    [N] cuda tensor."""
     T, K = X_host.shape
     N = Wq.shape[0]
     rc = load().bnb_int8_linear_from_host(_ptr(X_host), T, K, _ptr(Wq), _ptr(Wscale), _ptr(W16),
-                                          N, float(tau), _ptr(Y_host), _ptr(X_dev), _ptr(Y_dev),
+                                          _ptr(bias), N, float(tau), _ptr(Y_host), _ptr(X_dev), _ptr(Y_dev),
                                           _ptr(workspace), workspace.numel(), _stream(stream))
     _check(rc, "bnb_int8_linear_from_host")
     return Y_host

@@ -164,14 +164,17 @@ static bnb_status_t linear_check(const void *X, int64_t T, int64_t K, const int8
 }
 
 static bnb_status_t linear_impl(const void *X, int64_t T, int64_t K, const int8_t *Wq,
-                                const float *Wscale, const void *W16, int64_t N, float tau,
-                                void *Y, void *workspace, size_t workspace_bytes,
+                                const float *Wscale, const void *W16, const void *bias,
+                                int64_t N, float tau, void *Y, void *workspace,
+                                size_t workspace_bytes,
                                 void *stream_v, int8_t *dbg_xq, float *dbg_sx,
                                 int32_t *dbg_O, int32_t *dbg_nO, int32_t *dbg_acc) {
   bnb_status_t chk = linear_check(X, T, K, Wq, Wscale, W16, N, tau, Y, workspace, workspace_bytes);
   if (chk != BNB_OK) return chk;
   if ((dbg_xq && !aligned16(dbg_xq)) || (dbg_acc && !aligned16(dbg_acc)))
     return BNB_ERR_UNSUPPORTED;
+  if (bias && !aligned16(bias)) return BNB_ERR_UNSUPPORTED;
+  if (bias && overlaps(Y, (size_t)T * (size_t)N * 2, bias, (size_t)N * 2)) return BNB_ERR_INVALID_ARG;
   int dev = 0;
   bnb_status_t st = check_device(&dev);
   if (st != BNB_OK) return st;
@@ -182,7 +185,7 @@ static bnb_status_t linear_impl(const void *X, int64_t T, int64_t K, const int8_
   cudaError_t e;
   if (path == 1) {
     // decode: no memset, the act-pass kernel clears the status word
-    e = launch_decode(X, T, K, thr, Wq, Wscale, W16, N, Y, ws, dbg_xq, dbg_acc, stream);
+    e = launch_decode(X, T, K, thr, Wq, Wscale, W16, bias, N, Y, ws, dbg_xq, dbg_acc, stream);
     if (e != cudaSuccess) return BNB_ERR_CUDA;
   } else {
     if (!profile_only_main()) {
@@ -202,9 +205,9 @@ static bnb_status_t linear_impl(const void *X, int64_t T, int64_t K, const int8_
       if (e != cudaSuccess) return BNB_ERR_CUDA;
     }
     if (path == 2)
-      e = launch_gemm_tc(T, K, Wq, Wscale, W16, N, Y, ws, dbg_acc, device_sms(dev), stream);
+      e = launch_gemm_tc(T, K, Wq, Wscale, W16, bias, N, Y, ws, dbg_acc, device_sms(dev), stream);
     else
-      e = launch_gemm_mma(T, K, Wq, Wscale, W16, N, Y, ws, dbg_acc, stream);
+      e = launch_gemm_mma(T, K, Wq, Wscale, W16, bias, N, Y, ws, dbg_acc, stream);
     if (e != cudaSuccess) return BNB_ERR_CUDA;
   }
   if (dbg_sx && cudaMemcpyAsync(dbg_sx, ws.sx, (size_t)T * 4, cudaMemcpyDeviceToDevice, stream) != cudaSuccess)
@@ -283,13 +286,22 @@ bnb_status_t bnb_int8_dequantize_blockwise(const int8_t *codes, const float *abs
 bnb_status_t bnb_int8_linear(const void *X, int64_t T, int64_t K, const int8_t *Wq,
                              const float *Wscale, const void *W16, int64_t N, float tau,
                              void *Y, void *workspace, size_t workspace_bytes, void *stream) {
-  return linear_impl(X, T, K, Wq, Wscale, W16, N, tau, Y, workspace, workspace_bytes, stream,
-                     nullptr, nullptr, nullptr, nullptr, nullptr);
+  return linear_impl(X, T, K, Wq, Wscale, W16, nullptr, N, tau, Y, workspace, workspace_bytes,
+                     stream, nullptr, nullptr, nullptr, nullptr, nullptr);
+}
+
+bnb_status_t bnb_int8_linear_bias(const void *X, int64_t T, int64_t K, const int8_t *Wq,
+                                  const float *Wscale, const void *W16, const void *bias,
+                                  int64_t N, float tau, void *Y, void *workspace,
+                                  size_t workspace_bytes, void *stream) {
+  return linear_impl(X, T, K, Wq, Wscale, W16, bias, N, tau, Y, workspace, workspace_bytes,
+                     stream, nullptr, nullptr, nullptr, nullptr, nullptr);
 }
 
 bnb_status_t bnb_int8_linear_from_host(const void *X_host, int64_t T, int64_t K,
                                        const int8_t *Wq, const float *Wscale, const void *W16,
-                                       int64_t N, float tau, void *Y_host, void *X_dev,
+                                       const void *bias, int64_t N, float tau, void *Y_host,
+                                       void *X_dev,
                                        void *Y_dev, void *workspace, size_t workspace_bytes,
                                        void *stream) {
   if (!X_host || !Y_host || !X_dev || !Y_dev) return BNB_ERR_INVALID_ARG;
@@ -301,10 +313,12 @@ bnb_status_t bnb_int8_linear_from_host(const void *X_host, int64_t T, int64_t K,
   bnb_status_t r = linear_check(X_dev, T, K, Wq, Wscale, W16, N, tau, Y_dev, workspace,
                                 workspace_bytes);
   if (r != BNB_OK) return r;
+  if (bias && !aligned16(bias)) return BNB_ERR_UNSUPPORTED;
+  if (bias && overlaps(Y_dev, ybytes, bias, (size_t)N * 2)) return BNB_ERR_INVALID_ARG;
   if (cudaMemcpyAsync(X_dev, X_host, xbytes, cudaMemcpyHostToDevice, st) != cudaSuccess)
     return BNB_ERR_CUDA;
-  r = linear_impl(X_dev, T, K, Wq, Wscale, W16, N, tau, Y_dev, workspace, workspace_bytes,
-                  stream, nullptr, nullptr, nullptr, nullptr, nullptr);
+  r = linear_impl(X_dev, T, K, Wq, Wscale, W16, bias, N, tau, Y_dev, workspace,
+                  workspace_bytes, stream, nullptr, nullptr, nullptr, nullptr, nullptr);
   if (r != BNB_OK) return r;
   if (cudaMemcpyAsync(Y_host, Y_dev, ybytes, cudaMemcpyDeviceToHost, st) != cudaSuccess)
     return BNB_ERR_CUDA;
@@ -316,8 +330,8 @@ bnb_status_t bnb_int8_linear_debug(const void *X, int64_t T, int64_t K, const in
                                    void *Y, void *workspace, size_t workspace_bytes,
                                    void *stream, int8_t *Xq, float *Xscale,
                                    int32_t *outlier_idx, int32_t *n_outliers, int32_t *acc) {
-  return linear_impl(X, T, K, Wq, Wscale, W16, N, tau, Y, workspace, workspace_bytes, stream,
-                     Xq, Xscale, outlier_idx, n_outliers, acc);
+  return linear_impl(X, T, K, Wq, Wscale, W16, nullptr, N, tau, Y, workspace, workspace_bytes,
+                     stream, Xq, Xscale, outlier_idx, n_outliers, acc);
 }
 
 bnb_status_t bnb_last_device_status(const void *workspace, void *stream, int32_t *out) {

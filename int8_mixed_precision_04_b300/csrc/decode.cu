@@ -102,6 +102,7 @@ struct DecSmall {
   uint8_t fpart[kDecConsumers];  // [row group][vector] outlier flags
   uint32_t xo[16 * kDecOutSmall];  // [t][j] X at the first outlier columns (fp16 bits)
   uint32_t oc[kDecOutSmall];       // the first outlier columns
+  uint16_t bias[kDecMaxRows];      // the slice's fp16 bias (written before wobar's arrival)
 };
 
 struct DecArgs {
@@ -115,6 +116,7 @@ struct DecArgs {
   const int8_t *Wq;
   const float *sw;
   const unsigned short *W16;
+  const unsigned short *bias;  // [N] fp16 or null
   __half *Y;
   float *sx_out;               // [T]  (CTA 0)
   int32_t *O_out;              // [K]  (CTA 0)
@@ -236,10 +238,22 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     // are never written: the MMAs mask columns past K, and accumulator rows
     // >= T or columns >= rows are never stored.
     named_bar_sync(2, kDecThreads);  // X loads issued
+    // the slice's bias (rows <= 40: two per lane), loaded ahead of the weight
+    // stream and stored once the copies are out; lane 0's arrival on wobar
+    // below publishes it to the epilogue
+    uint16_t bv[2] = {0, 0};
+    if (p.bias)
+#pragma unroll
+      for (int i = 0; i < 2; i++)
+        if (lane + 32 * i < rows) bv[i] = __ldg(p.bias + n0 + lane + 32 * i);
     if (lane == 0) mbar_expect_tx(&sm.wbar, (uint32_t)(rows > 0 ? rows * K : 0));
     __syncwarp();
     for (int64_t r = lane; r < rows; r += 32)
       bulk_g2s(ws + r * pitch, p.Wq + (n0 + r) * K, (uint32_t)K, &sm.wbar);
+#pragma unroll
+    for (int i = 0; i < 2; i++)
+      if (lane + 32 * i < kDecMaxRows) sm.bias[lane + 32 * i] = bv[i];
+    __syncwarp();
     cluster_wait();
     // W16 at the first outlier columns for this slice, as soon as the columns
     // are known: one TMA box (8 columns x the slice's channels) per column.
@@ -586,7 +600,8 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     if (it < nitems && t < T && nl < rows && ok_o) {
       const int64_t n = n0 + nl;
       const float st = sxs[t] / 127.0f, sn = e_sw[it] / 127.0f;
-      const float y = fmaf((float)e_acc[it] * st, sn, e_out[it]);
+      const float b = h2f_bits(sm.bias[nl]);  // 0 without a bias
+      const float y = fmaf((float)e_acc[it] * st, sn, e_out[it] + b);
       p.Y[t * p.N + n] = __float2half_rn(y);
       if (p.dbg_acc) p.dbg_acc[t * p.N + n] = e_acc[it];
     }
@@ -700,8 +715,8 @@ int64_t decode_max_n(int dev, int64_t K) {
 }
 
 cudaError_t launch_decode(const void *X, int64_t T, int64_t K, uint32_t thr, const int8_t *Wq,
-                          const float *sw, const void *W16, int64_t N, void *Y,
-                          const Workspace &ws, int8_t *dbg_xq, int32_t *dbg_acc,
+                          const float *sw, const void *W16, const void *bias, int64_t N,
+                          void *Y, const Workspace &ws, int8_t *dbg_xq, int32_t *dbg_acc,
                           cudaStream_t stream) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) dev = -1;
@@ -733,6 +748,7 @@ cudaError_t launch_decode(const void *X, int64_t T, int64_t K, uint32_t thr, con
   a.Wq = Wq;
   a.sw = sw;
   a.W16 = reinterpret_cast<const unsigned short *>(W16);
+  a.bias = reinterpret_cast<const unsigned short *>(bias);
   a.Y = reinterpret_cast<__half *>(Y);
   a.sx_out = ws.sx;
   a.O_out = ws.O;

@@ -25,7 +25,8 @@ __global__ void __launch_bounds__(kMmaThreads) gemm_mma_kernel(
     const unsigned short *__restrict__ W16, int64_t N, __half *__restrict__ Y,
     const int8_t *__restrict__ xcodes, const float *__restrict__ sx,
     const int32_t *__restrict__ O, const uint32_t *__restrict__ counters,
-    const __half *__restrict__ xo, int64_t kpad, int32_t *__restrict__ dbg_acc) {
+    const __half *__restrict__ xo, int64_t kpad, const unsigned short *__restrict__ bias,
+    int32_t *__restrict__ dbg_acc) {
   __shared__ __align__(128) int8_t As[2][kMmaBM * kMmaBK];
   __shared__ __align__(128) int8_t Bs[2][kMmaBN * kMmaBK];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -99,6 +100,7 @@ __global__ void __launch_bounds__(kMmaThreads) gemm_mma_kernel(
         if (t < T && n < N) {
           if (dbg_acc) dbg_acc[t * N + n] = acc[mt][nt][i];
           v = (float)acc[mt][nt][i] * __fdiv_rn(sx[t], 127.0f) * __fdiv_rn(sw[n], 127.0f);
+          if (bias) v += h2f_bits(__ldg(bias + n));
         }
         y[mt][nt][i] = v;
       }
@@ -171,14 +173,15 @@ __global__ void __launch_bounds__(kMmaThreads) gemm_mma_kernel(
 }
 
 cudaError_t launch_gemm_mma(int64_t T, int64_t K, const int8_t *Wq, const float *sw,
-                            const void *W16, int64_t N, void *Y, const Workspace &ws,
+                            const void *W16, const void *bias, int64_t N, void *Y,
+                           const Workspace &ws,
                             int32_t *dbg_acc, cudaStream_t stream) {
   dim3 grid((unsigned)((N + kMmaBN - 1) / kMmaBN), (unsigned)((T + kMmaBM - 1) / kMmaBM));
   ProfScope ps(kKidGemmMma, stream);
   gemm_mma_kernel<<<grid, kMmaThreads, 0, stream>>>(
       T, K, Wq, sw, reinterpret_cast<const unsigned short *>(W16), N,
       reinterpret_cast<__half *>(Y), reinterpret_cast<const int8_t *>(ws.xcodes), ws.sx, ws.O,
-      ws.counters, ws.xo, ws.kpad, dbg_acc);
+      ws.counters, ws.xo, ws.kpad, reinterpret_cast<const unsigned short *>(bias), dbg_acc);
   note_launch();
   return cudaGetLastError();
 }

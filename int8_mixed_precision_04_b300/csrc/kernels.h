@@ -73,19 +73,21 @@ cudaError_t launch_dequantize_blockwise(const int8_t *codes, const float *absmax
 // of CTAs), launched with programmatic dependent launch.
 int64_t decode_max_n(int dev, int64_t K);
 cudaError_t launch_decode(const void *X, int64_t T, int64_t K, uint32_t thr, const int8_t *Wq,
-                          const float *sw, const void *W16, int64_t N, void *Y,
-                          const Workspace &ws, int8_t *dbg_xq, int32_t *dbg_acc,
+                          const float *sw, const void *W16, const void *bias, int64_t N,
+                          void *Y, const Workspace &ws, int8_t *dbg_xq, int32_t *dbg_acc,
                           cudaStream_t stream);
 
 // S4..S6 on tcgen05 tensor cores (fp16 integer codes from the activation
 // pass, code_mode 1), persistent over 128 x 256 output tiles.
 cudaError_t launch_gemm_tc(int64_t T, int64_t K, const int8_t *Wq, const float *sw,
-                           const void *W16, int64_t N, void *Y, const Workspace &ws,
+                           const void *W16, const void *bias, int64_t N, void *Y,
+                           const Workspace &ws,
                            int32_t *dbg_acc, int num_sms, cudaStream_t stream);
 
 // S4..S6 with warp-level mma.sync (legacy tensor path), int8 codes.
 cudaError_t launch_gemm_mma(int64_t T, int64_t K, const int8_t *Wq, const float *sw,
-                            const void *W16, int64_t N, void *Y, const Workspace &ws,
+                            const void *W16, const void *bias, int64_t N, void *Y,
+                           const Workspace &ws,
                             int32_t *dbg_acc, cudaStream_t stream);
 
 }  // namespace bnb

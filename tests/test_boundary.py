@@ -134,16 +134,18 @@ def test_missing_library_raises(tmp_path):
     (dict(T=0), binding.Status.INVALID_ARG),
     (dict(tau=-1.0), binding.Status.INVALID_ARG),
     (dict(K=250), binding.Status.UNSUPPORTED),
+    (dict(bias=FAKE * 3 + 4), binding.Status.UNSUPPORTED),     # misaligned bias
+    (dict(bias=FAKE * 96 + 64), binding.Status.INVALID_ARG),   # bias inside Y_dev
 ])
 def test_from_host_rejects_on_host(lib, case, want):
     """bnb_int8_linear_from_host checks its buffers and the layer's arguments
     before enqueuing a copy."""
     a = dict(xh=FAKE, T=16, K=256, N=256, tau=6.0, yh=FAKE * 2, xd=FAKE * 64,
-             yd=FAKE * 96, ws=FAKE * 256)
+             yd=FAKE * 96, ws=FAKE * 256, bias=None)
     a.update(case)
     T, K, N = a["T"], a["K"], a["N"]
     ws_bytes = lib.bnb_int8_linear_workspace_bytes(T, N, K) if min(T, K, N) > 0 else 0
-    rc = lib.bnb_int8_linear_from_host(a["xh"], T, K, FAKE, FAKE, FAKE, N,
+    rc = lib.bnb_int8_linear_from_host(a["xh"], T, K, FAKE, FAKE, FAKE, a["bias"], N,
                                        ctypes.c_float(a["tau"]), a["yh"], a["xd"], a["yd"],
                                        a["ws"], ws_bytes, None)
     assert rc == want
@@ -169,3 +171,19 @@ def test_blockwise_rejects_on_host(lib, case, want):
         rc = lib.bnb_int8_dequantize_blockwise(a["q"], a["a"], a["n"], a["block"], FAKE * 256, None)
         if case.get("q", 1) is None or case.get("a", 1) is None or "n" in case or "block" in case:
             assert rc == want
+
+
+@pytest.mark.parametrize("case,want", [
+    (dict(X=None), binding.Status.INVALID_ARG),
+    (dict(tau=math.nan), binding.Status.INVALID_ARG),
+    (dict(bias=FAKE * 64 + 8), binding.Status.UNSUPPORTED),    # misaligned bias
+    (dict(bias=FAKE * 64 + 256), binding.Status.INVALID_ARG),  # bias inside Y
+])
+def test_linear_bias_rejects_on_host(lib, case, want):
+    """bnb_int8_linear_bias runs the layer's checks, then its own on the bias."""
+    a = dict(X=FAKE, T=16, K=256, N=256, tau=6.0, bias=FAKE * 32, Y=FAKE * 64, ws=FAKE * 256)
+    a.update(case)
+    ws_bytes = lib.bnb_int8_linear_workspace_bytes(a["T"], a["N"], a["K"])
+    rc = lib.bnb_int8_linear_bias(a["X"], a["T"], a["K"], FAKE, FAKE, FAKE, a["bias"], a["N"],
+                                  ctypes.c_float(a["tau"]), a["Y"], a["ws"], ws_bytes, None)
+    assert rc == want
