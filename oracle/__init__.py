@@ -140,13 +140,16 @@ class Oracle:
     def linear(self, X16: np.ndarray, Wq: np.ndarray, sw: np.ndarray, W16: np.ndarray,
                tau: float, rows=None, bias=None):
         """Whole layer.  Returns a dict with O, Xq, sx (all rows) and, for
-        ``rows`` (default: all), acc (int32), out (float64) and Y (float16)."""
+        ``rows`` (default: all), acc (int32), out (float64) and Y (float16).
+        ``W16=None``: only the int8 weight is kept and the outlier weights are
+        its codes dequantized, Wq * sw / 127."""
         X16 = np.ascontiguousarray(X16, dtype=np.float16)
-        W16 = np.ascontiguousarray(W16, dtype=np.float16)
+        if W16 is not None:
+            W16 = np.ascontiguousarray(W16, dtype=np.float16)
         Wq = np.ascontiguousarray(Wq, dtype=np.int8)
         sw = np.ascontiguousarray(sw, dtype=np.float32)
         T, K = X16.shape
-        N = W16.shape[0]
+        N = Wq.shape[0]
         rows = np.arange(T, dtype=np.int64) if rows is None else np.asarray(rows, np.int64)
         R = len(rows)
         Xq = np.empty((T, K), np.int8)
@@ -158,7 +161,7 @@ class Oracle:
         Y = np.empty((R, N), np.float16)
         rc = self.lib.orc_linear_rows(
             _ptr(X16.view(np.uint16)), _I64(T), _I64(K), _ptr(Wq), _ptr(sw),
-            _ptr(W16.view(np.uint16)), _I64(N), ctypes.c_float(tau),
+            None if W16 is None else _ptr(W16.view(np.uint16)), _I64(N), ctypes.c_float(tau),
             None if bias is None else _ptr(np.ascontiguousarray(bias, dtype=np.float16).view(np.uint16)),
             _ptr(rows), _I64(R),
             _ptr(Xq), _ptr(sx), _ptr(O), ctypes.byref(nO), _ptr(acc), _ptr(out),

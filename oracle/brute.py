@@ -69,12 +69,14 @@ def code(x: Fraction, a: Fraction) -> int:
     return round_half_even(Fraction(127) * x / a)
 
 
-def linear(X_bits, W_bits, tau: float, bias_bits=None):
+def linear(X_bits, W_bits, tau: float, bias_bits=None, w16_free: bool = False):
     """The whole decomposition linear on tiny lists of fp16 bit patterns.
 
     X_bits: T lists of K ints, W_bits: N lists of K ints.  Returns a dict with
     O, Xq, sx, Wq, sw, acc and Y (fp16 bit patterns), all exact.  bias_bits:
     N fp16 bit patterns added before the final rounding (or None).
+    w16_free: the outlier weights are the codes dequantized, Wq * sw / 127,
+    instead of W itself.
     """
     T, K, N = len(X_bits), len(X_bits[0]) if X_bits else 0, len(W_bits)
     X = [[half_bits_to_fraction(b) for b in row] for row in X_bits]
@@ -97,7 +99,10 @@ def linear(X_bits, W_bits, tau: float, bias_bits=None):
         row = []
         for n in range(N):
             v = Fraction(acc[t][n]) * sx[t] * sw[n] / 16129
-            v += sum((X[t][k] * W[n][k] for k in O), Fraction(0))
+            if w16_free:
+                v += sum((X[t][k] * Wq[n][k] * sw[n] / 127 for k in O), Fraction(0))
+            else:
+                v += sum((X[t][k] * W[n][k] for k in O), Fraction(0))
             if bias_bits is not None:
                 v += half_bits_to_fraction(bias_bits[n])
             row.append(fraction_to_half_bits(v))

@@ -27,7 +27,12 @@
  *  - code q = rint(fl32(127*x) / a) in IEEE fp32, ties to even; a = 0 gives 0;
  *  - Y = fp16_rne(acc*sx*sw/127^2 + sum_j X[t,O_j]*W[n,O_j]), evaluated here
  *    in double, one final rounding to fp16;
- *  - the outlier weights are the fp16 weights W16, not dequantized codes;
+ *  - the outlier weights are the fp16 weights W16, not dequantized codes; with
+ *    W16 absent (only the int8 weight kept, half of fp16's bytes: Hugging
+ *    Face page, "Quick Comparison" table; bitsandbytes GPU page, section
+ *    "Why quantization matters for LLM deployment") they are the codes
+ *    dequantized, Wq[n,k] * sw[n] / 127, exact real values carried in
+ *    double;
  *  - an optional fp16 bias b[n] (the layer is a drop-in replacement for
  *    PyTorch's Linear: bitsandbytes GPU page, section "How LLM.int8()
  *    quantizes weights and activations") is added before the one rounding:
@@ -204,6 +209,24 @@ void orc_outlier_matmul_rows(const uint16_t *X, const uint16_t *W16, int64_t T,
   }
 }
 
+/* S5 without W16: the outlier weights dequantized from the int8 codes,
+ * w = Wq[n,k] * sw[n] / 127, then the same 16-bit-input product. */
+void orc_outlier_matmul_rows_wq(const uint16_t *X, const int8_t *Wq, const float *sw,
+                                int64_t N, int64_t K, const int32_t *O, int32_t nO,
+                                const int64_t *rows, int64_t nrows, double *out) {
+#pragma omp parallel for collapse(2) schedule(static)
+  for (int64_t r = 0; r < nrows; r++) {
+    for (int64_t n = 0; n < N; n++) {
+      double s = 0.0;
+      for (int32_t j = 0; j < nO; j++) {
+        double w = (double)Wq[n * K + O[j]] * (double)sw[n] / 127.0;
+        s += orc_half_to_double(X[rows[r] * K + O[j]]) * w;
+      }
+      out[r * N + n] = s;
+    }
+  }
+}
+
 /* S6: Y = fp16( acc * sx * sw / 127^2 + out ).  acc*sx*sw is exact in double
  * (at most 31 + 11 + 11 significant bits); one division, one addition, one
  * final rounding to fp16. */
@@ -224,7 +247,8 @@ void orc_dequant_rows(const int32_t *acc, const float *sx, const float *sw,
 /* The whole layer, S2..S6, for a chosen set of rows.  The outlier set and the
  * activation codes are computed over ALL T rows (the outlier set depends on
  * every row); S4..S6 only for `rows`.  Intermediates are optional outputs
- * (NULL to skip) except acc and out, which the caller provides as scratch. */
+ * (NULL to skip) except acc and out, which the caller provides as scratch.
+ * W16 NULL: the outlier weights come from the int8 codes (above). */
 int orc_linear_rows(const uint16_t *X, int64_t T, int64_t K, const int8_t *Wq,
                     const float *sw, const uint16_t *W16, int64_t N, float tau,
                     const uint16_t *bias, const int64_t *rows, int64_t nrows, int8_t *Xq,
@@ -235,7 +259,10 @@ int orc_linear_rows(const uint16_t *X, int64_t T, int64_t K, const int8_t *Wq,
   rc = orc_quantize_activations(X, T, K, O, *nO, Xq, sx, NULL);
   if (rc) return rc;
   rc = orc_int8_matmul_rows(Xq, Wq, T, N, K, rows, nrows, acc);
-  orc_outlier_matmul_rows(X, W16, T, N, K, O, *nO, rows, nrows, out);
+  if (W16)
+    orc_outlier_matmul_rows(X, W16, T, N, K, O, *nO, rows, nrows, out);
+  else  /* only the int8 weight is kept */
+    orc_outlier_matmul_rows_wq(X, Wq, sw, N, K, O, *nO, rows, nrows, out);
   orc_dequant_rows(acc, sx, sw, out, bias, rows, nrows, N, Y);
   return rc;
 }

@@ -185,6 +185,49 @@ def pin_bias_integer(orc):
     assert np.array_equal(r0["Y"].astype(np.float64), r1["Y"].astype(np.float64))
 
 
+def pin_w16_free_brute(orc):
+    """Only the int8 weight kept: the outlier weights are the codes
+    dequantized, Wq sw / 127.  Against the exact brute force on random tiny
+    shapes and thresholds (with a bias, and with an all-zero weight row)."""
+    rng = np.random.default_rng(13)
+    for T, K, N in ((1, 1, 1), (3, 5, 4), (7, 16, 9), (5, 24, 6)):
+        X = (rng.standard_normal((T, K)) * 3).astype(np.float16)
+        W = (rng.standard_normal((N, K)) * 0.05).astype(np.float16)
+        if N > 3:
+            W[2] = 0
+        bias = (rng.standard_normal(N) * 0.3).astype(np.float16)
+        for tau in (6.0, 1.5, 0.0, math.inf):
+            for b in (None, bias):
+                Wq, sw = orc.quantize_weight(W)
+                r = orc.linear(X, Wq, sw, None, tau, bias=b)
+                bb = brute.linear(_rows(X), _rows(W), tau,
+                                  None if b is None else _bits(b).tolist(), w16_free=True)
+                yb = np.array(bb["Y"], np.uint16).reshape(r["Y"].shape)
+                assert r["O"].tolist() == bb["O"]
+                assert np.array_equal(r["Y"].view(np.uint16), yb), (T, K, N, tau)
+
+
+def pin_w16_free_invariants(orc):
+    """Where the dequantized codes equal the weights -- integer weights with
+    +-127 in every row, so sw = 127 and Wq = W -- the int8-weight-only layer
+    gives the fp16-weight layer's Y bit for bit at every threshold; with no
+    outliers (tau = inf) it does so for any weight."""
+    rng = np.random.default_rng(14)
+    _, W = inputs.int_valued(4, 64, 24, seed=15)
+    X = (rng.standard_normal((9, 64)) * 4).astype(np.float16)
+    Wq, sw = orc.quantize_weight(W)
+    assert np.all(sw == 127) and np.array_equal(Wq, W.astype(np.int8))
+    for tau in (6.0, 3.0, 0.0):
+        a = orc.linear(X, Wq, sw, W, tau)["Y"]
+        b = orc.linear(X, Wq, sw, None, tau)["Y"]
+        assert np.array_equal(a.view(np.uint16), b.view(np.uint16)), tau
+    W2 = (rng.standard_normal((24, 64)) * 0.05).astype(np.float16)
+    Wq2, sw2 = orc.quantize_weight(W2)
+    a = orc.linear(X, Wq2, sw2, W2, math.inf)["Y"]
+    b = orc.linear(X, Wq2, sw2, None, math.inf)["Y"]
+    assert np.array_equal(a.view(np.uint16), b.view(np.uint16))
+
+
 # ---------------------------------------------------------------------------
 # invariants of the method
 # ---------------------------------------------------------------------------
@@ -386,9 +429,9 @@ def pin_blockwise_zero_and_scaling(orc):
 
 
 def pin_blockwise_memory(orc):
-    """8-bit codes take one quarter of the fp32 memory ("An 8-bit integer
-    requires one-quarter the memory of float32", bitsandbytes GPU page,
-    section "Quantization"), plus one fp32 scale per block."""
+    """8-bit codes take a quarter of the fp32 bytes (bitsandbytes GPU page,
+    section "Why quantization matters for LLM deployment"), plus one fp32
+    scale per block."""
     B, n = 256, 256 * 100 + 3
     q, a = orc.quantize_blockwise(np.ones(n, np.float32), B)
     assert q.nbytes == n and a.nbytes == 4 * ((n + B - 1) // B)
@@ -403,6 +446,8 @@ ALL_PINS = [
     pin_brute_random_small,
     pin_bias_brute,
     pin_bias_integer,
+    pin_w16_free_brute,
+    pin_w16_free_invariants,
     pin_tau_inf_integer_inputs,
     pin_tau_zero_is_fp16_matmul,
     pin_outliers_are_column_scan,

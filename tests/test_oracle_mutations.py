@@ -39,6 +39,12 @@ MUTATIONS = {
                   "if (bias) v -= orc_half_to_double(bias[n]);"),
     "bias_of_next_channel": ("if (bias) v += orc_half_to_double(bias[n]);",
                              "if (bias) v += orc_half_to_double(bias[(n + 1) % N]);"),
+    "w16_free_scale_128": ("double w = (double)Wq[n * K + O[j]] * (double)sw[n] / 127.0;",
+                           "double w = (double)Wq[n * K + O[j]] * (double)sw[n] / 128.0;"),
+    "w16_free_column_by_position": ("double w = (double)Wq[n * K + O[j]] * (double)sw[n] / 127.0;",
+                                    "double w = (double)Wq[n * K + j] * (double)sw[n] / 127.0;"),
+    "w16_free_scale_of_row_0": ("double w = (double)Wq[n * K + O[j]] * (double)sw[n] / 127.0;",
+                                "double w = (double)Wq[n * K + O[j]] * (double)sw[0] / 127.0;"),
     "blockwise_truncates": ("q[i] = (int8_t)rintf(num / a);", "q[i] = (int8_t)truncf(num / a);"),
     "blockwise_scale_of_whole_tensor": ("for (int64_t i = i0; i < i1; i++) {\n      const float v",
                                         "for (int64_t i = 0; i < n; i++) {\n      const float v"),
