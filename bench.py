@@ -85,10 +85,12 @@ def make_workload(name: str, T: int):
     raise ValueError(name)
 
 
-def algorithmic_bytes(T, N, K, nO, bias=False):
+def algorithmic_bytes(T, N, K, nO, bias=False, wq_only=False):
     """Bytes the method must move for one call: X read once, Wq + scales read
-    once, the outlier columns of W16, the fp16 bias if any, Y written once."""
-    return 2 * T * K + N * K + 4 * N + 2 * N * nO + 2 * T * N + (2 * N if bias else 0)
+    once, the outlier columns of W16 (none with only the int8 weight), the fp16
+    bias if any, Y written once."""
+    w16 = 0 if wq_only else 2 * N * nO
+    return 2 * T * K + N * K + 4 * N + w16 + 2 * T * N + (2 * N if bias else 0)
 
 
 # DRAM bytes per launch of a dominant kernel from an ncu capture of this
@@ -110,15 +112,16 @@ def measured_traffic(kernel, T, K, N):
     return rec[3] if digest == rec[1] else None
 
 
-def kernel_algorithmic(kernel, T, N, K, nO, bias=False):
+def kernel_algorithmic(kernel, T, N, K, nO, bias=False, wq_only=False):
     """(bytes, flops) per launch of one kernel, for the roofline."""
     b = 2 * N if bias else 0
+    w16 = 0 if wq_only else 2 * N * nO  # the int8-weight-only GEMM reads compacted codes instead
     if kernel == "dec_fused":
         # the whole decode call: X read once, weight codes + scales + outlier
         # weight columns (+ bias), Y written once
-        return 2 * T * K + N * K + 4 * N + 2 * N * nO + 2 * T * N + b, 2 * T * N * K
+        return 2 * T * K + N * K + 4 * N + w16 + 2 * T * N + b, 2 * T * N * K
     if kernel in ("gemm_mma", "gemm_tc"):
-        return (N * K + 2 * T * K + 2 * T * N + 2 * N * nO + b,
+        return (N * K + 2 * T * K + 2 * T * N + (2 * N * nO) + b,
                 2 * T * N * K + 2 * T * N * nO)
     if kernel == "outlier_scan":
         return 2 * T * K, 0
@@ -268,10 +271,11 @@ def run_ours(args, world, rank, local):
     W16_0 = torch.from_numpy(w.W).to(dev)
     W16s, Wqs, sws = [], [], []
     for i in range(layers):
-        # distinct copies of the same weight (same numbers, distinct memory)
+        # distinct copies of the same weight (same numbers, distinct memory);
+        # with --wq-only no fp16 weight stays resident
         Wc = W16_0.clone() if i else W16_0
         Wq, sw = binding.quantize_weight(Wc)
-        W16s.append(Wc)
+        W16s.append(None if args.wq_only else Wc)
         Wqs.append(Wq)
         sws.append(sw)
     Xs = [Xh.to(dev) for _ in range(layers)]
@@ -284,7 +288,10 @@ def run_ours(args, world, rank, local):
 
     def step(s):
         for i in range(layers):
-            if args.bias:
+            if args.wq_only:
+                binding.linear_wq_only(Xs[i], Wqs[i], sws[i], Bs[i], tau, Y=Ys[i], workspace=ws,
+                                       stream=s)
+            elif args.bias:
                 binding.linear_bias(Xs[i], Wqs[i], sws[i], W16s[i], Bs[i], tau, Y=Ys[i],
                                     workspace=ws, stream=s)
             else:
@@ -292,7 +299,7 @@ def run_ours(args, world, rank, local):
                                stream=s)
 
     # outlier count of this workload (for byte accounting)
-    dbg = binding.linear_debug(Xs[0], Wqs[0], sws[0], W16s[0], tau)
+    dbg = binding.linear_debug(Xs[0], Wqs[0], sws[0], W16_0, tau)
     nO = int(dbg["nO"].item())
     del dbg
 
@@ -344,7 +351,7 @@ def run_ours(args, world, rank, local):
     calls = args.steps * layers
     ops = 2 * T * N * K
     value = world * calls * ops / (ms * 1e-3) / 1e12
-    alg_bytes = algorithmic_bytes(T, N, K, nO, args.bias)
+    alg_bytes = algorithmic_bytes(T, N, K, nO, args.bias, args.wq_only)
     gbs = world * calls * alg_bytes / (ms * 1e-3) / 1e9
 
     # the dominant kernel alone: a graph of main-kernel-only launches (library
@@ -374,7 +381,7 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
     kms = k0.elapsed_time(k1)
     kavg_s = kms * 1e-3 / (reps * Gk * layers)
-    kb, kf = kernel_algorithmic(kname, T, N, K, nO, args.bias)
+    kb, kf = kernel_algorithmic(kname, T, N, K, nO, args.bias, args.wq_only)
     peaks, peak_src = load_peaks()
     if path == 1:
         roof = {"bound": "hbm", "achieved": kb / kavg_s / 1e9, "peak": peaks["hbm_gbs"],
@@ -384,7 +391,8 @@ def run_ours(args, world, rank, local):
                 "peak": peaks["bf16_tflops"], "unit": "TFLOP/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
     roof["traffic"] = (args.traffic if args.traffic is not None
-                       else None if args.bias else measured_traffic(kname, T, K, N))
+                       else None if args.bias or args.wq_only
+                       else measured_traffic(kname, T, K, N))
     roof["kernel"] = kname
     roof["peak_source"] = ("measured (MEASURED_PEAKS.json)" if peak_src == "measured"
                            else "fallback")
@@ -455,6 +463,7 @@ def run_ours(args, world, rank, local):
         "config": {
             "workload": f"{args.workload}: X fp16 [{T},{K}], W fp16 [{N},{K}], tau {tau}",
             "T": T, "K": K, "N": N, "tau": tau, "n_outliers": nO, "bias": bool(args.bias),
+            "fp16_weight_resident": not args.wq_only,
             "layers_per_step": layers,
             "l2": f"inputs larger than L2: {layers} distinct layers per step "
                   f"({layers * (wq_bytes + 2 * T * K) / 1e6:.0f} MB of int8 weights and fp16 "
@@ -710,6 +719,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--bias", action="store_true",
                     help="layers with an fp16 bias (bnb_int8_linear_bias)")
+    ap.add_argument("--wq-only", action="store_true",
+                    help="only the int8 weight resident (bnb_int8_linear_wq_only)")
     ap.add_argument("--traffic", type=float, default=None,
                     help="dram bytes per launch of the dominant kernel from an ncu capture")
     args = ap.parse_args()

@@ -124,6 +124,21 @@ bnb_status_t bnb_int8_linear_bias(const void *X, int64_t T, int64_t K, const int
                                   size_t workspace_bytes, void *stream);
 
 /*
+ * The layer with only the int8 weight resident: no fp16 copy of W is kept,
+ * which halves the weight's bytes against fp16 (Hugging Face page, "Quick
+ * Comparison" table; bitsandbytes GPU page, section "Why quantization matters
+ * for LLM deployment").  The outlier columns then use the codes dequantized,
+ * w[n,k] = Wq[n,k] sw[n] / 127, in the same 16-bit-input product:
+ *   Y[t,n] = fp16( (acc[t,n] sx[t]/127 + sum_{j in O} X[t,j] Wq[n,j]) sw[n]/127 + b[n] ),
+ * the sums in fp32 in any order, one rounding to fp16.  Arguments as for
+ * bnb_int8_linear_bias without W16 (bias may be NULL); errors likewise.
+ */
+bnb_status_t bnb_int8_linear_wq_only(const void *X, int64_t T, int64_t K, const int8_t *Wq,
+                                     const float *Wscale, const void *bias, int64_t N,
+                                     float tau, void *Y, void *workspace,
+                                     size_t workspace_bytes, void *stream);
+
+/*
  * bnb_int8_linear that also exports its intermediates (for parity tests).
  * Same arguments as bnb_int8_linear, then (each may be NULL to skip):
  *   Xq          [T x K] int8 activation codes (0 in outlier columns)
@@ -148,6 +163,7 @@ bnb_status_t bnb_int8_linear_debug(const void *X, int64_t T, int64_t K,
  * step's input in and its result out.  The pages have no counterpart to this
  * entry point; the layer itself is bnb_int8_linear_bias, unchanged.
  *   bias   [N] fp16 on the device or NULL, as for bnb_int8_linear_bias.
+ *   W16    may be NULL: the layer is then bnb_int8_linear_wq_only.
  *   X_host [T x K] fp16 and Y_host [T x N] fp16: host memory.  Page-locked
  *          (pinned) memory makes both copies asynchronous; with pageable
  *          memory the CUDA runtime stages them and the call may block.  The

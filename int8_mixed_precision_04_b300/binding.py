@@ -43,7 +43,8 @@ class Lib:
                "bnb_profile_enable", "bnb_profile_collect", "bnb_profile_kernel_count",
                "bnb_profile_kernel_name", "bnb_int8_linear_noalloc",
                "bnb_int8_linear_from_host", "bnb_int8_quantize_blockwise",
-               "bnb_int8_dequantize_blockwise", "bnb_int8_linear_bias")
+               "bnb_int8_dequantize_blockwise", "bnb_int8_linear_bias",
+               "bnb_int8_linear_wq_only")
 
     def __init__(self, path: str = LIB_PATH):
         if not os.path.exists(path):
@@ -61,6 +62,9 @@ class Lib:
         L.bnb_int8_linear_bias.restype = ctypes.c_int
         L.bnb_int8_linear_bias.argtypes = [_P, _I64, _I64, _P, _P, _P, _P, _I64, ctypes.c_float,
                                            _P, _P, ctypes.c_size_t, _P]
+        L.bnb_int8_linear_wq_only.restype = ctypes.c_int
+        L.bnb_int8_linear_wq_only.argtypes = [_P, _I64, _I64, _P, _P, _P, _I64, ctypes.c_float,
+                                              _P, _P, ctypes.c_size_t, _P]
         L.bnb_int8_linear_debug.restype = ctypes.c_int
         L.bnb_int8_linear_debug.argtypes = L.bnb_int8_linear.argtypes + [_P, _P, _P, _P, _P]
         L.bnb_int8_linear_noalloc.restype = ctypes.c_int
@@ -176,12 +180,30 @@ def linear_bias(X, Wq, Wscale, W16, bias, tau: float, Y=None, workspace=None, st
     return Y
 
 
+def linear_wq_only(X, Wq, Wscale, bias, tau: float, Y=None, workspace=None, stream=None):
+    """bnb_int8_linear_wq_only: the layer with only the int8 weight resident
+    (outlier weights dequantized from the codes); ``bias`` an fp16 [N] cuda
+    tensor or None."""
+    import torch
+    T, K = X.shape
+    N = Wq.shape[0]
+    if Y is None:
+        Y = torch.empty((T, N), dtype=torch.float16, device=X.device)
+    if workspace is None:
+        workspace = _alloc_ws(T, N, K, X.device)
+    rc = load().bnb_int8_linear_wq_only(_ptr(X), T, K, _ptr(Wq), _ptr(Wscale), _ptr(bias), N,
+                                        float(tau), _ptr(Y), _ptr(workspace), workspace.numel(),
+                                        _stream(stream))
+    _check(rc, "bnb_int8_linear_wq_only")
+    return Y
+
+
 def linear_from_host(X_host, Wq, Wscale, W16, tau: float, Y_host, X_dev, Y_dev, workspace,
                      stream=None, bias=None):
     """bnb_int8_linear_from_host: X_host [T,K] fp16 (pinned cpu tensor) -> Y_host
     [T,N] fp16 (pinned cpu tensor), through the caller's device buffers X_dev,
     Y_dev and workspace, all enqueued on `stream`; ``bias`` an optional fp16
-    [N] cuda tensor."""
+    [N] cuda tensor; ``W16=None`` runs the int8-weight-only layer."""
     T, K = X_host.shape
     N = Wq.shape[0]
     rc = load().bnb_int8_linear_from_host(_ptr(X_host), T, K, _ptr(Wq), _ptr(Wscale), _ptr(W16),

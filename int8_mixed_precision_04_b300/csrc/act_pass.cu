@@ -14,8 +14,9 @@
 //   multiple of 64, or, when outliers are dense (outlier_block_dense), X
 //   masked to the outlier columns (zero elsewhere) over all K columns.  For
 //   the tcgen05 GEMM with a sparse outlier set, the same launch also compacts
-//   W16's outlier columns once per call (w16o[n, j] = W16[n, O[j]]), so that
-//   the GEMM's token tiles read them by TMA.
+//   W16's outlier columns once per call (w16o[n, j] = W16[n, O[j]]; with only
+//   the int8 weight kept, Wq[n, O[j]] as an fp16 integer), so that the GEMM's
+//   token tiles read them by TMA.
 //
 // All three are HBM-bound: 16-byte coalesced loads, every load of a thread
 // issued before any is used (the row pass keeps its row in registers and
@@ -240,6 +241,7 @@ struct QuantArgs {
   int64_t kpad;
   int8_t *dbg_xq;
   const unsigned short *W16;   // null: no W16 gather
+  const int8_t *Wq;            // non-null (W16 null): gather the int8 weight's columns instead
   int64_t N;
   unsigned short *w16o;
   int64_t opad;
@@ -272,20 +274,24 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_rows_kernel(const Quan
   // W16 at a sparse outlier set, once per call: one warp per weight row,
   // w16o[n, j] = W16[n, O[j]] for j < |O|, zero up to the next multiple of
   // 64.  Each element is one scattered sector of W16, so every lane keeps
-  // four loads in flight.
-  if (p.W16 && !dense && nO > 0) {
+  // four loads in flight.  With only the int8 weight kept, its codes are
+  // gathered instead, as fp16 integers (exact).
+  if ((p.W16 || p.Wq) && !dense && nO > 0) {
     const int32_t jend = (nO + 63) & ~63;
     const int lane = threadIdx.x & 31;
     const int64_t warps = (int64_t)gridDim.x * (kQuantThreads / 32);
     for (int64_t n = (int64_t)blockIdx.x * (kQuantThreads / 32) + threadIdx.x / 32; n < p.N;
          n += warps) {
-      const unsigned short *wr = p.W16 + n * p.K;
+      const unsigned short *wr = p.W16 ? p.W16 + n * p.K : nullptr;
+      const int8_t *qr = p.Wq + n * p.K;
       for (int32_t j0 = 0; j0 < jend; j0 += 128) {
         unsigned short w[4];
 #pragma unroll
         for (int u = 0; u < 4; u++) {
           const int32_t j = j0 + lane + 32 * u;
-          w[u] = j < nO ? __ldg(wr + __ldg(p.O + j)) : (unsigned short)0;
+          w[u] = j >= nO ? (unsigned short)0
+                 : wr    ? __ldg(wr + __ldg(p.O + j))
+                         : __half_as_ushort(__short2half_rn((short)__ldg(qr + __ldg(p.O + j))));
         }
 #pragma unroll
         for (int u = 0; u < 4; u++) {
@@ -299,7 +305,8 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_rows_kernel(const Quan
 
 cudaError_t launch_act_pass(const void *X, int64_t T, int64_t K, uint32_t thr_bits,
                             const Workspace &ws, int code_mode, bool with_xo, const void *W16,
-                            int64_t N, int8_t *dbg_xq, int num_sms, cudaStream_t stream) {
+                            const int8_t *Wq, int64_t N, int8_t *dbg_xq, int num_sms,
+                            cudaStream_t stream) {
   // The caller has zeroed the status word, the counters and the column mask.
   cudaError_t e;
   // S2: 2-D grid, column slabs of 256 x row slabs, about 2 blocks per SM,
@@ -336,11 +343,12 @@ cudaError_t launch_act_pass(const void *X, int64_t T, int64_t K, uint32_t thr_bi
   a.kpad = ws.kpad;
   a.dbg_xq = dbg_xq;
   a.W16 = code_mode == 1 ? reinterpret_cast<const unsigned short *>(W16) : nullptr;
+  a.Wq = code_mode == 1 && W16 == nullptr ? Wq : nullptr;
   a.N = N;
   a.w16o = reinterpret_cast<unsigned short *>(ws.w16o);
   a.opad = ws.opad;
   int64_t qblocks = T < 16LL * num_sms ? T : 16LL * num_sms;
-  if (a.W16) {
+  if (a.W16 || a.Wq) {
     const int64_t gb = (N + 7) / 8 < 8LL * num_sms ? (N + 7) / 8 : 8LL * num_sms;
     if (gb > qblocks) qblocks = gb;
   }

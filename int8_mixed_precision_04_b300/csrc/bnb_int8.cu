@@ -143,21 +143,25 @@ static int choose_path(int64_t T, int64_t N, int64_t K, int dev) {
   return force_mma() ? 3 : 2;
 }
 
-// The argument checks of bnb_int8_linear (nothing is enqueued).
+// The argument checks of bnb_int8_linear (nothing is enqueued).  W16 may be
+// null only where the caller keeps the int8 weight alone (w16_optional).
 static bnb_status_t linear_check(const void *X, int64_t T, int64_t K, const int8_t *Wq,
                                  const float *Wscale, const void *W16, int64_t N, float tau,
-                                 const void *Y, const void *workspace, size_t workspace_bytes) {
-  if (!X || !Wq || !Wscale || !W16 || !Y || !workspace) return BNB_ERR_INVALID_ARG;
+                                 const void *Y, const void *workspace, size_t workspace_bytes,
+                                 bool w16_optional = false) {
+  if (!X || !Wq || !Wscale || !Y || !workspace) return BNB_ERR_INVALID_ARG;
+  if (!W16 && !w16_optional) return BNB_ERR_INVALID_ARG;
   if (T <= 0 || N <= 0 || K <= 0) return BNB_ERR_INVALID_ARG;
   if (std::isnan(tau) || tau < 0.0f) return BNB_ERR_INVALID_ARG;
   if (T > BNB_MAX_T || N > BNB_MAX_N || K > BNB_MAX_K) return BNB_ERR_UNSUPPORTED;
   if (workspace_bytes < bnb_int8_linear_workspace_bytes(T, N, K)) return BNB_ERR_INVALID_ARG;
   if (K % 16 != 0) return BNB_ERR_UNSUPPORTED;
-  if (!aligned16(X) || !aligned16(Wq) || !aligned16(Wscale) || !aligned16(W16) ||
+  if (!aligned16(X) || !aligned16(Wq) || !aligned16(Wscale) || (W16 && !aligned16(W16)) ||
       !aligned16(Y) || !aligned16(workspace))
     return BNB_ERR_UNSUPPORTED;
   const size_t ybytes = (size_t)T * (size_t)N * 2;
-  if (overlaps(Y, ybytes, X, (size_t)T * K * 2) || overlaps(Y, ybytes, W16, (size_t)N * K * 2) ||
+  if (overlaps(Y, ybytes, X, (size_t)T * K * 2) ||
+      (W16 && overlaps(Y, ybytes, W16, (size_t)N * K * 2)) ||
       overlaps(Y, ybytes, Wq, (size_t)N * K) || overlaps(Y, ybytes, workspace, workspace_bytes))
     return BNB_ERR_INVALID_ARG;
   return BNB_OK;
@@ -169,7 +173,9 @@ static bnb_status_t linear_impl(const void *X, int64_t T, int64_t K, const int8_
                                 size_t workspace_bytes,
                                 void *stream_v, int8_t *dbg_xq, float *dbg_sx,
                                 int32_t *dbg_O, int32_t *dbg_nO, int32_t *dbg_acc) {
-  bnb_status_t chk = linear_check(X, T, K, Wq, Wscale, W16, N, tau, Y, workspace, workspace_bytes);
+  // (the entry points check W16 themselves: null means the int8 weight alone)
+  bnb_status_t chk = linear_check(X, T, K, Wq, Wscale, W16, N, tau, Y, workspace, workspace_bytes,
+                                  /*w16_optional=*/true);
   if (chk != BNB_OK) return chk;
   if ((dbg_xq && !aligned16(dbg_xq)) || (dbg_acc && !aligned16(dbg_acc)))
     return BNB_ERR_UNSUPPORTED;
@@ -201,7 +207,7 @@ static bnb_status_t linear_impl(const void *X, int64_t T, int64_t K, const int8_
       // the tcgen05 GEMM reads fp16 integer codes, the mma GEMM int8 codes
       // (for the tcgen05 GEMM the same launch compacts W16 at a sparse outlier set)
       e = launch_act_pass(X, T, K, thr, ws, /*code_mode=*/path == 2 ? 1 : 0, /*with_xo=*/true,
-                          W16, N, dbg_xq, device_sms(dev), stream);
+                          W16, Wq, N, dbg_xq, device_sms(dev), stream);
       if (e != cudaSuccess) return BNB_ERR_CUDA;
     }
     if (path == 2)
@@ -286,6 +292,7 @@ bnb_status_t bnb_int8_dequantize_blockwise(const int8_t *codes, const float *abs
 bnb_status_t bnb_int8_linear(const void *X, int64_t T, int64_t K, const int8_t *Wq,
                              const float *Wscale, const void *W16, int64_t N, float tau,
                              void *Y, void *workspace, size_t workspace_bytes, void *stream) {
+  if (!W16) return BNB_ERR_INVALID_ARG;
   return linear_impl(X, T, K, Wq, Wscale, W16, nullptr, N, tau, Y, workspace, workspace_bytes,
                      stream, nullptr, nullptr, nullptr, nullptr, nullptr);
 }
@@ -294,7 +301,16 @@ bnb_status_t bnb_int8_linear_bias(const void *X, int64_t T, int64_t K, const int
                                   const float *Wscale, const void *W16, const void *bias,
                                   int64_t N, float tau, void *Y, void *workspace,
                                   size_t workspace_bytes, void *stream) {
+  if (!W16) return BNB_ERR_INVALID_ARG;
   return linear_impl(X, T, K, Wq, Wscale, W16, bias, N, tau, Y, workspace, workspace_bytes,
+                     stream, nullptr, nullptr, nullptr, nullptr, nullptr);
+}
+
+bnb_status_t bnb_int8_linear_wq_only(const void *X, int64_t T, int64_t K, const int8_t *Wq,
+                                     const float *Wscale, const void *bias, int64_t N,
+                                     float tau, void *Y, void *workspace,
+                                     size_t workspace_bytes, void *stream) {
+  return linear_impl(X, T, K, Wq, Wscale, nullptr, bias, N, tau, Y, workspace, workspace_bytes,
                      stream, nullptr, nullptr, nullptr, nullptr, nullptr);
 }
 
@@ -311,7 +327,7 @@ bnb_status_t bnb_int8_linear_from_host(const void *X_host, int64_t T, int64_t K,
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   // the layer's own argument checks run before anything is enqueued
   bnb_status_t r = linear_check(X_dev, T, K, Wq, Wscale, W16, N, tau, Y_dev, workspace,
-                                workspace_bytes);
+                                workspace_bytes, /*w16_optional=*/true);
   if (r != BNB_OK) return r;
   if (bias && !aligned16(bias)) return BNB_ERR_UNSUPPORTED;
   if (bias && overlaps(Y_dev, ybytes, bias, (size_t)N * 2)) return BNB_ERR_INVALID_ARG;
@@ -330,6 +346,7 @@ bnb_status_t bnb_int8_linear_debug(const void *X, int64_t T, int64_t K, const in
                                    void *Y, void *workspace, size_t workspace_bytes,
                                    void *stream, int8_t *Xq, float *Xscale,
                                    int32_t *outlier_idx, int32_t *n_outliers, int32_t *acc) {
+  if (!W16) return BNB_ERR_INVALID_ARG;
   return linear_impl(X, T, K, Wq, Wscale, W16, nullptr, N, tau, Y, workspace, workspace_bytes,
                      stream, Xq, Xscale, outlier_idx, n_outliers, acc);
 }

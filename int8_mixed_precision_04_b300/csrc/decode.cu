@@ -31,7 +31,10 @@
 // consumers split any further ones.  Epilogue (one output per consumer
 // thread): the int32 partials are summed, scaled by (sx/127)(sw/127), the
 // 16-bit outlier product is added ("converted back to 16-bit at the end",
-// same page, section 2) and Y is written once.
+// same page, section 2), then the bias if any, and Y is written once.
+// With only the int8 weight kept (W16 null) the outlier weights are the
+// slice's own codes, already in shared memory: Y = fp16((acc sx/127 +
+// sum_{k in O} X Wq) sw/127 + b), and no W16 byte is read.
 #include <atomic>
 #include <cstdlib>
 
@@ -178,7 +181,7 @@ __device__ __forceinline__ void dec_mma_range(const uint8_t *xs, const uint8_t *
   }
 }
 
-template <int kC>
+template <int kC, bool kWq>  // kWq: only the int8 weight is kept (W16 null)
 __global__ void __launch_bounds__(kDecThreads, 1)
     dec_fused_kernel(const __grid_constant__ CUtensorMap tm_w16, const DecArgs p) {
   using G = DecAct<kC>;
@@ -269,7 +272,9 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       for (int c = 0; c < kC; c++) nO += (int32_t)sm.pubs[c][16];
     const int32_t nsmall = min(nO, kDecOutSmall);
     if (rows > 0) {
-      const bool fetch = ok && nsmall > 0 && mbar_wait_cluster_bounded(&sm.xbar, 0, p.status);
+      // (without W16 the consumers read the outlier weights from the slice)
+      const bool fetch = !kWq && ok && nsmall > 0 &&
+                         mbar_wait_cluster_bounded(&sm.xbar, 0, p.status);
       if (lane == 0)
         mbar_expect_tx(&sm.wobar, fetch ? (uint32_t)(nsmall * 16 * p.rows_per_cta) : 0u);
       __syncwarp();
@@ -527,6 +532,21 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     else
       dec_mma_range<true>(xs, ws, pitch, g, q, k0, k1, ng, acc);
   }
+  // Only the int8 weight kept (W16 null): the outlier weights are the slice's
+  // own codes, Wq sw / 127, with sw / 127 applied in the epilogue.  The first
+  // outlier columns are read here, before the reduction reuses the weight
+  // region (every thread waits for the slice: some warps had no K-range).
+  constexpr bool wfree = kWq;
+  float e_small[2] = {0.f, 0.f};
+  if (wfree && mbar_wait_bounded(&sm.wbar, 0, p.status)) {
+    const int nsm = nO < kDecOutSmall ? nO : kDecOutSmall;
+#pragma unroll
+    for (int it = 0; it < 2; it++)
+      if (it < nitems && e_n[it] < rows)
+        for (int j = 0; j < nsm; j++)
+          e_small[it] = fmaf(h2f_bits(sm.xo[e_t[it] * kDecOutSmall + j]),
+                             (float)(int8_t)ws[e_n[it] * pitch + sm.oc[j]], e_small[it]);
+  }
   // outlier columns beyond the first kDecOutSmall: split over the consumer
   // warps, from the producer warp's list
   const bool big = nO > kDecOutSmall &&  // the same in every warp
@@ -539,10 +559,12 @@ __global__ void __launch_bounds__(kDecThreads, 1)
 #pragma unroll
     for (int gi = 0; gi < kDecGroups; gi++) {
       if (gi < ng) {
-        const int64_t na = n0 + min((int64_t)gi * 8 + 2 * q, rows - 1);
-        const int64_t nb = n0 + min((int64_t)gi * 8 + 2 * q + 1, rows - 1);
-        const float wa = h2f_bits(__ldg(p.W16 + na * K + k));
-        const float wb = h2f_bits(__ldg(p.W16 + nb * K + k));
+        const int64_t ra = min((int64_t)gi * 8 + 2 * q, rows - 1);
+        const int64_t rb = min((int64_t)gi * 8 + 2 * q + 1, rows - 1);
+        const float wa = wfree ? (float)(int8_t)ws[ra * pitch + k]
+                               : h2f_bits(__ldg(p.W16 + (n0 + ra) * K + k));
+        const float wb = wfree ? (float)(int8_t)ws[rb * pitch + k]
+                               : h2f_bits(__ldg(p.W16 + (n0 + rb) * K + k));
         o[gi][0] = fmaf(x0, wa, o[gi][0]);
         o[gi][1] = fmaf(x0, wb, o[gi][1]);
         o[gi][2] = fmaf(x1, wa, o[gi][2]);
@@ -568,7 +590,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
 #pragma unroll
       for (int w = 0; w < kDecWarps; w++) e_acc[it] += (int)red[(w * 32 + el) * kDecRedStride + idx];
     }
-  float e_out[2] = {0.f, 0.f};
+  float e_out[2] = {e_small[0], e_small[1]};
   if (big) {
     named_bar_sync(1, kDecConsumers);
 #pragma unroll
@@ -590,7 +612,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   const bool ok_o = mbar_wait_bounded(&sm.wobar, 0, p.status);
 #pragma unroll
   for (int it = 0; it < 2; it++)
-    if (it < nitems && e_n[it] < rows)
+    if (!wfree && it < nitems && e_n[it] < rows)
       for (int j = 0; j < nsmall; j++)
         e_out[it] = fmaf(h2f_bits(sm.xo[e_t[it] * kDecOutSmall + j]),
                          h2f_bits(sm.wos[j][e_n[it]][sm.oc[j] & 7u]), e_out[it]);
@@ -601,7 +623,8 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       const int64_t n = n0 + nl;
       const float st = sxs[t] / 127.0f, sn = e_sw[it] / 127.0f;
       const float b = h2f_bits(sm.bias[nl]);  // 0 without a bias
-      const float y = fmaf((float)e_acc[it] * st, sn, e_out[it] + b);
+      const float y = wfree ? fmaf(fmaf((float)e_acc[it], st, e_out[it]), sn, b)
+                            : fmaf((float)e_acc[it] * st, sn, e_out[it] + b);
       p.Y[t * p.N + n] = __float2half_rn(y);
       if (p.dbg_acc) p.dbg_acc[t * p.N + n] = e_acc[it];
     }
@@ -620,13 +643,14 @@ constexpr int kDecClusterSizes[3] = {8, 16, 4};  // order of preference (measure
 // fails); also opens the kernel's shared-memory limit to `dyn_max`.
 template <int kC>
 int dec_resident_ctas(int dyn_max) {
-  if (cudaFuncSetAttribute(dec_fused_kernel<kC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           dyn_max) != cudaSuccess)
-    return 0;
-  if (kC > 8 && cudaFuncSetAttribute(dec_fused_kernel<kC>,
-                                     cudaFuncAttributeNonPortableClusterSizeAllowed,
-                                     1) != cudaSuccess)
-    return 0;
+  for (auto *f : {dec_fused_kernel<kC, false>, dec_fused_kernel<kC, true>}) {
+    if (cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn_max) !=
+        cudaSuccess)
+      return 0;
+    if (kC > 8 &&
+        cudaFuncSetAttribute(f, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
+      return 0;
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(kC * 16);
   cfg.blockDim = dim3(kDecThreads);
@@ -638,9 +662,10 @@ int dec_resident_ctas(int dyn_max) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, dec_fused_kernel<kC>, &cfg) != cudaSuccess) n = 0;
-  return n * kC;
+  int n = 0, n1 = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, dec_fused_kernel<kC, false>, &cfg) != cudaSuccess) n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n1, dec_fused_kernel<kC, true>, &cfg) != cudaSuccess) n1 = 0;
+  return (n < n1 ? n : n1) * kC;  // both forms must fit
 }
 
 struct DecCfg {
@@ -662,7 +687,7 @@ DecCfg decode_cfg(int dev) {
   DecCfg r{{0, 0, 0}, 0};
   if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev < 0 ? 0 : dev) ==
           cudaSuccess &&
-      cudaFuncGetAttributes(&fa, dec_fused_kernel<8>) == cudaSuccess) {
+      cudaFuncGetAttributes(&fa, dec_fused_kernel<8, false>) == cudaSuccess) {
     r.dyn_max = optin - (int)fa.sharedSizeBytes;
     r.ctas[0] = dec_resident_ctas<8>(r.dyn_max);
     r.ctas[1] = dec_resident_ctas<16>(r.dyn_max);
@@ -740,11 +765,15 @@ cudaError_t launch_decode(const void *X, int64_t T, int64_t K, uint32_t thr, con
   a.wregion = dec_wregion(K, a.rows_per_cta);
   // W16 in boxes of 8 columns x one slice's channels (outlier columns only,
   // so no L2 promotion beyond the sector)
+  // (without W16 the map is never read: it then describes Wq)
   CUtensorMap tm;
-  if (!encode_2d(&tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, W16, (uint64_t)K, (uint64_t)N,
-                 (uint64_t)K * 2, 8, (uint32_t)a.rows_per_cta, CU_TENSOR_MAP_SWIZZLE_NONE,
-                 CU_TENSOR_MAP_L2_PROMOTION_NONE))
-    return cudaErrorInvalidValue;
+  const bool enc = W16 ? encode_2d(&tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, W16, (uint64_t)K,
+                                   (uint64_t)N, (uint64_t)K * 2, 8, (uint32_t)a.rows_per_cta,
+                                   CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE)
+                       : encode_2d(&tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, Wq, (uint64_t)K,
+                                   (uint64_t)N, (uint64_t)K, 16, (uint32_t)a.rows_per_cta,
+                                   CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE);
+  if (!enc) return cudaErrorInvalidValue;
   a.Wq = Wq;
   a.sw = sw;
   a.W16 = reinterpret_cast<const unsigned short *>(W16);
@@ -771,9 +800,11 @@ cudaError_t launch_decode(const void *X, int64_t T, int64_t K, uint32_t thr, con
   cfg.attrs = attr;
   cfg.numAttrs = profile_only_main() ? 1 : 2;  // profiling mode 2: no overlap with the previous call
   ProfScope ps(kKidDecFused, stream);
-  const cudaError_t e = kc == 8    ? cudaLaunchKernelEx(&cfg, dec_fused_kernel<8>, tm, a)
-                        : kc == 16 ? cudaLaunchKernelEx(&cfg, dec_fused_kernel<16>, tm, a)
-                                   : cudaLaunchKernelEx(&cfg, dec_fused_kernel<4>, tm, a);
+  const bool wq = W16 == nullptr;
+  const cudaError_t e =
+      kc == 8    ? cudaLaunchKernelEx(&cfg, wq ? dec_fused_kernel<8, true> : dec_fused_kernel<8, false>, tm, a)
+      : kc == 16 ? cudaLaunchKernelEx(&cfg, wq ? dec_fused_kernel<16, true> : dec_fused_kernel<16, false>, tm, a)
+                 : cudaLaunchKernelEx(&cfg, wq ? dec_fused_kernel<4, true> : dec_fused_kernel<4, false>, tm, a);
   note_launch();
   return e;
 }

@@ -7,7 +7,9 @@
 //      top of it in fp32 (the outlier dimensions "computed in 16-bit",
 //      "Hugging Face Quantization with bitsandbytes", section 2);
 // then Y is written once in fp16.  The outlier columns of W16 are gathered
-// into shared memory per 32-column block.
+// into shared memory per 32-column block.  With only the int8 weight kept
+// (W16 null) the gathered columns are Wq's codes as fp16 integers, and
+// sw / 127 scales the int8 and outlier sums together at the store.
 //
 // This is the legacy warp-level tensor path (compiled for sm_103a but not
 // tcgen05); it also serves as the exact-int8 comparison route.
@@ -99,8 +101,13 @@ __global__ void __launch_bounds__(kMmaThreads) gemm_mma_kernel(
         float v = 0.f;
         if (t < T && n < N) {
           if (dbg_acc) dbg_acc[t * N + n] = acc[mt][nt][i];
-          v = (float)acc[mt][nt][i] * __fdiv_rn(sx[t], 127.0f) * __fdiv_rn(sw[n], 127.0f);
-          if (bias) v += h2f_bits(__ldg(bias + n));
+          // with only the int8 weight, sw / 127 is applied at the store,
+          // to the int8 and outlier sums at once (and the bias after it)
+          v = (float)acc[mt][nt][i] * __fdiv_rn(sx[t], 127.0f);
+          if (W16) {
+            v *= __fdiv_rn(sw[n], 127.0f);
+            if (bias) v += h2f_bits(__ldg(bias + n));
+          }
         }
         y[mt][nt][i] = v;
       }
@@ -126,7 +133,9 @@ __global__ void __launch_bounds__(kMmaThreads) gemm_mma_kernel(
       for (int rr = 0; rr < 16; rr++) {
         const int r = warp * 16 + rr;
         unsigned short v = 0;
-        if (j < nO && n0 + r < N) v = __ldg(W16 + (n0 + r) * K + k);
+        if (j < nO && n0 + r < N)
+          v = W16 ? __ldg(W16 + (n0 + r) * K + k)
+                  : __half_as_ushort(__short2half_rn((short)__ldg(Wq + (n0 + r) * K + k)));
         Bh[r * 32 + lane] = v;
       }
     }
@@ -161,6 +170,15 @@ __global__ void __launch_bounds__(kMmaThreads) gemm_mma_kernel(
         const int64_t t = m0 + wm * 64 + mt * 16 + g + 8 * h;
         const int64_t n = n0 + wn * 32 + nt * 8 + 2 * q;
         if (t >= T) continue;
+        if (!W16) {
+#pragma unroll
+          for (int u = 0; u < 2; u++)
+            if (n + u < N) {
+              float &yy = y[mt][nt][2 * h + u];
+              yy *= __fdiv_rn(sw[n + u], 127.0f);
+              if (bias) yy += h2f_bits(__ldg(bias + n + u));
+            }
+        }
         const __half lo = __float2half_rn(y[mt][nt][2 * h]);
         const __half hi = __float2half_rn(y[mt][nt][2 * h + 1]);
         if (n + 1 < N && ((t * N + n) & 1) == 0) {

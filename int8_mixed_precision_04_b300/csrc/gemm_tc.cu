@@ -32,6 +32,11 @@
 // XO; or, when outliers are dense (more than K/16), a dense fp16 product over
 // all K columns with A = W16 tiles and B = X masked to the outlier columns.
 // The epilogue combines both and writes Y once.
+// With only the int8 weight kept (W16 null) the outlier weights are the codes
+// dequantized, Wq sw / 127: the sparse route reads Wq's compacted outlier
+// columns (fp16 integers), the dense route widens Wq's own tiles like the int8
+// stages, and the epilogue applies sw / 127 to the int8 and outlier sums at
+// once: Y = fp16((acc sx/127 + sum_{k in O} X Wq) sw/127 + b).
 //
 // Warp roles (20 warps): 0 TMA producer, 1 MMA issuer and tensor-memory
 // owner, 2-3 converters (two weight rows per thread), 4-19 epilogue (four
@@ -107,7 +112,7 @@ struct TcArgs {
   int t_tiles, n_tiles;
   int s_int;  // k stages of the int8 part, ceil(K / 64)
   const float *sw;
-  const unsigned short *W16;
+  const unsigned short *W16;  // null: only the int8 weight (outlier weights Wq sw / 127)
   const unsigned short *bias;  // [N] fp16 or null
   __half *Y;
   const float *sxd;  // [T] sx / 127
@@ -170,13 +175,14 @@ __device__ __forceinline__ void widen16(const uint4 &v, uint4 &g0, uint4 &g1) {
   s8x4_to_f16x4(v.w, g1.z, g1.w);
 }
 
-// Converter warps: widen the int8 weight tile of each int8 stage into the
-// fp16 A operand.  In the outlier stages TMA has put the fp16 A tile there
-// already (W16, or its compacted outlier columns); the converters only pass
-// the stage on to the MMA.
+// Converter warps: widen the int8 weight tile of each of the first s_conv
+// stages into the fp16 A operand: the int8 stages, and the dense outlier
+// stages when only the int8 weight is kept.  In the other outlier stages TMA
+// has put the fp16 A tile there already (W16, or the compacted outlier
+// columns); the converters only pass the stage on to the MMA.
 // Thread ct owns weight rows ct, ct + 32 * kConvWarps, ...
 __device__ __forceinline__ void converter_role(uint8_t *smem, TcSmem &sm, const TcArgs &p,
-                                               int s_int, int nst, int ntiles) {
+                                               int s_conv, int nst, int ntiles) {
   const int ct = threadIdx.x - kConvWarp0 * 32;  // 0 .. 32 * kConvWarps - 1
   const int lane = threadIdx.x & 31;
   uint32_t it = 0;
@@ -188,7 +194,7 @@ __device__ __forceinline__ void converter_role(uint8_t *smem, TcSmem &sm, const 
         ok = false;
         break;
       }
-      if (s < s_int) {
+      if (s < s_conv) {
 #pragma unroll
         for (int h = 0; h < kConvRows; ++h) {
           const int r = ct + kConvWarps * 32 * h;
@@ -262,6 +268,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int s_out = dense ? s_int : (nO + kBK - 1) / kBK;
   const int nst = s_int + s_out;
   const int ntiles = p.t_tiles * p.n_tiles;
+  // only the int8 weight kept: the dense outlier stages widen its tiles too
+  // (the sparse ones read its compacted outlier columns, already fp16)
+  const bool wq_out = dense && p.W16 == nullptr;
+  const int s_conv = wq_out ? nst : s_int;
 
   // Register split (see kRegs*): each warpgroup's branch starts with its own
   // setmaxnreg and never rejoins the others.
@@ -284,6 +294,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_expect_tx(&sm.full[st], kXBytes + kWqBytes);
             tma_load_2d(stage_x(smem, st), &tm_x, s * kBK, t0, &sm.full[st]);
             tma_load_2d(stage_wq(smem, st), &tm_w, s * kBK, n0, &sm.full[st]);
+          } else if (wq_out) {  // outlier stage on the int8 weight tile
+            mbar_expect_tx(&sm.full[st], kXBytes + kWqBytes);
+            tma_load_2d(stage_x(smem, st), &tm_xo, (s - s_int) * kBK, t0, &sm.full[st]);
+            tma_load_2d(stage_wq(smem, st), &tm_w, (s - s_int) * kBK, n0, &sm.full[st]);
           } else {  // outlier stage: fp16 A tile straight into the A operand slot
             mbar_expect_tx(&sm.full[st], kXBytes + kWhBytes);
             tma_load_2d(stage_x(smem, st), &tm_xo, (s - s_int) * kBK, t0, &sm.full[st]);
@@ -342,10 +356,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       tmem_dealloc(tmem, kTmemCols);
     }
-    if (kConvWarps == 2 && warp >= kConvWarp0) converter_role(smem, sm, p, s_int, nst, ntiles);
+    if (kConvWarps == 2 && warp >= kConvWarp0) converter_role(smem, sm, p, s_conv, nst, ntiles);
   } else if (kConvWarps == 4 && warp < kEpiWarp0) {
     regs_dec<kRegsConv>();
-    converter_role(smem, sm, p, s_int, nst, ntiles);
+    converter_role(smem, sm, p, s_conv, nst, ntiles);
   } else {
     regs_inc<kRegsEpi>();
     // ---------------- epilogue ----------------
@@ -411,9 +425,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         float sx[8];
         ld_scales8(p.sxd, tj, T, sx);
+        if (p.W16) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-          o[i] = __float_as_uint(fmaf((float)acc[8 * j + i] * sx[i], swn, __uint_as_float(o[i]) + bn));
+          for (int i = 0; i < 8; ++i)
+            o[i] = __float_as_uint(fmaf((float)acc[8 * j + i] * sx[i], swn, __uint_as_float(o[i]) + bn));
+        } else {  // the outlier sum is over the codes: scaled by sw / 127 with the int8 part
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            o[i] = __float_as_uint(fmaf(fmaf((float)acc[8 * j + i], sx[i], __uint_as_float(o[i])), swn, bn));
+        }
         // lanes pair up so that each store writes two adjacent channels
 #pragma unroll
         for (int i = 0; i < 8; i += 2) {
@@ -472,8 +492,13 @@ cudaError_t launch_gemm_tc(int64_t T, int64_t K, const int8_t *Wq, const float *
       // the outlier block's inner extent is K (columns past K read as zeros)
       !encode_2d(&tm_xo, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, ws.xo, (uint64_t)K, (uint64_t)T,
                  (uint64_t)ws.kpad * 2, kBK, kBN, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B) ||
-      !encode_2d(&tm_w16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, W16, (uint64_t)K, (uint64_t)N,
-                 (uint64_t)K * 2, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B) ||
+      // without W16 this map is never read; it then describes the compacted columns
+      !(W16 ? encode_2d(&tm_w16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, W16, (uint64_t)K, (uint64_t)N,
+                        (uint64_t)K * 2, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B)
+            : encode_2d(&tm_w16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, ws.w16o, (uint64_t)ws.opad,
+                        (uint64_t)N, (uint64_t)ws.opad * 2, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B)) ||
       !encode_2d(&tm_w16o, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, ws.w16o, (uint64_t)ws.opad,
                  (uint64_t)N, (uint64_t)ws.opad * 2, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B))
     return cudaErrorInvalidValue;

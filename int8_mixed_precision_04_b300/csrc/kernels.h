@@ -59,7 +59,8 @@ cudaError_t launch_quantize_weight(const void *W16, int64_t N, int64_t K, int8_t
 // the padded fp16 outlier block.
 cudaError_t launch_act_pass(const void *X, int64_t T, int64_t K, uint32_t thr_bits,
                             const Workspace &ws, int code_mode, bool with_xo, const void *W16,
-                            int64_t N, int8_t *dbg_xq, int num_sms, cudaStream_t stream);
+                            const int8_t *Wq, int64_t N, int8_t *dbg_xq, int num_sms,
+                            cudaStream_t stream);
 
 // The blockwise 8-bit codec (blocks of B values, B a power of two in
 // [64, 2048]): fp32 -> int8 codes + per-block absmax, and back.

@@ -187,3 +187,29 @@ def test_linear_bias_rejects_on_host(lib, case, want):
     rc = lib.bnb_int8_linear_bias(a["X"], a["T"], a["K"], FAKE, FAKE, FAKE, a["bias"], a["N"],
                                   ctypes.c_float(a["tau"]), a["Y"], a["ws"], ws_bytes, None)
     assert rc == want
+
+
+@pytest.mark.parametrize("case,want", [
+    (dict(X=None), binding.Status.INVALID_ARG),
+    (dict(Wq=None), binding.Status.INVALID_ARG),
+    (dict(K=24), binding.Status.UNSUPPORTED),
+    (dict(bias=FAKE * 64 + 8), binding.Status.UNSUPPORTED),
+    (dict(Y=FAKE), binding.Status.INVALID_ARG),                # Y aliases X
+])
+def test_linear_wq_only_rejects_on_host(lib, case, want):
+    """bnb_int8_linear_wq_only checks its arguments (no W16 to check)."""
+    a = dict(X=FAKE, T=16, K=256, N=256, tau=6.0, Wq=FAKE * 16, bias=None, Y=FAKE * 64,
+             ws=FAKE * 256)
+    a.update(case)
+    ws_bytes = lib.bnb_int8_linear_workspace_bytes(a["T"], a["N"], max(a["K"], 16))
+    rc = lib.bnb_int8_linear_wq_only(a["X"], a["T"], a["K"], a["Wq"], FAKE * 8, a["bias"], a["N"],
+                                     ctypes.c_float(a["tau"]), a["Y"], a["ws"], ws_bytes, None)
+    assert rc == want
+
+
+def test_fp16_weight_entry_points_need_w16(lib):
+    """Only the int8-weight-only entry points accept a NULL W16."""
+    ws_bytes = lib.bnb_int8_linear_workspace_bytes(16, 256, 256)
+    assert lib.bnb_int8_linear_bias(FAKE, 16, 256, FAKE, FAKE, None, None, 256,
+                                    ctypes.c_float(6.0), FAKE * 64, FAKE * 256, ws_bytes,
+                                    None) == binding.Status.INVALID_ARG
