@@ -40,6 +40,22 @@ def _ptr(a: np.ndarray):
     return a.ctypes.data_as(_P)
 
 
+_FMT = {"fp16": 0, "bf16": 1}
+
+
+def _bits16(a, fmt: str) -> np.ndarray:
+    """16-bit element bit patterns, C-contiguous: float16 arrays for fp16,
+    uint16 arrays of bfloat16 bit patterns for bf16."""
+    if fmt == "fp16":
+        return np.ascontiguousarray(a, dtype=np.float16).view(np.uint16)
+    if fmt == "bf16":
+        a = np.asarray(a)
+        if a.dtype != np.uint16:
+            raise TypeError("bf16 data is passed as uint16 bit patterns")
+        return np.ascontiguousarray(a)
+    raise ValueError(fmt)
+
+
 class Oracle:
     """ctypes front of ``liboracle.so`` (compiled on first use)."""
 
@@ -50,6 +66,10 @@ class Oracle:
         lib.orc_half_to_double.argtypes = [ctypes.c_uint16]
         lib.orc_double_to_half.restype = ctypes.c_uint16
         lib.orc_double_to_half.argtypes = [ctypes.c_double]
+        lib.orc_bf16_to_double.restype = ctypes.c_double
+        lib.orc_bf16_to_double.argtypes = [ctypes.c_uint16]
+        lib.orc_double_to_bf16.restype = ctypes.c_uint16
+        lib.orc_double_to_bf16.argtypes = [ctypes.c_double]
         for name in ("orc_quantize_weight", "orc_outlier_columns",
                      "orc_quantize_activations", "orc_int8_matmul_rows",
                      "orc_linear_rows", "orc_quantize_blockwise", "orc_dequantize_blockwise"):
@@ -65,6 +85,12 @@ class Oracle:
 
     def double_to_half(self, v: float) -> int:
         return self.lib.orc_double_to_half(v)
+
+    def bf16_to_double(self, bits: int) -> float:
+        return self.lib.orc_bf16_to_double(bits)
+
+    def double_to_bf16(self, v: float) -> int:
+        return self.lib.orc_double_to_bf16(v)
 
     # ---- the blockwise 8-bit codec of optimizer states ---------------------------
     def quantize_blockwise(self, x: np.ndarray, block: int):
@@ -88,38 +114,43 @@ class Oracle:
         return y
 
     # ---- S1 -------------------------------------------------------------------
-    def quantize_weight(self, W16: np.ndarray):
-        W16 = np.ascontiguousarray(W16, dtype=np.float16)
+    def quantize_weight(self, W16: np.ndarray, fmt: str = "fp16"):
+        """fmt "fp16": W16 float16; fmt "bf16": W16 holds bfloat16 bit
+        patterns (uint16)."""
+        W16 = _bits16(W16, fmt)
         N, K = W16.shape
         Wq = np.empty((N, K), np.int8)
         sw = np.empty(N, np.float32)
-        rc = self.lib.orc_quantize_weight(_ptr(W16.view(np.uint16)), _I64(N), _I64(K),
-                                          _ptr(Wq), _ptr(sw))
+        rc = self.lib.orc_quantize_weight(_ptr(W16), _I64(N), _I64(K),
+                                          _ptr(Wq), _ptr(sw), _FMT[fmt])
         assert rc == 0, rc
         return Wq, sw
 
     # ---- S2 -------------------------------------------------------------------
-    def outlier_columns(self, X16: np.ndarray, tau: float):
-        X16 = np.ascontiguousarray(X16, dtype=np.float16)
+    def outlier_columns(self, X16: np.ndarray, tau: float, fmt: str = "fp16"):
+        X16 = _bits16(X16, fmt)
         T, K = X16.shape
         O = np.empty(max(K, 1), np.int32)
         n = ctypes.c_int32(0)
-        rc = self.lib.orc_outlier_columns(_ptr(X16.view(np.uint16)), _I64(T), _I64(K),
-                                          ctypes.c_float(tau), _ptr(O), ctypes.byref(n))
+        rc = self.lib.orc_outlier_columns(_ptr(X16), _I64(T), _I64(K),
+                                          ctypes.c_float(tau), _ptr(O), ctypes.byref(n),
+                                          _FMT[fmt])
         assert rc == 0, rc
         return O[: n.value].copy()
 
     # ---- S3 -------------------------------------------------------------------
-    def quantize_activations(self, X16: np.ndarray, O: np.ndarray):
-        X16 = np.ascontiguousarray(X16, dtype=np.float16)
+    def quantize_activations(self, X16: np.ndarray, O: np.ndarray, fmt: str = "fp16"):
+        X16 = _bits16(X16, fmt)
         T, K = X16.shape
         O = np.ascontiguousarray(O, dtype=np.int32)
         Xq = np.empty((T, K), np.int8)
         sx = np.empty(T, np.float32)
-        XO = np.empty((T, len(O)), np.float16)
+        XO = np.empty((T, len(O)), np.uint16)
         rc = self.lib.orc_quantize_activations(
-            _ptr(X16.view(np.uint16)), _I64(T), _I64(K), _ptr(O), ctypes.c_int32(len(O)),
-            _ptr(Xq), _ptr(sx), _ptr(XO.view(np.uint16)) if len(O) else None)
+            _ptr(X16), _I64(T), _I64(K), _ptr(O), ctypes.c_int32(len(O)),
+            _ptr(Xq), _ptr(sx), _ptr(XO) if len(O) else None, _FMT[fmt])
+        if fmt == "fp16":
+            XO = XO.view(np.float16)
         assert rc == 0, rc
         return Xq, sx, XO
 
@@ -138,14 +169,15 @@ class Oracle:
 
     # ---- S2..S6 ---------------------------------------------------------------
     def linear(self, X16: np.ndarray, Wq: np.ndarray, sw: np.ndarray, W16: np.ndarray,
-               tau: float, rows=None, bias=None):
+               tau: float, rows=None, bias=None, fmt: str = "fp16"):
         """Whole layer.  Returns a dict with O, Xq, sx (all rows) and, for
         ``rows`` (default: all), acc (int32), out (float64) and Y (float16).
         ``W16=None``: only the int8 weight is kept and the outlier weights are
-        its codes dequantized, Wq * sw / 127."""
-        X16 = np.ascontiguousarray(X16, dtype=np.float16)
+        its codes dequantized, Wq * sw / 127.  fmt "bf16": X16, W16, bias
+        and the returned Y are bfloat16 bit patterns (uint16)."""
+        X16 = _bits16(X16, fmt)
         if W16 is not None:
-            W16 = np.ascontiguousarray(W16, dtype=np.float16)
+            W16 = _bits16(W16, fmt)
         Wq = np.ascontiguousarray(Wq, dtype=np.int8)
         sw = np.ascontiguousarray(sw, dtype=np.float32)
         T, K = X16.shape
@@ -158,15 +190,17 @@ class Oracle:
         nO = ctypes.c_int32(0)
         acc = np.empty((R, N), np.int32)
         out = np.empty((R, N), np.float64)
-        Y = np.empty((R, N), np.float16)
+        Y = np.empty((R, N), np.uint16)
+        bias = None if bias is None else _bits16(bias, fmt)
         rc = self.lib.orc_linear_rows(
-            _ptr(X16.view(np.uint16)), _I64(T), _I64(K), _ptr(Wq), _ptr(sw),
-            None if W16 is None else _ptr(W16.view(np.uint16)), _I64(N), ctypes.c_float(tau),
-            None if bias is None else _ptr(np.ascontiguousarray(bias, dtype=np.float16).view(np.uint16)),
-            _ptr(rows), _I64(R),
+            _ptr(X16), _I64(T), _I64(K), _ptr(Wq), _ptr(sw),
+            None if W16 is None else _ptr(W16), _I64(N), ctypes.c_float(tau),
+            None if bias is None else _ptr(bias), _ptr(rows), _I64(R),
             _ptr(Xq), _ptr(sx), _ptr(O), ctypes.byref(nO), _ptr(acc), _ptr(out),
-            _ptr(Y.view(np.uint16)))
+            _ptr(Y), _FMT[fmt])
         assert rc == 0, "int32 accumulator overflow"
+        if fmt == "fp16":
+            Y = Y.view(np.float16)
         return {"O": O[: nO.value].copy(), "Xq": Xq, "sx": sx, "acc": acc, "out": out,
                 "Y": Y, "rows": rows}
 

@@ -30,6 +30,15 @@ def half_bits_to_fraction(bits: int) -> Fraction:
     return Fraction(v)
 
 
+def bf16_bits_to_fraction(bits: int) -> Fraction:
+    """Exact value of a bfloat16 bit pattern (finite values only): the high
+    half of the binary32 with the same leading bits."""
+    (v,) = struct.unpack("<f", struct.pack("<I", (bits & 0xFFFF) << 16))
+    if math.isinf(v) or math.isnan(v):
+        raise ValueError("non-finite bf16")
+    return Fraction(v)
+
+
 def round_half_even(q: Fraction) -> int:
     """Nearest integer to q, ties to the even one."""
     fl = math.floor(q)
@@ -62,6 +71,27 @@ def fraction_to_half_bits(v: Fraction) -> int:
     return sign | ((E + 15) << 10) | (n - 1024)
 
 
+def fraction_to_bf16_bits(v: Fraction) -> int:
+    """Round an exact rational to bfloat16 (8 significand bits, exponents
+    -126..127, subnormal quantum 2^-133), nearest-even, overflow -> inf."""
+    sign = 0x8000 if v < 0 else 0
+    a = -v if v < 0 else v
+    if a == 0:
+        return sign
+    E = a.numerator.bit_length() - a.denominator.bit_length()
+    if Fraction(2) ** E > a:
+        E -= 1
+    if E < -126:
+        n = round_half_even(a * 2 ** 133)
+        return sign | n                   # n == 128 is the smallest normal
+    n = round_half_even(a / Fraction(2) ** (E - 7))
+    if n == 256:
+        n, E = 128, E + 1
+    if E > 127:
+        return sign | 0x7F80
+    return sign | ((E + 127) << 7) | (n - 128)
+
+
 def code(x: Fraction, a: Fraction) -> int:
     """Vector-wise int8 code of x against absmax a (0 when a == 0)."""
     if a == 0:
@@ -69,18 +99,22 @@ def code(x: Fraction, a: Fraction) -> int:
     return round_half_even(Fraction(127) * x / a)
 
 
-def linear(X_bits, W_bits, tau: float, bias_bits=None, w16_free: bool = False):
+def linear(X_bits, W_bits, tau: float, bias_bits=None, w16_free: bool = False,
+           fmt: str = "fp16"):
     """The whole decomposition linear on tiny lists of fp16 bit patterns.
 
     X_bits: T lists of K ints, W_bits: N lists of K ints.  Returns a dict with
     O, Xq, sx, Wq, sw, acc and Y (fp16 bit patterns), all exact.  bias_bits:
     N fp16 bit patterns added before the final rounding (or None).
     w16_free: the outlier weights are the codes dequantized, Wq * sw / 127,
-    instead of W itself.
+    instead of W itself.  fmt "bf16": every bit pattern (in and out) is
+    bfloat16 instead of fp16.
     """
+    to_frac = bf16_bits_to_fraction if fmt == "bf16" else half_bits_to_fraction
+    to_bits = fraction_to_bf16_bits if fmt == "bf16" else fraction_to_half_bits
     T, K, N = len(X_bits), len(X_bits[0]) if X_bits else 0, len(W_bits)
-    X = [[half_bits_to_fraction(b) for b in row] for row in X_bits]
-    W = [[half_bits_to_fraction(b) for b in row] for row in W_bits]
+    X = [[to_frac(b) for b in row] for row in X_bits]
+    W = [[to_frac(b) for b in row] for row in W_bits]
     tau_f = Fraction(tau) if math.isfinite(tau) else None
     # outlier feature columns: any row at or above the threshold
     O = [k for k in range(K)
@@ -104,7 +138,7 @@ def linear(X_bits, W_bits, tau: float, bias_bits=None, w16_free: bool = False):
             else:
                 v += sum((X[t][k] * W[n][k] for k in O), Fraction(0))
             if bias_bits is not None:
-                v += half_bits_to_fraction(bias_bits[n])
-            row.append(fraction_to_half_bits(v))
+                v += to_frac(bias_bits[n])
+            row.append(to_bits(v))
         Y.append(row)
     return {"O": O, "Xq": Xq, "sx": sx, "Wq": Wq, "sw": sw, "acc": acc, "Y": Y}

@@ -38,6 +38,12 @@
  *    quantizes weights and activations") is added before the one rounding:
  *    Y = fp16_rne(acc*sx*sw/127^2 + sum_j X[t,O_j]*W[n,O_j] + b[n]).
  *
+ * X, W16, the bias and Y are fp16, or all bf16 (the compute dtype the pages
+ * prefer where the hardware supports it: Hugging Face page, section 5); the
+ * arithmetic is the same, only the 16-bit format of inputs and output changes
+ * -- except that bf16 codes scale x and a by one power of two first, since
+ * bf16's range lets 127 x overflow fp32 (the code itself is unchanged).
+ *
  * Codes are decided in fp32 because the kernel decides them in fp32; the
  * tests pin this rule against exact rational rounding.
  *
@@ -96,30 +102,95 @@ uint16_t orc_double_to_half(double v) {
   return sign | (uint16_t)(((E + 15) << 10) | ((int)n - 1024));
 }
 
+/* ---- bfloat16 <-> double, from the format's definition: 1 sign bit, 8
+ * exponent bits (bias 127), 7 fraction bits; the compute dtype the pages
+ * prefer where the hardware has it (Hugging Face page, section 5 "Storage
+ * Precision vs. Compute Precision") ---- */
+
+double orc_bf16_to_double(uint16_t h) {
+  int sign = (h >> 15) & 1;
+  int e = (h >> 7) & 0xff;
+  int m = h & 0x7f;
+  double v;
+  if (e == 0)
+    v = ldexp((double)m, -133); /* subnormal: m * 2^-133 */
+  else if (e == 255)
+    v = m ? NAN : INFINITY;
+  else
+    v = ldexp((double)(128 + m), e - 134); /* (1.m) * 2^(e-127) */
+  return sign ? -v : v;
+}
+
+/* Round a double to bfloat16, nearest-even, in one step. */
+uint16_t orc_double_to_bf16(double v) {
+  uint16_t sign = signbit(v) ? 0x8000 : 0;
+  double a = fabs(v);
+  if (isnan(v)) return 0x7fc0;
+  if (a >= ldexp(511.0, 119)) return sign | 0x7f80; /* tie between the largest finite and 2^128 */
+  if (a < ldexp(1.0, -126)) {
+    /* subnormal range: quantum 2^-133 */
+    double n = rint(ldexp(a, 133));
+    return sign | (uint16_t)n; /* n == 128 gives the smallest normal */
+  }
+  int e;
+  frexp(a, &e);
+  int E = e - 1; /* a in [2^E, 2^(E+1)) */
+  double n = rint(ldexp(a, 7 - E)); /* significand in units of 2^(E-7), in [128, 256] */
+  if (n >= 256.0) {
+    n = 128.0;
+    E += 1;
+  }
+  if (E + 127 >= 255) return sign | 0x7f80;
+  return sign | (uint16_t)(((E + 127) << 7) | ((int)n - 128));
+}
+
+/* The 16-bit element format of X, W16, the bias and Y: 0 fp16, 1 bf16. */
+static double elem_to_double(uint16_t b, int fmt) {
+  return fmt ? orc_bf16_to_double(b) : orc_half_to_double(b);
+}
+static uint16_t double_to_elem(double v, int fmt) {
+  return fmt ? orc_double_to_bf16(v) : orc_double_to_half(v);
+}
+
 /* ---- vector-wise code: q = rint(fl32(127*x) / a), in fp32 ---- */
 static int8_t code_of(float x, float a) {
   if (a == 0.0f) return 0;
-  float num = 127.0f * x; /* exact for fp16 x */
+  float num = 127.0f * x; /* exact for fp16 and bf16 x */
   float q = rintf(num / a);
   return (int8_t)q;
+}
+
+/* The same code for bf16 x and a, whose range (2^-133 .. 2^128) lets 127 x
+ * and the quotient leave fp32's: x and a are first scaled by the same power
+ * of two (exact; the code 127 x / a is unchanged) so that a lies in [1, 2).
+ * A value whose scaled form underflows has a code of 0 either way. */
+static int8_t code_of_scaled(float x, float a) {
+  if (a == 0.0f) return 0;
+  int e;
+  frexpf(a, &e); /* a = f * 2^e, f in [0.5, 1) */
+  return code_of(ldexpf(x, 1 - e), ldexpf(a, 1 - e));
+}
+
+static int8_t code_fmt(float x, float a, int fmt) {
+  return fmt ? code_of_scaled(x, a) : code_of(x, a);
 }
 
 /* S1: per-output-channel absmax scale and int8 codes of the weight.
  * "quantizes weights on the fly as the model loads" (page "bitsandbytes",
  * d-central glossary); row-wise / per output channel. */
 int orc_quantize_weight(const uint16_t *W16, int64_t N, int64_t K, int8_t *Wq,
-                        float *sw) {
+                        float *sw, int fmt) {
   if (N < 0 || K < 0) return ORC_ERR_ARG;
 #pragma omp parallel for schedule(static)
   for (int64_t n = 0; n < N; n++) {
     float a = 0.0f;
     for (int64_t k = 0; k < K; k++) {
-      float x = fabsf((float)orc_half_to_double(W16[n * K + k]));
+      float x = fabsf((float)elem_to_double(W16[n * K + k], fmt));
       if (x > a) a = x;
     }
     sw[n] = a;
     for (int64_t k = 0; k < K; k++)
-      Wq[n * K + k] = code_of((float)orc_half_to_double(W16[n * K + k]), a);
+      Wq[n * K + k] = code_fmt((float)elem_to_double(W16[n * K + k], fmt), a, fmt);
   }
   return ORC_OK;
 }
@@ -127,13 +198,13 @@ int orc_quantize_weight(const uint16_t *W16, int64_t N, int64_t K, int8_t *Wq,
 /* S2: outlier feature columns.  Column k is an outlier when some row t has
  * |X[t,k]| >= tau.  O is ascending; *nO receives |O|. */
 int orc_outlier_columns(const uint16_t *X, int64_t T, int64_t K, float tau,
-                        int32_t *O, int32_t *nO) {
+                        int32_t *O, int32_t *nO, int fmt) {
   if (T < 0 || K < 0) return ORC_ERR_ARG;
   int32_t n = 0;
   for (int64_t k = 0; k < K; k++) {
     int hit = 0;
     for (int64_t t = 0; t < T && !hit; t++) {
-      float x = fabsf((float)orc_half_to_double(X[t * K + k]));
+      float x = fabsf((float)elem_to_double(X[t * K + k], fmt));
       if (x >= tau) hit = 1;
     }
     if (hit) O[n++] = (int32_t)k;
@@ -146,7 +217,7 @@ int orc_outlier_columns(const uint16_t *X, int64_t T, int64_t K, float tau,
  * columns), and the fp16 outlier block XO[t, j] = X[t, O[j]] (T x nO). */
 int orc_quantize_activations(const uint16_t *X, int64_t T, int64_t K,
                              const int32_t *O, int32_t nO, int8_t *Xq,
-                             float *sx, uint16_t *XO) {
+                             float *sx, uint16_t *XO, int fmt) {
   if (T < 0 || K < 0 || nO < 0) return ORC_ERR_ARG;
   /* column flags from the list */
   unsigned char *flag_buf = (unsigned char *)calloc((size_t)(K > 0 ? K : 1), 1);
@@ -157,13 +228,13 @@ int orc_quantize_activations(const uint16_t *X, int64_t T, int64_t K,
     float a = 0.0f;
     for (int64_t k = 0; k < K; k++) {
       if (flag_buf[k]) continue;
-      float x = fabsf((float)orc_half_to_double(X[t * K + k]));
+      float x = fabsf((float)elem_to_double(X[t * K + k], fmt));
       if (x > a) a = x;
     }
     sx[t] = a;
     for (int64_t k = 0; k < K; k++)
       Xq[t * K + k] =
-          flag_buf[k] ? 0 : code_of((float)orc_half_to_double(X[t * K + k]), a);
+          flag_buf[k] ? 0 : code_fmt((float)elem_to_double(X[t * K + k], fmt), a, fmt);
     if (XO)
       for (int32_t j = 0; j < nO; j++) XO[t * nO + j] = X[t * K + O[j]];
   }
@@ -195,15 +266,15 @@ int orc_int8_matmul_rows(const int8_t *Xq, const int8_t *Wq, int64_t T, int64_t 
  * operands, each product exact in double). */
 void orc_outlier_matmul_rows(const uint16_t *X, const uint16_t *W16, int64_t T,
                              int64_t N, int64_t K, const int32_t *O, int32_t nO,
-                             const int64_t *rows, int64_t nrows, double *out) {
+                             const int64_t *rows, int64_t nrows, double *out, int fmt) {
   (void)T;
 #pragma omp parallel for collapse(2) schedule(static)
   for (int64_t r = 0; r < nrows; r++) {
     for (int64_t n = 0; n < N; n++) {
       double s = 0.0;
       for (int32_t j = 0; j < nO; j++)
-        s += orc_half_to_double(X[rows[r] * K + O[j]]) *
-             orc_half_to_double(W16[n * K + O[j]]);
+        s += elem_to_double(X[rows[r] * K + O[j]], fmt) *
+             elem_to_double(W16[n * K + O[j]], fmt);
       out[r * N + n] = s;
     }
   }
@@ -213,14 +284,14 @@ void orc_outlier_matmul_rows(const uint16_t *X, const uint16_t *W16, int64_t T,
  * w = Wq[n,k] * sw[n] / 127, then the same 16-bit-input product. */
 void orc_outlier_matmul_rows_wq(const uint16_t *X, const int8_t *Wq, const float *sw,
                                 int64_t N, int64_t K, const int32_t *O, int32_t nO,
-                                const int64_t *rows, int64_t nrows, double *out) {
+                                const int64_t *rows, int64_t nrows, double *out, int fmt) {
 #pragma omp parallel for collapse(2) schedule(static)
   for (int64_t r = 0; r < nrows; r++) {
     for (int64_t n = 0; n < N; n++) {
       double s = 0.0;
       for (int32_t j = 0; j < nO; j++) {
         double w = (double)Wq[n * K + O[j]] * (double)sw[n] / 127.0;
-        s += orc_half_to_double(X[rows[r] * K + O[j]]) * w;
+        s += elem_to_double(X[rows[r] * K + O[j]], fmt) * w;
       }
       out[r * N + n] = s;
     }
@@ -232,14 +303,14 @@ void orc_outlier_matmul_rows_wq(const uint16_t *X, const int8_t *Wq, const float
  * final rounding to fp16. */
 void orc_dequant_rows(const int32_t *acc, const float *sx, const float *sw,
                       const double *out, const uint16_t *bias, const int64_t *rows,
-                      int64_t nrows, int64_t N, uint16_t *Y) {
+                      int64_t nrows, int64_t N, uint16_t *Y, int fmt) {
 #pragma omp parallel for collapse(2) schedule(static)
   for (int64_t r = 0; r < nrows; r++) {
     for (int64_t n = 0; n < N; n++) {
       double p = (double)acc[r * N + n] * (double)sx[rows[r]] * (double)sw[n];
       double v = p / 16129.0 + out[r * N + n];
-      if (bias) v += orc_half_to_double(bias[n]);  /* nn.Linear's bias, before the one rounding */
-      Y[r * N + n] = orc_double_to_half(v);
+      if (bias) v += elem_to_double(bias[n], fmt);  /* nn.Linear's bias, before the one rounding */
+      Y[r * N + n] = double_to_elem(v, fmt);
     }
   }
 }
@@ -248,22 +319,23 @@ void orc_dequant_rows(const int32_t *acc, const float *sx, const float *sw,
  * activation codes are computed over ALL T rows (the outlier set depends on
  * every row); S4..S6 only for `rows`.  Intermediates are optional outputs
  * (NULL to skip) except acc and out, which the caller provides as scratch.
- * W16 NULL: the outlier weights come from the int8 codes (above). */
+ * W16 NULL: the outlier weights come from the int8 codes (above).  fmt: the
+ * 16-bit format of X, W16, the bias and Y (0 fp16, 1 bf16). */
 int orc_linear_rows(const uint16_t *X, int64_t T, int64_t K, const int8_t *Wq,
                     const float *sw, const uint16_t *W16, int64_t N, float tau,
                     const uint16_t *bias, const int64_t *rows, int64_t nrows, int8_t *Xq,
                     float *sx, int32_t *O, int32_t *nO, int32_t *acc, double *out,
-                    uint16_t *Y) {
-  int rc = orc_outlier_columns(X, T, K, tau, O, nO);
+                    uint16_t *Y, int fmt) {
+  int rc = orc_outlier_columns(X, T, K, tau, O, nO, fmt);
   if (rc) return rc;
-  rc = orc_quantize_activations(X, T, K, O, *nO, Xq, sx, NULL);
+  rc = orc_quantize_activations(X, T, K, O, *nO, Xq, sx, NULL, fmt);
   if (rc) return rc;
   rc = orc_int8_matmul_rows(Xq, Wq, T, N, K, rows, nrows, acc);
   if (W16)
-    orc_outlier_matmul_rows(X, W16, T, N, K, O, *nO, rows, nrows, out);
+    orc_outlier_matmul_rows(X, W16, T, N, K, O, *nO, rows, nrows, out, fmt);
   else  /* only the int8 weight is kept */
-    orc_outlier_matmul_rows_wq(X, Wq, sw, N, K, O, *nO, rows, nrows, out);
-  orc_dequant_rows(acc, sx, sw, out, bias, rows, nrows, N, Y);
+    orc_outlier_matmul_rows_wq(X, Wq, sw, N, K, O, *nO, rows, nrows, out, fmt);
+  orc_dequant_rows(acc, sx, sw, out, bias, rows, nrows, N, Y, fmt);
   return rc;
 }
 

@@ -10,6 +10,7 @@ the oracle with a planted mistake and checks that some pin fails.
 from __future__ import annotations
 
 import math
+from fractions import Fraction
 
 import numpy as np
 
@@ -226,6 +227,140 @@ def pin_w16_free_invariants(orc):
     a = orc.linear(X, Wq2, sw2, W2, math.inf)["Y"]
     b = orc.linear(X, Wq2, sw2, None, math.inf)["Y"]
     assert np.array_equal(a.view(np.uint16), b.view(np.uint16))
+
+
+# ---------------------------------------------------------------------------
+# bfloat16 inputs and output (the compute dtype)
+# ---------------------------------------------------------------------------
+
+def _f32_to_bf16_bits(x) -> np.ndarray:
+    """float32 values -> bfloat16 bit patterns, nearest-even (torch's own
+    conversion, independent of the oracle)."""
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16).copy()
+
+
+def _bf16_bits_to_f64(b) -> np.ndarray:
+    return (np.asarray(b, np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def pin_bf16_roundtrip(orc):
+    """bf16 -> double decodes every finite bit pattern like the binary32 with
+    the same leading bits; double -> bf16 rounds like torch for values exact
+    in fp32 (ties, subnormals, the overflow boundary included) and like the
+    exact-rational rounding of the brute force for values that are not."""
+    allbits = np.arange(65536, dtype=np.uint32)
+    with np.errstate(invalid="ignore"):
+        vals = (allbits << 16).view(np.float32).astype(np.float64)
+    finite = np.isfinite(vals)
+    for b in allbits[finite][::5]:
+        assert orc.bf16_to_double(int(b)) == vals[b]
+    rng = np.random.default_rng(31)
+    fin = vals[finite & (vals > 0)]
+    f32 = np.concatenate([
+        (rng.standard_normal(3000) * 10.0 ** rng.integers(-40, 38, 3000)).astype(np.float32),
+        # exact midpoints of neighbouring bf16 values (exact in fp32): ties
+        ((fin[:-1:97] + fin[1::97]) / 2).astype(np.float32),
+        np.array([3.3895314e38, 3.3961775e38, 3.4028235e38, 2.0 ** -133, 2.0 ** -134,
+                  3 * 2.0 ** -135, 2.0 ** -126, 0.0, -0.0, 1.0 + 2.0 ** -8,
+                  1.0 + 3 * 2.0 ** -8], np.float32),
+    ])
+    f32 = f32[np.isfinite(f32)]
+    want = _f32_to_bf16_bits(f32)
+    for v, w in zip(f32.tolist(), want.tolist()):
+        got = orc.double_to_bf16(float(v))
+        assert got == w, (v, hex(got), hex(w))
+    for v in (rng.standard_normal(400) * 10.0 ** rng.integers(-40, 38, 400)).tolist():
+        got = orc.double_to_bf16(v)
+        want = brute.fraction_to_bf16_bits(Fraction(v))
+        assert got == want, (v, hex(got), hex(want))
+
+
+def _exact_codes_bf16(x: np.ndarray, a: float) -> np.ndarray:
+    """round_half_even(127 x / a) exactly, for bf16 values x, a (|x| <= a)."""
+    def split(v):
+        m, e = np.frexp(np.asarray(v, np.float64))
+        return np.rint(m * 256).astype(np.int64), e.astype(np.int64) - 8  # 8-bit significand
+    mx, ex = split(x)
+    ma, ea = split(np.full(len(x), a))
+    sh = ea - ex                                 # >= -1 since |x| <= a
+    num = 127 * mx
+    den = ma << np.clip(sh, 0, 40)               # past 2^40 the code is 0 either way
+    num = np.where(sh < 0, num << np.clip(-sh, 0, 1), num)
+    sign = np.sign(num)
+    q, r = np.divmod(np.abs(num), den)
+    up = (2 * r > den) | ((2 * r == den) & (q % 2 == 1))
+    return (sign * (q + up)).astype(np.int64)
+
+
+def pin_bf16_code_rule_exhaustive(orc, n_scales: int = 24):
+    """The fp32 code rule on bf16 inputs: for a spread of bf16 absmax values
+    (exact-tie scales 127 * 2^s, subnormal and huge ones), every bf16 x with
+    |x| <= a is coded like round_half_even(127 x / a)."""
+    pos = np.arange(0, 0x7F80, dtype=np.uint16)       # all finite >= 0
+    posv = _bf16_bits_to_f64(pos)
+    rng = np.random.default_rng(32)
+    scales = [int(b) for b in _f32_to_bf16_bits(127 * 2.0 ** np.arange(-8, 8, 2))]
+    scales += [int(b) for b in pos[rng.integers(1, len(pos), n_scales)]]
+    scales += [0x0001, 0x007F, 0x0080, 0x3F80, 0x40C0, 0x7F7F]
+    for ab in scales:
+        a = float(_bf16_bits_to_f64([ab])[0])
+        keep = posv <= a
+        xb = np.concatenate([pos[keep], pos[keep][1:] | 0x8000])
+        xv = _bf16_bits_to_f64(xb)
+        step = 8191
+        for s0 in range(0, len(xb), step):
+            chunk = xb[s0:s0 + step]
+            W = np.empty((1, len(chunk) + 1), np.uint16)
+            W[0, 0] = ab
+            W[0, 1:] = chunk
+            Wq, sw = orc.quantize_weight(W, fmt="bf16")
+            assert float(sw[0]) == a
+            want = _exact_codes_bf16(xv[s0:s0 + step], a)
+            got = Wq[0, 1:].astype(np.int64)
+            bad = np.flatnonzero(got != want)
+            assert len(bad) == 0, (a, xv[s0 + bad[:3]], got[bad[:3]], want[bad[:3]])
+
+
+def pin_bf16_brute(orc):
+    """The whole layer on bf16 bit patterns against the exact brute force:
+    random tiny shapes and thresholds, with a bias, and with only the int8
+    weight kept."""
+    rng = np.random.default_rng(33)
+    for T, K, N in ((1, 1, 1), (3, 5, 4), (7, 16, 9), (4, 24, 6)):
+        X = _f32_to_bf16_bits(rng.standard_normal((T, K)) * 3)
+        W = _f32_to_bf16_bits(rng.standard_normal((N, K)) * 0.05)
+        bias = _f32_to_bf16_bits(rng.standard_normal(N) * 0.3)
+        if T > 2:
+            X[1] = 0
+        for tau in (6.0, 1.5, 0.0, math.inf):
+            for b, free in ((None, False), (bias, False), (bias, True)):
+                Wq, sw = orc.quantize_weight(W, fmt="bf16")
+                r = orc.linear(X, Wq, sw, None if free else W, tau, bias=b, fmt="bf16")
+                bb = brute.linear(X.tolist(), W.tolist(), tau, None if b is None else b.tolist(),
+                                  w16_free=free, fmt="bf16")
+                assert r["O"].tolist() == bb["O"]
+                assert np.array_equal(Wq, np.array(bb["Wq"], np.int8).reshape(Wq.shape))
+                assert np.array_equal(r["acc"].astype(np.int64),
+                                      np.array(bb["acc"], np.int64).reshape(r["acc"].shape))
+                yb = np.array(bb["Y"], np.uint16).reshape(r["Y"].shape)
+                assert np.array_equal(r["Y"], yb), (T, K, N, tau, free)
+
+
+def pin_bf16_tau_inf_integer(orc):
+    """tau = inf, integer bf16 inputs with +-127 in every row: the codes are
+    the inputs and Y = bf16(X W^T), the exact integer product rounded once
+    (torch's float32 -> bf16 rounding of a value exact in fp32)."""
+    for adv, K in ((False, 256), (True, 256), (True, 16)):
+        X16, W16 = inputs.int_valued(8, K, 24, seed=34, adversarial=adv)
+        X = _f32_to_bf16_bits(X16.astype(np.float32))
+        W = _f32_to_bf16_bits(W16.astype(np.float32))
+        Wq, sw = orc.quantize_weight(W, fmt="bf16")
+        r = orc.linear(X, Wq, sw, W, math.inf, fmt="bf16")
+        assert np.all(sw == 127) and np.array_equal(Wq, W16.astype(np.int8))
+        exact = X16.astype(np.int64) @ W16.astype(np.int64).T
+        assert np.array_equal(r["Y"], _f32_to_bf16_bits(exact.astype(np.float32)))
 
 
 # ---------------------------------------------------------------------------
@@ -448,6 +583,10 @@ ALL_PINS = [
     pin_bias_integer,
     pin_w16_free_brute,
     pin_w16_free_invariants,
+    pin_bf16_roundtrip,
+    pin_bf16_code_rule_exhaustive,
+    pin_bf16_brute,
+    pin_bf16_tau_inf_integer,
     pin_tau_inf_integer_inputs,
     pin_tau_zero_is_fp16_matmul,
     pin_outliers_are_column_scan,

@@ -29,16 +29,24 @@ MUTATIONS = {
     "weight_index_reversed": ("s += (int64_t)x[k] * (int64_t)w[k];",
                               "s += (int64_t)x[k] * (int64_t)w[K - 1 - k];"),
     "transposed_weight": ("const int8_t *w = Wq + n * K;", "const int8_t *w = Wq + n;"),
-    "outlier_weight_from_row": ("orc_half_to_double(W16[n * K + O[j]]);",
-                                "orc_half_to_double(W16[O[j] * K + n % K]);"),
+    "outlier_weight_from_row": ("elem_to_double(W16[n * K + O[j]], fmt);",
+                                "elem_to_double(W16[O[j] * K + n % K], fmt);"),
     "half_round_floor": ("double n = rint(ldexp(a, 10 - E));", "double n = floor(ldexp(a, 10 - E));"),
     "weight_scale_first_col": ("if (x > a) a = x;\n    }\n    sw[n] = a;",
                                "if (k == 0) a = x;\n    }\n    sw[n] = a;"),
-    "bias_dropped": ("if (bias) v += orc_half_to_double(bias[n]);", "(void)bias;"),
-    "bias_sign": ("if (bias) v += orc_half_to_double(bias[n]);",
-                  "if (bias) v -= orc_half_to_double(bias[n]);"),
-    "bias_of_next_channel": ("if (bias) v += orc_half_to_double(bias[n]);",
-                             "if (bias) v += orc_half_to_double(bias[(n + 1) % N]);"),
+    "bias_dropped": ("if (bias) v += elem_to_double(bias[n], fmt);", "(void)bias;"),
+    "bias_sign": ("if (bias) v += elem_to_double(bias[n], fmt);",
+                  "if (bias) v -= elem_to_double(bias[n], fmt);"),
+    "bias_of_next_channel": ("if (bias) v += elem_to_double(bias[n], fmt);",
+                             "if (bias) v += elem_to_double(bias[(n + 1) % N], fmt);"),
+    "bf16_round_floor": ("double n = rint(ldexp(a, 7 - E));", "double n = floor(ldexp(a, 7 - E));"),
+    "bf16_exponent_bias": ("return sign | (uint16_t)(((E + 127) << 7) | ((int)n - 128));",
+                           "return sign | (uint16_t)(((E + 126) << 7) | ((int)n - 128));"),
+    "bf16_subnormal_quantum": ("double n = rint(ldexp(a, 133));", "double n = rint(ldexp(a, 132));"),
+    "bf16_code_unscaled": ("return code_of(ldexpf(x, 1 - e), ldexpf(a, 1 - e));",
+                           "return code_of(x, a);"),
+    "bf16_read_as_fp16": ("return fmt ? orc_bf16_to_double(b) : orc_half_to_double(b);",
+                          "return orc_half_to_double(b);"),
     "w16_free_scale_128": ("double w = (double)Wq[n * K + O[j]] * (double)sw[n] / 127.0;",
                            "double w = (double)Wq[n * K + O[j]] * (double)sw[n] / 128.0;"),
     "w16_free_column_by_position": ("double w = (double)Wq[n * K + O[j]] * (double)sw[n] / 127.0;",
