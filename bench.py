@@ -267,8 +267,10 @@ def run_ours(args, world, rank, local):
         layers = max(layers, 16)
     layers = min(layers, args.max_layers)
 
-    Xh = torch.from_numpy(w.X)
-    W16_0 = torch.from_numpy(w.W).to(dev)
+    # --bf16: the same workload with X, W16, bias and Y in bf16 (nearest-even casts)
+    edt = torch.bfloat16 if args.bf16 else torch.float16
+    Xh = torch.from_numpy(w.X).to(edt)
+    W16_0 = torch.from_numpy(w.W).to(dev).to(edt)
     W16s, Wqs, sws = [], [], []
     for i in range(layers):
         # distinct copies of the same weight (same numbers, distinct memory);
@@ -280,9 +282,9 @@ def run_ours(args, world, rank, local):
         sws.append(sw)
     Xs = [Xh.to(dev) for _ in range(layers)]
     # optional fp16 bias per layer (nn.Linear's), through bnb_int8_linear_bias
-    Bs = ([torch.from_numpy(inputs.bias(N, K, seed=i)).to(dev) for i in range(layers)]
+    Bs = ([torch.from_numpy(inputs.bias(N, K, seed=i)).to(dev).to(edt) for i in range(layers)]
           if args.bias else [None] * layers)
-    Ys = [torch.empty((T, N), dtype=torch.float16, device=dev) for _ in range(layers)]
+    Ys = [torch.empty((T, N), dtype=edt, device=dev) for _ in range(layers)]
     ws = torch.empty(binding.workspace_bytes(T, N, K), dtype=torch.uint8, device=dev)
     stream = torch.cuda.Stream(device=dev)
 
@@ -391,7 +393,7 @@ def run_ours(args, world, rank, local):
                 "peak": peaks["bf16_tflops"], "unit": "TFLOP/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
     roof["traffic"] = (args.traffic if args.traffic is not None
-                       else None if args.bias or args.wq_only
+                       else None if args.bias or args.wq_only or args.bf16
                        else measured_traffic(kname, T, K, N))
     roof["kernel"] = kname
     roof["peak_source"] = ("measured (MEASURED_PEAKS.json)" if peak_src == "measured"
@@ -417,7 +419,7 @@ def run_ours(args, world, rank, local):
     import torch
     streams2 = [stream, torch.cuda.Stream(device=dev)]
     Xpin = [Xh.pin_memory(), Xh.pin_memory()]
-    Ypin = [torch.empty((T, N), dtype=torch.float16).pin_memory() for _ in range(2)]
+    Ypin = [torch.empty((T, N), dtype=edt).pin_memory() for _ in range(2)]
     Xdev = [Xs[0], torch.empty_like(Xs[0])]
     Ydev = [Ys[0], torch.empty_like(Ys[0])]
     wss = [ws, torch.empty_like(ws)]
@@ -458,10 +460,12 @@ def run_ours(args, world, rank, local):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "int8xint8->int32 + fp16 outliers, fp16 out",
+        "dtype": ("int8xint8->int32 + bf16 outliers, bf16 out" if args.bf16
+                  else "int8xint8->int32 + fp16 outliers, fp16 out"),
         "data": "synthetic (seeded, inputs module)",
         "config": {
-            "workload": f"{args.workload}: X fp16 [{T},{K}], W fp16 [{N},{K}], tau {tau}",
+            "workload": (f"{args.workload}: X {'bf16' if args.bf16 else 'fp16'} [{T},{K}], "
+                         f"W {'bf16' if args.bf16 else 'fp16'} [{N},{K}], tau {tau}"),
             "T": T, "K": K, "N": N, "tau": tau, "n_outliers": nO, "bias": bool(args.bias),
             "fp16_weight_resident": not args.wq_only,
             "layers_per_step": layers,
@@ -719,6 +723,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--bias", action="store_true",
                     help="layers with an fp16 bias (bnb_int8_linear_bias)")
+    ap.add_argument("--bf16", action="store_true",
+                    help="X, W16, bias and Y in bf16 (bnb_int8_linear_ex)")
     ap.add_argument("--wq-only", action="store_true",
                     help="only the int8 weight resident (bnb_int8_linear_wq_only)")
     ap.add_argument("--traffic", type=float, default=None,

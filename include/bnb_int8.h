@@ -63,6 +63,12 @@ typedef enum {
                               through bnb_last_device_status */
 } bnb_status_t;
 
+/* The 16-bit element format of X, W16, the bias and Y (the codes, scales
+ * and accumulators do not depend on it).  bf16 is the compute dtype the pages
+ * prefer where the hardware supports it (Hugging Face page, section 5
+ * "Storage Precision vs. Compute Precision"). */
+typedef enum { BNB_DTYPE_FP16 = 0, BNB_DTYPE_BF16 = 1 } bnb_dtype_t;
+
 /* Size limits of one call. */
 #define BNB_MAX_K (1 << 20)
 #define BNB_MAX_T (1 << 22)
@@ -137,6 +143,38 @@ bnb_status_t bnb_int8_linear_wq_only(const void *X, int64_t T, int64_t K, const 
                                      const float *Wscale, const void *bias, int64_t N,
                                      float tau, void *Y, void *workspace,
                                      size_t workspace_bytes, void *stream);
+
+/*
+ * The general entry points, with the element format `dtype` (a bnb_dtype_t)
+ * of W (quantize) or of X, W16, bias and Y (the layer).  With BNB_DTYPE_BF16
+ * every fp16 array above is bf16 instead; the definitions are unchanged
+ * except that Y is rounded to bf16 (nearest-even) and the codes of bf16
+ * values are taken after scaling x and its absmax a by one power of two
+ * 2^(1-e), a = f 2^e with f in [0.5, 1) -- the same code 127 x / a, computed
+ * without leaving fp32's range (bf16 spans 2^-133 .. 2^128, where 127 x
+ * would overflow).  W16 may be NULL (bnb_int8_linear_wq_only) and bias may
+ * be NULL.  An unknown dtype is BNB_ERR_INVALID_ARG; other errors as for
+ * the fp16 entry points.
+ */
+bnb_status_t bnb_int8_quantize_weight_ex(const void *W, int64_t N, int64_t K, int dtype,
+                                         int8_t *Wq, float *Wscale, void *stream);
+bnb_status_t bnb_int8_linear_ex(const void *X, int64_t T, int64_t K, const int8_t *Wq,
+                                const float *Wscale, const void *W16, const void *bias, int64_t N,
+                                float tau, int dtype, void *Y, void *workspace,
+                                size_t workspace_bytes, void *stream);
+bnb_status_t bnb_int8_linear_from_host_ex(const void *X_host, int64_t T, int64_t K,
+                                          const int8_t *Wq, const float *Wscale, const void *W16,
+                                          const void *bias, int64_t N, float tau, int dtype,
+                                          void *Y_host, void *X_dev, void *Y_dev,
+                                          void *workspace, size_t workspace_bytes,
+                                          void *stream);
+/* bnb_int8_linear_debug's intermediates (same meaning) for bnb_int8_linear_ex. */
+bnb_status_t bnb_int8_linear_debug_ex(const void *X, int64_t T, int64_t K, const int8_t *Wq,
+                                      const float *Wscale, const void *W16, const void *bias,
+                                      int64_t N, float tau, int dtype, void *Y, void *workspace,
+                                      size_t workspace_bytes, void *stream, int8_t *Xq,
+                                      float *Xscale, int32_t *outlier_idx, int32_t *n_outliers,
+                                      int32_t *acc);
 
 /*
  * bnb_int8_linear that also exports its intermediates (for parity tests).

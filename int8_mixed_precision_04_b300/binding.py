@@ -44,7 +44,8 @@ class Lib:
                "bnb_profile_kernel_name", "bnb_int8_linear_noalloc",
                "bnb_int8_linear_from_host", "bnb_int8_quantize_blockwise",
                "bnb_int8_dequantize_blockwise", "bnb_int8_linear_bias",
-               "bnb_int8_linear_wq_only")
+               "bnb_int8_linear_wq_only", "bnb_int8_quantize_weight_ex", "bnb_int8_linear_ex",
+               "bnb_int8_linear_from_host_ex", "bnb_int8_linear_debug_ex")
 
     def __init__(self, path: str = LIB_PATH):
         if not os.path.exists(path):
@@ -65,6 +66,17 @@ class Lib:
         L.bnb_int8_linear_wq_only.restype = ctypes.c_int
         L.bnb_int8_linear_wq_only.argtypes = [_P, _I64, _I64, _P, _P, _P, _I64, ctypes.c_float,
                                               _P, _P, ctypes.c_size_t, _P]
+        L.bnb_int8_quantize_weight_ex.restype = ctypes.c_int
+        L.bnb_int8_quantize_weight_ex.argtypes = [_P, _I64, _I64, ctypes.c_int, _P, _P, _P]
+        L.bnb_int8_linear_ex.restype = ctypes.c_int
+        L.bnb_int8_linear_ex.argtypes = [_P, _I64, _I64, _P, _P, _P, _P, _I64, ctypes.c_float,
+                                         ctypes.c_int, _P, _P, ctypes.c_size_t, _P]
+        L.bnb_int8_linear_from_host_ex.restype = ctypes.c_int
+        L.bnb_int8_linear_from_host_ex.argtypes = [_P, _I64, _I64, _P, _P, _P, _P, _I64,
+                                                   ctypes.c_float, ctypes.c_int, _P, _P, _P, _P,
+                                                   ctypes.c_size_t, _P]
+        L.bnb_int8_linear_debug_ex.restype = ctypes.c_int
+        L.bnb_int8_linear_debug_ex.argtypes = L.bnb_int8_linear_ex.argtypes + [_P, _P, _P, _P, _P]
         L.bnb_int8_linear_debug.restype = ctypes.c_int
         L.bnb_int8_linear_debug.argtypes = L.bnb_int8_linear.argtypes + [_P, _P, _P, _P, _P]
         L.bnb_int8_linear_noalloc.restype = ctypes.c_int
@@ -125,19 +137,36 @@ def _check(rc, where):
         raise BnbError(rc, where)
 
 
+def _dtype_code(t) -> int:
+    """bnb_dtype_t of a tensor: 0 fp16, 1 bf16 (anything else raises)."""
+    import torch
+    if t.dtype == torch.float16:
+        return 0
+    if t.dtype == torch.bfloat16:
+        return 1
+    raise TypeError(f"fp16 or bf16 tensors only, got {t.dtype}")
+
+
 def workspace_bytes(T: int, N: int, K: int) -> int:
     return load().bnb_int8_linear_workspace_bytes(T, N, K)
 
 
 def quantize_weight(W16, Wq=None, Wscale=None, stream=None):
-    """bnb_int8_quantize_weight: W16 [N,K] fp16 (cuda) -> (Wq int8 [N,K], sw fp32 [N])."""
+    """bnb_int8_quantize_weight(_ex): W16 [N,K] fp16 or bf16 (cuda) -> (Wq int8
+    [N,K], sw fp32 [N])."""
     import torch
     N, K = W16.shape
     if Wq is None:
         Wq = torch.empty((N, K), dtype=torch.int8, device=W16.device)
     if Wscale is None:
         Wscale = torch.empty((N,), dtype=torch.float32, device=W16.device)
-    rc = load().bnb_int8_quantize_weight(_ptr(W16), N, K, _ptr(Wq), _ptr(Wscale), _stream(stream))
+    dt = _dtype_code(W16)
+    if dt == 0:
+        rc = load().bnb_int8_quantize_weight(_ptr(W16), N, K, _ptr(Wq), _ptr(Wscale),
+                                             _stream(stream))
+    else:
+        rc = load().bnb_int8_quantize_weight_ex(_ptr(W16), N, K, dt, _ptr(Wq), _ptr(Wscale),
+                                                _stream(stream))
     _check(rc, "bnb_int8_quantize_weight")
     return Wq, Wscale
 
@@ -147,9 +176,29 @@ def _alloc_ws(T, N, K, device):
     return torch.empty((workspace_bytes(T, N, K),), dtype=torch.uint8, device=device)
 
 
-def linear(X, Wq, Wscale, W16, tau: float, Y=None, workspace=None, stream=None):
-    """bnb_int8_linear: X [T,K] fp16 -> Y [T,N] fp16 (all cuda tensors)."""
+def linear_ex(X, Wq, Wscale, W16, bias, tau: float, Y=None, workspace=None, stream=None):
+    """bnb_int8_linear_ex: X [T,K] fp16 or bf16 -> Y [T,N] in X's dtype; W16
+    (X's dtype) and bias (X's dtype, [N]) may be None."""
     import torch
+    T, K = X.shape
+    N = Wq.shape[0]
+    if Y is None:
+        Y = torch.empty((T, N), dtype=X.dtype, device=X.device)
+    if workspace is None:
+        workspace = _alloc_ws(T, N, K, X.device)
+    rc = load().bnb_int8_linear_ex(_ptr(X), T, K, _ptr(Wq), _ptr(Wscale), _ptr(W16), _ptr(bias),
+                                   N, float(tau), _dtype_code(X), _ptr(Y), _ptr(workspace),
+                                   workspace.numel(), _stream(stream))
+    _check(rc, "bnb_int8_linear_ex")
+    return Y
+
+
+def linear(X, Wq, Wscale, W16, tau: float, Y=None, workspace=None, stream=None):
+    """bnb_int8_linear: X [T,K] fp16 -> Y [T,N] fp16 (all cuda tensors); bf16
+    X goes through bnb_int8_linear_ex."""
+    import torch
+    if _dtype_code(X) != 0:
+        return linear_ex(X, Wq, Wscale, W16, None, tau, Y, workspace, stream)
     T, K = X.shape
     N = Wq.shape[0]
     if Y is None:
@@ -167,6 +216,8 @@ def linear_bias(X, Wq, Wscale, W16, bias, tau: float, Y=None, workspace=None, st
     """bnb_int8_linear_bias: as :func:`linear`, plus an fp16 bias [N] (cuda)
     added before the rounding of Y; ``bias=None`` passes NULL."""
     import torch
+    if _dtype_code(X) != 0:
+        return linear_ex(X, Wq, Wscale, W16, bias, tau, Y, workspace, stream)
     T, K = X.shape
     N = Wq.shape[0]
     if Y is None:
@@ -185,6 +236,8 @@ def linear_wq_only(X, Wq, Wscale, bias, tau: float, Y=None, workspace=None, stre
     (outlier weights dequantized from the codes); ``bias`` an fp16 [N] cuda
     tensor or None."""
     import torch
+    if _dtype_code(X) != 0:
+        return linear_ex(X, Wq, Wscale, None, bias, tau, Y, workspace, stream)
     T, K = X.shape
     N = Wq.shape[0]
     if Y is None:
@@ -206,9 +259,11 @@ def linear_from_host(X_host, Wq, Wscale, W16, tau: float, Y_host, X_dev, Y_dev, 
     [N] cuda tensor; ``W16=None`` runs the int8-weight-only layer."""
     T, K = X_host.shape
     N = Wq.shape[0]
-    rc = load().bnb_int8_linear_from_host(_ptr(X_host), T, K, _ptr(Wq), _ptr(Wscale), _ptr(W16),
-                                          _ptr(bias), N, float(tau), _ptr(Y_host), _ptr(X_dev), _ptr(Y_dev),
-                                          _ptr(workspace), workspace.numel(), _stream(stream))
+    rc = load().bnb_int8_linear_from_host_ex(_ptr(X_host), T, K, _ptr(Wq), _ptr(Wscale),
+                                             _ptr(W16), _ptr(bias), N, float(tau),
+                                             _dtype_code(X_host), _ptr(Y_host), _ptr(X_dev),
+                                             _ptr(Y_dev), _ptr(workspace), workspace.numel(),
+                                             _stream(stream))
     _check(rc, "bnb_int8_linear_from_host")
     return Y_host
 
@@ -257,23 +312,26 @@ def linear_noalloc(X, Wq, Wscale, W16, tau: float, Y=None, stream=None):
     return Y
 
 
-def linear_debug(X, Wq, Wscale, W16, tau: float, stream=None, want_acc: bool = True):
-    """bnb_int8_linear_debug; returns dict(Y, Xq, sx, O, acc) as cuda tensors."""
+def linear_debug(X, Wq, Wscale, W16, tau: float, stream=None, want_acc: bool = True,
+                 bias=None):
+    """bnb_int8_linear_debug_ex (X fp16 or bf16, W16 and bias may be None);
+    returns dict(Y, Xq, sx, O, acc) as cuda tensors."""
     import torch
     T, K = X.shape
     N = Wq.shape[0]
     dev = X.device
-    Y = torch.empty((T, N), dtype=torch.float16, device=dev)
+    Y = torch.empty((T, N), dtype=X.dtype, device=dev)
     Xq = torch.empty((T, K), dtype=torch.int8, device=dev)
     sx = torch.empty((T,), dtype=torch.float32, device=dev)
     O = torch.empty((K,), dtype=torch.int32, device=dev)
     nO = torch.empty((1,), dtype=torch.int32, device=dev)
     acc = torch.empty((T, N), dtype=torch.int32, device=dev) if want_acc else None
     ws = _alloc_ws(T, N, K, dev)
-    rc = load().bnb_int8_linear_debug(_ptr(X), T, K, _ptr(Wq), _ptr(Wscale), _ptr(W16), N,
-                                      float(tau), _ptr(Y), _ptr(ws), ws.numel(), _stream(stream),
-                                      _ptr(Xq), _ptr(sx), _ptr(O), _ptr(nO), _ptr(acc))
-    _check(rc, "bnb_int8_linear_debug")
+    rc = load().bnb_int8_linear_debug_ex(_ptr(X), T, K, _ptr(Wq), _ptr(Wscale), _ptr(W16),
+                                         _ptr(bias), N, float(tau), _dtype_code(X), _ptr(Y),
+                                         _ptr(ws), ws.numel(), _stream(stream), _ptr(Xq),
+                                         _ptr(sx), _ptr(O), _ptr(nO), _ptr(acc))
+    _check(rc, "bnb_int8_linear_debug_ex")
     return {"Y": Y, "Xq": Xq, "sx": sx, "O": O, "nO": nO, "acc": acc, "workspace": ws}
 
 

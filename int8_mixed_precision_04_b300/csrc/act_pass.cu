@@ -17,6 +17,9 @@
 //   W16's outlier columns once per call (w16o[n, j] = W16[n, O[j]]; with only
 //   the int8 weight kept, Wq[n, O[j]] as an fp16 integer), so that the GEMM's
 //   token tiles read them by TMA.
+// X and W16 may be bf16 instead of fp16 (kBf): the bit-pattern tests are the
+// same, the outlier block and gathered columns stay in X's format, and the
+// codes are taken on x and sx scaled by one power of two (RowCode).
 //
 // All three are HBM-bound: 16-byte coalesced loads, every load of a thread
 // issued before any is used (the row pass keeps its row in registers and
@@ -26,17 +29,18 @@
 
 namespace bnb {
 
-// The int8 codes of one 16-byte vector (8 fp16 values, flags f: outlier
-// columns get 0) against row absmax a (r = 127 / a), as two words of four
+// The int8 codes of one 16-byte vector (8 fp16 or bf16 values, flags f:
+// outlier columns get 0) under the row's code rule rc, as two words of four
 // code bytes.  code_byte is exact and uses no conversion-pipe instruction;
 // the GEMM's fp16 integer codes come from the bytes by s8x4_to_f16x4.
-__device__ __forceinline__ void codes8(const uint32_t (&w)[4], uint32_t f, float a, float r,
+template <bool kBf>
+__device__ __forceinline__ void codes8(const uint32_t (&w)[4], uint32_t f, const RowCode<kBf> &rc,
                                        uint32_t &p0, uint32_t &p1) {
   uint32_t b[8];
 #pragma unroll
   for (int j = 0; j < 4; j++) {
-    b[2 * j] = ((f >> (2 * j)) & 1) ? 0u : code_byte(h2f_bits(w[j] & 0xffffu), a, r) & 0xffu;
-    b[2 * j + 1] = ((f >> (2 * j + 1)) & 1) ? 0u : code_byte(h2f_bits(w[j] >> 16), a, r) & 0xffu;
+    b[2 * j] = ((f >> (2 * j)) & 1) ? 0u : rc.byte(e2f<kBf>(w[j] & 0xffffu)) & 0xffu;
+    b[2 * j + 1] = ((f >> (2 * j + 1)) & 1) ? 0u : rc.byte(e2f<kBf>(w[j] >> 16)) & 0xffu;
   }
   p0 = b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24);
   p1 = b[4] | (b[5] << 8) | (b[6] << 16) | (b[7] << 24);
@@ -140,7 +144,7 @@ constexpr int kQuantRegVecs = 4;  // row vectors a thread keeps in registers (K 
 // kMode 0: int8 codes into `codes` (T x K int8); kMode 1: fp16 integer codes
 // (T x K fp16).  kReg: the row fits the block's registers (read once);
 // otherwise it is read twice (maximum, then codes), the second time from L2.
-template <int kMode, bool kReg>
+template <int kMode, bool kReg, bool kBf>
 __device__ __forceinline__ void quantize_row(const uint4 *__restrict__ row, int64_t t, int64_t vecs,
                                              const uint32_t *__restrict__ colmask, bool dense,
                                              float *__restrict__ sx, float *__restrict__ sxd,
@@ -188,8 +192,8 @@ __device__ __forceinline__ void quantize_row(const uint4 *__restrict__ row, int6
 #pragma unroll
   for (int w = 0; w < kQuantThreads / 32; w++) m = max(m, red[w]);
   __syncthreads();  // red is reused by the next row
-  const float a = h2f_bits(m);
-  const float r = code_recip(a);
+  const float a = e2f<kBf>(m);
+  const RowCode<kBf> rc(a);
   if (threadIdx.x == 0) {
     sx[t] = a;
     sxd[t] = __fdiv_rn(a, 127.0f);
@@ -198,7 +202,7 @@ __device__ __forceinline__ void quantize_row(const uint4 *__restrict__ row, int6
   auto emit = [&](int64_t v, const uint4 &u, uint32_t f) {
     const uint32_t w[4] = {u.x, u.y, u.z, u.w};
     uint32_t p0, p1;
-    codes8(w, f, a, r, p0, p1);
+    codes8<kBf>(w, f, rc, p0, p1);
     if (kMode == 0) {
       reinterpret_cast<uint2 *>(codes)[t * vecs + v] = make_uint2(p0, p1);
     } else {
@@ -247,7 +251,7 @@ struct QuantArgs {
   int64_t opad;
 };
 
-template <int kMode>
+template <int kMode, bool kBf>
 __global__ void __launch_bounds__(kQuantThreads) quantize_rows_kernel(const QuantArgs p) {
   __shared__ uint32_t red[kQuantThreads / 32];
   const int64_t vecs = p.K / 8;
@@ -257,10 +261,10 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_rows_kernel(const Quan
   for (int64_t t = blockIdx.x; t < p.T; t += gridDim.x) {
     const uint4 *row = p.X + t * vecs;
     if (reg)
-      quantize_row<kMode, true>(row, t, vecs, p.colmask, dense, p.sx, p.sxd, p.codes, p.xo,
+      quantize_row<kMode, true, kBf>(row, t, vecs, p.colmask, dense, p.sx, p.sxd, p.codes, p.xo,
                                 p.kpad, p.dbg_xq, red);
     else
-      quantize_row<kMode, false>(row, t, vecs, p.colmask, dense, p.sx, p.sxd, p.codes, p.xo,
+      quantize_row<kMode, false, kBf>(row, t, vecs, p.colmask, dense, p.sx, p.sxd, p.codes, p.xo,
                                  p.kpad, p.dbg_xq, red);
     if (p.xo && !dense) {  // compacted outlier block XO[t, j] = X[t, O[j]], zero to a multiple of 64
       const unsigned short *xr = reinterpret_cast<const unsigned short *>(row);
@@ -291,7 +295,7 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_rows_kernel(const Quan
           const int32_t j = j0 + lane + 32 * u;
           w[u] = j >= nO ? (unsigned short)0
                  : wr    ? __ldg(wr + __ldg(p.O + j))
-                         : __half_as_ushort(__short2half_rn((short)__ldg(qr + __ldg(p.O + j))));
+                         : f2e<kBf>((float)__ldg(qr + __ldg(p.O + j)));  // exact
         }
 #pragma unroll
         for (int u = 0; u < 4; u++) {
@@ -305,8 +309,8 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_rows_kernel(const Quan
 
 cudaError_t launch_act_pass(const void *X, int64_t T, int64_t K, uint32_t thr_bits,
                             const Workspace &ws, int code_mode, bool with_xo, const void *W16,
-                            const int8_t *Wq, int64_t N, int8_t *dbg_xq, int num_sms,
-                            cudaStream_t stream) {
+                            const int8_t *Wq, int64_t N, bool bf16, int8_t *dbg_xq,
+                            int num_sms, cudaStream_t stream) {
   // The caller has zeroed the status word, the counters and the column mask.
   cudaError_t e;
   // S2: 2-D grid, column slabs of 256 x row slabs, about 2 blocks per SM,
@@ -353,10 +357,9 @@ cudaError_t launch_act_pass(const void *X, int64_t T, int64_t K, uint32_t thr_bi
     if (gb > qblocks) qblocks = gb;
   }
   ProfScope ps(kKidQuantRows, stream);
-  if (code_mode == 0)
-    quantize_rows_kernel<0><<<(unsigned)qblocks, kQuantThreads, 0, stream>>>(a);
-  else
-    quantize_rows_kernel<1><<<(unsigned)qblocks, kQuantThreads, 0, stream>>>(a);
+  auto *kern = code_mode == 0 ? (bf16 ? quantize_rows_kernel<0, true> : quantize_rows_kernel<0, false>)
+                              : (bf16 ? quantize_rows_kernel<1, true> : quantize_rows_kernel<1, false>);
+  kern<<<(unsigned)qblocks, kQuantThreads, 0, stream>>>(a);
   note_launch();
   return cudaGetLastError();
 }

@@ -76,14 +76,23 @@ static double half_bits_value(uint32_t h) {
   return std::ldexp((double)(1024 + m), e - 25);
 }
 
-// Smallest non-negative fp16 bit pattern whose value is >= tau (0x7c00, the
-// infinity pattern, when no finite fp16 value reaches tau).  For finite fp16
-// x:  |x| >= tau  <=>  (bits(x) & 0x7fff) >= threshold_bits(tau).
-static uint32_t threshold_bits(float tau) {
-  uint32_t lo = 0, hi = 0x7c00;  // answer in [lo, hi]
+// Exact bf16 value of a bit pattern (host side): the binary32 with the same
+// leading 16 bits.
+static double bf16_bits_value(uint32_t h) {
+  uint32_t u = (h & 0xffffu) << 16;
+  float f;
+  std::memcpy(&f, &u, 4);
+  return (double)f;
+}
+
+// Smallest non-negative fp16 (bf16) bit pattern whose value is >= tau
+// (0x7c00 / 0x7f80, the infinity pattern, when no finite value reaches tau).
+// For finite x:  |x| >= tau  <=>  (bits(x) & 0x7fff) >= threshold_bits(tau).
+static uint32_t threshold_bits(float tau, bool bf16) {
+  uint32_t lo = 0, hi = bf16 ? 0x7f80 : 0x7c00;  // answer in [lo, hi]
   while (lo < hi) {
     const uint32_t mid = (lo + hi) / 2;
-    if (half_bits_value(mid) >= (double)tau)
+    if ((bf16 ? bf16_bits_value(mid) : half_bits_value(mid)) >= (double)tau)
       hi = mid;
     else
       lo = mid + 1;
@@ -169,7 +178,7 @@ static bnb_status_t linear_check(const void *X, int64_t T, int64_t K, const int8
 
 static bnb_status_t linear_impl(const void *X, int64_t T, int64_t K, const int8_t *Wq,
                                 const float *Wscale, const void *W16, const void *bias,
-                                int64_t N, float tau, void *Y, void *workspace,
+                                int64_t N, float tau, bool bf16, void *Y, void *workspace,
                                 size_t workspace_bytes,
                                 void *stream_v, int8_t *dbg_xq, float *dbg_sx,
                                 int32_t *dbg_O, int32_t *dbg_nO, int32_t *dbg_acc) {
@@ -187,11 +196,12 @@ static bnb_status_t linear_impl(const void *X, int64_t T, int64_t K, const int8_
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_v);
   const Workspace ws = carve(workspace, T, N, K);
   const int path = choose_path(T, N, K, dev);
-  const uint32_t thr = threshold_bits(tau);
+  const uint32_t thr = threshold_bits(tau, bf16);
   cudaError_t e;
   if (path == 1) {
     // decode: no memset, the act-pass kernel clears the status word
-    e = launch_decode(X, T, K, thr, Wq, Wscale, W16, bias, N, Y, ws, dbg_xq, dbg_acc, stream);
+    e = launch_decode(X, T, K, thr, Wq, Wscale, W16, bias, N, bf16, Y, ws, dbg_xq, dbg_acc,
+                      stream);
     if (e != cudaSuccess) return BNB_ERR_CUDA;
   } else {
     if (!profile_only_main()) {
@@ -207,13 +217,14 @@ static bnb_status_t linear_impl(const void *X, int64_t T, int64_t K, const int8_
       // the tcgen05 GEMM reads fp16 integer codes, the mma GEMM int8 codes
       // (for the tcgen05 GEMM the same launch compacts W16 at a sparse outlier set)
       e = launch_act_pass(X, T, K, thr, ws, /*code_mode=*/path == 2 ? 1 : 0, /*with_xo=*/true,
-                          W16, Wq, N, dbg_xq, device_sms(dev), stream);
+                          W16, Wq, N, bf16, dbg_xq, device_sms(dev), stream);
       if (e != cudaSuccess) return BNB_ERR_CUDA;
     }
     if (path == 2)
-      e = launch_gemm_tc(T, K, Wq, Wscale, W16, bias, N, Y, ws, dbg_acc, device_sms(dev), stream);
+      e = launch_gemm_tc(T, K, Wq, Wscale, W16, bias, N, bf16, Y, ws, dbg_acc, device_sms(dev),
+                         stream);
     else
-      e = launch_gemm_mma(T, K, Wq, Wscale, W16, bias, N, Y, ws, dbg_acc, stream);
+      e = launch_gemm_mma(T, K, Wq, Wscale, W16, bias, N, bf16, Y, ws, dbg_acc, stream);
     if (e != cudaSuccess) return BNB_ERR_CUDA;
   }
   if (dbg_sx && cudaMemcpyAsync(dbg_sx, ws.sx, (size_t)T * 4, cudaMemcpyDeviceToDevice, stream) != cudaSuccess)
@@ -236,8 +247,8 @@ size_t bnb_int8_linear_workspace_bytes(int64_t T, int64_t N, int64_t K) {
   return layout_of(T, N, K).total + kWsSlack;
 }
 
-bnb_status_t bnb_int8_quantize_weight(const void *W16, int64_t N, int64_t K, int8_t *Wq,
-                                      float *Wscale, void *stream) {
+static bnb_status_t quantize_weight_impl(const void *W16, int64_t N, int64_t K, bool bf16,
+                                         int8_t *Wq, float *Wscale, void *stream) {
   if (!W16 || !Wq || !Wscale) return BNB_ERR_INVALID_ARG;
   if (N <= 0 || K <= 0) return BNB_ERR_INVALID_ARG;
   if (N > BNB_MAX_N || K > BNB_MAX_K) return BNB_ERR_UNSUPPORTED;
@@ -247,8 +258,20 @@ bnb_status_t bnb_int8_quantize_weight(const void *W16, int64_t N, int64_t K, int
   int dev = 0;
   bnb_status_t st = check_device(&dev);
   if (st != BNB_OK) return st;
-  cudaError_t e = launch_quantize_weight(W16, N, K, Wq, Wscale, reinterpret_cast<cudaStream_t>(stream));
+  cudaError_t e =
+      launch_quantize_weight(W16, N, K, bf16, Wq, Wscale, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? BNB_OK : BNB_ERR_CUDA;
+}
+
+bnb_status_t bnb_int8_quantize_weight(const void *W16, int64_t N, int64_t K, int8_t *Wq,
+                                      float *Wscale, void *stream) {
+  return quantize_weight_impl(W16, N, K, false, Wq, Wscale, stream);
+}
+
+bnb_status_t bnb_int8_quantize_weight_ex(const void *W, int64_t N, int64_t K, int dtype,
+                                         int8_t *Wq, float *Wscale, void *stream) {
+  if (dtype != BNB_DTYPE_FP16 && dtype != BNB_DTYPE_BF16) return BNB_ERR_INVALID_ARG;
+  return quantize_weight_impl(W, N, K, dtype == BNB_DTYPE_BF16, Wq, Wscale, stream);
 }
 
 static bool blockwise_size_ok(int64_t block) {
@@ -293,7 +316,7 @@ bnb_status_t bnb_int8_linear(const void *X, int64_t T, int64_t K, const int8_t *
                              const float *Wscale, const void *W16, int64_t N, float tau,
                              void *Y, void *workspace, size_t workspace_bytes, void *stream) {
   if (!W16) return BNB_ERR_INVALID_ARG;
-  return linear_impl(X, T, K, Wq, Wscale, W16, nullptr, N, tau, Y, workspace, workspace_bytes,
+  return linear_impl(X, T, K, Wq, Wscale, W16, nullptr, N, tau, false, Y, workspace, workspace_bytes,
                      stream, nullptr, nullptr, nullptr, nullptr, nullptr);
 }
 
@@ -302,24 +325,33 @@ bnb_status_t bnb_int8_linear_bias(const void *X, int64_t T, int64_t K, const int
                                   int64_t N, float tau, void *Y, void *workspace,
                                   size_t workspace_bytes, void *stream) {
   if (!W16) return BNB_ERR_INVALID_ARG;
-  return linear_impl(X, T, K, Wq, Wscale, W16, bias, N, tau, Y, workspace, workspace_bytes,
+  return linear_impl(X, T, K, Wq, Wscale, W16, bias, N, tau, false, Y, workspace, workspace_bytes,
                      stream, nullptr, nullptr, nullptr, nullptr, nullptr);
+}
+
+bnb_status_t bnb_int8_linear_ex(const void *X, int64_t T, int64_t K, const int8_t *Wq,
+                                const float *Wscale, const void *W16, const void *bias, int64_t N,
+                                float tau, int dtype, void *Y, void *workspace,
+                                size_t workspace_bytes, void *stream) {
+  if (dtype != BNB_DTYPE_FP16 && dtype != BNB_DTYPE_BF16) return BNB_ERR_INVALID_ARG;
+  return linear_impl(X, T, K, Wq, Wscale, W16, bias, N, tau, dtype == BNB_DTYPE_BF16, Y,
+                     workspace, workspace_bytes, stream, nullptr, nullptr, nullptr, nullptr,
+                     nullptr);
 }
 
 bnb_status_t bnb_int8_linear_wq_only(const void *X, int64_t T, int64_t K, const int8_t *Wq,
                                      const float *Wscale, const void *bias, int64_t N,
                                      float tau, void *Y, void *workspace,
                                      size_t workspace_bytes, void *stream) {
-  return linear_impl(X, T, K, Wq, Wscale, nullptr, bias, N, tau, Y, workspace, workspace_bytes,
+  return linear_impl(X, T, K, Wq, Wscale, nullptr, bias, N, tau, false, Y, workspace, workspace_bytes,
                      stream, nullptr, nullptr, nullptr, nullptr, nullptr);
 }
 
-bnb_status_t bnb_int8_linear_from_host(const void *X_host, int64_t T, int64_t K,
-                                       const int8_t *Wq, const float *Wscale, const void *W16,
-                                       const void *bias, int64_t N, float tau, void *Y_host,
-                                       void *X_dev,
-                                       void *Y_dev, void *workspace, size_t workspace_bytes,
-                                       void *stream) {
+static bnb_status_t from_host_impl(const void *X_host, int64_t T, int64_t K, const int8_t *Wq,
+                                   const float *Wscale, const void *W16, const void *bias,
+                                   int64_t N, float tau, bool bf16, void *Y_host, void *X_dev,
+                                   void *Y_dev, void *workspace, size_t workspace_bytes,
+                                   void *stream) {
   if (!X_host || !Y_host || !X_dev || !Y_dev) return BNB_ERR_INVALID_ARG;
   if (T <= 0 || K <= 0 || N <= 0) return BNB_ERR_INVALID_ARG;
   const size_t xbytes = (size_t)T * (size_t)K * 2, ybytes = (size_t)T * (size_t)N * 2;
@@ -333,12 +365,32 @@ bnb_status_t bnb_int8_linear_from_host(const void *X_host, int64_t T, int64_t K,
   if (bias && overlaps(Y_dev, ybytes, bias, (size_t)N * 2)) return BNB_ERR_INVALID_ARG;
   if (cudaMemcpyAsync(X_dev, X_host, xbytes, cudaMemcpyHostToDevice, st) != cudaSuccess)
     return BNB_ERR_CUDA;
-  r = linear_impl(X_dev, T, K, Wq, Wscale, W16, bias, N, tau, Y_dev, workspace,
+  r = linear_impl(X_dev, T, K, Wq, Wscale, W16, bias, N, tau, bf16, Y_dev, workspace,
                   workspace_bytes, stream, nullptr, nullptr, nullptr, nullptr, nullptr);
   if (r != BNB_OK) return r;
   if (cudaMemcpyAsync(Y_host, Y_dev, ybytes, cudaMemcpyDeviceToHost, st) != cudaSuccess)
     return BNB_ERR_CUDA;
   return BNB_OK;
+}
+
+bnb_status_t bnb_int8_linear_from_host(const void *X_host, int64_t T, int64_t K,
+                                       const int8_t *Wq, const float *Wscale, const void *W16,
+                                       const void *bias, int64_t N, float tau, void *Y_host,
+                                       void *X_dev, void *Y_dev, void *workspace,
+                                       size_t workspace_bytes, void *stream) {
+  return from_host_impl(X_host, T, K, Wq, Wscale, W16, bias, N, tau, false, Y_host, X_dev, Y_dev,
+                        workspace, workspace_bytes, stream);
+}
+
+bnb_status_t bnb_int8_linear_from_host_ex(const void *X_host, int64_t T, int64_t K,
+                                          const int8_t *Wq, const float *Wscale, const void *W16,
+                                          const void *bias, int64_t N, float tau, int dtype,
+                                          void *Y_host, void *X_dev, void *Y_dev,
+                                          void *workspace, size_t workspace_bytes,
+                                          void *stream) {
+  if (dtype != BNB_DTYPE_FP16 && dtype != BNB_DTYPE_BF16) return BNB_ERR_INVALID_ARG;
+  return from_host_impl(X_host, T, K, Wq, Wscale, W16, bias, N, tau, dtype == BNB_DTYPE_BF16,
+                        Y_host, X_dev, Y_dev, workspace, workspace_bytes, stream);
 }
 
 bnb_status_t bnb_int8_linear_debug(const void *X, int64_t T, int64_t K, const int8_t *Wq,
@@ -347,8 +399,19 @@ bnb_status_t bnb_int8_linear_debug(const void *X, int64_t T, int64_t K, const in
                                    void *stream, int8_t *Xq, float *Xscale,
                                    int32_t *outlier_idx, int32_t *n_outliers, int32_t *acc) {
   if (!W16) return BNB_ERR_INVALID_ARG;
-  return linear_impl(X, T, K, Wq, Wscale, W16, nullptr, N, tau, Y, workspace, workspace_bytes,
+  return linear_impl(X, T, K, Wq, Wscale, W16, nullptr, N, tau, false, Y, workspace, workspace_bytes,
                      stream, Xq, Xscale, outlier_idx, n_outliers, acc);
+}
+
+bnb_status_t bnb_int8_linear_debug_ex(const void *X, int64_t T, int64_t K, const int8_t *Wq,
+                                      const float *Wscale, const void *W16, const void *bias,
+                                      int64_t N, float tau, int dtype, void *Y, void *workspace,
+                                      size_t workspace_bytes, void *stream, int8_t *Xq,
+                                      float *Xscale, int32_t *outlier_idx, int32_t *n_outliers,
+                                      int32_t *acc) {
+  if (dtype != BNB_DTYPE_FP16 && dtype != BNB_DTYPE_BF16) return BNB_ERR_INVALID_ARG;
+  return linear_impl(X, T, K, Wq, Wscale, W16, bias, N, tau, dtype == BNB_DTYPE_BF16, Y,
+                     workspace, workspace_bytes, stream, Xq, Xscale, outlier_idx, n_outliers, acc);
 }
 
 bnb_status_t bnb_last_device_status(const void *workspace, void *stream, int32_t *out) {

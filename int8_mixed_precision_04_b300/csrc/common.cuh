@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -110,6 +111,64 @@ __device__ __forceinline__ uint32_t code_byte(float x, float a, float r) {
 __device__ __forceinline__ int code_of(float x, float a, float r) {
   return a > 0.0f ? code_exact(x, a, r) : 0;
 }
+
+// ---- the 16-bit element format of X, W16, the bias and Y ----
+// kBf false: fp16; true: bf16 (1 sign, 8 exponent, 7 fraction bits).  For
+// both, |a| < |b| <=> (bits_a & 0x7fff) < (bits_b & 0x7fff) on finite values,
+// so thresholds and absmax work on bit patterns alike.
+template <bool kBf>
+__device__ __forceinline__ float e2f(uint32_t b) {  // low 16 bits -> float, exact
+  if constexpr (kBf)
+    return __uint_as_float(b << 16);
+  else
+    return h2f_bits(b);
+}
+template <bool kBf>
+__device__ __forceinline__ uint16_t f2e(float v) {  // nearest-even
+  if constexpr (kBf)
+    return __bfloat16_as_ushort(__float2bfloat16_rn(v));
+  else
+    return __half_as_ushort(__float2half_rn(v));
+}
+template <bool kBf>
+__device__ __forceinline__ uint32_t f2e2(float lo, float hi) {  // a packed pair, nearest-even
+  if constexpr (kBf) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t *>(&v);
+  } else {
+    const __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t *>(&v);
+  }
+}
+
+// The code rule of one row (absmax a).  bf16 spans 2^-133 .. 2^128, where
+// 127 x and 127 / a leave fp32's range, so for bf16 x and a are first scaled
+// by one power of two 2^(1-e) (a = f 2^e, f in [0.5, 1)), applied as two
+// normal factors so that every product is exact: the scaled a lies in
+// [1, 2), and the code 127 x / a is unchanged.  A value whose scaled form
+// underflows codes to 0 either way.
+template <bool kBf>
+struct RowCode {
+  float a, r, s1, s2;
+  RowCode() = default;
+  __device__ __forceinline__ explicit RowCode(float absmax) {
+    s1 = s2 = 1.0f;
+    if (kBf && absmax > 0.0f) {
+      const uint32_t b = __float_as_uint(absmax);
+      const int E = (int)((b >> 23) & 0xffu);
+      const int e = E ? E - 126 : 32 - (int)__clz(b & 0x7fffffu) - 149;
+      const int k = 1 - e, k1 = k / 2, k2 = k - k1;  // each in [-64, 75]
+      s1 = __uint_as_float((uint32_t)(k1 + 127) << 23);
+      s2 = __uint_as_float((uint32_t)(k2 + 127) << 23);
+    }
+    a = kBf ? (absmax * s1) * s2 : absmax;
+    r = code_recip(a);
+  }
+  // the code byte of x (|x| <= absmax), exact
+  __device__ __forceinline__ uint32_t byte(float x) const {
+    return code_byte(kBf ? (x * s1) * s2 : x, a, r);
+  }
+};
 
 // Four signed int8 codes (one 32-bit word) -> four fp16 integers (two half2
 // words).  fp16 with exponent field 25 has unit spacing on [1024, 2048), so

@@ -120,7 +120,7 @@ struct DecArgs {
   const float *sw;
   const unsigned short *W16;
   const unsigned short *bias;  // [N] fp16 or null
-  __half *Y;
+  uint16_t *Y;                 // [T x N] fp16 or bf16 bits
   float *sx_out;               // [T]  (CTA 0)
   int32_t *O_out;              // [K]  (CTA 0)
   uint32_t *nO_out;            // [1]  (CTA 0)
@@ -181,7 +181,8 @@ __device__ __forceinline__ void dec_mma_range(const uint8_t *xs, const uint8_t *
   }
 }
 
-template <int kC, bool kWq>  // kWq: only the int8 weight is kept (W16 null)
+// kWq: only the int8 weight is kept (W16 null); kBf: X, W16, bias and Y are bf16
+template <int kC, bool kWq, bool kBf>
 __global__ void __launch_bounds__(kDecThreads, 1)
     dec_fused_kernel(const __grid_constant__ CUtensorMap tm_w16, const DecArgs p) {
   using G = DecAct<kC>;
@@ -386,21 +387,21 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         nO += n;
         if (c < (int)crank) base += n;
       }
-      float a_r[G::kRpt], rc_r[G::kRpt];
+      // each row's code rule from sx (0 for rows >= T): one division per row
+      RowCode<kBf> rcs[G::kRpt];
 #pragma unroll
       for (int j = 0; j < G::kRpt; j++) {
         const int t = grp + kC * j;
         uint32_t m = 0;
 #pragma unroll
         for (int c = 0; c < kC; c++) m = max(m, sm.pubs[c][t]);
-        a_r[j] = h2f_bits(t < T ? m : 0u);  // sx; 0 for rows >= T
-        rc_r[j] = code_recip(a_r[j]);       // one division per row
+        rcs[j] = RowCode<kBf>(e2f<kBf>(t < T ? m : 0u));
       }
       if (threadIdx.x < 16) {
         uint32_t m = 0;
 #pragma unroll
         for (int c = 0; c < kC; c++) m = max(m, sm.pubs[c][threadIdx.x]);
-        sxs[threadIdx.x] = h2f_bits((int)threadIdx.x < T ? m : 0u);
+        sxs[threadIdx.x] = e2f<kBf>((int)threadIdx.x < T ? m : 0u);
       }
       // bytes every CTA receives: the codes of all T rows and every mask word
       // (cbar); the first outlier columns and their X values (xbar)
@@ -457,15 +458,15 @@ __global__ void __launch_bounds__(kDecThreads, 1)
 #pragma unroll
       for (int r = 0; r < G::kRpt; r++) {
         const int t = grp + kC * r;
-        const float a = a_r[r], rc = rc_r[r];
+        const RowCode<kBf> &rc = rcs[r];
         const uint32_t w[4] = {x[r].x, x[r].y, x[r].z, x[r].w};
         uint32_t p0 = 0, p1 = 0;
 #pragma unroll
         for (int i = 0; i < 4; i++) {
           const uint32_t c0 =
-              ((flags >> (2 * i)) & 1) ? 0u : code_byte(h2f_bits(w[i] & 0xffffu), a, rc);
+              ((flags >> (2 * i)) & 1) ? 0u : rc.byte(e2f<kBf>(w[i] & 0xffffu));
           const uint32_t c1 =
-              ((flags >> (2 * i + 1)) & 1) ? 0u : code_byte(h2f_bits(w[i] >> 16), a, rc);
+              ((flags >> (2 * i + 1)) & 1) ? 0u : rc.byte(e2f<kBf>(w[i] >> 16));
           const uint32_t two = (c0 & 0xffu) | ((c1 & 0xffu) << 8);
           if (i < 2)
             p0 |= two << (16 * i);
@@ -544,7 +545,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     for (int it = 0; it < 2; it++)
       if (it < nitems && e_n[it] < rows)
         for (int j = 0; j < nsm; j++)
-          e_small[it] = fmaf(h2f_bits(sm.xo[e_t[it] * kDecOutSmall + j]),
+          e_small[it] = fmaf(e2f<kBf>(sm.xo[e_t[it] * kDecOutSmall + j]),
                              (float)(int8_t)ws[e_n[it] * pitch + sm.oc[j]], e_small[it]);
   }
   // outlier columns beyond the first kDecOutSmall: split over the consumer
@@ -554,17 +555,17 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   float o[kDecGroups][4] = {};
   for (int32_t j = kDecOutSmall + warp; big && j < nO; j += kDecWarps) {
     const int64_t k = ocols[j];
-    const float x0 = g < T ? h2f_bits(__ldg(p.X16 + (int64_t)g * K + k)) : 0.f;
-    const float x1 = g + 8 < T ? h2f_bits(__ldg(p.X16 + (int64_t)(g + 8) * K + k)) : 0.f;
+    const float x0 = g < T ? e2f<kBf>(__ldg(p.X16 + (int64_t)g * K + k)) : 0.f;
+    const float x1 = g + 8 < T ? e2f<kBf>(__ldg(p.X16 + (int64_t)(g + 8) * K + k)) : 0.f;
 #pragma unroll
     for (int gi = 0; gi < kDecGroups; gi++) {
       if (gi < ng) {
         const int64_t ra = min((int64_t)gi * 8 + 2 * q, rows - 1);
         const int64_t rb = min((int64_t)gi * 8 + 2 * q + 1, rows - 1);
         const float wa = wfree ? (float)(int8_t)ws[ra * pitch + k]
-                               : h2f_bits(__ldg(p.W16 + (n0 + ra) * K + k));
+                               : e2f<kBf>(__ldg(p.W16 + (n0 + ra) * K + k));
         const float wb = wfree ? (float)(int8_t)ws[rb * pitch + k]
-                               : h2f_bits(__ldg(p.W16 + (n0 + rb) * K + k));
+                               : e2f<kBf>(__ldg(p.W16 + (n0 + rb) * K + k));
         o[gi][0] = fmaf(x0, wa, o[gi][0]);
         o[gi][1] = fmaf(x0, wb, o[gi][1]);
         o[gi][2] = fmaf(x1, wa, o[gi][2]);
@@ -614,18 +615,18 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   for (int it = 0; it < 2; it++)
     if (!wfree && it < nitems && e_n[it] < rows)
       for (int j = 0; j < nsmall; j++)
-        e_out[it] = fmaf(h2f_bits(sm.xo[e_t[it] * kDecOutSmall + j]),
-                         h2f_bits(sm.wos[j][e_n[it]][sm.oc[j] & 7u]), e_out[it]);
+        e_out[it] = fmaf(e2f<kBf>(sm.xo[e_t[it] * kDecOutSmall + j]),
+                         e2f<kBf>(sm.wos[j][e_n[it]][sm.oc[j] & 7u]), e_out[it]);
 #pragma unroll
   for (int it = 0; it < 2; it++) {
     const int t = e_t[it], nl = e_n[it];
     if (it < nitems && t < T && nl < rows && ok_o) {
       const int64_t n = n0 + nl;
       const float st = sxs[t] / 127.0f, sn = e_sw[it] / 127.0f;
-      const float b = h2f_bits(sm.bias[nl]);  // 0 without a bias
+      const float b = e2f<kBf>(sm.bias[nl]);  // 0 without a bias
       const float y = wfree ? fmaf(fmaf((float)e_acc[it], st, e_out[it]), sn, b)
                             : fmaf((float)e_acc[it] * st, sn, e_out[it] + b);
-      p.Y[t * p.N + n] = __float2half_rn(y);
+      p.Y[t * p.N + n] = f2e<kBf>(y);
       if (p.dbg_acc) p.dbg_acc[t * p.N + n] = e_acc[it];
     }
   }
@@ -643,7 +644,8 @@ constexpr int kDecClusterSizes[3] = {8, 16, 4};  // order of preference (measure
 // fails); also opens the kernel's shared-memory limit to `dyn_max`.
 template <int kC>
 int dec_resident_ctas(int dyn_max) {
-  for (auto *f : {dec_fused_kernel<kC, false>, dec_fused_kernel<kC, true>}) {
+  for (auto *f : {dec_fused_kernel<kC, false, false>, dec_fused_kernel<kC, true, false>,
+                  dec_fused_kernel<kC, false, true>, dec_fused_kernel<kC, true, true>}) {
     if (cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn_max) !=
         cudaSuccess)
       return 0;
@@ -662,10 +664,14 @@ int dec_resident_ctas(int dyn_max) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  int n = 0, n1 = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, dec_fused_kernel<kC, false>, &cfg) != cudaSuccess) n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n1, dec_fused_kernel<kC, true>, &cfg) != cudaSuccess) n1 = 0;
-  return (n < n1 ? n : n1) * kC;  // both forms must fit
+  int least = 1 << 30;
+  for (auto *f : {dec_fused_kernel<kC, false, false>, dec_fused_kernel<kC, true, false>,
+                  dec_fused_kernel<kC, false, true>, dec_fused_kernel<kC, true, true>}) {
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, f, &cfg) != cudaSuccess) n = 0;
+    least = n < least ? n : least;  // every form must fit
+  }
+  return least * kC;
 }
 
 struct DecCfg {
@@ -687,7 +693,7 @@ DecCfg decode_cfg(int dev) {
   DecCfg r{{0, 0, 0}, 0};
   if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev < 0 ? 0 : dev) ==
           cudaSuccess &&
-      cudaFuncGetAttributes(&fa, dec_fused_kernel<8, false>) == cudaSuccess) {
+      cudaFuncGetAttributes(&fa, dec_fused_kernel<8, false, false>) == cudaSuccess) {
     r.dyn_max = optin - (int)fa.sharedSizeBytes;
     r.ctas[0] = dec_resident_ctas<8>(r.dyn_max);
     r.ctas[1] = dec_resident_ctas<16>(r.dyn_max);
@@ -741,8 +747,8 @@ int64_t decode_max_n(int dev, int64_t K) {
 
 cudaError_t launch_decode(const void *X, int64_t T, int64_t K, uint32_t thr, const int8_t *Wq,
                           const float *sw, const void *W16, const void *bias, int64_t N,
-                          void *Y, const Workspace &ws, int8_t *dbg_xq, int32_t *dbg_acc,
-                          cudaStream_t stream) {
+                          bool bf16, void *Y, const Workspace &ws, int8_t *dbg_xq,
+                          int32_t *dbg_acc, cudaStream_t stream) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) dev = -1;
   const DecCfg dc = decode_cfg(dev);
@@ -767,7 +773,8 @@ cudaError_t launch_decode(const void *X, int64_t T, int64_t K, uint32_t thr, con
   // so no L2 promotion beyond the sector)
   // (without W16 the map is never read: it then describes Wq)
   CUtensorMap tm;
-  const bool enc = W16 ? encode_2d(&tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, W16, (uint64_t)K,
+  const bool enc = W16 ? encode_2d(&tm, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                              : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, W16, (uint64_t)K,
                                    (uint64_t)N, (uint64_t)K * 2, 8, (uint32_t)a.rows_per_cta,
                                    CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE)
                        : encode_2d(&tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, Wq, (uint64_t)K,
@@ -778,7 +785,7 @@ cudaError_t launch_decode(const void *X, int64_t T, int64_t K, uint32_t thr, con
   a.sw = sw;
   a.W16 = reinterpret_cast<const unsigned short *>(W16);
   a.bias = reinterpret_cast<const unsigned short *>(bias);
-  a.Y = reinterpret_cast<__half *>(Y);
+  a.Y = reinterpret_cast<uint16_t *>(Y);
   a.sx_out = ws.sx;
   a.O_out = ws.O;
   a.nO_out = ws.counters + 1;
@@ -800,11 +807,16 @@ cudaError_t launch_decode(const void *X, int64_t T, int64_t K, uint32_t thr, con
   cfg.attrs = attr;
   cfg.numAttrs = profile_only_main() ? 1 : 2;  // profiling mode 2: no overlap with the previous call
   ProfScope ps(kKidDecFused, stream);
-  const bool wq = W16 == nullptr;
-  const cudaError_t e =
-      kc == 8    ? cudaLaunchKernelEx(&cfg, wq ? dec_fused_kernel<8, true> : dec_fused_kernel<8, false>, tm, a)
-      : kc == 16 ? cudaLaunchKernelEx(&cfg, wq ? dec_fused_kernel<16, true> : dec_fused_kernel<16, false>, tm, a)
-                 : cudaLaunchKernelEx(&cfg, wq ? dec_fused_kernel<4, true> : dec_fused_kernel<4, false>, tm, a);
+  const int form = (W16 == nullptr ? 1 : 0) | (bf16 ? 2 : 0);
+  using Kern = void (*)(CUtensorMap, DecArgs);
+  static const Kern kerns[3][4] = {
+      {dec_fused_kernel<8, false, false>, dec_fused_kernel<8, true, false>,
+       dec_fused_kernel<8, false, true>, dec_fused_kernel<8, true, true>},
+      {dec_fused_kernel<16, false, false>, dec_fused_kernel<16, true, false>,
+       dec_fused_kernel<16, false, true>, dec_fused_kernel<16, true, true>},
+      {dec_fused_kernel<4, false, false>, dec_fused_kernel<4, true, false>,
+       dec_fused_kernel<4, false, true>, dec_fused_kernel<4, true, true>}};
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kerns[pick][form], tm, a);
   note_launch();
   return e;
 }

@@ -22,9 +22,10 @@ namespace bnb {
 constexpr int kMmaBM = 128, kMmaBN = 128, kMmaBK = 64;  // BK in bytes
 constexpr int kMmaThreads = 256;
 
+template <bool kBf>  // X, W16, the bias and Y bf16 instead of fp16
 __global__ void __launch_bounds__(kMmaThreads) gemm_mma_kernel(
     int64_t T, int64_t K, const int8_t *__restrict__ Wq, const float *__restrict__ sw,
-    const unsigned short *__restrict__ W16, int64_t N, __half *__restrict__ Y,
+    const unsigned short *__restrict__ W16, int64_t N, uint16_t *__restrict__ Y,
     const int8_t *__restrict__ xcodes, const float *__restrict__ sx,
     const int32_t *__restrict__ O, const uint32_t *__restrict__ counters,
     const __half *__restrict__ xo, int64_t kpad, const unsigned short *__restrict__ bias,
@@ -106,7 +107,7 @@ __global__ void __launch_bounds__(kMmaThreads) gemm_mma_kernel(
           v = (float)acc[mt][nt][i] * __fdiv_rn(sx[t], 127.0f);
           if (W16) {
             v *= __fdiv_rn(sw[n], 127.0f);
-            if (bias) v += h2f_bits(__ldg(bias + n));
+            if (bias) v += e2f<kBf>(__ldg(bias + n));
           }
         }
         y[mt][nt][i] = v;
@@ -135,7 +136,7 @@ __global__ void __launch_bounds__(kMmaThreads) gemm_mma_kernel(
         unsigned short v = 0;
         if (j < nO && n0 + r < N)
           v = W16 ? __ldg(W16 + (n0 + r) * K + k)
-                  : __half_as_ushort(__short2half_rn((short)__ldg(Wq + (n0 + r) * K + k)));
+                  : f2e<kBf>((float)__ldg(Wq + (n0 + r) * K + k));  // exact
         Bh[r * 32 + lane] = v;
       }
     }
@@ -156,7 +157,12 @@ __global__ void __launch_bounds__(kMmaThreads) gemm_mma_kernel(
 #pragma unroll
     for (int mt = 0; mt < 4; mt++)
 #pragma unroll
-      for (int nt = 0; nt < 4; nt++) mma_f16_block(y[mt][nt], fa[mt], fb[mt], fw[nt]);
+      for (int nt = 0; nt < 4; nt++) {
+        if (kBf)
+          mma_bf16_block(y[mt][nt], fa[mt], fb[mt], fw[nt]);
+        else
+          mma_f16_block(y[mt][nt], fa[mt], fb[mt], fw[nt]);
+      }
     __syncthreads();
   }
 
@@ -176,13 +182,13 @@ __global__ void __launch_bounds__(kMmaThreads) gemm_mma_kernel(
             if (n + u < N) {
               float &yy = y[mt][nt][2 * h + u];
               yy *= __fdiv_rn(sw[n + u], 127.0f);
-              if (bias) yy += h2f_bits(__ldg(bias + n + u));
+              if (bias) yy += e2f<kBf>(__ldg(bias + n + u));
             }
         }
-        const __half lo = __float2half_rn(y[mt][nt][2 * h]);
-        const __half hi = __float2half_rn(y[mt][nt][2 * h + 1]);
+        const uint16_t lo = f2e<kBf>(y[mt][nt][2 * h]);
+        const uint16_t hi = f2e<kBf>(y[mt][nt][2 * h + 1]);
         if (n + 1 < N && ((t * N + n) & 1) == 0) {
-          *reinterpret_cast<__half2 *>(Y + t * N + n) = __halves2half2(lo, hi);
+          *reinterpret_cast<uint32_t *>(Y + t * N + n) = (uint32_t)lo | ((uint32_t)hi << 16);
         } else {
           if (n < N) Y[t * N + n] = lo;
           if (n + 1 < N) Y[t * N + n + 1] = hi;
@@ -191,14 +197,13 @@ __global__ void __launch_bounds__(kMmaThreads) gemm_mma_kernel(
 }
 
 cudaError_t launch_gemm_mma(int64_t T, int64_t K, const int8_t *Wq, const float *sw,
-                            const void *W16, const void *bias, int64_t N, void *Y,
-                           const Workspace &ws,
-                            int32_t *dbg_acc, cudaStream_t stream) {
+                            const void *W16, const void *bias, int64_t N, bool bf16, void *Y,
+                            const Workspace &ws, int32_t *dbg_acc, cudaStream_t stream) {
   dim3 grid((unsigned)((N + kMmaBN - 1) / kMmaBN), (unsigned)((T + kMmaBM - 1) / kMmaBM));
   ProfScope ps(kKidGemmMma, stream);
-  gemm_mma_kernel<<<grid, kMmaThreads, 0, stream>>>(
+  (bf16 ? gemm_mma_kernel<true> : gemm_mma_kernel<false>)<<<grid, kMmaThreads, 0, stream>>>(
       T, K, Wq, sw, reinterpret_cast<const unsigned short *>(W16), N,
-      reinterpret_cast<__half *>(Y), reinterpret_cast<const int8_t *>(ws.xcodes), ws.sx, ws.O,
+      reinterpret_cast<uint16_t *>(Y), reinterpret_cast<const int8_t *>(ws.xcodes), ws.sx, ws.O,
       ws.counters, ws.xo, ws.kpad, reinterpret_cast<const unsigned short *>(bias), dbg_acc);
   note_launch();
   return cudaGetLastError();

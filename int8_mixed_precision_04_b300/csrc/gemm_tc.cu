@@ -95,6 +95,9 @@ constexpr size_t kSmemBytes = (size_t)kStages * kStageBytes + 1024;
 // Instruction descriptor of kind::f16: D fp32, A and B fp16, both K-major,
 // N = kBN, M = kBM.
 constexpr uint32_t kIdesc = (1u << 4) | ((uint32_t)(kBN >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
+// The same with A and B bf16 (format fields 1), for the outlier stages of a
+// bf16 layer; the int8 stages always multiply fp16 integer codes.
+constexpr uint32_t kIdescBf16 = kIdesc | (1u << 7) | (1u << 10);
 
 // Shared-memory matrix descriptor of a K-major tile with the 128-byte
 // swizzle: rows of 128 bytes, 8-row groups 1024 bytes apart.
@@ -114,7 +117,7 @@ struct TcArgs {
   const float *sw;
   const unsigned short *W16;  // null: only the int8 weight (outlier weights Wq sw / 127)
   const unsigned short *bias;  // [N] fp16 or null
-  __half *Y;
+  uint16_t *Y;  // [T x N] fp16 or bf16 bits
   const float *sxd;  // [T] sx / 127
   const int32_t *O;
   const uint32_t *nO;
@@ -167,6 +170,12 @@ __device__ __forceinline__ void ld_scales8(const float *sxd, int64_t t, int64_t 
   }
 }
 
+// Two fp16 integers -> the same two values as bf16 (exact for |v| <= 256).
+__device__ __forceinline__ void to_bf16x2(uint32_t &w) {
+  const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&w));
+  w = f2e2<true>(f.x, f.y);
+}
+
 // 16 int8 codes -> 16 fp16 integers (two 16-byte granules).
 __device__ __forceinline__ void widen16(const uint4 &v, uint4 &g0, uint4 &g1) {
   s8x4_to_f16x4(v.x, g0.x, g0.y);
@@ -180,9 +189,12 @@ __device__ __forceinline__ void widen16(const uint4 &v, uint4 &g0, uint4 &g1) {
 // stages when only the int8 weight is kept.  In the other outlier stages TMA
 // has put the fp16 A tile there already (W16, or the compacted outlier
 // columns); the converters only pass the stage on to the MMA.
-// Thread ct owns weight rows ct, ct + 32 * kConvWarps, ...
+// Thread ct owns weight rows ct, ct + 32 * kConvWarps, ...  In a bf16
+// layer the outlier stages' codes are widened to bf16 integers instead
+// (exact), so that both MMA operands have X's format.
+template <bool kBf>
 __device__ __forceinline__ void converter_role(uint8_t *smem, TcSmem &sm, const TcArgs &p,
-                                               int s_conv, int nst, int ntiles) {
+                                               int s_int, int s_conv, int nst, int ntiles) {
   const int ct = threadIdx.x - kConvWarp0 * 32;  // 0 .. 32 * kConvWarps - 1
   const int lane = threadIdx.x & 31;
   uint32_t it = 0;
@@ -206,6 +218,10 @@ __device__ __forceinline__ void converter_role(uint8_t *smem, TcSmem &sm, const 
             const uint4 v = *reinterpret_cast<const uint4 *>(wq + 16 * (q ^ ((r >> 1) & 3)));
             uint4 g0, g1;
             widen16(v, g0, g1);
+            if (kBf && s >= s_int) {
+              to_bf16x2(g0.x); to_bf16x2(g0.y); to_bf16x2(g0.z); to_bf16x2(g0.w);
+              to_bf16x2(g1.x); to_bf16x2(g1.y); to_bf16x2(g1.z); to_bf16x2(g1.w);
+            }
             *reinterpret_cast<uint4 *>(wh + 16 * ((2 * q) ^ (r & 7))) = g0;
             *reinterpret_cast<uint4 *>(wh + 16 * ((2 * q + 1) ^ (r & 7))) = g1;
           }
@@ -218,6 +234,7 @@ __device__ __forceinline__ void converter_role(uint8_t *smem, TcSmem &sm, const 
   }
 }
 
+template <bool kBf>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
                    const __grid_constant__ CUtensorMap tm_xo, const __grid_constant__ CUtensorMap tm_w16,
@@ -339,7 +356,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t bd = sw128_desc(smem_addr(stage_x(smem, st)));
 #pragma unroll
             for (int k = 0; k < kBK / 16; ++k)  // 16 fp16 = 32 bytes per MMA
-              umma_f16(d, ad + 2 * k, bd + 2 * k, kIdesc, (s > s0 || k > 0) ? 1u : 0u);
+              umma_f16(d, ad + 2 * k, bd + 2 * k, kBf && s >= s_int ? kIdescBf16 : kIdesc,
+                       (s > s0 || k > 0) ? 1u : 0u);
             umma_commit(&sm.empty[st]);
           }
           if (ok) umma_commit(&sm.accf[buf]);
@@ -356,10 +374,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       tmem_dealloc(tmem, kTmemCols);
     }
-    if (kConvWarps == 2 && warp >= kConvWarp0) converter_role(smem, sm, p, s_conv, nst, ntiles);
+    if (kConvWarps == 2 && warp >= kConvWarp0)
+      converter_role<kBf>(smem, sm, p, s_int, s_conv, nst, ntiles);
   } else if (kConvWarps == 4 && warp < kEpiWarp0) {
     regs_dec<kRegsConv>();
-    converter_role(smem, sm, p, s_conv, nst, ntiles);
+    converter_role<kBf>(smem, sm, p, s_int, s_conv, nst, ntiles);
   } else {
     regs_inc<kRegsEpi>();
     // ---------------- epilogue ----------------
@@ -410,7 +429,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
       }
       const float swn = n < N ? __fdiv_rn(__ldg(p.sw + n), 127.0f) : 0.0f;
-      const float bn = n < N && p.bias ? h2f_bits(__ldg(p.bias + n)) : 0.0f;
+      const float bn = n < N && p.bias ? e2f<kBf>(__ldg(p.bias + n)) : 0.0f;
       const uint32_t obase = tmem + lane_field + obuf * kBN + part * kEpiCols;
 #pragma unroll
       for (int j = 0; j < kEpiCols / 8; ++j) {
@@ -443,14 +462,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           if ((N & 1) == 0) {
             if (lane & 1) {
               if (ta + 1 < T && n < N)
-                *reinterpret_cast<__half2 *>(p.Y + (ta + 1) * N + n - 1) = __floats2half2_rn(recv, yb);
+                *reinterpret_cast<uint32_t *>(p.Y + (ta + 1) * N + n - 1) = f2e2<kBf>(recv, yb);
             } else {
               if (ta < T && n < N)
-                *reinterpret_cast<__half2 *>(p.Y + ta * N + n) = __floats2half2_rn(ya, recv);
+                *reinterpret_cast<uint32_t *>(p.Y + ta * N + n) = f2e2<kBf>(ya, recv);
             }
           } else if (n < N) {
-            if (ta < T) p.Y[ta * N + n] = __float2half_rn(ya);
-            if (ta + 1 < T) p.Y[(ta + 1) * N + n] = __float2half_rn(yb);
+            if (ta < T) p.Y[ta * N + n] = f2e<kBf>(ya);
+            if (ta + 1 < T) p.Y[(ta + 1) * N + n] = f2e<kBf>(yb);
           }
         }
       }
@@ -474,32 +493,37 @@ __global__ void __launch_bounds__(kThreads, 1)
 }  // namespace
 
 cudaError_t launch_gemm_tc(int64_t T, int64_t K, const int8_t *Wq, const float *sw,
-                           const void *W16, const void *bias, int64_t N, void *Y,
+                           const void *W16, const void *bias, int64_t N, bool bf16, void *Y,
                            const Workspace &ws,
                            int32_t *dbg_acc, int num_sms, cudaStream_t stream) {
   static bool attr_set = false;  // benign race: every writer sets the same value
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kSmemBytes);
-    if (e != cudaSuccess) return e;
+    for (auto *f : {gemm_tc_kernel<false>, gemm_tc_kernel<true>}) {
+      cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (int)kSmemBytes);
+      if (e != cudaSuccess) return e;
+    }
     attr_set = true;
   }
+  // X's 16-bit format for the outlier block and W16 (the copies do not convert)
+  const CUtensorMapDataType e16 =
+      bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   CUtensorMap tm_x, tm_w, tm_xo, tm_w16, tm_w16o;
   if (!encode_2d(&tm_x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, ws.xcodes, (uint64_t)K, (uint64_t)T,
                  (uint64_t)K * 2, kBK, kBN, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B) ||
       !encode_2d(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, Wq, (uint64_t)K, (uint64_t)N, (uint64_t)K,
                  kBK, kBM, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B) ||
       // the outlier block's inner extent is K (columns past K read as zeros)
-      !encode_2d(&tm_xo, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, ws.xo, (uint64_t)K, (uint64_t)T,
+      !encode_2d(&tm_xo, e16, ws.xo, (uint64_t)K, (uint64_t)T,
                  (uint64_t)ws.kpad * 2, kBK, kBN, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B) ||
       // without W16 this map is never read; it then describes the compacted columns
-      !(W16 ? encode_2d(&tm_w16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, W16, (uint64_t)K, (uint64_t)N,
+      !(W16 ? encode_2d(&tm_w16, e16, W16, (uint64_t)K, (uint64_t)N,
                         (uint64_t)K * 2, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B)
-            : encode_2d(&tm_w16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, ws.w16o, (uint64_t)ws.opad,
+            : encode_2d(&tm_w16, e16, ws.w16o, (uint64_t)ws.opad,
                         (uint64_t)N, (uint64_t)ws.opad * 2, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B)) ||
-      !encode_2d(&tm_w16o, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, ws.w16o, (uint64_t)ws.opad,
+      !encode_2d(&tm_w16o, e16, ws.w16o, (uint64_t)ws.opad,
                  (uint64_t)N, (uint64_t)ws.opad * 2, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B))
     return cudaErrorInvalidValue;
   TcArgs a;
@@ -512,7 +536,7 @@ cudaError_t launch_gemm_tc(int64_t T, int64_t K, const int8_t *Wq, const float *
   a.sw = sw;
   a.W16 = reinterpret_cast<const unsigned short *>(W16);
   a.bias = reinterpret_cast<const unsigned short *>(bias);
-  a.Y = reinterpret_cast<__half *>(Y);
+  a.Y = reinterpret_cast<uint16_t *>(Y);
   a.sxd = ws.sxd;
   a.O = ws.O;
   a.nO = ws.counters + 1;
@@ -531,7 +555,8 @@ cudaError_t launch_gemm_tc(int64_t T, int64_t K, const int8_t *Wq, const float *
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   ProfScope ps(kKidGemmTc, stream);
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_tc_kernel, tm_x, tm_w, tm_xo, tm_w16, tm_w16o, a);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, bf16 ? gemm_tc_kernel<true> : gemm_tc_kernel<false>,
+                                           tm_x, tm_w, tm_xo, tm_w16, tm_w16o, a);
   note_launch();
   return e;
 }

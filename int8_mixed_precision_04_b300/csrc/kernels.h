@@ -52,15 +52,15 @@ class ProfScope {
   cudaEvent_t a_;
 };
 
-cudaError_t launch_quantize_weight(const void *W16, int64_t N, int64_t K, int8_t *Wq,
+cudaError_t launch_quantize_weight(const void *W16, int64_t N, int64_t K, bool bf16, int8_t *Wq,
                                    float *sw, cudaStream_t stream);
 
 // S2 + S3.  code_mode 0: int8 codes, 1: fp16 integer codes.  with_xo: write
 // the padded fp16 outlier block.
 cudaError_t launch_act_pass(const void *X, int64_t T, int64_t K, uint32_t thr_bits,
                             const Workspace &ws, int code_mode, bool with_xo, const void *W16,
-                            const int8_t *Wq, int64_t N, int8_t *dbg_xq, int num_sms,
-                            cudaStream_t stream);
+                            const int8_t *Wq, int64_t N, bool bf16, int8_t *dbg_xq,
+                            int num_sms, cudaStream_t stream);
 
 // The blockwise 8-bit codec (blocks of B values, B a power of two in
 // [64, 2048]): fp32 -> int8 codes + per-block absmax, and back.
@@ -75,20 +75,19 @@ cudaError_t launch_dequantize_blockwise(const int8_t *codes, const float *absmax
 int64_t decode_max_n(int dev, int64_t K);
 cudaError_t launch_decode(const void *X, int64_t T, int64_t K, uint32_t thr, const int8_t *Wq,
                           const float *sw, const void *W16, const void *bias, int64_t N,
-                          void *Y, const Workspace &ws, int8_t *dbg_xq, int32_t *dbg_acc,
-                          cudaStream_t stream);
+                          bool bf16, void *Y, const Workspace &ws, int8_t *dbg_xq,
+                          int32_t *dbg_acc, cudaStream_t stream);
 
 // S4..S6 on tcgen05 tensor cores (fp16 integer codes from the activation
 // pass, code_mode 1), persistent over 128 x 256 output tiles.
 cudaError_t launch_gemm_tc(int64_t T, int64_t K, const int8_t *Wq, const float *sw,
-                           const void *W16, const void *bias, int64_t N, void *Y,
+                           const void *W16, const void *bias, int64_t N, bool bf16, void *Y,
                            const Workspace &ws,
                            int32_t *dbg_acc, int num_sms, cudaStream_t stream);
 
 // S4..S6 with warp-level mma.sync (legacy tensor path), int8 codes.
 cudaError_t launch_gemm_mma(int64_t T, int64_t K, const int8_t *Wq, const float *sw,
-                            const void *W16, const void *bias, int64_t N, void *Y,
-                           const Workspace &ws,
-                            int32_t *dbg_acc, cudaStream_t stream);
+                            const void *W16, const void *bias, int64_t N, bool bf16, void *Y,
+                            const Workspace &ws, int32_t *dbg_acc, cudaStream_t stream);
 
 }  // namespace bnb

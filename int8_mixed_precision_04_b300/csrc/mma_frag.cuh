@@ -38,6 +38,17 @@ __device__ __forceinline__ void mma_f16_16x8x16(float (&d)[4], uint32_t a0, uint
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// The same with bf16 operands.
+__device__ __forceinline__ void mma_bf16_16x8x16(float (&d)[4], uint32_t a0, uint32_t a1,
+                                                 uint32_t a2, uint32_t a3, uint32_t b0,
+                                                 uint32_t b1) {
+  asm(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
 // One 64-byte k-block: xa = row g, xb = row g+8 (A); w = row g of B.
 __device__ __forceinline__ void mma_s8_block(int (&d)[4], const uint4 &xa, const uint4 &xb,
                                              const uint4 &w) {
@@ -49,6 +60,11 @@ __device__ __forceinline__ void mma_f16_block(float (&d)[4], const uint4 &xa, co
                                               const uint4 &w) {
   mma_f16_16x8x16(d, xa.x, xb.x, xa.y, xb.y, w.x, w.y);
   mma_f16_16x8x16(d, xa.z, xb.z, xa.w, xb.w, w.z, w.w);
+}
+__device__ __forceinline__ void mma_bf16_block(float (&d)[4], const uint4 &xa, const uint4 &xb,
+                                               const uint4 &w) {
+  mma_bf16_16x8x16(d, xa.x, xb.x, xa.y, xb.y, w.x, w.y);
+  mma_bf16_16x8x16(d, xa.z, xb.z, xa.w, xb.w, w.z, w.w);
 }
 
 // Accumulator element i of an m16n8 tile: row g + 8*(i/2), column 2q + (i%2).

@@ -7,12 +7,14 @@
 // quantizes weights and activations"); the vector is the output channel.
 //
 // HBM-bound one-off pass: one warp per row, 16-byte loads, the absmax taken on
-// fp16 bit patterns (exact), the row read a second time (from L2) for codes.
+// fp16 (or bf16) bit patterns (exact), the row read a second time (from L2)
+// for codes.
 #include "common.cuh"
 #include "kernels.h"
 
 namespace bnb {
 
+template <bool kBf>
 __global__ void __launch_bounds__(256) quantize_weight_kernel(
     const uint4 *__restrict__ W16, int64_t N, int64_t K, int8_t *__restrict__ Wq,
     float *__restrict__ sw) {
@@ -31,8 +33,8 @@ __global__ void __launch_bounds__(256) quantize_weight_kernel(
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
-    const float a = h2f_bits(m);
-    const float r = code_recip(a);
+    const float a = e2f<kBf>(m);
+    const RowCode<kBf> rc(a);
     if (lane == 0) sw[n] = a;
     uint2 *out = reinterpret_cast<uint2 *>(Wq + n * K);
     for (int64_t v = lane; v < vecs; v += 32) {
@@ -41,9 +43,9 @@ __global__ void __launch_bounds__(256) quantize_weight_kernel(
       uint32_t packed[2] = {0, 0};
 #pragma unroll
       for (int i = 0; i < 4; i++) {
-        int c0 = code_of(h2f_bits(w[i] & 0xffffu), a, r);
-        int c1 = code_of(h2f_bits(w[i] >> 16), a, r);
-        uint32_t two = ((uint32_t)(c0 & 0xff)) | ((uint32_t)(c1 & 0xff) << 8);
+        const uint32_t c0 = rc.byte(e2f<kBf>(w[i] & 0xffffu));
+        const uint32_t c1 = rc.byte(e2f<kBf>(w[i] >> 16));
+        uint32_t two = (c0 & 0xffu) | ((c1 & 0xffu) << 8);
         packed[i / 2] |= two << (16 * (i % 2));
       }
       out[v] = make_uint2(packed[0], packed[1]);
@@ -51,13 +53,14 @@ __global__ void __launch_bounds__(256) quantize_weight_kernel(
   }
 }
 
-cudaError_t launch_quantize_weight(const void *W16, int64_t N, int64_t K, int8_t *Wq,
+cudaError_t launch_quantize_weight(const void *W16, int64_t N, int64_t K, bool bf16, int8_t *Wq,
                                    float *sw, cudaStream_t stream) {
   const int warps_per_block = 8;
   int64_t blocks = (N + warps_per_block - 1) / warps_per_block;
   if (blocks > 148 * 64) blocks = 148 * 64;
   ProfScope ps(kKidQuantWeight, stream);
-  quantize_weight_kernel<<<(unsigned)blocks, 32 * warps_per_block, 0, stream>>>(
+  (bf16 ? quantize_weight_kernel<true> : quantize_weight_kernel<false>)
+      <<<(unsigned)blocks, 32 * warps_per_block, 0, stream>>>(
       reinterpret_cast<const uint4 *>(W16), N, K, Wq, sw);
   note_launch();
   return cudaGetLastError();

@@ -17,27 +17,30 @@ from . import binding
 
 
 class Linear8bitLt(torch.nn.Module):
-    """y = x W^T + b through ``bnb_int8_linear_bias`` (fp16 in, fp16 out).
+    """y = x W^T + b through ``bnb_int8_linear_ex``, in the weight's dtype.
 
-    weight: [N, K] fp16 on a CUDA device (K a multiple of 16); bias: [N] fp16
-    or None; threshold: the outlier threshold tau (6.0 in the pages'
+    weight: [N, K] fp16 or bf16 on a CUDA device (K a multiple of 16); the
+    inputs are cast to its dtype and the output has it (bf16 is the compute
+    dtype the pages prefer where the hardware has it).  bias: [N] of the
+    weight's dtype or None; threshold: the outlier threshold tau (6.0 in the pages'
     experiments; ``math.inf`` turns the decomposition off, 0 sends every
-    column to fp16).  keep_fp16_weight: keep W16 as the source of the outlier
-    columns (``bnb_int8_linear_bias``), or keep only the int8 weight, half of
-    fp16's bytes, and take the outlier columns from the codes dequantized
-    (``bnb_int8_linear_wq_only``).  Inference only: no gradient flows
+    column to 16-bit).  keep_fp16_weight: keep the 16-bit weight as the
+    source of the outlier columns, or keep only the int8 weight, half of its
+    bytes, and take the outlier columns from the codes dequantized (W16 NULL).  Inference only: no gradient flows
     through the layer.
     """
 
     def __init__(self, weight: torch.Tensor, bias: torch.Tensor | None = None,
                  threshold: float = 6.0, keep_fp16_weight: bool = True):
         super().__init__()
-        if weight.dim() != 2 or weight.dtype != torch.float16 or not weight.is_cuda:
-            raise ValueError("weight must be a 2-D fp16 CUDA tensor")
+        if (weight.dim() != 2 or weight.dtype not in (torch.float16, torch.bfloat16)
+                or not weight.is_cuda):
+            raise ValueError("weight must be a 2-D fp16 or bf16 CUDA tensor")
         N, K = weight.shape
-        if bias is not None and (bias.shape != (N,) or bias.dtype != torch.float16
+        if bias is not None and (bias.shape != (N,) or bias.dtype != weight.dtype
                                  or bias.device != weight.device):
-            raise ValueError("bias must be an fp16 [N] tensor on the weight's device")
+            raise ValueError("bias must be an [N] tensor of the weight's dtype and device")
+        self.dtype = weight.dtype
         self.in_features, self.out_features = K, N
         self.threshold = float(threshold)
         W16 = weight.detach().contiguous()
@@ -50,12 +53,14 @@ class Linear8bitLt(torch.nn.Module):
 
     @classmethod
     def from_linear(cls, layer: torch.nn.Linear, threshold: float = 6.0,
-                    keep_fp16_weight: bool = True) -> "Linear8bitLt":
-        """The int8 layer for an existing ``nn.Linear`` (weights cast to fp16
-        on the current CUDA device if they are not there yet)."""
+                    keep_fp16_weight: bool = True,
+                    dtype: torch.dtype = torch.float16) -> "Linear8bitLt":
+        """The int8 layer for an existing ``nn.Linear`` (weights cast to
+        ``dtype``, fp16 or bf16, on the current CUDA device if they are not
+        there yet)."""
         dev = layer.weight.device if layer.weight.is_cuda else torch.device("cuda")
-        w = layer.weight.detach().to(dev, torch.float16)
-        b = None if layer.bias is None else layer.bias.detach().to(dev, torch.float16)
+        w = layer.weight.detach().to(dev, dtype)
+        b = None if layer.bias is None else layer.bias.detach().to(dev, dtype)
         return cls(w, b, threshold, keep_fp16_weight)
 
     def _workspace(self, T: int) -> torch.Tensor:
@@ -71,18 +76,15 @@ class Linear8bitLt(torch.nn.Module):
         if x.shape[-1] != self.in_features:
             raise ValueError(f"expected {self.in_features} input features, got {x.shape[-1]}")
         lead = x.shape[:-1]
-        X = x.reshape(-1, self.in_features).to(torch.float16).contiguous()
+        X = x.reshape(-1, self.in_features).to(self.dtype).contiguous()
         T = X.shape[0]
-        Y = torch.empty((T, self.out_features), dtype=torch.float16, device=X.device)
-        if T > 0 and self.W16 is not None:
-            binding.linear_bias(X, self.Wq, self.Wscale, self.W16, self.bias, self.threshold,
-                                Y=Y, workspace=self._workspace(T))
-        elif T > 0:
-            binding.linear_wq_only(X, self.Wq, self.Wscale, self.bias, self.threshold, Y=Y,
-                                   workspace=self._workspace(T))
+        Y = torch.empty((T, self.out_features), dtype=self.dtype, device=X.device)
+        if T > 0:
+            binding.linear_ex(X, self.Wq, self.Wscale, self.W16, self.bias, self.threshold,
+                              Y=Y, workspace=self._workspace(T))
         return Y.reshape(*lead, self.out_features)
 
     def extra_repr(self) -> str:
         return (f"in_features={self.in_features}, out_features={self.out_features}, "
-                f"bias={self.bias is not None}, threshold={self.threshold}, "
+                f"bias={self.bias is not None}, dtype={self.dtype}, threshold={self.threshold}, "
                 f"keep_fp16_weight={self.W16 is not None}")
