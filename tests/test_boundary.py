@@ -213,3 +213,42 @@ def test_fp16_weight_entry_points_need_w16(lib):
     assert lib.bnb_int8_linear_bias(FAKE, 16, 256, FAKE, FAKE, None, None, 256,
                                     ctypes.c_float(6.0), FAKE * 64, FAKE * 256, ws_bytes,
                                     None) == binding.Status.INVALID_ARG
+
+
+def test_ex_entry_points_check_dtype_on_host(lib):
+    """The general entry points reject an unknown element format, and run the
+    same argument checks as the fp16 ones, before touching a device."""
+    ws_bytes = lib.bnb_int8_linear_workspace_bytes(16, 256, 256)
+    tau = ctypes.c_float(6.0)
+    for dt in (2, -1):
+        assert lib.bnb_int8_quantize_weight_ex(FAKE, 256, 256, dt, FAKE * 8, FAKE * 16,
+                                               None) == binding.Status.INVALID_ARG
+        assert lib.bnb_int8_linear_ex(FAKE, 16, 256, FAKE * 8, FAKE * 16, FAKE * 24, None, 256,
+                                      tau, dt, FAKE * 64, FAKE * 256, ws_bytes,
+                                      None) == binding.Status.INVALID_ARG
+        assert lib.bnb_int8_linear_from_host_ex(FAKE, 16, 256, FAKE * 8, FAKE * 16, FAKE * 24,
+                                                None, 256, tau, dt, FAKE * 2, FAKE * 64,
+                                                FAKE * 96, FAKE * 256, ws_bytes,
+                                                None) == binding.Status.INVALID_ARG
+        assert lib.bnb_int8_linear_debug_ex(FAKE, 16, 256, FAKE * 8, FAKE * 16, FAKE * 24, None,
+                                            256, tau, dt, FAKE * 64, FAKE * 256, ws_bytes, None,
+                                            None, None, None, None,
+                                            None) == binding.Status.INVALID_ARG
+    # bf16 with the layer's own argument errors
+    assert lib.bnb_int8_quantize_weight_ex(FAKE, 256, 24, 1, FAKE * 8, FAKE * 16,
+                                           None) == binding.Status.UNSUPPORTED
+    assert lib.bnb_int8_linear_ex(FAKE, 16, 256, FAKE * 8, FAKE * 16, None, None, 256,
+                                  ctypes.c_float(math.nan), 1, FAKE * 64, FAKE * 256, ws_bytes,
+                                  None) == binding.Status.INVALID_ARG
+    assert lib.bnb_int8_linear_ex(FAKE, 16, 256, FAKE * 8, FAKE * 16, None, FAKE * 64 + 8, 256,
+                                  tau, 1, FAKE * 64, FAKE * 256, ws_bytes,
+                                  None) == binding.Status.UNSUPPORTED
+
+
+def test_binding_dtype_codes():
+    """The binding maps torch dtypes to bnb_dtype_t and refuses the rest."""
+    import torch
+    assert binding._dtype_code(torch.empty(1, dtype=torch.float16)) == 0
+    assert binding._dtype_code(torch.empty(1, dtype=torch.bfloat16)) == 1
+    with pytest.raises(TypeError):
+        binding._dtype_code(torch.empty(1, dtype=torch.float32))

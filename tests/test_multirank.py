@@ -59,6 +59,31 @@ def _worker(rank, port, q):
         y_cat = torch.cat(ys, dim=1).numpy().astype(np.uint16)
         out["nsplit_equal"] = bool(np.array_equal(y_cat, full["Y"].view(np.uint16)))
 
+        # the same split for the other forms of the layer: a bias (split with
+        # the channels), only the int8 weight, and bf16 X / W / bias / Y
+        bias = inputs.bias(40, 96, seed=5)
+        Wb = torch.from_numpy(w.W.astype(np.float32)).to(torch.bfloat16)
+        Wb = Wb.view(torch.int16).numpy().view(np.uint16)
+        Xb = torch.from_numpy(w.X.astype(np.float32)).to(torch.bfloat16)
+        Xb = Xb.view(torch.int16).numpy().view(np.uint16)
+        bb = torch.from_numpy(bias.astype(np.float32)).to(torch.bfloat16)
+        bb = bb.view(torch.int16).numpy().view(np.uint16)
+        Wqb, swb = orc.quantize_weight(Wb, fmt="bf16")
+        forms = {
+            "bias": (dict(X16=w.X, Wq=Wq, sw=sw, W16=w.W, bias=bias), {}),
+            "wq_only": (dict(X16=w.X, Wq=Wq, sw=sw, W16=None, bias=bias), {}),
+            "bf16": (dict(X16=Xb, Wq=Wqb, sw=swb, W16=Wb, bias=bb), {"fmt": "bf16"}),
+        }
+        for name, (a, kw) in forms.items():
+            full_f = orc.linear(a["X16"], a["Wq"], a["sw"], a["W16"], w.tau, bias=a["bias"], **kw)
+            mine_f = orc.linear(a["X16"], a["Wq"][n0:n1], a["sw"][n0:n1],
+                                None if a["W16"] is None else a["W16"][n0:n1], w.tau,
+                                bias=a["bias"][n0:n1], **kw)
+            ys = [torch.zeros(12, 20, dtype=torch.int32) for _ in range(WORLD)]
+            dist.all_gather(ys, torch.from_numpy(mine_f["Y"].view(np.uint16).astype(np.int32)))
+            y_cat = torch.cat(ys, dim=1).numpy().astype(np.uint16)
+            out["nsplit_equal_" + name] = bool(np.array_equal(y_cat, full_f["Y"].view(np.uint16)))
+
         # token split: OR all-reduce of the outlier column mask
         t0, t1 = rank * 6, (rank + 1) * 6
         X_loc = w.X[t0:t1]
@@ -101,6 +126,8 @@ def test_two_gloo_ranks():
         assert "error" not in res[r], res[r]
         assert res[r]["max"] == pytest.approx(3.0)
         assert res[r]["nsplit_equal"]
+        for name in ("bias", "wq_only", "bf16"):
+            assert res[r]["nsplit_equal_" + name], name
         assert res[r]["mask_equals_full_scan"]
         assert res[r]["tsplit_codes_equal"] and res[r]["tsplit_acc_equal"]
     # rank 0 does not see column 5's outlier: without the exchange it differs
