@@ -31,7 +31,8 @@
  *     given stream).
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *     stream).  Work is enqueued asynchronously on it.
- *   - fp16 data is IEEE binary16, passed as void*.
+ *   - fp16 data is IEEE binary16, passed as void*; the `_ex` entry points
+ *     also take bfloat16 (bnb_dtype_t) for X, W16, the bias and Y.
  *   - Argument errors are detected on the host before anything is enqueued;
  *     in that case nothing is written.
  *   - Alignment: every pointer 16-byte aligned, K a multiple of 16.

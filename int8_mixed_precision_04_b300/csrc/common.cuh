@@ -42,9 +42,9 @@ struct Workspace {
   float *sx;           // [T] row scales
   float *sxd;          // [T] row scales / 127 (GEMM epilogue)
   void *xcodes;        // [T x K] codes: int8 (decode) or fp16 integers (GEMM)
-  __half *xo;          // [T x kpad] fp16 outlier block (compacted, or masked X when dense)
+  __half *xo;          // [T x kpad] 16-bit outlier block in X's format (compacted, or masked X when dense)
   int64_t kpad;        // pitch of xo in elements (K rounded up to 64)
-  __half *w16o;        // [N x opad] W16 at the outlier columns (compacted; GEMM path, sparse)
+  __half *w16o;        // [N x opad] W16 (or Wq as 16-bit integers) at the outlier columns, X's format
   int64_t opad;        // pitch of w16o in elements: floor(K / 16) rounded up to 64
 };
 
