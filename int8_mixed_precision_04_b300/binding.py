@@ -182,6 +182,9 @@ def linear_ex(X, Wq, Wscale, W16, bias, tau: float, Y=None, workspace=None, stre
     import torch
     T, K = X.shape
     N = Wq.shape[0]
+    for name, t in (("W16", W16), ("bias", bias), ("Y", Y)):
+        if t is not None and t.dtype != X.dtype:  # one element format per call
+            raise TypeError(f"{name} is {t.dtype}, X is {X.dtype}")
     if Y is None:
         Y = torch.empty((T, N), dtype=X.dtype, device=X.device)
     if workspace is None:

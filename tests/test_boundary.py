@@ -252,3 +252,16 @@ def test_binding_dtype_codes():
     assert binding._dtype_code(torch.empty(1, dtype=torch.bfloat16)) == 1
     with pytest.raises(TypeError):
         binding._dtype_code(torch.empty(1, dtype=torch.float32))
+
+
+def test_binding_rejects_mixed_formats():
+    """One element format per call: the binding refuses a W16, bias or Y whose
+    dtype differs from X's before calling the library."""
+    import torch
+    X = torch.empty((16, 256), dtype=torch.bfloat16)
+    Wq = torch.empty((8, 256), dtype=torch.int8)
+    sw = torch.empty(8)
+    with pytest.raises(TypeError):
+        binding.linear_ex(X, Wq, sw, torch.empty((8, 256), dtype=torch.float16), None, 6.0)
+    with pytest.raises(TypeError):
+        binding.linear_ex(X, Wq, sw, None, torch.empty(8, dtype=torch.float16), 6.0)
