@@ -265,3 +265,17 @@ def test_binding_rejects_mixed_formats():
         binding.linear_ex(X, Wq, sw, torch.empty((8, 256), dtype=torch.float16), None, 6.0)
     with pytest.raises(TypeError):
         binding.linear_ex(X, Wq, sw, None, torch.empty(8, dtype=torch.float16), 6.0)
+
+
+def test_linear8bitlt_checks_its_weight():
+    """The module wants a 2-D fp16 or bf16 CUDA weight and a matching bias;
+    host tensors are refused before anything is quantized."""
+    import torch
+
+    from int8_mixed_precision_04_b300 import Linear8bitLt
+    with pytest.raises(ValueError):
+        Linear8bitLt(torch.zeros((8, 16), dtype=torch.float16))          # not on a GPU
+    with pytest.raises(ValueError):
+        Linear8bitLt(torch.zeros((8, 16), dtype=torch.float32))          # not 16-bit
+    with pytest.raises(ValueError):
+        Linear8bitLt(torch.zeros(16, dtype=torch.float16))               # not 2-D
