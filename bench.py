@@ -489,7 +489,7 @@ def run_ours(args, world, rank, local):
         "clocks": sampler.summary(),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_budget)
+        line["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_budget, **_forms(args))
     return line
 
 
@@ -502,11 +502,19 @@ class OracleArm:
     T rows, then S4..S6 for all T rows against a rotating slice of `n_slice`
     output channels."""
 
-    def __init__(self, w, n_slice: int):
+    def __init__(self, w, n_slice: int, bias: bool = False, wq_only: bool = False,
+                 bf16: bool = False):
         import oracle
         self.orc = oracle.get()
         self.w = w
-        self.Wq, self.sw = self.orc.quantize_weight(w.W)
+        self.fmt = "bf16" if bf16 else "fp16"
+        self.X, self.W = w.X, w.W
+        self.b = inputs.bias(w.N, w.K, seed=0) if bias else None
+        if bf16:  # the same values rounded to bf16, as the GPU arm's casts do
+            self.X, self.W = _bf16_bits(w.X), _bf16_bits(w.W)
+            self.b = None if self.b is None else _bf16_bits(self.b)
+        self.wq_only = wq_only
+        self.Wq, self.sw = self.orc.quantize_weight(self.W, fmt=self.fmt)
         self.n_slice = max(1, min(n_slice, w.N))
         self.pos = 0
 
@@ -514,12 +522,27 @@ class OracleArm:
         n0 = self.pos
         n1 = min(self.w.N, n0 + self.n_slice)
         self.pos = 0 if n1 >= self.w.N else n1
-        self.orc.linear(self.w.X, self.Wq[n0:n1], self.sw[n0:n1], self.w.W[n0:n1], self.w.tau)
+        self.orc.linear(self.X, self.Wq[n0:n1], self.sw[n0:n1],
+                        None if self.wq_only else self.W[n0:n1], self.w.tau,
+                        bias=None if self.b is None else self.b[n0:n1], fmt=self.fmt)
         return 2 * self.w.T * (n1 - n0) * self.w.K
 
 
-def _calibrate(w, target_s):
-    arm = OracleArm(w, 64)
+def _bf16_bits(a):
+    """fp16 (or fp32) values -> bfloat16 bit patterns, nearest-even."""
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16).copy()
+
+
+def _forms(args):
+    return dict(bias=bool(getattr(args, "bias", False)),
+                wq_only=bool(getattr(args, "wq_only", False)),
+                bf16=bool(getattr(args, "bf16", False)))
+
+
+def _calibrate(w, target_s, **forms):
+    arm = OracleArm(w, 64, **forms)
     t0 = time.perf_counter()
     arm.step()
     dt = time.perf_counter() - t0
@@ -527,10 +550,10 @@ def _calibrate(w, target_s):
     return max(1, int(target_s / max(per_chan, 1e-9)))
 
 
-def cpu_baseline(w, budget_s: float = 15.0):
+def cpu_baseline(w, budget_s: float = 15.0, **forms):
     import oracle
-    n_slice = _calibrate(w, budget_s / 4)
-    arm = OracleArm(w, n_slice)
+    n_slice = _calibrate(w, budget_s / 4, **forms)
+    arm = OracleArm(w, n_slice, **forms)
     ops = 0
     t0 = time.perf_counter()
     while time.perf_counter() - t0 < budget_s:
@@ -549,8 +572,9 @@ def run_reference(args, world, rank, local):
     w = make_workload(args.workload, args.T)
     total_steps = args.steps + args.warmup
     per_step = min(2.0, args.ref_budget / max(total_steps, 1))
-    n_slice = _calibrate(w, per_step)
-    arm = OracleArm(w, n_slice)
+    forms = _forms(args)
+    n_slice = _calibrate(w, per_step, **forms)
+    arm = OracleArm(w, n_slice, **forms)
     for _ in range(args.warmup):
         arm.step()
     ops = 0
@@ -567,10 +591,14 @@ def run_reference(args, world, rank, local):
         "metric": METRIC, "value": val, "unit": "TOPS", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "int8xint8->int32 + fp16 outliers (CPU oracle, fp64 epilogue)",
+        "dtype": (f"int8xint8->int32 + {'bf16' if forms['bf16'] else 'fp16'} outliers "
+                  f"(CPU oracle, fp64 epilogue)"),
         "data": "synthetic (seeded, inputs module)",
-        "config": {"workload": f"{args.workload}: X fp16 [{w.T},{w.K}], W fp16 [{w.N},{w.K}], "
-                               f"tau {w.tau}", "T": w.T, "K": w.K, "N": w.N, "tau": w.tau},
+        "config": {"workload": (f"{args.workload}: X {'bf16' if forms['bf16'] else 'fp16'} "
+                                f"[{w.T},{w.K}], W {'bf16' if forms['bf16'] else 'fp16'} "
+                                f"[{w.N},{w.K}], tau {w.tau}"),
+                   "T": w.T, "K": w.K, "N": w.N, "tau": w.tau, "bias": forms["bias"],
+                   "fp16_weight_resident": not forms["wq_only"]},
         "cpu_baseline": {"value": val, "unit": "TOPS", "cores": cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": val, "unit": "TOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
