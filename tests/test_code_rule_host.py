@@ -77,3 +77,36 @@ def test_bf16_scaled_rule_is_exact():
         want = oracle_pins._exact_codes_bf16(x.astype(np.float64), float(a))
         bad = np.flatnonzero(got != want)
         assert len(bad) == 0, (hex(ab), x[bad[:3]], got[bad[:3]], want[bad[:3]])
+
+
+def _bw_code(x: np.ndarray, a: np.float32) -> np.ndarray:
+    """The blockwise codec's fast path: p = fl32(127 x) * fl32(1 / a), a
+    magic-number rint, and the IEEE division only where p lies within 2^-14
+    of a half-integer."""
+    num = (np.float32(127.0) * x).astype(np.float32)
+    r = np.float32(1.0) / a
+    p = (num * r).astype(np.float32)
+    t = (p + KM).astype(np.float32)
+    e = (p - (t - KM).astype(np.float32)).astype(np.float32)
+    fast = (t.view(np.uint32) & 0xFF).astype(np.uint8).view(np.int8).astype(np.int64)
+    slow = np.rint((num / a).astype(np.float32)).astype(np.int64)
+    return np.where(np.abs(e) < np.float32(0.5 - 2.0 ** -14), fast, slow)
+
+
+def test_blockwise_fast_path_matches_the_division():
+    """The codec's reciprocal fast path gives rint(fl32(fl32(127 x) / a)) on
+    random states, exact ties and values right beside them."""
+    rng = np.random.default_rng(43)
+    for _ in range(200):
+        a = np.float32(np.abs(rng.standard_normal()) * 10.0 ** rng.integers(-20, 20) + 1e-30)
+        x = (rng.uniform(-1, 1, 20000) * a).astype(np.float32)
+        k = rng.integers(-127, 127, 4000)
+        ties = ((k + 0.5) * (float(a) / 127.0)).astype(np.float32)
+        near = np.concatenate([np.nextafter(ties, np.float32(np.inf)),
+                               np.nextafter(ties, np.float32(-np.inf))])
+        x = np.concatenate([x, ties, near, np.array([a, -a, 0.0], np.float32)])
+        x = x[np.abs(x) <= a]
+        want = np.rint(((np.float32(127.0) * x).astype(np.float32) / a).astype(np.float32))
+        got = _bw_code(x, a)
+        bad = np.flatnonzero(got != want.astype(np.int64))
+        assert len(bad) == 0, (float(a), x[bad[:3]], got[bad[:3]], want[bad[:3]])
