@@ -8,8 +8,10 @@ Two independent statements of the method:
 
 * ``oracle.c`` (through :class:`Oracle`): plain C loops with OpenMP, int64
   accumulation checked to fit int32, epilogue in double with one final
-  rounding to fp16.  Usable at full size for S1-S3 and on sampled rows for
-  S4-S6.
+  rounding to fp16 (or bf16).  Usable at full size for S1-S3 and on sampled
+  rows for S4-S6.  Forms: fp16 or bf16 data (``fmt``), an optional bias, and
+  the outlier weights from W16 or, with ``W16=None``, from the int8 codes
+  dequantized; and the blockwise 8-bit codec of optimizer states.
 * :mod:`oracle.brute`: pure Python with exact integers and
   :class:`fractions.Fraction`, for tiny inputs.
 
