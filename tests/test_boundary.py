@@ -279,3 +279,25 @@ def test_linear8bitlt_checks_its_weight():
         Linear8bitLt(torch.zeros((8, 16), dtype=torch.float32))          # not 16-bit
     with pytest.raises(ValueError):
         Linear8bitLt(torch.zeros(16, dtype=torch.float16))               # not 2-D
+
+
+def test_cuda_failure_surfaces_as_status(lib):
+    """A failing CUDA layer (here: no device at all) reaches the caller as
+    BNB_ERR_CUDA from every entry point once its argument checks pass, with
+    nothing enqueued and nothing crashing.  Runs only where no GPU is
+    visible: the pointers are fake."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is visible: the fake pointers must not reach a device")
+    ws_bytes = lib.bnb_int8_linear_workspace_bytes(16, 256, 256)
+    tau = ctypes.c_float(6.0)
+    cuda = binding.Status.CUDA
+    assert lib.bnb_int8_quantize_weight(FAKE, 256, 256, FAKE * 8, FAKE * 16, None) == cuda
+    assert lib.bnb_int8_linear(FAKE, 16, 256, FAKE * 8, FAKE * 16, FAKE * 24, 256, tau,
+                               FAKE * 64, FAKE * 256, ws_bytes, None) == cuda
+    assert lib.bnb_int8_linear_ex(FAKE, 16, 256, FAKE * 8, FAKE * 16, None, None, 256, tau, 1,
+                                  FAKE * 64, FAKE * 256, ws_bytes, None) == cuda
+    assert lib.bnb_int8_quantize_blockwise(FAKE, 1 << 16, 256, FAKE * 64, FAKE * 128,
+                                           None) == cuda
+    out = ctypes.c_int32(0)
+    assert lib.bnb_last_device_status(FAKE * 256, None, ctypes.byref(out)) == cuda
