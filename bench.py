@@ -735,6 +735,42 @@ def run_blockwise(args, world, rank, local):
     return line
 
 
+def run_reference_blockwise(args, world, rank, local):
+    """The reference arm of the codec workload: the oracle's codec, as it
+    stands, on a bounded sample of the same state (the first 2^22 values of a
+    seeded normal x 1e-3 state), each step one quantize + decode pass."""
+    if rank != 0:
+        return None
+    import oracle
+    orc = oracle.get()
+    n, B, m = 28672 * 8192, 256, 1 << 22
+    rng = np.random.default_rng(1234)
+    xs = (rng.standard_normal(m) * 1e-3).astype(np.float32)
+    step_bytes = 10 * m + 8 * ((m + B - 1) // B)
+    for _ in range(args.warmup):
+        orc.dequantize_blockwise(*orc.quantize_blockwise(xs, B), B)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        orc.dequantize_blockwise(*orc.quantize_blockwise(xs, B), B)
+    dt = time.perf_counter() - t0
+    val = args.steps * step_bytes / dt / 1e9
+    sample = f"the first {m} values of the state per step, blocks of {B}"
+    return {
+        "impl": "reference",
+        "metric": "blockwise int8 codec GB/s (algorithmic bytes of quantize + dequantize)",
+        "value": val, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "fp32 -> int8 + fp32 absmax -> fp32 (CPU oracle)",
+        "data": "synthetic (seeded normal x 1e-3)",
+        "config": {"workload": f"blockwise: fp32 state [{n}] (28672 x 8192), blocks of {B}",
+                   "n": n, "block": B},
+        "cpu_baseline": {"value": val, "unit": "GB/s", "cores": orc.num_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": val, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -761,7 +797,9 @@ def main():
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
     world, rank, local = dist_setup(args.gpus)
-    if args.impl == "reference":
+    if args.impl == "reference" and args.workload == "blockwise":
+        line = run_reference_blockwise(args, world, rank, local)
+    elif args.impl == "reference":
         line = run_reference(args, world, rank, local)
     elif args.workload == "blockwise":
         line = run_blockwise(args, world, rank, local)
