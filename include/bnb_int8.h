@@ -234,6 +234,11 @@ bnb_status_t bnb_int8_linear_from_host(const void *X_host, int64_t T, int64_t K,
  *     when a = 0), and absmax [ceil(n / block)] fp32.
  *   bnb_int8_dequantize_blockwise: codes [n], absmax -> y [n] fp32,
  *     y[i] = fl32(fl32(codes[i] * a) / 127).
+ *   Every finite fp32 input is accepted.  A block with a >= 2^120, where
+ *   127 x and codes * a would overflow fp32, is coded as if x and a were
+ *   multiplied by 2^-8 and decoded at that scale, the value multiplied back by
+ *   2^8.  Both give the formulas above wherever those are finite, and the
+ *   codes of such a block are still the integers nearest to 127 x / a.
  * Device pointers, 16-byte aligned, caller-owned; outputs must not overlap
  * inputs.  Errors: BNB_ERR_INVALID_ARG (NULL, n <= 0, overlap),
  * BNB_ERR_UNSUPPORTED (block size, alignment, n > BNB_MAX_BLOCKWISE_N,

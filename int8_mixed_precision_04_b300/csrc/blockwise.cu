@@ -9,7 +9,13 @@
 // the scale is the block's absmax a; the code is rint(fl32(fl32(127 x) / a)),
 // ties to even (0 when a = 0); the decoded value is fl32(fl32(q a) / 127).
 // Every operation is one IEEE fp32 rounding (no contraction), so codes and
-// decoded values are reproducible bit for bit.
+// decoded values are reproducible bit for bit.  For a >= 2^120, 127 x and
+// q a would overflow fp32 (FLT_MAX / 127 is about 2^121): such a block is
+// coded with x and a multiplied by 2^-8 and decoded at that scale, the value
+// multiplied back by 2^8.  A power-of-two factor commutes with every IEEE
+// rounding in the normal range, so this gives the plain formulas' results
+// wherever those are finite (values pushed below the normal range have code
+// 0 either way).
 //
 // Both kernels stream HBM: each thread moves 8 consecutive values (two
 // 16-byte loads or stores of fp32, one 8-byte access of codes); the B/8
@@ -30,6 +36,9 @@ constexpr int64_t kBwChunk = (int64_t)kBwThreads * kBwPerThread;
 // cannot cross a half-integer, only land on one) round like p, and rint(p)
 // -- one magic-number add, ties to even -- is the code.  Otherwise (rarely)
 // the IEEE division decides.
+// The factor of a block with absmax a (see above).
+__device__ __forceinline__ float bw_scale(float a) { return a >= 0x1p120f ? 0x1p-8f : 1.0f; }
+
 __device__ __forceinline__ int8_t bw_code(float x, float a, float r) {
   if (!(a > 0.0f)) return 0;
   constexpr float kM = 12582912.0f;  // 1.5 * 2^23: unit spacing
@@ -75,10 +84,11 @@ __global__ void __launch_bounds__(kBwThreads) quantize_blockwise_kernel(
     }
     if (e0 < n) {
       if ((tid % G) == 0) absmax[e0 / B] = m;
-      const float r = m > 0.0f ? __frcp_rn(m) : 0.0f;
+      const float s = bw_scale(m), ms = __fmul_rn(m, s);
+      const float r = ms > 0.0f ? __frcp_rn(ms) : 0.0f;
       int8_t q[kBwPerThread];
 #pragma unroll
-      for (int i = 0; i < kBwPerThread; i++) q[i] = bw_code(v[i], m, r);
+      for (int i = 0; i < kBwPerThread; i++) q[i] = bw_code(__fmul_rn(v[i], s), ms, r);
       if (e0 + kBwPerThread <= n) {
         uint2 w;
         w.x = (uint32_t)(uint8_t)q[0] | ((uint32_t)(uint8_t)q[1] << 8) |
@@ -101,7 +111,8 @@ __global__ void __launch_bounds__(kBwThreads) dequantize_blockwise_kernel(
   for (int64_t c = blockIdx.x; c < nchunks; c += gridDim.x) {
     const int64_t e0 = c * kBwChunk + (int64_t)threadIdx.x * kBwPerThread;
     if (e0 >= n) continue;
-    const float a = __ldg(absmax + e0 / B);  // the 8 values share one block (B >= 64)
+    const float a0 = __ldg(absmax + e0 / B);  // the 8 values share one block (B >= 64)
+    const float s = bw_scale(a0), a = __fmul_rn(a0, s), inv_s = a0 >= 0x1p120f ? 256.0f : 1.0f;
     int8_t q[kBwPerThread];
     if (e0 + kBwPerThread <= n) {
       const uint2 w = __ldg(reinterpret_cast<const uint2 *>(codes + e0));
@@ -116,7 +127,8 @@ __global__ void __launch_bounds__(kBwThreads) dequantize_blockwise_kernel(
     }
     float o[kBwPerThread];
 #pragma unroll
-    for (int i = 0; i < kBwPerThread; i++) o[i] = __fdiv_rn(__fmul_rn((float)q[i], a), 127.0f);
+    for (int i = 0; i < kBwPerThread; i++)
+      o[i] = __fmul_rn(__fdiv_rn(__fmul_rn((float)q[i], a), 127.0f), inv_s);
     if (e0 + kBwPerThread <= n) {
       float4 *dst = reinterpret_cast<float4 *>(y + e0);
       dst[0] = make_float4(o[0], o[1], o[2], o[3]);

@@ -348,7 +348,16 @@ int orc_linear_rows(const uint16_t *X, int64_t T, int64_t K, const int8_t *Wq,
  * block size and no code map): fp32 values in blocks of B consecutive
  * elements (the last block may be short), the block's scale is its absmax
  * a, the code is q = rint(fl32(fl32(127 * x) / a)) in IEEE fp32, ties to
- * even (0 when a = 0), and the decoded value is fl32(fl32(q * a) / 127). */
+ * even (0 when a = 0), and the decoded value is fl32(fl32(q * a) / 127).
+ * For a >= 2^120 those formulas leave fp32's range (127 x and q a reach
+ * 2^127 * 127 > FLT_MAX), so such a block is coded and decoded with x and a
+ * first multiplied by 2^-8 and the decoded value multiplied back by 2^8.
+ * A power-of-two factor commutes with every IEEE rounding in the normal
+ * range, so the scaled formulas give the plain ones' results wherever those
+ * are finite; values that the factor pushes below the normal range have
+ * code 0 either way (|127 x / a| < 2^-100 there). */
+static float codec_scale(float a) { return a >= 0x1p120f ? 0x1p-8f : 1.0f; }
+
 int orc_quantize_blockwise(const float *x, int64_t n, int64_t B, int8_t *q, float *absmax) {
   if (n < 0 || B <= 0) return ORC_ERR_ARG;
   const int64_t nb = (n + B - 1) / B;
@@ -361,12 +370,14 @@ int orc_quantize_blockwise(const float *x, int64_t n, int64_t B, int8_t *q, floa
       if (v > a) a = v;
     }
     absmax[b] = a;
+    const float s = codec_scale(a);
+    const float as = a * s;
     for (int64_t i = i0; i < i1; i++) {
       if (a == 0.0f) {
         q[i] = 0;
       } else {
-        const float num = 127.0f * x[i];
-        q[i] = (int8_t)rintf(num / a);
+        const float num = 127.0f * (x[i] * s);
+        q[i] = (int8_t)rintf(num / as);
       }
     }
   }
@@ -378,8 +389,9 @@ int orc_dequantize_blockwise(const int8_t *q, const float *absmax, int64_t n, in
   if (n < 0 || B <= 0) return ORC_ERR_ARG;
 #pragma omp parallel for schedule(static)
   for (int64_t i = 0; i < n; i++) {
-    const float prod = (float)q[i] * absmax[i / B];
-    y[i] = prod / 127.0f;
+    const float a = absmax[i / B], s = codec_scale(a);
+    const float prod = (float)q[i] * (a * s);
+    y[i] = (prod / 127.0f) / s;
   }
   return ORC_OK;
 }

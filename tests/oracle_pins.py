@@ -563,6 +563,59 @@ def pin_blockwise_zero_and_scaling(orc):
         assert np.array_equal(a2, a * np.float32(2.0 ** k))
 
 
+def pin_blockwise_huge_scale(orc):
+    """Blocks whose absmax is near the top of fp32's range, where 127 x and
+    q a overflow fp32 if computed as written: the codes are still the integers
+    nearest to 127 x / a (exact quotients, exact ties to the even neighbour,
+    +-127 at the absmax, +-FLT_MAX included), and every decoded value is
+    finite and within half a code step of x."""
+    rng = np.random.default_rng(15)
+    B = 64
+    # closed forms at a = 127 * 2^e for e up to 120 (a up to 1.7e38)
+    xs, qs, ys = [], [], []
+    for e in (110, 113, 114, 115, 116, 117, 118, 119, 120):
+        s = 2.0 ** e
+        k = rng.integers(-126, 127, size=B - 1)
+        tie = rng.integers(0, 2, size=B - 1).astype(bool)
+        vals = np.where(tie, (k + 0.5) * s, k * s)
+        codes = np.where(tie, np.where(k % 2 == 0, k, k + 1), k)
+        pos = int(rng.integers(0, B))
+        sign = 1 if e % 2 else -1
+        xs.append(np.insert(vals, pos, sign * 127 * s))
+        qs.append(np.insert(codes, pos, sign * 127))
+        ys.append(np.insert(codes * s, pos, sign * 127 * s))
+    x = np.concatenate(xs).astype(np.float32)
+    q, a = orc.quantize_blockwise(x, B)
+    assert np.array_equal(q.astype(np.int64), np.concatenate(qs))
+    y = orc.dequantize_blockwise(q, a, B)
+    assert np.array_equal(y, np.concatenate(ys).astype(np.float32))
+    # a = 2^127 (a power of two): 127 x / a is exact in binary for x with few
+    # significant bits, so the code is that quotient rounded half to even
+    k = rng.integers(-2 ** 16, 2 ** 16, size=(2, B))
+    xp = (k * 2.0 ** 111).astype(np.float32)
+    xp[0, 5], xp[1, 9] = 2.0 ** 127, -(2.0 ** 127)
+    q, a = orc.quantize_blockwise(xp.ravel(), B)
+    assert np.array_equal(a, np.float32([2.0 ** 127, 2.0 ** 127]))
+    want = [int(round(Fraction(127 * int(v), 2 ** 16))) for v in k.ravel()]
+    want = np.array(want).reshape(2, B)
+    want[0, 5], want[1, 9] = 127, -127
+    assert np.array_equal(q.astype(np.int64).reshape(2, B), want)
+    # +-FLT_MAX and random values below it: +-127 at the absmax, |q - 127x/a|
+    # at most 1/2, decoded values finite and within a / 254 (up to fp32 rounding)
+    fmax = np.finfo(np.float32).max
+    xr = (rng.uniform(-1, 1, size=3 * B) * fmax).astype(np.float32)
+    xr[7], xr[B + 3], xr[2 * B + 60] = fmax, -fmax, fmax
+    q, a = orc.quantize_blockwise(xr, B)
+    assert np.array_equal(a, np.full(3, fmax, np.float32))
+    assert q[7] == 127 and q[B + 3] == -127 and q[2 * B + 60] == 127
+    exact = 127 * xr.astype(np.float64) / np.float64(fmax)
+    assert np.abs(q.astype(np.float64) - exact).max() <= 0.5 + 1e-6
+    y = orc.dequantize_blockwise(q, a, B)
+    assert np.isfinite(y).all()
+    err = np.abs(y.astype(np.float64) - xr.astype(np.float64))
+    assert err.max() <= float(fmax) * (1 / 254 + 1e-6)
+
+
 def pin_blockwise_memory(orc):
     """8-bit codes take a quarter of the fp32 bytes (bitsandbytes GPU page,
     section "Why quantization matters for LLM deployment"), plus one fp32
@@ -597,4 +650,5 @@ ALL_PINS = [
     pin_blockwise_locality,
     pin_blockwise_zero_and_scaling,
     pin_blockwise_memory,
+    pin_blockwise_huge_scale,
 ]

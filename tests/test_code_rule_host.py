@@ -110,3 +110,27 @@ def test_blockwise_fast_path_matches_the_division():
         got = _bw_code(x, a)
         bad = np.flatnonzero(got != want.astype(np.int64))
         assert len(bad) == 0, (float(a), x[bad[:3]], got[bad[:3]], want[bad[:3]])
+
+
+def test_blockwise_fast_path_at_the_top_of_the_range():
+    """Blocks with absmax a >= 2^120 are coded at the scale 2^-8: the fast
+    path on the scaled values equals the scaled division, which equals the
+    unscaled one wherever 127 x stays finite, and gives +-127 at +-a."""
+    rng = np.random.default_rng(44)
+    s = np.float32(2.0 ** -8)
+    fmax = np.finfo(np.float32).max
+    for a in [fmax, np.float32(3e38), np.float32(2.0 ** 121), np.float32(2.0 ** 120),
+              *[np.float32(v) for v in 10.0 ** rng.uniform(36.13, 38.5, 60)]]:
+        a = np.float32(min(a, fmax))
+        x = (rng.uniform(-1, 1, 20000) * a).astype(np.float32)
+        x = np.concatenate([x, np.array([a, -a, 0.0, a / 254, -a / 254], np.float32)])
+        xs, as_ = (x * s).astype(np.float32), np.float32(a * s)
+        got = _bw_code(xs, as_)
+        want = np.rint(((np.float32(127.0) * xs).astype(np.float32) / as_).astype(np.float32))
+        assert np.array_equal(got, want.astype(np.int64))
+        assert got[-5] == 127 and got[-4] == -127
+        with np.errstate(over="ignore"):
+            plain = (np.float32(127.0) * x).astype(np.float32)
+        ok = np.isfinite(plain)
+        plain_q = np.rint((plain[ok] / a).astype(np.float32)).astype(np.int64)
+        assert np.array_equal(got[ok], plain_q)

@@ -53,11 +53,14 @@ MUTATIONS = {
                                     "double w = (double)Wq[n * K + j] * (double)sw[n] / 127.0;"),
     "w16_free_scale_of_row_0": ("double w = (double)Wq[n * K + O[j]] * (double)sw[n] / 127.0;",
                                 "double w = (double)Wq[n * K + O[j]] * (double)sw[0] / 127.0;"),
-    "blockwise_truncates": ("q[i] = (int8_t)rintf(num / a);", "q[i] = (int8_t)truncf(num / a);"),
+    "blockwise_truncates": ("q[i] = (int8_t)rintf(num / as);", "q[i] = (int8_t)truncf(num / as);"),
     "blockwise_scale_of_whole_tensor": ("for (int64_t i = i0; i < i1; i++) {\n      const float v",
                                         "for (int64_t i = 0; i < n; i++) {\n      const float v"),
     "blockwise_block_shifted": ("const int64_t i0 = b * B, i1", "const int64_t i0 = b * B + 1, i1"),
-    "blockwise_decode_128": ("y[i] = prod / 127.0f;", "y[i] = prod / 128.0f;"),
+    "blockwise_decode_128": ("y[i] = (prod / 127.0f) / s;", "y[i] = (prod / 128.0f) / s;"),
+    "blockwise_unscaled": ("return a >= 0x1p120f ? 0x1p-8f : 1.0f;", "return (void)a, 1.0f;"),
+    "blockwise_scale_threshold_late": ("return a >= 0x1p120f ? 0x1p-8f : 1.0f;",
+                                       "return a >= 0x1p122f ? 0x1p-8f : 1.0f;"),
     "blockwise_scale_of_first": ("if (v > a) a = v;", "if (i == i0) a = v;"),
 }
 
