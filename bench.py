@@ -2,31 +2,38 @@
 """Benchmark of the LLM.int8() decomposition linear on B300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload decode|prefill|large|sweep|tiny]
+                    [--workload large|prefill|decode|decode_k8192|sweep|tiny|blockwise]
 
 Prints ONE JSON line (rank 0).  Metric: effective TOPS = 2*T*N*K / time of
 the int8 decomposition linear, whole job.
 
-Default workload: the decode GEMV configuration (X fp16 [16, 4096] with 4
-seeded outlier columns x U(8,60), W fp16 [4096, 4096] ~ N(0, 0.02), tau 6).
-A step is one token batch through a stack of 16 such layers, each with its
-own weight, input and output, so that the 16 x 16.8 MB of int8 weights
-(268 MB) exceed the 126 MB L2 and every call streams its weight from HBM.
-The timed region replays CUDA graphs of captured library calls; inputs are
-resident in HBM.  `--workload prefill|large|sweep|tiny` runs the other named
-shapes the same way (with as many layers as it takes to exceed 2x L2).
+Default workload: the large MLP configuration (X fp16 [4096, 8192] with 8
+seeded outlier columns x U(8,60), W fp16 [28672, 8192] ~ N(0, 0.015), tau 6),
+the largest configuration that fits one GPU.  A step is R replays of a CUDA
+graph of L library calls, one per distinct layer (own int8 weight, fp16
+weight, input and output; L such that the streamed bytes exceed twice the L2,
+queried from the device), with R chosen so that the timed region lasts at
+least --min-timed-s (1.2 s) at the given --steps.  Inputs are resident in HBM.
+
+`roofline` is for the dominant kernel: its algorithmic flops (tensor-bound
+GEMM) or bytes (HBM-bound decode kernel) per launch over its average
+duration, timed with CUDA events over a loop of about a second of graphs of
+main-kernel-only calls (bnb_int8_linear_opts with BNB_OPT_MAIN_ONLY: the GEMM
+on the activation-pass results the timed calls left in the workspace, or the
+whole fused decode kernel).  The GEMM's denominator is the sustained bf16
+figure of MEASURED_PEAKS.json (the burst one beside it); the decode kernel's
+is the measured HBM copy bandwidth.
+
+`other_regimes` measures, in the same run and the same way, the decode GEMV
+configuration (X [16, 4096], W [4096, 4096]), a decode step through the large
+MLP weight (X [16, 8192], W [28672, 8192]) and the prefill configuration.
 
 `e2e` is the same metric through the public API with host buffers: every
 call is bnb_int8_linear_from_host (a pinned host->device copy of X, the
 layer, a device->host copy of Y), all inside the timed region; consecutive
 calls alternate over two streams with their own device buffers and
-workspaces, so that copies overlap the neighbouring call's kernel.
-
-`roofline` is for the dominant kernel: its algorithmic bytes (or flops) per
-launch over its average duration, measured with CUDA events around a CUDA
-graph of that kernel alone (library profiling mode 2, which launches only the
-main kernel of the path: the fused decode kernel, or the GEMM on the
-activation-pass results the timed calls left behind).
+workspaces, so that copies overlap the neighbouring call's kernel.  It has
+its own warm-up (--e2e-warmup calls) and at least --e2e-timed-s of calls.
 
 `--impl reference` times the CPU oracle (the reference arm of this build):
 each step is a bounded sample of the same workload (all rows of X, a
@@ -56,7 +63,6 @@ sys.path.insert(0, ROOT)
 import inputs  # noqa: E402
 
 METRIC = "int8-decomposed linear effective TOPS (2*T*N*K/s)"
-L2_BYTES = 126 * 1024 * 1024
 
 
 def load_peaks():
@@ -74,6 +80,10 @@ def load_peaks():
 def make_workload(name: str, T: int):
     if name == "decode":
         return inputs.decode(T=T)
+    if name == "decode_k8192":  # a decode step through the large MLP weight
+        return inputs.decode(T=T, K=8192, N=28672)
+    if name == "decode_n11008":  # a decode step through the prefill weight
+        return inputs.decode(T=T, K=4096, N=11008)
     if name == "prefill":
         return inputs.prefill()
     if name == "large":
@@ -247,27 +257,57 @@ def max_over_ranks(x: float, world: int, device=None) -> float:
 # our arm
 # ---------------------------------------------------------------------------
 
-def run_ours(args, world, rank, local):
+def _l2_bytes(dev) -> int:
+    import torch
+    v = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0)
+    return int(v) if v else 126 * 1024 * 1024
+
+
+def _graph(fn, stream):
+    import torch
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        fn()
+    return g
+
+
+def _time_replays(g, reps, stream, sampler=None, world=1, dev=None):
+    """ms of `reps` replays of graph g on `stream` (CUDA events, synchronised
+    on both sides; max over ranks)."""
+    import torch
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        barrier(world)
+        torch.cuda.synchronize()
+        if sampler:
+            sampler.mark_start()
+        e0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if sampler:
+            sampler.mark_stop()
+    barrier(world)
+    return max_over_ranks(e0.elapsed_time(e1), world, dev)
+
+
+def measure_layer(args, w, dev, world, local, steps, min_timed_s, min_layers=2,
+                  with_e2e=True, with_kernel=True):
+    """One workload measured the bench's way.  A step is R replays of a CUDA
+    graph of L library calls, one per distinct layer (own int8 weight, fp16
+    weight, input and output), with L large enough that the bytes the calls
+    stream exceed twice the L2 and R large enough that `steps` steps take at
+    least `min_timed_s`."""
     import torch
 
-    from int8_mixed_precision_04_b300 import binding, build
-    build.build()
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
+    from int8_mixed_precision_04_b300 import binding
     lib = binding.load()
-
-    w = make_workload(args.workload, args.T)
     T, K, N, tau = w.T, w.K, w.N, w.tau
-    wq_bytes = N * K
-    # enough distinct layers (own weight, input and output each) that the
-    # bytes one step streams (int8 weight + fp16 activations) exceed 2x L2,
-    # so no call finds its operands in L2 from the previous step
-    layers = max(1, math.ceil(2 * L2_BYTES / (wq_bytes + 2 * T * K)))
-    if args.workload == "decode":
-        layers = max(layers, 16)
+    l2 = _l2_bytes(dev)
+    layers = max(min_layers, math.ceil(2 * l2 / (N * K + 2 * T * K)))
     layers = min(layers, args.max_layers)
-
-    # --bf16: the same workload with X, W16, bias and Y in bf16 (nearest-even casts)
     edt = torch.bfloat16 if args.bf16 else torch.float16
     Xh = torch.from_numpy(w.X).to(edt)
     W16_0 = torch.from_numpy(w.W).to(dev).to(edt)
@@ -281,182 +321,198 @@ def run_ours(args, world, rank, local):
         Wqs.append(Wq)
         sws.append(sw)
     Xs = [Xh.to(dev) for _ in range(layers)]
-    # optional fp16 bias per layer (nn.Linear's), through bnb_int8_linear_bias
     Bs = ([torch.from_numpy(inputs.bias(N, K, seed=i)).to(dev).to(edt) for i in range(layers)]
           if args.bias else [None] * layers)
     Ys = [torch.empty((T, N), dtype=edt, device=dev) for _ in range(layers)]
     ws = torch.empty(binding.workspace_bytes(T, N, K), dtype=torch.uint8, device=dev)
     stream = torch.cuda.Stream(device=dev)
 
-    def step(s):
+    def calls(opts=0):
         for i in range(layers):
-            if args.wq_only:
+            if opts:
+                binding.linear_opts(Xs[i], Wqs[i], sws[i], W16s[i], tau, opts, bias=Bs[i],
+                                    Y=Ys[i], workspace=ws, stream=stream)
+            elif args.wq_only:
                 binding.linear_wq_only(Xs[i], Wqs[i], sws[i], Bs[i], tau, Y=Ys[i], workspace=ws,
-                                       stream=s)
-            elif args.bias:
-                binding.linear_bias(Xs[i], Wqs[i], sws[i], W16s[i], Bs[i], tau, Y=Ys[i],
-                                    workspace=ws, stream=s)
+                                       stream=stream)
+            elif args.bias or args.bf16:
+                binding.linear_ex(Xs[i], Wqs[i], sws[i], W16s[i], Bs[i], tau, Y=Ys[i],
+                                  workspace=ws, stream=stream)
             else:
                 binding.linear(Xs[i], Wqs[i], sws[i], W16s[i], tau, Y=Ys[i], workspace=ws,
-                               stream=s)
+                               stream=stream)
 
-    # outlier count of this workload (for byte accounting)
-    dbg = binding.linear_debug(Xs[0], Wqs[0], sws[0], W16_0, tau)
+    dbg = binding.linear_debug(Xs[0], Wqs[0], sws[0], W16s[0], tau, want_acc=False)
     nO = int(dbg["nO"].item())
     del dbg
-
     with torch.cuda.stream(stream):
         for _ in range(max(args.warmup, 3)):
-            step(stream)
+            calls()
     stream.synchronize()
-
-    # graphs: one graph per step-chunk of G steps
-    G = max(1, min(args.steps, 8 if layers >= 16 else 32))
     before = lib.bnb_launch_count()
-    g_main = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g_main, stream=stream):
-        for _ in range(G):
-            step(stream)
-    launches_per_step = (lib.bnb_launch_count() - before) / G
-    rem = args.steps % G
-    g_rem = None
-    if rem:
-        g_rem = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g_rem, stream=stream):
-            for _ in range(rem):
-                step(stream)
-    # CUDAGraph.replay() launches on torch's current stream: every replay and
-    # every event below runs with `stream` current, so the events time it
-    with torch.cuda.stream(stream):
-        for _ in range(2):
-            g_main.replay()
+    g = _graph(calls, stream)
+    launches_per_graph = lib.bnb_launch_count() - before
+    for _ in range(3):
+        with torch.cuda.stream(stream):
+            g.replay()
     torch.cuda.synchronize()
-
-    start = torch.cuda.Event(enable_timing=True)
-    stop = torch.cuda.Event(enable_timing=True)
+    probe_ms = _time_replays(g, 5, stream, world=world, dev=dev) / 5
+    R = max(1, math.ceil(min_timed_s * 1e3 / (steps * probe_ms)))
     sampler = ClockSampler(local)
-    with sampler, torch.cuda.stream(stream):
-        barrier(world)
-        torch.cuda.synchronize()
-        sampler.mark_start()
-        start.record(stream)
-        for _ in range(args.steps // G):
-            g_main.replay()
-        if g_rem is not None:
-            g_rem.replay()
-        stop.record(stream)
-        torch.cuda.synchronize()
-        sampler.mark_stop()
-    barrier(world)
-    ms = start.elapsed_time(stop)
-    ms = max_over_ranks(ms, world, dev)
-    calls = args.steps * layers
+    with sampler:
+        ms = _time_replays(g, steps * R, stream, sampler, world, dev)
+    ncalls = steps * R * layers
     ops = 2 * T * N * K
-    value = world * calls * ops / (ms * 1e-3) / 1e12
+    value = world * ncalls * ops / (ms * 1e-3) / 1e12
     alg_bytes = algorithmic_bytes(T, N, K, nO, args.bias, args.wq_only)
-    gbs = world * calls * alg_bytes / (ms * 1e-3) / 1e9
-
-    # the dominant kernel alone: a graph of main-kernel-only launches (library
-    # profiling mode 2 reuses the act-pass results left in the workspace by the
-    # calls above, same X and tau), timed with CUDA events on its stream
-    path = lib.bnb_int8_linear_path(T, N, K)
-    kname = {1: "dec_fused", 2: "gemm_tc", 3: "gemm_mma"}[path]
-    Gk = max(1, min(G, 8))
-    binding.profile_enable(2)
-    try:
-        g_k = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g_k, stream=stream):
-            for _ in range(Gk):
-                step(stream)
-    finally:
-        binding.profile_enable(0)
-    reps = max(3, min(args.steps // Gk, 2000))
-    k0 = torch.cuda.Event(enable_timing=True)
-    k1 = torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        g_k.replay()
-        torch.cuda.synchronize()
-        k0.record(stream)
-        for _ in range(reps):
-            g_k.replay()
-        k1.record(stream)
-    torch.cuda.synchronize()
-    kms = k0.elapsed_time(k1)
-    kavg_s = kms * 1e-3 / (reps * Gk * layers)
-    kb, kf = kernel_algorithmic(kname, T, N, K, nO, args.bias, args.wq_only)
+    out = {
+        "value": value, "ms_per_step": ms / steps, "us_per_call": ms * 1e3 / ncalls,
+        "calls_per_step": R * layers, "layers": layers, "graph_replays_per_step": R,
+        "timed_s": ms * 1e-3, "n_outliers": nO, "gb_per_s": world * ncalls * alg_bytes / (ms * 1e-3) / 1e9,
+        "alg_bytes_per_call": alg_bytes, "path": lib.bnb_int8_linear_path(T, N, K),
+        "gpu_launches": int(steps * R * launches_per_graph),
+        "launches_per_call": launches_per_graph / layers,
+        "clocks": sampler.summary(),
+        "l2_bytes": l2,
+    }
     peaks, peak_src = load_peaks()
-    if path == 1:
-        roof = {"bound": "hbm", "achieved": kb / kavg_s / 1e9, "peak": peaks["hbm_gbs"],
-                "unit": "GB/s"}
-    else:
-        roof = {"bound": "tensor", "achieved": kf / kavg_s / 1e12,
-                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s"}
-    roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = (args.traffic if args.traffic is not None
-                       else None if args.bias or args.wq_only or args.bf16
-                       else measured_traffic(kname, T, K, N))
-    roof["kernel"] = kname
-    roof["peak_source"] = ("measured (MEASURED_PEAKS.json)" if peak_src == "measured"
-                           else "fallback")
-    roof["kernel_avg_us"] = kavg_s * 1e6
-    roof["alg_bytes_per_launch"] = kb
-    roof["timing"] = f"graph of {Gk * layers} {kname} launches x {reps} replays, CUDA events"
+    if with_kernel:
+        # the dominant kernel alone: graphs of main-kernel-only calls (the GEMM
+        # on the activation-pass results the calls above left in the workspace,
+        # or the whole fused decode kernel), in the chain (programmatic
+        # dependent launch on, as the library runs) and, for decode, also with
+        # no overlap between consecutive launches
+        path = out["path"]
+        kname = {1: "dec_fused", 2: "gemm_tc", 3: "gemm_mma"}[path]
+        kb, kf = kernel_algorithmic(kname, T, N, K, nO, args.bias, args.wq_only)
+        res = {}
+        for tag, opts in (("chain", binding.OPT_MAIN_ONLY),
+                          ("alone", binding.OPT_MAIN_ONLY | binding.OPT_NO_PDL)):
+            if tag == "alone" and path != 1:
+                continue
+            gk = _graph(lambda: calls(opts), stream)
+            with torch.cuda.stream(stream):
+                gk.replay()
+            torch.cuda.synchronize()
+            pk = _time_replays(gk, 3, stream, world=world, dev=dev) / 3
+            Rk = max(3, math.ceil(min(args.kernel_timed_s, 2.0) * 1e3 / pk))
+            kms = _time_replays(gk, Rk, stream, world=world, dev=dev)
+            res[tag] = (kms * 1e-3 / (Rk * layers), Rk)
+        kavg_s, Rk = res["chain"]
+        if path == 1:
+            roof = {"bound": "hbm", "achieved": kb / kavg_s / 1e9, "peak": peaks["hbm_gbs"],
+                    "unit": "GB/s"}
+        else:
+            # timed over a loop of about a second: the sustained figure is the
+            # denominator; the burst one is reported beside it
+            roof = {"bound": "tensor", "achieved": kf / kavg_s / 1e12,
+                    "peak": peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]),
+                    "unit": "TFLOP/s",
+                    "peak_burst": peaks["bf16_tflops"],
+                    "frac_of_burst": kf / kavg_s / 1e12 / peaks["bf16_tflops"]}
+        roof["frac"] = roof["achieved"] / roof["peak"]
+        roof["traffic"] = (args.traffic if args.traffic is not None
+                           else None if args.bias or args.wq_only or args.bf16
+                           else measured_traffic(kname, T, K, N))
+        roof["kernel"] = kname
+        roof["peak_source"] = ("measured (MEASURED_PEAKS.json)" if peak_src == "measured"
+                               else "fallback")
+        roof["kernel_avg_us"] = kavg_s * 1e6
+        roof["alg_bytes_per_launch"] = kb
+        roof["alg_flops_per_launch"] = kf
+        roof["timing"] = (f"graph of {layers} main-kernel-only calls x {Rk} replays "
+                          f"(programmatic dependent launch on), CUDA events")
+        if "alone" in res:
+            a_s = res["alone"][0]
+            roof["alone_us"] = a_s * 1e6
+            roof["alone_frac"] = kb / a_s / 1e9 / peaks["hbm_gbs"]
+        if path != 1:
+            # the activation pass (workspace clear, column scan, row pass) alone
+            ga = _graph(lambda: calls(binding.OPT_ACT_ONLY), stream)
+            with torch.cuda.stream(stream):
+                ga.replay()
+            torch.cuda.synchronize()
+            pa = _time_replays(ga, 3, stream, world=world, dev=dev) / 3
+            Ra = max(3, math.ceil(0.3e3 / pa))
+            ams = _time_replays(ga, Ra, stream, world=world, dev=dev)
+            a_us = ams * 1e3 / (Ra * layers)
+            roof["act_pass_us"] = a_us
+            roof["act_pass_gbs"] = (4 * T * K + 2 * T * K) / (a_us * 1e-6) / 1e9
+        out["roofline"] = roof
 
-    # per-kernel breakdown of whole calls: eager, event-bracketed (includes
-    # launch gaps and loses the programmatic-launch overlap; shares only)
-    binding.profile_enable(1)
-    with torch.cuda.stream(stream):
-        for _ in range(max(1, min(args.steps, 2000 // layers))):
-            step(stream)
-    stream.synchronize()
-    binding.profile_enable(0)
-    prof = binding.profile_collect()
+    if with_e2e:
+        # e2e through the public API with host buffers: bnb_int8_linear_from_host
+        # (pinned H2D of X, the layer, D2H of Y in one call), calls alternating
+        # over two streams, each with its own device buffers and workspace
+        streams2 = [stream, torch.cuda.Stream(device=dev)]
+        Xpin = [Xh.pin_memory(), Xh.pin_memory()]
+        Ypin = [torch.empty((T, N), dtype=edt).pin_memory() for _ in range(2)]
+        Xdev = [Xs[0], torch.empty_like(Xs[0])]
+        Ydev = [Ys[0], torch.empty_like(Ys[0])]
+        wss = [ws, torch.empty_like(ws)]
 
-    # e2e through the public API with host buffers: bnb_int8_linear_from_host
-    # (pinned H2D of X, the layer, D2H of Y in one call), calls alternating
-    # over two streams, each with its own device buffers and workspace, so
-    # that one call's copies overlap its neighbour's kernel
+        def e2e_call(i):
+            j = i % 2
+            binding.linear_from_host(Xpin[j], Wqs[i % layers], sws[i % layers], W16s[i % layers],
+                                     tau, Ypin[j], Xdev[j], Ydev[j], wss[j], stream=streams2[j],
+                                     bias=Bs[i % layers])
+
+        def e2e_run(n):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            eb = torch.cuda.Event()
+            torch.cuda.synchronize()
+            barrier(world)
+            e0.record(streams2[0])
+            streams2[1].wait_event(e0)
+            for i in range(n):
+                e2e_call(i)
+            eb.record(streams2[1])
+            streams2[0].wait_event(eb)
+            e1.record(streams2[0])
+            torch.cuda.synchronize()
+            return max_over_ranks(e0.elapsed_time(e1), world, dev)
+
+        warm = e2e_run(max(2, args.e2e_warmup))  # also the estimate of a call's time
+        per_call_ms = warm / max(2, args.e2e_warmup)
+        n = int(min(args.e2e_calls, max(50, math.ceil(args.e2e_timed_s * 1e3 / per_call_ms))))
+        e2e_ms = e2e_run(n)
+        xb, yb = 2 * T * K, 2 * T * N
+        out["e2e"] = {"value": world * n * ops / (e2e_ms * 1e-3) / 1e12, "unit": "TOPS",
+                      "h2d_bytes_per_step": xb * R * layers, "d2h_bytes_per_step": yb * R * layers,
+                      "calls": n, "warmup_calls": max(2, args.e2e_warmup),
+                      "us_per_call": e2e_ms * 1e3 / n,
+                      "note": "a step is the same calls_per_step calls; each call is "
+                              "bnb_int8_linear_from_host (pinned H2D of X, the layer, D2H of Y); "
+                              "calls alternate over two streams with their own device buffers "
+                              "and workspaces"}
+    del Xs, Ys, Wqs, W16s, ws
+    torch.cuda.empty_cache()
+    return out
+
+
+def run_ours(args, world, rank, local):
     import torch
-    streams2 = [stream, torch.cuda.Stream(device=dev)]
-    Xpin = [Xh.pin_memory(), Xh.pin_memory()]
-    Ypin = [torch.empty((T, N), dtype=edt).pin_memory() for _ in range(2)]
-    Xdev = [Xs[0], torch.empty_like(Xs[0])]
-    Ydev = [Ys[0], torch.empty_like(Ys[0])]
-    wss = [ws, torch.empty_like(ws)]
-    e2e_calls = min(calls, args.e2e_calls)
 
-    def e2e_call(i):
-        j = i % 2
-        binding.linear_from_host(Xpin[j], Wqs[i % layers], sws[i % layers], W16s[i % layers], tau,
-                                 Ypin[j], Xdev[j], Ydev[j], wss[j], stream=streams2[j],
-                                 bias=Bs[i % layers])
+    from int8_mixed_precision_04_b300 import binding, build
+    build.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    binding.load()
 
-    for i in range(min(10, e2e_calls)):
-        e2e_call(i)
-    torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    eb = torch.cuda.Event()
-    barrier(world)
-    e0.record(streams2[0])
-    streams2[1].wait_event(e0)
-    for i in range(e2e_calls):
-        e2e_call(i)
-    eb.record(streams2[1])
-    streams2[0].wait_event(eb)
-    e1.record(streams2[0])
-    torch.cuda.synchronize()
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
-    e2e_val = world * e2e_calls * ops / (e2e_ms * 1e-3) / 1e12
-
+    w = make_workload(args.workload, args.T)
+    main = measure_layer(args, w, dev, world, local, args.steps, args.min_timed_s,
+                         min_layers=16 if args.workload == "decode" else 2)
+    T, K, N, tau = w.T, w.K, w.N, w.tau
+    form = "bf16" if args.bf16 else "fp16"
     line = {
         "metric": METRIC,
-        "value": value,
+        "value": main["value"],
         "unit": "TOPS",
         "n_gpus": world,
         "steps": args.steps,
         "warmup": args.warmup,
-        "ms_per_step": ms / args.steps,
+        "ms_per_step": main["ms_per_step"],
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
@@ -464,30 +520,41 @@ def run_ours(args, world, rank, local):
                   else "int8xint8->int32 + fp16 outliers, fp16 out"),
         "data": "synthetic (seeded, inputs module)",
         "config": {
-            "workload": (f"{args.workload}: X {'bf16' if args.bf16 else 'fp16'} [{T},{K}], "
-                         f"W {'bf16' if args.bf16 else 'fp16'} [{N},{K}], tau {tau}"),
-            "T": T, "K": K, "N": N, "tau": tau, "n_outliers": nO, "bias": bool(args.bias),
-            "fp16_weight_resident": not args.wq_only,
-            "layers_per_step": layers,
-            "l2": f"inputs larger than L2: {layers} distinct layers per step "
-                  f"({layers * (wq_bytes + 2 * T * K) / 1e6:.0f} MB of int8 weights and fp16 "
-                  f"activations) vs 126 MB L2",
-            "timing": "CUDA graph replay of captured library calls, CUDA events",
+            "workload": f"{args.workload}: X {form} [{T},{K}], W {form} [{N},{K}], tau {tau}",
+            "T": T, "K": K, "N": N, "tau": tau, "n_outliers": main["n_outliers"],
+            "bias": bool(args.bias), "fp16_weight_resident": not args.wq_only,
+            "layers": main["layers"], "calls_per_step": main["calls_per_step"],
+            "l2": (f"inputs larger than L2: {main['layers']} distinct layers cycled "
+                   f"({main['layers'] * (N * K + 2 * T * K) / 1e6:.0f} MB of int8 weights and "
+                   f"16-bit activations) vs {main['l2_bytes'] / 2**20:.0f} MiB L2"),
+            "timing": (f"CUDA graph of {main['layers']} library calls replayed "
+                       f"{main['graph_replays_per_step']} times per step; CUDA events; "
+                       f"timed region {main['timed_s']:.2f} s"),
             "parallelism": f"replicas x{world}",
-            "path": lib.bnb_int8_linear_path(T, N, K),
+            "path": main["path"],
         },
-        "gb_per_s": gbs,
-        "alg_bytes_per_call": alg_bytes,
-        "e2e": {"value": e2e_val, "unit": "TOPS", "h2d_bytes_per_step": 2 * T * K,
-                "d2h_bytes_per_step": 2 * T * N, "calls": e2e_calls,
-                "note": "per call: bnb_int8_linear_from_host (pinned H2D of X, the layer, D2H of Y), calls alternating over two streams with their own device buffers and workspaces"},
-        "gpu_launches": int(round(launches_per_step * args.steps)),
-        "launches_per_step": launches_per_step,
-        "roofline": roof,
-        "kernels_eager_events": {k: {"avg_us": v[0] / v[1] * 1e3, "launches": v[1]}
-                                 for k, v in prof.items()},
-        "clocks": sampler.summary(),
+        "us_per_call": main["us_per_call"],
+        "gb_per_s": main["gb_per_s"],
+        "alg_bytes_per_call": main["alg_bytes_per_call"],
+        "e2e": main["e2e"],
+        "gpu_launches": main["gpu_launches"],
+        "launches_per_call": main["launches_per_call"],
+        "roofline": main["roofline"],
+        "clocks": main["clocks"],
     }
+    # the other regimes of the layer, measured the same way in the same run
+    subs = {}
+    for name in [s for s in args.sub.split(",") if s and s != args.workload]:
+        ws_ = make_workload(name, args.T)
+        r = measure_layer(args, ws_, dev, world, local, args.steps, args.sub_timed_s,
+                          min_layers=16 if name.startswith("decode") else 2, with_e2e=False)
+        subs[name] = {"workload": f"X [{ws_.T},{ws_.K}], W [{ws_.N},{ws_.K}], tau {ws_.tau}",
+                      "value_tops": r["value"], "us_per_call": r["us_per_call"],
+                      "gb_per_s": r["gb_per_s"], "path": r["path"], "layers": r["layers"],
+                      "calls_timed": args.steps * r["calls_per_step"],
+                      "roofline": r["roofline"], "clocks": r["clocks"]}
+    if subs:
+        line["other_regimes"] = subs
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_budget, **_forms(args))
     return line
@@ -774,14 +841,24 @@ def run_reference_blockwise(args, world, rank, local):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10000)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="decode",
-                    choices=["decode", "prefill", "large", "sweep", "tiny", "blockwise"])
-    ap.add_argument("--T", type=int, default=16, help="tokens of the decode workload")
+    ap.add_argument("--workload", default="large",
+                    choices=["decode", "decode_k8192", "decode_n11008", "prefill", "large",
+                             "sweep", "tiny", "blockwise"])
+    ap.add_argument("--T", type=int, default=16, help="tokens of the decode workloads")
     ap.add_argument("--max-layers", type=int, default=64)
+    ap.add_argument("--min-timed-s", type=float, default=1.2,
+                    help="the timed region lasts at least this long (graph replays per step)")
+    ap.add_argument("--kernel-timed-s", type=float, default=1.0,
+                    help="length of the dominant-kernel timing loop")
+    ap.add_argument("--sub", default="decode,decode_k8192,prefill",
+                    help="other regimes measured in the same run (comma list, '' for none)")
+    ap.add_argument("--sub-timed-s", type=float, default=0.5)
     ap.add_argument("--e2e-calls", type=int, default=2000)
+    ap.add_argument("--e2e-warmup", type=int, default=100)
+    ap.add_argument("--e2e-timed-s", type=float, default=2.0)
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--ref-budget", type=float, default=120.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")

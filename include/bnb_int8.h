@@ -277,7 +277,10 @@ bnb_status_t bnb_last_device_status(const void *workspace, void *stream, int32_t
  *   anything is enqueued (at K = N = 4096 that admits T up to 382).
  *   The first call on a device looks up the array's device address with
  *   that device current (cudaGetSymbolAddress) and caches it; make that first
- *   call before any stream capture.  BNB_ERR_CUDA if the lookup fails.
+ *   call before any stream capture.  BNB_ERR_CUDA if the lookup fails.  The
+ *   cache assumes that the device's primary context lives as long as the
+ *   process uses this entry point: after cudaDeviceReset the cached address
+ *   is stale, so do not call this entry point again after a reset.
  *   Every call, on every stream, shares the one array and leaves its contents
  *   behind; each call clears on the device what must start at zero.  Calls
  *   that may overlap on the GPU (different streams, or concurrent host
@@ -300,40 +303,60 @@ const char *bnb_status_string(bnb_status_t s);
 uint64_t bnb_launch_count(void);
 
 /*
- * Which kernel path bnb_int8_linear takes for a shape on the current device:
- * 1 = decode (T <= 16, K <= 4096 and N within what the decode kernel's
- * resident CTAs hold at up to 40 output channels each: 4620 at K = 4096 on
- * B300), 2 = tensor-core GEMM (tcgen05), 3 = warp-level mma GEMM.
+ * Which kernel path bnb_int8_linear takes for a shape: 1 = decode (T <= 16 and
+ * K <= 8192, any N: one kernel per call, K split across a thread-block
+ * cluster), 2 = tensor-core GEMM (tcgen05), 3 = warp-level mma GEMM (only
+ * through bnb_int8_linear_opts with BNB_OPT_LEGACY_MMA).
  */
 int bnb_int8_linear_path(int64_t T, int64_t N, int64_t K);
 
 /*
- * Profiling aids (off by default; for benchmarks, not for production calls).
- *   bnb_profile_enable(1)  per-kernel timing: every launch the library
- *                          enqueues is bracketed by two CUDA events recorded
- *                          on the launch's stream (events are created on
- *                          demand and reused; no device memory is allocated).
- *                          Do not use while a stream is being captured.
- *   bnb_profile_enable(2)  main-kernel-only mode: bnb_int8_linear enqueues
- *                          only the main kernel of its path (the decode GEMV
- *                          or the GEMM), reusing the activation-pass results
- *                          that the previous full call on the same workspace
- *                          left there.  Its result is correct only if that
- *                          call had the same X and tau.  Used to time the
- *                          dominant kernel alone.
- *   bnb_profile_enable(0)  back to normal operation.
- *   bnb_profile_collect(ms, n)  waits for the recorded events, adds each
- *                               kernel's summed duration (ms) and launch count
- *                               into ms[id] and n[id] for id in
- *                               [0, bnb_profile_kernel_count()), then forgets
- *                               the records.  Returns BNB_ERR_CUDA if an event
- *                               query failed.
- *   bnb_profile_kernel_name(id) static name of kernel id (NULL if out of range).
+ * Per-call options for benchmarks and tests: bnb_int8_linear_opts is
+ * bnb_int8_linear_debug_ex with a set of flags that change only that call.
+ * The library keeps no switch of its own, so no option can change another
+ * caller's results.
+ *   BNB_OPT_MAIN_ONLY   enqueue only the main kernel of the path (the decode
+ *                       kernel, or the GEMM on the activation-pass results
+ *                       that the previous full call on the same workspace
+ *                       left there).  Y is correct only if that call had the
+ *                       same X and tau; the decode kernel recomputes its
+ *                       activation pass and is unaffected.  For timing the
+ *                       dominant kernel alone.
+ *   BNB_OPT_ACT_ONLY    T > 16 path: enqueue only the activation pass (the
+ *                       workspace clear, the column scan and the row pass);
+ *                       Y is not written.
+ *   BNB_OPT_NO_PDL      launch without programmatic dependent launch, so the
+ *                       call's kernels start only after the stream's previous
+ *                       work has completed.
+ *   BNB_OPT_LEGACY_MMA  T > 16 path: the warp-level mma.sync GEMM (sm_80-style
+ *                       tensor path, for comparison) instead of tcgen05.
+ *   BNB_OPT_CLUSTER(c)  decode path: thread-block clusters of c CTAs (c <= 8)
+ *                       instead of the size the library picks, ceil(K / 1024),
+ *                       when c is at least that size (CTAs past K then hold
+ *                       no columns).
+ *   BNB_OPT_FORCE_TIMEOUT  one thread of the call's main kernel waits, with a
+ *                       limit of about 0.1 ms, on an mbarrier that nothing
+ *                       completes, and then takes the kernel's timeout path
+ *                       (BNB_ERR_TIMEOUT in the status word, Y unspecified).
+ *                       Every other wait keeps its normal limit, and every copy
+ *                       in flight lands before the kernel exits.  For testing
+ *                       the timeout path; the next call on the workspace runs
+ *                       normally.
+ * Errors as for bnb_int8_linear_debug_ex, plus BNB_ERR_INVALID_ARG for an
+ * unknown flag or cluster size.
  */
-void bnb_profile_enable(int mode);
-bnb_status_t bnb_profile_collect(double *ms, uint64_t *n);
-int bnb_profile_kernel_count(void);
-const char *bnb_profile_kernel_name(int id);
+#define BNB_OPT_MAIN_ONLY 0x1u
+#define BNB_OPT_ACT_ONLY 0x2u
+#define BNB_OPT_NO_PDL 0x4u
+#define BNB_OPT_LEGACY_MMA 0x8u
+#define BNB_OPT_FORCE_TIMEOUT 0x10u
+#define BNB_OPT_CLUSTER(c) ((uint32_t)(c) << 8)
+bnb_status_t bnb_int8_linear_opts(const void *X, int64_t T, int64_t K, const int8_t *Wq,
+                                  const float *Wscale, const void *W16, const void *bias,
+                                  int64_t N, float tau, int dtype, void *Y, void *workspace,
+                                  size_t workspace_bytes, void *stream, int8_t *Xq,
+                                  float *Xscale, int32_t *outlier_idx, int32_t *n_outliers,
+                                  int32_t *acc, uint32_t opts);
 
 #ifdef __cplusplus
 }

@@ -40,8 +40,7 @@ class Lib:
     SYMBOLS = ("bnb_int8_linear_workspace_bytes", "bnb_int8_quantize_weight",
                "bnb_int8_linear", "bnb_int8_linear_debug", "bnb_last_device_status",
                "bnb_status_string", "bnb_launch_count", "bnb_int8_linear_path",
-               "bnb_profile_enable", "bnb_profile_collect", "bnb_profile_kernel_count",
-               "bnb_profile_kernel_name", "bnb_int8_linear_noalloc",
+               "bnb_int8_linear_opts", "bnb_int8_linear_noalloc",
                "bnb_int8_linear_from_host", "bnb_int8_quantize_blockwise",
                "bnb_int8_dequantize_blockwise", "bnb_int8_linear_bias",
                "bnb_int8_linear_wq_only", "bnb_int8_quantize_weight_ex", "bnb_int8_linear_ex",
@@ -97,15 +96,8 @@ class Lib:
         L.bnb_launch_count.argtypes = []
         L.bnb_int8_linear_path.restype = ctypes.c_int
         L.bnb_int8_linear_path.argtypes = [_I64, _I64, _I64]
-        L.bnb_profile_enable.restype = None
-        L.bnb_profile_enable.argtypes = [ctypes.c_int]
-        L.bnb_profile_collect.restype = ctypes.c_int
-        L.bnb_profile_collect.argtypes = [ctypes.POINTER(ctypes.c_double),
-                                          ctypes.POINTER(ctypes.c_uint64)]
-        L.bnb_profile_kernel_count.restype = ctypes.c_int
-        L.bnb_profile_kernel_count.argtypes = []
-        L.bnb_profile_kernel_name.restype = ctypes.c_char_p
-        L.bnb_profile_kernel_name.argtypes = [ctypes.c_int]
+        L.bnb_int8_linear_opts.restype = ctypes.c_int
+        L.bnb_int8_linear_opts.argtypes = L.bnb_int8_linear_debug_ex.argtypes + [ctypes.c_uint32]
         self.c = L
 
     def __getattr__(self, name):
@@ -303,8 +295,14 @@ def dequantize_blockwise(codes, absmax, block: int = BLOCKWISE_DEFAULT, y=None, 
 
 def linear_noalloc(X, Wq, Wscale, W16, tau: float, Y=None, stream=None):
     """bnb_int8_linear_noalloc: as :func:`linear`, with the library's static
-    scratch array instead of a workspace (for callers that cannot allocate)."""
+    scratch array instead of a workspace (for callers that cannot allocate).
+    The C entry point is fp16 only: X, W16 and a given Y must be fp16."""
     import torch
+    for name, t in (("X", X), ("W16", W16), ("Y", Y)):
+        if t is not None and t.dtype != torch.float16:
+            raise TypeError(f"bnb_int8_linear_noalloc takes fp16 tensors, {name} is {t.dtype}")
+    if Wq.dtype != torch.int8 or Wscale.dtype != torch.float32:
+        raise TypeError("Wq must be int8 and Wscale float32")
     T, K = X.shape
     N = Wq.shape[0]
     if Y is None:
@@ -353,16 +351,47 @@ def linear_path(T: int, N: int, K: int) -> int:
     return load().bnb_int8_linear_path(T, N, K)
 
 
-def profile_enable(mode) -> None:
-    """0 off, 1 per-kernel event timing, 2 main-kernel-only launches."""
-    load().bnb_profile_enable(int(mode))
+# Flags of bnb_int8_linear_opts (include/bnb_int8.h): per-call options for
+# benchmarks and tests.
+OPT_MAIN_ONLY = 0x1
+OPT_ACT_ONLY = 0x2
+OPT_NO_PDL = 0x4
+OPT_LEGACY_MMA = 0x8
+OPT_FORCE_TIMEOUT = 0x10
 
 
-def profile_collect() -> dict:
-    """{kernel name: (total ms, launches)} recorded since the last collect."""
-    L = load()
-    n = L.bnb_profile_kernel_count()
-    ms = (ctypes.c_double * n)()
-    cnt = (ctypes.c_uint64 * n)()
-    _check(L.bnb_profile_collect(ms, cnt), "bnb_profile_collect")
-    return {L.bnb_profile_kernel_name(i).decode(): (ms[i], cnt[i]) for i in range(n) if cnt[i]}
+def OPT_CLUSTER(c: int) -> int:
+    return int(c) << 8
+
+
+def linear_opts(X, Wq, Wscale, W16, tau: float, opts: int, bias=None, Y=None, workspace=None,
+                stream=None, debug: bool = False, want_acc: bool = True):
+    """bnb_int8_linear_opts: the layer with per-call options (``OPT_*``).
+    With ``debug`` the intermediates are exported as in :func:`linear_debug`
+    and a dict is returned; otherwise Y."""
+    import torch
+    T, K = X.shape
+    N = Wq.shape[0]
+    dev = X.device
+    if Y is None:
+        Y = torch.empty((T, N), dtype=X.dtype, device=dev)
+    if workspace is None:
+        workspace = _alloc_ws(T, N, K, dev)
+    d = {}
+    if debug:
+        d = {"Xq": torch.empty((T, K), dtype=torch.int8, device=dev),
+             "sx": torch.empty((T,), dtype=torch.float32, device=dev),
+             "O": torch.empty((K,), dtype=torch.int32, device=dev),
+             "nO": torch.empty((1,), dtype=torch.int32, device=dev),
+             "acc": torch.empty((T, N), dtype=torch.int32, device=dev) if want_acc else None}
+    rc = load().bnb_int8_linear_opts(_ptr(X), T, K, _ptr(Wq), _ptr(Wscale), _ptr(W16), _ptr(bias),
+                                     N, float(tau), _dtype_code(X), _ptr(Y), _ptr(workspace),
+                                     workspace.numel(), _stream(stream), _ptr(d.get("Xq")),
+                                     _ptr(d.get("sx")), _ptr(d.get("O")), _ptr(d.get("nO")),
+                                     _ptr(d.get("acc")), ctypes.c_uint32(int(opts)))
+    _check(rc, "bnb_int8_linear_opts")
+    if debug:
+        d["Y"] = Y
+        d["workspace"] = workspace
+        return d
+    return Y

@@ -322,12 +322,9 @@ cudaError_t launch_act_pass(const void *X, int64_t T, int64_t K, uint32_t thr_bi
   if (rows_per_block < 32) rows_per_block = 32;
   const int64_t row_blocks = (T + rows_per_block - 1) / rows_per_block;
   dim3 grid((unsigned)slabs, (unsigned)row_blocks);
-  {
-    ProfScope ps(kKidOutlierScan, stream);
-    outlier_scan_kernel<<<grid, kScanThreads, 0, stream>>>(
-        reinterpret_cast<const uint4 *>(X), T, K, thr_bits, rows_per_block, ws.colmask,
-        ws.counters, ws.O);
-  }
+  outlier_scan_kernel<<<grid, kScanThreads, 0, stream>>>(
+      reinterpret_cast<const uint4 *>(X), T, K, thr_bits, rows_per_block, ws.colmask,
+      ws.counters, ws.O);
   note_launch();
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
@@ -356,7 +353,6 @@ cudaError_t launch_act_pass(const void *X, int64_t T, int64_t K, uint32_t thr_bi
     const int64_t gb = (N + 7) / 8 < 8LL * num_sms ? (N + 7) / 8 : 8LL * num_sms;
     if (gb > qblocks) qblocks = gb;
   }
-  ProfScope ps(kKidQuantRows, stream);
   auto *kern = code_mode == 0 ? (bf16 ? quantize_rows_kernel<0, true> : quantize_rows_kernel<0, false>)
                               : (bf16 ? quantize_rows_kernel<1, true> : quantize_rows_kernel<1, false>);
   kern<<<(unsigned)qblocks, kQuantThreads, 0, stream>>>(a);

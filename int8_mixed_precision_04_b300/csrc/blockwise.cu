@@ -148,7 +148,6 @@ static int64_t bw_grid(int64_t n, int num_sms) {
 
 cudaError_t launch_quantize_blockwise(const float *x, int64_t n, int B, int8_t *codes,
                                       float *absmax, int num_sms, cudaStream_t stream) {
-  ProfScope ps(kKidQuantBlockwise, stream);
   quantize_blockwise_kernel<<<(unsigned)bw_grid(n, num_sms), kBwThreads, 0, stream>>>(
       x, n, B, codes, absmax);
   note_launch();
@@ -157,7 +156,6 @@ cudaError_t launch_quantize_blockwise(const float *x, int64_t n, int B, int8_t *
 
 cudaError_t launch_dequantize_blockwise(const int8_t *codes, const float *absmax, int64_t n,
                                         int B, float *y, int num_sms, cudaStream_t stream) {
-  ProfScope ps(kKidDequantBlockwise, stream);
   dequantize_blockwise_kernel<<<(unsigned)bw_grid(n, num_sms), kBwThreads, 0, stream>>>(
       codes, absmax, n, B, y);
   note_launch();

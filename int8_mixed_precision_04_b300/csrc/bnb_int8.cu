@@ -135,21 +135,12 @@ static bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
   return x < y + nb && y < x + na;
 }
 
-// Environment override BNB_GEMM=mma selects the legacy warp-level GEMM for
-// shapes that would take the tcgen05 GEMM (for side-by-side measurement).
-static bool force_mma() {
-  static const bool v = [] {
-    const char *e = std::getenv("BNB_GEMM");
-    return e != nullptr && std::strcmp(e, "mma") == 0;
-  }();
-  return v;
-}
-
-// 1: decode (T <= 16, K <= kDecodeMaxK, N within what the resident decode
-// CTAs hold in one wave); 2: tcgen05 GEMM; 3: legacy mma GEMM.
-static int choose_path(int64_t T, int64_t N, int64_t K, int dev) {
-  if (T <= 16 && K <= kDecodeMaxK && N <= decode_max_n(dev, K)) return 1;
-  return force_mma() ? 3 : 2;
+// 1: decode (T <= 16, K <= kDecodeMaxK, any N); 2: tcgen05 GEMM; 3: legacy
+// mma GEMM (only when a call's options ask for it).
+static int choose_path(int64_t T, int64_t N, int64_t K, uint32_t opts = 0) {
+  (void)N;
+  if (T <= 16 && K <= kDecodeMaxK) return 1;
+  return (opts & BNB_OPT_LEGACY_MMA) ? 3 : 2;
 }
 
 // The argument checks of bnb_int8_linear (nothing is enqueued).  W16 may be
@@ -181,7 +172,8 @@ static bnb_status_t linear_impl(const void *X, int64_t T, int64_t K, const int8_
                                 int64_t N, float tau, bool bf16, void *Y, void *workspace,
                                 size_t workspace_bytes,
                                 void *stream_v, int8_t *dbg_xq, float *dbg_sx,
-                                int32_t *dbg_O, int32_t *dbg_nO, int32_t *dbg_acc) {
+                                int32_t *dbg_O, int32_t *dbg_nO, int32_t *dbg_acc,
+                                uint32_t opts = 0) {
   // (the entry points check W16 themselves: null means the int8 weight alone)
   bnb_status_t chk = linear_check(X, T, K, Wq, Wscale, W16, N, tau, Y, workspace, workspace_bytes,
                                   /*w16_optional=*/true);
@@ -195,24 +187,22 @@ static bnb_status_t linear_impl(const void *X, int64_t T, int64_t K, const int8_
   if (st != BNB_OK) return st;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_v);
   const Workspace ws = carve(workspace, T, N, K);
-  const int path = choose_path(T, N, K, dev);
+  const int path = choose_path(T, N, K, opts);
   const uint32_t thr = threshold_bits(tau, bf16);
   cudaError_t e;
   if (path == 1) {
-    // decode: no memset, the act-pass kernel clears the status word
-    e = launch_decode(X, T, K, thr, Wq, Wscale, W16, bias, N, bf16, Y, ws, dbg_xq, dbg_acc,
-                      stream);
-    if (e != cudaSuccess) return BNB_ERR_CUDA;
+    // decode: no memset, the kernel clears the status word itself
+    if (!(opts & BNB_OPT_ACT_ONLY)) {
+      e = launch_decode(X, T, K, thr, Wq, Wscale, W16, bias, N, bf16, Y, ws, dbg_xq, dbg_acc,
+                        opts, stream);
+      if (e != cudaSuccess) return BNB_ERR_CUDA;
+    }
   } else {
-    if (!profile_only_main()) {
+    if (!(opts & BNB_OPT_MAIN_ONLY)) {
       // status word, counters and the outlier column mask are contiguous and
       // zeroed by every call with one memset
       const size_t zero_bytes = 512 + (size_t)((K + 255) / 256) * 8 * 4;
-      {
-        ProfScope ps(kKidMemset, stream);
-        if (cudaMemsetAsync(ws.status, 0, zero_bytes, stream) != cudaSuccess)
-          return BNB_ERR_CUDA;
-      }
+      if (cudaMemsetAsync(ws.status, 0, zero_bytes, stream) != cudaSuccess) return BNB_ERR_CUDA;
       note_launch();
       // the tcgen05 GEMM reads fp16 integer codes, the mma GEMM int8 codes
       // (for the tcgen05 GEMM the same launch compacts W16 at a sparse outlier set)
@@ -220,12 +210,14 @@ static bnb_status_t linear_impl(const void *X, int64_t T, int64_t K, const int8_
                           W16, Wq, N, bf16, dbg_xq, device_sms(dev), stream);
       if (e != cudaSuccess) return BNB_ERR_CUDA;
     }
-    if (path == 2)
-      e = launch_gemm_tc(T, K, Wq, Wscale, W16, bias, N, bf16, Y, ws, dbg_acc, device_sms(dev),
-                         stream);
-    else
-      e = launch_gemm_mma(T, K, Wq, Wscale, W16, bias, N, bf16, Y, ws, dbg_acc, stream);
-    if (e != cudaSuccess) return BNB_ERR_CUDA;
+    if (!(opts & BNB_OPT_ACT_ONLY)) {
+      if (path == 2)
+        e = launch_gemm_tc(T, K, Wq, Wscale, W16, bias, N, bf16, Y, ws, dbg_acc, device_sms(dev),
+                           opts, stream);
+      else
+        e = launch_gemm_mma(T, K, Wq, Wscale, W16, bias, N, bf16, Y, ws, dbg_acc, stream);
+      if (e != cudaSuccess) return BNB_ERR_CUDA;
+    }
   }
   if (dbg_sx && cudaMemcpyAsync(dbg_sx, ws.sx, (size_t)T * 4, cudaMemcpyDeviceToDevice, stream) != cudaSuccess)
     return BNB_ERR_CUDA;
@@ -414,6 +406,24 @@ bnb_status_t bnb_int8_linear_debug_ex(const void *X, int64_t T, int64_t K, const
                      workspace, workspace_bytes, stream, Xq, Xscale, outlier_idx, n_outliers, acc);
 }
 
+bnb_status_t bnb_int8_linear_opts(const void *X, int64_t T, int64_t K, const int8_t *Wq,
+                                  const float *Wscale, const void *W16, const void *bias,
+                                  int64_t N, float tau, int dtype, void *Y, void *workspace,
+                                  size_t workspace_bytes, void *stream, int8_t *Xq,
+                                  float *Xscale, int32_t *outlier_idx, int32_t *n_outliers,
+                                  int32_t *acc, uint32_t opts) {
+  if (dtype != BNB_DTYPE_FP16 && dtype != BNB_DTYPE_BF16) return BNB_ERR_INVALID_ARG;
+  constexpr uint32_t kKnown = BNB_OPT_MAIN_ONLY | BNB_OPT_ACT_ONLY | BNB_OPT_NO_PDL |
+                              BNB_OPT_LEGACY_MMA | BNB_OPT_FORCE_TIMEOUT | BNB_OPT_CLUSTER(0xff);
+  if (opts & ~kKnown) return BNB_ERR_INVALID_ARG;
+  const uint32_t c = (opts >> 8) & 0xffu;
+  if (c > 8) return BNB_ERR_INVALID_ARG;
+  if ((opts & BNB_OPT_MAIN_ONLY) && (opts & BNB_OPT_ACT_ONLY)) return BNB_ERR_INVALID_ARG;
+  return linear_impl(X, T, K, Wq, Wscale, W16, bias, N, tau, dtype == BNB_DTYPE_BF16, Y,
+                     workspace, workspace_bytes, stream, Xq, Xscale, outlier_idx, n_outliers, acc,
+                     opts);
+}
+
 bnb_status_t bnb_last_device_status(const void *workspace, void *stream, int32_t *out) {
   if (!workspace || !out) return BNB_ERR_INVALID_ARG;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -441,9 +451,7 @@ uint64_t bnb_launch_count(void) { return g_launches.load(std::memory_order_relax
 
 int bnb_int8_linear_path(int64_t T, int64_t N, int64_t K) {
   if (T <= 0 || N <= 0 || K <= 0) return 0;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) dev = -1;
-  return choose_path(T, N, K, dev);
+  return choose_path(T, N, K);
 }
 
 }  // extern "C"

@@ -18,10 +18,9 @@ constexpr int32_t kDevTimeout = BNB_ERR_TIMEOUT;
 // device attribute, this is only a default for host-side heuristics.
 constexpr int kB300Sms = 148;
 
-// Largest K of the decode path: 32 weight rows and 16 code rows of K + 64
-// bytes plus the outlier list fit in 227 KB, and the activation pass gives
-// each of 16 warps x 32 lanes one 8-column vector.
-constexpr int64_t kDecodeMaxK = 4096;
+// Largest K of the decode path (T <= 16): a cluster of at most 8 CTAs splits
+// K in ranges of 1024 columns.
+constexpr int64_t kDecodeMaxK = 8192;
 
 // The fp16 outlier block of the GEMM path is dense (X masked to the outlier
 // columns over all K, multiplied as one dense fp16 GEMM against W16 tiles)

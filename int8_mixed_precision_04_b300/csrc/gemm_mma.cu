@@ -200,7 +200,6 @@ cudaError_t launch_gemm_mma(int64_t T, int64_t K, const int8_t *Wq, const float 
                             const void *W16, const void *bias, int64_t N, bool bf16, void *Y,
                             const Workspace &ws, int32_t *dbg_acc, cudaStream_t stream) {
   dim3 grid((unsigned)((N + kMmaBN - 1) / kMmaBN), (unsigned)((T + kMmaBM - 1) / kMmaBM));
-  ProfScope ps(kKidGemmMma, stream);
   (bf16 ? gemm_mma_kernel<true> : gemm_mma_kernel<false>)<<<grid, kMmaThreads, 0, stream>>>(
       T, K, Wq, sw, reinterpret_cast<const unsigned short *>(W16), N,
       reinterpret_cast<uint16_t *>(Y), reinterpret_cast<const int8_t *>(ws.xcodes), ws.sx, ws.O,

@@ -123,6 +123,7 @@ struct TcArgs {
   const uint32_t *nO;
   int32_t *dbg_acc;
   int32_t *status;
+  int force_timeout;  // test option: the first epilogue warp waits on `never` and gives up
 };
 
 struct TcSmem {
@@ -133,6 +134,7 @@ struct TcSmem {
   uint64_t acce[2];         // epilogue finished reading buffer b
   uint64_t fin;             // MMA warp's own completion fence at exit
   uint64_t done;            // every epilogue warp has finished with tensor memory
+  uint64_t never;           // completed by nothing (forced-timeout test option)
   uint32_t tmem_base;
   int abort;
 };
@@ -256,6 +258,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(&sm.fin, 1);
     mbar_init(&sm.done, kEpiWarps);
+    mbar_init(&sm.never, 1);
     sm.abort = 0;
     mbar_init_fence();
   }
@@ -389,6 +392,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int nci = (s_int + kChunkStages - 1) / kChunkStages;
     uint32_t g = 0;
     bool ok = true;
+    if (p.force_timeout && e == 0) {
+      // forced-timeout test option: a wait that nothing completes gives up,
+      // raises the abort flag and records BNB_ERR_TIMEOUT; every role then
+      // leaves through its own timeout path
+      ok = __all_sync(0xffffffffu, mbar_wait_abortable(&sm.never, 0, &sm.abort, p.status,
+                                                        kForcedWaitNs));
+    }
     for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
       const int64_t t0 = (int64_t)(tile % p.t_tiles) * kBN + part * kEpiCols;
       const int64_t n = (int64_t)(tile / p.t_tiles) * kBM + 32 * quad + lane;
@@ -494,8 +504,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 cudaError_t launch_gemm_tc(int64_t T, int64_t K, const int8_t *Wq, const float *sw,
                            const void *W16, const void *bias, int64_t N, bool bf16, void *Y,
-                           const Workspace &ws,
-                           int32_t *dbg_acc, int num_sms, cudaStream_t stream) {
+                           const Workspace &ws, int32_t *dbg_acc, int num_sms, uint32_t opts,
+                           cudaStream_t stream) {
   static bool attr_set = false;  // benign race: every writer sets the same value
   if (!attr_set) {
     for (auto *f : {gemm_tc_kernel<false>, gemm_tc_kernel<true>}) {
@@ -542,6 +552,7 @@ cudaError_t launch_gemm_tc(int64_t T, int64_t K, const int8_t *Wq, const float *
   a.nO = ws.counters + 1;
   a.dbg_acc = dbg_acc;
   a.status = ws.status;
+  a.force_timeout = (opts & BNB_OPT_FORCE_TIMEOUT) ? 1 : 0;
   const int64_t tiles = (int64_t)a.t_tiles * a.n_tiles;
   const unsigned grid = (unsigned)(tiles < num_sms ? tiles : num_sms);
   cudaLaunchConfig_t cfg = {};
@@ -553,8 +564,7 @@ cudaError_t launch_gemm_tc(int64_t T, int64_t K, const int8_t *Wq, const float *
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  ProfScope ps(kKidGemmTc, stream);
+  cfg.numAttrs = (opts & BNB_OPT_NO_PDL) ? 0 : 1;
   const cudaError_t e = cudaLaunchKernelEx(&cfg, bf16 ? gemm_tc_kernel<true> : gemm_tc_kernel<false>,
                                            tm_x, tm_w, tm_xo, tm_w16, tm_w16o, a);
   note_launch();

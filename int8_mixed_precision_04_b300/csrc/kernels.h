@@ -19,39 +19,6 @@ bool encode_2d(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint64_
                uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
                CUtensorMapSwizzle swz, CUtensorMapL2promotion l2);
 
-// Kernel ids of the per-kernel event timing (names in profile.cu).
-enum KernelId {
-  kKidMemset = 0,
-  kKidOutlierScan,
-  kKidQuantRows,
-  kKidDecFused,
-  kKidGemmMma,
-  kKidGemmTc,
-  kKidQuantWeight,
-  kKidQuantBlockwise,
-  kKidDequantBlockwise,
-  kKernelCount
-};
-
-// Profiling mode 2: launch only the main (dominant) kernel of a path,
-// reusing the activation-pass results already in the workspace.
-bool profile_only_main();
-
-// Brackets one launch with two events when profiling mode 1 is enabled
-// (no-op otherwise).
-class ProfScope {
- public:
-  ProfScope(int kid, cudaStream_t s);
-  ~ProfScope();
-  ProfScope(const ProfScope &) = delete;
-  ProfScope &operator=(const ProfScope &) = delete;
-
- private:
-  int kid_;
-  cudaStream_t s_;
-  cudaEvent_t a_;
-};
-
 cudaError_t launch_quantize_weight(const void *W16, int64_t N, int64_t K, bool bf16, int8_t *Wq,
                                    float *sw, cudaStream_t stream);
 
@@ -69,21 +36,20 @@ cudaError_t launch_quantize_blockwise(const float *x, int64_t n, int B, int8_t *
 cudaError_t launch_dequantize_blockwise(const int8_t *codes, const float *absmax, int64_t n,
                                         int B, float *y, int num_sms, cudaStream_t stream);
 
-// The whole layer for T <= 16, K <= kDecodeMaxK, N <= decode_max_n(dev, K)
-// in one kernel (activation pass fused into the GEMV and shared by clusters
-// of CTAs), launched with programmatic dependent launch.
-int64_t decode_max_n(int dev, int64_t K);
+// The whole layer for T <= 16 and K <= kDecodeMaxK, any N, in one kernel (K
+// split across a thread-block cluster), launched with programmatic dependent
+// launch unless the call's options turn it off.
 cudaError_t launch_decode(const void *X, int64_t T, int64_t K, uint32_t thr, const int8_t *Wq,
                           const float *sw, const void *W16, const void *bias, int64_t N,
                           bool bf16, void *Y, const Workspace &ws, int8_t *dbg_xq,
-                          int32_t *dbg_acc, cudaStream_t stream);
+                          int32_t *dbg_acc, uint32_t opts, cudaStream_t stream);
 
 // S4..S6 on tcgen05 tensor cores (fp16 integer codes from the activation
 // pass, code_mode 1), persistent over 128 x 256 output tiles.
 cudaError_t launch_gemm_tc(int64_t T, int64_t K, const int8_t *Wq, const float *sw,
                            const void *W16, const void *bias, int64_t N, bool bf16, void *Y,
-                           const Workspace &ws,
-                           int32_t *dbg_acc, int num_sms, cudaStream_t stream);
+                           const Workspace &ws, int32_t *dbg_acc, int num_sms, uint32_t opts,
+                           cudaStream_t stream);
 
 // S4..S6 with warp-level mma.sync (legacy tensor path), int8 codes.
 cudaError_t launch_gemm_mma(int64_t T, int64_t K, const int8_t *Wq, const float *sw,

@@ -10,7 +10,9 @@
 // In host code the name g_scratch is only a host-side stand-in for the
 // array, not a device address.  The device address is looked up once per
 // device, with that device current, by cudaGetSymbolAddress, and cached; the
-// first call on a device does this set-up.
+// first call on a device does this set-up.  The cache is valid for the life
+// of the device's primary context: a cudaDeviceReset invalidates it (the
+// header tells callers not to use this entry point after one).
 #include <atomic>
 
 #include "common.cuh"

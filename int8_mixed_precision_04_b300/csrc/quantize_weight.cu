@@ -58,7 +58,6 @@ cudaError_t launch_quantize_weight(const void *W16, int64_t N, int64_t K, bool b
   const int warps_per_block = 8;
   int64_t blocks = (N + warps_per_block - 1) / warps_per_block;
   if (blocks > 148 * 64) blocks = 148 * 64;
-  ProfScope ps(kKidQuantWeight, stream);
   (bf16 ? quantize_weight_kernel<true> : quantize_weight_kernel<false>)
       <<<(unsigned)blocks, 32 * warps_per_block, 0, stream>>>(
       reinterpret_cast<const uint4 *>(W16), N, K, Wq, sw);

@@ -47,12 +47,13 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;  // every device-side wait give
 // Wait with a time limit; on expiry record a timeout in the workspace status
 // word and return false.  (Inlined: callers may run under different
 // setmaxnreg register budgets, which a shared out-of-line function cannot.)
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, int32_t *status) {
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, int32_t *status,
+                                                  uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 1;; it++) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 255u) == 0 && global_timer_ns() - t0 > kWaitLimitNs) {
+    if ((it & 255u) == 0 && global_timer_ns() - t0 > limit_ns) {
       atomicExch(status, kDevTimeout);
       return false;
     }
@@ -64,14 +65,15 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
 // timeout.  Lets every role of a warp-specialised kernel leave its loops
 // promptly once one of them has timed out.
 __device__ __forceinline__ bool mbar_wait_abortable(uint64_t *bar, uint32_t parity,
-                                                 volatile int *abort, int32_t *status) {
+                                                 volatile int *abort, int32_t *status,
+                                                 uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 1;; it++) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 127u) == 0) {
       if (*abort) return false;
-      if (global_timer_ns() - t0 > kWaitLimitNs) {
+      if (global_timer_ns() - t0 > limit_ns) {
         *abort = 1;
         atomicExch(status, kDevTimeout);
         return false;
@@ -79,6 +81,10 @@ __device__ __forceinline__ bool mbar_wait_abortable(uint64_t *bar, uint32_t pari
     }
   }
 }
+
+// The wait limit of the one wait that a forced-timeout call (test option)
+// makes on an mbarrier nothing completes.
+constexpr uint64_t kForcedWaitNs = 100000ull;
 
 // ---- bulk and tensor copies -------------------------------------------------
 

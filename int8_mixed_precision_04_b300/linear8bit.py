@@ -6,7 +6,14 @@ activations"): the weight is quantized row-wise once, at construction, and
 every forward call runs the mixed-precision decomposition (outlier columns of
 X with |x| >= threshold in fp16, the rest in 8 bits) in the CUDA library,
 bias included.  This class only keeps the tensors, reshapes the input to
-[T, K] and caches a workspace per row count; it computes nothing itself.
+[T, K] and caches a workspace per (row count, CUDA stream); it computes
+nothing itself.
+
+Concurrency: a call's workspace must not be shared with a call that may run
+at the same time on the GPU.  Forward calls on one stream are ordered, so
+they share one workspace; calls on different streams get different ones.
+The cache grows with the distinct (row count, stream) pairs seen; ``clear_
+workspaces()`` drops it.
 """
 
 from __future__ import annotations
@@ -49,7 +56,7 @@ class Linear8bitLt(torch.nn.Module):
         self.register_buffer("Wq", Wq)
         self.register_buffer("Wscale", sw)
         self.register_buffer("bias", None if bias is None else bias.detach().contiguous())
-        self._ws: dict[int, torch.Tensor] = {}
+        self._ws: dict[tuple[int, int], torch.Tensor] = {}
 
     @classmethod
     def from_linear(cls, layer: torch.nn.Linear, threshold: float = 6.0,
@@ -64,12 +71,19 @@ class Linear8bitLt(torch.nn.Module):
         return cls(w, b, threshold, keep_fp16_weight)
 
     def _workspace(self, T: int) -> torch.Tensor:
-        ws = self._ws.get(T)
+        # one workspace per (T, stream): calls on one stream are ordered and
+        # may share it, calls on different streams may overlap and may not
+        key = (T, torch.cuda.current_stream(self.Wq.device).cuda_stream)
+        ws = self._ws.get(key)
         if ws is None:
             ws = torch.empty((binding.workspace_bytes(T, self.out_features, self.in_features),),
                              dtype=torch.uint8, device=self.Wq.device)
-            self._ws[T] = ws
+            self._ws[key] = ws
         return ws
+
+    def clear_workspaces(self) -> None:
+        """Drop the cached workspaces (after the streams that used them are done)."""
+        self._ws.clear()
 
     @torch.no_grad()
     def forward(self, x: torch.Tensor) -> torch.Tensor:

@@ -48,8 +48,9 @@ def sample_rows(T: int, n: int = 64, seed: int = 0) -> np.ndarray:
 
 
 def run_and_compare(orc, X16: np.ndarray, W16: np.ndarray, tau: float, rows=None,
-                    what: str = "", check_weights: bool = True):
-    """CUDA path (debug entry point, same kernels as bnb_int8_linear) vs oracle."""
+                    what: str = "", check_weights: bool = True, opts: int = 0):
+    """CUDA path (debug entry point, same kernels as bnb_int8_linear; with
+    ``opts``, bnb_int8_linear_opts with those per-call options) vs oracle."""
     import torch
 
     from int8_mixed_precision_04_b300 import binding
@@ -59,7 +60,8 @@ def run_and_compare(orc, X16: np.ndarray, W16: np.ndarray, tau: float, rows=None
     X = torch.from_numpy(np.ascontiguousarray(X16)).cuda()
     W = torch.from_numpy(np.ascontiguousarray(W16)).cuda()
     Wq, sw = binding.quantize_weight(W)
-    r = binding.linear_debug(X, Wq, sw, W, tau)
+    r = (binding.linear_opts(X, Wq, sw, W, tau, opts, debug=True) if opts
+         else binding.linear_debug(X, Wq, sw, W, tau))
     torch.cuda.synchronize()
     assert binding.last_device_status(r["workspace"]) == 0
     Wq_o, sw_o = orc.quantize_weight(W16)

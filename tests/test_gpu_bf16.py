@@ -11,10 +11,6 @@ the second term the fp32 accumulation error.
 """
 
 import math
-import os
-import subprocess
-import sys
-
 import numpy as np
 import pytest
 
@@ -74,14 +70,18 @@ def check_y_bf16(y_bits, ref, sw, bias_bits, what):
                            f"{bad[0].tolist()}: {y[tuple(bad[0])]} vs {v[tuple(bad[0])]}")
 
 
-def run_bf16(orc, Xb, Wb, tau, bias=None, wq_only=False, rows=None, what=""):
+def run_bf16(orc, Xb, Wb, tau, bias=None, wq_only=False, rows=None, what="", opts=0):
     import torch
 
     from int8_mixed_precision_04_b300 import binding
     W = _dev(Wb)
     Wq, sw = binding.quantize_weight(W)
-    r = binding.linear_debug(_dev(Xb), Wq, sw, None if wq_only else W, tau,
-                             bias=None if bias is None else _dev(bias))
+    if opts:
+        r = binding.linear_opts(_dev(Xb), Wq, sw, None if wq_only else W, tau, opts,
+                                bias=None if bias is None else _dev(bias), debug=True)
+    else:
+        r = binding.linear_debug(_dev(Xb), Wq, sw, None if wq_only else W, tau,
+                                 bias=None if bias is None else _dev(bias))
     torch.cuda.synchronize()
     assert binding.last_device_status(r["workspace"]) == 0
     Wq_o, sw_o = orc.quantize_weight(Wb, fmt="bf16")
@@ -196,17 +196,3 @@ def test_bf16_module_and_from_host(orc):
         bias_b = _host_bits(lin.bias.detach().to(torch.bfloat16))
         ref = orc.linear(Xb, Wq_o, sw_o, Wb if keep else None, 6.0, bias=bias_b, fmt="bf16")
         check_y_bf16(_host_bits(Y_ref), ref, sw_o, bias_b, f"module keep={keep}")
-
-
-def test_bf16_mma_path():
-    """The legacy mma GEMM in bf16 (a child process with BNB_GEMM=mma)."""
-    if os.environ.get("BNB_GEMM") == "mma":
-        pytest.skip("already the mma path")
-    env = dict(os.environ, BNB_GEMM="mma")
-    r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-m", "gpu", __file__,
-                        "-k", "(test_bf16_parity and (272 or 1024 or 2064 or 512)) or "
-                              "test_bf16_integer_exact",
-                        "-p", "no:cacheprovider"],
-                       env=env, capture_output=True, text=True, timeout=600)
-    assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-2000:]
-    assert " passed" in r.stdout

@@ -1,12 +1,8 @@
 """The layer with a bias (bnb_int8_linear_bias) and the Linear8bitLt wrapper,
-against the oracle, on every path: decode (T <= 16), the tcgen05 GEMM and,
-in a child process with BNB_GEMM=mma, the legacy mma GEMM (GPU)."""
+against the oracle, on every path: decode (T <= 16) and the tcgen05 GEMM
+(the legacy mma GEMM in test_gpu_options.py) (GPU)."""
 
 import math
-import os
-import subprocess
-import sys
-
 import numpy as np
 import pytest
 
@@ -102,17 +98,3 @@ def test_linear8bitlt(orc):
     nobias = Linear8bitLt(torch.from_numpy(W16).cuda(), None, threshold=math.inf)
     ref_nb = orc.linear(w.X, Wq_o, sw_o, W16, math.inf)
     check_y(nobias(torch.from_numpy(w.X).cuda()).cpu().numpy(), ref_nb["Y"], "no bias")
-
-
-def test_bias_parity_mma_path():
-    """The legacy mma GEMM's epilogue with a bias (the path is chosen once per
-    process, so the GEMM-sized cases run again in a child with BNB_GEMM=mma)."""
-    if os.environ.get("BNB_GEMM") == "mma":
-        pytest.skip("already the mma path")
-    env = dict(os.environ, BNB_GEMM="mma")
-    r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-m", "gpu", __file__,
-                        "-k", "(test_bias_parity and (272 or 1024 or 2064)) or test_bias_integer_exact",
-                        "-p", "no:cacheprovider"],
-                       env=env, capture_output=True, text=True, timeout=600)
-    assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-2000:]
-    assert " passed" in r.stdout

@@ -32,22 +32,22 @@ def test_decode(orc, T):
     run_and_compare(orc, w.X, w.W, w.tau, what=f"decode T={T}")
 
 
-@pytest.mark.parametrize("cluster", [16, 8, 4])
+@pytest.mark.parametrize("cluster", [8, 4, 2, 1])
 @pytest.mark.parametrize("T,K,N,ncols", [
     (16, 4096, 1024, 4), (5, 272, 200, 2), (16, 1040, 96, 70), (11, 2048, 520, 9),
     (16, 4096, 3900, 70),
 ])
-def test_decode_cluster_sizes(orc, monkeypatch, cluster, T, K, N, ncols):
+def test_decode_cluster_sizes(orc, cluster, T, K, N, ncols):
     """The decode kernel with each cluster size it can run (16, 8 or 4 CTAs
     sharing one activation pass): CTAs with few or no columns, slices of up
     to 35 channels (a partial fifth 8-channel group), and more outlier columns
     than the producer warp sums alone.  A size whose resident CTAs cannot
     hold the call falls back to one that can."""
     from int8_mixed_precision_04_b300 import binding
-    monkeypatch.setenv("BNB_DECODE_CLUSTER", str(cluster))
     assert binding.load().bnb_int8_linear_path(T, N, K) == 1
     w = inputs.random_small(T, K, N, ncols, seed=K + N + cluster, tau=6.0)
-    run_and_compare(orc, w.X, w.W, 6.0, what=f"decode cluster {cluster} T{T} K{K} N{N}")
+    run_and_compare(orc, w.X, w.W, 6.0, what=f"decode cluster {cluster} T{T} K{K} N{N}",
+                    opts=binding.OPT_CLUSTER(cluster))
 
 
 @pytest.mark.parametrize("T,K,N,ncols", [
@@ -190,3 +190,29 @@ def test_large_full(orc):
 def test_sweep_full(orc, frac, tau):
     w = inputs.sweep(frac, tau)
     run_and_compare(orc, w.X, w.W, tau, rows=sample_rows(w.T, 32), what=f"sweep f{frac} tau{tau}")
+
+
+# ---- the decode path at every weight shape ---------------------------------
+
+@pytest.mark.parametrize("T", [1, 16])
+@pytest.mark.parametrize("K,N", [(4096, 11008), (8192, 28672)])
+def test_decode_large_weights(orc, T, K, N):
+    """A decode step (T <= 16) through the prefill and the large MLP weights:
+    the decode kernel (K split across a cluster of K / 1024 CTAs, channels in
+    double-buffered batches), every row and channel against the oracle."""
+    from int8_mixed_precision_04_b300 import binding
+    assert binding.load().bnb_int8_linear_path(T, N, K) == 1
+    w = inputs.decode(T=T, K=K, N=N)
+    run_and_compare(orc, w.X, w.W, w.tau, what=f"decode T{T} K{K} N{N}")
+
+
+@pytest.mark.parametrize("T,K,N,ncols,tau", [
+    (16, 1040, 3000, 6, 6.0), (7, 3072, 2056, 3, 6.0), (16, 8192, 1000, 40, 3.0),
+    (2, 5120, 9000, 2, 6.0), (16, 2048, 40000, 5, 6.0), (9, 16, 37, 1, 0.0),
+    (16, 6144, 777, 0, math.inf),
+])
+def test_decode_shapes(orc, T, K, N, ncols, tau):
+    """Ragged K (a CTA with a partial K-range), N not a multiple of 8, many
+    batches per cluster, dense outlier sets, tiny shapes."""
+    w = inputs.random_small(T, K, N, ncols, seed=T * 5 + K + N, tau=tau)
+    run_and_compare(orc, w.X, w.W, tau, what=f"decode shape T{T} K{K} N{N} tau{tau}")

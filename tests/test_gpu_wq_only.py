@@ -2,14 +2,9 @@
 the outlier columns use the codes dequantized, Wq sw / 127.  Against the
 oracle's int8-weight-only leg on every path: decode (T <= 16, with more
 outlier columns than the exchange carries), the tcgen05 GEMM with a sparse and
-a dense outlier set, and, in a child process with BNB_GEMM=mma, the legacy
-mma GEMM (GPU)."""
+a dense outlier set (the legacy mma GEMM in test_gpu_options.py) (GPU)."""
 
 import math
-import os
-import subprocess
-import sys
-
 import numpy as np
 import pytest
 
@@ -89,17 +84,3 @@ def test_wq_only_from_host_and_module(orc):
     assert torch.equal(layer(torch.from_numpy(w.X).cuda()), Y_ref)
     Wq_o, sw_o = orc.quantize_weight(w.W)
     check_y(Y_ref.cpu().numpy(), orc.linear(w.X, Wq_o, sw_o, None, 6.0, bias=b)["Y"], "module")
-
-
-def test_wq_only_mma_path():
-    """The legacy mma GEMM without W16 (the path is chosen once per process,
-    so the GEMM-sized cases run again in a child with BNB_GEMM=mma)."""
-    if os.environ.get("BNB_GEMM") == "mma":
-        pytest.skip("already the mma path")
-    env = dict(os.environ, BNB_GEMM="mma")
-    r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-m", "gpu", __file__,
-                        "-k", "test_wq_only_parity and (272 or 1024 or 2064 or 512)",
-                        "-p", "no:cacheprovider"],
-                       env=env, capture_output=True, text=True, timeout=600)
-    assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-2000:]
-    assert " passed" in r.stdout
