@@ -108,7 +108,6 @@ def algorithmic_bytes(T, N, K, nO, bias=False, wq_only=False):
 # is the one that was captured (first 16 hex digits of its SHA-256).
 MEASURED_TRAFFIC = {
     # kernel: (source file, source digest, (T, K, N), dram read + write bytes)
-    "dec_fused": ("decode.cu", "66cf605688f65818", (16, 4096, 4096), 19112704 + 0),
 }
 
 
@@ -118,6 +117,8 @@ def measured_traffic(kernel, T, K, N):
     if rec is None or rec[2] != (T, K, N):
         return None
     path = os.path.join(ROOT, "int8_mixed_precision_04_b300", "csrc", rec[0])
+    if not os.path.exists(path):
+        return None
     digest = hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
     return rec[3] if digest == rec[1] else None
 
@@ -411,6 +412,10 @@ def measure_layer(args, w, dev, world, local, steps, min_timed_s, min_layers=2,
                     "peak_burst": peaks["bf16_tflops"],
                     "frac_of_burst": kf / kavg_s / 1e12 / peaks["bf16_tflops"]}
         roof["frac"] = roof["achieved"] / roof["peak"]
+        # every kernel's algorithmic bytes against HBM too (the bound of
+        # decode-sized calls, whichever kernel runs them)
+        roof["alg_gbs"] = kb / kavg_s / 1e9
+        roof["hbm_frac"] = roof["alg_gbs"] / peaks["hbm_gbs"]
         roof["traffic"] = (args.traffic if args.traffic is not None
                            else None if args.bias or args.wq_only or args.bf16
                            else measured_traffic(kname, T, K, N))
@@ -853,7 +858,7 @@ def main():
                     help="the timed region lasts at least this long (graph replays per step)")
     ap.add_argument("--kernel-timed-s", type=float, default=1.0,
                     help="length of the dominant-kernel timing loop")
-    ap.add_argument("--sub", default="decode,decode_k8192,prefill",
+    ap.add_argument("--sub", default="decode,decode_k8192,decode_n11008,prefill",
                     help="other regimes measured in the same run (comma list, '' for none)")
     ap.add_argument("--sub-timed-s", type=float, default=0.5)
     ap.add_argument("--e2e-calls", type=int, default=2000)

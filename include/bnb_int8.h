@@ -303,10 +303,12 @@ const char *bnb_status_string(bnb_status_t s);
 uint64_t bnb_launch_count(void);
 
 /*
- * Which kernel path bnb_int8_linear takes for a shape: 1 = decode (T <= 16 and
- * K <= 8192, any N: one kernel per call, K split across a thread-block
- * cluster), 2 = tensor-core GEMM (tcgen05), 3 = warp-level mma GEMM (only
- * through bnb_int8_linear_opts with BNB_OPT_LEGACY_MMA).
+ * Which kernel path bnb_int8_linear takes for a shape on the current device:
+ * 1 = decode (T <= 16, K <= 4096 and N within what the decode kernel's
+ * resident CTAs hold at up to 40 output channels each: 4620 at K = 4096 on
+ * B300), 2 = tensor-core GEMM (tcgen05; every other shape, decode-sized T
+ * included), 3 = warp-level mma GEMM (only through bnb_int8_linear_opts with
+ * BNB_OPT_LEGACY_MMA).
  */
 int bnb_int8_linear_path(int64_t T, int64_t N, int64_t K);
 
@@ -330,10 +332,10 @@ int bnb_int8_linear_path(int64_t T, int64_t N, int64_t K);
  *                       work has completed.
  *   BNB_OPT_LEGACY_MMA  T > 16 path: the warp-level mma.sync GEMM (sm_80-style
  *                       tensor path, for comparison) instead of tcgen05.
- *   BNB_OPT_CLUSTER(c)  decode path: thread-block clusters of c CTAs (c <= 8)
- *                       instead of the size the library picks, ceil(K / 1024),
- *                       when c is at least that size (CTAs past K then hold
- *                       no columns).
+ *   BNB_OPT_CLUSTER(c)  decode path: thread-block clusters of c CTAs (c = 4,
+ *                       8 or 16) sharing one activation pass, instead of the
+ *                       size the library picks, when clusters of that size
+ *                       hold the call.
  *   BNB_OPT_FORCE_TIMEOUT  one thread of the call's main kernel waits, with a
  *                       limit of about 0.1 ms, on an mbarrier that nothing
  *                       completes, and then takes the kernel's timeout path

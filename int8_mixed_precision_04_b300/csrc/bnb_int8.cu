@@ -135,11 +135,11 @@ static bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
   return x < y + nb && y < x + na;
 }
 
-// 1: decode (T <= 16, K <= kDecodeMaxK, any N); 2: tcgen05 GEMM; 3: legacy
-// mma GEMM (only when a call's options ask for it).
-static int choose_path(int64_t T, int64_t N, int64_t K, uint32_t opts = 0) {
-  (void)N;
-  if (T <= 16 && K <= kDecodeMaxK) return 1;
+// 1: decode (T <= 16, K <= kDecodeMaxK, N within what the resident decode
+// CTAs hold in one wave); 2: tcgen05 GEMM (every other shape, decode-sized T
+// included); 3: legacy mma GEMM (only when a call's options ask for it).
+static int choose_path(int64_t T, int64_t N, int64_t K, int dev, uint32_t opts = 0) {
+  if (T <= 16 && K <= kDecodeMaxK && N <= decode_max_n(dev, K)) return 1;
   return (opts & BNB_OPT_LEGACY_MMA) ? 3 : 2;
 }
 
@@ -187,7 +187,7 @@ static bnb_status_t linear_impl(const void *X, int64_t T, int64_t K, const int8_
   if (st != BNB_OK) return st;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_v);
   const Workspace ws = carve(workspace, T, N, K);
-  const int path = choose_path(T, N, K, opts);
+  const int path = choose_path(T, N, K, dev, opts);
   const uint32_t thr = threshold_bits(tau, bf16);
   cudaError_t e;
   if (path == 1) {
@@ -417,7 +417,7 @@ bnb_status_t bnb_int8_linear_opts(const void *X, int64_t T, int64_t K, const int
                               BNB_OPT_LEGACY_MMA | BNB_OPT_FORCE_TIMEOUT | BNB_OPT_CLUSTER(0xff);
   if (opts & ~kKnown) return BNB_ERR_INVALID_ARG;
   const uint32_t c = (opts >> 8) & 0xffu;
-  if (c > 8) return BNB_ERR_INVALID_ARG;
+  if (c != 0 && c != 4 && c != 8 && c != 16) return BNB_ERR_INVALID_ARG;
   if ((opts & BNB_OPT_MAIN_ONLY) && (opts & BNB_OPT_ACT_ONLY)) return BNB_ERR_INVALID_ARG;
   return linear_impl(X, T, K, Wq, Wscale, W16, bias, N, tau, dtype == BNB_DTYPE_BF16, Y,
                      workspace, workspace_bytes, stream, Xq, Xscale, outlier_idx, n_outliers, acc,
@@ -451,7 +451,9 @@ uint64_t bnb_launch_count(void) { return g_launches.load(std::memory_order_relax
 
 int bnb_int8_linear_path(int64_t T, int64_t N, int64_t K) {
   if (T <= 0 || N <= 0 || K <= 0) return 0;
-  return choose_path(T, N, K);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) dev = -1;
+  return choose_path(T, N, K, dev);
 }
 
 }  // extern "C"

@@ -18,9 +18,10 @@ constexpr int32_t kDevTimeout = BNB_ERR_TIMEOUT;
 // device attribute, this is only a default for host-side heuristics.
 constexpr int kB300Sms = 148;
 
-// Largest K of the decode path (T <= 16): a cluster of at most 8 CTAs splits
-// K in ranges of 1024 columns.
-constexpr int64_t kDecodeMaxK = 8192;
+// Largest K of the decode path: 32 weight rows and 16 code rows of K + 64
+// bytes plus the outlier list fit in 227 KB, and the activation pass gives
+// each of 16 warps x 32 lanes one 8-column vector.
+constexpr int64_t kDecodeMaxK = 4096;
 
 // The fp16 outlier block of the GEMM path is dense (X masked to the outlier
 // columns over all K, multiplied as one dense fp16 GEMM against W16 tiles)
@@ -107,6 +108,21 @@ __device__ __forceinline__ uint32_t code_byte(float x, float a, float r) {
   return fb + (s < 0.0f ? 1u : (s == 0.0f ? (fb & 1u) : 0u));
 }
 
+// The same code byte, from the product p = x * r first.  r = fl32(127 / a)
+// and p = fl32(x r) put p within |v| (2^-23 + 2^-48) < 2^-16 of v = 127 x / a
+// (|v| <= 127).  So when p lies more than 2^-15 from every half-integer, v
+// rounds like p and is no tie: the code is rint(p), one magic-number add
+// (ties to even) whose low byte is the code.  Otherwise (about one value in
+// 2^14) code_byte decides exactly.  Requires what code_byte requires.
+__device__ __forceinline__ uint32_t code_byte_fast(float x, float a, float r) {
+  constexpr float kM = 12582912.0f;
+  const float p = x * r;
+  const float t = p + kM;          // M + rint(p), exact for |p| < 2^22
+  const float e = p - (t - kM);    // p - rint(p), exact
+  if (fabsf(e) < 0.5f - 0x1p-15f) return __float_as_uint(t);
+  return code_byte(x, a, r);
+}
+
 __device__ __forceinline__ int code_of(float x, float a, float r) {
   return a > 0.0f ? code_exact(x, a, r) : 0;
 }
@@ -165,7 +181,7 @@ struct RowCode {
   }
   // the code byte of x (|x| <= absmax), exact
   __device__ __forceinline__ uint32_t byte(float x) const {
-    return code_byte(kBf ? (x * s1) * s2 : x, a, r);
+    return code_byte_fast(kBf ? (x * s1) * s2 : x, a, r);
   }
 };
 

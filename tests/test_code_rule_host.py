@@ -4,7 +4,9 @@ The CUDA code takes vector-wise codes without a division or a conversion
 instruction: p = x r with r = fl32(127 / a); f = floor(p) from a magic-number
 round; the sign of (f + 1/2) a - 127 x, which one fma gives exactly, decides
 between f and f + 1 (ties to even); for bf16, x and a are first scaled by one
-power of two built from a's exponent bits.  Here the same fp32 steps run in
+power of two built from a's exponent bits.  Its fast path takes rint(p)
+directly whenever p lies more than 2^-15 from every half-integer (p is within
+2^-16 of 127 x / a) and falls back to the rule above otherwise.  Here the same fp32 steps run in
 numpy (the fma's sign from an exact float64 product) over every finite fp16
 or bf16 x against a spread of scales, including both ends of bf16's range,
 and must equal round_half_even(127 x / a) in exact arithmetic.  This checks
@@ -42,6 +44,17 @@ def _bf16_scale(a: np.float32):
     return s1, s2
 
 
+def _code_byte_fast(x: np.ndarray, a: np.float32) -> np.ndarray:
+    """The fast path: rint(p) by the magic-number add when p = x fl32(127/a)
+    lies more than 2^-15 from every half-integer, the exact rule otherwise."""
+    r = np.float32(127.0) / a
+    p = (x * r).astype(np.float32)
+    t = (p + KM).astype(np.float32)
+    e = (p - (t - KM).astype(np.float32)).astype(np.float32)
+    fast = (t.view(np.uint32) & 0xFF).astype(np.uint8).view(np.int8).astype(np.int64)
+    return np.where(np.abs(e) < np.float32(0.5 - 2.0 ** -15), fast, _code_byte(x, a))
+
+
 def test_fp16_rule_is_exact():
     allv = np.arange(0, 0x7C00, dtype=np.uint16).view(np.float16)
     rng = np.random.default_rng(41)
@@ -51,10 +64,12 @@ def test_fp16_rule_is_exact():
         a16 = np.float16(a16)
         xs = allv[allv.astype(np.float64) <= float(a16)]
         xs = np.concatenate([xs, -xs[1:]])
-        got = _code_byte(xs.astype(np.float32), np.float32(a16))
         want = oracle_pins._exact_codes(xs, np.full(len(xs), a16, dtype=np.float16))
-        bad = np.flatnonzero(got != want)
-        assert len(bad) == 0, (float(a16), xs[bad[:3]], got[bad[:3]], want[bad[:3]])
+        for rule in (_code_byte, _code_byte_fast):
+            got = rule(xs.astype(np.float32), np.float32(a16))
+            bad = np.flatnonzero(got != want)
+            assert len(bad) == 0, (rule.__name__, float(a16), xs[bad[:3]], got[bad[:3]],
+                                   want[bad[:3]])
 
 
 def test_bf16_scaled_rule_is_exact():
@@ -73,10 +88,12 @@ def test_bf16_scaled_rule_is_exact():
         assert 1.0 <= a_s < 2.0, (ab, a_s)
         with np.errstate(under="ignore"):
             x_s = ((x * s1).astype(np.float32) * s2).astype(np.float32)
-        got = _code_byte(x_s, a_s)
         want = oracle_pins._exact_codes_bf16(x.astype(np.float64), float(a))
-        bad = np.flatnonzero(got != want)
-        assert len(bad) == 0, (hex(ab), x[bad[:3]], got[bad[:3]], want[bad[:3]])
+        for rule in (_code_byte, _code_byte_fast):
+            got = rule(x_s, a_s)
+            bad = np.flatnonzero(got != want)
+            assert len(bad) == 0, (rule.__name__, hex(ab), x[bad[:3]], got[bad[:3]],
+                                   want[bad[:3]])
 
 
 def _bw_code(x: np.ndarray, a: np.float32) -> np.ndarray:

@@ -126,7 +126,7 @@ def test_unknown_options_are_rejected():
     X = torch.zeros((4, 64), dtype=torch.float16, device="cuda")
     W = torch.zeros((32, 64), dtype=torch.float16, device="cuda")
     Wq, sw = binding.quantize_weight(W)
-    for bad in (0x20, binding.OPT_CLUSTER(9), binding.OPT_CLUSTER(32),
+    for bad in (0x20, binding.OPT_CLUSTER(3), binding.OPT_CLUSTER(32),
                 binding.OPT_MAIN_ONLY | binding.OPT_ACT_ONLY):
         with pytest.raises(binding.BnbError) as e:
             binding.linear_opts(X, Wq, sw, W, 6.0, bad)
