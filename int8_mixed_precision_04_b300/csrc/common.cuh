@@ -23,6 +23,10 @@ constexpr int kB300Sms = 148;
 // each of 16 warps x 32 lanes one 8-column vector.
 constexpr int64_t kDecodeMaxK = 4096;
 
+// Largest T of the GEMM's 32-token tile (decode-sized calls the decode kernel
+// does not hold); larger T take the 256-token tile.
+constexpr int64_t kGemmSmallT = 32;
+
 // The fp16 outlier block of the GEMM path is dense (X masked to the outlier
 // columns over all K, multiplied as one dense fp16 GEMM against W16 tiles)
 // when more than 1/16 of the columns are outliers; otherwise it is

@@ -58,9 +58,8 @@ namespace bnb {
 namespace {
 
 constexpr int kBM = 128;       // output channels per tile
-constexpr int kBN = 256;       // tokens per tile
 constexpr int kBK = 64;        // k columns per stage (128 bytes of fp16)
-constexpr int kStages = 4;
+constexpr int kMaxStages = 8;
 constexpr int kChunkStages = 16;  // 16 x 64 = 1024 columns per exact fp32 chunk
 // Converter warps: 4 (warpgroup 1 of their own; measured 1.36x faster than 2,
 // because widening the weight tile bounds the MMA rate) or 2 (warps 2-3 of
@@ -82,22 +81,33 @@ constexpr int kRegsEpi = kConvWarps == 2 ? 104 : 96;
 static_assert(kConvWarps == 2 ? 128 * kRegsWG0 + 512 * kRegsEpi <= 640 * 96
                               : 128 * kRegsWG0 + 128 * kRegsConv + 512 * kRegsEpi <= 768 * 80,
               "register split exceeds the launch budget");
-constexpr int kEpiCols = kBN / 4;  // columns per epilogue thread
-constexpr uint32_t kTmemCols = 512;  // two fp32 buffers of kBN columns
-
-constexpr int kXBytes = kBN * kBK * 2;   // B operand tile (fp16)
 constexpr int kWhBytes = kBM * kBK * 2;  // A operand tile (fp16)
 constexpr int kWqBytes = kBM * kBK;      // int8 weight tile
-constexpr int kStageBytes = kXBytes + kWhBytes + kWqBytes;
-static_assert(kStageBytes % 1024 == 0, "stages must keep 1024-byte swizzle alignment");
-constexpr size_t kSmemBytes = (size_t)kStages * kStageBytes + 1024;
 
-// Instruction descriptor of kind::f16: D fp32, A and B fp16, both K-major,
-// N = kBN, M = kBM.
-constexpr uint32_t kIdesc = (1u << 4) | ((uint32_t)(kBN >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
-// The same with A and B bf16 (format fields 1), for the outlier stages of a
-// bf16 layer; the int8 stages always multiply fp16 integer codes.
-constexpr uint32_t kIdescBf16 = kIdesc | (1u << 7) | (1u << 10);
+// The token tile: 256 tokens for T > 32 (4 pipeline stages); 32 tokens for
+// decode-sized T (T <= 32), where a 256-token tile would spend almost every
+// MMA on padding rows: its small activation tile leaves room for 8 stages, so
+// that more of the weight stream is in flight.
+template <int kBNt>
+struct Tile {
+  static constexpr int kBN = kBNt;                      // tokens per tile (MMA N)
+  static constexpr int kStages = kBNt == 256 ? 4 : 8;
+  static constexpr int kEpiCols = kBN / 4;              // columns per epilogue thread
+  static constexpr uint32_t kTmemCols = 2 * kBN < 32 ? 32 : 2 * kBN;  // two fp32 buffers
+  static constexpr int kXBytes = kBN * kBK * 2;         // B operand tile (fp16)
+  static constexpr int kStageBytes = kXBytes + kWhBytes + kWqBytes;
+  static constexpr size_t kSmemBytes = (size_t)kStages * kStageBytes + 1024;
+  // Instruction descriptor of kind::f16: D fp32, A and B fp16, both K-major,
+  // N = kBN, M = kBM.
+  static constexpr uint32_t kIdesc =
+      (1u << 4) | ((uint32_t)(kBN >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
+  // The same with A and B bf16 (format fields 1), for the outlier stages of a
+  // bf16 layer; the int8 stages always multiply fp16 integer codes.
+  static constexpr uint32_t kIdescBf16 = kIdesc | (1u << 7) | (1u << 10);
+  static_assert(kStageBytes % 1024 == 0, "stages must keep 1024-byte swizzle alignment");
+  static_assert(kStages <= kMaxStages && kSmemBytes <= 232448 - 1024, "shared memory");
+  static_assert(kEpiCols % 8 == 0 && (kTmemCols & (kTmemCols - 1)) == 0, "tile geometry");
+};
 
 // Shared-memory matrix descriptor of a K-major tile with the 128-byte
 // swizzle: rows of 128 bytes, 8-row groups 1024 bytes apart.
@@ -127,9 +137,9 @@ struct TcArgs {
 };
 
 struct TcSmem {
-  uint64_t full[kStages];   // TMA bytes landed
-  uint64_t conv[kStages];   // widened / gathered A operand written
-  uint64_t empty[kStages];  // MMAs reading the stage done
+  uint64_t full[kMaxStages];   // TMA bytes landed
+  uint64_t conv[kMaxStages];   // widened / gathered A operand written
+  uint64_t empty[kMaxStages];  // MMAs reading the stage done
   uint64_t accf[2];         // chunk complete in tensor-memory buffer b
   uint64_t acce[2];         // epilogue finished reading buffer b
   uint64_t fin;             // MMA warp's own completion fence at exit
@@ -139,12 +149,17 @@ struct TcSmem {
   int abort;
 };
 
-__device__ __forceinline__ uint8_t *stage_x(uint8_t *s, int st) { return s + st * kStageBytes; }
-__device__ __forceinline__ uint8_t *stage_wh(uint8_t *s, int st) {
-  return s + st * kStageBytes + kXBytes;
+template <int kBNt>
+__device__ __forceinline__ uint8_t *stage_x(uint8_t *s, int st) {
+  return s + st * Tile<kBNt>::kStageBytes;
 }
+template <int kBNt>
+__device__ __forceinline__ uint8_t *stage_wh(uint8_t *s, int st) {
+  return s + st * Tile<kBNt>::kStageBytes + Tile<kBNt>::kXBytes;
+}
+template <int kBNt>
 __device__ __forceinline__ uint8_t *stage_wq(uint8_t *s, int st) {
-  return s + st * kStageBytes + kXBytes + kWhBytes;
+  return s + st * Tile<kBNt>::kStageBytes + Tile<kBNt>::kXBytes + kWhBytes;
 }
 
 // All lanes wait (each acquires the barrier's phase); the outcome is made
@@ -194,9 +209,10 @@ __device__ __forceinline__ void widen16(const uint4 &v, uint4 &g0, uint4 &g1) {
 // Thread ct owns weight rows ct, ct + 32 * kConvWarps, ...  In a bf16
 // layer the outlier stages' codes are widened to bf16 integers instead
 // (exact), so that both MMA operands have X's format.
-template <bool kBf>
+template <bool kBf, int kBNt>
 __device__ __forceinline__ void converter_role(uint8_t *smem, TcSmem &sm, const TcArgs &p,
                                                int s_int, int s_conv, int nst, int ntiles) {
+  constexpr int kStages = Tile<kBNt>::kStages;
   const int ct = threadIdx.x - kConvWarp0 * 32;  // 0 .. 32 * kConvWarps - 1
   const int lane = threadIdx.x & 31;
   uint32_t it = 0;
@@ -213,8 +229,8 @@ __device__ __forceinline__ void converter_role(uint8_t *smem, TcSmem &sm, const 
         for (int h = 0; h < kConvRows; ++h) {
           const int r = ct + kConvWarps * 32 * h;
           // int8 row r: 64 bytes, 16-byte chunk q stored at q ^ ((r >> 1) & 3)
-          const uint8_t *wq = stage_wq(smem, st) + r * 64;
-          uint8_t *wh = stage_wh(smem, st) + r * 128;
+          const uint8_t *wq = stage_wq<kBNt>(smem, st) + r * 64;
+          uint8_t *wh = stage_wh<kBNt>(smem, st) + r * 128;
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             const uint4 v = *reinterpret_cast<const uint4 *>(wq + 16 * (q ^ ((r >> 1) & 3)));
@@ -236,11 +252,15 @@ __device__ __forceinline__ void converter_role(uint8_t *smem, TcSmem &sm, const 
   }
 }
 
-template <bool kBf>
+template <bool kBf, int kBNt>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
                    const __grid_constant__ CUtensorMap tm_xo, const __grid_constant__ CUtensorMap tm_w16,
                    const __grid_constant__ CUtensorMap tm_w16o, const TcArgs p) {
+  using Tl = Tile<kBNt>;
+  constexpr int kBN = Tl::kBN, kStages = Tl::kStages, kEpiCols = Tl::kEpiCols;
+  constexpr int kXBytes = Tl::kXBytes;
+  constexpr uint32_t kTmemCols = Tl::kTmemCols, kIdesc = Tl::kIdesc, kIdescBf16 = Tl::kIdescBf16;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   __shared__ TcSmem sm;
@@ -312,16 +332,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (s < s_int) {
             mbar_expect_tx(&sm.full[st], kXBytes + kWqBytes);
-            tma_load_2d(stage_x(smem, st), &tm_x, s * kBK, t0, &sm.full[st]);
-            tma_load_2d(stage_wq(smem, st), &tm_w, s * kBK, n0, &sm.full[st]);
+            tma_load_2d(stage_x<kBNt>(smem, st), &tm_x, s * kBK, t0, &sm.full[st]);
+            tma_load_2d(stage_wq<kBNt>(smem, st), &tm_w, s * kBK, n0, &sm.full[st]);
           } else if (wq_out) {  // outlier stage on the int8 weight tile
             mbar_expect_tx(&sm.full[st], kXBytes + kWqBytes);
-            tma_load_2d(stage_x(smem, st), &tm_xo, (s - s_int) * kBK, t0, &sm.full[st]);
-            tma_load_2d(stage_wq(smem, st), &tm_w, (s - s_int) * kBK, n0, &sm.full[st]);
+            tma_load_2d(stage_x<kBNt>(smem, st), &tm_xo, (s - s_int) * kBK, t0, &sm.full[st]);
+            tma_load_2d(stage_wq<kBNt>(smem, st), &tm_w, (s - s_int) * kBK, n0, &sm.full[st]);
           } else {  // outlier stage: fp16 A tile straight into the A operand slot
             mbar_expect_tx(&sm.full[st], kXBytes + kWhBytes);
-            tma_load_2d(stage_x(smem, st), &tm_xo, (s - s_int) * kBK, t0, &sm.full[st]);
-            tma_load_2d(stage_wh(smem, st), dense ? &tm_w16 : &tm_w16o, (s - s_int) * kBK, n0,
+            tma_load_2d(stage_x<kBNt>(smem, st), &tm_xo, (s - s_int) * kBK, t0, &sm.full[st]);
+            tma_load_2d(stage_wh<kBNt>(smem, st), dense ? &tm_w16 : &tm_w16o, (s - s_int) * kBK, n0,
                         &sm.full[st]);
           }
         }
@@ -355,8 +375,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               break;
             }
             tc_fence_after();
-            const uint64_t ad = sw128_desc(smem_addr(stage_wh(smem, st)));
-            const uint64_t bd = sw128_desc(smem_addr(stage_x(smem, st)));
+            const uint64_t ad = sw128_desc(smem_addr(stage_wh<kBNt>(smem, st)));
+            const uint64_t bd = sw128_desc(smem_addr(stage_x<kBNt>(smem, st)));
 #pragma unroll
             for (int k = 0; k < kBK / 16; ++k)  // 16 fp16 = 32 bytes per MMA
               umma_f16(d, ad + 2 * k, bd + 2 * k, kBf && s >= s_int ? kIdescBf16 : kIdesc,
@@ -378,10 +398,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_dealloc(tmem, kTmemCols);
     }
     if (kConvWarps == 2 && warp >= kConvWarp0)
-      converter_role<kBf>(smem, sm, p, s_int, s_conv, nst, ntiles);
+      converter_role<kBf, kBNt>(smem, sm, p, s_int, s_conv, nst, ntiles);
   } else if (kConvWarps == 4 && warp < kEpiWarp0) {
     regs_dec<kRegsConv>();
-    converter_role<kBf>(smem, sm, p, s_int, s_conv, nst, ntiles);
+    converter_role<kBf, kBNt>(smem, sm, p, s_int, s_conv, nst, ntiles);
   } else {
     regs_inc<kRegsEpi>();
     // ---------------- epilogue ----------------
@@ -500,17 +520,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ---- host side ----------------------------------------------------------------
 
-}  // namespace
-
-cudaError_t launch_gemm_tc(int64_t T, int64_t K, const int8_t *Wq, const float *sw,
-                           const void *W16, const void *bias, int64_t N, bool bf16, void *Y,
-                           const Workspace &ws, int32_t *dbg_acc, int num_sms, uint32_t opts,
-                           cudaStream_t stream) {
+template <int kBNt>
+cudaError_t launch_tc(int64_t T, int64_t K, const int8_t *Wq, const float *sw, const void *W16,
+                      const void *bias, int64_t N, bool bf16, void *Y, const Workspace &ws,
+                      int32_t *dbg_acc, int num_sms, uint32_t opts, cudaStream_t stream) {
+  using Tl = Tile<kBNt>;
   static bool attr_set = false;  // benign race: every writer sets the same value
   if (!attr_set) {
-    for (auto *f : {gemm_tc_kernel<false>, gemm_tc_kernel<true>}) {
+    for (auto *f : {gemm_tc_kernel<false, kBNt>, gemm_tc_kernel<true, kBNt>}) {
       cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           (int)kSmemBytes);
+                                           (int)Tl::kSmemBytes);
       if (e != cudaSuccess) return e;
     }
     attr_set = true;
@@ -520,12 +539,12 @@ cudaError_t launch_gemm_tc(int64_t T, int64_t K, const int8_t *Wq, const float *
       bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   CUtensorMap tm_x, tm_w, tm_xo, tm_w16, tm_w16o;
   if (!encode_2d(&tm_x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, ws.xcodes, (uint64_t)K, (uint64_t)T,
-                 (uint64_t)K * 2, kBK, kBN, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B) ||
+                 (uint64_t)K * 2, kBK, kBNt, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B) ||
       !encode_2d(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, Wq, (uint64_t)K, (uint64_t)N, (uint64_t)K,
                  kBK, kBM, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B) ||
       // the outlier block's inner extent is K (columns past K read as zeros)
       !encode_2d(&tm_xo, e16, ws.xo, (uint64_t)K, (uint64_t)T,
-                 (uint64_t)ws.kpad * 2, kBK, kBN, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B) ||
+                 (uint64_t)ws.kpad * 2, kBK, kBNt, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B) ||
       // without W16 this map is never read; it then describes the compacted columns
       !(W16 ? encode_2d(&tm_w16, e16, W16, (uint64_t)K, (uint64_t)N,
                         (uint64_t)K * 2, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -540,7 +559,7 @@ cudaError_t launch_gemm_tc(int64_t T, int64_t K, const int8_t *Wq, const float *
   a.T = T;
   a.K = K;
   a.N = N;
-  a.t_tiles = (int)((T + kBN - 1) / kBN);
+  a.t_tiles = (int)((T + kBNt - 1) / kBNt);
   a.n_tiles = (int)((N + kBM - 1) / kBM);
   a.s_int = (int)((K + kBK - 1) / kBK);
   a.sw = sw;
@@ -558,17 +577,30 @@ cudaError_t launch_gemm_tc(int64_t T, int64_t K, const int8_t *Wq, const float *
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.dynamicSmemBytes = Tl::kSmemBytes;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = (opts & BNB_OPT_NO_PDL) ? 0 : 1;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, bf16 ? gemm_tc_kernel<true> : gemm_tc_kernel<false>,
-                                           tm_x, tm_w, tm_xo, tm_w16, tm_w16o, a);
+  const cudaError_t e = cudaLaunchKernelEx(
+      &cfg, bf16 ? gemm_tc_kernel<true, kBNt> : gemm_tc_kernel<false, kBNt>, tm_x, tm_w, tm_xo,
+      tm_w16, tm_w16o, a);
   note_launch();
   return e;
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_tc(int64_t T, int64_t K, const int8_t *Wq, const float *sw,
+                           const void *W16, const void *bias, int64_t N, bool bf16, void *Y,
+                           const Workspace &ws, int32_t *dbg_acc, int num_sms, uint32_t opts,
+                           cudaStream_t stream) {
+  // decode-sized calls take the 32-token tile (kGemmSmallT), the rest the 256-token one
+  if (T <= kGemmSmallT)
+    return launch_tc<32>(T, K, Wq, sw, W16, bias, N, bf16, Y, ws, dbg_acc, num_sms, opts, stream);
+  return launch_tc<256>(T, K, Wq, sw, W16, bias, N, bf16, Y, ws, dbg_acc, num_sms, opts, stream);
 }
 
 }  // namespace bnb
