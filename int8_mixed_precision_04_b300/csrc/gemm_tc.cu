@@ -21,7 +21,7 @@
 //
 // Tile: 128 output channels (MMA M, tensor-memory lanes) x 256 tokens (MMA N,
 // tensor-memory columns); k advances 64 columns per pipeline stage.
-//   A operand  W codes widened to fp16 integers by four converter warps from
+//   A operand  W codes widened to fp16 integers by the converter warps from
 //              an int8 tile (TMA, 64-byte swizzle) into the 128-byte-swizzled
 //              K-major layout the MMA reads.
 //   B operand  activation codes, already fp16 integers in HBM (written by the
@@ -38,10 +38,11 @@
 // stages, and the epilogue applies sw / 127 to the int8 and outlier sums at
 // once: Y = fp16((acc sx/127 + sum_{k in O} X Wq) sw/127 + b).
 //
-// Warp roles (20 warps): 0 TMA producer, 1 MMA issuer and tensor-memory
-// owner, 2-3 converters (two weight rows per thread), 4-19 epilogue (four
-// warps per 32-lane quadrant of tensor memory, one per 64-column quarter, so
-// that each thread holds 64 int32 running sums in registers).  Persistent CTAs, one
+// Warp roles (28 warps with the default 8 converters): 0 TMA producer, 1 MMA
+// issuer and tensor-memory owner, 2-3 idle, 4-11 converters (half a weight row
+// per thread), 12-27 epilogue (four warps per 32-lane quadrant of tensor
+// memory, one per quarter of the token columns, so that each thread holds
+// kBN / 4 int32 running sums in registers).  Persistent CTAs, one
 // per SM, walk the tiles with the token tile fastest so that concurrently
 // running CTAs share weight tiles in L2.  Every wait is bounded; a timeout
 // raises a CTA-wide abort flag, records BNB_ERR_TIMEOUT and lets all roles
@@ -61,25 +62,26 @@ constexpr int kBM = 128;       // output channels per tile
 constexpr int kBK = 64;        // k columns per stage (128 bytes of fp16)
 constexpr int kMaxStages = 8;
 constexpr int kChunkStages = 16;  // 16 x 64 = 1024 columns per exact fp32 chunk
-// Converter warps: 4 (warpgroup 1 of their own; measured 1.36x faster than 2,
-// because widening the weight tile bounds the MMA rate) or 2 (warps 2-3 of
-// warpgroup 0).
+// Converter warps: 4 (warpgroup 1) or 8 (warpgroups 1 and 2), in warpgroups of
+// their own.  Widening the weight tile sits on every stage's path to the MMA
+// (measured: skipping it made the prefill GEMM 12% faster), so more converter
+// warps shorten each stage's conversion.
 #ifndef BNB_TC_CONV_WARPS
-#define BNB_TC_CONV_WARPS 4
+#define BNB_TC_CONV_WARPS 8
 #endif
 constexpr int kConvWarps = BNB_TC_CONV_WARPS;
-static_assert(kConvWarps == 2 || kConvWarps == 4, "2 or 4 converter warps");
-constexpr int kConvWarp0 = kConvWarps == 2 ? 2 : 4;
-constexpr int kConvRows = kBM / (kConvWarps * 32);  // weight rows per converter thread
-constexpr int kEpiWarp0 = kConvWarps == 2 ? 4 : 8, kEpiWarps = 16;
+static_assert(kConvWarps == 4 || kConvWarps == 8, "4 or 8 converter warps");
+constexpr int kConvWarp0 = 4;
+constexpr int kConvThreadsPerRow = kConvWarps * 32 / kBM;  // 1 or 2
+constexpr int kEpiWarp0 = kConvWarp0 + kConvWarps, kEpiWarps = 16;
 constexpr int kThreads = (kEpiWarp0 + kEpiWarps) * 32;
 // Register split; the sum never exceeds the launch's threads x registers
-// (640 x 96 or 768 x 80, what ptxas grants under __launch_bounds__(kThreads, 1)).
-constexpr int kRegsWG0 = kConvWarps == 2 ? 64 : 32;
-constexpr int kRegsConv = 64;  // warpgroup 1 when it holds the converters
-constexpr int kRegsEpi = kConvWarps == 2 ? 104 : 96;
-static_assert(kConvWarps == 2 ? 128 * kRegsWG0 + 512 * kRegsEpi <= 640 * 96
-                              : 128 * kRegsWG0 + 128 * kRegsConv + 512 * kRegsEpi <= 768 * 80,
+// (768 x 80 or 896 x 72, what ptxas grants under __launch_bounds__(kThreads, 1)).
+constexpr int kRegsWG0 = 32;
+constexpr int kRegsConv = kConvWarps == 4 ? 64 : 40;  // each converter warpgroup
+constexpr int kRegsEpi = 96;
+static_assert(128 * kRegsWG0 + 32 * kConvWarps * kRegsConv + 512 * kRegsEpi <=
+                  kThreads * (kConvWarps == 4 ? 80 : 72),
               "register split exceeds the launch budget");
 constexpr int kWhBytes = kBM * kBK * 2;  // A operand tile (fp16)
 constexpr int kWqBytes = kBM * kBK;      // int8 weight tile
@@ -206,7 +208,8 @@ __device__ __forceinline__ void widen16(const uint4 &v, uint4 &g0, uint4 &g1) {
 // stages when only the int8 weight is kept.  In the other outlier stages TMA
 // has put the fp16 A tile there already (W16, or the compacted outlier
 // columns); the converters only pass the stage on to the MMA.
-// Thread ct owns weight rows ct, ct + 32 * kConvWarps, ...  In a bf16
+// Thread ct owns weight row ct / kConvThreadsPerRow, 16-byte chunks
+// [4 / kConvThreadsPerRow * (ct % kConvThreadsPerRow), ...).  In a bf16
 // layer the outlier stages' codes are widened to bf16 integers instead
 // (exact), so that both MMA operands have X's format.
 template <bool kBf, int kBNt>
@@ -225,14 +228,14 @@ __device__ __forceinline__ void converter_role(uint8_t *smem, TcSmem &sm, const 
         break;
       }
       if (s < s_conv) {
-#pragma unroll
-        for (int h = 0; h < kConvRows; ++h) {
-          const int r = ct + kConvWarps * 32 * h;
+        {
+          constexpr int kQ = 4 / kConvThreadsPerRow;  // 16-byte chunks per thread
+          const int r = ct / kConvThreadsPerRow, q0 = kQ * (ct % kConvThreadsPerRow);
           // int8 row r: 64 bytes, 16-byte chunk q stored at q ^ ((r >> 1) & 3)
           const uint8_t *wq = stage_wq<kBNt>(smem, st) + r * 64;
           uint8_t *wh = stage_wh<kBNt>(smem, st) + r * 128;
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
+          for (int q = q0; q < q0 + kQ; ++q) {
             const uint4 v = *reinterpret_cast<const uint4 *>(wq + 16 * (q ^ ((r >> 1) & 3)));
             uint4 g0, g1;
             widen16(v, g0, g1);
@@ -397,9 +400,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       tmem_dealloc(tmem, kTmemCols);
     }
-    if (kConvWarps == 2 && warp >= kConvWarp0)
-      converter_role<kBf, kBNt>(smem, sm, p, s_int, s_conv, nst, ntiles);
-  } else if (kConvWarps == 4 && warp < kEpiWarp0) {
+  } else if (warp < kEpiWarp0) {
     regs_dec<kRegsConv>();
     converter_role<kBf, kBNt>(smem, sm, p, s_int, s_conv, nst, ntiles);
   } else {
