@@ -332,6 +332,9 @@ int bnb_int8_linear_path(int64_t T, int64_t N, int64_t K);
  *                       work has completed.
  *   BNB_OPT_LEGACY_MMA  T > 16 path: the warp-level mma.sync GEMM (sm_80-style
  *                       tensor path, for comparison) instead of tcgen05.
+ *   BNB_OPT_SINGLE_CTA  T > 32 on the tcgen05 GEMM: each 128 x 256 tile on
+ *                       one CTA (cta_group::1) instead of 256 x 256 tiles on
+ *                       CTA pairs (cta_group::2), for comparison.
  *   BNB_OPT_CLUSTER(c)  decode path: thread-block clusters of c CTAs (c = 4,
  *                       8 or 16) sharing one activation pass, instead of the
  *                       size the library picks, when clusters of that size
@@ -352,6 +355,7 @@ int bnb_int8_linear_path(int64_t T, int64_t N, int64_t K);
 #define BNB_OPT_NO_PDL 0x4u
 #define BNB_OPT_LEGACY_MMA 0x8u
 #define BNB_OPT_FORCE_TIMEOUT 0x10u
+#define BNB_OPT_SINGLE_CTA 0x20u
 #define BNB_OPT_CLUSTER(c) ((uint32_t)(c) << 8)
 bnb_status_t bnb_int8_linear_opts(const void *X, int64_t T, int64_t K, const int8_t *Wq,
                                   const float *Wscale, const void *W16, const void *bias,

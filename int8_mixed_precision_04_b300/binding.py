@@ -358,6 +358,7 @@ OPT_ACT_ONLY = 0x2
 OPT_NO_PDL = 0x4
 OPT_LEGACY_MMA = 0x8
 OPT_FORCE_TIMEOUT = 0x10
+OPT_SINGLE_CTA = 0x20
 
 
 def OPT_CLUSTER(c: int) -> int:

@@ -414,7 +414,8 @@ bnb_status_t bnb_int8_linear_opts(const void *X, int64_t T, int64_t K, const int
                                   int32_t *acc, uint32_t opts) {
   if (dtype != BNB_DTYPE_FP16 && dtype != BNB_DTYPE_BF16) return BNB_ERR_INVALID_ARG;
   constexpr uint32_t kKnown = BNB_OPT_MAIN_ONLY | BNB_OPT_ACT_ONLY | BNB_OPT_NO_PDL |
-                              BNB_OPT_LEGACY_MMA | BNB_OPT_FORCE_TIMEOUT | BNB_OPT_CLUSTER(0xff);
+                              BNB_OPT_LEGACY_MMA | BNB_OPT_FORCE_TIMEOUT | BNB_OPT_SINGLE_CTA |
+                              BNB_OPT_CLUSTER(0xff);
   if (opts & ~kKnown) return BNB_ERR_INVALID_ARG;
   const uint32_t c = (opts >> 8) & 0xffu;
   if (c != 0 && c != 4 && c != 8 && c != 16) return BNB_ERR_INVALID_ARG;

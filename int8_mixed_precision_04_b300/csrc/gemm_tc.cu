@@ -50,6 +50,8 @@
 // memory is freed.
 #include <cuda.h>
 
+#include <atomic>
+
 #include "common.cuh"
 #include "kernels.h"
 #include "sm100_ptx.cuh"
@@ -86,28 +88,40 @@ static_assert(128 * kRegsWG0 + 32 * kConvWarps * kRegsConv + 512 * kRegsEpi <=
 constexpr int kWhBytes = kBM * kBK * 2;  // A operand tile (fp16)
 constexpr int kWqBytes = kBM * kBK;      // int8 weight tile
 
-// The token tile: 256 tokens for T > 32 (4 pipeline stages); 32 tokens for
-// decode-sized T (T <= 32), where a 256-token tile would spend almost every
-// MMA on padding rows: its small activation tile leaves room for 8 stages, so
-// that more of the weight stream is in flight.
-template <int kBNt>
+// The token tile: 256 tokens for T > 32; 32 tokens for decode-sized T
+// (T <= 32), where a 256-token tile would spend almost every MMA on padding
+// rows: its small activation tile leaves room for 8 stages, so that more of
+// the weight stream is in flight.
+// kPairT: the tile is computed by a CTA pair (a cluster of two, tcgen05
+// cta_group::2): MMA M = 256 output channels, 128 from each CTA's own weight
+// rows, and each CTA loads only its half of the token rows (MMA N); the
+// even CTA issues the MMAs for both.  Each SM then stages 40 KB per 64-column
+// stage instead of 56 KB (the activation tile is shared through the pair),
+// which leaves room for 5 stages and halves the activation bytes each SM
+// reads from L2 and writes into shared memory.
+template <int kBNt, bool kPairT = false>
 struct Tile {
+  static constexpr bool kPair = kPairT;
+  static constexpr int kCtas = kPair ? 2 : 1;
   static constexpr int kBN = kBNt;                      // tokens per tile (MMA N)
-  static constexpr int kStages = kBNt == 256 ? 4 : 8;
+  static constexpr int kBNc = kBNt / kCtas;             // token rows this CTA loads
+  static constexpr int kBMt = kBM * kCtas;              // output channels per tile (MMA M)
   static constexpr int kEpiCols = kBN / 4;              // columns per epilogue thread
   static constexpr uint32_t kTmemCols = 2 * kBN < 32 ? 32 : 2 * kBN;  // two fp32 buffers
-  static constexpr int kXBytes = kBN * kBK * 2;         // B operand tile (fp16)
+  static constexpr int kXBytes = kBNc * kBK * 2;        // this CTA's B operand rows (fp16)
   static constexpr int kStageBytes = kXBytes + kWhBytes + kWqBytes;
+  static constexpr int kStages =
+      (232448 - 2048) / kStageBytes < kMaxStages ? (232448 - 2048) / kStageBytes : kMaxStages;
   static constexpr size_t kSmemBytes = (size_t)kStages * kStageBytes + 1024;
   // Instruction descriptor of kind::f16: D fp32, A and B fp16, both K-major,
-  // N = kBN, M = kBM.
+  // N = kBN, M = kBMt.
   static constexpr uint32_t kIdesc =
-      (1u << 4) | ((uint32_t)(kBN >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
+      (1u << 4) | ((uint32_t)(kBN >> 3) << 17) | ((uint32_t)(kBMt >> 4) << 24);
   // The same with A and B bf16 (format fields 1), for the outlier stages of a
   // bf16 layer; the int8 stages always multiply fp16 integer codes.
   static constexpr uint32_t kIdescBf16 = kIdesc | (1u << 7) | (1u << 10);
   static_assert(kStageBytes % 1024 == 0, "stages must keep 1024-byte swizzle alignment");
-  static_assert(kStages <= kMaxStages && kSmemBytes <= 232448 - 1024, "shared memory");
+  static_assert(kStages >= 4 && kSmemBytes <= 232448 - 1024, "shared memory");
   static_assert(kEpiCols % 8 == 0 && (kTmemCols & (kTmemCols - 1)) == 0, "tile geometry");
 };
 
@@ -151,17 +165,17 @@ struct TcSmem {
   int abort;
 };
 
-template <int kBNt>
+template <class Tl>
 __device__ __forceinline__ uint8_t *stage_x(uint8_t *s, int st) {
-  return s + st * Tile<kBNt>::kStageBytes;
+  return s + st * Tl::kStageBytes;
 }
-template <int kBNt>
+template <class Tl>
 __device__ __forceinline__ uint8_t *stage_wh(uint8_t *s, int st) {
-  return s + st * Tile<kBNt>::kStageBytes + Tile<kBNt>::kXBytes;
+  return s + st * Tl::kStageBytes + Tl::kXBytes;
 }
-template <int kBNt>
+template <class Tl>
 __device__ __forceinline__ uint8_t *stage_wq(uint8_t *s, int st) {
-  return s + st * Tile<kBNt>::kStageBytes + Tile<kBNt>::kXBytes + kWhBytes;
+  return s + st * Tl::kStageBytes + Tl::kXBytes + kWhBytes;
 }
 
 // All lanes wait (each acquires the barrier's phase); the outcome is made
@@ -212,15 +226,16 @@ __device__ __forceinline__ void widen16(const uint4 &v, uint4 &g0, uint4 &g1) {
 // [4 / kConvThreadsPerRow * (ct % kConvThreadsPerRow), ...).  In a bf16
 // layer the outlier stages' codes are widened to bf16 integers instead
 // (exact), so that both MMA operands have X's format.
-template <bool kBf, int kBNt>
+template <bool kBf, class Tl>
 __device__ __forceinline__ void converter_role(uint8_t *smem, TcSmem &sm, const TcArgs &p,
-                                               int s_int, int s_conv, int nst, int ntiles) {
-  constexpr int kStages = Tile<kBNt>::kStages;
+                                               int s_int, int s_conv, int nst, int ntiles,
+                                               int cid, int ncl) {
+  constexpr int kStages = Tl::kStages;
   const int ct = threadIdx.x - kConvWarp0 * 32;  // 0 .. 32 * kConvWarps - 1
   const int lane = threadIdx.x & 31;
   uint32_t it = 0;
   bool ok = true;
-  for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+  for (int tile = cid; tile < ntiles && ok; tile += ncl) {
     for (int s = 0; s < nst; ++s, ++it) {
       const int st = it % kStages;
       if (!warp_wait(&sm.full[st], (it / kStages) & 1u, sm, p.status)) {
@@ -228,56 +243,79 @@ __device__ __forceinline__ void converter_role(uint8_t *smem, TcSmem &sm, const 
         break;
       }
       if (s < s_conv) {
-        {
-          constexpr int kQ = 4 / kConvThreadsPerRow;  // 16-byte chunks per thread
-          const int r = ct / kConvThreadsPerRow, q0 = kQ * (ct % kConvThreadsPerRow);
-          // int8 row r: 64 bytes, 16-byte chunk q stored at q ^ ((r >> 1) & 3)
-          const uint8_t *wq = stage_wq<kBNt>(smem, st) + r * 64;
-          uint8_t *wh = stage_wh<kBNt>(smem, st) + r * 128;
+        constexpr int kQ = 4 / kConvThreadsPerRow;  // 16-byte chunks per thread
+        const int r = ct / kConvThreadsPerRow, q0 = kQ * (ct % kConvThreadsPerRow);
+        // int8 row r: 64 bytes, 16-byte chunk q stored at q ^ ((r >> 1) & 3)
+        const uint8_t *wq = stage_wq<Tl>(smem, st) + r * 64;
+        uint8_t *wh = stage_wh<Tl>(smem, st) + r * 128;
 #pragma unroll
-          for (int q = q0; q < q0 + kQ; ++q) {
-            const uint4 v = *reinterpret_cast<const uint4 *>(wq + 16 * (q ^ ((r >> 1) & 3)));
-            uint4 g0, g1;
-            widen16(v, g0, g1);
-            if (kBf && s >= s_int) {
-              to_bf16x2(g0.x); to_bf16x2(g0.y); to_bf16x2(g0.z); to_bf16x2(g0.w);
-              to_bf16x2(g1.x); to_bf16x2(g1.y); to_bf16x2(g1.z); to_bf16x2(g1.w);
-            }
-            *reinterpret_cast<uint4 *>(wh + 16 * ((2 * q) ^ (r & 7))) = g0;
-            *reinterpret_cast<uint4 *>(wh + 16 * ((2 * q + 1) ^ (r & 7))) = g1;
+        for (int q = q0; q < q0 + kQ; ++q) {
+          const uint4 v = *reinterpret_cast<const uint4 *>(wq + 16 * (q ^ ((r >> 1) & 3)));
+          uint4 g0, g1;
+          widen16(v, g0, g1);
+          if (kBf && s >= s_int) {
+            to_bf16x2(g0.x); to_bf16x2(g0.y); to_bf16x2(g0.z); to_bf16x2(g0.w);
+            to_bf16x2(g1.x); to_bf16x2(g1.y); to_bf16x2(g1.z); to_bf16x2(g1.w);
           }
+          *reinterpret_cast<uint4 *>(wh + 16 * ((2 * q) ^ (r & 7))) = g0;
+          *reinterpret_cast<uint4 *>(wh + 16 * ((2 * q + 1) ^ (r & 7))) = g1;
         }
       }
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.conv[st]);
+      if (lane == 0) {
+        // a pair's MMAs are issued by the even CTA: both CTAs' stages are
+        // counted on its barrier
+        if constexpr (Tl::kPair) mbar_arrive_remote(mapa(smem_addr(&sm.conv[st]), 0));
+        else mbar_arrive(&sm.conv[st]);
+      }
     }
   }
 }
 
-template <bool kBf, int kBNt>
+// Every thread of both CTAs of a pair passes this once, as the last thing it
+// does: no CTA leaves while the other may still read its shared memory
+// (MMA operands) or arrive on its barriers.
+__device__ __forceinline__ void pair_exit() {
+  __syncwarp();
+  cluster_arrive();
+  cluster_wait();
+}
+
+template <bool kBf, int kBNt, bool kPair>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
                    const __grid_constant__ CUtensorMap tm_xo, const __grid_constant__ CUtensorMap tm_w16,
                    const __grid_constant__ CUtensorMap tm_w16o, const TcArgs p) {
-  using Tl = Tile<kBNt>;
-  constexpr int kBN = Tl::kBN, kStages = Tl::kStages, kEpiCols = Tl::kEpiCols;
-  constexpr int kXBytes = Tl::kXBytes;
+  using Tl = Tile<kBNt, kPair>;
+  constexpr int kBN = Tl::kBN, kBNc = Tl::kBNc, kBMt = Tl::kBMt, kStages = Tl::kStages;
+  constexpr int kEpiCols = Tl::kEpiCols, kXBytes = Tl::kXBytes, kG = Tl::kCtas;
   constexpr uint32_t kTmemCols = Tl::kTmemCols, kIdesc = Tl::kIdesc, kIdescBf16 = Tl::kIdescBf16;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   __shared__ TcSmem sm;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // the tile walk: one CTA, or one pair (cluster), per unit
+  uint32_t rank = 0;
+  int cid = blockIdx.x, ncl = gridDim.x;
+  if constexpr (kPair) {
+    uint32_t c, nc;
+    asm("mov.u32 %0, %%cluster_ctarank;" : "=r"(rank));
+    asm("mov.u32 %0, %%clusterid.x;" : "=r"(c));
+    asm("mov.u32 %0, %%nclusterid.x;" : "=r"(nc));
+    cid = (int)c;
+    ncl = (int)nc;
+  }
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; i++) {
       mbar_init(&sm.full[i], 1);
-      mbar_init(&sm.conv[i], kConvWarps);
+      mbar_init(&sm.conv[i], kConvWarps * kG);
       mbar_init(&sm.empty[i], 1);
     }
     for (int b = 0; b < 2; b++) {
       mbar_init(&sm.accf[b], 1);
-      mbar_init(&sm.acce[b], kEpiWarps);
+      mbar_init(&sm.acce[b], kEpiWarps * kG);
     }
     mbar_init(&sm.fin, 1);
     mbar_init(&sm.done, kEpiWarps);
@@ -293,11 +331,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tm_w16o);
   }
   if (warp == 1) {
-    tmem_alloc(&sm.tmem_base, kTmemCols);
-    tmem_relinquish();
+    tmem_alloc<kG>(&sm.tmem_base, kTmemCols);
+    tmem_relinquish<kG>();
   }
   tc_fence_before();
-  __syncthreads();
+  if constexpr (kPair) {
+    // both CTAs' barriers are initialised before either arrives on the other's
+    cluster_arrive();
+    cluster_wait();
+  } else {
+    __syncthreads();
+  }
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
 
@@ -324,8 +368,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0 && lane == 0) {
       uint32_t it = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
-        const int t0 = (tile % p.t_tiles) * kBN, n0 = (tile / p.t_tiles) * kBM;
+      for (int tile = cid; tile < ntiles && ok; tile += ncl) {
+        // this CTA's token rows and weight rows of the tile
+        const int t0 = (tile % p.t_tiles) * kBN + (int)rank * kBNc;
+        const int n0 = (tile / p.t_tiles) * kBMt + (int)rank * kBM;
         for (int s = 0; s < nst; ++s, ++it) {
           const int st = it % kStages;
           const uint32_t ph = (it / kStages) & 1u;
@@ -335,16 +381,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (s < s_int) {
             mbar_expect_tx(&sm.full[st], kXBytes + kWqBytes);
-            tma_load_2d(stage_x<kBNt>(smem, st), &tm_x, s * kBK, t0, &sm.full[st]);
-            tma_load_2d(stage_wq<kBNt>(smem, st), &tm_w, s * kBK, n0, &sm.full[st]);
+            tma_load_2d(stage_x<Tl>(smem, st), &tm_x, s * kBK, t0, &sm.full[st]);
+            tma_load_2d(stage_wq<Tl>(smem, st), &tm_w, s * kBK, n0, &sm.full[st]);
           } else if (wq_out) {  // outlier stage on the int8 weight tile
             mbar_expect_tx(&sm.full[st], kXBytes + kWqBytes);
-            tma_load_2d(stage_x<kBNt>(smem, st), &tm_xo, (s - s_int) * kBK, t0, &sm.full[st]);
-            tma_load_2d(stage_wq<kBNt>(smem, st), &tm_w, (s - s_int) * kBK, n0, &sm.full[st]);
+            tma_load_2d(stage_x<Tl>(smem, st), &tm_xo, (s - s_int) * kBK, t0, &sm.full[st]);
+            tma_load_2d(stage_wq<Tl>(smem, st), &tm_w, (s - s_int) * kBK, n0, &sm.full[st]);
           } else {  // outlier stage: fp16 A tile straight into the A operand slot
             mbar_expect_tx(&sm.full[st], kXBytes + kWhBytes);
-            tma_load_2d(stage_x<kBNt>(smem, st), &tm_xo, (s - s_int) * kBK, t0, &sm.full[st]);
-            tma_load_2d(stage_wh<kBNt>(smem, st), dense ? &tm_w16 : &tm_w16o, (s - s_int) * kBK, n0,
+            tma_load_2d(stage_x<Tl>(smem, st), &tm_xo, (s - s_int) * kBK, t0, &sm.full[st]);
+            tma_load_2d(stage_wh<Tl>(smem, st), dense ? &tm_w16 : &tm_w16o, (s - s_int) * kBK, n0,
                         &sm.full[st]);
           }
         }
@@ -353,18 +399,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (uint32_t j = it > (uint32_t)kStages ? it - kStages : 0; j < it; ++j)
         mbar_wait_bounded(&sm.full[j % kStages], (j / kStages) & 1u, p.status);
     }
-    // ---------------- MMA issuer ----------------
-    if (warp == 1 && lane == 0) {
+    // ---------------- MMA issuer (the even CTA of a pair) ----------------
+    if (warp == 1 && lane == 0 && rank == 0) {
       uint32_t it = 0, g = 0;
       bool ok = true;
       const int nci = (s_int + kChunkStages - 1) / kChunkStages;
       const int nchunks = nci + (s_out > 0 ? 1 : 0);
-      for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+      for (int tile = cid; tile < ntiles && ok; tile += ncl) {
         int s = 0;
         for (int c = 0; c < nchunks && ok; ++c, ++g) {
           const int s_end = c < nci ? min(s_int, (c + 1) * kChunkStages) : nst;
           const uint32_t buf = g & 1u;
-          if (!mbar_wait_abortable(&sm.acce[buf], ((g >> 1) & 1u) ^ 1u, &sm.abort, p.status)) {
+          if (!mbar_wait_abortable(&sm.acce[buf], ((g >> 1) & 1u) ^ 1u, &sm.abort,
+                                          p.status)) {
             ok = false;
             break;
           }
@@ -373,36 +420,43 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int s0 = s;
           for (; s < s_end; ++s, ++it) {
             const int st = it % kStages;
-            if (!mbar_wait_abortable(&sm.conv[st], (it / kStages) & 1u, &sm.abort, p.status)) {
+            if (!mbar_wait_abortable(&sm.conv[st], (it / kStages) & 1u, &sm.abort,
+                                            p.status)) {
               ok = false;
               break;
             }
             tc_fence_after();
-            const uint64_t ad = sw128_desc(smem_addr(stage_wh<kBNt>(smem, st)));
-            const uint64_t bd = sw128_desc(smem_addr(stage_x<kBNt>(smem, st)));
+            const uint64_t ad = sw128_desc(smem_addr(stage_wh<Tl>(smem, st)));
+            const uint64_t bd = sw128_desc(smem_addr(stage_x<Tl>(smem, st)));
 #pragma unroll
             for (int k = 0; k < kBK / 16; ++k)  // 16 fp16 = 32 bytes per MMA
-              umma_f16(d, ad + 2 * k, bd + 2 * k, kBf && s >= s_int ? kIdescBf16 : kIdesc,
-                       (s > s0 || k > 0) ? 1u : 0u);
-            umma_commit(&sm.empty[st]);
+              umma_f16<kG>(d, ad + 2 * k, bd + 2 * k, kBf && s >= s_int ? kIdescBf16 : kIdesc,
+                           (s > s0 || k > 0) ? 1u : 0u);
+            umma_commit<kG>(&sm.empty[st]);
           }
-          if (ok) umma_commit(&sm.accf[buf]);
+          if (ok) umma_commit<kG>(&sm.accf[buf]);
         }
       }
       // every MMA issued above has completed before tensor memory is freed
-      umma_commit(&sm.fin);
+      umma_commit<kG>(&sm.fin);
       mbar_wait_bounded(&sm.fin, 0, p.status);
     }
     if (warp == 1) {
-      // free tensor memory once every epilogue warp is done reading it
+      // free tensor memory once every epilogue warp is done reading it (and,
+      // in a pair, once the even CTA's MMAs into it have completed)
       __syncwarp();
       mbar_wait_bounded(&sm.done, 0, p.status);
+      if (kPair && rank != 0) mbar_wait_cluster_bounded(&sm.fin, 0, p.status);
+      if constexpr (kPair) pair_exit();
       tc_fence_after();
-      tmem_dealloc(tmem, kTmemCols);
+      tmem_dealloc<kG>(tmem, kTmemCols);
+    } else if constexpr (kPair) {
+      pair_exit();
     }
   } else if (warp < kEpiWarp0) {
     regs_dec<kRegsConv>();
-    converter_role<kBf, kBNt>(smem, sm, p, s_int, s_conv, nst, ntiles);
+    converter_role<kBf, Tl>(smem, sm, p, s_int, s_conv, nst, ntiles, cid, ncl);
+    if constexpr (kPair) pair_exit();
   } else {
     regs_inc<kRegsEpi>();
     // ---------------- epilogue ----------------
@@ -411,6 +465,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_field = (uint32_t)(32 * quad) << 16;
     const int64_t T = p.T, N = p.N;
     const int nci = (s_int + kChunkStages - 1) / kChunkStages;
+    // where this warp reports a drained buffer: the MMA issuer's CTA
+    const uint32_t acce_at = kPair ? mapa(smem_addr(&sm.acce[0]), 0) : smem_addr(&sm.acce[0]);
     uint32_t g = 0;
     bool ok = true;
     if (p.force_timeout && e == 0) {
@@ -420,9 +476,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __all_sync(0xffffffffu, mbar_wait_abortable(&sm.never, 0, &sm.abort, p.status,
                                                         kForcedWaitNs));
     }
-    for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
+    for (int tile = cid; tile < ntiles && ok; tile += ncl) {
       const int64_t t0 = (int64_t)(tile % p.t_tiles) * kBN + part * kEpiCols;
-      const int64_t n = (int64_t)(tile / p.t_tiles) * kBM + 32 * quad + lane;
+      const int64_t n = (int64_t)(tile / p.t_tiles) * kBMt + (int64_t)rank * kBM + 32 * quad + lane;
       int acc[kEpiCols];
       for (int c = 0; c < nci; ++c, ++g) {
         const uint32_t buf = g & 1u;
@@ -445,7 +501,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.acce[buf]);
+        if (lane == 0) {
+          if constexpr (kPair) mbar_arrive_remote(acce_at + buf * 8);
+          else mbar_arrive(&sm.acce[buf]);
+        }
       }
       if (!ok) break;
       if (p.dbg_acc && n < N) {
@@ -507,28 +566,62 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (has_out) {
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.acce[obuf]);
+        if (lane == 0) {
+          if constexpr (kPair) mbar_arrive_remote(acce_at + obuf * 8);
+          else mbar_arrive(&sm.acce[obuf]);
+        }
         ++g;
       }
     }
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive(&sm.done);
+    if constexpr (kPair) pair_exit();
   }
   // No block-wide barrier follows: the warpgroups run under different
-  // register budgets and leave independently.
+  // register budgets and leave independently (a pair's CTAs after one
+  // cluster barrier that every thread of both passes in its own branch).
 }
 
 // ---- host side ----------------------------------------------------------------
 
-template <int kBNt>
+// CTA pairs of the pair kernels that are resident at once on device `dev`
+// (the persistent grid), queried once per device; 0 if the query fails.
+int pair_clusters(int dev) {
+  static std::atomic<int> cache[64];
+  if (dev < 0 || dev >= 64) return 0;
+  int n = cache[dev].load(std::memory_order_relaxed);
+  if (n > 0) return n;
+  using Tl = Tile<256, true>;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * 512);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = Tl::kSmemBytes;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int least = 1 << 30;
+  for (auto *f : {gemm_tc_kernel<false, 256, true>, gemm_tc_kernel<true, 256, true>}) {
+    int c = 0;
+    if (cudaOccupancyMaxActiveClusters(&c, f, &cfg) != cudaSuccess) c = 0;
+    least = c < least ? c : least;  // both forms must fit
+  }
+  if (least > 0) cache[dev].store(least, std::memory_order_relaxed);
+  return least;
+}
+
+template <int kBNt, bool kPair>
 cudaError_t launch_tc(int64_t T, int64_t K, const int8_t *Wq, const float *sw, const void *W16,
                       const void *bias, int64_t N, bool bf16, void *Y, const Workspace &ws,
                       int32_t *dbg_acc, int num_sms, uint32_t opts, cudaStream_t stream) {
-  using Tl = Tile<kBNt>;
+  using Tl = Tile<kBNt, kPair>;
   static bool attr_set = false;  // benign race: every writer sets the same value
   if (!attr_set) {
-    for (auto *f : {gemm_tc_kernel<false, kBNt>, gemm_tc_kernel<true, kBNt>}) {
+    for (auto *f : {gemm_tc_kernel<false, kBNt, kPair>, gemm_tc_kernel<true, kBNt, kPair>}) {
       cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            (int)Tl::kSmemBytes);
       if (e != cudaSuccess) return e;
@@ -540,12 +633,12 @@ cudaError_t launch_tc(int64_t T, int64_t K, const int8_t *Wq, const float *sw, c
       bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   CUtensorMap tm_x, tm_w, tm_xo, tm_w16, tm_w16o;
   if (!encode_2d(&tm_x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, ws.xcodes, (uint64_t)K, (uint64_t)T,
-                 (uint64_t)K * 2, kBK, kBNt, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B) ||
+                 (uint64_t)K * 2, kBK, Tl::kBNc, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B) ||
       !encode_2d(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, Wq, (uint64_t)K, (uint64_t)N, (uint64_t)K,
                  kBK, kBM, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B) ||
       // the outlier block's inner extent is K (columns past K read as zeros)
       !encode_2d(&tm_xo, e16, ws.xo, (uint64_t)K, (uint64_t)T,
-                 (uint64_t)ws.kpad * 2, kBK, kBNt, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B) ||
+                 (uint64_t)ws.kpad * 2, kBK, Tl::kBNc, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B) ||
       // without W16 this map is never read; it then describes the compacted columns
       !(W16 ? encode_2d(&tm_w16, e16, W16, (uint64_t)K, (uint64_t)N,
                         (uint64_t)K * 2, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -561,7 +654,7 @@ cudaError_t launch_tc(int64_t T, int64_t K, const int8_t *Wq, const float *sw, c
   a.K = K;
   a.N = N;
   a.t_tiles = (int)((T + kBNt - 1) / kBNt);
-  a.n_tiles = (int)((N + kBM - 1) / kBM);
+  a.n_tiles = (int)((N + Tl::kBMt - 1) / Tl::kBMt);
   a.s_int = (int)((K + kBK - 1) / kBK);
   a.sw = sw;
   a.W16 = reinterpret_cast<const unsigned short *>(W16);
@@ -574,20 +667,38 @@ cudaError_t launch_tc(int64_t T, int64_t K, const int8_t *Wq, const float *sw, c
   a.status = ws.status;
   a.force_timeout = (opts & BNB_OPT_FORCE_TIMEOUT) ? 1 : 0;
   const int64_t tiles = (int64_t)a.t_tiles * a.n_tiles;
-  const unsigned grid = (unsigned)(tiles < num_sms ? tiles : num_sms);
+  int units = num_sms;  // persistent CTAs, or CTA pairs
+  if (kPair) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+    units = pair_clusters(dev);
+    if (units <= 0) return cudaErrorInvalidConfiguration;
+  }
+  const unsigned grid = (unsigned)(tiles < units ? tiles : units) * Tl::kCtas;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = Tl::kSmemBytes;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  if (kPair) {
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = 2;
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
+  }
+  if (!(opts & BNB_OPT_NO_PDL)) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = (opts & BNB_OPT_NO_PDL) ? 0 : 1;
+  cfg.numAttrs = na;
   const cudaError_t e = cudaLaunchKernelEx(
-      &cfg, bf16 ? gemm_tc_kernel<true, kBNt> : gemm_tc_kernel<false, kBNt>, tm_x, tm_w, tm_xo,
-      tm_w16, tm_w16o, a);
+      &cfg, bf16 ? gemm_tc_kernel<true, kBNt, kPair> : gemm_tc_kernel<false, kBNt, kPair>, tm_x,
+      tm_w, tm_xo, tm_w16, tm_w16o, a);
   note_launch();
   return e;
 }
@@ -598,10 +709,16 @@ cudaError_t launch_gemm_tc(int64_t T, int64_t K, const int8_t *Wq, const float *
                            const void *W16, const void *bias, int64_t N, bool bf16, void *Y,
                            const Workspace &ws, int32_t *dbg_acc, int num_sms, uint32_t opts,
                            cudaStream_t stream) {
-  // decode-sized calls take the 32-token tile (kGemmSmallT), the rest the 256-token one
+  // decode-sized calls take the 32-token tile (kGemmSmallT), the rest the
+  // 256-token one on CTA pairs (on single CTAs with BNB_OPT_SINGLE_CTA)
   if (T <= kGemmSmallT)
-    return launch_tc<32>(T, K, Wq, sw, W16, bias, N, bf16, Y, ws, dbg_acc, num_sms, opts, stream);
-  return launch_tc<256>(T, K, Wq, sw, W16, bias, N, bf16, Y, ws, dbg_acc, num_sms, opts, stream);
+    return launch_tc<32, false>(T, K, Wq, sw, W16, bias, N, bf16, Y, ws, dbg_acc, num_sms, opts,
+                                stream);
+  if (opts & BNB_OPT_SINGLE_CTA)
+    return launch_tc<256, false>(T, K, Wq, sw, W16, bias, N, bf16, Y, ws, dbg_acc, num_sms, opts,
+                                 stream);
+  return launch_tc<256, true>(T, K, Wq, sw, W16, bias, N, bf16, Y, ws, dbg_acc, num_sms, opts,
+                              stream);
 }
 
 }  // namespace bnb

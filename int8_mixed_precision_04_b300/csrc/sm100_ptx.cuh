@@ -42,6 +42,27 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
   return ok != 0;
 }
 
+// mbarrier wait whose acquire covers writes made by other CTAs of the cluster.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Arrival on the mbarrier at cluster address `caddr` (mapa), possibly in
+// another CTA of the cluster.  Default (CTA-scope) release: the pipelines
+// that use it hand over shared-memory operands read by the tensor core and
+// tensor-memory buffers, ordered by the proxy and tcgen05 fences around the
+// barrier; a cluster-scope release on every stage was measured to halve the
+// GEMM's throughput.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t caddr) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(caddr) : "memory");
+}
+
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // every device-side wait gives up after ~2 s
 
 // Wait with a time limit; on expiry record a timeout in the workspace status
@@ -122,22 +143,39 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 
 // ---- tcgen05 ----------------------------------------------------------------
 
-// Tensor-memory allocation; executed by one whole warp.  The base address is
-// written to *slot (shared memory).
+// Tensor-memory allocation; executed by one whole warp (kG = 1), or by one
+// warp in each CTA of a pair together (kG = 2: the cta_group::2 forms, which a
+// kernel uses for all its tcgen05 allocation, MMA and commit instructions).
+// The base address is written to *slot (shared memory).
+template <int kG = 1>
 __device__ __forceinline__ void tmem_alloc(uint32_t *slot, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                   smem_addr(slot)),
-               "r"(ncols)
-               : "memory");
+  if constexpr (kG == 1)
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_addr(slot)),
+                 "r"(ncols)
+                 : "memory");
+  else
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_addr(slot)),
+                 "r"(ncols)
+                 : "memory");
 }
+template <int kG = 1>
 __device__ __forceinline__ void tmem_relinquish() {
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  if constexpr (kG == 1)
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  else
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
 }
+template <int kG = 1>
 __device__ __forceinline__ void tmem_dealloc(uint32_t base, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(base), "r"(ncols)
-               : "memory");
+  if constexpr (kG == 1)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(base), "r"(ncols)
+                 : "memory");
+  else
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(base), "r"(ncols)
+                 : "memory");
 }
-
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
@@ -146,22 +184,42 @@ __device__ __forceinline__ void tc_fence_after() {
 }
 
 // D[tmem] (+)= A[smem desc] x B[smem desc]^T, fp16 inputs, fp32 accumulate.
+// kG = 2: issued by the even CTA of a pair for both; A's rows and B's rows
+// (the N dimension) come half from each CTA's shared memory at the same
+// offsets, and each CTA's tensor memory receives its own half of D's rows.
+template <int kG = 1>
 __device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
                                          uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
+  if constexpr (kG == 1)
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+  else
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
 }
 
 // `bar` receives one arrival when every tcgen05 operation issued so far by
-// this thread has completed.
+// this thread has completed.  kG = 2: the mbarrier at the same offset in both
+// CTAs of the pair receives it.
+template <int kG = 1>
 __device__ __forceinline__ void umma_commit(uint64_t *bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-          smem_addr(bar))
-      : "memory");
+  if constexpr (kG == 1)
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+            smem_addr(bar))
+        : "memory");
+  else
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;" ::"r"(smem_addr(bar)),
+        "h"((uint16_t)3)
+        : "memory");
 }
 
 // 32 lanes x 16 consecutive 32-bit columns: thread i of the warp receives
@@ -228,17 +286,6 @@ __device__ __forceinline__ void st_async_v4(uint32_t raddr, uint32_t a, uint32_t
       "[%5];" ::"r"(raddr),
       "r"(a), "r"(b), "r"(c), "r"(d), "r"(rbar)
       : "memory");
-}
-// mbarrier wait whose acquire covers writes made by other CTAs of the cluster.
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
-      " selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(smem_addr(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
 }
 __device__ __forceinline__ bool mbar_wait_cluster_bounded(uint64_t *bar, uint32_t parity,
                                                           int32_t *status) {

@@ -4,6 +4,9 @@
   form (fp16 with W16, a bias, the int8 weight alone, bf16);
 - BNB_OPT_MAIN_ONLY and BNB_OPT_NO_PDL change how the call is launched, not
   what it computes: Y is bit-identical to the plain call's;
+- BNB_OPT_SINGLE_CTA: the 128 x 256 tile on single CTAs instead of the
+  256 x 256 tile on CTA pairs (the default for T > 32): the same int32
+  accumulators and Y bit for bit, and both match the oracle;
 - BNB_OPT_FORCE_TIMEOUT: the main kernel takes its timeout path, the host
   reads BNB_ERR_TIMEOUT through bnb_last_device_status, and the next call on
   the same workspace (and context) runs normally and matches the oracle.
@@ -95,9 +98,31 @@ def test_launch_options_keep_results(T, K, N):
     assert binding.last_device_status(ws) == 0
 
 
-@pytest.mark.parametrize("T,K,N", [(16, 4096, 4096), (3, 272, 129), (300, 1024, 200),
-                                   (2048, 4096, 1024)])
-def test_forced_timeout_then_normal_call(orc, T, K, N):
+@pytest.mark.parametrize("T,K,N,ncols", [(33, 256, 100, 3), (40, 272, 129, 3), (300, 1024, 200, 4),
+                                         (257, 2064, 1000, 7), (130, 512, 257, 40)])
+@pytest.mark.parametrize("tau", [6.0, 0.0])
+def test_cta_pair_and_single_cta_agree(orc, T, K, N, ncols, tau):
+    """Both tile forms sum each output over K in the same order: identical
+    accumulators and Y.  The single-CTA form also against the oracle (the
+    pair form is what every other parity test runs for T > 32)."""
+    import torch
+
+    from int8_mixed_precision_04_b300 import binding
+    w = inputs.random_small(T, K, N, ncols, seed=5 * T + N + K, tau=tau)
+    r1, _ = run_and_compare(orc, w.X, w.W, tau, what=f"single-CTA T{T} K{K} N{N} tau{tau}",
+                            opts=binding.OPT_SINGLE_CTA)
+    X = torch.from_numpy(w.X).cuda()
+    W = torch.from_numpy(w.W).cuda()
+    Wq, sw = binding.quantize_weight(W)
+    r2 = binding.linear_debug(X, Wq, sw, W, tau)
+    torch.cuda.synchronize()
+    assert binding.last_device_status(r2["workspace"]) == 0
+    assert torch.equal(r1["acc"], r2["acc"]) and torch.equal(r1["Y"], r2["Y"])
+
+
+@pytest.mark.parametrize("T,K,N,form", [(16, 4096, 4096, ""), (3, 272, 129, ""), (300, 1024, 200, ""),
+                                        (2048, 4096, 1024, ""), (300, 1024, 200, "single_cta")])
+def test_forced_timeout_then_normal_call(orc, T, K, N, form):
     """A wait that gives up is reported through the status word, and the
     context and workspace stay usable: the next call is correct."""
     import torch
@@ -108,7 +133,8 @@ def test_forced_timeout_then_normal_call(orc, T, K, N):
     W = torch.from_numpy(w.W).cuda()
     Wq, sw = binding.quantize_weight(W)
     ws = torch.empty(binding.workspace_bytes(T, N, K), dtype=torch.uint8, device="cuda")
-    binding.linear_opts(X, Wq, sw, W, 6.0, binding.OPT_FORCE_TIMEOUT, workspace=ws)
+    opts = binding.OPT_SINGLE_CTA if form == "single_cta" else 0
+    binding.linear_opts(X, Wq, sw, W, 6.0, binding.OPT_FORCE_TIMEOUT | opts, workspace=ws)
     assert binding.last_device_status(ws) == binding.Status.TIMEOUT
     # the status word was read and cleared; the same workspace, a normal call
     Y = binding.linear(X, Wq, sw, W, 6.0, workspace=ws)
@@ -126,7 +152,7 @@ def test_unknown_options_are_rejected():
     X = torch.zeros((4, 64), dtype=torch.float16, device="cuda")
     W = torch.zeros((32, 64), dtype=torch.float16, device="cuda")
     Wq, sw = binding.quantize_weight(W)
-    for bad in (0x20, binding.OPT_CLUSTER(3), binding.OPT_CLUSTER(32),
+    for bad in (0x40, binding.OPT_CLUSTER(3), binding.OPT_CLUSTER(32),
                 binding.OPT_MAIN_ONLY | binding.OPT_ACT_ONLY):
         with pytest.raises(binding.BnbError) as e:
             binding.linear_opts(X, Wq, sw, W, 6.0, bad)
