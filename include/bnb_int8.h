@@ -335,6 +335,9 @@ int bnb_int8_linear_path(int64_t T, int64_t N, int64_t K);
  *   BNB_OPT_SINGLE_CTA  T > 32 on the tcgen05 GEMM: each 128 x 256 tile on
  *                       one CTA (cta_group::1) instead of 256 x 256 tiles on
  *                       CTA pairs (cta_group::2), for comparison.
+ *   BNB_OPT_GEMM        T <= 16: the activation pass and the GEMM (path 2, or
+ *                       3 with BNB_OPT_LEGACY_MMA) even where the decode
+ *                       kernel holds the call, for comparison and tests.
  *   BNB_OPT_CLUSTER(c)  decode path: thread-block clusters of c CTAs (c = 4,
  *                       8 or 16) sharing one activation pass, instead of the
  *                       size the library picks, when clusters of that size
@@ -356,6 +359,7 @@ int bnb_int8_linear_path(int64_t T, int64_t N, int64_t K);
 #define BNB_OPT_LEGACY_MMA 0x8u
 #define BNB_OPT_FORCE_TIMEOUT 0x10u
 #define BNB_OPT_SINGLE_CTA 0x20u
+#define BNB_OPT_GEMM 0x40u
 #define BNB_OPT_CLUSTER(c) ((uint32_t)(c) << 8)
 bnb_status_t bnb_int8_linear_opts(const void *X, int64_t T, int64_t K, const int8_t *Wq,
                                   const float *Wscale, const void *W16, const void *bias,

@@ -359,6 +359,7 @@ OPT_NO_PDL = 0x4
 OPT_LEGACY_MMA = 0x8
 OPT_FORCE_TIMEOUT = 0x10
 OPT_SINGLE_CTA = 0x20
+OPT_GEMM = 0x40
 
 
 def OPT_CLUSTER(c: int) -> int:

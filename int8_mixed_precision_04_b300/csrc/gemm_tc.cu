@@ -125,17 +125,6 @@ struct Tile {
   static_assert(kEpiCols % 8 == 0 && (kTmemCols & (kTmemCols - 1)) == 0, "tile geometry");
 };
 
-// Shared-memory matrix descriptor of a K-major tile with the 128-byte
-// swizzle: rows of 128 bytes, 8-row groups 1024 bytes apart.
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
-  uint64_t d = (uint64_t)((saddr >> 4) & 0x3FFFu);  // start address
-  d |= (uint64_t)1 << 16;                            // leading offset (unused with this swizzle)
-  d |= (uint64_t)(1024 >> 4) << 32;                  // stride offset: next 8-row group
-  d |= (uint64_t)1 << 46;                            // descriptor version of tcgen05
-  d |= (uint64_t)2 << 61;                            // 128-byte swizzle
-  return d;
-}
-
 struct TcArgs {
   int64_t T, K, N;
   int t_tiles, n_tiles;

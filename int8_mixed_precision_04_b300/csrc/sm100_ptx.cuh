@@ -204,6 +204,18 @@ __device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t adesc, uint64
         : "memory");
 }
 
+// Shared-memory matrix descriptor of a K-major operand tile with the 128-byte
+// swizzle: rows of 128 bytes (64 fp16), 8-row groups 1024 bytes apart.  A
+// step of 16 fp16 along K is +2 on the descriptor (32 bytes in units of 16).
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  uint64_t d = (uint64_t)((saddr >> 4) & 0x3FFFu);  // start address
+  d |= (uint64_t)1 << 16;                            // leading offset (unused with this swizzle)
+  d |= (uint64_t)(1024 >> 4) << 32;                  // stride offset: next 8-row group
+  d |= (uint64_t)1 << 46;                            // descriptor version of tcgen05
+  d |= (uint64_t)2 << 61;                            // 128-byte swizzle
+  return d;
+}
+
 // `bar` receives one arrival when every tcgen05 operation issued so far by
 // this thread has completed.  kG = 2: the mbarrier at the same offset in both
 // CTAs of the pair receives it.

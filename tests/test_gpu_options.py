@@ -121,7 +121,8 @@ def test_cta_pair_and_single_cta_agree(orc, T, K, N, ncols, tau):
 
 
 @pytest.mark.parametrize("T,K,N,form", [(16, 4096, 4096, ""), (3, 272, 129, ""), (300, 1024, 200, ""),
-                                        (2048, 4096, 1024, ""), (300, 1024, 200, "single_cta")])
+                                        (2048, 4096, 1024, ""), (300, 1024, 200, "single_cta"),
+                                        (9, 8192, 300, "")])
 def test_forced_timeout_then_normal_call(orc, T, K, N, form):
     """A wait that gives up is reported through the status word, and the
     context and workspace stay usable: the next call is correct."""
@@ -152,7 +153,7 @@ def test_unknown_options_are_rejected():
     X = torch.zeros((4, 64), dtype=torch.float16, device="cuda")
     W = torch.zeros((32, 64), dtype=torch.float16, device="cuda")
     Wq, sw = binding.quantize_weight(W)
-    for bad in (0x40, binding.OPT_CLUSTER(3), binding.OPT_CLUSTER(32),
+    for bad in (0x80, binding.OPT_CLUSTER(3), binding.OPT_CLUSTER(32),
                 binding.OPT_MAIN_ONLY | binding.OPT_ACT_ONLY):
         with pytest.raises(binding.BnbError) as e:
             binding.linear_opts(X, Wq, sw, W, 6.0, bad)

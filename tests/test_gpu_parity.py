@@ -50,6 +50,16 @@ def test_decode_cluster_sizes(orc, cluster, T, K, N, ncols):
                     opts=binding.OPT_CLUSTER(cluster))
 
 
+@pytest.mark.parametrize("T", [1, 5, 16])
+def test_decode_on_the_gemm(orc, T):
+    """The decode workload through the tcgen05 GEMM's 32-token tile
+    (BNB_OPT_GEMM), which a T <= 16 call otherwise takes only for weights the
+    decode kernel cannot hold."""
+    from int8_mixed_precision_04_b300 import binding
+    w = inputs.decode(T=T)
+    run_and_compare(orc, w.X, w.W, w.tau, what=f"decode on the GEMM T={T}", opts=binding.OPT_GEMM)
+
+
 @pytest.mark.parametrize("T,K,N,ncols", [
     (1, 16, 1, 0), (3, 48, 7, 1), (16, 272, 129, 2), (17, 64, 300, 3), (33, 1040, 65, 4),
     (130, 512, 257, 5), (200, 2064, 131, 7), (257, 128, 1000, 2), (64, 4096, 64, 9),
