@@ -313,10 +313,12 @@ cudaError_t launch_act_pass(const void *X, int64_t T, int64_t K, uint32_t thr_bi
                             int num_sms, cudaStream_t stream) {
   // The caller has zeroed the status word, the counters and the column mask.
   cudaError_t e;
-  // S2: 2-D grid, column slabs of 256 x row slabs, about 2 blocks per SM,
-  // each warp with kScanUnroll rows in flight.
+  // S2: 2-D grid, column slabs of 256 x row slabs, about 8 blocks per SM,
+  // each warp with kScanUnroll rows in flight: some 128 KB of loads in flight
+  // per SM, to cover HBM latency (at 2 blocks per SM a 4096 x 8192 scan ran
+  // at 0.4 of the copy bandwidth, latency-bound).
   const int64_t slabs = (K + 255) / 256;
-  int64_t want_rows_blocks = (2LL * num_sms + slabs - 1) / slabs;
+  int64_t want_rows_blocks = (8LL * num_sms + slabs - 1) / slabs;
   if (want_rows_blocks < 1) want_rows_blocks = 1;
   int64_t rows_per_block = (T + want_rows_blocks - 1) / want_rows_blocks;
   if (rows_per_block < 32) rows_per_block = 32;
