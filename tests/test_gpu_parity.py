@@ -70,6 +70,20 @@ def test_ragged_shapes(orc, T, K, N, ncols, tau):
     run_and_compare(orc, w.X, w.W, tau, what=f"T{T} K{K} N{N} tau{tau}")
 
 
+@pytest.mark.parametrize("T,K,N,ncols,single", [
+    (2049, 272, 300, 3, False), (2573, 64, 520, 2, False), (4100, 128, 257, 4, False),
+    (2573, 64, 520, 2, True),
+])
+def test_token_tile_groups(orc, T, K, N, ncols, single):
+    """The GEMM walks token tiles in groups of 8 (2048 tokens): a last group of
+    one tile, a ragged last tile, a third group; every element against the
+    oracle, on CTA pairs and (once) on single CTAs."""
+    from int8_mixed_precision_04_b300 import binding
+    w = inputs.random_small(T, K, N, ncols, seed=T + 3 * K + N, tau=6.0)
+    run_and_compare(orc, w.X, w.W, 6.0, what=f"tile groups T{T} K{K} N{N}",
+                    opts=binding.OPT_SINGLE_CTA if single else 0)
+
+
 @pytest.mark.parametrize("T,K,N,ncols,tau", [
     (300, 1024, 200, 5, 6.0), (149, 4096, 96, 70, 6.0), (40, 2048, 64, 3, 0.0),
     (700, 512, 130, 40, 3.0), (17, 256, 300, 1, 6.0), (33, 16384, 64, 9, 6.0),
