@@ -33,7 +33,8 @@ call is bnb_int8_linear_from_host (a pinned host->device copy of X, the
 layer, a device->host copy of Y), all inside the timed region; consecutive
 calls alternate over two streams with their own device buffers and
 workspaces, so that copies overlap the neighbouring call's kernel.  It has
-its own warm-up (--e2e-warmup calls) and at least --e2e-timed-s of calls.
+its own warm-up (--e2e-warmup calls), then --e2e-calls timed calls (2000), fewer only
+where they would take longer than --e2e-timed-s (10 s).
 
 `--impl reference` times the CPU oracle (the reference arm of this build):
 each step is a bounded sample of the same workload (all rows of X, a
@@ -867,7 +868,8 @@ def main():
     ap.add_argument("--sub-timed-s", type=float, default=0.5)
     ap.add_argument("--e2e-calls", type=int, default=2000)
     ap.add_argument("--e2e-warmup", type=int, default=100)
-    ap.add_argument("--e2e-timed-s", type=float, default=2.0)
+    ap.add_argument("--e2e-timed-s", type=float, default=10.0,
+                    help="upper bound on the e2e timed region: --e2e-calls calls unless fewer fit")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--ref-budget", type=float, default=120.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
