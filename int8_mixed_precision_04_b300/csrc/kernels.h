@@ -47,7 +47,9 @@ cudaError_t launch_decode(const void *X, int64_t T, int64_t K, uint32_t thr, con
                           int32_t *dbg_acc, uint32_t opts, cudaStream_t stream);
 
 // S4..S6 on tcgen05 tensor cores (fp16 integer codes from the activation
-// pass, code_mode 1), persistent over 128 x 256 output tiles.
+// pass, code_mode 1), persistent over 256 x 256 output tiles on CTA pairs
+// (T > 32; 128 x 256 on single CTAs with BNB_OPT_SINGLE_CTA) or 128 x 32
+// tiles (T <= 32).
 cudaError_t launch_gemm_tc(int64_t T, int64_t K, const int8_t *Wq, const float *sw,
                            const void *W16, const void *bias, int64_t N, bool bf16, void *Y,
                            const Workspace &ws, int32_t *dbg_acc, int num_sms, uint32_t opts,
