@@ -1,4 +1,5 @@
-// S4..S6 on the fifth-generation tensor core (tcgen05), for T > 16.
+// S4..S6 on the fifth-generation tensor core (tcgen05), for T > 16 (and for
+// decode-sized calls whose weight the decode kernel cannot hold).
 //
 // What is computed (per output element, t a token, n an output channel):
 //   acc[t,n] = sum_k Xq[t,k] Wq[n,k]                 exact int32
@@ -19,8 +20,11 @@
 // buffers alternate between chunks, so the drain of one overlaps the MMAs of
 // the next.
 //
-// Tile: 128 output channels (MMA M, tensor-memory lanes) x 256 tokens (MMA N,
-// tensor-memory columns); k advances 64 columns per pipeline stage.
+// Tile (T > 32): 256 output channels x 256 tokens on a CTA pair (cta_group::2,
+// MMA M = 256: each CTA's 128 weight rows are its tensor-memory lanes; MMA N =
+// 256 token columns, each CTA loading half of them); with BNB_OPT_SINGLE_CTA,
+// 128 x 256 on one CTA.  T <= 32: 128 x 32 on one CTA.  k advances 64 columns
+// per pipeline stage.
 //   A operand  W codes widened to fp16 integers by the converter warps from
 //              an int8 tile (TMA, 64-byte swizzle) into the 128-byte-swizzled
 //              K-major layout the MMA reads.
@@ -42,11 +46,11 @@
 // issuer and tensor-memory owner, 2-3 idle, 4-11 converters (half a weight row
 // per thread), 12-27 epilogue (four warps per 32-lane quadrant of tensor
 // memory, one per quarter of the token columns, so that each thread holds
-// kBN / 4 int32 running sums in registers).  Persistent CTAs, one
-// per SM (or pair), walk the tiles in token-tile groups (tile_coords) so that
-// concurrently running CTAs share weight tiles in L2.  Every wait is bounded; a timeout
-// raises a CTA-wide abort flag, records BNB_ERR_TIMEOUT and lets all roles
-// leave, after which in-flight copies and MMAs are waited for and tensor
+// kBN / 4 int32 running sums in registers).  Persistent CTAs (or CTA pairs),
+// one per SM, walk the tiles in token-tile groups (tile_coords) so that
+// concurrently running CTAs share weight tiles in L2.  Every wait is bounded;
+// a timeout raises a CTA-wide abort flag, records BNB_ERR_TIMEOUT and lets all
+// roles leave, after which in-flight copies and MMAs are waited for and tensor
 // memory is freed.
 #include <cuda.h>
 
