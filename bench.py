@@ -381,6 +381,10 @@ def measure_layer(args, w, dev, world, local, steps, min_timed_s, min_layers=2,
         "clocks": sampler.summary(),
         "l2_bytes": l2,
     }
+    # time x clock: SM cycles per call at the median clock of the timed region,
+    # comparable between runs that the power cap holds at different clocks
+    if out["clocks"].get("sm_mhz"):
+        out["clocks"]["sm_cycles_per_call"] = out["us_per_call"] * out["clocks"]["sm_mhz"]
     peaks, peak_src = load_peaks()
     if with_kernel:
         # the dominant kernel alone: graphs of main-kernel-only calls (the GEMM
