@@ -1,7 +1,7 @@
 // The whole layer for decode-sized T (T <= 16) in one kernel per call.
 //
 // dec_fused: one CTA per slice of at most 40 output channels (one CTA per
-// SM), in thread-block clusters of kC CTAs (16, 8 or 4: the first whose
+// SM), in thread-block clusters of kC CTAs (8, 16 or 4: the first whose
 // resident clusters hold every slice at once).  Right behind its X loads the
 // producer warp puts the CTA's whole int8 weight slice in flight on the copy
 // engine (one bulk copy per row).  While the weight streams in, the cluster
@@ -659,11 +659,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
 
 namespace {
 
-constexpr int kDecClusterSizes[3] = {8, 16, 4};  // the kernels built (index into DecCfg::ctas)
-// Order of preference over kDecClusterSizes (measured, 16-layer CUDA graph at
-// T 16 and N 4096: 16 and 8 tie at K 4096 (11.54 us), 16 is 5.6 % faster at
-// K 2048, 4 is the slowest at both)
-constexpr int kDecPreference[3] = {1, 0, 2};
+constexpr int kDecClusterSizes[3] = {8, 16, 4};  // order of preference (measured)
 
 // CTAs of dec_fused<kC> resident at once, in whole clusters (0 if the query
 // fails); also opens the kernel's shared-memory limit to `dyn_max`.
@@ -742,19 +738,16 @@ int64_t dec_rows_cap(const DecCfg &c, int64_t K) {
   return rows;
 }
 
-// The index (into kDecClusterSizes) of the first cluster size, in
-// kDecPreference's order, whose resident CTAs hold N output channels in one
-// wave; -1 if none does.  A call may ask for a size (`want`, 0 = no
-// preference), which is taken whenever it holds the call.
+// The first cluster size, in kDecClusterSizes' order, whose resident CTAs
+// hold N output channels in one wave; -1 if none does.  A call may ask for a
+// size (`want`, 0 = no preference), which is taken whenever it holds the call.
 int decode_pick(const DecCfg &c, int64_t N, int64_t K, int want) {
   const int64_t cap = dec_rows_cap(c, K);
   const int64_t need = (N + cap - 1) / cap;
   for (int i = 0; i < 3; i++)
     if (want != 0 && kDecClusterSizes[i] == want && c.ctas[i] >= need) return i;
-  for (int j = 0; j < 3; j++) {
-    const int i = kDecPreference[j];
+  for (int i = 0; i < 3; i++)
     if (c.ctas[i] >= need) return i;
-  }
   return -1;
 }
 
