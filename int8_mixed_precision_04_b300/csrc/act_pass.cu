@@ -55,6 +55,8 @@ __global__ void __launch_bounds__(kScanThreads) outlier_scan_kernel(
     int32_t *__restrict__ O) {
   __shared__ uint32_t part[kScanThreads / 32][32];
   __shared__ uint32_t is_last;
+  // the row pass may launch now (it waits for this grid before reading it)
+  pdl_trigger();
   const uint32_t lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t vecs = K / 8;
   const int64_t v = (int64_t)blockIdx.x * 32 + lane;  // this lane's 8-column vector
@@ -254,6 +256,11 @@ struct QuantArgs {
 template <int kMode, bool kBf>
 __global__ void __launch_bounds__(kQuantThreads) quantize_rows_kernel(const QuantArgs p) {
   __shared__ uint32_t red[kQuantThreads / 32];
+  // launched with programmatic dependent launch behind the column scan:
+  // everything below reads what the scan wrote.  (No early trigger here: a
+  // GEMM CTA needs a whole SM, and one launched early would hold SMs the
+  // remaining row blocks need.)
+  pdl_wait();
   const int64_t vecs = p.K / 8;
   const int32_t nO = (int32_t)__ldcg(p.counters + 1);
   const bool dense = kMode == 1 && outlier_block_dense(nO, p.K);  // the tcgen05 GEMM's form
@@ -310,7 +317,7 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_rows_kernel(const Quan
 cudaError_t launch_act_pass(const void *X, int64_t T, int64_t K, uint32_t thr_bits,
                             const Workspace &ws, int code_mode, bool with_xo, const void *W16,
                             const int8_t *Wq, int64_t N, bool bf16, int8_t *dbg_xq,
-                            int num_sms, cudaStream_t stream) {
+                            int num_sms, cudaStream_t stream, bool pdl) {
   // The caller has zeroed the status word, the counters and the column mask.
   cudaError_t e;
   // S2: 2-D grid, column slabs of 256 x row slabs, about 8 blocks per SM,
@@ -357,9 +364,18 @@ cudaError_t launch_act_pass(const void *X, int64_t T, int64_t K, uint32_t thr_bi
   }
   auto *kern = code_mode == 0 ? (bf16 ? quantize_rows_kernel<0, true> : quantize_rows_kernel<0, false>)
                               : (bf16 ? quantize_rows_kernel<1, true> : quantize_rows_kernel<1, false>);
-  kern<<<(unsigned)qblocks, kQuantThreads, 0, stream>>>(a);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)qblocks);
+  cfg.blockDim = dim3(kQuantThreads);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  e = cudaLaunchKernelEx(&cfg, kern, a);
   note_launch();
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace bnb

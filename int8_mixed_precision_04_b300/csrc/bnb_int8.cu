@@ -207,7 +207,8 @@ static bnb_status_t linear_impl(const void *X, int64_t T, int64_t K, const int8_
       // the tcgen05 GEMM reads fp16 integer codes, the mma GEMM int8 codes
       // (for the tcgen05 GEMM the same launch compacts W16 at a sparse outlier set)
       e = launch_act_pass(X, T, K, thr, ws, /*code_mode=*/path == 2 ? 1 : 0, /*with_xo=*/true,
-                          W16, Wq, N, bf16, dbg_xq, device_sms(dev), stream);
+                          W16, Wq, N, bf16, dbg_xq, device_sms(dev), stream,
+                          /*pdl=*/!(opts & BNB_OPT_NO_PDL));
       if (e != cudaSuccess) return BNB_ERR_CUDA;
     }
     if (!(opts & BNB_OPT_ACT_ONLY)) {

@@ -23,11 +23,12 @@ cudaError_t launch_quantize_weight(const void *W16, int64_t N, int64_t K, bool b
                                    float *sw, cudaStream_t stream);
 
 // S2 + S3.  code_mode 0: int8 codes, 1: fp16 integer codes.  with_xo: write
-// the padded fp16 outlier block.
+// the padded fp16 outlier block.  pdl: launch the row pass with programmatic
+// dependent launch behind the column scan.
 cudaError_t launch_act_pass(const void *X, int64_t T, int64_t K, uint32_t thr_bits,
                             const Workspace &ws, int code_mode, bool with_xo, const void *W16,
                             const int8_t *Wq, int64_t N, bool bf16, int8_t *dbg_xq,
-                            int num_sms, cudaStream_t stream);
+                            int num_sms, cudaStream_t stream, bool pdl);
 
 // The blockwise 8-bit codec (blocks of B values, B a power of two in
 // [64, 2048]): fp32 -> int8 codes + per-block absmax, and back.
