@@ -112,7 +112,7 @@ MEASURED_TRAFFIC = {
     # one ncu capture of the large workload's GEMM launch: 930.92 MB read + 247.37 MB written
     ("gemm_tc", 4096, 8192, 28672): ("gemm_tc.cu", "25383f2e26f639e0", 1_178_290_000),
     # one ncu capture of the decode workload's kernel: 19.12 MB read, 0 written
-    ("dec_fused", 16, 4096, 4096): ("decode.cu", "058e0e1d5737dadd", 19_116_544),
+    ("dec_fused", 16, 4096, 4096): ("decode.cu", "c4c27dae43364fcd", 19_116_544),
 }
 
 

@@ -1,8 +1,9 @@
 // The whole layer for decode-sized T (T <= 16) in one kernel per call.
 //
 // dec_fused: one CTA per slice of at most 40 output channels (one CTA per
-// SM), in thread-block clusters of kC CTAs (8, 16 or 4: the first whose
-// resident clusters hold every slice at once).  Right behind its X loads the
+// SM), in thread-block clusters of kC CTAs (16, 8 or 4 where T K <= 32768,
+// else 8, 16 or 4: the first whose resident clusters hold every slice at
+// once).  Right behind its X loads the
 // producer warp puts the CTA's whole int8 weight slice in flight on the copy
 // engine (one bulk copy per row).  While the weight streams in, the cluster
 // runs the activation pass cooperatively, so that no second kernel and no
@@ -659,7 +660,15 @@ __global__ void __launch_bounds__(kDecThreads, 1)
 
 namespace {
 
-constexpr int kDecClusterSizes[3] = {8, 16, 4};  // order of preference (measured)
+constexpr int kDecClusterSizes[3] = {8, 16, 4};  // the kernels built (index into DecCfg::ctas)
+// Order of preference over kDecClusterSizes, measured per call in 16-layer
+// CUDA graphs at N 3900 (both sizes hold it): 16-CTA clusters are 3-8 %
+// faster than 8-CTA ones while T K <= 32768 (every T <= 16 at K 2048, T <= 8
+// at K 4096), 8-CTA ones faster beyond (6 % at T 16, K 4096; 2 % at T 16,
+// K 3072).  4-CTA clusters were the slowest everywhere.
+constexpr int64_t kDecSmallWork = 32768;
+constexpr int kDecPreferSmall[3] = {1, 0, 2};  // T K <= kDecSmallWork: 16, 8, 4
+constexpr int kDecPreferLarge[3] = {0, 1, 2};  // otherwise: 8, 16, 4
 
 // CTAs of dec_fused<kC> resident at once, in whole clusters (0 if the query
 // fails); also opens the kernel's shared-memory limit to `dyn_max`.
@@ -738,16 +747,18 @@ int64_t dec_rows_cap(const DecCfg &c, int64_t K) {
   return rows;
 }
 
-// The first cluster size, in kDecClusterSizes' order, whose resident CTAs
-// hold N output channels in one wave; -1 if none does.  A call may ask for a
-// size (`want`, 0 = no preference), which is taken whenever it holds the call.
-int decode_pick(const DecCfg &c, int64_t N, int64_t K, int want) {
+// The index (into kDecClusterSizes) of the first cluster size, in the order
+// of preference for T K, whose resident CTAs hold N output channels in one
+// wave; -1 if none does.  A call may ask for a size (`want`, 0 = no
+// preference), which is taken whenever it holds the call.
+int decode_pick(const DecCfg &c, int64_t T, int64_t N, int64_t K, int want) {
   const int64_t cap = dec_rows_cap(c, K);
   const int64_t need = (N + cap - 1) / cap;
   for (int i = 0; i < 3; i++)
     if (want != 0 && kDecClusterSizes[i] == want && c.ctas[i] >= need) return i;
-  for (int i = 0; i < 3; i++)
-    if (c.ctas[i] >= need) return i;
+  const int *order = T * K <= kDecSmallWork ? kDecPreferSmall : kDecPreferLarge;
+  for (int j = 0; j < 3; j++)
+    if (c.ctas[order[j]] >= need) return order[j];
   return -1;
 }
 
@@ -769,7 +780,7 @@ cudaError_t launch_decode(const void *X, int64_t T, int64_t K, uint32_t thr, con
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) dev = -1;
   const DecCfg dc = decode_cfg(dev);
-  const int pick = decode_pick(dc, N, K, (int)((opts >> 8) & 0xffu));
+  const int pick = decode_pick(dc, T, N, K, (int)((opts >> 8) & 0xffu));
   if (pick < 0) return cudaErrorInvalidValue;  // the host routes only shapes that fit here
   const int kc = kDecClusterSizes[pick];
   DecArgs a;
