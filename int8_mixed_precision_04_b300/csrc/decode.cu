@@ -81,12 +81,13 @@ __host__ __device__ constexpr int64_t dec_wregion(int64_t K, int64_t rows) {
 }
 __host__ __device__ constexpr int64_t dec_ocap(int64_t K) { return (K + 7) / 8 * 8; }
 
-// dynamic: weight rows, code rows, outlier column list (uint16).  The MMAs
-// also read the (unused) rows past `rows` of a partial 8-channel group: at
-// most 7 rows, which land in the code rows.
-size_t decode_smem_bytes(int64_t K, int64_t rows) {
-  return (size_t)(dec_wregion(K, rows) + 16 * dec_pitch(K) + 2 * dec_ocap(K));
+// dynamic: weight rows, code rows (xrows: 8 when T <= 8, else 16), outlier
+// column list (uint16).  The MMAs also read the (unused) rows past `rows` of a
+// partial 8-channel group: at most 7 rows, which land in the code rows.
+size_t decode_smem_bytes(int64_t K, int64_t rows, int64_t xrows = 16) {
+  return (size_t)(dec_wregion(K, rows) + xrows * dec_pitch(K) + 2 * dec_ocap(K));
 }
+constexpr int64_t dec_xrows(int64_t T) { return T <= 8 ? 8 : 16; }
 
 // small static buffers of one CTA (partly written by the other CTAs of its cluster)
 struct DecSmall {
@@ -117,6 +118,7 @@ struct DecArgs {
   int64_t K, N;
   uint32_t thr;                // smallest fp16 magnitude bits >= tau
   int64_t rows_per_cta;        // <= kDecMaxRows
+  int xrows;                   // code rows held: dec_xrows(T)
   int64_t wregion;             // bytes of the weight region, dec_wregion(K, rows_per_cta)
   const int8_t *Wq;
   const float *sw;
@@ -155,10 +157,13 @@ __device__ __forceinline__ void widen16(const uint4 &v, uint32_t (&h)[8]) {
 // kRagged: the range ends inside a 64-column block, whose columns past k1
 // (never written in shared memory) are fed as zeros; otherwise no lane needs
 // a mask.
+// xhi: the code row the MMA's rows 8..15 read, row g + 8 when those rows
+// are held (T > 8); with the 8-row code region it is row g again, whose
+// products land in rows that no token reads.
 template <bool kRagged>
-__device__ __forceinline__ void dec_mma_range(const uint8_t *xs, const uint8_t *ws,
-                                              int64_t pitch, int g, int q, int64_t k0,
-                                              int64_t k1, int ng,
+__device__ __forceinline__ void dec_mma_range(const uint8_t *xs, const uint8_t *xhi,
+                                              const uint8_t *ws, int64_t pitch, int g, int q,
+                                              int64_t k0, int64_t k1, int ng,
                                               int (&acc)[kDecGroups][4]) {
   float f[kDecGroups][4] = {};
   int nb = 0;
@@ -166,7 +171,7 @@ __device__ __forceinline__ void dec_mma_range(const uint8_t *xs, const uint8_t *
     const uint32_t lv = (!kRagged || kb + 16 * q < k1) ? 0xffffffffu : 0u;
     uint32_t xa[8], xb[8];
     widen16(*reinterpret_cast<const uint4 *>(xs + g * pitch + kb + 16 * q), xa);
-    widen16(*reinterpret_cast<const uint4 *>(xs + (g + 8) * pitch + kb + 16 * q), xb);
+    widen16(*reinterpret_cast<const uint4 *>(xhi + kb + 16 * q), xb);
 #pragma unroll
     for (int gi = 0; gi < kDecGroups; gi++) {
       if (gi < ng) {
@@ -199,8 +204,8 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   extern __shared__ __align__(128) uint8_t smem[];
   const int64_t K = p.K, pitch = dec_pitch(K), range = dec_range(K);
   uint8_t *ws = smem;                                          // [rows][pitch] weight codes
-  uint8_t *xs = smem + p.wregion;                              // [16][pitch] activation codes
-  uint16_t *ocols = reinterpret_cast<uint16_t *>(xs + 16 * pitch);  // outlier columns
+  uint8_t *xs = smem + p.wregion;                              // [xrows][pitch] activation codes
+  uint16_t *ocols = reinterpret_cast<uint16_t *>(xs + p.xrows * pitch);  // outlier columns
   __shared__ DecSmall sm;
   float *sxs = sm.sxs;
   uint32_t *red = reinterpret_cast<uint32_t *>(smem);  // [16 warps][32][21], after the main loop
@@ -549,10 +554,11 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   const int64_t k0 = warp * range, k1 = min(K, k0 + range);
   int acc[kDecGroups][4] = {};
   if (k1 > k0 && mbar_wait_bounded(&sm.wbar, 0, p.status)) {
+    const uint8_t *xhi = xs + (g + (p.xrows > 8 ? 8 : 0)) * pitch;
     if (((k1 - k0) & 63) == 0)
-      dec_mma_range<false>(xs, ws, pitch, g, q, k0, k1, ng, acc);
+      dec_mma_range<false>(xs, xhi, ws, pitch, g, q, k0, k1, ng, acc);
     else
-      dec_mma_range<true>(xs, ws, pitch, g, q, k0, k1, ng, acc);
+      dec_mma_range<true>(xs, xhi, ws, pitch, g, q, k0, k1, ng, acc);
   }
   // Only the int8 weight kept (W16 null): the outlier weights are the slice's
   // own codes, Wq sw / 127, with sw / 127 applied in the epilogue.  The first
@@ -741,9 +747,9 @@ DecCfg decode_cfg(int dev) {
 }
 
 // Output channels a CTA can hold at this K (at most kDecMaxRows).
-int64_t dec_rows_cap(const DecCfg &c, int64_t K) {
+int64_t dec_rows_cap(const DecCfg &c, int64_t K, int64_t xrows = 16) {
   int64_t rows = kDecMaxRows;
-  while (rows > 8 && decode_smem_bytes(K, rows) > (size_t)c.dyn_max) rows--;
+  while (rows > 8 && decode_smem_bytes(K, rows, xrows) > (size_t)c.dyn_max) rows--;
   return rows;
 }
 
@@ -752,7 +758,7 @@ int64_t dec_rows_cap(const DecCfg &c, int64_t K) {
 // wave; -1 if none does.  A call may ask for a size (`want`, 0 = no
 // preference), which is taken whenever it holds the call.
 int decode_pick(const DecCfg &c, int64_t T, int64_t N, int64_t K, int want) {
-  const int64_t cap = dec_rows_cap(c, K);
+  const int64_t cap = dec_rows_cap(c, K, dec_xrows(T));
   const int64_t need = (N + cap - 1) / cap;
   for (int i = 0; i < 3; i++)
     if (want != 0 && kDecClusterSizes[i] == want && c.ctas[i] >= need) return i;
@@ -797,6 +803,7 @@ cudaError_t launch_decode(const void *X, int64_t T, int64_t K, uint32_t thr, con
   const int64_t used = (N + a.rows_per_cta - 1) / a.rows_per_cta;
   const int64_t ctas = (used + kc - 1) / kc * kc;
   a.wregion = dec_wregion(K, a.rows_per_cta);
+  a.xrows = (int)dec_xrows(T);
   // W16 in boxes of 8 columns x one slice's channels (outlier columns only,
   // so no L2 promotion beyond the sector)
   // (without W16 the map is never read: it then describes Wq)
@@ -824,7 +831,7 @@ cudaError_t launch_decode(const void *X, int64_t T, int64_t K, uint32_t thr, con
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)ctas);
   cfg.blockDim = dim3(kDecThreads);
-  cfg.dynamicSmemBytes = decode_smem_bytes(K, a.rows_per_cta);
+  cfg.dynamicSmemBytes = decode_smem_bytes(K, a.rows_per_cta, a.xrows);
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
