@@ -339,9 +339,10 @@ int bnb_int8_linear_path(int64_t T, int64_t N, int64_t K);
  *                       3 with BNB_OPT_LEGACY_MMA) even where the decode
  *                       kernel holds the call, for comparison and tests.
  *   BNB_OPT_CLUSTER(c)  decode path: thread-block clusters of c CTAs (c = 4,
- *                       8 or 16) sharing one activation pass, instead of the
- *                       size the library picks, when clusters of that size
- *                       hold the call.
+ *                       8 or 16) sharing one activation pass, or (c = 1, for
+ *                       T <= 8) no clusters, every CTA running the whole
+ *                       activation pass itself, instead of the form the
+ *                       library picks, when that form holds the call.
  *   BNB_OPT_FORCE_TIMEOUT  one thread of the call's main kernel waits, with a
  *                       limit of about 0.1 ms, on an mbarrier that nothing
  *                       completes, and then takes the kernel's timeout path

@@ -32,7 +32,9 @@ namespace bnb {
 // The int8 codes of one 16-byte vector (8 fp16 or bf16 values, flags f:
 // outlier columns get 0) under the row's code rule rc, as two words of four
 // code bytes.  code_byte is exact and uses no conversion-pipe instruction;
-// the GEMM's fp16 integer codes come from the bytes by s8x4_to_f16x4.
+// the GEMM's fp16 integer codes come from the bytes by s8x4_to_f16x4.  (One
+// value at a time: RowCode::codes8's eight values at once raised this
+// kernel's registers from 64 to 117 and made the row pass slower.)
 template <bool kBf>
 __device__ __forceinline__ void codes8(const uint32_t (&w)[4], uint32_t f, const RowCode<kBf> &rc,
                                        uint32_t &p0, uint32_t &p1) {

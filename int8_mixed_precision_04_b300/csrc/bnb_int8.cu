@@ -139,7 +139,7 @@ static bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
 // CTAs hold in one wave); 2: tcgen05 GEMM (every other shape, decode-sized T
 // included); 3: legacy mma GEMM (only when a call's options ask for it).
 static int choose_path(int64_t T, int64_t N, int64_t K, int dev, uint32_t opts = 0) {
-  if (T <= 16 && !(opts & BNB_OPT_GEMM) && K <= kDecodeMaxK && N <= decode_max_n(dev, K)) return 1;
+  if (T <= 16 && !(opts & BNB_OPT_GEMM) && K <= kDecodeMaxK && N <= decode_max_n(dev, T, K)) return 1;
   return (opts & BNB_OPT_LEGACY_MMA) ? 3 : 2;
 }
 
@@ -419,7 +419,7 @@ bnb_status_t bnb_int8_linear_opts(const void *X, int64_t T, int64_t K, const int
                               BNB_OPT_GEMM | BNB_OPT_CLUSTER(0xff);
   if (opts & ~kKnown) return BNB_ERR_INVALID_ARG;
   const uint32_t c = (opts >> 8) & 0xffu;
-  if (c != 0 && c != 4 && c != 8 && c != 16) return BNB_ERR_INVALID_ARG;
+  if (c != 0 && c != 1 && c != 4 && c != 8 && c != 16) return BNB_ERR_INVALID_ARG;
   if ((opts & BNB_OPT_MAIN_ONLY) && (opts & BNB_OPT_ACT_ONLY)) return BNB_ERR_INVALID_ARG;
   return linear_impl(X, T, K, Wq, Wscale, W16, bias, N, tau, dtype == BNB_DTYPE_BF16, Y,
                      workspace, workspace_bytes, stream, Xq, Xscale, outlier_idx, n_outliers, acc,

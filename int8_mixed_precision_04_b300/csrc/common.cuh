@@ -187,6 +187,34 @@ struct RowCode {
   __device__ __forceinline__ uint32_t byte(float x) const {
     return code_byte_fast(kBf ? (x * s1) * s2 : x, a, r);
   }
+  // The code bytes of one 16-byte vector (eight 16-bit values; value 2j is
+  // the low half of w[j]), 0 where bit i of f is set, packed little-endian
+  // into two words.  The same bytes as byte(): code_byte_fast's rounding for
+  // all eight, and only for a vector with a value near a half-integer (about
+  // one value in 2^14) code_byte_fast again, whose exact rule decides those.
+  __device__ __forceinline__ void codes8(const uint32_t (&w)[4], uint32_t f, uint32_t &p0,
+                                         uint32_t &p1) const {
+    constexpr float kM = 12582912.0f;
+    uint32_t b[8];
+    bool near = false;
+#pragma unroll
+    for (int i = 0; i < 8; i++) {
+      const float x0 = e2f<kBf>((i & 1) ? (w[i >> 1] >> 16) : (w[i >> 1] & 0xffffu));
+      const float p = (kBf ? (x0 * s1) * s2 : x0) * r;
+      const float t = p + kM;  // M + rint(p), exact for |p| < 2^22
+      near |= !(fabsf(p - (t - kM)) < 0.5f - 0x1p-15f);
+      b[i] = __float_as_uint(t);
+    }
+    if (near) {
+#pragma unroll
+      for (int i = 0; i < 8; i++)
+        b[i] = byte(e2f<kBf>((i & 1) ? (w[i >> 1] >> 16) : (w[i >> 1] & 0xffffu)));
+    }
+#pragma unroll
+    for (int i = 0; i < 8; i++) b[i] = ((f >> i) & 1u) ? 0u : b[i];
+    p0 = __byte_perm(__byte_perm(b[0], b[1], 0x0040), __byte_perm(b[2], b[3], 0x0040), 0x5410);
+    p1 = __byte_perm(__byte_perm(b[4], b[5], 0x0040), __byte_perm(b[6], b[7], 0x0040), 0x5410);
+  }
 };
 
 // Four signed int8 codes (one 32-bit word) -> four fp16 integers (two half2

@@ -1,4 +1,6 @@
-// The whole layer for decode-sized T (T <= 16) in one kernel per call.
+// The whole layer for decode-sized T (T <= 16) in one kernel per call: for
+// T <= 4 dec_local (below the clustered kernel), where every CTA runs the
+// whole activation pass itself, otherwise dec_fused.
 //
 // dec_fused: one CTA per slice of at most 40 output channels (one CTA per
 // SM), in thread-block clusters of kC CTAs (16, 8 or 4 where T K <= 32768,
@@ -475,21 +477,9 @@ __global__ void __launch_bounds__(kDecThreads, 1)
 #pragma unroll
       for (int r = 0; r < G::kRpt; r++) {
         const int t = grp + kC * r;
-        const RowCode<kBf> &rc = rcs[r];
         const uint32_t w[4] = {x[r].x, x[r].y, x[r].z, x[r].w};
-        uint32_t p0 = 0, p1 = 0;
-#pragma unroll
-        for (int i = 0; i < 4; i++) {
-          const uint32_t c0 =
-              ((flags >> (2 * i)) & 1) ? 0u : rc.byte(e2f<kBf>(w[i] & 0xffffu));
-          const uint32_t c1 =
-              ((flags >> (2 * i + 1)) & 1) ? 0u : rc.byte(e2f<kBf>(w[i] >> 16));
-          const uint32_t two = (c0 & 0xffu) | ((c1 & 0xffu) << 8);
-          if (i < 2)
-            p0 |= two << (16 * i);
-          else
-            p1 |= two << (16 * (i - 2));
-        }
+        uint32_t p0, p1;
+        rcs[r].codes8(w, flags, p0, p1);
         // even lanes store 16 codes (their vector and the next lane's) at once:
         // vpc is even, so an even thread's vector is even (16-byte aligned codes)
         // and its odd neighbour is live with it
@@ -661,12 +651,369 @@ __global__ void __launch_bounds__(kDecThreads, 1)
 }
 
 // ---------------------------------------------------------------------------
+// dec_local: T <= 8 without a cluster.  Every CTA runs the whole activation
+// pass itself (each consumer thread one 8-column vector of every row: a
+// column's outlier flag and its codes need no other thread), so the codes are
+// in shared memory about a microsecond after the X loads, and all SMs take a
+// weight slice.  The MMAs swap roles: the weight is the 16-row A operand (up
+// to three 16-channel tiles per slice) and the codes of X the 8-column B
+// operand, one column per token, so no MMA row is spent on padding tokens.
+// Each tile has its own weight barrier, and the MMA warps take the tiles in
+// the order the producer put them in flight.
+// ---------------------------------------------------------------------------
+
+constexpr int kLocMaxT = 8;                     // tokens of a dec_local call, at most
+constexpr int kLocTiles = (kDecMaxRows + 15) / 16;  // 16-channel tiles of a slice
+constexpr int kLocRedStride = kLocTiles * 4 + 1;    // words per lane in the reduction (odd)
+static_assert(kDecodeMaxK <= kDecConsumers * 8, "one 8-column vector per consumer thread");
+static_assert(kDecodeMaxK / kDecWarps <= kDecChunkK, "one K-range sums exactly in fp32");
+static_assert(kDecWarps * 32 * kLocRedStride * 4 <= kDecRedBytes, "reduction fits the weight region");
+
+struct DecLocSmall {
+  uint64_t wbar[kLocTiles];  // tile i of the weight slice has landed
+  uint64_t wobar;            // W16 at the first outlier columns is in wos
+  uint64_t lbar;             // the outlier list (oc, nO) is complete (or a wait gave up)
+  uint64_t never;            // completed by nothing (forced-timeout test option)
+  // [j][row][8]: W16[n0 + row, 8 (O[j] / 8) .. + 8), one TMA box per outlier column j
+  alignas(128) uint16_t wos[kDecOutSmall][kDecMaxRows][8];
+  uint32_t part[kDecWarps][kLocMaxT];  // [warp][t] partial row maxima (16-bit magnitude bits)
+  uint32_t wcnt[kDecWarps];            // outliers of each warp's 256 columns
+  uint32_t wbase[kDecWarps];           // outliers of the warps before it
+  uint32_t sxb[kLocMaxT];              // row maxima (16-bit bits)
+  float4 rcv[kLocMaxT];                // each row's code rule (RowCode a, r, s1, s2)
+  uint32_t nO;
+  uint32_t xo[kLocMaxT * kDecOutSmall];  // [t][j] X at the first outlier columns (16-bit bits)
+  uint32_t oc[kDecOutSmall];             // the first outlier columns
+  uint16_t bias[kDecMaxRows];            // the slice's 16-bit bias (0 without one)
+};
+
+// kWq: only the int8 weight is kept (W16 null); kBf: X, W16, bias and Y are bf16
+template <bool kWq, bool kBf>
+__global__ void __launch_bounds__(kDecThreads, 1)
+    dec_local_kernel(const __grid_constant__ CUtensorMap tm_w16, const DecArgs p) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int64_t K = p.K, pitch = dec_pitch(K), range = dec_range(K);
+  uint8_t *ws = smem;                                        // [rows][pitch] weight codes
+  uint8_t *xs = smem + p.wregion;                            // [8][pitch] activation codes
+  uint16_t *ocols = reinterpret_cast<uint16_t *>(xs + kLocMaxT * pitch);  // outlier columns
+  __shared__ DecLocSmall sm;
+  uint32_t *red = reinterpret_cast<uint32_t *>(smem);  // [16 warps][32][13], after the MMAs
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int T = p.T;
+  const int64_t n0 = (int64_t)blockIdx.x * p.rows_per_cta;
+  const int64_t rows = min(p.N, n0 + p.rows_per_cta) - n0;  // 1 .. 40
+  const int nt = (int)((rows + 15) / 16);                    // weight tiles
+
+  if (warp == kDecWarps && lane == 0) {
+#pragma unroll
+    for (int i = 0; i < kLocTiles; i++) mbar_init(&sm.wbar[i], 1);
+    mbar_init(&sm.wobar, 1);
+    mbar_init(&sm.lbar, 1);
+    mbar_init(&sm.never, 1);
+    mbar_init_fence();
+  }
+  __syncthreads();
+  pdl_trigger();  // the next kernel on the stream may launch; it waits for our completion
+  pdl_wait();     // X may be the output of the previous kernel on the stream
+  if (blockIdx.x == 0 && threadIdx.x == 0) *p.status = kDevOk;  // a wait that gives up overwrites it
+
+  const int64_t vecs = K / 8;
+  if (warp == kDecWarps) {
+    // The whole weight slice in flight at once, tile by tile, one bulk copy
+    // per row, right behind the X loads.  Rows past `rows` and the pads past
+    // K are never written: the MMA warps read row rows - 1 in place of the
+    // former and zero the codes of X at the latter.
+    named_bar_sync(2, kDecThreads);  // X loads issued
+    uint16_t bv[2] = {0, 0};
+    if (p.bias)
+#pragma unroll
+      for (int i = 0; i < 2; i++)
+        if (lane + 32 * i < rows) bv[i] = __ldg(p.bias + n0 + lane + 32 * i);
+    if (lane < nt) mbar_expect_tx(&sm.wbar[lane], (uint32_t)(min((int64_t)16, rows - 16 * lane) * K));
+    __syncwarp();
+    for (int64_t r = lane; r < rows; r += 32)
+      bulk_g2s(ws + r * pitch, p.Wq + (n0 + r) * K, (uint32_t)K, &sm.wbar[r / 16]);
+#pragma unroll
+    for (int i = 0; i < 2; i++)
+      if (lane + 32 * i < kDecMaxRows) sm.bias[lane + 32 * i] = bv[i];
+    __syncwarp();  // lane 0's arrival on wobar below publishes the bias to the epilogue
+    // W16 at the first outlier columns, one TMA box (8 columns x the slice's
+    // channels) per column, once the consumers have listed them
+    const bool ok = mbar_wait_bounded(&sm.lbar, 0, p.status);
+    const int32_t nsmall = ok ? min((int32_t)sm.nO, kDecOutSmall) : 0;
+    const bool fetch = !kWq && nsmall > 0;
+    if (lane == 0) mbar_expect_tx(&sm.wobar, fetch ? (uint32_t)(nsmall * 16 * p.rows_per_cta) : 0u);
+    __syncwarp();
+    if (fetch && lane < nsmall)
+      tma_load_2d(&sm.wos[lane][0][0], &tm_w16, (int32_t)(sm.oc[lane] & ~7u), (int32_t)n0,
+                  &sm.wobar);
+    // no copy outlives the CTA
+    for (int i = 0; i < nt; i++) (void)mbar_wait_bounded(&sm.wbar[i], 0, p.status);
+    (void)mbar_wait_bounded(&sm.wobar, 0, p.status);
+    return;
+  }
+
+  // ---- activation pass: thread v owns columns [8v, 8v + 8) of every row ----
+  const int64_t v = threadIdx.x;
+  const bool live = v < vecs;
+  uint4 x[kLocMaxT];
+#pragma unroll
+  for (int t = 0; t < kLocMaxT; t++)  // all loads in flight before any is used
+    x[t] = (t < T && live) ? __ldg(p.X + t * vecs + v) : make_uint4(0, 0, 0, 0);
+  named_bar_arrive(2, kDecThreads);
+  // a column is an outlier if any of the call's rows has |x| >= tau there
+  uint32_t flags = 0;
+#pragma unroll
+  for (int t = 0; t < kLocMaxT; t++) {
+    if (t < T) {
+      const uint32_t w[4] = {x[t].x, x[t].y, x[t].z, x[t].w};
+#pragma unroll
+      for (int i = 0; i < 4; i++) {
+        flags |= (uint32_t)(abs_bits_lo(w[i]) >= p.thr) << (2 * i);
+        flags |= (uint32_t)(abs_bits_hi(w[i]) >= p.thr) << (2 * i + 1);
+      }
+    }
+  }
+  if (!live) flags = 0;
+  // each row's maximum over the non-outlier columns, and the outlier count
+#pragma unroll
+  for (int t = 0; t < kLocMaxT; t++) {
+    if (t < T) {
+      const uint32_t w[4] = {x[t].x, x[t].y, x[t].z, x[t].w};
+      uint32_t m = 0;
+#pragma unroll
+      for (int i = 0; i < 4; i++) {
+        if (!((flags >> (2 * i)) & 1)) m = max(m, abs_bits_lo(w[i]));
+        if (!((flags >> (2 * i + 1)) & 1)) m = max(m, abs_bits_hi(w[i]));
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+      if (lane == 0) sm.part[warp][t] = m;
+    }
+  }
+  const uint32_t pc = __popc(flags);
+  uint32_t incl = pc;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) sm.wcnt[warp] = incl;
+  named_bar_sync(1, kDecConsumers);
+  if (warp == 0) {
+    if (lane < kLocMaxT) {
+      uint32_t m = 0;
+      if (lane < T)
+#pragma unroll
+        for (int w = 0; w < kDecWarps; w++) m = max(m, sm.part[w][lane]);
+      sm.sxb[lane] = m;
+      const RowCode<kBf> rc(e2f<kBf>(m));  // one division per row, for every thread
+      sm.rcv[lane] = make_float4(rc.a, rc.r, rc.s1, rc.s2);
+    } else if (lane < kLocMaxT + kDecWarps) {
+      const int w = lane - kLocMaxT;
+      uint32_t b = 0;
+      for (int u = 0; u < w; u++) b += sm.wcnt[u];
+      sm.wbase[w] = b;
+      if (w == kDecWarps - 1) sm.nO = b + sm.wcnt[w];
+    }
+  }
+  named_bar_sync(1, kDecConsumers);
+  // codes rint(fl32(127 x) / sx) of the non-outlier columns, 0 at the outliers
+#pragma unroll
+  for (int t = 0; t < kLocMaxT; t++) {
+    if (t < T && live) {
+      const float4 cv = sm.rcv[t];
+      RowCode<kBf> rc;
+      rc.a = cv.x;
+      rc.r = cv.y;
+      rc.s1 = cv.z;
+      rc.s2 = cv.w;
+      const uint32_t w[4] = {x[t].x, x[t].y, x[t].z, x[t].w};
+      uint32_t p0, p1;
+      rc.codes8(w, flags, p0, p1);
+      *reinterpret_cast<uint2 *>(xs + t * pitch + 8 * v) = make_uint2(p0, p1);
+    }
+  }
+  // the ascending outlier list (thread order is column order), and X at the
+  // first kDecOutSmall of them
+  const uint32_t nO = sm.nO;
+  if (flags) {
+    uint32_t j = sm.wbase[warp] + incl - pc;
+    for (int b = 0; b < 8; b++)
+      if ((flags >> b) & 1) {
+        const uint32_t col = (uint32_t)(8 * v + b);
+        ocols[j] = (uint16_t)col;
+        if (blockIdx.x == 0) p.O_out[j] = (int32_t)col;
+        if (j < (uint32_t)kDecOutSmall) {
+          sm.oc[j] = col;
+#pragma unroll
+          for (int t = 0; t < kLocMaxT; t++)
+            if (t < T) sm.xo[t * kDecOutSmall + j] = ((&x[t].x)[b >> 1] >> (16 * (b & 1))) & 0xffffu;
+        }
+        ++j;
+      }
+  }
+  if (blockIdx.x == 0 && threadIdx.x == 0) *p.nO_out = nO;
+  bool have = true;
+  // forced-timeout test option: one thread of CTA 0 waits on a barrier
+  // nothing completes and gives up, so that CTA's consumers take the timeout
+  // path below
+  if (p.force_timeout && blockIdx.x == 0 && threadIdx.x == 0 &&
+      !mbar_wait_bounded(&sm.never, 0, p.status, kForcedWaitNs))
+    have = false;
+  // codes, outlier list and X values in place (the same outcome for every
+  // consumer thread)
+  have = named_bar_and(1, kDecConsumers, have);
+  if (threadIdx.x == 0) mbar_arrive(&sm.lbar);  // the producer may fetch W16's columns
+  if (blockIdx.x == 0) {  // the activation pass's results, for the debug entry point
+    if (threadIdx.x < T) p.sx_out[threadIdx.x] = e2f<kBf>(sm.sxb[threadIdx.x]);
+    if (p.dbg_xq)
+      for (int64_t i = threadIdx.x; i < (int64_t)T * vecs; i += kDecConsumers) {
+        const int64_t t = i / vecs, vv = i - t * vecs;
+        reinterpret_cast<uint2 *>(p.dbg_xq)[i] = *reinterpret_cast<const uint2 *>(xs + t * pitch + 8 * vv);
+      }
+  }
+  if (!have) return;  // the producer still waits for every copy before it exits
+
+  // ---- MMA warps: K-range [k0, k1) of every tile, A = weight, B = codes of X ----
+  const int g = lane >> 2, q = lane & 3;
+  // epilogue item of this thread: accumulator word idx = i / 32 of lane i % 32
+  // (tile idx / 4, word idx % 4: channel 16 tile + g' + 8 (word / 2), token
+  // 2 q' + word % 2); the channel scale is loaded while the MMAs run
+  const int el = threadIdx.x & 31, eidx = threadIdx.x >> 5;
+  const bool eitem = eidx < 4 * kLocTiles;
+  const int e_n = (eidx >> 2) * 16 + (el >> 2) + 8 * ((eidx & 3) >> 1);
+  const int e_t = 2 * (el & 3) + (eidx & 1);
+  const bool e_live = eitem && e_n < rows && e_t < T;
+  const float e_sw = e_live ? __ldg(p.sw + n0 + e_n) : 0.f;
+
+  const int64_t k0 = warp * range, k1 = min(K, k0 + range);
+  const int nkb = k1 > k0 ? (int)((k1 - k0 + 63) / 64) : 0;  // <= 4
+  uint32_t xg[4][8];  // token g's codes of this warp's blocks, widened (0 past K)
+#pragma unroll
+  for (int b = 0; b < 4; b++) {
+    const int64_t kb = k0 + 64 * b;
+    if (b < nkb && kb + 16 * q < k1) {
+      widen16(*reinterpret_cast<const uint4 *>(xs + g * pitch + kb + 16 * q), xg[b]);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; i++) xg[b][i] = 0u;
+    }
+  }
+  int acc[kLocTiles][4] = {};
+  bool landed = true;
+#pragma unroll
+  for (int ti = 0; ti < kLocTiles; ti++) {
+    if (ti < nt) {
+      landed = mbar_wait_bounded(&sm.wbar[ti], 0, p.status) && landed;
+      const uint8_t *wa = ws + min((int64_t)(16 * ti + g), rows - 1) * pitch + 16 * q;
+      const uint8_t *wb = ws + min((int64_t)(16 * ti + g + 8), rows - 1) * pitch + 16 * q;
+      float f[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int b = 0; b < 4; b++) {
+        if (b < nkb) {
+          const int64_t kb = k0 + 64 * b;
+          uint32_t ha[8], hb[8];
+          widen16(*reinterpret_cast<const uint4 *>(wa + kb), ha);
+          widen16(*reinterpret_cast<const uint4 *>(wb + kb), hb);
+#pragma unroll
+          for (int mm = 0; mm < 4; mm++)
+            mma_f16_16x8x16(f, ha[2 * mm], hb[2 * mm], ha[2 * mm + 1], hb[2 * mm + 1],
+                            xg[b][2 * mm], xg[b][2 * mm + 1]);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 4; j++) acc[ti][j] = __float2int_rn(f[j]);
+    }
+  }
+  // Only the int8 weight kept (W16 null): the outlier weights are the slice's
+  // own codes, Wq sw / 127, with sw / 127 applied in the epilogue; they are
+  // read before the reduction reuses the weight region.
+  const int nsmall = nO < (uint32_t)kDecOutSmall ? (int)nO : kDecOutSmall;
+  float e_out = 0.f;
+  if (kWq) {
+    bool all = true;
+    for (int ti = 0; ti < nt; ti++) all = mbar_wait_bounded(&sm.wbar[ti], 0, p.status) && all;
+    if (all && e_live)
+      for (int j = 0; j < nsmall; j++)
+        e_out = fmaf(e2f<kBf>(sm.xo[e_t * kDecOutSmall + j]),
+                     (float)(int8_t)ws[e_n * pitch + sm.oc[j]], e_out);
+  }
+  // outlier columns beyond the first kDecOutSmall: split over the warps
+  const bool big = nO > (uint32_t)kDecOutSmall;  // the same in every warp
+  float o[kLocTiles][4] = {};
+  for (uint32_t j = kDecOutSmall + warp; big && j < nO; j += kDecWarps) {
+    const int64_t k = ocols[j];
+    const float x0 = 2 * q < T ? e2f<kBf>(__ldg(p.X16 + (int64_t)(2 * q) * K + k)) : 0.f;
+    const float x1 = 2 * q + 1 < T ? e2f<kBf>(__ldg(p.X16 + (int64_t)(2 * q + 1) * K + k)) : 0.f;
+#pragma unroll
+    for (int ti = 0; ti < kLocTiles; ti++) {
+      if (ti < nt) {
+        const int64_t ra = min((int64_t)(16 * ti + g), rows - 1);
+        const int64_t rb = min((int64_t)(16 * ti + g + 8), rows - 1);
+        const float wa = kWq ? (float)(int8_t)ws[ra * pitch + k]
+                             : e2f<kBf>(__ldg(p.W16 + (n0 + ra) * K + k));
+        const float wb = kWq ? (float)(int8_t)ws[rb * pitch + k]
+                             : e2f<kBf>(__ldg(p.W16 + (n0 + rb) * K + k));
+        o[ti][0] = fmaf(wa, x0, o[ti][0]);
+        o[ti][1] = fmaf(wa, x1, o[ti][1]);
+        o[ti][2] = fmaf(wb, x0, o[ti][2]);
+        o[ti][3] = fmaf(wb, x1, o[ti][3]);
+      }
+    }
+  }
+  // cross-warp reduction in the weight region, once every warp is past its MMAs
+  named_bar_sync(1, kDecConsumers);
+  uint32_t *mine = red + (warp * 32 + lane) * kLocRedStride;
+#pragma unroll
+  for (int ti = 0; ti < kLocTiles; ti++)
+#pragma unroll
+    for (int j = 0; j < 4; j++) mine[ti * 4 + j] = (uint32_t)acc[ti][j];
+  named_bar_sync(1, kDecConsumers);
+  int e_acc = 0;
+  if (eitem)
+#pragma unroll
+    for (int w = 0; w < kDecWarps; w++) e_acc += (int)red[(w * 32 + el) * kLocRedStride + eidx];
+  if (big) {
+    named_bar_sync(1, kDecConsumers);
+#pragma unroll
+    for (int ti = 0; ti < kLocTiles; ti++)
+#pragma unroll
+      for (int j = 0; j < 4; j++) mine[ti * 4 + j] = __float_as_uint(o[ti][j]);
+    named_bar_sync(1, kDecConsumers);
+    if (eitem)
+#pragma unroll
+      for (int w = 0; w < kDecWarps; w++)
+        e_out += __uint_as_float(red[(w * 32 + el) * kLocRedStride + eidx]);
+  }
+  // the first outlier columns: X from the activation pass, W16 from the TMA boxes
+  const bool ok_o = mbar_wait_bounded(&sm.wobar, 0, p.status);
+  if (!kWq && e_live)
+    for (int j = 0; j < nsmall; j++)
+      e_out = fmaf(e2f<kBf>(sm.xo[e_t * kDecOutSmall + j]),
+                   e2f<kBf>(sm.wos[j][e_n][sm.oc[j] & 7u]), e_out);
+  if (e_live && ok_o && landed) {
+    const int64_t n = n0 + e_n;
+    const float st = e2f<kBf>(sm.sxb[e_t]) / 127.0f, sn = e_sw / 127.0f;
+    const float b = e2f<kBf>(sm.bias[e_n]);  // 0 without a bias
+    const float y = kWq ? fmaf(fmaf((float)e_acc, st, e_out), sn, b)
+                        : fmaf((float)e_acc * st, sn, e_out + b);
+    p.Y[e_t * p.N + n] = f2e<kBf>(y);
+    if (p.dbg_acc) p.dbg_acc[e_t * p.N + n] = e_acc;
+  }
+}
+
+// ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
 
 namespace {
 
-constexpr int kDecClusterSizes[3] = {8, 16, 4};  // the kernels built (index into DecCfg::ctas)
+// the kernels built (index into DecCfg::ctas): dec_fused in clusters of 8, 16
+// or 4 CTAs, and dec_local (1: no cluster)
+constexpr int kDecClusterSizes[4] = {8, 16, 4, 1};
+constexpr int kDecLocal = 3;
 // Order of preference over kDecClusterSizes, measured per call in 16-layer
 // CUDA graphs at N 3900 (both sizes hold it): 16-CTA clusters are 3-8 %
 // faster than 8-CTA ones while T K <= 32768 (every T <= 16 at K 2048, T <= 8
@@ -675,6 +1022,12 @@ constexpr int kDecClusterSizes[3] = {8, 16, 4};  // the kernels built (index int
 constexpr int64_t kDecSmallWork = 32768;
 constexpr int kDecPreferSmall[3] = {1, 0, 2};  // T K <= kDecSmallWork: 16, 8, 4
 constexpr int kDecPreferLarge[3] = {0, 1, 2};  // otherwise: 8, 16, 4
+// dec_local comes first for T <= kLocFirstT, and serves T <= kLocMaxT where
+// no cluster size holds the call.  Measured per call at K = N = 4096 (16-layer
+// CUDA graphs): 7.8 / 8.2 / 9.1 / 10.6 us at T 1 / 2 / 4 / 8, against
+// 9.6 / 9.6 / 9.7 / 10.2 us for the best cluster size; its activation pass
+// costs every CTA the whole T x K codes.
+constexpr int64_t kLocFirstT = 4;
 
 // CTAs of dec_fused<kC> resident at once, in whole clusters (0 if the query
 // fails); also opens the kernel's shared-memory limit to `dyn_max`.
@@ -710,38 +1063,62 @@ int dec_resident_ctas(int dyn_max) {
   return least * kC;
 }
 
+// CTAs of dec_local resident at once (0 if the query fails); also opens the
+// kernel's shared-memory limit to `dyn_max`.
+int dec_local_ctas(int dev, int dyn_max) {
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  int least = 1 << 30;
+  for (auto *f : {dec_local_kernel<false, false>, dec_local_kernel<true, false>,
+                  dec_local_kernel<false, true>, dec_local_kernel<true, true>}) {
+    if (cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn_max) !=
+        cudaSuccess)
+      return 0;
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+            &n, f, kDecThreads, decode_smem_bytes(kDecodeMaxK, 32, kLocMaxT)) != cudaSuccess)
+      n = 0;
+    least = n < least ? n : least;  // every form must fit
+  }
+  return least * sms;
+}
+
 struct DecCfg {
-  int ctas[3];  // resident CTAs for each entry of kDecClusterSizes (0: not available)
+  int ctas[4];  // resident CTAs for each entry of kDecClusterSizes (0: not available)
   int dyn_max;  // dynamic shared memory a CTA may use
 };
 
 // Queried once per device; the nominal B300 figures when no device answers.
 DecCfg decode_cfg(int dev) {
-  static std::atomic<int64_t> cache[64][2];
-  if (dev >= 0 && dev < 64) {
-    const int64_t v = cache[dev][0].load(std::memory_order_relaxed);
-    if (v > 0)
-      return DecCfg{{(int)(v & 0xffff), (int)((v >> 16) & 0xffff), (int)(v >> 32)},
-                    (int)cache[dev][1].load(std::memory_order_relaxed)};
+  static std::atomic<int> cache[64][6];  // ctas[0..3], dyn_max, valid
+  if (dev >= 0 && dev < 64 && cache[dev][5].load(std::memory_order_acquire) == 1) {
+    DecCfg r;
+    for (int i = 0; i < 4; i++) r.ctas[i] = cache[dev][i].load(std::memory_order_relaxed);
+    r.dyn_max = cache[dev][4].load(std::memory_order_relaxed);
+    return r;
   }
   int optin = 0;
-  cudaFuncAttributes fa = {};
-  DecCfg r{{0, 0, 0}, 0};
-  if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev < 0 ? 0 : dev) ==
+  cudaFuncAttributes fa = {}, fl = {};
+  DecCfg r{{0, 0, 0, 0}, 0};
+  const int qdev = dev < 0 ? 0 : dev;
+  if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, qdev) ==
           cudaSuccess &&
-      cudaFuncGetAttributes(&fa, dec_fused_kernel<8, false, false>) == cudaSuccess) {
-    r.dyn_max = optin - (int)fa.sharedSizeBytes;
+      cudaFuncGetAttributes(&fa, dec_fused_kernel<8, false, false>) == cudaSuccess &&
+      cudaFuncGetAttributes(&fl, dec_local_kernel<false, false>) == cudaSuccess) {
+    r.dyn_max = optin - (int)(fa.sharedSizeBytes > fl.sharedSizeBytes ? fa.sharedSizeBytes
+                                                                       : fl.sharedSizeBytes);
     r.ctas[0] = dec_resident_ctas<8>(r.dyn_max);
     r.ctas[1] = dec_resident_ctas<16>(r.dyn_max);
     r.ctas[2] = dec_resident_ctas<4>(r.dyn_max);
+    r.ctas[3] = dec_local_ctas(qdev, r.dyn_max);
   }
   (void)cudaGetLastError();  // a failed query is not a launch error
-  if (r.ctas[0] + r.ctas[1] + r.ctas[2] == 0)
-    return DecCfg{{0, 0, kB300Sms / 4 * 4}, (int)decode_smem_bytes(kDecodeMaxK, 32)};
+  if (r.ctas[0] + r.ctas[1] + r.ctas[2] + r.ctas[3] == 0)
+    return DecCfg{{0, 0, kB300Sms / 4 * 4, 0}, (int)decode_smem_bytes(kDecodeMaxK, 32)};
   if (dev >= 0 && dev < 64) {
-    cache[dev][1].store(r.dyn_max, std::memory_order_relaxed);
-    cache[dev][0].store((int64_t)r.ctas[0] | ((int64_t)r.ctas[1] << 16) | ((int64_t)r.ctas[2] << 32),
-                        std::memory_order_relaxed);
+    for (int i = 0; i < 4; i++) cache[dev][i].store(r.ctas[i], std::memory_order_relaxed);
+    cache[dev][4].store(r.dyn_max, std::memory_order_relaxed);
+    cache[dev][5].store(1, std::memory_order_release);
   }
   return r;
 }
@@ -753,30 +1130,42 @@ int64_t dec_rows_cap(const DecCfg &c, int64_t K, int64_t xrows = 16) {
   return rows;
 }
 
-// The index (into kDecClusterSizes) of the first cluster size, in the order
-// of preference for T K, whose resident CTAs hold N output channels in one
-// wave; -1 if none does.  A call may ask for a size (`want`, 0 = no
-// preference), which is taken whenever it holds the call.
+// Whether the resident CTAs of kernel i (index into kDecClusterSizes) hold
+// N output channels in one wave.
+bool decode_holds(const DecCfg &c, int i, int64_t T, int64_t N, int64_t K) {
+  if (i == kDecLocal && T > kLocMaxT) return false;
+  const int64_t cap = dec_rows_cap(c, K, i == kDecLocal ? kLocMaxT : dec_xrows(T));
+  return c.ctas[i] >= (N + cap - 1) / cap;
+}
+
+// The index (into kDecClusterSizes) of the first kernel, in the order of
+// preference for T and K, that holds the call; -1 if none does.  A call may
+// ask for a cluster size (`want`, 0 = no preference; 1 = dec_local), which is
+// taken whenever it holds the call.
 int decode_pick(const DecCfg &c, int64_t T, int64_t N, int64_t K, int want) {
-  const int64_t cap = dec_rows_cap(c, K, dec_xrows(T));
-  const int64_t need = (N + cap - 1) / cap;
-  for (int i = 0; i < 3; i++)
-    if (want != 0 && kDecClusterSizes[i] == want && c.ctas[i] >= need) return i;
+  for (int i = 0; i < 4; i++)
+    if (want != 0 && kDecClusterSizes[i] == want && decode_holds(c, i, T, N, K)) return i;
+  if (T <= kLocFirstT && decode_holds(c, kDecLocal, T, N, K)) return kDecLocal;
   const int *order = T * K <= kDecSmallWork ? kDecPreferSmall : kDecPreferLarge;
   for (int j = 0; j < 3; j++)
-    if (c.ctas[order[j]] >= need) return order[j];
-  return -1;
+    if (decode_holds(c, order[j], T, N, K)) return order[j];
+  return decode_holds(c, kDecLocal, T, N, K) ? kDecLocal : -1;
 }
 
 }  // namespace
 
-// Output channels the decode path takes at this K: what the resident CTAs of
-// the best-covered cluster size hold.
-int64_t decode_max_n(int dev, int64_t K) {
+// Output channels the decode path takes at this T and K: what the resident
+// CTAs of the best-covered kernel hold.
+int64_t decode_max_n(int dev, int64_t T, int64_t K) {
   const DecCfg c = decode_cfg(dev);
   const int most = c.ctas[0] > c.ctas[1] ? (c.ctas[0] > c.ctas[2] ? c.ctas[0] : c.ctas[2])
                                          : (c.ctas[1] > c.ctas[2] ? c.ctas[1] : c.ctas[2]);
-  return (int64_t)most * dec_rows_cap(c, K);
+  int64_t n = (int64_t)most * dec_rows_cap(c, K, dec_xrows(T));
+  if (T <= kLocMaxT) {
+    const int64_t nl = (int64_t)c.ctas[kDecLocal] * dec_rows_cap(c, K, kLocMaxT);
+    n = nl > n ? nl : n;
+  }
+  return n;
 }
 
 cudaError_t launch_decode(const void *X, int64_t T, int64_t K, uint32_t thr, const int8_t *Wq,
@@ -788,6 +1177,7 @@ cudaError_t launch_decode(const void *X, int64_t T, int64_t K, uint32_t thr, con
   const DecCfg dc = decode_cfg(dev);
   const int pick = decode_pick(dc, T, N, K, (int)((opts >> 8) & 0xffu));
   if (pick < 0) return cudaErrorInvalidValue;  // the host routes only shapes that fit here
+  const bool local = pick == kDecLocal;
   const int kc = kDecClusterSizes[pick];
   DecArgs a;
   a.X = reinterpret_cast<const uint4 *>(X);
@@ -803,7 +1193,7 @@ cudaError_t launch_decode(const void *X, int64_t T, int64_t K, uint32_t thr, con
   const int64_t used = (N + a.rows_per_cta - 1) / a.rows_per_cta;
   const int64_t ctas = (used + kc - 1) / kc * kc;
   a.wregion = dec_wregion(K, a.rows_per_cta);
-  a.xrows = (int)dec_xrows(T);
+  a.xrows = local ? kLocMaxT : (int)dec_xrows(T);
   // W16 in boxes of 8 columns x one slice's channels (outlier columns only,
   // so no L2 promotion beyond the sector)
   // (without W16 the map is never read: it then describes Wq)
@@ -834,23 +1224,32 @@ cudaError_t launch_decode(const void *X, int64_t T, int64_t K, uint32_t thr, con
   cfg.dynamicSmemBytes = decode_smem_bytes(K, a.rows_per_cta, a.xrows);
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = (unsigned)kc;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  unsigned na = 0;
+  if (!local) {
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = (unsigned)kc;
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = 1;
+    na++;
+  }
+  if (!(opts & BNB_OPT_NO_PDL)) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    na++;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = (opts & BNB_OPT_NO_PDL) ? 1 : 2;
+  cfg.numAttrs = na;
   const int form = (W16 == nullptr ? 1 : 0) | (bf16 ? 2 : 0);
   using Kern = void (*)(CUtensorMap, DecArgs);
-  static const Kern kerns[3][4] = {
+  static const Kern kerns[4][4] = {
       {dec_fused_kernel<8, false, false>, dec_fused_kernel<8, true, false>,
        dec_fused_kernel<8, false, true>, dec_fused_kernel<8, true, true>},
       {dec_fused_kernel<16, false, false>, dec_fused_kernel<16, true, false>,
        dec_fused_kernel<16, false, true>, dec_fused_kernel<16, true, true>},
       {dec_fused_kernel<4, false, false>, dec_fused_kernel<4, true, false>,
-       dec_fused_kernel<4, false, true>, dec_fused_kernel<4, true, true>}};
+       dec_fused_kernel<4, false, true>, dec_fused_kernel<4, true, true>},
+      {dec_local_kernel<false, false>, dec_local_kernel<true, false>,
+       dec_local_kernel<false, true>, dec_local_kernel<true, true>}};
   const cudaError_t e = cudaLaunchKernelEx(&cfg, kerns[pick][form], tm, a);
   note_launch();
   return e;

@@ -37,11 +37,11 @@ cudaError_t launch_quantize_blockwise(const float *x, int64_t n, int B, int8_t *
 cudaError_t launch_dequantize_blockwise(const int8_t *codes, const float *absmax, int64_t n,
                                         int B, float *y, int num_sms, cudaStream_t stream);
 
-// The whole layer for T <= 16, K <= kDecodeMaxK, N <= decode_max_n(dev, K)
-// in one kernel (activation pass fused into the GEMV and shared by clusters
-// of CTAs), launched with programmatic dependent launch unless the call's
-// options turn it off.
-int64_t decode_max_n(int dev, int64_t K);
+// The whole layer for T <= 16, K <= kDecodeMaxK, N <= decode_max_n(dev, T, K)
+// in one kernel (activation pass fused into the GEMV: shared by clusters of
+// CTAs, or repeated by every CTA for T <= 8), launched with programmatic
+// dependent launch unless the call's options turn it off.
+int64_t decode_max_n(int dev, int64_t T, int64_t K);
 cudaError_t launch_decode(const void *X, int64_t T, int64_t K, uint32_t thr, const int8_t *Wq,
                           const float *sw, const void *W16, const void *bias, int64_t N,
                           bool bf16, void *Y, const Workspace &ws, int8_t *dbg_xq,

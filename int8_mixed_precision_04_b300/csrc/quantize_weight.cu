@@ -39,16 +39,10 @@ __global__ void __launch_bounds__(256) quantize_weight_kernel(
     uint2 *out = reinterpret_cast<uint2 *>(Wq + n * K);
     for (int64_t v = lane; v < vecs; v += 32) {
       uint4 q = __ldg(row + v);
-      uint32_t w[4] = {q.x, q.y, q.z, q.w};
-      uint32_t packed[2] = {0, 0};
-#pragma unroll
-      for (int i = 0; i < 4; i++) {
-        const uint32_t c0 = rc.byte(e2f<kBf>(w[i] & 0xffffu));
-        const uint32_t c1 = rc.byte(e2f<kBf>(w[i] >> 16));
-        uint32_t two = (c0 & 0xffu) | ((c1 & 0xffu) << 8);
-        packed[i / 2] |= two << (16 * (i % 2));
-      }
-      out[v] = make_uint2(packed[0], packed[1]);
+      const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+      uint32_t p0, p1;
+      rc.codes8(w, 0u, p0, p1);
+      out[v] = make_uint2(p0, p1);
     }
   }
 }

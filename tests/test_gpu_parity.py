@@ -50,6 +50,25 @@ def test_decode_cluster_sizes(orc, cluster, T, K, N, ncols):
                     opts=binding.OPT_CLUSTER(cluster))
 
 
+@pytest.mark.parametrize("cluster", [1, 16, 8])
+@pytest.mark.parametrize("T,K,N,ncols", [
+    (1, 4096, 4096, 4), (8, 4096, 5900, 70), (2, 272, 200, 2), (7, 1040, 96, 70),
+    (3, 2048, 520, 9), (8, 16, 1, 0), (4, 4096, 40, 12), (5, 4096, 4100, 1),
+])
+def test_decode_local(orc, cluster, T, K, N, ncols):
+    """T <= 8 without clusters (every CTA runs the whole activation pass and
+    takes up to three 16-channel weight tiles as A operands; BNB_OPT_CLUSTER(1),
+    the default there), against the clustered kernel forced on the same
+    shapes: slices of 8 to 40 channels (a partial last tile), K not a multiple
+    of the warps' K-ranges, more outlier columns than the TMA boxes take, and
+    N up to what the resident CTAs hold without clusters."""
+    from int8_mixed_precision_04_b300 import binding
+    assert binding.load().bnb_int8_linear_path(T, N, K) == 1
+    w = inputs.random_small(T, K, N, ncols, seed=3 * K + N + T, tau=6.0)
+    run_and_compare(orc, w.X, w.W, 6.0, what=f"decode local/cluster {cluster} T{T} K{K} N{N}",
+                    opts=binding.OPT_CLUSTER(cluster))
+
+
 @pytest.mark.parametrize("T", [1, 5, 16])
 def test_decode_on_the_gemm(orc, T):
     """The decode workload through the tcgen05 GEMM's 32-token tile
