@@ -676,11 +676,8 @@ struct DecLocSmall {
   uint64_t never;            // completed by nothing (forced-timeout test option)
   // [j][row][8]: W16[n0 + row, 8 (O[j] / 8) .. + 8), one TMA box per outlier column j
   alignas(128) uint16_t wos[kDecOutSmall][kDecMaxRows][8];
-  uint32_t part[kDecWarps][kLocMaxT];  // [warp][t] partial row maxima (16-bit magnitude bits)
   uint32_t wcnt[kDecWarps];            // outliers of each warp's 256 columns
-  uint32_t wbase[kDecWarps];           // outliers of the warps before it
-  uint32_t sxb[kLocMaxT];              // row maxima (16-bit bits)
-  float4 rcv[kLocMaxT];                // each row's code rule (RowCode a, r, s1, s2)
+  uint32_t sxb[kLocMaxT];              // row maxima (16-bit magnitude bits; shared atomic max)
   uint32_t nO;
   uint32_t xo[kLocMaxT * kDecOutSmall];  // [t][j] X at the first outlier columns (16-bit bits)
   uint32_t oc[kDecOutSmall];             // the first outlier columns
@@ -713,6 +710,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     mbar_init(&sm.never, 1);
     mbar_init_fence();
   }
+  if (threadIdx.x < kLocMaxT) sm.sxb[threadIdx.x] = 0u;
   __syncthreads();
   pdl_trigger();  // the next kernel on the stream may launch; it waits for our completion
   pdl_wait();     // X may be the output of the previous kernel on the stream
@@ -789,7 +787,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
-      if (lane == 0) sm.part[warp][t] = m;
+      if (lane == 0) atomicMax(&sm.sxb[t], m);
     }
   }
   const uint32_t pc = __popc(flags);
@@ -801,45 +799,37 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   }
   if (lane == 31) sm.wcnt[warp] = incl;
   named_bar_sync(1, kDecConsumers);
-  if (warp == 0) {
-    if (lane < kLocMaxT) {
-      uint32_t m = 0;
-      if (lane < T)
+  // The row maxima are final (shared atomic max); every warp sums the 16
+  // warps' outlier counts itself (lane w reads warp w's), and lane t builds
+  // row t's code rule (its one division) for the warp.
+  const uint32_t lc = lane < kDecWarps ? sm.wcnt[lane] : 0u;
+  uint32_t before = lane < warp ? lc : 0u, nO = lc;
 #pragma unroll
-        for (int w = 0; w < kDecWarps; w++) m = max(m, sm.part[w][lane]);
-      sm.sxb[lane] = m;
-      const RowCode<kBf> rc(e2f<kBf>(m));  // one division per row, for every thread
-      sm.rcv[lane] = make_float4(rc.a, rc.r, rc.s1, rc.s2);
-    } else if (lane < kLocMaxT + kDecWarps) {
-      const int w = lane - kLocMaxT;
-      uint32_t b = 0;
-      for (int u = 0; u < w; u++) b += sm.wcnt[u];
-      sm.wbase[w] = b;
-      if (w == kDecWarps - 1) sm.nO = b + sm.wcnt[w];
-    }
+  for (int o = 16; o > 0; o >>= 1) {
+    before += __shfl_xor_sync(0xffffffffu, before, o);
+    nO += __shfl_xor_sync(0xffffffffu, nO, o);
   }
-  named_bar_sync(1, kDecConsumers);
+  if (threadIdx.x == 0) sm.nO = nO;  // for the producer warp
+  const RowCode<kBf> rc_lane(e2f<kBf>(lane < T ? sm.sxb[lane] : 0u));
   // codes rint(fl32(127 x) / sx) of the non-outlier columns, 0 at the outliers
 #pragma unroll
   for (int t = 0; t < kLocMaxT; t++) {
-    if (t < T && live) {
-      const float4 cv = sm.rcv[t];
+    if (t < T) {
       RowCode<kBf> rc;
-      rc.a = cv.x;
-      rc.r = cv.y;
-      rc.s1 = cv.z;
-      rc.s2 = cv.w;
+      rc.a = __shfl_sync(0xffffffffu, rc_lane.a, t);
+      rc.r = __shfl_sync(0xffffffffu, rc_lane.r, t);
+      rc.s1 = kBf ? __shfl_sync(0xffffffffu, rc_lane.s1, t) : 1.0f;
+      rc.s2 = kBf ? __shfl_sync(0xffffffffu, rc_lane.s2, t) : 1.0f;
       const uint32_t w[4] = {x[t].x, x[t].y, x[t].z, x[t].w};
       uint32_t p0, p1;
       rc.codes8(w, flags, p0, p1);
-      *reinterpret_cast<uint2 *>(xs + t * pitch + 8 * v) = make_uint2(p0, p1);
+      if (live) *reinterpret_cast<uint2 *>(xs + t * pitch + 8 * v) = make_uint2(p0, p1);
     }
   }
   // the ascending outlier list (thread order is column order), and X at the
   // first kDecOutSmall of them
-  const uint32_t nO = sm.nO;
   if (flags) {
-    uint32_t j = sm.wbase[warp] + incl - pc;
+    uint32_t j = before + incl - pc;
     for (int b = 0; b < 8; b++)
       if ((flags >> b) & 1) {
         const uint32_t col = (uint32_t)(8 * v + b);
@@ -1024,7 +1014,7 @@ constexpr int kDecPreferSmall[3] = {1, 0, 2};  // T K <= kDecSmallWork: 16, 8, 4
 constexpr int kDecPreferLarge[3] = {0, 1, 2};  // otherwise: 8, 16, 4
 // dec_local comes first for T <= kLocFirstT, and serves T <= kLocMaxT where
 // no cluster size holds the call.  Measured per call at K = N = 4096 (16-layer
-// CUDA graphs): 7.8 / 8.2 / 9.1 / 10.6 us at T 1 / 2 / 4 / 8, against
+// CUDA graphs): 7.4 / 7.8 / 8.7 / 10.5 us at T 1 / 2 / 4 / 8, against
 // 9.6 / 9.6 / 9.7 / 10.2 us for the best cluster size; its activation pass
 // costs every CTA the whole T x K codes.
 constexpr int64_t kLocFirstT = 4;
