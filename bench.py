@@ -111,10 +111,10 @@ MEASURED_TRAFFIC = {
     # (kernel, T, K, N): (source file, source digest, dram read + write bytes)
     # one ncu capture of the large workload's GEMM launch: 930.92 MB read + 247.37 MB written
     ("gemm_tc", 4096, 8192, 28672): ("gemm_tc.cu", "25383f2e26f639e0", 1_178_290_000),
-    # one ncu capture of the decode workload's kernel (ncu's MB, two decimals):
-    # T 16: 19.12 MB read, 0 written; T 1: 18.99 MB read, 0 written
-    ("dec_fused", 16, 4096, 4096): ("decode.cu", "4104509d23800c34", 19_120_000),
-    ("dec_fused", 1, 4096, 4096): ("decode.cu", "4104509d23800c34", 18_990_000),
+    # one ncu capture of the decode workload's kernel (bytes): T 16 (the
+    # clustered kernel) and T 1 (the kernel without clusters), nothing written
+    ("dec_fused", 16, 4096, 4096): ("decode.cu", "adcba4d3afe72bc6", 19_117_824),
+    ("dec_local", 1, 4096, 4096): ("decode.cu", "adcba4d3afe72bc6", 18_989_312),
 }
 
 
@@ -134,7 +134,7 @@ def kernel_algorithmic(kernel, T, N, K, nO, bias=False, wq_only=False):
     """(bytes, flops) per launch of one kernel, for the roofline."""
     b = 2 * N if bias else 0
     w16 = 0 if wq_only else 2 * N * nO  # the int8-weight-only GEMM reads compacted codes instead
-    if kernel == "dec_fused":
+    if kernel in ("dec_fused", "dec_local"):
         # the whole decode call: X read once, weight codes + scales + outlier
         # weight columns (+ bias), Y written once
         return 2 * T * K + N * K + 4 * N + w16 + 2 * T * N + b, 2 * T * N * K
@@ -396,6 +396,8 @@ def measure_layer(args, w, dev, world, local, steps, min_timed_s, min_layers=2,
         # no overlap between consecutive launches
         path = out["path"]
         kname = {1: "dec_fused", 2: "gemm_tc", 3: "gemm_mma"}[path]
+        if path == 1 and binding.decode_cluster(T, N, K) == 1:
+            kname = "dec_local"  # the decode kernel without clusters
         kb, kf = kernel_algorithmic(kname, T, N, K, nO, args.bias, args.wq_only)
         res = {}
         for tag, opts in (("chain", binding.OPT_MAIN_ONLY),

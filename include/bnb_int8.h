@@ -304,13 +304,22 @@ uint64_t bnb_launch_count(void);
 
 /*
  * Which kernel path bnb_int8_linear takes for a shape on the current device:
- * 1 = decode (T <= 16, K <= 4096 and N within what the decode kernel's
- * resident CTAs hold at up to 40 output channels each: 4620 at K = 4096 on
- * B300), 2 = tensor-core GEMM (tcgen05; every other shape, decode-sized T
- * included), 3 = warp-level mma GEMM (only through bnb_int8_linear_opts with
- * BNB_OPT_LEGACY_MMA).
+ * 1 = decode (T <= 16, K <= 4096 and N within what the decode kernels'
+ * resident CTAs hold at up to 40 output channels each: at K = 4096 on B300,
+ * 4200 for T > 8 and 5920 for T <= 8), 2 = tensor-core GEMM (tcgen05; every
+ * other shape, decode-sized T included), 3 = warp-level mma GEMM (only
+ * through bnb_int8_linear_opts with BNB_OPT_LEGACY_MMA).
  */
 int bnb_int8_linear_path(int64_t T, int64_t N, int64_t K);
+
+/*
+ * For a shape that takes the decode path (bnb_int8_linear_path == 1): the
+ * form of the decode kernel bnb_int8_linear launches on the current device,
+ * as a cluster size: 16, 8 or 4 (CTAs in thread-block clusters sharing one
+ * activation pass) or 1 (no clusters: every CTA runs the whole activation
+ * pass; T <= 4 by default).  0 for any other shape.  For benchmarks and tests.
+ */
+int bnb_int8_decode_cluster(int64_t T, int64_t N, int64_t K);
 
 /*
  * Per-call options for benchmarks and tests: bnb_int8_linear_opts is

@@ -40,6 +40,7 @@ class Lib:
     SYMBOLS = ("bnb_int8_linear_workspace_bytes", "bnb_int8_quantize_weight",
                "bnb_int8_linear", "bnb_int8_linear_debug", "bnb_last_device_status",
                "bnb_status_string", "bnb_launch_count", "bnb_int8_linear_path",
+               "bnb_int8_decode_cluster",
                "bnb_int8_linear_opts", "bnb_int8_linear_noalloc",
                "bnb_int8_linear_from_host", "bnb_int8_quantize_blockwise",
                "bnb_int8_dequantize_blockwise", "bnb_int8_linear_bias",
@@ -96,6 +97,8 @@ class Lib:
         L.bnb_launch_count.argtypes = []
         L.bnb_int8_linear_path.restype = ctypes.c_int
         L.bnb_int8_linear_path.argtypes = [_I64, _I64, _I64]
+        L.bnb_int8_decode_cluster.restype = ctypes.c_int
+        L.bnb_int8_decode_cluster.argtypes = [_I64, _I64, _I64]
         L.bnb_int8_linear_opts.restype = ctypes.c_int
         L.bnb_int8_linear_opts.argtypes = L.bnb_int8_linear_debug_ex.argtypes + [ctypes.c_uint32]
         self.c = L
@@ -349,6 +352,12 @@ def launch_count() -> int:
 
 def linear_path(T: int, N: int, K: int) -> int:
     return load().bnb_int8_linear_path(T, N, K)
+
+
+def decode_cluster(T: int, N: int, K: int) -> int:
+    """The decode kernel's form for this shape (16, 8, 4: clusters; 1: none;
+    0: not the decode path)."""
+    return load().bnb_int8_decode_cluster(T, N, K)
 
 
 # Flags of bnb_int8_linear_opts (include/bnb_int8.h): per-call options for

@@ -458,4 +458,11 @@ int bnb_int8_linear_path(int64_t T, int64_t N, int64_t K) {
   return choose_path(T, N, K, dev);
 }
 
+int bnb_int8_decode_cluster(int64_t T, int64_t N, int64_t K) {
+  if (T <= 0 || N <= 0 || K <= 0) return 0;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) dev = -1;
+  return choose_path(T, N, K, dev) == 1 ? decode_cluster_size(dev, T, N, K) : 0;
+}
+
 }  // extern "C"

@@ -1158,6 +1158,11 @@ int64_t decode_max_n(int dev, int64_t T, int64_t K) {
   return n;
 }
 
+int decode_cluster_size(int dev, int64_t T, int64_t N, int64_t K) {
+  const int pick = decode_pick(decode_cfg(dev), T, N, K, 0);
+  return pick < 0 ? 0 : kDecClusterSizes[pick];
+}
+
 cudaError_t launch_decode(const void *X, int64_t T, int64_t K, uint32_t thr, const int8_t *Wq,
                           const float *sw, const void *W16, const void *bias, int64_t N,
                           bool bf16, void *Y, const Workspace &ws, int8_t *dbg_xq,

@@ -42,6 +42,9 @@ cudaError_t launch_dequantize_blockwise(const int8_t *codes, const float *absmax
 // CTAs, or repeated by every CTA for T <= 8), launched with programmatic
 // dependent launch unless the call's options turn it off.
 int64_t decode_max_n(int dev, int64_t T, int64_t K);
+// The cluster size launch_decode picks for this shape (1: no clusters), 0 if
+// none holds it.
+int decode_cluster_size(int dev, int64_t T, int64_t N, int64_t K);
 cudaError_t launch_decode(const void *X, int64_t T, int64_t K, uint32_t thr, const int8_t *Wq,
                           const float *sw, const void *W16, const void *bias, int64_t N,
                           bool bf16, void *Y, const Workspace &ws, int8_t *dbg_xq,

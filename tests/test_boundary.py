@@ -118,6 +118,11 @@ def test_paths(lib):
     assert lib.bnb_int8_linear_path(17, 4096, 4096) in (2, 3)
     assert lib.bnb_int8_linear_path(2048, 11008, 4096) in (2, 3)
     assert lib.bnb_int8_linear_path(0, 1, 16) == 0
+    # the decode kernel's form: a cluster size, 1 for no clusters, 0 off the decode path
+    assert lib.bnb_int8_decode_cluster(16, 4096, 4096) in (4, 8, 16)
+    assert lib.bnb_int8_decode_cluster(1, 4096, 4096) in (1, 4, 8, 16)
+    assert lib.bnb_int8_decode_cluster(17, 4096, 4096) == 0
+    assert lib.bnb_int8_decode_cluster(0, 1, 16) == 0
 
 
 def test_missing_library_raises(tmp_path):
