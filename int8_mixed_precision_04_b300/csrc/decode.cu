@@ -270,8 +270,9 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         if (lane + 32 * i < rows) bv[i] = __ldg(p.bias + n0 + lane + 32 * i);
     if (lane == 0) mbar_expect_tx(&sm.wbar, (uint32_t)(rows > 0 ? rows * K : 0));
     __syncwarp();
+    const uint64_t pol = l2_evict_first_policy();  // the slice is read once per call
     for (int64_t r = lane; r < rows; r += 32)
-      bulk_g2s(ws + r * pitch, p.Wq + (n0 + r) * K, (uint32_t)K, &sm.wbar);
+      bulk_g2s_once(ws + r * pitch, p.Wq + (n0 + r) * K, (uint32_t)K, &sm.wbar, pol);
 #pragma unroll
     for (int i = 0; i < 2; i++)
       if (lane + 32 * i < kDecMaxRows) sm.bias[lane + 32 * i] = bv[i];
@@ -730,8 +731,9 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         if (lane + 32 * i < rows) bv[i] = __ldg(p.bias + n0 + lane + 32 * i);
     if (lane < nt) mbar_expect_tx(&sm.wbar[lane], (uint32_t)(min((int64_t)16, rows - 16 * lane) * K));
     __syncwarp();
+    const uint64_t pol = l2_evict_first_policy();  // the slice is read once per call
     for (int64_t r = lane; r < rows; r += 32)
-      bulk_g2s(ws + r * pitch, p.Wq + (n0 + r) * K, (uint32_t)K, &sm.wbar[r / 16]);
+      bulk_g2s_once(ws + r * pitch, p.Wq + (n0 + r) * K, (uint32_t)K, &sm.wbar[r / 16], pol);
 #pragma unroll
     for (int i = 0; i < 2; i++)
       if (lane + 32 * i < kDecMaxRows) sm.bias[lane + 32 * i] = bv[i];

@@ -120,6 +120,23 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
       : "memory");
 }
 
+// The same for data read once (a decode call's weight slice): an L2
+// evict-first hint, so that the stream does not push out what later calls
+// read again.
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+__device__ __forceinline__ void bulk_g2s_once(void *dst, const void *src, uint32_t bytes,
+                                              uint64_t *bar, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1], %2, [%3], %4;" ::"r"(smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(pol)
+      : "memory");
+}
+
 // 2-D tiled tensor copy global -> shared at element coordinates (x inner, y
 // outer).  x times the element size must be a multiple of 16 bytes.
 __device__ __forceinline__ void tma_load_2d(void *dst, const void *tmap, int32_t x, int32_t y,
