@@ -49,7 +49,7 @@ __device__ __forceinline__ void codes8(const uint32_t (&w)[4], uint32_t f, const
 }
 
 constexpr int kScanThreads = 256;  // 32 lanes x 8 columns = 256 columns per block row
-constexpr int kScanUnroll = 4;     // rows of X in flight per warp
+constexpr int kScanUnroll = 8;     // rows of X in flight per warp
 
 __global__ void __launch_bounds__(kScanThreads) outlier_scan_kernel(
     const uint4 *__restrict__ X, int64_t T, int64_t K, uint32_t thr_bits,
@@ -98,8 +98,9 @@ __global__ void __launch_bounds__(kScanThreads) outlier_scan_kernel(
     const int64_t wi = (int64_t)blockIdx.x * 8 + (lane >> 2);
     if ((lane & 3) == 0 && word != 0 && wi * 32 < K) atomicOr(colmask + wi, word);
   }
-  // last-block compaction
-  __threadfence();
+  // last-block compaction (the lanes that published mask words order them
+  // before the block's count)
+  if (warp == 0) __threadfence();
   __syncthreads();
   if (threadIdx.x == 0) {
     const uint32_t total = gridDim.x * gridDim.y;
@@ -330,7 +331,8 @@ cudaError_t launch_act_pass(const void *X, int64_t T, int64_t K, uint32_t thr_bi
   int64_t want_rows_blocks = (8LL * num_sms + slabs - 1) / slabs;
   if (want_rows_blocks < 1) want_rows_blocks = 1;
   int64_t rows_per_block = (T + want_rows_blocks - 1) / want_rows_blocks;
-  if (rows_per_block < 32) rows_per_block = 32;
+  // at least one full round of loads per warp (8 warps x kScanUnroll rows)
+  if (rows_per_block < 8 * kScanUnroll) rows_per_block = 8 * kScanUnroll;
   const int64_t row_blocks = (T + rows_per_block - 1) / rows_per_block;
   dim3 grid((unsigned)slabs, (unsigned)row_blocks);
   outlier_scan_kernel<<<grid, kScanThreads, 0, stream>>>(
