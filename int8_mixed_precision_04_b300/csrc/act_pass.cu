@@ -32,20 +32,11 @@ namespace bnb {
 // The int8 codes of one 16-byte vector (8 fp16 or bf16 values, flags f:
 // outlier columns get 0) under the row's code rule rc, as two words of four
 // code bytes.  code_byte is exact and uses no conversion-pipe instruction;
-// the GEMM's fp16 integer codes come from the bytes by s8x4_to_f16x4.  (One
-// value at a time: RowCode::codes8's eight values at once raised this
-// kernel's registers from 64 to 117 and made the row pass slower.)
+// the GEMM's fp16 integer codes come from the bytes by s8x4_to_f16x4.
 template <bool kBf>
 __device__ __forceinline__ void codes8(const uint32_t (&w)[4], uint32_t f, const RowCode<kBf> &rc,
                                        uint32_t &p0, uint32_t &p1) {
-  uint32_t b[8];
-#pragma unroll
-  for (int j = 0; j < 4; j++) {
-    b[2 * j] = ((f >> (2 * j)) & 1) ? 0u : rc.byte(e2f<kBf>(w[j] & 0xffffu)) & 0xffu;
-    b[2 * j + 1] = ((f >> (2 * j + 1)) & 1) ? 0u : rc.byte(e2f<kBf>(w[j] >> 16)) & 0xffu;
-  }
-  p0 = b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24);
-  p1 = b[4] | (b[5] << 8) | (b[6] << 16) | (b[7] << 24);
+  rc.codes8(w, f, p0, p1);
 }
 
 constexpr int kScanThreads = 256;  // 32 lanes x 8 columns = 256 columns per block row
@@ -257,7 +248,9 @@ struct QuantArgs {
 };
 
 template <int kMode, bool kBf>
-__global__ void __launch_bounds__(kQuantThreads) quantize_rows_kernel(const QuantArgs p) {
+// (Three blocks per SM: the eight-at-a-time code rule fits 80 registers;
+// unbounded it took 117, and at one value at a time the pass was slower.)
+__global__ void __launch_bounds__(kQuantThreads, 3) quantize_rows_kernel(const QuantArgs p) {
   __shared__ uint32_t red[kQuantThreads / 32];
   // launched with programmatic dependent launch behind the column scan:
   // everything below reads what the scan wrote.  (No early trigger here: a
