@@ -435,9 +435,13 @@ def measure_layer(args, w, dev, world, local, steps, min_timed_s, min_layers=2,
         roof["kernel"] = kname
         roof["peak_source"] = ("measured (MEASURED_PEAKS.json)" if peak_src == "measured"
                                else "fallback")
-        roof["kernel_avg_us"] = kavg_s * 1e6
-        roof["alg_bytes_per_launch"] = kb
-        roof["alg_flops_per_launch"] = kf
+        # a decode call whose channels take several launches: per-launch figures
+        # are the call's over its launches (achieved is the same either way)
+        lpc = out["launches_per_call"] if path == 1 else 1
+        roof["launches_per_call"] = lpc
+        roof["kernel_avg_us"] = kavg_s * 1e6 / lpc
+        roof["alg_bytes_per_launch"] = kb / lpc
+        roof["alg_flops_per_launch"] = kf / lpc
         roof["timing"] = (f"graph of {layers} main-kernel-only calls x {Rk} replays "
                           f"(programmatic dependent launch on), CUDA events")
         if "alone" in res:

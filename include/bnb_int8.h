@@ -305,10 +305,11 @@ uint64_t bnb_launch_count(void);
 /*
  * Which kernel path bnb_int8_linear takes for a shape on the current device:
  * 1 = decode (T <= 16, K <= 4096 and N within what the decode kernels'
- * resident CTAs hold at up to 40 output channels each: at K = 4096 on B300,
- * 4200 for T > 8 and 5920 for T <= 8), 2 = tensor-core GEMM (tcgen05; every
- * other shape, decode-sized T included), 3 = warp-level mma GEMM (only
- * through bnb_int8_linear_opts with BNB_OPT_LEGACY_MMA).
+ * resident CTAs hold at up to 40 output channels each in at most three
+ * launches: at K = 4096 on B300, 13860 for T > 8 and 17760 for T <= 8), 2 =
+ * tensor-core GEMM (tcgen05; every other shape, decode-sized T included), 3 =
+ * warp-level mma GEMM (only through bnb_int8_linear_opts with
+ * BNB_OPT_LEGACY_MMA).
  */
 int bnb_int8_linear_path(int64_t T, int64_t N, int64_t K);
 
@@ -351,7 +352,8 @@ int bnb_int8_decode_cluster(int64_t T, int64_t N, int64_t K);
  *                       8 or 16) sharing one activation pass, or (c = 1, for
  *                       T <= 8) no clusters, every CTA running the whole
  *                       activation pass itself, instead of the form the
- *                       library picks, when that form holds the call.
+ *                       library picks, when that form holds the call in one
+ *                       launch.
  *   BNB_OPT_FORCE_TIMEOUT  one thread of the call's main kernel waits, with a
  *                       limit of about 0.1 ms, on an mbarrier that nothing
  *                       completes, and then takes the kernel's timeout path

@@ -119,6 +119,8 @@ struct DecArgs {
   int T;
   int64_t K, N;
   uint32_t thr;                // smallest fp16 magnitude bits >= tau
+  int64_t n_base, n_end;       // this launch's output channels [n_base, n_end) of N
+  int reset_status;            // the call's first launch: clears the status word
   int64_t rows_per_cta;        // <= kDecMaxRows
   int xrows;                   // code rows held: dec_xrows(T)
   int64_t wregion;             // bytes of the weight region, dec_wregion(K, rows_per_cta)
@@ -214,8 +216,8 @@ __global__ void __launch_bounds__(kDecThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int T = p.T;
-  const int64_t n0 = (int64_t)blockIdx.x * p.rows_per_cta;
-  const int64_t rows = min(p.N, n0 + p.rows_per_cta) - n0;  // <= 40; <= 0 for trailing CTAs
+  const int64_t n0 = p.n_base + (int64_t)blockIdx.x * p.rows_per_cta;
+  const int64_t rows = min(p.n_end, n0 + p.rows_per_cta) - n0;  // <= 40; <= 0 for trailing CTAs
 
   if (warp == kDecWarps && lane == 0) {
     mbar_init(&sm.wbar, 1);
@@ -237,7 +239,8 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   pdl_trigger();
   // X may be the output of the previous kernel on the stream
   pdl_wait();
-  if (blockIdx.x == 0 && threadIdx.x == 0) *p.status = kDevOk;  // a wait that gives up overwrites it
+  // a wait that gives up overwrites it (a later launch of the same call keeps it)
+  if (p.reset_status && blockIdx.x == 0 && threadIdx.x == 0) *p.status = kDevOk;
 
   uint32_t crank;
   asm("mov.u32 %0, %%cluster_ctarank;" : "=r"(crank));
@@ -699,8 +702,8 @@ __global__ void __launch_bounds__(kDecThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int T = p.T;
-  const int64_t n0 = (int64_t)blockIdx.x * p.rows_per_cta;
-  const int64_t rows = min(p.N, n0 + p.rows_per_cta) - n0;  // 1 .. 40
+  const int64_t n0 = p.n_base + (int64_t)blockIdx.x * p.rows_per_cta;
+  const int64_t rows = min(p.n_end, n0 + p.rows_per_cta) - n0;  // 1 .. 40
   const int nt = (int)((rows + 15) / 16);                    // weight tiles
 
   if (warp == kDecWarps && lane == 0) {
@@ -715,7 +718,8 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   __syncthreads();
   pdl_trigger();  // the next kernel on the stream may launch; it waits for our completion
   pdl_wait();     // X may be the output of the previous kernel on the stream
-  if (blockIdx.x == 0 && threadIdx.x == 0) *p.status = kDevOk;  // a wait that gives up overwrites it
+  // a wait that gives up overwrites it (a later launch of the same call keeps it)
+  if (p.reset_status && blockIdx.x == 0 && threadIdx.x == 0) *p.status = kDevOk;
 
   const int64_t vecs = K / 8;
   if (warp == kDecWarps) {
@@ -1124,40 +1128,61 @@ int64_t dec_rows_cap(const DecCfg &c, int64_t K, int64_t xrows = 16) {
 
 // Whether the resident CTAs of kernel i (index into kDecClusterSizes) hold
 // N output channels in one wave.
-bool decode_holds(const DecCfg &c, int i, int64_t T, int64_t N, int64_t K) {
-  if (i == kDecLocal && T > kLocMaxT) return false;
-  const int64_t cap = dec_rows_cap(c, K, i == kDecLocal ? kLocMaxT : dec_xrows(T));
-  return c.ctas[i] >= (N + cap - 1) / cap;
+// Output channels one launch of kernel i (index into kDecClusterSizes) holds
+// in one wave of its resident CTAs; 0 where the kernel does not apply.
+int64_t decode_wave(const DecCfg &c, int i, int64_t T, int64_t K) {
+  if (i == kDecLocal && T > kLocMaxT) return 0;
+  return (int64_t)c.ctas[i] * dec_rows_cap(c, K, i == kDecLocal ? kLocMaxT : dec_xrows(T));
 }
 
-// The index (into kDecClusterSizes) of the first kernel, in the order of
-// preference for T and K, that holds the call; -1 if none does.  A call may
-// ask for a cluster size (`want`, 0 = no preference; 1 = dec_local), which is
-// taken whenever it holds the call.
+// Launches of kernel i a call of N channels takes (one wave each); a large
+// number where the kernel does not apply.
+int64_t decode_launches(const DecCfg &c, int i, int64_t T, int64_t N, int64_t K) {
+  const int64_t w = decode_wave(c, i, T, K);
+  return w > 0 ? (N + w - 1) / w : (int64_t)1 << 40;
+}
+
+// The decode path splits the channels over at most this many launches (each
+// runs the activation pass again); beyond it the GEMM's 32-token tile is
+// faster.  Measured at T 16, K 4096: N 11008 in three launches, 34 us
+// against 41 us on the GEMM.
+constexpr int64_t kDecMaxLaunches = 3;
+
+// The index (into kDecClusterSizes) of the kernel a call runs: the first, in
+// the order of preference for T and K, that takes the call in one launch;
+// otherwise the one with the fewest launches (at most kDecMaxLaunches; ties
+// in that order); -1 if none.  A call may ask for a cluster size (`want`, 0 =
+// no preference; 1 = dec_local), taken whenever it holds the call in one
+// launch.
 int decode_pick(const DecCfg &c, int64_t T, int64_t N, int64_t K, int want) {
   for (int i = 0; i < 4; i++)
-    if (want != 0 && kDecClusterSizes[i] == want && decode_holds(c, i, T, N, K)) return i;
-  if (T <= kLocFirstT && decode_holds(c, kDecLocal, T, N, K)) return kDecLocal;
-  const int *order = T * K <= kDecSmallWork ? kDecPreferSmall : kDecPreferLarge;
-  for (int j = 0; j < 3; j++)
-    if (decode_holds(c, order[j], T, N, K)) return order[j];
-  return decode_holds(c, kDecLocal, T, N, K) ? kDecLocal : -1;
+    if (want != 0 && kDecClusterSizes[i] == want && decode_launches(c, i, T, N, K) == 1) return i;
+  int order[4], n = 0;
+  if (T <= kLocFirstT) order[n++] = kDecLocal;
+  const int *pref = T * K <= kDecSmallWork ? kDecPreferSmall : kDecPreferLarge;
+  for (int j = 0; j < 3; j++) order[n++] = pref[j];
+  if (T > kLocFirstT) order[n++] = kDecLocal;
+  int best = -1;
+  for (int j = 0; j < n; j++) {
+    const int64_t l = decode_launches(c, order[j], T, N, K);
+    if (l == 1) return order[j];
+    if (l <= kDecMaxLaunches && (best < 0 || l < decode_launches(c, best, T, N, K))) best = order[j];
+  }
+  return best;
 }
 
 }  // namespace
 
 // Output channels the decode path takes at this T and K: what the resident
-// CTAs of the best-covered kernel hold.
+// CTAs of the best-covered kernel hold in kDecMaxLaunches launches.
 int64_t decode_max_n(int dev, int64_t T, int64_t K) {
   const DecCfg c = decode_cfg(dev);
-  const int most = c.ctas[0] > c.ctas[1] ? (c.ctas[0] > c.ctas[2] ? c.ctas[0] : c.ctas[2])
-                                         : (c.ctas[1] > c.ctas[2] ? c.ctas[1] : c.ctas[2]);
-  int64_t n = (int64_t)most * dec_rows_cap(c, K, dec_xrows(T));
-  if (T <= kLocMaxT) {
-    const int64_t nl = (int64_t)c.ctas[kDecLocal] * dec_rows_cap(c, K, kLocMaxT);
-    n = nl > n ? nl : n;
+  int64_t n = 0;
+  for (int i = 0; i < 4; i++) {
+    const int64_t w = decode_wave(c, i, T, K);
+    n = w > n ? w : n;
   }
-  return n;
+  return kDecMaxLaunches * n;
 }
 
 int decode_cluster_size(int dev, int64_t T, int64_t N, int64_t K) {
@@ -1176,6 +1201,17 @@ cudaError_t launch_decode(const void *X, int64_t T, int64_t K, uint32_t thr, con
   if (pick < 0) return cudaErrorInvalidValue;  // the host routes only shapes that fit here
   const bool local = pick == kDecLocal;
   const int kc = kDecClusterSizes[pick];
+  const int form = (W16 == nullptr ? 1 : 0) | (bf16 ? 2 : 0);
+  using Kern = void (*)(CUtensorMap, DecArgs);
+  static const Kern kerns[4][4] = {
+      {dec_fused_kernel<8, false, false>, dec_fused_kernel<8, true, false>,
+       dec_fused_kernel<8, false, true>, dec_fused_kernel<8, true, true>},
+      {dec_fused_kernel<16, false, false>, dec_fused_kernel<16, true, false>,
+       dec_fused_kernel<16, false, true>, dec_fused_kernel<16, true, true>},
+      {dec_fused_kernel<4, false, false>, dec_fused_kernel<4, true, false>,
+       dec_fused_kernel<4, false, true>, dec_fused_kernel<4, true, true>},
+      {dec_local_kernel<false, false>, dec_local_kernel<true, false>,
+       dec_local_kernel<false, true>, dec_local_kernel<true, true>}};
   DecArgs a;
   a.X = reinterpret_cast<const uint4 *>(X);
   a.X16 = reinterpret_cast<const unsigned short *>(X);
@@ -1183,26 +1219,7 @@ cudaError_t launch_decode(const void *X, int64_t T, int64_t K, uint32_t thr, con
   a.K = K;
   a.N = N;
   a.thr = thr;
-  // the resident CTAs (whole clusters) share the channels evenly, at least 8
-  // per CTA
-  const int64_t want = min((int64_t)dc.ctas[pick], ((N + 7) / 8 + kc - 1) / kc * kc);
-  a.rows_per_cta = (N + want - 1) / want;
-  const int64_t used = (N + a.rows_per_cta - 1) / a.rows_per_cta;
-  const int64_t ctas = (used + kc - 1) / kc * kc;
-  a.wregion = dec_wregion(K, a.rows_per_cta);
   a.xrows = local ? kLocMaxT : (int)dec_xrows(T);
-  // W16 in boxes of 8 columns x one slice's channels (outlier columns only,
-  // so no L2 promotion beyond the sector)
-  // (without W16 the map is never read: it then describes Wq)
-  CUtensorMap tm;
-  const bool enc = W16 ? encode_2d(&tm, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
-                                              : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, W16, (uint64_t)K,
-                                   (uint64_t)N, (uint64_t)K * 2, 8, (uint32_t)a.rows_per_cta,
-                                   CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE)
-                       : encode_2d(&tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, Wq, (uint64_t)K,
-                                   (uint64_t)N, (uint64_t)K, 16, (uint32_t)a.rows_per_cta,
-                                   CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE);
-  if (!enc) return cudaErrorInvalidValue;
   a.Wq = Wq;
   a.sw = sw;
   a.W16 = reinterpret_cast<const unsigned short *>(W16);
@@ -1215,40 +1232,61 @@ cudaError_t launch_decode(const void *X, int64_t T, int64_t K, uint32_t thr, con
   a.dbg_acc = dbg_acc;
   a.status = ws.status;
   a.force_timeout = (opts & BNB_OPT_FORCE_TIMEOUT) ? 1 : 0;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)ctas);
-  cfg.blockDim = dim3(kDecThreads);
-  cfg.dynamicSmemBytes = decode_smem_bytes(K, a.rows_per_cta, a.xrows);
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[2];
-  unsigned na = 0;
-  if (!local) {
-    attr[na].id = cudaLaunchAttributeClusterDimension;
-    attr[na].val.clusterDim.x = (unsigned)kc;
-    attr[na].val.clusterDim.y = 1;
-    attr[na].val.clusterDim.z = 1;
-    na++;
+  // One launch per wave of the resident CTAs, each over an equal share of
+  // the channels (every launch runs the activation pass; each later one
+  // waits for the one before through programmatic dependent launch).
+  const int64_t wave = decode_wave(dc, pick, T, K);
+  const int64_t nl = (N + wave - 1) / wave;
+  const int64_t share = (N + nl - 1) / nl;
+  cudaError_t e = cudaSuccess;
+  for (int64_t nb = 0; nb < N && e == cudaSuccess; nb += share) {
+    const int64_t nn = min(share, N - nb);
+    a.n_base = nb;
+    a.n_end = nb + nn;
+    a.reset_status = nb == 0 ? 1 : 0;
+    // the resident CTAs (whole clusters) share the channels evenly, at least
+    // 8 per CTA
+    const int64_t want = min((int64_t)dc.ctas[pick], ((nn + 7) / 8 + kc - 1) / kc * kc);
+    a.rows_per_cta = (nn + want - 1) / want;
+    const int64_t used = (nn + a.rows_per_cta - 1) / a.rows_per_cta;
+    const int64_t ctas = (used + kc - 1) / kc * kc;
+    a.wregion = dec_wregion(K, a.rows_per_cta);
+    // W16 in boxes of 8 columns x one slice's channels (outlier columns only,
+    // so no L2 promotion beyond the sector)
+    // (without W16 the map is never read: it then describes Wq)
+    CUtensorMap tm;
+    const bool enc = W16 ? encode_2d(&tm, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, W16, (uint64_t)K,
+                                     (uint64_t)N, (uint64_t)K * 2, 8, (uint32_t)a.rows_per_cta,
+                                     CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE)
+                         : encode_2d(&tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, Wq, (uint64_t)K,
+                                     (uint64_t)N, (uint64_t)K, 16, (uint32_t)a.rows_per_cta,
+                                     CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE);
+    if (!enc) return cudaErrorInvalidValue;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)ctas);
+    cfg.blockDim = dim3(kDecThreads);
+    cfg.dynamicSmemBytes = decode_smem_bytes(K, a.rows_per_cta, a.xrows);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    unsigned na = 0;
+    if (!local) {
+      attr[na].id = cudaLaunchAttributeClusterDimension;
+      attr[na].val.clusterDim.x = (unsigned)kc;
+      attr[na].val.clusterDim.y = 1;
+      attr[na].val.clusterDim.z = 1;
+      na++;
+    }
+    if (!(opts & BNB_OPT_NO_PDL)) {
+      attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+      attr[na].val.programmaticStreamSerializationAllowed = 1;
+      na++;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = na;
+    e = cudaLaunchKernelEx(&cfg, kerns[pick][form], tm, a);
+    note_launch();
   }
-  if (!(opts & BNB_OPT_NO_PDL)) {
-    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[na].val.programmaticStreamSerializationAllowed = 1;
-    na++;
-  }
-  cfg.attrs = attr;
-  cfg.numAttrs = na;
-  const int form = (W16 == nullptr ? 1 : 0) | (bf16 ? 2 : 0);
-  using Kern = void (*)(CUtensorMap, DecArgs);
-  static const Kern kerns[4][4] = {
-      {dec_fused_kernel<8, false, false>, dec_fused_kernel<8, true, false>,
-       dec_fused_kernel<8, false, true>, dec_fused_kernel<8, true, true>},
-      {dec_fused_kernel<16, false, false>, dec_fused_kernel<16, true, false>,
-       dec_fused_kernel<16, false, true>, dec_fused_kernel<16, true, true>},
-      {dec_fused_kernel<4, false, false>, dec_fused_kernel<4, true, false>,
-       dec_fused_kernel<4, false, true>, dec_fused_kernel<4, true, true>},
-      {dec_local_kernel<false, false>, dec_local_kernel<true, false>,
-       dec_local_kernel<false, true>, dec_local_kernel<true, true>}};
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, kerns[pick][form], tm, a);
-  note_launch();
   return e;
 }
 

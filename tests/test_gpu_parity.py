@@ -248,6 +248,20 @@ def test_decode_large_weights(orc, T, K, N):
     run_and_compare(orc, w.X, w.W, w.tau, what=f"decode T{T} K{K} N{N}")
 
 
+@pytest.mark.parametrize("T,K,N,ncols", [
+    (16, 4096, 5000, 4), (2, 4096, 6000, 70), (1, 4096, 17000, 3), (9, 2048, 9601, 9),
+    (3, 272, 17000, 2),
+])
+def test_decode_several_launches(orc, T, K, N, ncols):
+    """Channels beyond one wave of the decode kernel's resident CTAs: the
+    call splits them over up to three launches (each with the activation
+    pass), every element against the oracle."""
+    from int8_mixed_precision_04_b300 import binding
+    assert binding.load().bnb_int8_linear_path(T, N, K) == 1
+    w = inputs.random_small(T, K, N, ncols, seed=7 * K + N + T, tau=6.0)
+    run_and_compare(orc, w.X, w.W, 6.0, what=f"decode, several launches, T{T} K{K} N{N}")
+
+
 @pytest.mark.parametrize("T,K,N,ncols,tau", [
     (16, 1040, 3000, 6, 6.0), (7, 3072, 2056, 3, 6.0), (16, 8192, 1000, 40, 3.0),
     (2, 5120, 9000, 2, 6.0), (16, 2048, 40000, 5, 6.0), (9, 16, 37, 1, 0.0),
