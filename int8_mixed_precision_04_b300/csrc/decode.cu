@@ -1,6 +1,7 @@
-// The whole layer for decode-sized T (T <= 16) in one kernel per call: for
-// T <= 4 dec_local (below the clustered kernel), where every CTA runs the
-// whole activation pass itself, otherwise dec_fused.
+// The whole layer for decode-sized T (T <= 16) in one kernel launch per wave
+// of channels (at most three): for T <= 4 dec_local (below the clustered
+// kernel), where every CTA runs the whole activation pass itself, otherwise
+// dec_fused.
 //
 // dec_fused: one CTA per slice of at most 40 output channels (one CTA per
 // SM), in thread-block clusters of kC CTAs (16, 8 or 4 where T K <= 32768,
