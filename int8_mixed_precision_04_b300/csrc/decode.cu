@@ -430,7 +430,9 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       // bytes every CTA receives: the codes of all T rows and every mask word
       // (cbar); the first outlier columns and their X values (xbar)
       if (threadIdx.x == 0) {
-        mbar_expect_tx(&sm.cbar, (uint32_t)T * (uint32_t)K + 4u * (uint32_t)words);
+        // every code but this CTA's own columns (stored locally), every mask word
+        const int64_t own = min(vpc, max((int64_t)0, vecs - (int64_t)crank * vpc));
+        mbar_expect_tx(&sm.cbar, (uint32_t)T * (uint32_t)(K - 8 * own) + 4u * (uint32_t)words);
         mbar_expect_tx(&sm.xbar, 4u * (1u + (uint32_t)T) * min(nO, (uint32_t)kDecOutSmall));
       }
       const uint32_t cbar = smem_addr(&sm.cbar), xbar = smem_addr(&sm.xbar);
@@ -491,9 +493,13 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         const uint32_t q0 = __shfl_down_sync(0xffffffffu, p0, 1);
         const uint32_t q1 = __shfl_down_sync(0xffffffffu, p1, 1);
         if (t >= T || !live || (lane & 1)) continue;
+        // this CTA's copy by a plain store (the barrier before the MMAs
+        // publishes it), the other CTAs' by remote stores
+        *reinterpret_cast<uint4 *>(xs + t * pitch + 8 * v) = make_uint4(p0, p1, q0, q1);
         const uint32_t dst = smem_addr(xs + t * pitch + 8 * v);
 #pragma unroll
-        for (int c = 0; c < kC; c++) st_async_v4(mapa(dst, c), p0, p1, q0, q1, mapa(cbar, c));
+        for (int c = 0; c < kC; c++)
+          if (c != (int)crank) st_async_v4(mapa(dst, c), p0, p1, q0, q1, mapa(cbar, c));
       }
     }
   }
