@@ -113,8 +113,8 @@ MEASURED_TRAFFIC = {
     ("gemm_tc", 4096, 8192, 28672): ("gemm_tc.cu", "25383f2e26f639e0", 1_178_290_000),
     # one ncu capture of the decode workload's kernel (bytes): T 16 (the
     # clustered kernel) and T 1 (the kernel without clusters), nothing written
-    ("dec_fused", 16, 4096, 4096): ("decode.cu", "ee3b51df0d4bf774", 19_116_032),
-    ("dec_local", 1, 4096, 4096): ("decode.cu", "ee3b51df0d4bf774", 18_989_312),
+    ("dec_fused", 16, 4096, 4096): ("decode.cu", "2d72ed8fa793ddf4", 19_116_800),
+    ("dec_local", 1, 4096, 4096): ("decode.cu", "2d72ed8fa793ddf4", 18_989_056),
 }
 
 
