@@ -256,10 +256,22 @@ def test_decode_several_launches(orc, T, K, N, ncols):
     """Channels beyond one wave of the decode kernel's resident CTAs: the
     call splits them over up to three launches (each with the activation
     pass), every element against the oracle."""
+    import torch
+
     from int8_mixed_precision_04_b300 import binding
-    assert binding.load().bnb_int8_linear_path(T, N, K) == 1
+    lib = binding.load()
+    assert lib.bnb_int8_linear_path(T, N, K) == 1
     w = inputs.random_small(T, K, N, ncols, seed=7 * K + N + T, tau=6.0)
     run_and_compare(orc, w.X, w.W, 6.0, what=f"decode, several launches, T{T} K{K} N{N}")
+    # one call is more than one launch of the decode kernel, three at most
+    X = torch.from_numpy(w.X).cuda()
+    W = torch.from_numpy(w.W).cuda()
+    Wq, sw = binding.quantize_weight(W)
+    torch.cuda.synchronize()
+    before = lib.bnb_launch_count()
+    binding.linear(X, Wq, sw, W, 6.0)
+    torch.cuda.synchronize()
+    assert 2 <= lib.bnb_launch_count() - before <= 3
 
 
 @pytest.mark.parametrize("T,K,N,ncols,tau", [
