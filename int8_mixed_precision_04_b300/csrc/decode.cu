@@ -1,7 +1,7 @@
 // The whole layer for decode-sized T (T <= 16) in one kernel launch per wave
-// of channels (at most three): for T <= 4 dec_local (below the clustered
-// kernel), where every CTA runs the whole activation pass itself, otherwise
-// dec_fused.
+// of channels (at most three): for T <= 4 (T <= 6 at K > 2048) dec_local
+// (below the clustered kernel), where every CTA runs the whole activation
+// pass itself, otherwise dec_fused.
 //
 // dec_fused: one CTA per slice of at most 40 output channels (one CTA per
 // SM), in thread-block clusters of kC CTAs (16, 8 or 4 where T K <= 32768,
@@ -1025,12 +1025,14 @@ constexpr int kDecLocal = 3;
 constexpr int64_t kDecSmallWork = 32768;
 constexpr int kDecPreferSmall[3] = {1, 0, 2};  // T K <= kDecSmallWork: 16, 8, 4
 constexpr int kDecPreferLarge[3] = {0, 1, 2};  // otherwise: 8, 16, 4
-// dec_local comes first for T <= kLocFirstT, and serves T <= kLocMaxT where
-// no cluster size holds the call.  Measured per call at K = N = 4096 (16-layer
-// CUDA graphs): 7.4 / 7.8 / 8.7 / 10.5 us at T 1 / 2 / 4 / 8, against
-// 9.6 / 9.6 / 9.7 / 10.2 us for the best cluster size; its activation pass
-// costs every CTA the whole T x K codes.
-constexpr int64_t kLocFirstT = 4;
+// dec_local comes first for T <= dec_local_first(K), and serves T <= kLocMaxT
+// where no cluster size holds the call.  Its activation pass costs every CTA
+// the whole T x K codes, the clustered kernel's exchange grows with K.
+// Measured per call (16-layer CUDA graphs, N 4096) against 16-CTA clusters:
+// at K 4096, 8.45 / 8.96 / 9.40 / 9.87 / 10.37 us at T 4 / 5 / 6 / 7 / 8
+// against 9.60 / 9.80 / 9.84 / 9.90 / 10.13; at K 2048, 7.68 / 8.14 / 8.66 at
+// T 4 / 5 / 6 against 8.19 / 8.08 / 8.24.
+constexpr int64_t dec_local_first(int64_t K) { return K > 2048 ? 6 : 4; }
 
 // CTAs of dec_fused<kC> resident at once, in whole clusters (0 if the query
 // fails); also opens the kernel's shared-memory limit to `dyn_max`.
@@ -1165,10 +1167,11 @@ int decode_pick(const DecCfg &c, int64_t T, int64_t N, int64_t K, int want) {
   for (int i = 0; i < 4; i++)
     if (want != 0 && kDecClusterSizes[i] == want && decode_launches(c, i, T, N, K) == 1) return i;
   int order[4], n = 0;
-  if (T <= kLocFirstT) order[n++] = kDecLocal;
+  const bool local_first = T <= dec_local_first(K);
+  if (local_first) order[n++] = kDecLocal;
   const int *pref = T * K <= kDecSmallWork ? kDecPreferSmall : kDecPreferLarge;
   for (int j = 0; j < 3; j++) order[n++] = pref[j];
-  if (T > kLocFirstT) order[n++] = kDecLocal;
+  if (!local_first) order[n++] = kDecLocal;
   int best = -1;
   for (int j = 0; j < n; j++) {
     const int64_t l = decode_launches(c, order[j], T, N, K);
