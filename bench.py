@@ -113,11 +113,8 @@ MEASURED_TRAFFIC = {
     ("gemm_tc", 4096, 8192, 28672): ("gemm_tc.cu", "25383f2e26f639e0", 1_178_290_000),
     # one ncu capture of the decode workload's kernel (bytes): T 16 (the
     # clustered kernel) and T 1 (the kernel without clusters), nothing written
-    # (captured on decode.cu 2d72ed8fa793ddf4, whose kernels the recorded
-    # source keeps unchanged: it differs in comments and the host's choice of
-    # kernel for T 5-6)
-    ("dec_fused", 16, 4096, 4096): ("decode.cu", "1ba6e9b2840c5bbe", 19_116_800),
-    ("dec_local", 1, 4096, 4096): ("decode.cu", "1ba6e9b2840c5bbe", 18_989_056),
+    ("dec_fused", 16, 4096, 4096): ("decode.cu", "902e6ba0c69afeb9", 19_117_824),
+    ("dec_local", 1, 4096, 4096): ("decode.cu", "902e6ba0c69afeb9", 18_957_568),
 }
 
 

@@ -318,7 +318,7 @@ int bnb_int8_linear_path(int64_t T, int64_t N, int64_t K);
  * form of the decode kernel bnb_int8_linear launches on the current device,
  * as a cluster size: 16, 8 or 4 (CTAs in thread-block clusters sharing one
  * activation pass) or 1 (no clusters: every CTA runs the whole activation
- * pass; by default T <= 4, and T <= 6 at K > 2048).  0 for any other shape.
+ * pass; by default T <= 5, and T <= 6 at K > 2048).  0 for any other shape.
  * For benchmarks and tests.
  */
 int bnb_int8_decode_cluster(int64_t T, int64_t N, int64_t K);

@@ -1,5 +1,5 @@
 // The whole layer for decode-sized T (T <= 16) in one kernel launch per wave
-// of channels (at most three): for T <= 4 (T <= 6 at K > 2048) dec_local
+// of channels (at most three): for T <= 5 (T <= 6 at K > 2048) dec_local
 // (below the clustered kernel), where every CTA runs the whole activation
 // pass itself, otherwise dec_fused.
 //
@@ -695,8 +695,13 @@ struct DecLocSmall {
   uint16_t bias[kDecMaxRows];            // the slice's 16-bit bias (0 without one)
 };
 
-// kWq: only the int8 weight is kept (W16 null); kBf: X, W16, bias and Y are bf16
-template <bool kWq, bool kBf>
+// kWq: only the int8 weight is kept (W16 null); kBf: X, W16, bias and Y are
+// bf16; kMT: the call's tokens at most (1, 2, 4, 6 or kLocMaxT).  The
+// activation pass's loops over the rows are unrolled that far, and the
+// smaller code is what a decode call spends its first microseconds fetching:
+// measured at K = N = 4096, T 1 took 6.28 us with kMT 4 against 7.32 us with
+// kMT 8.
+template <bool kWq, bool kBf, int kMT>
 __global__ void __launch_bounds__(kDecThreads, 1)
     dec_local_kernel(const __grid_constant__ CUtensorMap tm_w16, const DecArgs p) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -768,15 +773,15 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   // ---- activation pass: thread v owns columns [8v, 8v + 8) of every row ----
   const int64_t v = threadIdx.x;
   const bool live = v < vecs;
-  uint4 x[kLocMaxT];
+  uint4 x[kMT];
 #pragma unroll
-  for (int t = 0; t < kLocMaxT; t++)  // all loads in flight before any is used
+  for (int t = 0; t < kMT; t++)  // all loads in flight before any is used
     x[t] = (t < T && live) ? __ldg(p.X + t * vecs + v) : make_uint4(0, 0, 0, 0);
   named_bar_arrive(2, kDecThreads);
   // a column is an outlier if any of the call's rows has |x| >= tau there
   uint32_t flags = 0;
 #pragma unroll
-  for (int t = 0; t < kLocMaxT; t++) {
+  for (int t = 0; t < kMT; t++) {
     if (t < T) {
       const uint32_t w[4] = {x[t].x, x[t].y, x[t].z, x[t].w};
 #pragma unroll
@@ -789,7 +794,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   if (!live) flags = 0;
   // each row's maximum over the non-outlier columns, and the outlier count
 #pragma unroll
-  for (int t = 0; t < kLocMaxT; t++) {
+  for (int t = 0; t < kMT; t++) {
     if (t < T) {
       const uint32_t w[4] = {x[t].x, x[t].y, x[t].z, x[t].w};
       uint32_t m = 0;
@@ -826,7 +831,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   const RowCode<kBf> rc_lane(e2f<kBf>(lane < T ? sm.sxb[lane] : 0u));
   // codes rint(fl32(127 x) / sx) of the non-outlier columns, 0 at the outliers
 #pragma unroll
-  for (int t = 0; t < kLocMaxT; t++) {
+  for (int t = 0; t < kMT; t++) {
     if (t < T) {
       RowCode<kBf> rc;
       rc.a = __shfl_sync(0xffffffffu, rc_lane.a, t);
@@ -851,7 +856,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         if (j < (uint32_t)kDecOutSmall) {
           sm.oc[j] = col;
 #pragma unroll
-          for (int t = 0; t < kLocMaxT; t++)
+          for (int t = 0; t < kMT; t++)
             if (t < T) sm.xo[t * kDecOutSmall + j] = ((&x[t].x)[b >> 1] >> (16 * (b & 1))) & 0xffffu;
         }
         ++j;
@@ -1013,6 +1018,11 @@ __global__ void __launch_bounds__(kDecThreads, 1)
 
 namespace {
 
+// dec_local's four forms (kWq, kBf) for a token bound
+#define DEC_LOCAL_FORMS(mt)                                                          \
+  dec_local_kernel<false, false, mt>, dec_local_kernel<true, false, mt>,             \
+      dec_local_kernel<false, true, mt>, dec_local_kernel<true, true, mt>
+
 // the kernels built (index into DecCfg::ctas): dec_fused in clusters of 8, 16
 // or 4 CTAs, and dec_local (1: no cluster)
 constexpr int kDecClusterSizes[4] = {8, 16, 4, 1};
@@ -1029,10 +1039,10 @@ constexpr int kDecPreferLarge[3] = {0, 1, 2};  // otherwise: 8, 16, 4
 // where no cluster size holds the call.  Its activation pass costs every CTA
 // the whole T x K codes, the clustered kernel's exchange grows with K.
 // Measured per call (16-layer CUDA graphs, N 4096) against 16-CTA clusters:
-// at K 4096, 8.45 / 8.96 / 9.40 / 9.87 / 10.37 us at T 4 / 5 / 6 / 7 / 8
-// against 9.60 / 9.80 / 9.84 / 9.90 / 10.13; at K 2048, 7.68 / 8.14 / 8.66 at
-// T 4 / 5 / 6 against 8.19 / 8.08 / 8.24.
-constexpr int64_t dec_local_first(int64_t K) { return K > 2048 ? 6 : 4; }
+// at K 4096, 5.94 / 7.81 / 8.57 / 9.08 / 9.88 / 10.37 us at T 1 / 4 / 5 / 6 /
+// 7 / 8 against 9.54 / 9.61 / 9.83 / 9.85 / 9.90 / 10.14; at K 2048, 4.92 /
+// 7.04 / 7.81 / 8.32 at T 1 / 4 / 5 / 6 against 7.98 / 8.19 / 8.08 / 8.25.
+constexpr int64_t dec_local_first(int64_t K) { return K > 2048 ? 6 : 5; }
 
 // CTAs of dec_fused<kC> resident at once, in whole clusters (0 if the query
 // fails); also opens the kernel's shared-memory limit to `dyn_max`.
@@ -1074,8 +1084,8 @@ int dec_local_ctas(int dev, int dyn_max) {
   int sms = 0;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
   int least = 1 << 30;
-  for (auto *f : {dec_local_kernel<false, false>, dec_local_kernel<true, false>,
-                  dec_local_kernel<false, true>, dec_local_kernel<true, true>}) {
+  for (auto *f : {DEC_LOCAL_FORMS(1), DEC_LOCAL_FORMS(2), DEC_LOCAL_FORMS(4),
+                  DEC_LOCAL_FORMS(6), DEC_LOCAL_FORMS(kLocMaxT)}) {
     if (cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn_max) !=
         cudaSuccess)
       return 0;
@@ -1109,7 +1119,7 @@ DecCfg decode_cfg(int dev) {
   if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, qdev) ==
           cudaSuccess &&
       cudaFuncGetAttributes(&fa, dec_fused_kernel<8, false, false>) == cudaSuccess &&
-      cudaFuncGetAttributes(&fl, dec_local_kernel<false, false>) == cudaSuccess) {
+      cudaFuncGetAttributes(&fl, dec_local_kernel<false, false, kLocMaxT>) == cudaSuccess) {
     r.dyn_max = optin - (int)(fa.sharedSizeBytes > fl.sharedSizeBytes ? fa.sharedSizeBytes
                                                                        : fl.sharedSizeBytes);
     r.ctas[0] = dec_resident_ctas<8>(r.dyn_max);
@@ -1220,8 +1230,12 @@ cudaError_t launch_decode(const void *X, int64_t T, int64_t K, uint32_t thr, con
        dec_fused_kernel<16, false, true>, dec_fused_kernel<16, true, true>},
       {dec_fused_kernel<4, false, false>, dec_fused_kernel<4, true, false>,
        dec_fused_kernel<4, false, true>, dec_fused_kernel<4, true, true>},
-      {dec_local_kernel<false, false>, dec_local_kernel<true, false>,
-       dec_local_kernel<false, true>, dec_local_kernel<true, true>}};
+      {DEC_LOCAL_FORMS(kLocMaxT)}};
+  // the kernel without clusters, by the call's tokens at most
+  static const Kern kerns_local[4][4] = {
+      {DEC_LOCAL_FORMS(1)}, {DEC_LOCAL_FORMS(2)}, {DEC_LOCAL_FORMS(4)}, {DEC_LOCAL_FORMS(6)}};
+  const int mt = T <= 1 ? 0 : T <= 2 ? 1 : T <= 4 ? 2 : T <= 6 ? 3 : 4;
+  const Kern kern = local && mt < 4 ? kerns_local[mt][form] : kerns[pick][form];
   DecArgs a;
   a.X = reinterpret_cast<const uint4 *>(X);
   a.X16 = reinterpret_cast<const unsigned short *>(X);
@@ -1294,7 +1308,7 @@ cudaError_t launch_decode(const void *X, int64_t T, int64_t K, uint32_t thr, con
     }
     cfg.attrs = attr;
     cfg.numAttrs = na;
-    e = cudaLaunchKernelEx(&cfg, kerns[pick][form], tm, a);
+    e = cudaLaunchKernelEx(&cfg, kern, tm, a);
     note_launch();
   }
   return e;

@@ -40,7 +40,7 @@ cudaError_t launch_dequantize_blockwise(const int8_t *codes, const float *absmax
 // The whole layer for T <= 16, K <= kDecodeMaxK, N <= decode_max_n(dev, T, K)
 // in one kernel launch per wave of channels, at most three (activation pass
 // fused into the GEMV: shared by clusters of CTAs, or repeated by every CTA
-// for T <= 4, T <= 6 at K > 2048), launched with programmatic dependent launch unless the call's
+// for T <= 5, T <= 6 at K > 2048), launched with programmatic dependent launch unless the call's
 // options turn it off.
 int64_t decode_max_n(int dev, int64_t T, int64_t K);
 // The cluster size launch_decode picks for this shape (1: no clusters), 0 if

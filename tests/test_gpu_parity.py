@@ -64,7 +64,7 @@ def test_decode_local(orc, cluster, T, K, N, ncols):
     N up to what the resident CTAs hold without clusters."""
     from int8_mixed_precision_04_b300 import binding
     assert binding.load().bnb_int8_linear_path(T, N, K) == 1
-    assert binding.decode_cluster(T, N, K) == 1 if T <= (6 if K > 2048 else 4) else binding.decode_cluster(T, N, K) in (1, 4, 8, 16)
+    assert binding.decode_cluster(T, N, K) == 1 if T <= (6 if K > 2048 else 5) else binding.decode_cluster(T, N, K) in (1, 4, 8, 16)
     w = inputs.random_small(T, K, N, ncols, seed=3 * K + N + T, tau=6.0)
     run_and_compare(orc, w.X, w.W, 6.0, what=f"decode local/cluster {cluster} T{T} K{K} N{N}",
                     opts=binding.OPT_CLUSTER(cluster))
