@@ -109,6 +109,7 @@ def _workload(T, K, N, ncols, seed, tau):
 @pytest.mark.parametrize("T,K,N,ncols", [
     (1, 256, 64, 2), (16, 4096, 4096, 4), (11, 1040, 520, 9), (16, 1040, 96, 70),
     (17, 272, 129, 3), (300, 1024, 200, 4), (257, 2064, 1000, 7), (130, 512, 257, 40),
+    (2, 512, 100, 2), (3, 2048, 300, 5), (6, 4096, 500, 3),
 ])
 @pytest.mark.parametrize("tau", [6.0, 0.0, math.inf])
 @pytest.mark.parametrize("form", ["w16", "bias", "wq_only"])
