@@ -81,6 +81,8 @@ def load_peaks():
 def make_workload(name: str, T: int):
     if name == "decode":
         return inputs.decode(T=T)
+    if name == "decode_t1":  # the decode workload at one token (batch-1 generation)
+        return inputs.decode(T=1)
     if name == "decode_k8192":  # a decode step through the large MLP weight
         return inputs.decode(T=T, K=8192, N=28672)
     if name == "decode_n11008":  # a decode step through the prefill weight
@@ -867,15 +869,15 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="large",
-                    choices=["decode", "decode_k8192", "decode_n11008", "prefill", "large",
-                             "sweep", "tiny", "blockwise"])
+                    choices=["decode", "decode_t1", "decode_k8192", "decode_n11008", "prefill",
+                             "large", "sweep", "tiny", "blockwise"])
     ap.add_argument("--T", type=int, default=16, help="tokens of the decode workloads")
     ap.add_argument("--max-layers", type=int, default=64)
     ap.add_argument("--min-timed-s", type=float, default=1.2,
                     help="the timed region lasts at least this long (graph replays per step)")
     ap.add_argument("--kernel-timed-s", type=float, default=1.0,
                     help="length of the dominant-kernel timing loop")
-    ap.add_argument("--sub", default="decode,decode_k8192,decode_n11008,prefill",
+    ap.add_argument("--sub", default="decode,decode_t1,decode_k8192,decode_n11008,prefill",
                     help="other regimes measured in the same run (comma list, '' for none)")
     ap.add_argument("--sub-timed-s", type=float, default=0.5)
     ap.add_argument("--e2e-calls", type=int, default=2000)
