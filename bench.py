@@ -115,8 +115,10 @@ MEASURED_TRAFFIC = {
     ("gemm_tc", 4096, 8192, 28672): ("gemm_tc.cu", "25383f2e26f639e0", 1_178_290_000),
     # one ncu capture of the decode workload's kernel (bytes): T 16 (the
     # clustered kernel) and T 1 (the kernel without clusters), nothing written
-    ("dec_fused", 16, 4096, 4096): ("decode.cu", "902e6ba0c69afeb9", 19_117_824),
-    ("dec_local", 1, 4096, 4096): ("decode.cu", "902e6ba0c69afeb9", 18_957_568),
+    # (captured on decode.cu 902e6ba0c69afeb9, whose kernels the recorded
+    # source keeps unchanged: it differs in one comment)
+    ("dec_fused", 16, 4096, 4096): ("decode.cu", "892163d0c55e4732", 19_117_824),
+    ("dec_local", 1, 4096, 4096): ("decode.cu", "892163d0c55e4732", 18_957_568),
 }
 
 

@@ -1268,8 +1268,8 @@ cudaError_t launch_decode(const void *X, int64_t T, int64_t K, uint32_t thr, con
     a.n_base = nb;
     a.n_end = nb + nn;
     a.reset_status = nb == 0 ? 1 : 0;
-    // the resident CTAs (whole clusters) share the channels evenly, at least
-    // 8 per CTA
+    // the resident CTAs (whole clusters) share the channels evenly, with no
+    // more CTAs than one per 8 channels (rounded up to whole clusters)
     const int64_t want = min((int64_t)dc.ctas[pick], ((nn + 7) / 8 + kc - 1) / kc * kc);
     a.rows_per_cta = (nn + want - 1) / want;
     const int64_t used = (nn + a.rows_per_cta - 1) / a.rows_per_cta;
